@@ -1,0 +1,113 @@
+"""Pins of the oracle's tile binning (Kopanas, Step 1 (b): exact conic-tile spans) and of
+its pair ordering (Step 1 (d)) and LPT order (Ryu & Yoo, Sec. 4.1)."""
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import definitional as D
+import synthetic_scenes as ss
+
+CASES = [(0, 37, 53, 60), (1, 128, 128, 120), (2, 150, 97, 140), (3, 64, 40, 300)]
+
+
+def _scene(seed, W, H, n):
+    rng = np.random.default_rng(seed)
+    # a mix of tiny, medium and large, strongly anisotropic splats
+    sc, cam = ss.random_scene(rng, n, W, H, sh_degree=0, log_scale=(-3.0, 1.0), spread=1.2)
+    return sc, cam
+
+
+@pytest.mark.parametrize("seed,W,H,n", CASES)
+def test_emitted_tiles_are_exact_and_complete(seed, W, H, n):
+    """A tile is emitted iff the support ellipse q(d) <= tau meets the hull of its pixel
+    centres -- decided here by the exact minimum of q over the rectangle, not by spans.
+    Emitted tiles may lie within the documented pad; tiles that truly meet the ellipse
+    are always emitted."""
+    sc, cam = _scene(seed, W, H, n)
+    p = oracle.project(sc, cam)
+    ntx, nty = oracle.n_tiles(cam)
+    nvis = 0
+    for g in range(sc.n):
+        rec = p.splat[g]
+        if p.tiles_touched[g] == 0:
+            # culled: either invisible, or the ellipse meets no tile
+            if rec[6] > 0 and rec[2] > 0:
+                for t in range(ntx * nty):
+                    x0, x1, y0, y1 = D.tile_hull(cam, t)
+                    qmin = D.rect_min_q(rec[2], rec[3], rec[4], x0 - rec[0], x1 - rec[0],
+                                        y0 - rec[1], y1 - rec[1])
+                    assert qmin > rec[6] * (1 - 1e-5)
+            continue
+        nvis += 1
+        tiles = set(oracle.splat_tiles(cam, rec).tolist())
+        assert len(tiles) == p.tiles_touched[g]
+        a, b, c, tau = rec[2], rec[3], rec[4], rec[6]
+        rx, ry = np.sqrt(tau * rec[8]), np.sqrt(tau * rec[10])
+        padx = 2.0 ** -8 + rx * 2.0 ** -14 + 1e-4
+        pady = 2.0 ** -8 + ry * 2.0 ** -14 + 1e-4
+        for t in range(ntx * nty):
+            x0, x1, y0, y1 = D.tile_hull(cam, t)
+            qmin = D.rect_min_q(a, b, c, x0 - rec[0], x1 - rec[0], y0 - rec[1], y1 - rec[1])
+            if t in tiles:
+                qpad = D.rect_min_q(a, b, c, x0 - padx - rec[0], x1 + padx - rec[0],
+                                    y0 - pady - rec[1], y1 + pady - rec[1])
+                assert qpad <= tau * (1 + 1e-5), (g, t)
+            else:
+                assert qmin > tau * (1 - 1e-5), (g, t)
+    assert nvis > n // 3
+
+
+@pytest.mark.parametrize("seed,W,H,n", CASES)
+def test_sorted_pairs_ranges_and_lpt_order(seed, W, H, n):
+    sc, cam = _scene(seed, W, H, n)
+    p = oracle.project(sc, cam)
+    b = oracle.bin_sort(cam, p)
+    ntx, nty = oracle.n_tiles(cam)
+    # reference ordering: Python's sort over (tile, depth, id)
+    pairs = []
+    for g in np.nonzero(p.visible)[0]:
+        for t in oracle.splat_tiles(cam, p.splat[g]):
+            pairs.append((int(t), float(p.splat[g, 7]), int(g)))
+    pairs.sort()
+    ref_ids = np.array([g for _, _, g in pairs], np.int32)
+    ref_tiles = np.array([t for t, _, _ in pairs], np.int64)
+    np.testing.assert_array_equal(b.ids, ref_ids)
+    counts = np.bincount(ref_tiles, minlength=ntx * nty)
+    np.testing.assert_array_equal(b.counts, counts)
+    ends = np.cumsum(counts)
+    np.testing.assert_array_equal(b.ranges[:, 1], ends)
+    np.testing.assert_array_equal(b.ranges[:, 0], ends - counts)
+    lpt = sorted(range(ntx * nty), key=lambda t: (-counts[t], t))
+    np.testing.assert_array_equal(b.lpt_order, lpt)
+    assert b.n_pairs == int(p.tiles_touched.sum())
+
+
+def test_tile_selection_matches_full_list():
+    sc, cam = _scene(2, 150, 97, 140)
+    p = oracle.project(sc, cam)
+    full = oracle.bin_sort(cam, p)
+    sel = np.zeros(len(full.counts), np.uint8)
+    sel[[0, 3, 7, 20, 41]] = 1
+    part = oracle.bin_sort(cam, p, sel)
+    for t in np.nonzero(sel)[0]:
+        s, e = full.ranges[t]
+        np.testing.assert_array_equal(part.tile_ids(t), full.ids[s:e])
+    np.testing.assert_array_equal(part.counts, full.counts)
+
+
+def test_three_sigma_square_contains_emitted_tiles_when_tau_le_9():
+    """With tau <= 9 (o <= e^4.5 / 255) the support ellipse lies inside the 3-sigma
+    circle of the classic conservative bound, so every emitted tile meets that square."""
+    sc, cam = _scene(1, 128, 128, 200)
+    p = oracle.project(sc, cam)
+    checked = 0
+    for g in np.nonzero(p.visible & (p.splat[:, 6] <= 9.0))[0]:
+        P = np.array([[p.splat[g, 8], p.splat[g, 9]], [p.splat[g, 9], p.splat[g, 10]]])
+        r3 = 3.0 * np.sqrt(np.linalg.eigvalsh(P).max()) + 0.01
+        for t in oracle.splat_tiles(cam, p.splat[g]):
+            x0, x1, y0, y1 = D.tile_hull(cam, int(t))
+            assert x0 <= p.splat[g, 0] + r3 and x1 >= p.splat[g, 0] - r3
+            assert y0 <= p.splat[g, 1] + r3 and y1 >= p.splat[g, 1] - r3
+            checked += 1
+    assert checked > 50
