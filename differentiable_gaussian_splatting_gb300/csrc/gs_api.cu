@@ -1,0 +1,268 @@
+// gs_api.cu -- the extern "C" entry points of libgs (see include/gs.h).
+//
+// Host side only: argument validation (synchronous, before anything is
+// enqueued), workspace carving and kernel launches on the caller's stream.
+// The library allocates no device memory.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/gs.h"
+#include "gs_internal.h"
+
+using namespace gs;
+
+namespace {
+
+constexpr int kDefaultHMax = 256;
+constexpr int32_t kMaxImageSide = 1 << 15;
+constexpr int64_t kMaxIds = (int64_t(1) << 31) - 1;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool finite_f(float x) { return std::isfinite(x); }
+
+bool camera_ok(const gs_camera* cam) {
+    if (!cam) return false;
+    if (cam->width < 1 || cam->height < 1 || cam->width > kMaxImageSide ||
+        cam->height > kMaxImageSide)
+        return false;
+    for (int i = 0; i < 16; ++i)
+        if (!finite_f(cam->viewmat[i])) return false;
+    if (!finite_f(cam->fx) || !finite_f(cam->fy) || !finite_f(cam->cx) || !finite_f(cam->cy))
+        return false;
+    if (!(cam->znear > 0.f) || !finite_f(cam->znear)) return false;
+    return true;
+}
+
+CamParams cam_params(const gs_camera* cam) {
+    CamParams c{};
+    for (int r = 0; r < 3; ++r)
+        for (int k = 0; k < 4; ++k) c.V[4 * r + k] = cam->viewmat[4 * r + k];
+    c.fx = cam->fx;
+    c.fy = cam->fy;
+    c.cx = cam->cx;
+    c.cy = cam->cy;
+    c.znear = cam->znear;
+    c.W = cam->width;
+    c.H = cam->height;
+    c.ntx = (cam->width + GS_TILE - 1) / GS_TILE;
+    c.nty = (cam->height + GS_TILE - 1) / GS_TILE;
+    // camera centre c_w = -W^T t_v
+    for (int j = 0; j < 3; ++j) {
+        double acc = 0.0;
+        for (int r = 0; r < 3; ++r) acc -= (double)cam->viewmat[4 * r + j] * cam->viewmat[4 * r + 3];
+        c.cw[j] = (float)acc;
+    }
+    return c;
+}
+
+bool settings_ok(const gs_settings* s) {
+    if (s->split_mode < 0 || s->split_mode > 2) return false;
+    if (s->h_max < 1 || s->h_max > 65536) return false;
+    if (s->split_mode == 2) {
+        if (s->force_h < 0 || s->force_h > s->h_max) return false;
+        if (s->force_h > 0 && (s->force_k < 2 || s->force_k > GS_MAX_CHUNKS)) return false;
+    }
+    if (!(s->policy_lambda >= 0.f) || !(s->policy_beta >= 0.f) || !finite_f(s->policy_lambda) ||
+        !finite_f(s->policy_beta))
+        return false;
+    if (!(s->policy_eps >= 0.f && s->policy_eps < 1.f)) return false;
+    return true;
+}
+
+RasterConfig raster_config(const gs_settings* s) {
+    RasterConfig c{};
+    c.split_mode = s->split_mode;
+    c.force_h = s->force_h;
+    c.force_k = s->force_k;
+    c.h_max = s->h_max;
+    c.lambda = s->policy_lambda;
+    c.beta = s->policy_beta;
+    c.eps = s->policy_eps;
+    return c;
+}
+
+gs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GS_OK : GS_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+gs_settings gs_default_settings(void) {
+    gs_settings s;
+    s.split_mode = 0;
+    s.force_h = 0;
+    s.force_k = 4;
+    s.h_max = kDefaultHMax;
+    s.policy_lambda = 256.f;
+    s.policy_beta = 0.05f;
+    s.policy_eps = 0.10f;
+    return s;
+}
+
+const char* gs_status_string(gs_status status) {
+    switch (status) {
+        case GS_OK: return "ok";
+        case GS_ERR_INVALID_ARG: return "invalid argument";
+        case GS_ERR_CUDA: return "CUDA error";
+        case GS_ERR_CAPACITY: return "pair list capacity exceeded";
+        case GS_ERR_TIMEOUT: return "device wait timed out";
+        case GS_ERR_WORKSPACE: return "workspace too small";
+        default: return "unknown status";
+    }
+}
+
+int64_t gs_num_tiles(int32_t width, int32_t height) {
+    if (width < 1 || height < 1) return 0;
+    return (int64_t)((width + GS_TILE - 1) / GS_TILE) * ((height + GS_TILE - 1) / GS_TILE);
+}
+
+gs_status gs_project(const gs_camera* cam, int64_t n, int32_t sh_degree, const float* means,
+                     const float* scales, const float* quats, const float* opacities,
+                     const float* sh, float* splats, float* depths, int32_t* radii,
+                     int32_t* tiles_touched, void* stream) {
+    if (!camera_ok(cam) || n < 0 || n > kMaxIds || sh_degree < 0 || sh_degree > 3)
+        return GS_ERR_INVALID_ARG;
+    if (n == 0) return GS_OK;
+    const void* ptrs[] = {means, scales, quats, opacities, sh, splats, depths, radii, tiles_touched};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return GS_ERR_INVALID_ARG;
+    return cuda_status(launch_project(cam_params(cam), n, sh_degree, means, scales, quats,
+                                      opacities, sh, splats, depths, radii, tiles_touched,
+                                      (cudaStream_t)stream));
+}
+
+size_t gs_bin_sort_workspace_bytes(int64_t n, int64_t capacity, int32_t width, int32_t height) {
+    if (n < 0 || n > kMaxIds || capacity < 1 || capacity > kMaxIds || width < 1 || height < 1 ||
+        width > kMaxImageSide || height > kMaxImageSide)
+        return 0;
+    return binsort_layout(n, capacity, gs_num_tiles(width, height)).total;
+}
+
+gs_status gs_bin_sort(const gs_camera* cam, int64_t n, const float* splats, const float* depths,
+                      const int32_t* tiles_touched, void* workspace, size_t workspace_bytes,
+                      int32_t* sorted_ids, int64_t capacity, int32_t* tile_ranges,
+                      int32_t* lpt_order, int64_t* counts_device, int64_t* n_pairs_host,
+                      void* stream) {
+    if (!camera_ok(cam) || n < 0 || n > kMaxIds || capacity < 1 || capacity > kMaxIds)
+        return GS_ERR_INVALID_ARG;
+    if (n > 0) {
+        const void* ptrs[] = {splats, depths, tiles_touched};
+        for (const void* p : ptrs)
+            if (!p || !aligned16(p)) return GS_ERR_INVALID_ARG;
+    }
+    const void* outs[] = {workspace, sorted_ids, tile_ranges, lpt_order};
+    for (const void* p : outs)
+        if (!p || !aligned16(p)) return GS_ERR_INVALID_ARG;
+    if (counts_device && (reinterpret_cast<uintptr_t>(counts_device) & 7u)) return GS_ERR_INVALID_ARG;
+    const int64_t nt = gs_num_tiles(cam->width, cam->height);
+    const BinSortLayout L = binsort_layout(n, capacity, nt);
+    if (workspace_bytes < L.total) return GS_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    char* ws = static_cast<char*>(workspace);
+    cudaError_t err = run_bin_sort(cam_params(cam), n, splats, depths, tiles_touched, ws, L,
+                                   sorted_ids, capacity, tile_ranges, lpt_order, st);
+    if (err != cudaSuccess) return GS_ERR_CUDA;
+    const int64_t* counts = reinterpret_cast<const int64_t*>(ws + L.off_counts);
+    if (counts_device) {
+        err = cudaMemcpyAsync(counts_device, counts, 2 * sizeof(int64_t), cudaMemcpyDeviceToDevice, st);
+        if (err != cudaSuccess) return GS_ERR_CUDA;
+    }
+    if (n_pairs_host) {
+        int64_t host_counts[2] = {0, 0};
+        err = cudaMemcpyAsync(host_counts, counts, 2 * sizeof(int64_t), cudaMemcpyDeviceToHost, st);
+        if (err != cudaSuccess) return GS_ERR_CUDA;
+        err = cudaStreamSynchronize(st);
+        if (err != cudaSuccess) return GS_ERR_CUDA;
+        *n_pairs_host = host_counts[1];
+        if (host_counts[1] > capacity) return GS_ERR_CAPACITY;
+    }
+    return GS_OK;
+}
+
+size_t gs_raster_workspace_bytes(int32_t width, int32_t height, const gs_settings* settings) {
+    gs_settings s = settings ? *settings : gs_default_settings();
+    if (width < 1 || height < 1 || !settings_ok(&s)) return 0;
+    return raster_layout(width, height, s.h_max).total;
+}
+
+gs_status gs_rasterize_fwd(const gs_camera* cam, const gs_settings* settings, int64_t n,
+                           const float* splats, const int32_t* sorted_ids,
+                           const int32_t* tile_ranges, const int32_t* lpt_order, void* workspace,
+                           size_t workspace_bytes, float* image, float* t_final,
+                           int32_t* n_contrib, int32_t* last_idx, void* stream) {
+    gs_settings s = settings ? *settings : gs_default_settings();
+    if (!camera_ok(cam) || !settings_ok(&s) || n < 0 || n > kMaxIds) return GS_ERR_INVALID_ARG;
+    const void* ptrs[] = {sorted_ids, tile_ranges, lpt_order, workspace, image, t_final,
+                          n_contrib, last_idx};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return GS_ERR_INVALID_ARG;
+    if (n > 0 && (!splats || !aligned16(splats))) return GS_ERR_INVALID_ARG;
+    const RasterLayout L = raster_layout(cam->width, cam->height, s.h_max);
+    if (workspace_bytes < L.total) return GS_ERR_WORKSPACE;
+    return cuda_status(run_raster_fwd(cam_params(cam), raster_config(&s), splats, sorted_ids,
+                                      tile_ranges, lpt_order, static_cast<char*>(workspace), L,
+                                      image, t_final, n_contrib, last_idx, (cudaStream_t)stream));
+}
+
+gs_status gs_rasterize_bwd(const gs_camera* cam, const gs_settings* settings, int64_t n,
+                           const float* splats, const int32_t* sorted_ids,
+                           const int32_t* tile_ranges, const int32_t* lpt_order, void* workspace,
+                           size_t workspace_bytes, const float* t_final, const int32_t* last_idx,
+                           const float* dL_dimage, const float* dL_dt_final, float* grad2d,
+                           uint8_t* touched, void* stream) {
+    gs_settings s = settings ? *settings : gs_default_settings();
+    if (!camera_ok(cam) || !settings_ok(&s) || n < 0 || n > kMaxIds) return GS_ERR_INVALID_ARG;
+    const void* ptrs[] = {sorted_ids, tile_ranges, lpt_order, workspace, t_final, last_idx,
+                          dL_dimage};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return GS_ERR_INVALID_ARG;
+    if (n > 0 && (!splats || !aligned16(splats) || !grad2d || !aligned16(grad2d)))
+        return GS_ERR_INVALID_ARG;
+    if (dL_dt_final && !aligned16(dL_dt_final)) return GS_ERR_INVALID_ARG;
+    const RasterLayout L = raster_layout(cam->width, cam->height, s.h_max);
+    if (workspace_bytes < L.total) return GS_ERR_WORKSPACE;
+    return cuda_status(run_raster_bwd(cam_params(cam), raster_config(&s), n, splats, sorted_ids,
+                                      tile_ranges, lpt_order, static_cast<char*>(workspace), L,
+                                      t_final, last_idx, dL_dimage, dL_dt_final, grad2d, touched,
+                                      (cudaStream_t)stream));
+}
+
+gs_status gs_project_bwd(const gs_camera* cam, int64_t n, int32_t sh_degree, const float* means,
+                         const float* scales, const float* quats, const float* opacities,
+                         const float* sh, const int32_t* tiles_touched, const float* grad2d,
+                         const uint8_t* touched, float* dmeans, float* dscales, float* dquats,
+                         float* dopacities, float* dsh, void* stream) {
+    if (!camera_ok(cam) || n < 0 || n > kMaxIds || sh_degree < 0 || sh_degree > 3)
+        return GS_ERR_INVALID_ARG;
+    if (n == 0) return GS_OK;
+    const void* ptrs[] = {means, scales, quats, sh, tiles_touched, grad2d,
+                          dmeans, dscales, dquats, dopacities, dsh};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return GS_ERR_INVALID_ARG;
+    return cuda_status(launch_project_bwd(cam_params(cam), n, sh_degree, means, scales, quats,
+                                          opacities, sh, tiles_touched, grad2d, touched, dmeans,
+                                          dscales, dquats, dopacities, dsh, (cudaStream_t)stream));
+}
+
+gs_status gs_raster_stats(const void* workspace, size_t workspace_bytes, int64_t* out,
+                          void* stream) {
+    if (!workspace || !out || workspace_bytes < kCtlWords * sizeof(int)) return GS_ERR_INVALID_ARG;
+    int ctrl[kCtlWords];
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t err = cudaMemcpyAsync(ctrl, workspace, sizeof(ctrl), cudaMemcpyDeviceToHost, st);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(st);
+    if (err != cudaSuccess) return GS_ERR_CUDA;
+    for (int i = 0; i < 8; ++i) out[i] = 0;
+    out[0] = ctrl[kCtlH];
+    out[1] = ctrl[kCtlK];
+    out[2] = ctrl[kCtlResident];
+    out[3] = ctrl[kCtlItems];
+    out[4] = ctrl[kCtlError];
+    return GS_OK;
+}
+
+}  // extern "C"

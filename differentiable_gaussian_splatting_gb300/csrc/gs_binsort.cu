@@ -1,0 +1,510 @@
+// gs_binsort.cu -- tile binning and the two-stage radix sort.
+//
+// "What the 3DGS Literature Left on the Table" (Kopanas), Step 1 (b): each
+// visible splat's tiles come from exact per-row spans of its support ellipse;
+// Step 1 (d): the visible Gaussians are sorted once by a 32-bit depth key and
+// the (tile, Gaussian) pairs, emitted in that depth order, are then sorted by
+// a narrow tile key with a stable radix sort.  "Mitigating SM-Level Load
+// Imbalance in 3D Gaussian Splatting on GPUs" (Ryu & Yoo), Sec. 4.1: the tile
+// indices are radix-sorted by descending pair count (LPT order).
+//
+// Everything stays on the device: element counts that depend on the data
+// (visible Gaussians M, pairs I) are read by the kernels from device memory,
+// so the whole call can run without a host synchronisation.
+//
+// Radix sort: LSD, 8-bit digits, per pass three kernels -- per-block digit
+// counts (upsweep), an exclusive scan of every digit's row of block counts
+// (one block per digit), and a stable scatter in which each warp ranks its
+// keys with __match_any_sync and each block combines its warps' counts.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "gs_device.cuh"
+#include "gs_internal.h"
+
+namespace gs {
+
+namespace {
+
+constexpr int kRsBlock = 256;
+constexpr int kRsIpt = 16;
+constexpr int kRsTile = kRsBlock * kRsIpt;  // 4096 keys per block
+constexpr int kRsWarps = kRsBlock / 32;
+constexpr int kScanThreads = 1024;
+
+__host__ __device__ inline int64_t nblk_of(int64_t n) { return (n + kRsTile - 1) / kRsTile; }
+
+__device__ __forceinline__ int64_t count_of(const int64_t* n_dev, int64_t n_static) {
+    return n_dev ? *n_dev : n_static;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// exclusive scan of one value per thread over a block of kRsBlock threads
+template <typename T>
+__device__ __forceinline__ T block_exclusive_scan_256(T v, T* s_warp, T* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    T x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        T y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        T w = lane < kRsWarps ? s_warp[lane] : T(0);
+#pragma unroll
+        for (int o = 1; o < kRsWarps; o <<= 1) {
+            T y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < kRsWarps) s_warp[lane] = w;  // inclusive warp prefix
+    }
+    __syncthreads();
+    T warp_excl = warp > 0 ? s_warp[warp - 1] : T(0);
+    *total = s_warp[kRsWarps - 1];
+    __syncthreads();
+    return warp_excl + x - v;
+}
+
+// ---------------------------------------------------------------------------
+// radix sort kernels
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kRsBlock) rs_upsweep(const uint32_t* __restrict__ keys,
+                                                       const int64_t* n_dev, int64_t n_static,
+                                                       int shift, uint32_t* __restrict__ hist) {
+    const int64_t n = count_of(n_dev, n_static);
+    const int64_t nblk = nblk_of(n);
+    const int64_t b = blockIdx.x;
+    if (b >= nblk) return;
+    __shared__ uint32_t cnt[256];
+    cnt[threadIdx.x] = 0;
+    __syncthreads();
+    const int64_t base = b * kRsTile;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < kRsTile; i += kRsBlock) {
+        int64_t idx = base + i;
+        if (idx < n) atomicAdd(&cnt[(__ldg(keys + idx) >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    hist[(int64_t)threadIdx.x * nblk + b] = cnt[threadIdx.x];
+}
+
+// one block per digit: exclusive scan of the digit's row of block counts
+__global__ void __launch_bounds__(kRsBlock) rs_scan_rows(uint32_t* __restrict__ hist,
+                                                         const int64_t* n_dev, int64_t n_static,
+                                                         uint32_t* __restrict__ dtot) {
+    const int64_t n = count_of(n_dev, n_static);
+    const int64_t nblk = nblk_of(n);
+    const int d = blockIdx.x;
+    __shared__ uint32_t s_warp[kRsWarps];
+    uint32_t* row = hist + (int64_t)d * nblk;
+    const int64_t per = (nblk + kRsBlock - 1) / kRsBlock;
+    const int64_t lo = min64(nblk, per * threadIdx.x);
+    const int64_t hi = min64(nblk, lo + per);
+    uint32_t sum = 0;
+    for (int64_t j = lo; j < hi; ++j) sum += row[j];
+    uint32_t total;
+    uint32_t run = block_exclusive_scan_256<uint32_t>(sum, s_warp, &total);
+    for (int64_t j = lo; j < hi; ++j) {
+        uint32_t c = row[j];
+        row[j] = run;
+        run += c;
+    }
+    if (threadIdx.x == 0) dtot[d] = total;
+}
+
+__global__ void __launch_bounds__(kRsBlock) rs_downsweep(
+    const uint32_t* __restrict__ keys_in, const int32_t* __restrict__ vals_in,
+    uint32_t* __restrict__ keys_out, int32_t* __restrict__ vals_out, const int64_t* n_dev,
+    int64_t n_static, int shift, const uint32_t* __restrict__ hist,
+    const uint32_t* __restrict__ dtot) {
+    const int64_t n = count_of(n_dev, n_static);
+    const int64_t nblk = nblk_of(n);
+    const int64_t b = blockIdx.x;
+    if (b >= nblk) return;
+    __shared__ uint32_t s_base[256];
+    __shared__ uint32_t s_wcnt[kRsWarps][256];
+    __shared__ uint32_t s_warp[kRsWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int w = 0; w < kRsWarps; ++w) s_wcnt[w][tid] = 0;
+    {
+        uint32_t total;
+        uint32_t dbase = block_exclusive_scan_256<uint32_t>(dtot[tid], s_warp, &total);
+        s_base[tid] = dbase + hist[(int64_t)tid * nblk + b];
+    }
+    __syncthreads();
+
+    const int64_t wbase = b * kRsTile + (int64_t)warp * (32 * kRsIpt);
+    uint32_t k[kRsIpt];
+    int32_t v[kRsIpt];
+    uint32_t loc[kRsIpt];
+#pragma unroll
+    for (int r = 0; r < kRsIpt; ++r) {
+        const int64_t idx = wbase + r * 32 + lane;
+        const bool valid = idx < n;
+        k[r] = valid ? __ldg(keys_in + idx) : 0u;
+        v[r] = valid ? __ldg(vals_in + idx) : 0;
+        const uint32_t d = (k[r] >> shift) & 255u;
+        const uint32_t peers = __match_any_sync(0xffffffffu, valid ? d : 256u + lane);
+        const uint32_t rank = __popc(peers & lanemask_lt());
+        const uint32_t prev = s_wcnt[warp][d & 255u];
+        loc[r] = prev + rank;
+        __syncwarp();
+        if (valid && rank == 0) s_wcnt[warp][d] = prev + __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    {
+        uint32_t run = 0;
+#pragma unroll
+        for (int w = 0; w < kRsWarps; ++w) {
+            uint32_t c = s_wcnt[w][tid];
+            s_wcnt[w][tid] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kRsIpt; ++r) {
+        const int64_t idx = wbase + r * 32 + lane;
+        if (idx < n) {
+            const uint32_t d = (k[r] >> shift) & 255u;
+            const uint32_t pos = s_base[d] + s_wcnt[warp][d] + loc[r];
+            keys_out[pos] = k[r];
+            vals_out[pos] = v[r];
+        }
+    }
+}
+
+// Stable LSD radix sort of (keys, vals) on bits [0, bits).  The count is read
+// from n_dev (device) when given, else n_static; n_max bounds it.  Passes
+// ping-pong between (k0, v0) and (k1, v1), starting from (k0, v0).  The last
+// pass writes its values to vf when given (a buffer distinct from v0, v1) and
+// its keys to the scratch buffer the pass did not read; *kres / *vres return
+// where the sorted keys and values are.
+cudaError_t radix_sort(uint32_t* k0, int32_t* v0, uint32_t* k1, int32_t* v1, int32_t* vf,
+                       const int64_t* n_dev, int64_t n_static, int64_t n_max, int bits,
+                       uint32_t* hist, uint32_t* dtot, cudaStream_t st, uint32_t** kres,
+                       int32_t** vres) {
+    const int passes = std::max(1, (bits + 7) / 8);
+    const unsigned grid = (unsigned)std::max<int64_t>(1, nblk_of(n_max));
+    uint32_t* kin = k0;
+    int32_t* vin = v0;
+    for (int p = 0; p < passes; ++p) {
+        const bool last = p == passes - 1;
+        uint32_t* kout = kin == k0 ? k1 : k0;
+        int32_t* vout = (last && vf) ? vf : (vin == v0 ? v1 : v0);
+        const int shift = 8 * p;
+        rs_upsweep<<<grid, kRsBlock, 0, st>>>(kin, n_dev, n_static, shift, hist);
+        rs_scan_rows<<<256, kRsBlock, 0, st>>>(hist, n_dev, n_static, dtot);
+        rs_downsweep<<<grid, kRsBlock, 0, st>>>(kin, vin, kout, vout, n_dev, n_static, shift, hist,
+                                                dtot);
+        kin = kout;
+        vin = vout;
+    }
+    if (kres) *kres = kin;
+    if (vres) *vres = vin;
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// scans: per-block sums, a single-block scan of the sums, per-block writes
+// ---------------------------------------------------------------------------
+// exclusive scan in place of bsum[0 .. nb), nb = ceil(count / kRsTile);
+// count = *count_dev (or count_static).  Writes the grand total to *total_out
+// and min(total, cap) to *capped_out (if given).
+__global__ void __launch_bounds__(kScanThreads) scan_block_sums(int64_t* __restrict__ bsum,
+                                                                const int64_t* count_dev,
+                                                                int64_t count_static,
+                                                                int64_t* total_out,
+                                                                int64_t cap, int64_t* capped_out) {
+    const int64_t nb = nblk_of(count_of(count_dev, count_static));
+    __shared__ int64_t s_part[kScanThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t per = (nb + kScanThreads - 1) / kScanThreads;
+    const int64_t lo = min64(nb, per * tid), hi = min64(nb, lo + per);
+    int64_t sum = 0;
+    for (int64_t j = lo; j < hi; ++j) sum += bsum[j];
+    int64_t x = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_part[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t w = s_part[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        s_part[lane] = w;
+    }
+    __syncthreads();
+    int64_t run = (warp > 0 ? s_part[warp - 1] : 0) + x - sum;
+    for (int64_t j = lo; j < hi; ++j) {
+        int64_t c = bsum[j];
+        bsum[j] = run;
+        run += c;
+    }
+    if (tid == kScanThreads - 1) {
+        int64_t total = s_part[31];
+        *total_out = total;
+        if (capped_out) *capped_out = total < cap ? total : cap;
+    }
+}
+
+// visible Gaussians: per-block counts
+__global__ void __launch_bounds__(kRsBlock) vis_count(const int32_t* __restrict__ tiles_touched,
+                                                      int64_t n, int64_t* __restrict__ bsum) {
+    __shared__ int64_t s_warp[kRsWarps];
+    const int64_t base = (int64_t)blockIdx.x * kRsTile;
+    int64_t c = 0;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < kRsTile; i += kRsBlock) {
+        int64_t idx = base + i;
+        if (idx < n && tiles_touched[idx] > 0) ++c;
+    }
+    int64_t total;
+    block_exclusive_scan_256<int64_t>(c, s_warp, &total);
+    if (threadIdx.x == 0) bsum[blockIdx.x] = total;
+}
+
+// visible Gaussians, in id order: (depth key, id)
+__global__ void __launch_bounds__(kRsBlock) vis_write(const int32_t* __restrict__ tiles_touched,
+                                                      const float* __restrict__ depths, int64_t n,
+                                                      const int64_t* __restrict__ bsum,
+                                                      uint32_t* __restrict__ keys,
+                                                      int32_t* __restrict__ vals) {
+    __shared__ int64_t s_warp[kRsWarps];
+    const int64_t base = (int64_t)blockIdx.x * kRsTile;
+    int64_t run = bsum[blockIdx.x];
+    for (int r = 0; r < kRsIpt; ++r) {
+        const int64_t idx = base + (int64_t)r * kRsBlock + threadIdx.x;
+        const bool vis = idx < n && tiles_touched[idx] > 0;
+        int64_t total;
+        int64_t off = block_exclusive_scan_256<int64_t>(vis ? 1 : 0, s_warp, &total);
+        if (vis) {
+            keys[run + off] = __float_as_uint(depths[idx]);  // depth > znear > 0: bits are ordered
+            vals[run + off] = (int32_t)idx;
+        }
+        run += total;
+    }
+}
+
+// pairs per visible Gaussian in depth order: per-block sums
+__global__ void __launch_bounds__(kRsBlock) pairs_count(const int32_t* __restrict__ order,
+                                                        const int32_t* __restrict__ tiles_touched,
+                                                        const int64_t* __restrict__ m_dev,
+                                                        int64_t* __restrict__ bsum) {
+    const int64_t m = *m_dev;
+    if ((int64_t)blockIdx.x >= nblk_of(m)) return;
+    __shared__ int64_t s_warp[kRsWarps];
+    const int64_t base = (int64_t)blockIdx.x * kRsTile;
+    int64_t c = 0;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < kRsTile; i += kRsBlock) {
+        int64_t j = base + i;
+        if (j < m) c += tiles_touched[order[j]];
+    }
+    int64_t total;
+    block_exclusive_scan_256<int64_t>(c, s_warp, &total);
+    if (threadIdx.x == 0) bsum[blockIdx.x] = total;
+}
+
+__global__ void __launch_bounds__(kRsBlock) pairs_offsets(const int32_t* __restrict__ order,
+                                                          const int32_t* __restrict__ tiles_touched,
+                                                          const int64_t* __restrict__ m_dev,
+                                                          const int64_t* __restrict__ bsum,
+                                                          int64_t* __restrict__ poff) {
+    const int64_t m = *m_dev;
+    if ((int64_t)blockIdx.x >= nblk_of(m)) return;
+    __shared__ int64_t s_warp[kRsWarps];
+    const int64_t base = (int64_t)blockIdx.x * kRsTile;
+    int64_t run = bsum[blockIdx.x];
+    for (int r = 0; r < kRsIpt; ++r) {
+        const int64_t j = base + (int64_t)r * kRsBlock + threadIdx.x;
+        const int64_t c = j < m ? (int64_t)tiles_touched[order[j]] : 0;
+        int64_t total;
+        int64_t off = block_exclusive_scan_256<int64_t>(c, s_warp, &total);
+        if (j < m) poff[j] = run + off;
+        run += total;
+    }
+}
+
+// emit (tile, Gaussian) pairs in depth order from the exact row spans
+__global__ void __launch_bounds__(256) emit_pairs(CamParams cam, const float4* __restrict__ splats,
+                                                  const int32_t* __restrict__ order,
+                                                  const int64_t* __restrict__ poff,
+                                                  const int64_t* __restrict__ m_dev,
+                                                  int64_t capacity, uint32_t* __restrict__ pkeys,
+                                                  int32_t* __restrict__ pvals) {
+    const int64_t m = *m_dev;
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < m;
+         j += (int64_t)gridDim.x * blockDim.x) {
+        const int32_t g = order[j];
+        int64_t off = poff[j];
+        const float4 r0 = __ldg(splats + 3 * (int64_t)g), r1 = __ldg(splats + 3 * (int64_t)g + 1),
+                     r2 = __ldg(splats + 3 * (int64_t)g + 2);
+        const Ellipse e = ellipse_of(r0, r1, r2);
+        int ty0, ty1, tx0, tx1;
+        row_range(e, cam.nty, &ty0, &ty1);
+        for (int ty = ty0; ty < ty1; ++ty) {
+            if (!row_span(e, ty, cam.W, cam.H, cam.ntx, &tx0, &tx1)) continue;
+            const uint32_t rowkey = (uint32_t)ty * (uint32_t)cam.ntx;
+            for (int tx = tx0; tx < tx1; ++tx, ++off) {
+                if (off < capacity) {
+                    pkeys[off] = rowkey + (uint32_t)tx;
+                    pvals[off] = g;
+                }
+            }
+        }
+    }
+}
+
+// tile ranges [start, end) from the sorted keys (ranges zeroed beforehand)
+__global__ void tile_ranges_kernel(const uint32_t* __restrict__ keys, const int64_t* __restrict__ n_dev,
+                                   int2* __restrict__ ranges) {
+    const int64_t n = *n_dev;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint32_t t = keys[i];
+        if (i == 0 || keys[i - 1] != t) ranges[t].x = (int)i;
+        if (i == n - 1 || keys[i + 1] != t) ranges[t].y = (int)(i + 1);
+    }
+}
+
+// LPT keys: descending pair count = ascending (maxk - count); stable -> ties by tile id
+__global__ void lpt_keys_kernel(const int2* __restrict__ ranges, int64_t nt, uint32_t maxk,
+                                uint32_t* __restrict__ keys, int32_t* __restrict__ vals) {
+    int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= nt) return;
+    int2 r = ranges[t];
+    keys[t] = maxk - (uint32_t)(r.y - r.x);
+    vals[t] = (int32_t)t;
+}
+
+size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+int bits_for(int64_t v) {
+    int b = 0;
+    while (b < 62 && (int64_t(1) << b) <= v) ++b;
+    return std::max(b, 1);
+}
+
+}  // namespace
+
+BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles) {
+    BinSortLayout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off = align_up(off + bytes);
+        return o;
+    };
+    const int64_t nn = std::max<int64_t>(n, 1), cap = std::max<int64_t>(capacity, 1);
+    const int64_t nt = std::max<int64_t>(n_tiles, 1);
+    const int64_t hist_blocks = nblk_of(std::max({nn, cap, nt}));
+    L.off_counts = take(4 * sizeof(int64_t));
+    L.off_bsum = take((size_t)(nblk_of(nn) + 1) * sizeof(int64_t));
+    L.off_dkeys0 = take((size_t)nn * 4);
+    L.off_dkeys1 = take((size_t)nn * 4);
+    L.off_dvals0 = take((size_t)nn * 4);
+    L.off_dvals1 = take((size_t)nn * 4);
+    L.off_poff = take((size_t)(nn + 1) * sizeof(int64_t));
+    L.off_pkeys0 = take((size_t)cap * 4);
+    L.off_pkeys1 = take((size_t)cap * 4);
+    L.off_pvals0 = take((size_t)cap * 4);
+    L.off_pvals1 = take((size_t)cap * 4);
+    L.off_hist = take((size_t)256 * hist_blocks * 4);
+    L.off_dtot = take(256 * 4);
+    L.off_lkeys0 = take((size_t)nt * 4);
+    L.off_lkeys1 = take((size_t)nt * 4);
+    L.off_lvals0 = take((size_t)nt * 4);
+    L.off_lvals1 = take((size_t)nt * 4);
+    L.total = off;
+    return L;
+}
+
+cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, const float* depths,
+                         const int32_t* tiles_touched, char* ws, const BinSortLayout& L,
+                         int32_t* sorted_ids, int64_t capacity, int32_t* tile_ranges,
+                         int32_t* lpt_order, cudaStream_t st) {
+    auto* counts = reinterpret_cast<int64_t*>(ws + L.off_counts);
+    auto* bsum = reinterpret_cast<int64_t*>(ws + L.off_bsum);
+    auto* dk0 = reinterpret_cast<uint32_t*>(ws + L.off_dkeys0);
+    auto* dk1 = reinterpret_cast<uint32_t*>(ws + L.off_dkeys1);
+    auto* dv0 = reinterpret_cast<int32_t*>(ws + L.off_dvals0);
+    auto* dv1 = reinterpret_cast<int32_t*>(ws + L.off_dvals1);
+    auto* poff = reinterpret_cast<int64_t*>(ws + L.off_poff);
+    auto* pk0 = reinterpret_cast<uint32_t*>(ws + L.off_pkeys0);
+    auto* pk1 = reinterpret_cast<uint32_t*>(ws + L.off_pkeys1);
+    auto* pv0 = reinterpret_cast<int32_t*>(ws + L.off_pvals0);
+    auto* pv1 = reinterpret_cast<int32_t*>(ws + L.off_pvals1);
+    auto* hist = reinterpret_cast<uint32_t*>(ws + L.off_hist);
+    auto* dtot = reinterpret_cast<uint32_t*>(ws + L.off_dtot);
+    auto* lk0 = reinterpret_cast<uint32_t*>(ws + L.off_lkeys0);
+    auto* lk1 = reinterpret_cast<uint32_t*>(ws + L.off_lkeys1);
+    auto* lv0 = reinterpret_cast<int32_t*>(ws + L.off_lvals0);
+    auto* lv1 = reinterpret_cast<int32_t*>(ws + L.off_lvals1);
+    const int64_t nt = (int64_t)cam.ntx * cam.nty;
+    cudaError_t err;
+
+    err = cudaMemsetAsync(counts, 0, 4 * sizeof(int64_t), st);
+    if (err != cudaSuccess) return err;
+    err = cudaMemsetAsync(tile_ranges, 0, (size_t)nt * 2 * sizeof(int32_t), st);
+    if (err != cudaSuccess) return err;
+
+    if (n > 0) {
+        const unsigned nb = (unsigned)nblk_of(n);
+        // 1. compact the visible Gaussians (id order) into (depth key, id)
+        vis_count<<<nb, kRsBlock, 0, st>>>(tiles_touched, n, bsum);
+        scan_block_sums<<<1, kScanThreads, 0, st>>>(bsum, nullptr, n, counts + 0, 0, nullptr);
+        vis_write<<<nb, kRsBlock, 0, st>>>(tiles_touched, depths, n, bsum, dk0, dv0);
+        // 2. stable depth sort of the M visible (31 significant key bits)
+        uint32_t* dks = nullptr;
+        int32_t* dvs = nullptr;
+        err = radix_sort(dk0, dv0, dk1, dv1, nullptr, counts + 0, 0, n, 31, hist, dtot, st, &dks,
+                         &dvs);
+        if (err != cudaSuccess) return err;
+        // 3. pair offsets in depth order, I = total, min(I, capacity)
+        pairs_count<<<nb, kRsBlock, 0, st>>>(dvs, tiles_touched, counts + 0, bsum);
+        scan_block_sums<<<1, kScanThreads, 0, st>>>(bsum, counts + 0, 0, counts + 1, capacity,
+                                                     counts + 2);
+        pairs_offsets<<<nb, kRsBlock, 0, st>>>(dvs, tiles_touched, counts + 0, bsum, poff);
+        // 4. emit pairs in depth order
+        const unsigned eg = (unsigned)std::min<int64_t>((n + 255) / 256, 65535);
+        emit_pairs<<<eg, 256, 0, st>>>(cam, reinterpret_cast<const float4*>(splats), dvs, poff,
+                                       counts + 0, capacity, pk0, pv0);
+        // 5. stable sort by tile key; values land in sorted_ids
+        uint32_t* pks = nullptr;
+        err = radix_sort(pk0, pv0, pk1, pv1, sorted_ids, counts + 2, 0, capacity,
+                         bits_for(nt - 1), hist, dtot, st, &pks, nullptr);
+        if (err != cudaSuccess) return err;
+        // 6. tile ranges
+        tile_ranges_kernel<<<1024, 256, 0, st>>>(pks, counts + 2, reinterpret_cast<int2*>(tile_ranges));
+    }
+    // 7. LPT order: tiles by descending count, ties by tile id
+    {
+        const int bits = bits_for(std::max<int64_t>(capacity, 1));
+        const uint32_t maxk = bits >= 32 ? 0xffffffffu : ((1u << bits) - 1u);
+        lpt_keys_kernel<<<(unsigned)((nt + 255) / 256), 256, 0, st>>>(
+            reinterpret_cast<const int2*>(tile_ranges), nt, maxk, lk0, lv0);
+        err = radix_sort(lk0, lv0, lk1, lv1, lpt_order, nullptr, nt, nt, bits, hist, dtot, st,
+                         nullptr, nullptr);
+        if (err != cudaSuccess) return err;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace gs

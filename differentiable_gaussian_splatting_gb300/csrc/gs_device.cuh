@@ -1,0 +1,163 @@
+// gs_device.cuh -- device helpers shared by the libgs kernels (sm_103a).
+//
+// The projection chain, the tile spans and the per-pixel quadratic decide
+// integers (radii, tile counts, pair lists, hit tests).  They are written
+// with explicit round-to-nearest intrinsics in one fixed operation order so
+// that no multiply-add is contracted and every result is reproducible bit for
+// bit, as the hit test must be ("What the 3DGS Literature Left on the Table",
+// Step 5: exact round-to-nearest quadratic evaluation).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gs {
+
+constexpr int kTile = 16;
+constexpr float kTMin = 1e-4f;
+constexpr float kAlphaMax = 0.99f;
+constexpr float kNegHalfLog2e = -0.72134752044448170368f;  // -log2(e) / 2
+constexpr float kPadUnit = 0.00390625f;                     // 2^-8 px
+constexpr float kPadScale = 6.103515625e-05f;               // 2^-14
+constexpr int kRadiusMax = 1 << 30;
+constexpr int kMaxChunks = 16;  // largest k of the chunking policy
+
+__host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+// ---------------------------------------------------------------------------
+// round-to-nearest fp32 arithmetic (never contracted)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float rmul(float a, float b) { return __fmul_rn(a, b); }
+__device__ __forceinline__ float radd(float a, float b) { return __fadd_rn(a, b); }
+__device__ __forceinline__ float rsub(float a, float b) { return __fsub_rn(a, b); }
+__device__ __forceinline__ float rdiv(float a, float b) { return __fdiv_rn(a, b); }
+__device__ __forceinline__ float rsqrt_exact(float a) { return __fsqrt_rn(a); }
+__device__ __forceinline__ float rfma(float a, float b, float c) { return __fmaf_rn(a, b, c); }
+// min / max with the semantics of `x < y ? x : y` (no NaN special-casing)
+__device__ __forceinline__ float smin(float x, float y) { return x < y ? x : y; }
+__device__ __forceinline__ float smax(float x, float y) { return x > y ? x : y; }
+
+// 2^x on the SFU (flush-to-zero); results are tested against the oracle's exp()
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ int to_int_clamped(float f, int lo, int hi) {
+    if (!(f >= (float)lo)) return lo;
+    if (f > (float)hi) return hi;
+    return (int)f;
+}
+
+// ---------------------------------------------------------------------------
+// splat record: three float4 per splat (48 bytes, 16-byte aligned)
+//   r0 = (mux, muy, a, b)   r1 = (c, tau, log2 o, rx)   r2 = (r, g, b, ry)
+// ---------------------------------------------------------------------------
+struct Ellipse {
+    float mux, muy, a, b, c, tau, rx, ry;
+};
+
+__device__ __forceinline__ Ellipse ellipse_of(const float4& r0, const float4& r1, const float4& r2) {
+    return Ellipse{r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.w, r2.w};
+}
+
+// ---------------------------------------------------------------------------
+// exact row spans ("What the 3DGS Literature Left on the Table", Step 1 (b))
+// ---------------------------------------------------------------------------
+// The support ellipse q(d) <= tau has right boundary
+//   x_r(dy) = (sqrt(a tau - detL dy^2) - b dy) / a,
+// concave in dy with its vertex at dy = -b rx / c; the left boundary is
+// x_l(dy) = -x_r(-dy).  Bands are widened by pady and extents by padx,
+// pad = 2^-8 px + r 2^-14, so that every pixel whose fp32 hit test passes
+// lies in an emitted tile.
+__device__ __forceinline__ float xr_at(const Ellipse& s, float detL, float dy) {
+    float disc = rsub(rmul(s.a, s.tau), rmul(detL, rmul(dy, dy)));
+    if (!(disc > 0.f)) disc = 0.f;
+    return rdiv(rsub(rsqrt_exact(disc), rmul(s.b, dy)), s.a);
+}
+
+__device__ __forceinline__ float pad_of(float r) { return radd(kPadUnit, rmul(r, kPadScale)); }
+
+// x-extent [*Xlo, *Xhi] of the padded support over the y band [y0, y1] (pixel
+// coordinates, y1 already clipped to the image); false if the band misses it.
+__device__ __forceinline__ bool band_extent(const Ellipse& s, float y0, float y1, float* Xlo,
+                                            float* Xhi) {
+    float padx = pad_of(s.rx);
+    float ryp = radd(s.ry, pad_of(s.ry));
+    float lo = smax(rsub(y0, s.muy), -ryp);
+    float hi = smin(rsub(y1, s.muy), ryp);
+    if (!(lo <= hi)) return false;
+    float detL = rsub(rmul(s.a, s.c), rmul(s.b, s.b));
+    float dyv = -rdiv(rmul(s.b, s.rx), s.c);
+    float dh = smin(smax(smin(smax(dyv, lo), hi), -s.ry), s.ry);
+    float dl = smin(smax(smin(smax(dyv, -hi), -lo), -s.ry), s.ry);
+    float xhi = radd(xr_at(s, detL, dh), padx);
+    float xlo_neg = radd(xr_at(s, detL, dl), padx);
+    *Xhi = radd(s.mux, xhi);
+    *Xlo = rsub(s.mux, xlo_neg);
+    return true;
+}
+
+// Rows [*ty0, *ty1) the padded support may cover.
+__device__ __forceinline__ void row_range(const Ellipse& s, int nty, int* ty0, int* ty1) {
+    float ryp = radd(s.ry, pad_of(s.ry));
+    float f0 = ceilf(rmul(rsub(rsub(s.muy, ryp), 15.5f), 0.0625f));
+    float f1 = radd(floorf(rmul(rsub(radd(s.muy, ryp), 0.5f), 0.0625f)), 1.0f);
+    *ty0 = to_int_clamped(f0, 0, nty);
+    *ty1 = to_int_clamped(f1, 0, nty);
+}
+
+// Tile columns [*tx0, *tx1) of row ty; false when empty.  A tile's region is
+// the closed hull of its pixel centres, clipped to the W x H image.
+__device__ __forceinline__ bool row_span(const Ellipse& s, int ty, int W, int H, int ntx, int* tx0,
+                                         int* tx1) {
+    float y0 = radd((float)(16 * ty), 0.5f);
+    float y1 = smin(radd((float)(16 * ty), 15.5f), rsub((float)H, 0.5f));
+    float Xlo, Xhi;
+    if (!band_extent(s, y0, y1, &Xlo, &Xhi)) return false;
+    if (Xlo > rsub((float)W, 0.5f) || Xhi < 0.5f) return false;
+    float f0 = ceilf(rmul(rsub(Xlo, 15.5f), 0.0625f));
+    float f1 = radd(floorf(rmul(rsub(Xhi, 0.5f), 0.0625f)), 1.0f);
+    *tx0 = to_int_clamped(f0, 0, ntx);
+    *tx1 = to_int_clamped(f1, 0, ntx);
+    return *tx0 < *tx1;
+}
+
+// ---------------------------------------------------------------------------
+// per-pixel quadratic: q = fma(fma(c, dy, B), dy, A), A = (a dx) dx, B = (2b) dx
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float quad_A(float a, float dx) { return rmul(rmul(a, dx), dx); }
+__device__ __forceinline__ float quad_B(float b, float dx) { return rmul(rmul(2.0f, b), dx); }
+__device__ __forceinline__ float quad_q(float c, float A, float B, float dy) {
+    return rfma(rfma(c, dy, B), dy, A);
+}
+
+// ---------------------------------------------------------------------------
+// 8x4 sub-tile mask ("What the 3DGS Literature Left on the Table", Step 1 (c)):
+// bit w set iff the padded support meets the pixel-centre hull of the 8x4
+// sub-tile of warp w (warp w covers columns 8 (w & 1) .. +7, rows 4 (w >> 1) .. +3
+// of the tile).  Conservative: every hit pixel of a warp has its bit set.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t subtile_mask(const Ellipse& s, int tx, int ty, int W, int H) {
+    uint32_t m = 0;
+    const float xb = (float)(16 * tx);
+    const float xl0 = radd(xb, 0.5f), xl1 = radd(xb, 7.5f);
+    const float xr0 = radd(xb, 8.5f);
+    const float xr1 = smin(radd(xb, 15.5f), rsub((float)W, 0.5f));
+    const float ylim = rsub((float)H, 0.5f);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        float y0 = radd((float)(16 * ty + 4 * r), 0.5f);
+        if (y0 > ylim) break;
+        float y1 = smin(radd(y0, 3.0f), ylim);
+        float Xlo, Xhi;
+        if (!band_extent(s, y0, y1, &Xlo, &Xhi)) continue;
+        if (Xhi >= xl0 && Xlo <= xl1) m |= 1u << (2 * r);
+        if (xr0 <= xr1 && Xhi >= xr0 && Xlo <= xr1) m |= 1u << (2 * r + 1);
+    }
+    return m;
+}
+
+}  // namespace gs

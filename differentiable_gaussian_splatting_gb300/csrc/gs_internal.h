@@ -1,0 +1,94 @@
+// gs_internal.h -- launch parameters and kernel-launch declarations shared by
+// the libgs translation units (host and device side).  Not part of the C ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gs {
+
+// Camera as the kernels see it: rows 0..2 of the view matrix, intrinsics,
+// image and tile grid, and the camera centre in world space (for SH).
+struct CamParams {
+    float V[12];
+    float fx, fy, cx, cy, znear;
+    int W, H, ntx, nty;
+    float cw[3];
+};
+
+// ---- projection (gs_project.cu) -------------------------------------------
+cudaError_t launch_project(const CamParams& cam, int64_t n, int sh_degree, const float* means,
+                           const float* scales, const float* quats, const float* opacities,
+                           const float* sh, float* splats, float* depths, int32_t* radii,
+                           int32_t* tiles_touched, cudaStream_t st);
+
+cudaError_t launch_project_bwd(const CamParams& cam, int64_t n, int sh_degree, const float* means,
+                               const float* scales, const float* quats, const float* opacities,
+                               const float* sh, const int32_t* tiles_touched, const float* grad2d,
+                               const uint8_t* touched, float* dmeans, float* dscales,
+                               float* dquats, float* dopacities, float* dsh, cudaStream_t st);
+
+// ---- binning + sort (gs_binsort.cu) ---------------------------------------
+struct BinSortLayout {
+    size_t total;
+    size_t off_counts;   // int64[4]: M, I, pad, pad
+    size_t off_bsum;     // int64[nblk_n + 1] scan block sums
+    size_t off_dkeys0, off_dkeys1, off_dvals0, off_dvals1;  // uint32 / int32 [n]
+    size_t off_poff;     // int64[n + 1]: pair offsets in depth order
+    size_t off_pkeys0, off_pkeys1, off_pvals0, off_pvals1;  // [capacity]
+    size_t off_hist;     // uint32[256 * nblk_max]
+    size_t off_dtot;     // uint32[256] digit totals
+    size_t off_lkeys0, off_lkeys1, off_lvals0, off_lvals1;  // [n_tiles]
+};
+BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles);
+
+cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, const float* depths,
+                         const int32_t* tiles_touched, char* ws, const BinSortLayout& L,
+                         int32_t* sorted_ids, int64_t capacity, int32_t* tile_ranges,
+                         int32_t* lpt_order, cudaStream_t st);
+
+// ---- rasterization (gs_raster.cu) ------------------------------------------
+struct RasterConfig {
+    int split_mode, force_h, force_k, h_max;
+    float lambda, beta, eps;
+};
+
+struct RasterLayout {
+    size_t total;
+    size_t off_ctrl;     // int32[16] control words
+    size_t off_sat;      // int32[h_max] saturation flags
+    size_t off_done;     // int32[h_max] finished-chunk counters
+    size_t off_part_c;   // float4[h_max][16][256]: chunk partial (C.rgb, T)
+    size_t off_part_n;   // int2[h_max][16][256]: chunk partial (n, last)
+    size_t off_bwd;      // float4[h_max][16][256]: (T after chunk, colour behind chunk)
+};
+RasterLayout raster_layout(int W, int H, int h_max);
+
+// control word indices
+enum : int {
+    kCtlQueueFwd = 0,
+    kCtlQueueBwd = 1,
+    kCtlH = 2,
+    kCtlK = 3,
+    kCtlItems = 4,
+    kCtlResident = 5,
+    kCtlError = 6,
+    kCtlWords = 16
+};
+
+int raster_resident_ctas(int device);
+
+cudaError_t run_raster_fwd(const CamParams& cam, const RasterConfig& cfg, const float* splats,
+                           const int32_t* sorted_ids, const int32_t* tile_ranges,
+                           const int32_t* lpt_order, char* ws, const RasterLayout& L, float* image,
+                           float* t_final, int32_t* n_contrib, int32_t* last_idx, cudaStream_t st);
+
+cudaError_t run_raster_bwd(const CamParams& cam, const RasterConfig& cfg, int64_t n,
+                           const float* splats, const int32_t* sorted_ids,
+                           const int32_t* tile_ranges, const int32_t* lpt_order, char* ws,
+                           const RasterLayout& L, const float* t_final, const int32_t* last_idx,
+                           const float* dL_dimage, const float* dL_dt, float* grad2d,
+                           uint8_t* touched, cudaStream_t st);
+
+}  // namespace gs

@@ -1,0 +1,492 @@
+// gs_project.cu -- per-Gaussian projection (forward) and its chain rule
+// (backward), one thread per Gaussian, streaming from HBM.
+//
+// Forward: "Mitigating SM-Level Load Imbalance in 3D Gaussian Splatting on
+// GPUs" (Ryu & Yoo), Sec. 2.1, Eq. 1; "What the 3DGS Literature Left on the
+// Table" (Kopanas), Step 1 (b) opacity-aware support and exact spans, (c)
+// 48-byte record, (e) visibility-gated SH with 16-byte loads; Step 3 (SH
+// streamed in groups of four basis functions).
+// Backward: the chain rule of the same formulas (Kopanas, Step 3: 59 gradient
+// floats per Gaussian; culled rows are written as zeros in-kernel).
+#include <cuda_runtime.h>
+
+#include "gs_device.cuh"
+#include "gs_internal.h"
+
+namespace gs {
+
+// ---------------------------------------------------------------------------
+// real spherical harmonics, degree <= 3, no Condon-Shortley phase, in the
+// order l = 0..3, m = -l..l (polynomials of the unit view direction)
+// ---------------------------------------------------------------------------
+constexpr float kY0 = 0.28209479177387814f;   // sqrt(1 / 4pi)
+constexpr float kY1 = 0.48860251190291992f;   // sqrt(3 / 4pi)
+constexpr float kY2a = 1.0925484305920792f;   // sqrt(15 / 4pi)
+constexpr float kY2b = 0.31539156525252005f;  // sqrt(5 / 16pi)
+constexpr float kY2c = 0.54627421529603959f;  // sqrt(15 / 16pi)
+constexpr float kY3a = 0.59004358992664352f;  // sqrt(35 / 32pi)
+constexpr float kY3b = 2.8906114426405538f;   // sqrt(105 / 4pi)
+constexpr float kY3c = 0.45704579946446572f;  // sqrt(21 / 32pi)
+constexpr float kY3d = 0.37317633259011540f;  // sqrt(7 / 16pi)
+constexpr float kY3e = 1.4453057213202769f;   // sqrt(105 / 16pi)
+
+__device__ __forceinline__ void sh_values(float x, float y, float z, float Y[16]) {
+    float xx = x * x, yy = y * y, zz = z * z;
+    Y[0] = kY0;
+    Y[1] = kY1 * y;
+    Y[2] = kY1 * z;
+    Y[3] = kY1 * x;
+    Y[4] = kY2a * x * y;
+    Y[5] = kY2a * y * z;
+    Y[6] = kY2b * (3.f * zz - 1.f);
+    Y[7] = kY2a * x * z;
+    Y[8] = kY2c * (xx - yy);
+    Y[9] = kY3a * y * (3.f * xx - yy);
+    Y[10] = kY3b * x * y * z;
+    Y[11] = kY3c * y * (5.f * zz - 1.f);
+    Y[12] = kY3d * z * (5.f * zz - 3.f);
+    Y[13] = kY3c * x * (5.f * zz - 1.f);
+    Y[14] = kY3e * z * (xx - yy);
+    Y[15] = kY3a * x * (xx - 3.f * yy);
+}
+
+// Cartesian gradient of basis function k at (x, y, z).
+__device__ __forceinline__ float3 sh_grad(int k, float x, float y, float z) {
+    switch (k) {
+        case 1: return make_float3(0.f, kY1, 0.f);
+        case 2: return make_float3(0.f, 0.f, kY1);
+        case 3: return make_float3(kY1, 0.f, 0.f);
+        case 4: return make_float3(kY2a * y, kY2a * x, 0.f);
+        case 5: return make_float3(0.f, kY2a * z, kY2a * y);
+        case 6: return make_float3(0.f, 0.f, 6.f * kY2b * z);
+        case 7: return make_float3(kY2a * z, 0.f, kY2a * x);
+        case 8: return make_float3(2.f * kY2c * x, -2.f * kY2c * y, 0.f);
+        case 9: return make_float3(6.f * kY3a * x * y, 3.f * kY3a * (x * x - y * y), 0.f);
+        case 10: return make_float3(kY3b * y * z, kY3b * x * z, kY3b * x * y);
+        case 11: return make_float3(0.f, kY3c * (5.f * z * z - 1.f), 10.f * kY3c * y * z);
+        case 12: return make_float3(0.f, 0.f, kY3d * (15.f * z * z - 3.f));
+        case 13: return make_float3(kY3c * (5.f * z * z - 1.f), 0.f, 10.f * kY3c * x * z);
+        case 14: return make_float3(2.f * kY3e * x * z, -2.f * kY3e * y * z, kY3e * (x * x - y * y));
+        case 15: return make_float3(3.f * kY3a * (x * x - y * y), -6.f * kY3a * x * y, 0.f);
+        default: return make_float3(0.f, 0.f, 0.f);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// the fp32 projection chain (fixed order, round-to-nearest)
+// ---------------------------------------------------------------------------
+struct Projected {
+    bool ok;
+    float tx, ty, tz;
+    float mux, muy, a, b, c, tau, rx, ry;
+};
+
+__device__ __forceinline__ Projected project_chain(const CamParams& cam, float mx, float my,
+                                                   float mz, float s0, float s1, float s2,
+                                                   float4 q4, float opac) {
+    Projected P;
+    P.ok = false;
+    const float* V = cam.V;
+    float tx = radd(radd(radd(rmul(V[0], mx), rmul(V[1], my)), rmul(V[2], mz)), V[3]);
+    float ty = radd(radd(radd(rmul(V[4], mx), rmul(V[5], my)), rmul(V[6], mz)), V[7]);
+    float tz = radd(radd(radd(rmul(V[8], mx), rmul(V[9], my)), rmul(V[10], mz)), V[11]);
+    P.tx = tx;
+    P.ty = ty;
+    P.tz = tz;
+    if (!(tz > cam.znear) || !isfinite(tx) || !isfinite(ty) || !isfinite(tz)) return P;
+
+    float n2 = radd(radd(radd(rmul(q4.x, q4.x), rmul(q4.y, q4.y)), rmul(q4.z, q4.z)),
+                    rmul(q4.w, q4.w));
+    if (!(n2 > 0.f) || !isfinite(n2)) return P;
+    float nr = rsqrt_exact(n2);
+    float w = rdiv(q4.x, nr), x = rdiv(q4.y, nr), y = rdiv(q4.z, nr), z = rdiv(q4.w, nr);
+    float R[9];
+    R[0] = rsub(1.f, rmul(2.f, radd(rmul(y, y), rmul(z, z))));
+    R[1] = rmul(2.f, rsub(rmul(x, y), rmul(w, z)));
+    R[2] = rmul(2.f, radd(rmul(x, z), rmul(w, y)));
+    R[3] = rmul(2.f, radd(rmul(x, y), rmul(w, z)));
+    R[4] = rsub(1.f, rmul(2.f, radd(rmul(x, x), rmul(z, z))));
+    R[5] = rmul(2.f, rsub(rmul(y, z), rmul(w, x)));
+    R[6] = rmul(2.f, rsub(rmul(x, z), rmul(w, y)));
+    R[7] = rmul(2.f, radd(rmul(y, z), rmul(w, x)));
+    R[8] = rsub(1.f, rmul(2.f, radd(rmul(x, x), rmul(y, y))));
+    float M[9];
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        M[3 * i + 0] = rmul(R[3 * i + 0], s0);
+        M[3 * i + 1] = rmul(R[3 * i + 1], s1);
+        M[3 * i + 2] = rmul(R[3 * i + 2], s2);
+    }
+    float S[9];
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+#pragma unroll
+        for (int j = i; j < 3; ++j) {
+            float v = radd(radd(rmul(M[3 * i], M[3 * j]), rmul(M[3 * i + 1], M[3 * j + 1])),
+                           rmul(M[3 * i + 2], M[3 * j + 2]));
+            S[3 * i + j] = v;
+            S[3 * j + i] = v;
+        }
+    float u = rdiv(tx, tz), v = rdiv(ty, tz);
+    float mux = radd(rmul(cam.fx, u), cam.cx);
+    float muy = radd(rmul(cam.fy, v), cam.cy);
+    float j00 = rdiv(cam.fx, tz), j11 = rdiv(cam.fy, tz);
+    float j02 = -rmul(j00, u), j12 = -rmul(j11, v);
+    float T0[3], T1[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        T0[k] = radd(rmul(j00, V[k]), rmul(j02, V[8 + k]));
+        T1[k] = radd(rmul(j11, V[4 + k]), rmul(j12, V[8 + k]));
+    }
+    float U0[3], U1[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        U0[k] = radd(radd(rmul(T0[0], S[k]), rmul(T0[1], S[3 + k])), rmul(T0[2], S[6 + k]));
+        U1[k] = radd(radd(rmul(T1[0], S[k]), rmul(T1[1], S[3 + k])), rmul(T1[2], S[6 + k]));
+    }
+    float P00 = radd(radd(rmul(U0[0], T0[0]), rmul(U0[1], T0[1])), rmul(U0[2], T0[2]));
+    float P01 = radd(radd(rmul(U0[0], T1[0]), rmul(U0[1], T1[1])), rmul(U0[2], T1[2]));
+    float P11 = radd(radd(rmul(U1[0], T1[0]), rmul(U1[1], T1[1])), rmul(U1[2], T1[2]));
+    float det = rsub(rmul(P00, P11), rmul(P01, P01));
+    if (!(det > 0.f) || !(P00 > 0.f) || !(P11 > 0.f) || !isfinite(det)) return P;
+    float a = rdiv(P11, det);
+    float b = -rdiv(P01, det);
+    float c = rdiv(P00, det);
+    // tau = fp32 rounding of 2 ln(255 o), evaluated in double
+    double td = 2.0 * log(255.0 * (double)opac);
+    float tau = __double2float_rn(td);
+    if (!(tau > 0.f)) return P;
+    float rx = rsqrt_exact(rmul(tau, P00));
+    float ry = rsqrt_exact(rmul(tau, P11));
+    if (!isfinite(mux) || !isfinite(muy) || !isfinite(a) || !isfinite(b) || !isfinite(c) ||
+        !isfinite(rx) || !isfinite(ry))
+        return P;
+    P.mux = mux;
+    P.muy = muy;
+    P.a = a;
+    P.b = b;
+    P.c = c;
+    P.tau = tau;
+    P.rx = rx;
+    P.ry = ry;
+    P.ok = true;
+    return P;
+}
+
+// ---------------------------------------------------------------------------
+// forward projection kernel
+// ---------------------------------------------------------------------------
+template <int K>
+__global__ void __launch_bounds__(256) project_kernel(CamParams cam, int64_t n,
+                                                      const float* __restrict__ means,
+                                                      const float* __restrict__ scales,
+                                                      const float4* __restrict__ quats,
+                                                      const float* __restrict__ opac,
+                                                      const float* __restrict__ sh,
+                                                      float4* __restrict__ splats,
+                                                      float* __restrict__ depths,
+                                                      int2* __restrict__ radii,
+                                                      int* __restrict__ tiles_touched) {
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float mx = means[3 * i], my = means[3 * i + 1], mz = means[3 * i + 2];
+    float o = opac[i];
+    Projected P = project_chain(cam, mx, my, mz, scales[3 * i], scales[3 * i + 1],
+                                scales[3 * i + 2], quats[i], o);
+    int tiles = 0;
+    if (P.ok) {
+        Ellipse e{P.mux, P.muy, P.a, P.b, P.c, P.tau, P.rx, P.ry};
+        int ty0, ty1, tx0, tx1;
+        row_range(e, cam.nty, &ty0, &ty1);
+        for (int ty = ty0; ty < ty1; ++ty)
+            if (row_span(e, ty, cam.W, cam.H, cam.ntx, &tx0, &tx1)) tiles += tx1 - tx0;
+    }
+    float4* rec = splats + 3 * i;
+    if (!P.ok || tiles == 0) {
+        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        rec[0] = z;
+        rec[1] = z;
+        rec[2] = z;
+        depths[i] = 0.f;
+        radii[i] = make_int2(0, 0);
+        tiles_touched[i] = 0;
+        return;
+    }
+    // colour, only for visible Gaussians: c = sum_k Y_k(d) s_k
+    float dx = mx - cam.cw[0], dy = my - cam.cw[1], dz = mz - cam.cw[2];
+    float inv = rsqrtf(dx * dx + dy * dy + dz * dz);
+    float Y[16];
+    sh_values(dx * inv, dy * inv, dz * inv, Y);
+    float cr = 0.f, cg = 0.f, cb = 0.f;
+    const float* row = sh + (int64_t)i * (K * 3);
+    if constexpr ((K * 3) % 4 == 0) {
+        // groups of four basis functions = three float4 (Kopanas, Step 3)
+        const float4* r4 = reinterpret_cast<const float4*>(row);
+#pragma unroll
+        for (int g = 0; g < K / 4; ++g) {
+            float4 v0 = __ldg(r4 + 3 * g), v1 = __ldg(r4 + 3 * g + 1), v2 = __ldg(r4 + 3 * g + 2);
+            float y0 = Y[4 * g], y1 = Y[4 * g + 1], y2 = Y[4 * g + 2], y3 = Y[4 * g + 3];
+            cr += y0 * v0.x + y1 * v0.w + y2 * v1.z + y3 * v2.y;
+            cg += y0 * v0.y + y1 * v1.x + y2 * v1.w + y3 * v2.z;
+            cb += y0 * v0.z + y1 * v1.y + y2 * v2.x + y3 * v2.w;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            cr += Y[k] * __ldg(row + 3 * k);
+            cg += Y[k] * __ldg(row + 3 * k + 1);
+            cb += Y[k] * __ldg(row + 3 * k + 2);
+        }
+    }
+    rec[0] = make_float4(P.mux, P.muy, P.a, P.b);
+    rec[1] = make_float4(P.c, P.tau, log2f(o), P.rx);
+    rec[2] = make_float4(cr, cg, cb, P.ry);
+    depths[i] = P.tz;
+    radii[i] = make_int2(to_int_clamped(ceilf(P.rx), 0, kRadiusMax),
+                         to_int_clamped(ceilf(P.ry), 0, kRadiusMax));
+    tiles_touched[i] = tiles;
+}
+
+cudaError_t launch_project(const CamParams& cam, int64_t n, int sh_degree, const float* means,
+                           const float* scales, const float* quats, const float* opacities,
+                           const float* sh, float* splats, float* depths, int32_t* radii,
+                           int32_t* tiles_touched, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    dim3 block(256), grid((unsigned)((n + 255) / 256));
+    auto q4 = reinterpret_cast<const float4*>(quats);
+    auto s4 = reinterpret_cast<float4*>(splats);
+    auto r2 = reinterpret_cast<int2*>(radii);
+    switch (sh_degree) {
+        case 0: project_kernel<1><<<grid, block, 0, st>>>(cam, n, means, scales, q4, opacities, sh, s4, depths, r2, tiles_touched); break;
+        case 1: project_kernel<4><<<grid, block, 0, st>>>(cam, n, means, scales, q4, opacities, sh, s4, depths, r2, tiles_touched); break;
+        case 2: project_kernel<9><<<grid, block, 0, st>>>(cam, n, means, scales, q4, opacities, sh, s4, depths, r2, tiles_touched); break;
+        default: project_kernel<16><<<grid, block, 0, st>>>(cam, n, means, scales, q4, opacities, sh, s4, depths, r2, tiles_touched); break;
+    }
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// backward: nine screen-space derivatives -> 59 parameter gradients
+// ---------------------------------------------------------------------------
+template <int K>
+__global__ void __launch_bounds__(256) project_bwd_kernel(
+    CamParams cam, int64_t n, const float* __restrict__ means, const float* __restrict__ scales,
+    const float4* __restrict__ quats, const float* __restrict__ sh,
+    const int* __restrict__ tiles_touched, const float* __restrict__ grad2d,
+    const uint8_t* __restrict__ touched, float* __restrict__ dmeans, float* __restrict__ dscales,
+    float4* __restrict__ dquats, float* __restrict__ dopac, float* __restrict__ dsh) {
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float* dshrow = dsh + (int64_t)i * (K * 3);
+    bool live = tiles_touched[i] > 0 && (touched == nullptr || touched[i] != 0);
+    float g[9];
+    if (live) {
+#pragma unroll
+        for (int r = 0; r < 9; ++r) g[r] = grad2d[9 * i + r];
+    }
+    if (!live) {
+        dmeans[3 * i] = dmeans[3 * i + 1] = dmeans[3 * i + 2] = 0.f;
+        dscales[3 * i] = dscales[3 * i + 1] = dscales[3 * i + 2] = 0.f;
+        dquats[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        dopac[i] = 0.f;
+        if constexpr ((K * 3) % 4 == 0) {
+            float4* d4 = reinterpret_cast<float4*>(dshrow);
+#pragma unroll
+            for (int j = 0; j < K * 3 / 4; ++j) d4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+#pragma unroll
+            for (int j = 0; j < K * 3; ++j) dshrow[j] = 0.f;
+        }
+        return;
+    }
+    const float* V = cam.V;
+    float m[3] = {means[3 * i], means[3 * i + 1], means[3 * i + 2]};
+    float s[3] = {scales[3 * i], scales[3 * i + 1], scales[3 * i + 2]};
+    float4 q4 = quats[i];
+
+    // ---- forward recomputation (fp32) ----
+    float t[3];
+#pragma unroll
+    for (int r = 0; r < 3; ++r) t[r] = V[4 * r] * m[0] + V[4 * r + 1] * m[1] + V[4 * r + 2] * m[2] + V[4 * r + 3];
+    float qn = sqrtf(q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w);
+    float iqn = 1.f / qn;
+    float w = q4.x * iqn, x = q4.y * iqn, y = q4.z * iqn, z = q4.w * iqn;
+    float R[9] = {1.f - 2.f * (y * y + z * z), 2.f * (x * y - w * z), 2.f * (x * z + w * y),
+                  2.f * (x * y + w * z), 1.f - 2.f * (x * x + z * z), 2.f * (y * z - w * x),
+                  2.f * (x * z - w * y), 2.f * (y * z + w * x), 1.f - 2.f * (x * x + y * y)};
+    float M[9];
+#pragma unroll
+    for (int r = 0; r < 3; ++r)
+#pragma unroll
+        for (int c = 0; c < 3; ++c) M[3 * r + c] = R[3 * r + c] * s[c];
+    float S[9];
+#pragma unroll
+    for (int r = 0; r < 3; ++r)
+#pragma unroll
+        for (int c = r; c < 3; ++c) {
+            float v = M[3 * r] * M[3 * c] + M[3 * r + 1] * M[3 * c + 1] + M[3 * r + 2] * M[3 * c + 2];
+            S[3 * r + c] = v;
+            S[3 * c + r] = v;
+        }
+    float tz = t[2], iz = 1.f / tz;
+    float u = t[0] * iz, v = t[1] * iz;
+    float j00 = cam.fx * iz, j11 = cam.fy * iz, j02 = -j00 * u, j12 = -j11 * v;
+    float T0[3], T1[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        T0[k] = j00 * V[k] + j02 * V[8 + k];
+        T1[k] = j11 * V[4 + k] + j12 * V[8 + k];
+    }
+    float ST0[3], ST1[3];
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+        ST0[r] = S[3 * r] * T0[0] + S[3 * r + 1] * T0[1] + S[3 * r + 2] * T0[2];
+        ST1[r] = S[3 * r] * T1[0] + S[3 * r + 1] * T1[1] + S[3 * r + 2] * T1[2];
+    }
+    float P00 = T0[0] * ST0[0] + T0[1] * ST0[1] + T0[2] * ST0[2];
+    float P01 = T0[0] * ST1[0] + T0[1] * ST1[1] + T0[2] * ST1[2];
+    float P11 = T1[0] * ST1[0] + T1[1] * ST1[1] + T1[2] * ST1[2];
+    float idet = 1.f / (P00 * P11 - P01 * P01);
+    float ca = P11 * idet, cb = -P01 * idet, cc = P00 * idet;
+
+    // ---- conic -> Sigma': dSigma' = -Lambda G Lambda, G = [[ga, gb/2], [gb/2, gc]] ----
+    float ga = g[2], gbh = 0.5f * g[3], gc = g[4];
+    float X00 = ca * ga + cb * gbh, X01 = ca * gbh + cb * gc;
+    float X10 = cb * ga + cc * gbh, X11 = cb * gbh + cc * gc;
+    float dP00 = -(X00 * ca + X01 * cb);
+    float dP01 = -2.f * (X00 * cb + X01 * cc);
+    float dP11 = -(X10 * cb + X11 * cc);
+
+    // ---- Sigma' = T Sigma T^T -> dT, dM ----
+    float dT0[3], dT1[3];
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+        dT0[r] = 2.f * dP00 * ST0[r] + dP01 * ST1[r];
+        dT1[r] = dP01 * ST0[r] + 2.f * dP11 * ST1[r];
+    }
+    float ds[3], dR[9];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        float a0 = T0[0] * M[k] + T0[1] * M[3 + k] + T0[2] * M[6 + k];
+        float a1 = T1[0] * M[k] + T1[1] * M[3 + k] + T1[2] * M[6 + k];
+        float c0 = 2.f * dP00 * a0 + dP01 * a1;
+        float c1 = dP01 * a0 + 2.f * dP11 * a1;
+        float acc = 0.f;
+#pragma unroll
+        for (int r = 0; r < 3; ++r) {
+            float dMrk = T0[r] * c0 + T1[r] * c1;
+            acc += dMrk * R[3 * r + k];
+            dR[3 * r + k] = dMrk * s[k];
+        }
+        ds[k] = acc;
+    }
+
+    // ---- T = J W -> dJ; (mu', J) -> dt -> dm ----
+    float dj00 = dT0[0] * V[0] + dT0[1] * V[1] + dT0[2] * V[2];
+    float dj02 = dT0[0] * V[8] + dT0[1] * V[9] + dT0[2] * V[10];
+    float dj11 = dT1[0] * V[4] + dT1[1] * V[5] + dT1[2] * V[6];
+    float dj12 = dT1[0] * V[8] + dT1[1] * V[9] + dT1[2] * V[10];
+    float gmx = g[0], gmy = g[1];
+    float dtx = (gmx - dj02 * iz) * j00;
+    float dty = (gmy - dj12 * iz) * j11;
+    float dtz = -(gmx * j00 * u + gmy * j11 * v) - (dj00 * j00 + dj11 * j11) * iz +
+                2.f * (dj02 * j00 * u + dj12 * j11 * v) * iz;
+    float dm[3];
+#pragma unroll
+    for (int c = 0; c < 3; ++c) dm[c] = V[c] * dtx + V[4 + c] * dty + V[8 + c] * dtz;
+
+    // ---- R(w, x, y, z) -> normalised quaternion -> raw quaternion ----
+    float dw = -2.f * z * dR[1] + 2.f * y * dR[2] + 2.f * z * dR[3] - 2.f * x * dR[5] -
+               2.f * y * dR[6] + 2.f * x * dR[7];
+    float dx_ = 2.f * y * dR[1] + 2.f * z * dR[2] + 2.f * y * dR[3] - 4.f * x * dR[4] -
+                2.f * w * dR[5] + 2.f * z * dR[6] + 2.f * w * dR[7] - 4.f * x * dR[8];
+    float dy_ = -4.f * y * dR[0] + 2.f * x * dR[1] + 2.f * w * dR[2] + 2.f * x * dR[3] +
+                2.f * z * dR[5] - 2.f * w * dR[6] + 2.f * z * dR[7] - 4.f * y * dR[8];
+    float dz_ = -4.f * z * dR[0] - 2.f * w * dR[1] + 2.f * x * dR[2] + 2.f * w * dR[3] -
+                4.f * z * dR[4] + 2.f * y * dR[5] + 2.f * x * dR[6] + 2.f * y * dR[7];
+    float dot = w * dw + x * dx_ + y * dy_ + z * dz_;
+    float4 dq = make_float4((dw - w * dot) * iqn, (dx_ - x * dot) * iqn, (dy_ - y * dot) * iqn,
+                            (dz_ - z * dot) * iqn);
+
+    // ---- colour -> SH coefficients and view direction ----
+    float ex = m[0] - cam.cw[0], ey = m[1] - cam.cw[1], ez = m[2] - cam.cw[2];
+    float ilen = rsqrtf(ex * ex + ey * ey + ez * ez);
+    float hx = ex * ilen, hy = ey * ilen, hz = ez * ilen;
+    float Y[16];
+    sh_values(hx, hy, hz, Y);
+    float gr = g[6], gg = g[7], gbl = g[8];
+    const float* row = sh + (int64_t)i * (K * 3);
+    float gdx = 0.f, gdy = 0.f, gdz = 0.f;
+    if constexpr ((K * 3) % 4 == 0) {
+        const float4* r4 = reinterpret_cast<const float4*>(row);
+        float4* d4 = reinterpret_cast<float4*>(dshrow);
+#pragma unroll
+        for (int gi = 0; gi < K / 4; ++gi) {
+            float4 v0 = __ldg(r4 + 3 * gi), v1 = __ldg(r4 + 3 * gi + 1), v2 = __ldg(r4 + 3 * gi + 2);
+            float c[12] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w, v2.x, v2.y, v2.z, v2.w};
+            float o[12];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                int k = 4 * gi + j;
+                o[3 * j] = Y[k] * gr;
+                o[3 * j + 1] = Y[k] * gg;
+                o[3 * j + 2] = Y[k] * gbl;
+                float p = gr * c[3 * j] + gg * c[3 * j + 1] + gbl * c[3 * j + 2];
+                float3 dY = sh_grad(k, hx, hy, hz);
+                gdx += p * dY.x;
+                gdy += p * dY.y;
+                gdz += p * dY.z;
+            }
+            d4[3 * gi] = make_float4(o[0], o[1], o[2], o[3]);
+            d4[3 * gi + 1] = make_float4(o[4], o[5], o[6], o[7]);
+            d4[3 * gi + 2] = make_float4(o[8], o[9], o[10], o[11]);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            float c0 = __ldg(row + 3 * k), c1 = __ldg(row + 3 * k + 1), c2 = __ldg(row + 3 * k + 2);
+            dshrow[3 * k] = Y[k] * gr;
+            dshrow[3 * k + 1] = Y[k] * gg;
+            dshrow[3 * k + 2] = Y[k] * gbl;
+            float p = gr * c0 + gg * c1 + gbl * c2;
+            float3 dY = sh_grad(k, hx, hy, hz);
+            gdx += p * dY.x;
+            gdy += p * dY.y;
+            gdz += p * dY.z;
+        }
+    }
+    float dd = hx * gdx + hy * gdy + hz * gdz;
+    dm[0] += (gdx - hx * dd) * ilen;
+    dm[1] += (gdy - hy * dd) * ilen;
+    dm[2] += (gdz - hz * dd) * ilen;
+
+    dmeans[3 * i] = dm[0];
+    dmeans[3 * i + 1] = dm[1];
+    dmeans[3 * i + 2] = dm[2];
+    dscales[3 * i] = ds[0];
+    dscales[3 * i + 1] = ds[1];
+    dscales[3 * i + 2] = ds[2];
+    dquats[i] = dq;
+    dopac[i] = g[5];
+}
+
+cudaError_t launch_project_bwd(const CamParams& cam, int64_t n, int sh_degree, const float* means,
+                               const float* scales, const float* quats, const float* opacities,
+                               const float* sh, const int32_t* tiles_touched, const float* grad2d,
+                               const uint8_t* touched, float* dmeans, float* dscales,
+                               float* dquats, float* dopacities, float* dsh, cudaStream_t st) {
+    (void)opacities;
+    if (n == 0) return cudaSuccess;
+    dim3 block(256), grid((unsigned)((n + 255) / 256));
+    auto q4 = reinterpret_cast<const float4*>(quats);
+    auto dq4 = reinterpret_cast<float4*>(dquats);
+    switch (sh_degree) {
+        case 0: project_bwd_kernel<1><<<grid, block, 0, st>>>(cam, n, means, scales, q4, sh, tiles_touched, grad2d, touched, dmeans, dscales, dq4, dopacities, dsh); break;
+        case 1: project_bwd_kernel<4><<<grid, block, 0, st>>>(cam, n, means, scales, q4, sh, tiles_touched, grad2d, touched, dmeans, dscales, dq4, dopacities, dsh); break;
+        case 2: project_bwd_kernel<9><<<grid, block, 0, st>>>(cam, n, means, scales, q4, sh, tiles_touched, grad2d, touched, dmeans, dscales, dq4, dopacities, dsh); break;
+        default: project_bwd_kernel<16><<<grid, block, 0, st>>>(cam, n, means, scales, q4, sh, tiles_touched, grad2d, touched, dmeans, dscales, dq4, dopacities, dsh); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace gs

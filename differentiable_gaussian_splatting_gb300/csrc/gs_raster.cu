@@ -1,0 +1,710 @@
+// gs_raster.cu -- per-tile alpha blending (forward) and its gradient (backward).
+//
+// Forward ("Mitigating SM-Level Load Imbalance in 3D Gaussian Splatting on
+// GPUs", Ryu & Yoo): Eq. 2-3 per pixel; Sec. 4.1 a persistent kernel of K
+// resident CTAs takes work from a queue in LPT order (one atomicAdd per fetch);
+// Sec. 4.2 the heaviest tiles are split into k depth-contiguous chunks that
+// blend from unit transmittance, signal saturation through a per-tile
+// atomicMin flag that later chunks check once per 256-splat batch, and are
+// composed with Eq. 5; Sec. 4.3-4.4 the per-frame policy of Eq. 6 picks how
+// many tiles to split and how deeply.  Chunk items and whole-tile items share
+// one queue (heavy chunks first), which is the fused form of the selective
+// chunking; the CTA that finishes a split tile's last chunk composes it.
+// Composition replays, for a pixel, the chunk in which the sequential blend
+// would stop, so the result equals the sequential definition.
+//
+// Per tile ("What the 3DGS Literature Left on the Table", Kopanas): 256
+// threads, 8 warps of 8x4 pixels; batches of 256 splat records (three float4
+// each) are staged in shared memory with an 8-bit sub-tile mask per splat;
+// each warp walks the splats of its sub-tile with __ballot_sync / __ffs (Step
+// 1 (c)); misses are predicated to alpha = 0 (Step 5); the quadratic is
+// evaluated with round-to-nearest operations so forward and backward agree
+// bit for bit on every hit (Step 5); opacity is folded into the base-2
+// exponent (Step 6.3).
+//
+// Backward (Kopanas, Step 1 (a), Step 2): back to front from each pixel's
+// last blended splat, T recovered by division by (1 - alpha); the nine
+// per-splat derivatives of a warp are summed by a halving reduce-scatter of
+// 12 shuffles, after which nine lanes add them atomically.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <mutex>
+
+#include "gs_device.cuh"
+#include "gs_internal.h"
+
+namespace gs {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kBatch = 256;
+constexpr int kPolicyThreads = 1024;
+
+struct RasterArgs {
+    int W, H, ntx, nty;
+    const float4* splats;
+    const int32_t* ids;
+    const int2* ranges;
+    const int32_t* lpt;
+    int* ctrl;
+    int* sat;
+    int* done;
+    float4* part_c;
+    int2* part_n;
+    float4* bstate;
+    // forward outputs
+    float* image;
+    float* t_final;
+    int32_t* n_contrib;
+    int32_t* last_idx;
+    // backward inputs / outputs
+    const float* t_final_in;
+    const int32_t* last_in;
+    const float* dimg;
+    const float* dT;
+    float* grad2d;
+    uint8_t* touched;
+};
+
+__device__ __forceinline__ int64_t chunk_lo(int64_t s, int64_t len, int p, int k) {
+    return s + (len * p) / k;
+}
+
+// pixel of thread tid inside its tile: warp w covers the 8x4 sub-tile
+// (8 (w & 1), 4 (w >> 1)); lane l is pixel (l & 7, l >> 3) of it
+__device__ __forceinline__ void tile_pixel(int tid, int* lx, int* ly) {
+    const int w = tid >> 5, l = tid & 31;
+    *lx = ((w & 1) << 3) + (l & 7);
+    *ly = ((w >> 1) << 2) + (l >> 3);
+}
+
+struct WorkItem {
+    int tile;
+    int slot;   // split-tile index (0..h-1), -1 for a whole tile
+    int chunk;  // chunk index p
+    int k;
+    int64_t s, e;
+};
+
+__device__ __forceinline__ WorkItem decode_item(const RasterArgs& A, int item, int h, int k) {
+    WorkItem it;
+    if (item < h * k) {
+        it.slot = item / k;
+        it.chunk = item - it.slot * k;
+        it.k = k;
+        it.tile = A.lpt[it.slot];
+        const int2 r = A.ranges[it.tile];
+        const int64_t len = (int64_t)r.y - r.x;
+        it.s = chunk_lo(r.x, len, it.chunk, k);
+        it.e = chunk_lo(r.x, len, it.chunk + 1, k);
+    } else {
+        it.slot = -1;
+        it.chunk = 0;
+        it.k = 1;
+        it.tile = A.lpt[h + (item - h * k)];
+        const int2 r = A.ranges[it.tile];
+        it.s = r.x;
+        it.e = r.y;
+    }
+    return it;
+}
+
+struct PixelState {
+    float T, cr, cg, cb;
+    int n, last;
+    bool done;
+};
+
+struct Smem {
+    float4 r0[kBatch];
+    float4 r1[kBatch];
+    float4 r2[kBatch];
+    int32_t gid[kBatch];
+    uint8_t mask[kBatch];
+    int item;
+    int flag;
+};
+
+// Front-to-back blend of list positions [s, e) for the calling thread's pixel.
+// All threads of the CTA must call it.  When sat_slot >= 0 the chunk stops
+// early once sat[sat_slot] < chunk (an earlier chunk saturated the tile).
+// Returns true if it stopped on that signal.
+__device__ bool blend_range(const RasterArgs& A, Smem& S, int tx, int ty, float px, float py,
+                            int64_t s, int64_t e, PixelState& st, int sat_slot, int chunk) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int64_t bs = s; bs < e; bs += kBatch) {
+        if (tid == 0)
+            S.flag = (sat_slot >= 0 && chunk > 0) ? (*(volatile int*)(A.sat + sat_slot) < chunk) : 0;
+        const int live = __syncthreads_or(!st.done);
+        if (!live) return false;
+        if (S.flag) return true;
+        const int64_t j = bs + tid;
+        if (j < e) {
+            const int32_t g = __ldg(A.ids + j);
+            const float4 r0 = __ldg(A.splats + 3 * (int64_t)g);
+            const float4 r1 = __ldg(A.splats + 3 * (int64_t)g + 1);
+            const float4 r2 = __ldg(A.splats + 3 * (int64_t)g + 2);
+            S.r0[tid] = r0;
+            S.r1[tid] = r1;
+            S.r2[tid] = r2;
+            S.mask[tid] = (uint8_t)subtile_mask(ellipse_of(r0, r1, r2), tx, ty, A.W, A.H);
+        } else {
+            S.mask[tid] = 0;
+        }
+        __syncthreads();
+        const int nb = (int)min64(kBatch, e - bs);
+        for (int c = 0; c < nb; c += 32) {
+            if (__ballot_sync(0xffffffffu, !st.done) == 0) break;
+            const int jj = c + lane;
+            const uint32_t bit = jj < nb ? (S.mask[jj] >> warp) & 1u : 0u;
+            uint32_t work = __ballot_sync(0xffffffffu, bit);
+            while (work) {
+                const int q = __ffs(work) - 1;
+                work &= work - 1;
+                const int idx = c + q;
+                const float4 r0 = S.r0[idx], r1 = S.r1[idx], r2 = S.r2[idx];
+                const float dx = rsub(px, r0.x), dy = rsub(py, r0.y);
+                const float qv = quad_q(r1.x, quad_A(r0.z, dx), quad_B(r0.w, dx), dy);
+                const bool hit = (qv <= r1.y) && !st.done;
+                float alpha = fminf(ex2_approx(fmaf(qv, kNegHalfLog2e, r1.z)), kAlphaMax);
+                alpha = hit ? alpha : 0.f;
+                const float w = alpha * st.T;
+                st.cr = fmaf(w, r2.x, st.cr);
+                st.cg = fmaf(w, r2.y, st.cg);
+                st.cb = fmaf(w, r2.z, st.cb);
+                st.T = st.T * (1.f - alpha);
+                if (hit) {
+                    st.n += 1;
+                    st.last = (int)(bs + idx);
+                }
+                st.done = st.done || (st.T < kTMin);
+            }
+        }
+        __syncthreads();
+    }
+    return false;
+}
+
+// ---------------------------------------------------------------------------
+// per-frame chunking policy (Ryu & Yoo, Eq. 6), one block
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* __restrict__ lpt,
+                                                                const int2* __restrict__ ranges,
+                                                                int nt, int K, RasterConfig cfg,
+                                                                int* ctrl, int* sat, int* done) {
+    __shared__ double s_tot[32];
+    __shared__ double s_cost[32];
+    __shared__ int s_h[32], s_k[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    double tot = 0.0;
+    for (int t = tid; t < nt; t += kPolicyThreads) {
+        const int2 r = ranges[t];
+        tot += (double)(r.y - r.x);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    if (lane == 0) s_tot[warp] = tot;
+    __syncthreads();
+    tot = 0.0;
+    for (int w = 0; w < kPolicyThreads / 32; ++w) tot += s_tot[w];
+    auto count_at = [&](int j) -> double {
+        if (j >= nt) return 0.0;
+        const int2 r = ranges[lpt[j]];
+        return (double)(r.y - r.x);
+    };
+    const double N1 = count_at(0);
+    const double lam = cfg.lambda, beta = cfg.beta;
+    const double base = fmax(tot / (double)K, N1) + beta * N1;
+    int bh = 0, bk = 1;
+    if (cfg.split_mode == 2) {
+        bh = min(min(cfg.force_h, cfg.h_max), nt);
+        bk = bh > 0 ? cfg.force_k : 1;
+    } else if (cfg.split_mode == 0) {
+        const int hm = min(nt, cfg.h_max);
+        const int ks[4] = {2, 4, 8, 16};
+        double best = base;
+        int h_best = 0, k_best = 1;
+        for (int cand = tid; cand < hm * 4; cand += kPolicyThreads) {
+            const int h = 1 + cand / 4;
+            const int k = ks[cand % 4];
+            const double l = fmax(N1 / (double)k, count_at(h));
+            const double cost = fmax((tot + lam * (double)h * (double)k) / (double)K, l) + beta * l;
+            // lexicographic (cost, h, k): candidates are visited in increasing (h, k)
+            if (cost < best) {
+                best = cost;
+                h_best = h;
+                k_best = k;
+            }
+        }
+        // block argmin with the same order
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const double oc = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oh = __shfl_xor_sync(0xffffffffu, h_best, o);
+            const int ok = __shfl_xor_sync(0xffffffffu, k_best, o);
+            const bool take = oc < best || (oc == best && (oh < h_best || (oh == h_best && ok < k_best)));
+            if (take) {
+                best = oc;
+                h_best = oh;
+                k_best = ok;
+            }
+        }
+        if (lane == 0) {
+            s_cost[warp] = best;
+            s_h[warp] = h_best;
+            s_k[warp] = k_best;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            for (int w = 1; w < kPolicyThreads / 32; ++w) {
+                const bool take = s_cost[w] < best ||
+                                  (s_cost[w] == best &&
+                                   (s_h[w] < h_best || (s_h[w] == h_best && s_k[w] < k_best)));
+                if (take) {
+                    best = s_cost[w];
+                    h_best = s_h[w];
+                    k_best = s_k[w];
+                }
+            }
+            if (h_best > 0 && !(best <= (1.0 - (double)cfg.eps) * base)) {
+                h_best = 0;
+                k_best = 1;
+            }
+            s_h[0] = h_best;
+            s_k[0] = k_best;
+        }
+        __syncthreads();
+        bh = s_h[0];
+        bk = s_k[0];
+    }
+    for (int j = tid; j < bh; j += kPolicyThreads) {
+        sat[j] = INT_MAX;
+        done[j] = 0;
+    }
+    if (tid == 0) {
+        ctrl[kCtlH] = bh;
+        ctrl[kCtlK] = bk;
+        ctrl[kCtlItems] = bh * bk + (nt - bh);
+        ctrl[kCtlResident] = K;
+        ctrl[kCtlQueueFwd] = 0;
+        ctrl[kCtlQueueBwd] = 0;
+        ctrl[kCtlError] = 0;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// forward: persistent kernel over whole tiles and depth chunks
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) raster_fwd_kernel(RasterArgs A) {
+    __shared__ Smem S;
+    const int tid = threadIdx.x;
+    const int h = A.ctrl[kCtlH], k = A.ctrl[kCtlK], nitems = A.ctrl[kCtlItems];
+    int lx, ly;
+    tile_pixel(tid, &lx, &ly);
+    while (true) {
+        if (tid == 0) S.item = atomicAdd(A.ctrl + kCtlQueueFwd, 1);
+        __syncthreads();
+        const int item = S.item;
+        __syncthreads();
+        if (item >= nitems) break;
+        const WorkItem it = decode_item(A, item, h, k);
+        const int tx = it.tile % A.ntx, ty = it.tile / A.ntx;
+        const int x = tx * kTile + lx, y = ty * kTile + ly;
+        const bool inside = x < A.W && y < A.H;
+        const float px = (float)x + 0.5f, py = (float)y + 0.5f;
+        PixelState st{1.f, 0.f, 0.f, 0.f, 0, -1, !inside};
+        if (it.slot < 0) {
+            blend_range(A, S, tx, ty, px, py, it.s, it.e, st, -1, 0);
+            if (inside) {
+                const int64_t p = (int64_t)y * A.W + x;
+                A.image[3 * p] = st.cr;
+                A.image[3 * p + 1] = st.cg;
+                A.image[3 * p + 2] = st.cb;
+                A.t_final[p] = st.T;
+                A.n_contrib[p] = st.n;
+                A.last_idx[p] = st.last;
+            }
+            continue;
+        }
+        // ---- a depth chunk of a split tile: blend from T = 1 ----
+        blend_range(A, S, tx, ty, px, py, it.s, it.e, st, it.slot, it.chunk);
+        const int64_t pidx = ((int64_t)it.slot * kMaxChunks + it.chunk) * kThreads + tid;
+        A.part_c[pidx] = make_float4(st.cr, st.cg, st.cb, st.T);
+        A.part_n[pidx] = make_int2(st.n, st.last);
+        const int saturated = __syncthreads_and(st.done);
+        if (tid == 0 && saturated) atomicMin(A.sat + it.slot, it.chunk);
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) S.flag = (atomicAdd(A.done + it.slot, 1) == it.k - 1);
+        __syncthreads();
+        if (!S.flag) continue;
+        __threadfence();
+        // ---- last chunk of this tile to finish: compose the chunks (Eq. 5) ----
+        PixelState acc{1.f, 0.f, 0.f, 0.f, 0, -1, !inside};
+        const int2 rr = A.ranges[it.tile];
+        const int64_t len = (int64_t)rr.y - rr.x;
+        for (int p = 0; p < it.k; ++p) {
+            const int64_t slotp = ((int64_t)it.slot * kMaxChunks + p) * kThreads + tid;
+            const float Tb = acc.T;
+            const float cr0 = acc.cr, cg0 = acc.cg, cb0 = acc.cb;
+            bool replay = false;
+            if (!acc.done) {
+                const float4 pc = __ldcg(A.part_c + slotp);
+                const int2 pn = __ldcg(A.part_n + slotp);
+                const float Tn = acc.T * pc.w;
+                if (pc.w >= kTMin && Tn >= kTMin) {
+                    // no stop can fall inside the chunk: T is monotone
+                    acc.cr = fmaf(acc.T, pc.x, acc.cr);
+                    acc.cg = fmaf(acc.T, pc.y, acc.cg);
+                    acc.cb = fmaf(acc.T, pc.z, acc.cb);
+                    acc.T = Tn;
+                    acc.n += pn.x;
+                    if (pn.x > 0) acc.last = pn.y;
+                } else {
+                    replay = true;
+                }
+            }
+            if (__syncthreads_or(replay)) {
+                // replay chunk p sequentially from the running state for the
+                // pixels whose stop lies in it
+                PixelState rs = acc;
+                rs.done = !replay;
+                blend_range(A, S, tx, ty, px, py, chunk_lo(rr.x, len, p, it.k),
+                            chunk_lo(rr.x, len, p + 1, it.k), rs, -1, 0);
+                if (replay) {
+                    acc = rs;
+                    acc.done = rs.T < kTMin;
+                }
+            }
+            // state for the backward of chunk p: T after the chunk, colour it added
+            A.bstate[slotp] = make_float4(acc.T, acc.cr - cr0, acc.cg - cg0, acc.cb - cb0);
+            (void)Tb;
+        }
+        // colour added by chunks q > p ("colour behind" chunk p)
+        {
+            float br = 0.f, bg = 0.f, bb = 0.f;
+            for (int p = it.k - 1; p >= 0; --p) {
+                const int64_t slotp = ((int64_t)it.slot * kMaxChunks + p) * kThreads + tid;
+                float4 v = A.bstate[slotp];
+                const float ir = v.y, ig = v.z, ib = v.w;
+                A.bstate[slotp] = make_float4(v.x, br, bg, bb);
+                br += ir;
+                bg += ig;
+                bb += ib;
+            }
+        }
+        if (inside) {
+            const int64_t p = (int64_t)y * A.W + x;
+            A.image[3 * p] = acc.cr;
+            A.image[3 * p + 1] = acc.cg;
+            A.image[3 * p + 2] = acc.cb;
+            A.t_final[p] = acc.T;
+            A.n_contrib[p] = acc.n;
+            A.last_idx[p] = acc.last;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// backward
+// ---------------------------------------------------------------------------
+// Halving reduce-scatter of nine values over a warp (5 + 3 + 2 + 1 + 1 = 12
+// shuffles).  Afterwards the even lane 2j' of each pair holds the warp sum of
+// component comp_of_lane(lane) (valid when >= 0).
+__device__ __forceinline__ float reduce_scatter9(float v[9], int lane) {
+    const unsigned F = 0xffffffffu;
+    // xor 16: lower half keeps components 0..4, upper half 5..8
+    const bool lo16 = !(lane & 16);
+    float u[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+        const float send = lo16 ? (i < 4 ? v[5 + i] : 0.f) : v[i];
+        const float r = __shfl_xor_sync(F, send, 16);
+        u[i] = lo16 ? v[i] + r : (i < 4 ? v[5 + i] + r : 0.f);
+    }
+    // xor 8: 5 -> 3 (lower) / 2 (upper)
+    const bool lo8 = !(lane & 8);
+    float w3[3];
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        const float send = lo8 ? (i < 2 ? u[3 + i] : 0.f) : u[i];
+        const float r = __shfl_xor_sync(F, send, 8);
+        w3[i] = lo8 ? u[i] + r : (i < 2 ? u[3 + i] + r : 0.f);
+    }
+    // xor 4: 3 -> 2 / 1
+    const bool lo4 = !(lane & 4);
+    float w2[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = lo4 ? (i == 0 ? w3[2] : 0.f) : w3[i];
+        const float r = __shfl_xor_sync(F, send, 4);
+        w2[i] = lo4 ? w3[i] + r : (i == 0 ? w3[2] + r : 0.f);
+    }
+    // xor 2: 2 -> 1 / 1
+    const bool lo2 = !(lane & 2);
+    const float send = lo2 ? w2[1] : w2[0];
+    const float r = __shfl_xor_sync(F, send, 2);
+    float x = lo2 ? w2[0] + r : w2[1] + r;
+    // xor 1: sum the pair
+    x += __shfl_xor_sync(F, x, 1);
+    return x;
+}
+
+// component held by `lane` after reduce_scatter9, or -1 (a padding slot).
+// Lane bits 4, 3, 2, 1 pick the half kept at the xor-16, 8, 4, 2 steps:
+//   xor 16: {0..4} | {5..8, pad};  xor 8: first three | last two of those;
+//   xor 4: first two | third;  xor 2: first | second.
+__device__ __forceinline__ int comp_of_lane(int lane) {
+    switch (lane >> 1) {
+        case 0: return 0;   // lanes 0, 1
+        case 1: return 1;   // lanes 2, 3
+        case 2: return 2;   // lanes 4, 5
+        case 4: return 3;   // lanes 8, 9
+        case 5: return 4;   // lanes 10, 11
+        case 8: return 5;   // lanes 16, 17
+        case 9: return 6;   // lanes 18, 19
+        case 10: return 7;  // lanes 20, 21
+        case 12: return 8;  // lanes 24, 25
+        default: return -1;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) raster_bwd_kernel(RasterArgs A) {
+    __shared__ Smem S;
+    __shared__ int s_last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int h = A.ctrl[kCtlH], k = A.ctrl[kCtlK], nitems = A.ctrl[kCtlItems];
+    const int my_comp = comp_of_lane(lane);
+    const bool writer = !(lane & 1) && my_comp >= 0;
+    int lx, ly;
+    tile_pixel(tid, &lx, &ly);
+    while (true) {
+        if (tid == 0) {
+            S.item = atomicAdd(A.ctrl + kCtlQueueBwd, 1);
+            s_last = -1;
+        }
+        __syncthreads();
+        const int item = S.item;
+        if (item >= nitems) break;
+        const WorkItem it = decode_item(A, item, h, k);
+        const int tx = it.tile % A.ntx, ty = it.tile / A.ntx;
+        const int x = tx * kTile + lx, y = ty * kTile + ly;
+        const bool inside = x < A.W && y < A.H;
+        const float px = (float)x + 0.5f, py = (float)y + 0.5f;
+        int last = -1;
+        float T = 1.f, accum = 0.f, Gr = 0.f, Gg = 0.f, Gb = 0.f, gTT = 0.f;
+        if (inside) {
+            const int64_t p = (int64_t)y * A.W + x;
+            last = A.last_in[p];
+            const float Tfin = A.t_final_in[p];
+            Gr = A.dimg[3 * p];
+            Gg = A.dimg[3 * p + 1];
+            Gb = A.dimg[3 * p + 2];
+            gTT = A.dT ? A.dT[p] * Tfin : 0.f;
+            if (it.slot < 0) {
+                T = Tfin;
+            } else {
+                const int64_t slotp =
+                    ((int64_t)it.slot * kMaxChunks + it.chunk) * kThreads + tid;
+                const float4 b = A.bstate[slotp];
+                T = b.x;
+                accum = b.y * Gr + b.z * Gg + b.w * Gb;
+            }
+        }
+        // last list position any pixel of this item needs
+        const int mylast = (int)min64((int64_t)last, it.e - 1);
+        int wlast = mylast;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) wlast = max(wlast, __shfl_xor_sync(0xffffffffu, wlast, o));
+        if (lane == 0 && wlast >= 0) atomicMax(&s_last, wlast);
+        __syncthreads();
+        const int64_t hi = (int64_t)s_last + 1;
+        __syncthreads();
+        for (int64_t be = hi; be > it.s; be -= kBatch) {
+            const int64_t bs = max64(it.s, be - kBatch);
+            const int nb = (int)(be - bs);
+            if (tid < nb) {
+                const int32_t g = __ldg(A.ids + bs + tid);
+                const float4 r0 = __ldg(A.splats + 3 * (int64_t)g);
+                const float4 r1 = __ldg(A.splats + 3 * (int64_t)g + 1);
+                const float4 r2 = __ldg(A.splats + 3 * (int64_t)g + 2);
+                S.r0[tid] = r0;
+                S.r1[tid] = r1;
+                S.r2[tid] = r2;
+                S.gid[tid] = g;
+                S.mask[tid] = (uint8_t)subtile_mask(ellipse_of(r0, r1, r2), tx, ty, A.W, A.H);
+            }
+            __syncthreads();
+            for (int c = ((nb - 1) >> 5) << 5; c >= 0; c -= 32) {
+                const int jj = c + lane;
+                uint32_t bit = jj < nb ? (S.mask[jj] >> warp) & 1u : 0u;
+                if (bs + jj > wlast) bit = 0;
+                uint32_t work = __ballot_sync(0xffffffffu, bit);
+                while (work) {
+                    const int q = 31 - __clz(work);
+                    work &= ~(1u << q);
+                    const int idx = c + q;
+                    const int64_t gpos = bs + idx;
+                    const float4 r0 = S.r0[idx], r1 = S.r1[idx], r2 = S.r2[idx];
+                    const float dx = rsub(px, r0.x), dy = rsub(py, r0.y);
+                    const float qv = quad_q(r1.x, quad_A(r0.z, dx), quad_B(r0.w, dx), dy);
+                    const bool act = (qv <= r1.y) && gpos <= (int64_t)last;
+                    const float araw = ex2_approx(fmaf(qv, kNegHalfLog2e, r1.z));
+                    float alpha = fminf(araw, kAlphaMax);
+                    alpha = act ? alpha : 0.f;
+                    const float inv = __fdividef(1.f, 1.f - alpha);
+                    const float Tb = T * inv;
+                    const float wgt = alpha * Tb;
+                    const float cG = r2.x * Gr + r2.y * Gg + r2.z * Gb;
+                    const float dalpha = Tb * cG - (accum + gTT) * inv;
+                    accum = fmaf(cG, wgt, accum);
+                    const float gs = (act && araw < kAlphaMax) ? araw * dalpha : 0.f;
+                    T = act ? Tb : T;
+                    if (__ballot_sync(0xffffffffu, act) == 0) continue;
+                    float v[9];
+                    v[0] = gs * (r0.z * dx + r0.w * dy);
+                    v[1] = gs * (r0.w * dx + r1.x * dy);
+                    v[2] = -0.5f * gs * dx * dx;
+                    v[3] = -gs * dx * dy;
+                    v[4] = -0.5f * gs * dy * dy;
+                    v[5] = gs;
+                    v[6] = wgt * Gr;
+                    v[7] = wgt * Gg;
+                    v[8] = wgt * Gb;
+                    float sum = reduce_scatter9(v, lane);
+                    const int32_t g = S.gid[idx];
+                    if (writer) {
+                        if (my_comp == 5) sum *= ex2_approx(-r1.z);  // / opacity
+                        atomicAdd(A.grad2d + 9 * (int64_t)g + my_comp, sum);
+                    }
+                    if (lane == 0 && A.touched) A.touched[g] = 1;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+int g_resident[64][2];
+std::mutex g_mu;
+
+}  // namespace
+
+int raster_resident_ctas(int device) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (device < 0 || device >= 64) return 0;
+    if (g_resident[device][0] == 0) {
+        int sms = 0, per = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, raster_fwd_kernel, kThreads, 0);
+        g_resident[device][0] = std::max(1, sms * std::max(per, 1));
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, raster_bwd_kernel, kThreads, 0);
+        g_resident[device][1] = std::max(1, sms * std::max(per, 1));
+    }
+    return g_resident[device][0];
+}
+
+static int resident_bwd(int device) {
+    raster_resident_ctas(device);
+    std::lock_guard<std::mutex> lk(g_mu);
+    return g_resident[device][1];
+}
+
+RasterLayout raster_layout(int W, int H, int h_max) {
+    (void)W;
+    (void)H;
+    RasterLayout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off = (off + bytes + 255) & ~size_t(255);
+        return o;
+    };
+    const size_t hm = (size_t)std::max(h_max, 1);
+    const size_t px = hm * kMaxChunks * kThreads;
+    L.off_ctrl = take(kCtlWords * sizeof(int));
+    L.off_sat = take(hm * sizeof(int));
+    L.off_done = take(hm * sizeof(int));
+    L.off_part_c = take(px * sizeof(float4));
+    L.off_part_n = take(px * sizeof(int2));
+    L.off_bwd = take(px * sizeof(float4));
+    L.total = off;
+    return L;
+}
+
+static RasterArgs make_args(const CamParams& cam, const float* splats, const int32_t* ids,
+                            const int32_t* ranges, const int32_t* lpt, char* ws,
+                            const RasterLayout& L) {
+    RasterArgs A{};
+    A.W = cam.W;
+    A.H = cam.H;
+    A.ntx = cam.ntx;
+    A.nty = cam.nty;
+    A.splats = reinterpret_cast<const float4*>(splats);
+    A.ids = ids;
+    A.ranges = reinterpret_cast<const int2*>(ranges);
+    A.lpt = lpt;
+    A.ctrl = reinterpret_cast<int*>(ws + L.off_ctrl);
+    A.sat = reinterpret_cast<int*>(ws + L.off_sat);
+    A.done = reinterpret_cast<int*>(ws + L.off_done);
+    A.part_c = reinterpret_cast<float4*>(ws + L.off_part_c);
+    A.part_n = reinterpret_cast<int2*>(ws + L.off_part_n);
+    A.bstate = reinterpret_cast<float4*>(ws + L.off_bwd);
+    return A;
+}
+
+cudaError_t run_raster_fwd(const CamParams& cam, const RasterConfig& cfg, const float* splats,
+                           const int32_t* sorted_ids, const int32_t* tile_ranges,
+                           const int32_t* lpt_order, char* ws, const RasterLayout& L, float* image,
+                           float* t_final, int32_t* n_contrib, int32_t* last_idx, cudaStream_t st) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int K = raster_resident_ctas(dev);
+    RasterArgs A = make_args(cam, splats, sorted_ids, tile_ranges, lpt_order, ws, L);
+    A.image = image;
+    A.t_final = t_final;
+    A.n_contrib = n_contrib;
+    A.last_idx = last_idx;
+    const int nt = cam.ntx * cam.nty;
+    policy_kernel<<<1, kPolicyThreads, 0, st>>>(lpt_order, A.ranges, nt, K, cfg, A.ctrl, A.sat,
+                                                A.done);
+    raster_fwd_kernel<<<K, kThreads, 0, st>>>(A);
+    return cudaGetLastError();
+}
+
+cudaError_t run_raster_bwd(const CamParams& cam, const RasterConfig& cfg, int64_t n,
+                           const float* splats, const int32_t* sorted_ids,
+                           const int32_t* tile_ranges, const int32_t* lpt_order, char* ws,
+                           const RasterLayout& L, const float* t_final, const int32_t* last_idx,
+                           const float* dL_dimage, const float* dL_dt, float* grad2d,
+                           uint8_t* touched, cudaStream_t st) {
+    (void)cfg;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int K = resident_bwd(dev);
+    RasterArgs A = make_args(cam, splats, sorted_ids, tile_ranges, lpt_order, ws, L);
+    A.t_final_in = t_final;
+    A.last_in = last_idx;
+    A.dimg = dL_dimage;
+    A.dT = dL_dt;
+    A.grad2d = grad2d;
+    A.touched = touched;
+    cudaError_t err;
+    if (n > 0) {
+        err = cudaMemsetAsync(grad2d, 0, (size_t)n * 9 * sizeof(float), st);
+        if (err != cudaSuccess) return err;
+        if (touched) {
+            err = cudaMemsetAsync(touched, 0, (size_t)n, st);
+            if (err != cudaSuccess) return err;
+        }
+    }
+    err = cudaMemsetAsync(A.ctrl + kCtlQueueBwd, 0, sizeof(int), st);
+    if (err != cudaSuccess) return err;
+    raster_bwd_kernel<<<K, kThreads, 0, st>>>(A);
+    return cudaGetLastError();
+}
+
+}  // namespace gs

@@ -1,0 +1,259 @@
+/*
+ * gs.h -- C ABI of libgs, a tile-based differentiable 3D Gaussian splatting
+ * rasterizer (forward and backward) for NVIDIA GB300 (sm_103a).
+ *
+ * The five calls below are the hot path, in the order a training step runs
+ * them:
+ *
+ *   gs_project        3D Gaussians -> 2D splat records, depths, tile counts
+ *   gs_bin_sort       splats -> (tile, depth, id)-ordered id lists, tile
+ *                     ranges, heavy-tile-first (LPT) tile order
+ *   gs_rasterize_fwd  front-to-back alpha blending per pixel
+ *   gs_rasterize_bwd  per-pixel gradient recomputation -> nine screen-space
+ *                     derivatives per splat
+ *   gs_project_bwd    chain rule back to means, scales, quaternions,
+ *                     opacities and SH coefficients
+ *
+ * Sources (page title, section / equation):
+ *   [RY]  Ryu & Yoo, "Mitigating SM-Level Load Imbalance in 3D Gaussian
+ *         Splatting on GPUs": Sec. 2.1 Eq. 1 (projection), Eq. 2 (alpha),
+ *         Eq. 3 (blending, 1e-4 stop), Sec. 4.1 (LPT persistent kernel),
+ *         Sec. 4.2 Eq. 4-5 (depth-wise chunking, saturation signalling),
+ *         Sec. 4.3 (selective chunking), Sec. 4.4 Eq. 6 (per-frame policy).
+ *   [K]   Kopanas, "What the 3DGS Literature Left on the Table": Step 1 (a)
+ *         warp reduction of the nine gradients, (b) opacity-aware exact
+ *         conic-tile spans, (c) sub-tile masks and the 48-byte splat record,
+ *         (d) two-stage depth / tile radix sort, (e) gated SH and base-2
+ *         exponentials; Step 2 (reduce-scatter); Step 3 (SH, 59 gradient
+ *         floats per Gaussian); Step 5 (round-to-nearest quadratic).
+ *
+ * Conventions for every call
+ *   - All array arguments are DEVICE pointers (CUDA global memory), fp32 or
+ *     int32 unless stated, row-major and contiguous, 16-byte aligned.  The
+ *     caller owns every buffer; the library allocates no device memory.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *     enqueued on it and the call returns without waiting, except
+ *     gs_bin_sort when `n_pairs_host` is non-NULL (one stream sync).
+ *   - Argument errors are detected synchronously on the host and returned
+ *     as GS_ERR_INVALID_ARG before anything is enqueued.  A failed launch
+ *     returns GS_ERR_CUDA.
+ *   - Fixed method constants: 16x16 pixel tiles, alpha cutoff 1/255 (a
+ *     splat reaches pixel offset d iff q(d) <= tau = 2 ln(255 o)), alpha
+ *     clamp 0.99, transmittance stop 1e-4.  Pixel centres are at
+ *     (x + 0.5, y + 0.5); the principal point (cx, cy) is in the same frame.
+ *   - Activations are the caller's: scales > 0 and opacities in (0, 1) are
+ *     passed activated; quaternions (w, x, y, z) are normalised inside and
+ *     their gradient is taken w.r.t. the raw input.
+ */
+#ifndef GS_H
+#define GS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GS_TILE 16
+#define GS_ALPHA_MAX 0.99f
+#define GS_T_MIN 1e-4f
+#define GS_SPLAT_FLOATS 12 /* floats per splat record */
+#define GS_GRAD2D_FLOATS 9 /* screen-space derivatives per splat */
+#define GS_MAX_CHUNKS 16   /* largest k of the chunking policy */
+
+typedef enum {
+    GS_OK = 0,
+    GS_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or setting */
+    GS_ERR_CUDA = 2,        /* a CUDA runtime call or launch failed */
+    GS_ERR_CAPACITY = 3,    /* the pair list does not fit: see gs_bin_sort */
+    GS_ERR_TIMEOUT = 4,     /* reserved: a bounded device wait gave up */
+    GS_ERR_WORKSPACE = 5    /* workspace smaller than the size query returned */
+} gs_status;
+
+/* Pinhole camera.  viewmat is the row-major 4x4 world->camera matrix (rows 0..2
+ * used: rotation W and translation t_v); camera axes x right, y down, z forward.
+ * Gaussians with camera depth t_z <= znear (> 0) are culled. */
+typedef struct gs_camera {
+    float viewmat[16];
+    float fx, fy, cx, cy;
+    int32_t width, height;
+    float znear;
+} gs_camera;
+
+/* Scheduling of the blending kernels ([RY] Sec. 4.3-4.4).  These choose how the
+ * work is split across CTAs; they never change results. */
+typedef struct gs_settings {
+    int32_t split_mode;  /* 0: per-frame policy (Eq. 6); 1: never split;
+                            2: split the force_h heaviest tiles into force_k chunks */
+    int32_t force_h;     /* split_mode 2: number of tiles to split (<= h_max) */
+    int32_t force_k;     /* split_mode 2: chunks per split tile, 2..GS_MAX_CHUNKS */
+    int32_t h_max;       /* most tiles that may be split (sizes the workspace) */
+    float policy_lambda; /* per-chunk overhead in Gaussian-equivalents (Eq. 6) */
+    float policy_beta;   /* residual-imbalance penalty (Eq. 6) */
+    float policy_eps;    /* split only if the estimate improves by this fraction */
+} gs_settings;
+
+/* Default settings: policy on, h_max 256, lambda 256, beta 0.05, eps 0.10. */
+gs_settings gs_default_settings(void);
+
+/* Human-readable name of a status code (static string). */
+const char* gs_status_string(gs_status status);
+
+/* Number of 16x16 tiles of a width x height image: ceil(w/16) * ceil(h/16). */
+int64_t gs_num_tiles(int32_t width, int32_t height);
+
+/*
+ * gs_project -- [RY] Eq. 1; [K] Step 1 (b), (c), (e); Step 3.
+ * Per Gaussian i: camera-space t = W m + t_v; projected centre mu' (pinhole);
+ * Sigma = R(q) S S^T R(q)^T; Sigma' = J W Sigma W^T J^T with J the Jacobian of
+ * the projection at t; conic (a, b, c) = inverse of Sigma' with
+ * q(d) = a dx^2 + 2 b dx dy + c dy^2; tau = 2 ln(255 o) (fp32 rounding of the
+ * exact value); support half-extents rx = sqrt(tau Sigma'_xx),
+ * ry = sqrt(tau Sigma'_yy); the number of tiles whose pixel-centre hull meets
+ * the support ellipse (exact row spans); colour c = sum_k Y_k(d) s_k over the
+ * (sh_degree+1)^2 real SH basis functions at the unit view direction d (no
+ * offset, no clamp), evaluated only for visible Gaussians.
+ * The chain that decides integers (mu', conic, tau, extents, spans) is
+ * evaluated in fp32 with one fixed operation order (round-to-nearest, no
+ * contraction), so its results are reproducible bit for bit.
+ *
+ *   n              number of Gaussians (>= 0)
+ *   sh_degree      0..3; K = (sh_degree + 1)^2 coefficients per channel
+ *   means [n][3], scales [n][3] (> 0), quats [n][4] (w, x, y, z),
+ *   opacities [n] (in (0, 1)), sh [n][K][3]
+ * Outputs (visible = tiles_touched > 0; culled rows are all zero):
+ *   splats [n][12]  mux, muy, a, b | c, tau, log2(o), rx | r, g, b, ry
+ *   depths [n]      camera depth t_z
+ *   radii [n][2]    ceil(rx), ceil(ry) (clamped to 2^30)
+ *   tiles_touched [n]
+ */
+gs_status gs_project(const gs_camera* cam, int64_t n, int32_t sh_degree, const float* means,
+                     const float* scales, const float* quats, const float* opacities,
+                     const float* sh, float* splats, float* depths, int32_t* radii,
+                     int32_t* tiles_touched, void* stream);
+
+/* Workspace bytes gs_bin_sort needs for n Gaussians, a pair capacity and an
+ * image size (an upper bound; 0 on invalid arguments). */
+size_t gs_bin_sort_workspace_bytes(int64_t n, int64_t capacity, int32_t width, int32_t height);
+
+/*
+ * gs_bin_sort -- [K] Step 1 (b), (d); [RY] Sec. 4.1 (LPT ordering).
+ * Two-stage sort: the visible Gaussians are radix-sorted by depth (stable, so
+ * equal depths keep id order), every (tile, Gaussian) pair is emitted in that
+ * order from the exact row spans, and the pairs are radix-sorted by tile
+ * (stable).  The pair list is therefore ordered by (tile, depth, id).
+ *
+ *   splats, depths, tiles_touched   outputs of gs_project
+ *   workspace       device scratch of >= gs_bin_sort_workspace_bytes(...)
+ *   sorted_ids [capacity]     Gaussian id of every pair, in list order
+ *   tile_ranges [n_tiles][2]  [start, end) of each tile in sorted_ids
+ *   lpt_order [n_tiles]       tiles by descending pair count, ties by
+ *                             ascending tile id (heavy tiles first)
+ *   counts_device  optional device int64[2]: visible Gaussians M, pairs I
+ *   n_pairs_host   optional host int64: if non-NULL the call synchronises
+ *                  the stream and stores I; if I > capacity it returns
+ *                  GS_ERR_CAPACITY (outputs are then invalid: retry with a
+ *                  larger list).  With n_pairs_host NULL the call never
+ *                  synchronises and the caller must ensure I <= capacity
+ *                  (writes beyond capacity are always suppressed).
+ */
+gs_status gs_bin_sort(const gs_camera* cam, int64_t n, const float* splats, const float* depths,
+                      const int32_t* tiles_touched, void* workspace, size_t workspace_bytes,
+                      int32_t* sorted_ids, int64_t capacity, int32_t* tile_ranges,
+                      int32_t* lpt_order, int64_t* counts_device, int64_t* n_pairs_host,
+                      void* stream);
+
+/* Workspace bytes the two rasterize calls share for an image size and the
+ * given settings (NULL = defaults). */
+size_t gs_raster_workspace_bytes(int32_t width, int32_t height, const gs_settings* settings);
+
+/*
+ * gs_rasterize_fwd -- [RY] Eq. 2-5, Sec. 4.1-4.4; [K] Step 1 (c), Step 5, 6.
+ * Per pixel, front to back over its tile's list: stop before a splat once
+ * T < 1e-4; a splat is hit iff q <= tau, q = fma(fma(c, dy, B), dy, A) with
+ * A = (a dx) dx, B = (2b) dx, dx = (x + 0.5) - mux, dy = (y + 0.5) - muy in
+ * fp32 round-to-nearest; alpha = min(0.99, o exp(-q/2)); C += c alpha T;
+ * T *= 1 - alpha.  A persistent kernel takes work from a queue in LPT order;
+ * the heaviest tiles may be split into depth chunks whose partial results
+ * are composed with Eq. 5 (replaying the chunk that holds a pixel's stop, so
+ * the result is the sequential one).
+ *
+ *   settings        NULL = gs_default_settings()
+ *   workspace       >= gs_raster_workspace_bytes(...); it carries state to
+ *                   gs_rasterize_bwd and must not change between the calls
+ * Outputs:
+ *   image [H][W][3], t_final [H][W] (final transmittance; no background),
+ *   n_contrib [H][W] (blended splats), last_idx [H][W] (position in
+ *   sorted_ids of the last blended splat, -1 if none)
+ */
+gs_status gs_rasterize_fwd(const gs_camera* cam, const gs_settings* settings, int64_t n,
+                           const float* splats, const int32_t* sorted_ids,
+                           const int32_t* tile_ranges, const int32_t* lpt_order, void* workspace,
+                           size_t workspace_bytes, float* image, float* t_final,
+                           int32_t* n_contrib, int32_t* last_idx, void* stream);
+
+/*
+ * gs_rasterize_bwd -- [K] Step 1 (a), (e); Step 2; Step 5.
+ * Per pixel, back to front from last_idx, recovering T by division by
+ * (1 - alpha): for each blended splat with transmittance T_k before it,
+ * G = dL/dC and gT = dL/dT_final,
+ *   dL/dc       = alpha T_k G
+ *   dL/dalpha   = T_k (c . G) - (B_k . G) / (1 - alpha) - gT T_final / (1 - alpha)
+ *   (B_k the colour blended behind the splat) and, unless the 0.99 clamp is
+ *   active, dL/do = exp(-q/2) dL/dalpha, dL/dq = -(alpha/2) dL/dalpha,
+ *   dL/dmu' = -2 [a dx + b dy, b dx + c dy] dL/dq,
+ *   dL/d(a, b, c) = (dx^2, 2 dx dy, dy^2) dL/dq.
+ * Each warp reduces the nine values over its pixels (reduce-scatter of warp
+ * shuffles) before nine lanes add them atomically to grad2d.
+ *
+ *   splats .. workspace        as passed to gs_rasterize_fwd
+ *   t_final, last_idx          outputs of gs_rasterize_fwd
+ *   dL_dimage [H][W][3]
+ *   dL_dt_final [H][W]         optional (NULL = 0)
+ * Outputs (zeroed by the call first):
+ *   grad2d [n][9]   mux, muy, a, b, c, opacity, r, g, b
+ *   touched [n]     1 where a splat received a gradient (optional)
+ */
+gs_status gs_rasterize_bwd(const gs_camera* cam, const gs_settings* settings, int64_t n,
+                           const float* splats, const int32_t* sorted_ids,
+                           const int32_t* tile_ranges, const int32_t* lpt_order, void* workspace,
+                           size_t workspace_bytes, const float* t_final, const int32_t* last_idx,
+                           const float* dL_dimage, const float* dL_dt_final, float* grad2d,
+                           uint8_t* touched, void* stream);
+
+/*
+ * gs_project_bwd -- chain rule of gs_project ([RY] Eq. 1; [K] Step 3).
+ * From grad2d (the nine screen-space derivatives) to the 59 parameter
+ * gradients per Gaussian: conic -> Sigma' -> (Sigma, J) -> (scales,
+ * quaternion, t) -> means; colour -> SH coefficients and, through the view
+ * direction, -> means.  Gaussians that are culled (tiles_touched == 0) or
+ * untouched (touched == 0 when touched is given) get exact zeros; every row
+ * of every output is written.
+ *
+ *   inputs as for gs_project, plus tiles_touched (from gs_project),
+ *   grad2d [n][9] and touched [n] (optional) from gs_rasterize_bwd
+ * Outputs: dmeans [n][3], dscales [n][3], dquats [n][4], dopacities [n],
+ *   dsh [n][K][3]
+ */
+gs_status gs_project_bwd(const gs_camera* cam, int64_t n, int32_t sh_degree, const float* means,
+                         const float* scales, const float* quats, const float* opacities,
+                         const float* sh, const int32_t* tiles_touched, const float* grad2d,
+                         const uint8_t* touched, float* dmeans, float* dscales, float* dquats,
+                         float* dopacities, float* dsh, void* stream);
+
+/*
+ * gs_raster_stats -- diagnostics of the last gs_rasterize_fwd on a workspace.
+ * Synchronises the stream and copies to host out[8]:
+ *   out[0] h*  (tiles split)        out[1] k*  (chunks per split tile)
+ *   out[2] K   (resident CTAs)      out[3] work items of the persistent kernel
+ *   out[4] device error word (0 = none)
+ */
+gs_status gs_raster_stats(const void* workspace, size_t workspace_bytes, int64_t* out,
+                          void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GS_H */

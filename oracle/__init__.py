@@ -121,7 +121,7 @@ def n_tiles(cam) -> tuple[int, int]:
 # --------------------------------------------------------------------------
 @dataclass
 class Projection:
-    splat: np.ndarray          # [N, 11] mux, muy, a, b, c, opacity, tau, depth, P00, P01, P11
+    splat: np.ndarray          # [N, 13] mux, muy, a, b, c, opacity, tau, depth, P00, P01, P11, rx, ry
     rgb: np.ndarray            # [N, 3] float64
     radii: np.ndarray          # [N, 2] int32
     tiles_touched: np.ndarray  # [N] int32
@@ -138,7 +138,7 @@ def project(scene, cam, variant: str = "f32") -> Projection:
     vm, intr, W, H, zn = _cam_args(cam)
     means, scales, quats = _f32(scene.means), _f32(scene.scales), _f32(scene.quats)
     opac, sh = _f32(scene.opacities), _f32(scene.sh)
-    splat = np.zeros((n, 11), np.float64)
+    splat = np.zeros((n, 13), np.float64)
     rgb = np.zeros((n, 3), np.float64)
     radii = np.zeros((n, 2), np.int32)
     tt = np.zeros(n, np.int32)

@@ -57,6 +57,7 @@ typedef float dreal;
 #define ALPHA_MAX 0.99
 #define CUTOFF_INV 255.0 /* alpha cutoff 1/255 */
 #define RADIUS_MAX (1 << 30) /* radii are reported clamped to this */
+#define REC 13               /* doubles per exported splat record */
 
 /* ------------------------------------------------------------------------ */
 /* Camera                                                                    */
@@ -370,7 +371,7 @@ int ora_is_f64(void) { return DREAL_IS_DOUBLE; }
 /* ------------------------------------------------------------------------ */
 /*
  * Outputs per Gaussian i (culled Gaussians get zeros and tiles_touched 0):
- *   splat[i][0..10] = mux, muy, a, b, c, opacity, tau, depth t_z, P00, P01, P11
+ *   splat[i][0..12] = mux, muy, a, b, c, opacity, tau, depth t_z, P00, P01, P11, rx, ry
  *   rgb[i][0..2]    = sum_k Y_k(d) s_k (double; no offset, no clamp)
  *   radii[i][0..1]  = ceil(rx), ceil(ry)
  *   tiles_touched[i]
@@ -388,8 +389,8 @@ void ora_project(int64_t n, int sh_degree, const float* viewmat, const float* in
         splat_t s;
         project_one(&cam, means + 3 * i, scales + 3 * i, quats + 4 * i, opac[i], &s);
         int64_t nt = s.visible ? count_tiles(&cam, &s) : 0;
-        double* o = splat + 11 * i;
-        memset(o, 0, 11 * sizeof(double));
+        double* o = splat + REC * i;
+        memset(o, 0, REC * sizeof(double));
         rgb[3 * i] = rgb[3 * i + 1] = rgb[3 * i + 2] = 0;
         radii[2 * i] = radii[2 * i + 1] = 0;
         tiles_touched[i] = 0;
@@ -398,6 +399,7 @@ void ora_project(int64_t n, int sh_degree, const float* viewmat, const float* in
         o[2] = s.a;  o[3] = s.b;  o[4] = s.c;
         o[5] = opac[i];  o[6] = s.tau;  o[7] = s.tz;
         o[8] = s.P00;  o[9] = s.P01;  o[10] = s.P11;
+        o[11] = s.rx;  o[12] = s.ry;
         radii[2 * i] = to_int_clamped(ceil(s.rx), 0, RADIUS_MAX);
         radii[2 * i + 1] = to_int_clamped(ceil(s.ry), 0, RADIUS_MAX);
         tiles_touched[i] = (int32_t)nt;
@@ -425,8 +427,8 @@ static void splat_from_record(const double* o, splat_t* s) {
     s->P00 = (dreal)o[8];
     s->P01 = (dreal)o[9];
     s->P11 = (dreal)o[10];
-    s->rx = sqrt(s->tau * s->P00);
-    s->ry = sqrt(s->tau * s->P11);
+    s->rx = (dreal)o[11];
+    s->ry = (dreal)o[12];
     s->visible = 1;
 }
 
@@ -503,7 +505,7 @@ int64_t ora_bin(int64_t n, const float* viewmat, const float* intr, int W, int H
     for (int64_t i = 0; i < n; ++i) {
         if (tiles_touched[i] <= 0) continue;
         splat_t s;
-        splat_from_record(splat + 11 * i, &s);
+        splat_from_record(splat + REC * i, &s);
         int ty0, ty1, tx0, tx1;
         row_range(&cam, &s, &ty0, &ty1);
         for (int ty = ty0; ty < ty1; ++ty)
@@ -537,7 +539,7 @@ int64_t ora_bin(int64_t n, const float* viewmat, const float* intr, int W, int H
     for (int64_t i = 0; i < n; ++i) {
         if (tiles_touched[i] <= 0) continue;
         splat_t s;
-        splat_from_record(splat + 11 * i, &s);
+        splat_from_record(splat + REC * i, &s);
         int ty0, ty1, tx0, tx1;
         row_range(&cam, &s, &ty0, &ty1);
         for (int ty = ty0; ty < ty1; ++ty)
@@ -546,8 +548,8 @@ int64_t ora_bin(int64_t n, const float* viewmat, const float* intr, int W, int H
                     int64_t t = (int64_t)ty * cam.ntx + tx;
                     if (sel && !sel[t]) continue;
                     pairs[k].tile = (int32_t)t;
-                    pairs[k].depth = (float)splat[11 * i + 7];
-                    pairs[k].depth_d = splat[11 * i + 7];
+                    pairs[k].depth = (float)splat[REC * i + 7];
+                    pairs[k].depth_d = splat[REC * i + 7];
                     pairs[k].id = (int32_t)i;
                     ++k;
                 }
@@ -625,7 +627,7 @@ void ora_blend(int W, int H, const double* splat, const double* rgb, const int64
                         if (fabs(T - T_MIN) <= 2.0 * err * T) fl |= 1;
                         if (T < T_MIN) break;
                         int32_t g = ids[sel_off[t] + (k - s0)];
-                        const double* rec = splat + 11 * (int64_t)g;
+                        const double* rec = splat + REC * (int64_t)g;
                         dreal q;
                         double dx, dy;
                         if (!hit_test(rec, px, py, &q, &dx, &dy)) continue;
@@ -692,7 +694,7 @@ void ora_blend_bwd(int W, int H, const double* splat, const double* rgb, const i
                     for (int64_t k = s0; k < s1; ++k) {
                         if (T < T_MIN) break;
                         int32_t g = ids[sel_off[t] + (k - s0)];
-                        const double* rec = splat + 11 * (int64_t)g;
+                        const double* rec = splat + REC * (int64_t)g;
                         dreal q;
                         double dx, dy;
                         if (!hit_test(rec, px, py, &q, &dx, &dy)) continue;
@@ -721,7 +723,7 @@ void ora_blend_bwd(int W, int H, const double* splat, const double* rgb, const i
                     double behind[3] = {0, 0, 0};
                     for (int64_t j = nb - 1; j >= 0; --j) {
                         blended_t* e = &list[j];
-                        const double* rec = splat + 11 * (int64_t)e->g;
+                        const double* rec = splat + REC * (int64_t)e->g;
                         const double* col = rgb + 3 * (int64_t)e->g;
                         double* gr = grad2d + 9 * (int64_t)e->g;
                         double* ga = gabs + 9 * (int64_t)e->g;

@@ -158,7 +158,9 @@ def config3(rng, n):
     quats = _unit_quats(rng, n)
     logits = rng.normal(0.0, 2.0, n)
     sh = _sh_deg3(rng, n)
-    cam = pinhole(np.eye(4), 1150.0, 1297, 840)
+    # inside the scene's extent (z in [-8, 8]) at z = -6 looking +z: about a third of the
+    # Gaussians are visible, as in the garden scene of the pages (507K of 1.5M)
+    cam = pinhole(look_at((0, 0, -6), (0, 0, 0)), 1150.0, 1297, 840)
     return _pack(means, log_scales, quats, logits, sh, 3), cam
 
 
