@@ -1,0 +1,401 @@
+"""Benchmark of the differentiable 3DGS rasterizer hot path on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 3] [--impl reference]
+
+A step is one pass of the whole hot path over one synthetic view: gs_project,
+gs_bin_sort, gs_rasterize_fwd, gs_rasterize_bwd (dL/dimage = w, loss = sum w*img)
+and gs_project_bwd, on the 1.5M-Gaussian 1297x840 SH-3 scene by default (inputs
+resident in HBM; they are larger than L2, 354 MB of parameters plus 354 MB of
+gradients per step).  The metric is tile-Gaussian pairs per second (higher is
+better); ms_per_step is the matching ms/iter.
+
+Rank 0 prints ONE JSON line.  Under torchrun (N > 1) every rank renders its own
+replica of the view (the path does not shard across GPUs: replicas only), the
+time is the max over ranks and `value` counts the pairs of all ranks.
+
+--impl reference times the CPU oracle (oracle/, plain C, one core) on a bounded
+sample of the same workload and prints the same line with "impl": "reference".
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synthetic_scenes as ss  # noqa: E402
+
+METRIC = "raster fwd+bwd ms/iter & tile-Gaussian pairs/s, 1.5M Gaussians @1297×840"
+UNIT = "pairs/s"
+
+# Algorithmic work per contributing pixel-splat pair E (counted from the
+# oracle's scalar formulas, an FMA counted as 2 flops; exponentials and
+# reciprocals run on the SFU and are not counted):
+#   forward : dx, dy 2; A 2; B 2; q 4; exponent 2; clamp 1; w 1; C 6; T 2   = 22
+#   backward: the 13 of the quadratic / exponent / clamp; 1 - alpha 1; T_k 1;
+#             w 1; c.G 5; dL/dalpha 4; colour-behind 2; g 1; nine outputs 20 = 48
+FLOPS_FWD_PER_E = 22
+FLOPS_BWD_PER_E = 48
+FP32_LANES_PER_SM = 128
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--config", type=int, default=3)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import differentiable_gaussian_splatting_gb300 as gs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    sc, cam = ss.make_config(args.config)
+    w = ss.loss_weights(args.config, cam.height, cam.width)
+    H, W = cam.height, cam.width
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    inputs = [to_dev(x) for x in (sc.means, sc.scales, sc.quats, sc.opacities, sc.sh)]
+    dimg = to_dev(w)
+    r = gs.Rasterizer(cam, sc.sh_degree, sc.n, device=dev)
+    r.forward(*inputs)  # sizes the pair list (one host sync, outside the timed region)
+    n_pairs = r.n_pairs
+    cap = int(n_pairs * 1.25) + 1024
+    r._alloc_pairs(cap)
+    r.forward(*inputs)
+    torch.cuda.synchronize()
+    E = int(r.n_contrib.sum().item())  # contributing pixel-splat pairs
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        n = r.n
+        if ev:
+            ev[0].record(stream)
+        gs.gs_project(r.cam, n, r.sh_degree, *inputs, r.splats, r.depths, r.radii, r.tiles_touched)
+        if ev:
+            ev[1].record(stream)
+        gs.gs_bin_sort(r.cam, n, r.splats, r.depths, r.tiles_touched, r.bin_ws, r.sorted_ids,
+                       r.capacity, r.tile_ranges, r.lpt_order, r.counts, sync_pairs=False)
+        if ev:
+            ev[2].record(stream)
+        gs.gs_rasterize_fwd(r.cam, n, r.splats, r.sorted_ids, r.tile_ranges, r.lpt_order,
+                            r.raster_ws, r.image, r.t_final, r.n_contrib, r.last_idx, r.settings)
+        if ev:
+            ev[3].record(stream)
+        gs.gs_rasterize_bwd(r.cam, n, r.splats, r.sorted_ids, r.tile_ranges, r.lpt_order,
+                            r.raster_ws, r.t_final, r.last_idx, dimg, None, r.grad2d, r.touched,
+                            r.settings)
+        if ev:
+            ev[4].record(stream)
+        gs.gs_project_bwd(r.cam, n, r.sh_degree, *inputs, r.tiles_touched, r.grad2d, r.touched,
+                          *grads)
+        if ev:
+            ev[5].record(stream)
+
+    K = (sc.sh_degree + 1) ** 2
+    grads = [torch.empty((sc.n, 3), device=dev), torch.empty((sc.n, 3), device=dev),
+             torch.empty((sc.n, 4), device=dev), torch.empty(sc.n, device=dev),
+             torch.empty((sc.n, K, 3), device=dev)]
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(stop)
+    counts = r.counts.cpu().numpy()
+    assert counts[1] == n_pairs and counts[1] <= r.capacity, counts
+    calls = ["gs_project", "gs_bin_sort", "gs_rasterize_fwd", "gs_rasterize_bwd", "gs_project_bwd"]
+    per_call = {c: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
+                for j, c in enumerate(calls)}
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * n_pairs / (ms_per_step * 1e-3)
+
+    # roofline of the dominant call (all its work is one kernel launch after small set-up)
+    peaks = measured_peaks()
+    clocks = clk.summary()
+    props = torch.cuda.get_device_properties(dev)
+    sm_mhz = clocks["sm_mhz"] or peaks.get("clocks_under_load", {}).get("sm_mhz_median") or 1462.0
+    dom = max(per_call, key=per_call.get)
+    roof = roofline(dom, per_call[dom], sc, n_pairs, E, H, W, peaks, props.multi_processor_count,
+                    sm_mhz)
+    launches = kernel_launches(sc.n, r.capacity, W, H)
+
+    e2e = None if args.no_e2e else run_e2e(gs, r, sc, cam, w, dev, args, n_pairs)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(sc, cam, w)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": ss.CONFIG_NAMES[args.config], "gaussians": sc.n,
+                       "image": f"{W}x{H}", "sh_degree": sc.sh_degree, "tile_pairs": n_pairs,
+                       "contributing_pairs": E, "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (354 MB parameters + 354 MB gradients)"},
+            "per_call_ms": per_call,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
+                       "reasons": clocks["reasons"]},
+            "gpu_launches": launches * args.steps,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def roofline(call, ms, sc, n_pairs, E, H, W, peaks, n_sm, sm_mhz):
+    """Algorithmic work of one launch / its average duration, against the binding peak."""
+    if call in ("gs_rasterize_fwd", "gs_rasterize_bwd"):
+        per = FLOPS_FWD_PER_E if call == "gs_rasterize_fwd" else FLOPS_BWD_PER_E
+        flops = per * E
+        peak = 2.0 * FP32_LANES_PER_SM * n_sm * sm_mhz * 1e6 / 1e12  # FMA = 2 flops
+        achieved = flops / (ms * 1e-3) / 1e12
+        return {"kernel": call, "bound": "alu", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "peak_source": f"{n_sm} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 x {sm_mhz:.0f} MHz (sampled)",
+                "work": f"{per} flops x {E} contributing pairs"}
+    N = sc.n
+    K = (sc.sh_degree + 1) ** 2
+    if call == "gs_project":
+        byts = N * (12 + 12 + 16 + 4 + 48 + 4 + 8 + 4) + N * 12 * K
+    elif call == "gs_project_bwd":
+        byts = N * (12 + 12 + 16 + 4 + 4 + 1 + 36) + N * 12 * K + N * (12 + 12 + 16 + 4 + 12 * K)
+    else:  # gs_bin_sort
+        byts = 8 * N * 8 + 8 * n_pairs * 5
+    achieved = byts / (ms * 1e-3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    return {"kernel": call, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": None,
+            "peak_source": f"{peaks['source']} copy bandwidth"}
+
+
+def kernel_launches(n, capacity, W, H) -> int:
+    """Kernels one step launches (memsets excluded)."""
+    nt = ((W + 15) // 16) * ((H + 15) // 16)
+
+    def passes(bits):
+        return max(1, (bits + 7) // 8)
+
+    tile_bits = max(1, int(nt - 1).bit_length())
+    cap_bits = max(1, int(capacity).bit_length())
+    bin_sort = 3 + 3 * passes(31) + 3 + 1 + 3 * passes(tile_bits) + 2 + 1 + 3 * passes(cap_bits)
+    return 1 + bin_sort + 2 + 1 + 1
+
+
+def run_e2e(gs, r, sc, cam, w, dev, args, n_pairs):
+    """Same metric through the public API with host buffers: pinned inputs copied in and
+    the image and all parameter gradients copied out inside the timed region."""
+    import torch
+
+    host_in = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+               for a in (sc.means, sc.scales, sc.quats, sc.opacities, sc.sh, w)]
+    dev_in = [torch.empty(h.shape, dtype=h.dtype, device=dev) for h in host_in]
+    K = (sc.sh_degree + 1) ** 2
+    out_shapes = [(cam.height, cam.width, 3), (sc.n, 3), (sc.n, 3), (sc.n, 4), (sc.n,), (sc.n, K, 3)]
+    host_out = [torch.empty(s, dtype=torch.float32).pin_memory() for s in out_shapes]
+    bi = sum(h.numel() * h.element_size() for h in host_in)
+    bo = sum(h.numel() * h.element_size() for h in host_out)
+
+    def step():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        r.forward(*dev_in[:5], sync_pairs=False)
+        g = r.backward(dev_in[5])
+        outs = [r.image, g.means, g.scales, g.quats, g.opacities, g.sh]
+        for h, d in zip(host_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / args.steps
+    return {"value": n_pairs / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+def oracle_sample_step(sc, cam, w, tile_stride: int):
+    """One bounded oracle step: projection and binning of the whole view, then the
+    forward and backward blend of every tile_stride-th tile (in LPT order, so the
+    sample spans heavy and light tiles).  Returns (pairs processed, seconds)."""
+    import oracle
+
+    t0 = time.perf_counter()
+    proj = oracle.project(sc, cam)
+    ntx, nty = oracle.n_tiles(cam)
+    counts = oracle.bin_sort(cam, proj, np.zeros(ntx * nty, np.uint8))
+    sel = np.zeros(ntx * nty, np.uint8)
+    sel[counts.lpt_order[::tile_stride]] = 1
+    b = oracle.bin_sort(cam, proj, sel)
+    oracle.blend(cam, proj, b)
+    g2, _ = oracle.blend_bwd(cam, proj, b, w)
+    oracle.project_bwd(sc, cam, proj, g2)
+    dt = time.perf_counter() - t0
+    return int(b.counts[sel.astype(bool)].sum()), dt
+
+
+def cpu_baseline(sc, cam, w, stride: int = 8):
+    pairs, dt = oracle_sample_step(sc, cam, w, stride)
+    return {"value": pairs / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"one view: all projections and tile counts, forward + backward of every "
+                      f"{stride}th tile in LPT order ({pairs} pairs), {dt:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    sc, cam = ss.make_config(args.config)
+    w = ss.loss_weights(args.config, cam.height, cam.width)
+    stride = 32
+    for _ in range(args.warmup):
+        oracle_sample_step(sc, cam, w, stride)
+    tot_pairs, tot_s = 0, 0.0
+    for _ in range(args.steps):
+        p, dt = oracle_sample_step(sc, cam, w, stride)
+        tot_pairs += p
+        tot_s += dt
+    value = tot_pairs / tot_s
+    sample = (f"each step: all projections and tile counts, forward + backward of every "
+              f"{stride}th tile in LPT order ({tot_pairs // args.steps} pairs)")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": ss.CONFIG_NAMES[args.config]},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_gpu(a)

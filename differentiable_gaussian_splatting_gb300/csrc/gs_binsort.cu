@@ -384,6 +384,48 @@ __global__ void tile_ranges_kernel(const uint32_t* __restrict__ keys, const int6
     }
 }
 
+// empty tiles get [p, p) with p the end of the last non-empty tile before them
+// (so that starts are the exclusive prefix sum of the counts); one block
+__global__ void __launch_bounds__(kScanThreads) fill_empty_ranges(int2* __restrict__ ranges,
+                                                                  int64_t nt) {
+    __shared__ int s_part[kScanThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t per = (nt + kScanThreads - 1) / kScanThreads;
+    const int64_t lo = min64(nt, per * tid), hi = min64(nt, lo + per);
+    int m = 0;
+    for (int64_t t = lo; t < hi; ++t) m = max(m, ranges[t].y);
+    int x = m;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x = max(x, y);
+    }
+    if (lane == 31) s_part[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = s_part[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w = max(w, y);
+        }
+        s_part[lane] = w;
+    }
+    __syncthreads();
+    // exclusive running max of the ends before this thread's segment
+    int run = warp > 0 ? s_part[warp - 1] : 0;
+    int prev_lane = __shfl_up_sync(0xffffffffu, x, 1);
+    if (lane > 0) run = max(run, prev_lane);
+    for (int64_t t = lo; t < hi; ++t) {
+        int2 r = ranges[t];
+        if (r.y == 0) {
+            ranges[t] = make_int2(run, run);
+        } else {
+            run = max(run, r.y);
+        }
+    }
+}
+
 // LPT keys: descending pair count = ascending (maxk - count); stable -> ties by tile id
 __global__ void lpt_keys_kernel(const int2* __restrict__ ranges, int64_t nt, uint32_t maxk,
                                 uint32_t* __restrict__ keys, int32_t* __restrict__ vals) {
@@ -493,6 +535,7 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
         if (err != cudaSuccess) return err;
         // 6. tile ranges
         tile_ranges_kernel<<<1024, 256, 0, st>>>(pks, counts + 2, reinterpret_cast<int2*>(tile_ranges));
+        fill_empty_ranges<<<1, kScanThreads, 0, st>>>(reinterpret_cast<int2*>(tile_ranges), nt);
     }
     // 7. LPT order: tiles by descending count, ties by tile id
     {

@@ -18,7 +18,7 @@ constexpr float kTMin = 1e-4f;
 constexpr float kAlphaMax = 0.99f;
 constexpr float kNegHalfLog2e = -0.72134752044448170368f;  // -log2(e) / 2
 constexpr float kPadUnit = 0.00390625f;                     // 2^-8 px
-constexpr float kPadScale = 6.103515625e-05f;               // 2^-14
+constexpr float kPadScale = 0.00390625f;                    // 2^-8
 constexpr int kRadiusMax = 1 << 30;
 constexpr int kMaxChunks = 16;  // largest k of the chunking policy
 
@@ -53,10 +53,14 @@ __device__ __forceinline__ int to_int_clamped(float f, int lo, int hi) {
 
 // ---------------------------------------------------------------------------
 // splat record: three float4 per splat (48 bytes, 16-byte aligned)
-//   r0 = (mux, muy, a, b)   r1 = (c, tau, log2 o, rx)   r2 = (r, g, b, ry)
+//   r0 = (mux, muy, l11, l12)   r1 = (l22, tau, log2 o, rx)   r2 = (r, g, b, ry)
+// The conic Lambda = Sigma'^-1 is carried by its Cholesky factor
+// L = [[l11, l12], [0, l22]] (Lambda = L^T L), so that the quadratic
+// q = (l11 dx + l12 dy)^2 + (l22 dy)^2 is a sum of non-negative terms and its
+// fp32 evaluation stays well conditioned for thin splats far from the image.
 // ---------------------------------------------------------------------------
 struct Ellipse {
-    float mux, muy, a, b, c, tau, rx, ry;
+    float mux, muy, l11, l12, l22, tau, rx, ry;
 };
 
 __device__ __forceinline__ Ellipse ellipse_of(const float4& r0, const float4& r1, const float4& r2) {
@@ -67,15 +71,23 @@ __device__ __forceinline__ Ellipse ellipse_of(const float4& r0, const float4& r1
 // exact row spans ("What the 3DGS Literature Left on the Table", Step 1 (b))
 // ---------------------------------------------------------------------------
 // The support ellipse q(d) <= tau has right boundary
-//   x_r(dy) = (sqrt(a tau - detL dy^2) - b dy) / a,
-// concave in dy with its vertex at dy = -b rx / c; the left boundary is
-// x_l(dy) = -x_r(-dy).  Bands are widened by pady and extents by padx,
-// pad = 2^-8 px + r 2^-14, so that every pixel whose fp32 hit test passes
-// lies in an emitted tile.
-__device__ __forceinline__ float xr_at(const Ellipse& s, float detL, float dy) {
-    float disc = rsub(rmul(s.a, s.tau), rmul(detL, rmul(dy, dy)));
+//   x_r(dy) = (sqrt(tau - (l22 dy)^2) - l12 dy) / l11,
+// concave in dy with its vertex at dy = -sqrt(tau) l12 / (l22 h),
+// h = sqrt(l12^2 + l22^2); the left boundary is x_l(dy) = -x_r(-dy).  Bands
+// are widened by pady and extents by padx, pad = 2^-8 px + r 2^-8, so that
+// every pixel whose fp32 hit test passes lies in an emitted tile: near the
+// tips of the ellipse the fp32 boundary is uncertain by about sqrt(u) times
+// the half-width (u = 2^-24), which the r 2^-8 term covers.
+__device__ __forceinline__ float xr_at(const Ellipse& s, float dy) {
+    float t = rmul(s.l22, dy);
+    float disc = rsub(s.tau, rmul(t, t));
     if (!(disc > 0.f)) disc = 0.f;
-    return rdiv(rsub(rsqrt_exact(disc), rmul(s.b, dy)), s.a);
+    return rdiv(rsub(rsqrt_exact(disc), rmul(s.l12, dy)), s.l11);
+}
+
+__device__ __forceinline__ float vertex_dy(const Ellipse& s) {
+    float h = rsqrt_exact(radd(rmul(s.l12, s.l12), rmul(s.l22, s.l22)));
+    return -rdiv(rmul(rsqrt_exact(s.tau), s.l12), rmul(s.l22, h));
 }
 
 __device__ __forceinline__ float pad_of(float r) { return radd(kPadUnit, rmul(r, kPadScale)); }
@@ -89,12 +101,11 @@ __device__ __forceinline__ bool band_extent(const Ellipse& s, float y0, float y1
     float lo = smax(rsub(y0, s.muy), -ryp);
     float hi = smin(rsub(y1, s.muy), ryp);
     if (!(lo <= hi)) return false;
-    float detL = rsub(rmul(s.a, s.c), rmul(s.b, s.b));
-    float dyv = -rdiv(rmul(s.b, s.rx), s.c);
+    float dyv = vertex_dy(s);
     float dh = smin(smax(smin(smax(dyv, lo), hi), -s.ry), s.ry);
     float dl = smin(smax(smin(smax(dyv, -hi), -lo), -s.ry), s.ry);
-    float xhi = radd(xr_at(s, detL, dh), padx);
-    float xlo_neg = radd(xr_at(s, detL, dl), padx);
+    float xhi = radd(xr_at(s, dh), padx);
+    float xlo_neg = radd(xr_at(s, dl), padx);
     *Xhi = radd(s.mux, xhi);
     *Xlo = rsub(s.mux, xlo_neg);
     return true;
@@ -126,12 +137,15 @@ __device__ __forceinline__ bool row_span(const Ellipse& s, int ty, int W, int H,
 }
 
 // ---------------------------------------------------------------------------
-// per-pixel quadratic: q = fma(fma(c, dy, B), dy, A), A = (a dx) dx, B = (2b) dx
+// per-pixel quadratic: q = fma(u1, u1, u2 u2), u1 = fma(l11, dx, l12 dy), u2 = l22 dy
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float quad_A(float a, float dx) { return rmul(rmul(a, dx), dx); }
-__device__ __forceinline__ float quad_B(float b, float dx) { return rmul(rmul(2.0f, b), dx); }
-__device__ __forceinline__ float quad_q(float c, float A, float B, float dy) {
-    return rfma(rfma(c, dy, B), dy, A);
+__device__ __forceinline__ float quad_q(float l11, float l12, float l22, float dx, float dy,
+                                        float* u1_out, float* u2_out) {
+    const float u1 = rfma(l11, dx, rmul(l12, dy));
+    const float u2 = rmul(l22, dy);
+    *u1_out = u1;
+    *u2_out = u2;
+    return rfma(u1, u1, rmul(u2, u2));
 }
 
 // ---------------------------------------------------------------------------

@@ -78,7 +78,7 @@ __device__ __forceinline__ float3 sh_grad(int k, float x, float y, float z) {
 struct Projected {
     bool ok;
     float tx, ty, tz;
-    float mux, muy, a, b, c, tau, rx, ry;
+    float mux, muy, l11, l12, l22, tau, rx, ry;
 };
 
 __device__ __forceinline__ Projected project_chain(const CamParams& cam, float mx, float my,
@@ -152,6 +152,11 @@ __device__ __forceinline__ Projected project_chain(const CamParams& cam, float m
     float a = rdiv(P11, det);
     float b = -rdiv(P01, det);
     float c = rdiv(P00, det);
+    // Cholesky factor of the conic from Sigma' (no cancellation beyond det):
+    // l22 = 1/sqrt(P11), l11 = sqrt(P11/det), l12 = -(P01/P11) l11
+    float l22 = rdiv(1.f, rsqrt_exact(P11));
+    float l11 = rsqrt_exact(rdiv(P11, det));
+    float l12 = -rmul(rdiv(P01, P11), l11);
     // tau = fp32 rounding of 2 ln(255 o), evaluated in double
     double td = 2.0 * log(255.0 * (double)opac);
     float tau = __double2float_rn(td);
@@ -159,13 +164,13 @@ __device__ __forceinline__ Projected project_chain(const CamParams& cam, float m
     float rx = rsqrt_exact(rmul(tau, P00));
     float ry = rsqrt_exact(rmul(tau, P11));
     if (!isfinite(mux) || !isfinite(muy) || !isfinite(a) || !isfinite(b) || !isfinite(c) ||
-        !isfinite(rx) || !isfinite(ry))
+        !isfinite(l11) || !isfinite(l12) || !isfinite(l22) || !isfinite(rx) || !isfinite(ry))
         return P;
     P.mux = mux;
     P.muy = muy;
-    P.a = a;
-    P.b = b;
-    P.c = c;
+    P.l11 = l11;
+    P.l12 = l12;
+    P.l22 = l22;
     P.tau = tau;
     P.rx = rx;
     P.ry = ry;
@@ -195,7 +200,7 @@ __global__ void __launch_bounds__(256) project_kernel(CamParams cam, int64_t n,
                                 scales[3 * i + 2], quats[i], o);
     int tiles = 0;
     if (P.ok) {
-        Ellipse e{P.mux, P.muy, P.a, P.b, P.c, P.tau, P.rx, P.ry};
+        Ellipse e{P.mux, P.muy, P.l11, P.l12, P.l22, P.tau, P.rx, P.ry};
         int ty0, ty1, tx0, tx1;
         row_range(e, cam.nty, &ty0, &ty1);
         for (int ty = ty0; ty < ty1; ++ty)
@@ -238,8 +243,8 @@ __global__ void __launch_bounds__(256) project_kernel(CamParams cam, int64_t n,
             cb += Y[k] * __ldg(row + 3 * k + 2);
         }
     }
-    rec[0] = make_float4(P.mux, P.muy, P.a, P.b);
-    rec[1] = make_float4(P.c, P.tau, log2f(o), P.rx);
+    rec[0] = make_float4(P.mux, P.muy, P.l11, P.l12);
+    rec[1] = make_float4(P.l22, P.tau, log2f(o), P.rx);
     rec[2] = make_float4(cr, cg, cb, P.ry);
     depths[i] = P.tz;
     radii[i] = make_int2(to_int_clamped(ceilf(P.rx), 0, kRadiusMax),

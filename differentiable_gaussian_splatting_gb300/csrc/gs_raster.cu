@@ -167,7 +167,8 @@ __device__ bool blend_range(const RasterArgs& A, Smem& S, int tx, int ty, float 
                 const int idx = c + q;
                 const float4 r0 = S.r0[idx], r1 = S.r1[idx], r2 = S.r2[idx];
                 const float dx = rsub(px, r0.x), dy = rsub(py, r0.y);
-                const float qv = quad_q(r1.x, quad_A(r0.z, dx), quad_B(r0.w, dx), dy);
+                float u1, u2;
+                const float qv = quad_q(r0.z, r0.w, r1.x, dx, dy, &u1, &u2);
                 const bool hit = (qv <= r1.y) && !st.done;
                 float alpha = fminf(ex2_approx(fmaf(qv, kNegHalfLog2e, r1.z)), kAlphaMax);
                 alpha = hit ? alpha : 0.f;
@@ -550,7 +551,8 @@ __global__ void __launch_bounds__(kThreads) raster_bwd_kernel(RasterArgs A) {
                     const int64_t gpos = bs + idx;
                     const float4 r0 = S.r0[idx], r1 = S.r1[idx], r2 = S.r2[idx];
                     const float dx = rsub(px, r0.x), dy = rsub(py, r0.y);
-                    const float qv = quad_q(r1.x, quad_A(r0.z, dx), quad_B(r0.w, dx), dy);
+                    float u1, u2;
+                    const float qv = quad_q(r0.z, r0.w, r1.x, dx, dy, &u1, &u2);
                     const bool act = (qv <= r1.y) && gpos <= (int64_t)last;
                     const float araw = ex2_approx(fmaf(qv, kNegHalfLog2e, r1.z));
                     float alpha = fminf(araw, kAlphaMax);
@@ -564,9 +566,11 @@ __global__ void __launch_bounds__(kThreads) raster_bwd_kernel(RasterArgs A) {
                     const float gs = (act && araw < kAlphaMax) ? araw * dalpha : 0.f;
                     T = act ? Tb : T;
                     if (__ballot_sync(0xffffffffu, act) == 0) continue;
+                    // conic of the evaluated quadratic: a = l11^2, b = l11 l12,
+                    // c = l12^2 + l22^2, so a dx + b dy = l11 u1, b dx + c dy = l12 u1 + l22 u2
                     float v[9];
-                    v[0] = gs * (r0.z * dx + r0.w * dy);
-                    v[1] = gs * (r0.w * dx + r1.x * dy);
+                    v[0] = gs * (r0.z * u1);
+                    v[1] = gs * fmaf(r0.w, u1, r1.x * u2);
                     v[2] = -0.5f * gs * dx * dx;
                     v[3] = -gs * dx * dy;
                     v[4] = -0.5f * gs * dy * dy;

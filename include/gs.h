@@ -108,7 +108,10 @@ int64_t gs_num_tiles(int32_t width, int32_t height);
  * Per Gaussian i: camera-space t = W m + t_v; projected centre mu' (pinhole);
  * Sigma = R(q) S S^T R(q)^T; Sigma' = J W Sigma W^T J^T with J the Jacobian of
  * the projection at t; conic (a, b, c) = inverse of Sigma' with
- * q(d) = a dx^2 + 2 b dx dy + c dy^2; tau = 2 ln(255 o) (fp32 rounding of the
+ * q(d) = a dx^2 + 2 b dx dy + c dy^2, carried by its Cholesky factor
+ * (l11, l12, l22), a = l11^2, b = l11 l12, c = l12^2 + l22^2, taken from
+ * Sigma' as l22 = 1/sqrt(Sigma'_yy), l11 = sqrt(Sigma'_yy / det Sigma'),
+ * l12 = -(Sigma'_xy / Sigma'_yy) l11; tau = 2 ln(255 o) (fp32 rounding of the
  * exact value); support half-extents rx = sqrt(tau Sigma'_xx),
  * ry = sqrt(tau Sigma'_yy); the number of tiles whose pixel-centre hull meets
  * the support ellipse (exact row spans); colour c = sum_k Y_k(d) s_k over the
@@ -123,7 +126,7 @@ int64_t gs_num_tiles(int32_t width, int32_t height);
  *   means [n][3], scales [n][3] (> 0), quats [n][4] (w, x, y, z),
  *   opacities [n] (in (0, 1)), sh [n][K][3]
  * Outputs (visible = tiles_touched > 0; culled rows are all zero):
- *   splats [n][12]  mux, muy, a, b | c, tau, log2(o), rx | r, g, b, ry
+ *   splats [n][12]  mux, muy, l11, l12 | l22, tau, log2(o), rx | r, g, b, ry
  *   depths [n]      camera depth t_z
  *   radii [n][2]    ceil(rx), ceil(ry) (clamped to 2^30)
  *   tiles_touched [n]
@@ -171,9 +174,10 @@ size_t gs_raster_workspace_bytes(int32_t width, int32_t height, const gs_setting
 /*
  * gs_rasterize_fwd -- [RY] Eq. 2-5, Sec. 4.1-4.4; [K] Step 1 (c), Step 5, 6.
  * Per pixel, front to back over its tile's list: stop before a splat once
- * T < 1e-4; a splat is hit iff q <= tau, q = fma(fma(c, dy, B), dy, A) with
- * A = (a dx) dx, B = (2b) dx, dx = (x + 0.5) - mux, dy = (y + 0.5) - muy in
- * fp32 round-to-nearest; alpha = min(0.99, o exp(-q/2)); C += c alpha T;
+ * T < 1e-4; a splat is hit iff q <= tau, q = fma(u1, u1, u2 u2) with
+ * u1 = fma(l11, dx, l12 dy), u2 = l22 dy, dx = (x + 0.5) - mux,
+ * dy = (y + 0.5) - muy in fp32 round-to-nearest (a sum of non-negative terms,
+ * well conditioned for thin splats); alpha = min(0.99, o exp(-q/2)); C += c alpha T;
  * T *= 1 - alpha.  A persistent kernel takes work from a queue in LPT order;
  * the heaviest tiles may be split into depth chunks whose partial results
  * are composed with Eq. 5 (replaying the chunk that holds a pixel's stop, so

@@ -45,6 +45,7 @@ _LIBS: dict[str, C.CDLL] = {}
 TILE = 16
 T_MIN = 1e-4
 ALPHA_MAX = 0.99
+REC = 16  # doubles per projected splat record
 
 
 def lib_path(variant: str) -> str:
@@ -121,7 +122,8 @@ def n_tiles(cam) -> tuple[int, int]:
 # --------------------------------------------------------------------------
 @dataclass
 class Projection:
-    splat: np.ndarray          # [N, 13] mux, muy, a, b, c, opacity, tau, depth, P00, P01, P11, rx, ry
+    splat: np.ndarray          # [N, 16] mux, muy, a, b, c, opacity, tau, depth, P00, P01, P11,
+    #                            rx, ry, l11, l12, l22 (conic = L^T L, L = [[l11, l12], [0, l22]])
     rgb: np.ndarray            # [N, 3] float64
     radii: np.ndarray          # [N, 2] int32
     tiles_touched: np.ndarray  # [N] int32
@@ -129,6 +131,11 @@ class Projection:
     @property
     def visible(self) -> np.ndarray:
         return self.tiles_touched > 0
+
+    def conic_of_factor(self) -> np.ndarray:
+        """[N, 3] conic (a, b, c) of the evaluated quadratic, from its Cholesky factor."""
+        l11, l12, l22 = self.splat[:, 13], self.splat[:, 14], self.splat[:, 15]
+        return np.stack([l11 * l11, l11 * l12, l12 * l12 + l22 * l22], 1)
 
 
 def project(scene, cam, variant: str = "f32") -> Projection:
@@ -138,7 +145,7 @@ def project(scene, cam, variant: str = "f32") -> Projection:
     vm, intr, W, H, zn = _cam_args(cam)
     means, scales, quats = _f32(scene.means), _f32(scene.scales), _f32(scene.quats)
     opac, sh = _f32(scene.opacities), _f32(scene.sh)
-    splat = np.zeros((n, 13), np.float64)
+    splat = np.zeros((n, REC), np.float64)
     rgb = np.zeros((n, 3), np.float64)
     radii = np.zeros((n, 2), np.int32)
     tt = np.zeros(n, np.int32)
@@ -244,8 +251,9 @@ def blend_bwd(cam, proj: Projection, b: Binning, dL_dimg: np.ndarray,
               dL_dT: np.ndarray | None = None, variant: str = "f32"):
     """Nine screen-space derivatives per splat, summed over the selected tiles.
 
-    Returns (grad2d [N, 9], gabs [N, 9]) with columns (mux, muy, a, b, c, opacity, r, g, b);
-    gabs is the sum of |term| (for diagnosing cancellation)."""
+    Returns (grad2d [N, 9], gmag [N, 9]) with columns (mux, muy, a, b, c, opacity, r, g, b);
+    gmag is the magnitude of what each element sums (every product and every addend of
+    dL/dalpha in absolute value); it equals |grad2d| when nothing cancels."""
     lib = _lib(variant)
     W, H = int(cam.width), int(cam.height)
     n = int(proj.splat.shape[0])
@@ -265,6 +273,21 @@ class ParamGrads:
     quats: np.ndarray      # [N, 4]
     opacities: np.ndarray  # [N]
     sh: np.ndarray         # [N, K, 3]
+
+
+def project_bwd_magnitude(scene, cam, proj: Projection, gmag: np.ndarray) -> ParamGrads:
+    """|J| gmag: the magnitudes of the 9 screen-space sums carried to the 59 parameter
+    gradients through the absolute value of the (linear) chain rule J, column by column."""
+    n = int(scene.means.shape[0])
+    out = None
+    for c in range(9):
+        e = np.zeros((n, 9))
+        e[:, c] = 1.0
+        J = project_bwd(scene, cam, proj, e)
+        part = [np.abs(getattr(J, k)) * (gmag[:, c].reshape((-1,) + (1,) * (getattr(J, k).ndim - 1)))
+                for k in ("means", "scales", "quats", "opacities", "sh")]
+        out = part if out is None else [o + p for o, p in zip(out, part)]
+    return ParamGrads(*out)
 
 
 def project_bwd(scene, cam, proj: Projection, grad2d: np.ndarray, variant: str = "f32") -> ParamGrads:

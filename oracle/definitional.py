@@ -43,21 +43,23 @@ def fma_f32(x, y, z):
     return r
 
 
-def quad_f32(a, b, c, dx, dy):
-    """q = fma(fma(c, dy, B), dy, A), A = (a dx) dx, B = (2b) dx, in fp32 round-to-nearest
-    (the reproducible evaluation of the quadratic form that Kopanas, Step 5, requires)."""
+def quad_f32(l11, l12, l22, dx, dy):
+    """q = fma(u1, u1, u2 u2), u1 = fma(l11, dx, l12 dy), u2 = l22 dy, in fp32
+    round-to-nearest: d^T Lambda d through the Cholesky factor of the conic (the
+    reproducible evaluation of the quadratic that Kopanas, Step 5, requires)."""
     f = np.float32
-    a, b, c, dx, dy = (np.asarray(v, f) for v in (a, b, c, dx, dy))
-    A = (a * dx) * dx
-    B = (f(2) * b) * dx
-    return fma_f32(fma_f32(c, dy, B), dy, A)
+    l11, l12, l22, dx, dy = (np.asarray(v, f) for v in (l11, l12, l22, dx, dy))
+    u1 = fma_f32(l11, dx, l12 * dy)
+    u2 = l22 * dy
+    return fma_f32(u1, u1, u2 * u2)
 
 
 def brute_force_blend(cam, splat: np.ndarray, rgb: np.ndarray, visible: np.ndarray,
                       tie_rel: float = 1e-5, fp32_quadratic: bool = True):
     """Blend every visible splat over every pixel, front to back.
 
-    splat rows: mux, muy, a, b, c, opacity, tau, depth (the oracle's record).
+    splat rows: the oracle's record (mux, muy, a, b, c, opacity, tau, depth, ...,
+    l11, l12, l22 in columns 13..15).
     With fp32_quadratic the quadratic form is the fp32 round-to-nearest
     evaluation of ``quad_f32``; otherwise plain float64.
     Returns img [H, W, 3], T [H, W], n_contrib [H, W], ambiguous [H, W] where
@@ -76,11 +78,13 @@ def brute_force_blend(cam, splat: np.ndarray, rgb: np.ndarray, visible: np.ndarr
     amb = np.zeros((H, W), bool)
     for g in order:
         mux, muy, a, b, c, o, tau = splat[g, :7]
+        l11, l12, l22 = splat[g, 13:16]
         if fp32_quadratic:
             dx = px - np.float32(mux)
             dy = py - np.float32(muy)
-            q = quad_f32(a, b, c, dx, dy).astype(np.float64)
+            q = quad_f32(l11, l12, l22, dx, dy).astype(np.float64)
         else:
+            a, b, c = l11 * l11, l11 * l12, l12 * l12 + l22 * l22
             dx = px.astype(np.float64) - mux
             dy = py.astype(np.float64) - muy
             q = a * dx * dx + 2.0 * b * dx * dy + c * dy * dy

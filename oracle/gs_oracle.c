@@ -57,7 +57,7 @@ typedef float dreal;
 #define ALPHA_MAX 0.99
 #define CUTOFF_INV 255.0 /* alpha cutoff 1/255 */
 #define RADIUS_MAX (1 << 30) /* radii are reported clamped to this */
-#define REC 13               /* doubles per exported splat record */
+#define REC 16               /* doubles per exported splat record */
 
 /* ------------------------------------------------------------------------ */
 /* Camera                                                                    */
@@ -95,6 +95,7 @@ typedef struct {
     dreal mux, muy;
     dreal P00, P01, P11; /* Sigma' */
     dreal a, b, c;       /* conic = inverse of Sigma'; q = a dx^2 + 2 b dx dy + c dy^2 */
+    dreal l11, l12, l22; /* conic = L^T L, L = [[l11, l12], [0, l22]] */
     dreal tau;           /* support threshold 2 ln(255 o) */
     dreal rx, ry;        /* half extents of the support ellipse */
 } splat_t;
@@ -186,13 +187,18 @@ static void project_one(const camera_t* cam, const float* m3, const float* s3, c
     dreal a = P11 / det;
     dreal b = -(P01 / det);
     dreal c = P00 / det;
+    /* Cholesky factor of the conic, taken from Sigma' without cancellation:
+     * l22 = 1/sqrt(P11), l11 = sqrt(P11/det), l12 = -(P01/P11) l11 */
+    dreal l22 = 1 / sqrt(P11);
+    dreal l11 = sqrt(P11 / det);
+    dreal l12 = -((P01 / P11) * l11);
 
     dreal tau = support_tau(opac);
     if (!(tau > 0)) return;
     dreal rx = sqrt(tau * P00);
     dreal ry = sqrt(tau * P11);
     if (!finite_d(mux) || !finite_d(muy) || !finite_d(a) || !finite_d(b) || !finite_d(c) ||
-        !finite_d(rx) || !finite_d(ry))
+        !finite_d(l11) || !finite_d(l12) || !finite_d(l22) || !finite_d(rx) || !finite_d(ry))
         return;
 
     sp->mux = mux;
@@ -203,6 +209,9 @@ static void project_one(const camera_t* cam, const float* m3, const float* s3, c
     sp->a = a;
     sp->b = b;
     sp->c = c;
+    sp->l11 = l11;
+    sp->l12 = l12;
+    sp->l22 = l22;
     sp->tau = tau;
     sp->rx = rx;
     sp->ry = ry;
@@ -215,19 +224,27 @@ static void project_one(const camera_t* cam, const float* m3, const float* s3, c
 /*
  * A tile's region is the closed hull of its pixel centres (x + 0.5, y + 0.5)
  * clipped to the image.  For each tile row, the support ellipse
- * q(d) <= tau, inflated by pad = 2^-8 px + r * 2^-14, is intersected with the
+ * q(d) <= tau, inflated by pad = 2^-8 px + r * 2^-8, is intersected with the
  * row's band and the covered tile columns [tx0, tx1) follow in closed form.
- * The band is widened by pady; x_r is evaluated at the band point nearest its
- * vertex, clamped to |dy| <= ry, and the result widened by padx.
- * The right boundary of the ellipse is x_r(dy) = (sqrt(a tau - detL dy^2) -
- * b dy) / a; it is concave in dy with its vertex at dy = -b rx / c, and the
- * left boundary is x_l(dy) = -x_r(-dy).
+ * With q = (l11 dx + l12 dy)^2 + (l22 dy)^2 the right boundary is
+ * x_r(dy) = (sqrt(tau - (l22 dy)^2) - l12 dy) / l11, concave in dy with its
+ * vertex at dy = -sqrt(tau) l12 / (l22 h), h = sqrt(l12^2 + l22^2); the left
+ * boundary is x_l(dy) = -x_r(-dy).  The band is widened by pady; x_r is
+ * evaluated at the band point nearest its vertex, clamped to |dy| <= ry, and
+ * the result widened by padx.  Near the ellipse's tips the fp32 boundary is
+ * uncertain by about sqrt(u) r (u = 2^-24); the r 2^-8 term covers that.
  */
 
-static dreal xr_at(const splat_t* s, dreal detL, dreal dy) {
-    dreal disc = s->a * s->tau - detL * (dy * dy);
+static dreal xr_at(const splat_t* s, dreal dy) {
+    dreal t = s->l22 * dy;
+    dreal disc = s->tau - t * t;
     if (!(disc > 0)) disc = 0;
-    return (sqrt(disc) - s->b * dy) / s->a;
+    return (sqrt(disc) - s->l12 * dy) / s->l11;
+}
+
+static dreal vertex_dy(const splat_t* s) {
+    dreal h = sqrt(s->l12 * s->l12 + s->l22 * s->l22);
+    return -((sqrt(s->tau) * s->l12) / (s->l22 * h));
 }
 
 static dreal dmin(dreal x, dreal y) { return x < y ? x : y; }
@@ -242,8 +259,8 @@ static int to_int_clamped(dreal f, int lo, int hi) {
 
 /* rows [*ty0, *ty1) that the padded ellipse may cover */
 static void row_range(const camera_t* cam, const splat_t* s, int* ty0, int* ty1) {
-    const dreal pad_unit = (dreal)0.00390625;      /* 2^-8 */
-    const dreal pad_scale = (dreal)6.103515625e-05; /* 2^-14 */
+    const dreal pad_unit = (dreal)0.00390625;  /* 2^-8 */
+    const dreal pad_scale = (dreal)0.00390625; /* 2^-8 */
     dreal pady = pad_unit + s->ry * pad_scale;
     dreal ryp = s->ry + pady;
     dreal f0 = ceil(((s->muy - ryp) - (dreal)15.5) * (dreal)0.0625);
@@ -254,8 +271,8 @@ static void row_range(const camera_t* cam, const splat_t* s, int* ty0, int* ty1)
 
 /* span of tile columns [*tx0, *tx1) in row ty; returns 0 when empty */
 static int row_span(const camera_t* cam, const splat_t* s, int ty, int* tx0, int* tx1) {
-    const dreal pad_unit = (dreal)0.00390625;
-    const dreal pad_scale = (dreal)6.103515625e-05;
+    const dreal pad_unit = (dreal)0.00390625;  /* 2^-8 */
+    const dreal pad_scale = (dreal)0.00390625; /* 2^-8 */
     dreal padx = pad_unit + s->rx * pad_scale;
     dreal pady = pad_unit + s->ry * pad_scale;
     dreal ryp = s->ry + pady;
@@ -264,13 +281,12 @@ static int row_span(const camera_t* cam, const splat_t* s, int ty, int* tx0, int
     dreal lo = dmax(y0 - s->muy, -ryp);
     dreal hi = dmin(y1 - s->muy, ryp);
     if (!(lo <= hi)) return 0;
-    dreal detL = s->a * s->c - s->b * s->b;
-    dreal dyv = -((s->b * s->rx) / s->c);
+    dreal dyv = vertex_dy(s);
     /* evaluate x_r only on the ellipse itself: |dy| <= ry */
     dreal dh = dmin(dmax(dmin(dmax(dyv, lo), hi), -s->ry), s->ry);
     dreal dl = dmin(dmax(dmin(dmax(dyv, -hi), -lo), -s->ry), s->ry);
-    dreal xhi = xr_at(s, detL, dh) + padx;
-    dreal xlo_neg = xr_at(s, detL, dl) + padx;
+    dreal xhi = xr_at(s, dh) + padx;
+    dreal xlo_neg = xr_at(s, dl) + padx;
     dreal Xhi = s->mux + xhi;
     dreal Xlo = s->mux - xlo_neg;
     if (Xlo > (dreal)cam->W - (dreal)0.5 || Xhi < (dreal)0.5) return 0;
@@ -371,7 +387,8 @@ int ora_is_f64(void) { return DREAL_IS_DOUBLE; }
 /* ------------------------------------------------------------------------ */
 /*
  * Outputs per Gaussian i (culled Gaussians get zeros and tiles_touched 0):
- *   splat[i][0..12] = mux, muy, a, b, c, opacity, tau, depth t_z, P00, P01, P11, rx, ry
+ *   splat[i][0..15] = mux, muy, a, b, c, opacity, tau, depth t_z, P00, P01, P11, rx, ry,
+ *                     l11, l12, l22
  *   rgb[i][0..2]    = sum_k Y_k(d) s_k (double; no offset, no clamp)
  *   radii[i][0..1]  = ceil(rx), ceil(ry)
  *   tiles_touched[i]
@@ -400,6 +417,7 @@ void ora_project(int64_t n, int sh_degree, const float* viewmat, const float* in
         o[5] = opac[i];  o[6] = s.tau;  o[7] = s.tz;
         o[8] = s.P00;  o[9] = s.P01;  o[10] = s.P11;
         o[11] = s.rx;  o[12] = s.ry;
+        o[13] = s.l11;  o[14] = s.l12;  o[15] = s.l22;
         radii[2 * i] = to_int_clamped(ceil(s.rx), 0, RADIUS_MAX);
         radii[2 * i + 1] = to_int_clamped(ceil(s.ry), 0, RADIUS_MAX);
         tiles_touched[i] = (int32_t)nt;
@@ -429,6 +447,9 @@ static void splat_from_record(const double* o, splat_t* s) {
     s->P11 = (dreal)o[10];
     s->rx = (dreal)o[11];
     s->ry = (dreal)o[12];
+    s->l11 = (dreal)o[13];
+    s->l12 = (dreal)o[14];
+    s->l22 = (dreal)o[15];
     s->visible = 1;
 }
 
@@ -566,8 +587,10 @@ int64_t ora_bin(int64_t n, const float* viewmat, const float* intr, int W, int H
 /*
  * Per pixel of every selected tile, front to back over the tile's list:
  *   stop before a splat once T < 1e-4;
- *   hit iff q <= tau with q = fma(fma(c, dy, B), dy, A), A = (a dx) dx,
- *   B = (2b) dx, dx = (x + 0.5) - mux, dy = (y + 0.5) - muy (all in dreal);
+ *   hit iff q <= tau with q = fma(u1, u1, u2 u2), u1 = fma(l11, dx, l12 dy),
+ *   u2 = l22 dy, dx = (x + 0.5) - mux, dy = (y + 0.5) - muy (all in dreal):
+ *   the quadratic form d^T Lambda d evaluated through the Cholesky factor of
+ *   the conic, a sum of non-negative terms (well conditioned for thin splats);
  *   alpha = min(0.99, o exp(-q/2));  C += c alpha T;  T *= 1 - alpha.
  * Outputs: img[H][W][3], T_final[H][W], n_contrib[H][W] (blended splats) and
  * last_idx[H][W] (position in the full sorted pair list of the last blended
@@ -596,13 +619,13 @@ typedef struct {
 static int hit_test(const double* rec, int px, int py, dreal* q_out, double* dx_out,
                     double* dy_out) {
     dreal mux = (dreal)rec[0], muy = (dreal)rec[1];
-    dreal a = (dreal)rec[2], b = (dreal)rec[3], c = (dreal)rec[4];
+    dreal l11 = (dreal)rec[13], l12 = (dreal)rec[14], l22 = (dreal)rec[15];
     dreal tau = (dreal)rec[6];
     dreal dx = ((dreal)px + (dreal)0.5) - mux;
     dreal dy = ((dreal)py + (dreal)0.5) - muy;
-    dreal A = (a * dx) * dx;
-    dreal B = (2 * b) * dx;
-    dreal q = fma(fma(c, dy, B), dy, A);
+    dreal u1 = fma(l11, dx, l12 * dy);
+    dreal u2 = l22 * dy;
+    dreal q = fma(u1, u1, u2 * u2);
     *q_out = q;
     *dx_out = (double)dx;
     *dy_out = (double)dy;
@@ -666,7 +689,12 @@ void ora_blend(int W, int H, const double* splat, const double* rgb, const int64
  *   dL/dmux = -2 (a dx + b dy) dL/dq,  dL/dmuy = -2 (b dx + c dy) dL/dq,
  *   dL/da = dx^2 dL/dq,  dL/db = 2 dx dy dL/dq,  dL/dc = dy^2 dL/dq.
  * grad2d[g][0..8] = (mux, muy, a, b, c, opacity, r, g, b), accumulated in
- * double over every selected tile; gabs[g][0..8] accumulates |term|.
+ * double over every selected tile.  gabs[g][0..8] accumulates the magnitude
+ * of each term: the same product with every factor, and every addend of
+ * dL/dalpha (T_k |c.G|, sum_{j>k} |c_j.G| alpha_j T_j / (1 - alpha_k),
+ * |gT| T_final / (1 - alpha_k)), taken in absolute value.  It bounds the sum
+ * of absolute values of what a floating-point evaluation adds up, and equals
+ * |grad2d| when nothing cancels.
  */
 typedef struct {
     int32_t g;
@@ -721,6 +749,7 @@ void ora_blend_bwd(int W, int H, const double* splat, const double* rgb, const i
                     double gT = dL_dT ? dL_dT[p] : 0.0;
                     double Tfin = T;
                     double behind[3] = {0, 0, 0};
+                    double behind_abs = 0;
                     for (int64_t j = nb - 1; j >= 0; --j) {
                         blended_t* e = &list[j];
                         const double* rec = splat + REC * (int64_t)e->g;
@@ -728,26 +757,44 @@ void ora_blend_bwd(int W, int H, const double* splat, const double* rgb, const i
                         double* gr = grad2d + 9 * (int64_t)e->g;
                         double* ga = gabs + 9 * (int64_t)e->g;
                         double term[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+                        double mag[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
                         double w = e->alpha * e->T;
-                        for (int ch = 0; ch < 3; ++ch) term[6 + ch] = w * G[ch];
+                        for (int ch = 0; ch < 3; ++ch) {
+                            term[6 + ch] = w * G[ch];
+                            mag[6 + ch] = fabs(term[6 + ch]);
+                        }
                         double cG = col[0] * G[0] + col[1] * G[1] + col[2] * G[2];
                         double bG = behind[0] * G[0] + behind[1] * G[1] + behind[2] * G[2];
                         double dalpha = e->T * cG - bG / (1.0 - e->alpha) -
                                         gT * Tfin / (1.0 - e->alpha);
+                        double dalpha_mag = e->T * fabs(cG) + behind_abs / (1.0 - e->alpha) +
+                                            fabs(gT) * Tfin / (1.0 - e->alpha);
                         for (int ch = 0; ch < 3; ++ch) behind[ch] += col[ch] * w;
+                        behind_abs += fabs(cG) * w;
                         if (!e->clamped) {
                             double dq = -0.5 * e->alpha * dalpha;
-                            double a = rec[2], b = rec[3], c = rec[4];
+                            /* conic of the evaluated quadratic: a = l11^2,
+                             * b = l11 l12, c = l12^2 + l22^2 */
+                            double l11 = rec[13], l12 = rec[14], l22 = rec[15];
+                            double a = l11 * l11, b = l11 * l12, c = l12 * l12 + l22 * l22;
                             term[5] = exp(-0.5 * e->q) * dalpha;
                             term[0] = -2.0 * (a * e->dx + b * e->dy) * dq;
                             term[1] = -2.0 * (b * e->dx + c * e->dy) * dq;
                             term[2] = e->dx * e->dx * dq;
                             term[3] = 2.0 * e->dx * e->dy * dq;
                             term[4] = e->dy * e->dy * dq;
+                            double dq_mag = 0.5 * e->alpha * dalpha_mag;
+                            double u1 = fabs(l11 * e->dx) + fabs(l12 * e->dy);
+                            mag[5] = exp(-0.5 * e->q) * dalpha_mag;
+                            mag[0] = 2.0 * fabs(l11) * u1 * dq_mag;
+                            mag[1] = 2.0 * (fabs(l12) * u1 + l22 * l22 * fabs(e->dy)) * dq_mag;
+                            mag[2] = e->dx * e->dx * dq_mag;
+                            mag[3] = 2.0 * fabs(e->dx * e->dy) * dq_mag;
+                            mag[4] = e->dy * e->dy * dq_mag;
                         }
                         for (int r = 0; r < 9; ++r) {
                             gr[r] += term[r];
-                            ga[r] += fabs(term[r]);
+                            ga[r] += mag[r];
                         }
                     }
                 }

@@ -1,8 +1,11 @@
 """Helpers for the GPU parity tests: run the C-ABI path on the device and compare it with
 the CPU oracle.  Tolerances (north star of the method): bit-exact integers; RGB and final
 transmittance within 1e-5 relative / 1e-6 absolute; gradients within 1e-4 relative /
-1e-6 absolute of the oracle.  Pixels whose stop decision the oracle flags as a fp32
-near-tie are excluded from the forward comparison and have dL/dC = 0 for the backward."""
+1e-6 absolute, relative to the magnitude of what each gradient sums (the oracle's sum of
+the absolute values of every product and addend; it equals |gradient| when nothing
+cancels, and a floating-point sum's error is bounded in proportion to it).  Pixels whose
+stop decision the oracle flags as a fp32 near-tie are excluded from the forward comparison
+and have dL/dC = 0 for the backward."""
 
 from __future__ import annotations
 
@@ -71,9 +74,9 @@ def check_projection(g: GpuRun, ref: oracle.Projection, sc, rows=None):
     vis = rows[ref.tiles_touched[rows] > 0]
     gs_ = g.splats[vis]
     rs = ref.splat[vis].astype(np.float32)
-    # record: mux, muy, a, b | c, tau, log2 o, rx | r, g, b, ry
-    for gi, ri, name in ((0, 0, "mux"), (1, 1, "muy"), (2, 2, "a"), (3, 3, "b"), (4, 4, "c"),
-                         (5, 6, "tau"), (7, 11, "rx"), (11, 12, "ry")):
+    # record: mux, muy, l11, l12 | l22, tau, log2 o, rx | r, g, b, ry
+    for gi, ri, name in ((0, 0, "mux"), (1, 1, "muy"), (2, 13, "l11"), (3, 14, "l12"),
+                         (4, 15, "l22"), (5, 6, "tau"), (7, 11, "rx"), (11, 12, "ry")):
         bad = np.nonzero(gs_[:, gi] != rs[:, ri])[0]
         assert len(bad) == 0, f"{name} differs at {len(bad)} Gaussians, e.g. {vis[bad[:5]]}"
     np.testing.assert_array_equal(g.depths[vis], rs[:, 7])
@@ -110,14 +113,18 @@ def masked_weights(w, im: oracle.Image):
     return (w * (im.flags == 0)[..., None]).astype(np.float32)
 
 
-def assert_grads_close(gpu, ref, name, rtol=GRAD_RTOL, atol=GRAD_ATOL):
+def assert_grads_close(gpu, ref, name, mag=None, rtol=GRAD_RTOL, atol=GRAD_ATOL):
+    """|gpu - ref| <= atol + rtol * magnitude, the magnitude being the oracle's magnitude of
+    the summed terms (>= |ref|; equal to it when nothing cancels), or |ref| if not given."""
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
+    scale = np.abs(ref) if mag is None else np.maximum(np.asarray(mag, np.float64), np.abs(ref))
     err = np.abs(gpu - ref)
-    lim = atol + rtol * np.abs(ref)
+    lim = atol + rtol * scale
     bad = err > lim
     if bad.any():
         i = np.argmax(err / lim)
         raise AssertionError(f"{name}: {bad.sum()} / {bad.size} outside tolerance; worst "
-                             f"gpu={gpu.flat[i]:.9g} ref={ref.flat[i]:.9g} (|err|/tol "
-                             f"{(err / lim).flat[i]:.3g})")
+                             f"gpu={gpu.flat[i]:.9g} ref={ref.flat[i]:.9g} magnitude "
+                             f"{scale.flat[i]:.4g} (|err|/tol {(err / lim).flat[i]:.3g})")
+    return float((err / np.maximum(scale, 1e-30)).max()) if err.size else 0.0

@@ -16,6 +16,40 @@ from gpu_util import (assert_grads_close, check_binning, check_forward, check_pr
 pytestmark = pytest.mark.gpu
 
 
+def _check_param_grads(sc, cam, proj, pg, r2, mag, rows=None):
+    """End to end: GPU chain(GPU grad2d) vs oracle chain(oracle grad2d), against the
+    grad2d magnitudes carried through |J|."""
+    rows = np.arange(sc.n) if rows is None else rows
+    sub = sc.subset(rows)
+    p = oracle.Projection(proj.splat[rows], proj.rgb[rows], proj.radii[rows],
+                          proj.tiles_touched[rows])
+    rp = oracle.project_bwd(sub, cam, p, r2[rows])
+    pm = oracle.project_bwd_magnitude(sub, cam, p, mag[rows])
+    for k in ("means", "scales", "quats", "opacities", "sh"):
+        assert_grads_close(pg[k][rows], getattr(rp, k), k, getattr(pm, k))
+
+
+def _check_project_bwd_alone(sc, cam, proj, r2):
+    """The chain rule by itself: the GPU's gs_project_bwd fed the oracle's grad2d."""
+    import torch
+
+    import differentiable_gaussian_splatting_gb300 as gs
+    from gpu_util import t
+
+    n, K = sc.n, (sc.sh_degree + 1) ** 2
+    outs = [torch.empty((n, 3), device="cuda"), torch.empty((n, 3), device="cuda"),
+            torch.empty((n, 4), device="cuda"), torch.empty(n, device="cuda"),
+            torch.empty((n, K, 3), device="cuda")]
+    gs.gs_project_bwd(gs.Camera.of(cam), n, sc.sh_degree, t(sc.means), t(sc.scales),
+                      t(sc.quats), t(sc.opacities), t(sc.sh), t(proj.tiles_touched),
+                      t(r2.astype(np.float32)), None, *outs)
+    torch.cuda.synchronize()
+    rp = oracle.project_bwd(sc, cam, proj, r2)
+    pm = oracle.project_bwd_magnitude(sc, cam, proj, np.abs(r2))
+    for k, o in zip(("means", "scales", "quats", "opacities", "sh"), outs):
+        assert_grads_close(o.cpu().numpy(), getattr(rp, k), "alone:" + k, getattr(pm, k))
+
+
 def _full_parity(sc, cam, w, v=None, settings=None):
     g = run_forward(sc, cam, settings=settings)
     ref = oracle.render(sc, cam)
@@ -25,11 +59,10 @@ def _full_parity(sc, cam, w, v=None, settings=None):
     wm = masked_weights(w, ref.image)
     vm = None if v is None else (v * (ref.image.flags == 0)).astype(np.float32)
     g2, touched, pg = run_backward(g, wm, vm)
-    r2, _ = oracle.blend_bwd(cam, ref.proj, ref.binning, wm, vm)
-    assert_grads_close(g2, r2, "grad2d")
-    rp = oracle.project_bwd(sc, cam, ref.proj, r2)
-    for k in ("means", "scales", "quats", "opacities", "sh"):
-        assert_grads_close(pg[k], getattr(rp, k), k, rtol=1e-3, atol=1e-5)
+    r2, mag = oracle.blend_bwd(cam, ref.proj, ref.binning, wm, vm)
+    assert_grads_close(g2, r2, "grad2d", mag)
+    _check_param_grads(sc, cam, ref.proj, pg, r2, mag)
+    _check_project_bwd_alone(sc, cam, ref.proj, r2)
     return g, ref
 
 
@@ -107,13 +140,9 @@ def _sampled_parity(c, n_gauss=48, n_rand_tiles=12, n_heavy=6):
     check_forward(g, im)
     wm = masked_weights(w, im)
     g2, _, pg = run_backward(g, wm)
-    r2, _ = oracle.blend_bwd(cam, proj, b, wm)
-    assert_grads_close(g2[sample], r2[sample], "grad2d")
-    rp = oracle.project_bwd(sc.subset(sample), cam, oracle.Projection(
-        proj.splat[sample], proj.rgb[sample], proj.radii[sample], proj.tiles_touched[sample]),
-        r2[sample])
-    for k in ("means", "scales", "quats", "opacities", "sh"):
-        assert_grads_close(pg[k][sample], getattr(rp, k), k, rtol=1e-3, atol=1e-5)
+    r2, mag = oracle.blend_bwd(cam, proj, b, wm)
+    assert_grads_close(g2[sample], r2[sample], "grad2d", mag[sample])
+    _check_param_grads(sc, cam, proj, pg, r2, mag, rows=sample)
     culled = proj.tiles_touched == 0
     for k in ("means", "scales", "quats", "opacities", "sh"):
         assert np.all(pg[k][culled] == 0), k

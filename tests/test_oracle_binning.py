@@ -32,20 +32,23 @@ def test_emitted_tiles_are_exact_and_complete(seed, W, H, n):
         rec = p.splat[g]
         if p.tiles_touched[g] == 0:
             # culled: either invisible, or the ellipse meets no tile
-            if rec[6] > 0 and rec[2] > 0:
+            if rec[6] > 0 and rec[13] > 0:
+                a, b, c = p.conic_of_factor()[g]
                 for t in range(ntx * nty):
                     x0, x1, y0, y1 = D.tile_hull(cam, t)
-                    qmin = D.rect_min_q(rec[2], rec[3], rec[4], x0 - rec[0], x1 - rec[0],
+                    qmin = D.rect_min_q(a, b, c, x0 - rec[0], x1 - rec[0],
                                         y0 - rec[1], y1 - rec[1])
                     assert qmin > rec[6] * (1 - 1e-5)
             continue
         nvis += 1
         tiles = set(oracle.splat_tiles(cam, rec).tolist())
         assert len(tiles) == p.tiles_touched[g]
-        a, b, c, tau = rec[2], rec[3], rec[4], rec[6]
-        rx, ry = np.sqrt(tau * rec[8]), np.sqrt(tau * rec[10])
-        padx = 2.0 ** -8 + rx * 2.0 ** -14 + 1e-4
-        pady = 2.0 ** -8 + ry * 2.0 ** -14 + 1e-4
+        # the quadratic is evaluated through its Cholesky factor: its conic
+        a, b, c = p.conic_of_factor()[g]
+        tau = rec[6]
+        rx, ry = rec[11], rec[12]
+        padx = 2.0 ** -8 + rx * 2.0 ** -8 + 1e-4
+        pady = 2.0 ** -8 + ry * 2.0 ** -8 + 1e-4
         for t in range(ntx * nty):
             x0, x1, y0, y1 = D.tile_hull(cam, t)
             qmin = D.rect_min_q(a, b, c, x0 - rec[0], x1 - rec[0], y0 - rec[1], y1 - rec[1])
@@ -104,10 +107,75 @@ def test_three_sigma_square_contains_emitted_tiles_when_tau_le_9():
     checked = 0
     for g in np.nonzero(p.visible & (p.splat[:, 6] <= 9.0))[0]:
         P = np.array([[p.splat[g, 8], p.splat[g, 9]], [p.splat[g, 9], p.splat[g, 10]]])
-        r3 = 3.0 * np.sqrt(np.linalg.eigvalsh(P).max()) + 0.01
+        r3 = 3.0 * np.sqrt(np.linalg.eigvalsh(P).max()) * (1 + 2.0 ** -8) + 2.0 ** -8 + 0.01
         for t in oracle.splat_tiles(cam, p.splat[g]):
             x0, x1, y0, y1 = D.tile_hull(cam, int(t))
             assert x0 <= p.splat[g, 0] + r3 and x1 >= p.splat[g, 0] - r3
             assert y0 <= p.splat[g, 1] + r3 and y1 >= p.splat[g, 1] - r3
             checked += 1
     assert checked > 50
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_every_fp32_hit_pixel_lies_in_an_emitted_tile(seed):
+    """Completeness against the hit test itself (the fp32 round-to-nearest quadratic,
+    emulated exactly), on huge and needle-like splats whose tips are ill-conditioned."""
+    rng = np.random.default_rng(100 + seed)
+    W, H, n = 300, 200, 60
+    sc, cam = ss.random_scene(rng, n, W, H, sh_degree=0, log_scale=(-1.0, 1.2), depth=(1.0, 4.0))
+    # a third of them needles: one long axis, two very short ones
+    k = n // 3
+    sc.scales[:k] = np.stack([rng.uniform(0.5, 3.0, k), np.full(k, 1e-3), np.full(k, 2e-3)],
+                             1).astype(np.float32)
+    p = oracle.project(sc, cam)
+    ntx, _ = oracle.n_tiles(cam)
+    ys, xs = np.mgrid[0:H, 0:W]
+    px = xs.astype(np.float32) + np.float32(0.5)
+    py = ys.astype(np.float32) + np.float32(0.5)
+    tile_of = (ys // 16) * ntx + xs // 16
+    checked = 0
+    for g in np.nonzero(p.visible)[0]:
+        r = p.splat[g]
+        dx = px - np.float32(r[0])
+        dy = py - np.float32(r[1])
+        q = D.quad_f32(r[13], r[14], r[15], dx, dy)
+        hit = q <= np.float32(r[6])
+        need = set(np.unique(tile_of[hit]).tolist())
+        have = set(oracle.splat_tiles(cam, r).tolist())
+        assert need <= have, (g, sorted(need - have)[:5])
+        checked += int(hit.sum())
+    assert checked > 100000
+
+
+def test_completeness_for_ground_splats_under_the_camera():
+    """Flat Gaussians on a ground plane just below and ahead of the camera project to
+    huge, thin ellipses centred far outside the image (the street workload has many);
+    every pixel their fp32 hit test accepts must lie in an emitted tile."""
+    rng = np.random.default_rng(7)
+    n, W, H = 400, 320, 240
+    means = np.stack([rng.uniform(-8, 8, n), np.full(n, 1.6), rng.uniform(0.21, 1.0, n)], 1)
+    scales = np.stack([np.exp(rng.normal(0.0, 1.0, n)), np.full(n, 2e-3),
+                       np.exp(rng.normal(0.0, 1.0, n))], 1)
+    ax = rng.normal(0, 0.05, (n, 3))  # nearly horizontal discs
+    quats = np.concatenate([np.ones((n, 1)), ax], 1)
+    quats /= np.linalg.norm(quats, axis=1, keepdims=True)
+    sc = ss.Scene(means.astype(np.float32), scales.astype(np.float32), quats.astype(np.float32),
+                  rng.uniform(0.05, 0.99, n).astype(np.float32), np.zeros((n, 1, 3), np.float32), 0)
+    cam = ss.pinhole(np.eye(4), 200.0, W, H)
+    p = oracle.project(sc, cam)
+    ntx, _ = oracle.n_tiles(cam)
+    ys, xs = np.mgrid[0:H, 0:W]
+    px = xs.astype(np.float32) + np.float32(0.5)
+    py = ys.astype(np.float32) + np.float32(0.5)
+    tile_of = (ys // 16) * ntx + xs // 16
+    far = thin = 0
+    for g in np.nonzero(p.visible)[0]:
+        r = p.splat[g]
+        P = np.array([[r[8], r[9]], [r[9], r[10]]])
+        ev = np.linalg.eigvalsh(P)
+        thin += ev[1] / ev[0] > 1e4
+        far += abs(r[0]) > 3 * W or abs(r[1]) > 3 * H
+        q = D.quad_f32(r[13], r[14], r[15], px - np.float32(r[0]), py - np.float32(r[1]))
+        need = set(np.unique(tile_of[q <= np.float32(r[6])]).tolist())
+        assert need <= set(oracle.splat_tiles(cam, r).tolist()), g
+    assert thin > 50 and far > 200, (thin, far)

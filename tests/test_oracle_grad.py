@@ -27,6 +27,14 @@ def _scene(seed, n=40, W=64, H=48, deg=3):
     return sc, cam, w, v
 
 
+def _refactor(proj, g):
+    """Cholesky factor of the (perturbed) conic a, b, c of splat g, in float64."""
+    a, b, c = proj.splat[g, 2:5]
+    l11 = np.sqrt(a)
+    l12 = b / l11
+    proj.splat[g, 13:16] = [l11, l12, np.sqrt(c - l12 * l12)]
+
+
 def _loss_from_records(cam, proj, b, w, v):
     im = oracle.blend(cam, proj, b, V64)
     return float((w * im.img).sum() + (v * im.T).sum()), im
@@ -56,6 +64,9 @@ def test_screen_space_gradients_match_finite_differences(seed):
                 h = 1e-5 * max(abs(x), 1e-3) if col in (2, 3, 4, 5) else 1e-5
                 p_hi.splat[g, col] = x + h
                 p_lo.splat[g, col] = x - h
+                if col in (2, 3, 4):  # the quadratic reads the conic through its factor
+                    for pp in (p_hi, p_lo):
+                        _refactor(pp, g)
             L1, i1 = _loss_from_records(cam, p_hi, b, w, v)
             L2, i2 = _loss_from_records(cam, p_lo, b, w, v)
             if not (np.array_equal(i1.n_contrib, im0.n_contrib) and
