@@ -110,23 +110,6 @@ __device__ __forceinline__ Projected project_chain(const CamParams& cam, float m
     R[6] = rmul(2.f, rsub(rmul(x, z), rmul(w, y)));
     R[7] = rmul(2.f, radd(rmul(y, z), rmul(w, x)));
     R[8] = rsub(1.f, rmul(2.f, radd(rmul(x, x), rmul(y, y))));
-    float M[9];
-#pragma unroll
-    for (int i = 0; i < 3; ++i) {
-        M[3 * i + 0] = rmul(R[3 * i + 0], s0);
-        M[3 * i + 1] = rmul(R[3 * i + 1], s1);
-        M[3 * i + 2] = rmul(R[3 * i + 2], s2);
-    }
-    float S[9];
-#pragma unroll
-    for (int i = 0; i < 3; ++i)
-#pragma unroll
-        for (int j = i; j < 3; ++j) {
-            float v = radd(radd(rmul(M[3 * i], M[3 * j]), rmul(M[3 * i + 1], M[3 * j + 1])),
-                           rmul(M[3 * i + 2], M[3 * j + 2]));
-            S[3 * i + j] = v;
-            S[3 * j + i] = v;
-        }
     float u = rdiv(tx, tz), v = rdiv(ty, tz);
     float mux = radd(rmul(cam.fx, u), cam.cx);
     float muy = radd(rmul(cam.fy, v), cam.cy);
@@ -138,16 +121,29 @@ __device__ __forceinline__ Projected project_chain(const CamParams& cam, float m
         T0[k] = radd(rmul(j00, V[k]), rmul(j02, V[8 + k]));
         T1[k] = radd(rmul(j11, V[4 + k]), rmul(j12, V[8 + k]));
     }
-    float U0[3], U1[3];
+    // Sigma' = N N^T with N = (T R) diag(s), T = J W (Eq. 1 with Sigma = R S S^T R^T)
+    const float sv[3] = {s0, s1, s2};
+    float n0[3], n1[3];
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
-        U0[k] = radd(radd(rmul(T0[0], S[k]), rmul(T0[1], S[3 + k])), rmul(T0[2], S[6 + k]));
-        U1[k] = radd(radd(rmul(T1[0], S[k]), rmul(T1[1], S[3 + k])), rmul(T1[2], S[6 + k]));
+        n0[k] = rmul(radd(radd(rmul(T0[0], R[k]), rmul(T0[1], R[3 + k])), rmul(T0[2], R[6 + k])), sv[k]);
+        n1[k] = rmul(radd(radd(rmul(T1[0], R[k]), rmul(T1[1], R[3 + k])), rmul(T1[2], R[6 + k])), sv[k]);
     }
-    float P00 = radd(radd(rmul(U0[0], T0[0]), rmul(U0[1], T0[1])), rmul(U0[2], T0[2]));
-    float P01 = radd(radd(rmul(U0[0], T1[0]), rmul(U0[1], T1[1])), rmul(U0[2], T1[2]));
-    float P11 = radd(radd(rmul(U1[0], T1[0]), rmul(U1[1], T1[1])), rmul(U1[2], T1[2]));
-    float det = rsub(rmul(P00, P11), rmul(P01, P01));
+    float P00 = radd(radd(rmul(n0[0], n0[0]), rmul(n0[1], n0[1])), rmul(n0[2], n0[2]));
+    float P01 = radd(radd(rmul(n0[0], n1[0]), rmul(n0[1], n1[1])), rmul(n0[2], n1[2]));
+    float P11 = radd(radd(rmul(n1[0], n1[0]), rmul(n1[1], n1[1])), rmul(n1[2], n1[2]));
+    // det Sigma' = |n0 x n1|^2 (Lagrange's identity) with n0 x n1 = s0 s1 s2 S^-1 R^T (T0 x T1):
+    // a sum of squares, free of the cancellation of P00 P11 - P01^2 for thin splats
+    float w0 = rsub(rmul(T0[1], T1[2]), rmul(T0[2], T1[1]));
+    float w1 = rsub(rmul(T0[2], T1[0]), rmul(T0[0], T1[2]));
+    float w2 = rsub(rmul(T0[0], T1[1]), rmul(T0[1], T1[0]));
+    float c0 = radd(radd(rmul(R[0], w0), rmul(R[3], w1)), rmul(R[6], w2));
+    float c1 = radd(radd(rmul(R[1], w0), rmul(R[4], w1)), rmul(R[7], w2));
+    float c2 = radd(radd(rmul(R[2], w0), rmul(R[5], w1)), rmul(R[8], w2));
+    float e0 = rmul(rmul(s1, s2), c0);
+    float e1 = rmul(rmul(s0, s2), c1);
+    float e2 = rmul(rmul(s0, s1), c2);
+    float det = radd(radd(rmul(e0, e0), rmul(e1, e1)), rmul(e2, e2));
     if (!(det > 0.f) || !(P00 > 0.f) || !(P11 > 0.f) || !isfinite(det)) return P;
     float a = rdiv(P11, det);
     float b = -rdiv(P01, det);
@@ -319,20 +315,6 @@ __global__ void __launch_bounds__(256) project_bwd_kernel(
     float R[9] = {1.f - 2.f * (y * y + z * z), 2.f * (x * y - w * z), 2.f * (x * z + w * y),
                   2.f * (x * y + w * z), 1.f - 2.f * (x * x + z * z), 2.f * (y * z - w * x),
                   2.f * (x * z - w * y), 2.f * (y * z + w * x), 1.f - 2.f * (x * x + y * y)};
-    float M[9];
-#pragma unroll
-    for (int r = 0; r < 3; ++r)
-#pragma unroll
-        for (int c = 0; c < 3; ++c) M[3 * r + c] = R[3 * r + c] * s[c];
-    float S[9];
-#pragma unroll
-    for (int r = 0; r < 3; ++r)
-#pragma unroll
-        for (int c = r; c < 3; ++c) {
-            float v = M[3 * r] * M[3 * c] + M[3 * r + 1] * M[3 * c + 1] + M[3 * r + 2] * M[3 * c + 2];
-            S[3 * r + c] = v;
-            S[3 * c + r] = v;
-        }
     float tz = t[2], iz = 1.f / tz;
     float u = t[0] * iz, v = t[1] * iz;
     float j00 = cam.fx * iz, j11 = cam.fy * iz, j02 = -j00 * u, j12 = -j11 * v;
@@ -342,48 +324,53 @@ __global__ void __launch_bounds__(256) project_bwd_kernel(
         T0[k] = j00 * V[k] + j02 * V[8 + k];
         T1[k] = j11 * V[4 + k] + j12 * V[8 + k];
     }
-    float ST0[3], ST1[3];
+    // Sigma' = N N^T, N = A diag(s), A = T R
+    float A0[3], A1[3], n0[3], n1[3];
 #pragma unroll
-    for (int r = 0; r < 3; ++r) {
-        ST0[r] = S[3 * r] * T0[0] + S[3 * r + 1] * T0[1] + S[3 * r + 2] * T0[2];
-        ST1[r] = S[3 * r] * T1[0] + S[3 * r + 1] * T1[1] + S[3 * r + 2] * T1[2];
+    for (int k = 0; k < 3; ++k) {
+        A0[k] = T0[0] * R[k] + T0[1] * R[3 + k] + T0[2] * R[6 + k];
+        A1[k] = T1[0] * R[k] + T1[1] * R[3 + k] + T1[2] * R[6 + k];
+        n0[k] = A0[k] * s[k];
+        n1[k] = A1[k] * s[k];
     }
-    float P00 = T0[0] * ST0[0] + T0[1] * ST0[1] + T0[2] * ST0[2];
-    float P01 = T0[0] * ST1[0] + T0[1] * ST1[1] + T0[2] * ST1[2];
-    float P11 = T1[0] * ST1[0] + T1[1] * ST1[1] + T1[2] * ST1[2];
-    float idet = 1.f / (P00 * P11 - P01 * P01);
-    float ca = P11 * idet, cb = -P01 * idet, cc = P00 * idet;
+    // nu = n0 x n1 = s0 s1 s2 S^-1 R^T (T0 x T1) and det Sigma' = |nu|^2 (see the forward)
+    float w0 = T0[1] * T1[2] - T0[2] * T1[1];
+    float w1 = T0[2] * T1[0] - T0[0] * T1[2];
+    float w2 = T0[0] * T1[1] - T0[1] * T1[0];
+    float nu[3] = {s[1] * s[2] * (R[0] * w0 + R[3] * w1 + R[6] * w2),
+                   s[0] * s[2] * (R[1] * w0 + R[4] * w1 + R[7] * w2),
+                   s[0] * s[1] * (R[2] * w0 + R[5] * w1 + R[8] * w2)};
+    float idet = 1.f / (nu[0] * nu[0] + nu[1] * nu[1] + nu[2] * nu[2]);
+    // dual basis of N's rows, M = Lambda N: m0 = (n1 x nu) / det, m1 = (nu x n0) / det;
+    // Lambda = M M^T.  Forming Lambda a_k through adj(Sigma') cancels for thin splats.
+    float m0[3] = {(n1[1] * nu[2] - n1[2] * nu[1]) * idet, (n1[2] * nu[0] - n1[0] * nu[2]) * idet,
+                   (n1[0] * nu[1] - n1[1] * nu[0]) * idet};
+    float m1[3] = {(nu[1] * n0[2] - nu[2] * n0[1]) * idet, (nu[2] * n0[0] - nu[0] * n0[2]) * idet,
+                   (nu[0] * n0[1] - nu[1] * n0[0]) * idet};
+    float L00 = m0[0] * m0[0] + m0[1] * m0[1] + m0[2] * m0[2];
+    float L01 = m0[0] * m1[0] + m0[1] * m1[1] + m0[2] * m1[2];
+    float L11 = m1[0] * m1[0] + m1[1] * m1[1] + m1[2] * m1[2];
 
-    // ---- conic -> Sigma': dSigma' = -Lambda G Lambda, G = [[ga, gb/2], [gb/2, gc]] ----
+    // ---- conic -> Sigma' = N N^T -> N: dL/dN = 2 dSigma' N = -2 Lambda G M,
+    //      G = [[ga, gb/2], [gb/2, gc]] ----
     float ga = g[2], gbh = 0.5f * g[3], gc = g[4];
-    float X00 = ca * ga + cb * gbh, X01 = ca * gbh + cb * gc;
-    float X10 = cb * ga + cc * gbh, X11 = cb * gbh + cc * gc;
-    float dP00 = -(X00 * ca + X01 * cb);
-    float dP01 = -2.f * (X00 * cb + X01 * cc);
-    float dP11 = -(X10 * cb + X11 * cc);
-
-    // ---- Sigma' = T Sigma T^T -> dT, dM ----
-    float dT0[3], dT1[3];
-#pragma unroll
-    for (int r = 0; r < 3; ++r) {
-        dT0[r] = 2.f * dP00 * ST0[r] + dP01 * ST1[r];
-        dT1[r] = dP01 * ST0[r] + 2.f * dP11 * ST1[r];
-    }
+    // ---- N = A diag(s) -> ds, dA; A = T R -> dT, dR ----
+    float dT0[3] = {0.f, 0.f, 0.f}, dT1[3] = {0.f, 0.f, 0.f};
     float ds[3], dR[9];
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
-        float a0 = T0[0] * M[k] + T0[1] * M[3 + k] + T0[2] * M[6 + k];
-        float a1 = T1[0] * M[k] + T1[1] * M[3 + k] + T1[2] * M[6 + k];
-        float c0 = 2.f * dP00 * a0 + dP01 * a1;
-        float c1 = dP01 * a0 + 2.f * dP11 * a1;
-        float acc = 0.f;
+        const float gm0 = ga * m0[k] + gbh * m1[k];
+        const float gm1 = gbh * m0[k] + gc * m1[k];
+        const float dn0 = -2.f * (L00 * gm0 + L01 * gm1);
+        const float dn1 = -2.f * (L01 * gm0 + L11 * gm1);
+        ds[k] = dn0 * A0[k] + dn1 * A1[k];
+        const float dA0 = dn0 * s[k], dA1 = dn1 * s[k];
 #pragma unroll
         for (int r = 0; r < 3; ++r) {
-            float dMrk = T0[r] * c0 + T1[r] * c1;
-            acc += dMrk * R[3 * r + k];
-            dR[3 * r + k] = dMrk * s[k];
+            dT0[r] += R[3 * r + k] * dA0;
+            dT1[r] += R[3 * r + k] * dA1;
+            dR[3 * r + k] = T0[r] * dA0 + T1[r] * dA1;
         }
-        ds[k] = acc;
     }
 
     // ---- T = J W -> dJ; (mu', J) -> dt -> dm ----

@@ -95,6 +95,8 @@ def _declare(lib: C.CDLL) -> None:
     lib.ora_blend_bwd.argtypes = [_I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
     lib.ora_project_bwd.argtypes = [_I64, _I32, _P, _P, _I32, _I32, C.c_float,
                                     _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+    lib.ora_project_bwd_mag.argtypes = [_I64, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                        _P, _P]
     lib.ora_policy.argtypes = [_I64, _P, _I64, C.c_double, C.c_double, C.c_double, _I64, _P, _P]
     lib.ora_policy.restype = C.c_double
 
@@ -276,18 +278,22 @@ class ParamGrads:
 
 
 def project_bwd_magnitude(scene, cam, proj: Projection, gmag: np.ndarray) -> ParamGrads:
-    """|J| gmag: the magnitudes of the 9 screen-space sums carried to the 59 parameter
-    gradients through the absolute value of the (linear) chain rule J, column by column."""
+    """Magnitudes of the 59 parameter gradients: the chain rule of project_bwd evaluated
+    stage by stage on absolute values, from the magnitudes gmag [N, 9] of grad2d (a
+    running error bound: a floating-point evaluation errs by a small multiple of u
+    times these)."""
+    lib = _lib("f32")
     n = int(scene.means.shape[0])
-    out = None
-    for c in range(9):
-        e = np.zeros((n, 9))
-        e[:, c] = 1.0
-        J = project_bwd(scene, cam, proj, e)
-        part = [np.abs(getattr(J, k)) * (gmag[:, c].reshape((-1,) + (1,) * (getattr(J, k).ndim - 1)))
-                for k in ("means", "scales", "quats", "opacities", "sh")]
-        out = part if out is None else [o + p for o, p in zip(out, part)]
-    return ParamGrads(*out)
+    K = (int(scene.sh_degree) + 1) ** 2
+    vm, intr, W, H, zn = _cam_args(cam)
+    out = ParamGrads(np.zeros((n, 3)), np.zeros((n, 3)), np.zeros((n, 4)), np.zeros(n),
+                     np.zeros((n, K, 3)))
+    gm = np.ascontiguousarray(np.abs(gmag), dtype=np.float64)
+    lib.ora_project_bwd_mag(n, int(scene.sh_degree), _p(vm), _p(intr), _p(_f32(scene.means)),
+                            _p(_f32(scene.scales)), _p(_f32(scene.quats)), _p(_f32(scene.sh)),
+                            _p(proj.tiles_touched), _p(gm), _p(out.means), _p(out.scales),
+                            _p(out.quats), _p(out.opacities), _p(out.sh))
+    return out
 
 
 def project_bwd(scene, cam, proj: Projection, grad2d: np.ndarray, variant: str = "f32") -> ParamGrads:

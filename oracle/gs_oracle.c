@@ -140,22 +140,7 @@ static void project_one(const camera_t* cam, const float* m3, const float* s3, c
     R[7] = 2 * (y * z + w * x);
     R[8] = 1 - 2 * (x * x + y * y);
 
-    /* M = R diag(s);  Sigma = M M^T */
     dreal s0 = s3[0], s1 = s3[1], s2 = s3[2];
-    dreal M[9];
-    for (int i = 0; i < 3; ++i) {
-        M[3 * i + 0] = R[3 * i + 0] * s0;
-        M[3 * i + 1] = R[3 * i + 1] * s1;
-        M[3 * i + 2] = R[3 * i + 2] * s2;
-    }
-    dreal S[9];
-    for (int i = 0; i < 3; ++i)
-        for (int j = i; j < 3; ++j) {
-            dreal v = (M[3 * i + 0] * M[3 * j + 0] + M[3 * i + 1] * M[3 * j + 1]) +
-                      M[3 * i + 2] * M[3 * j + 2];
-            S[3 * i + j] = v;
-            S[3 * j + i] = v;
-        }
 
     /* pinhole projection and its Jacobian J evaluated at t */
     dreal u = tx / tz, v = ty / tz;
@@ -172,17 +157,28 @@ static void project_one(const camera_t* cam, const float* m3, const float* s3, c
         T0[k] = j00 * V[k] + j02 * V[8 + k];
         T1[k] = j11 * V[4 + k] + j12 * V[8 + k];
     }
-    /* U = T Sigma */
-    dreal U0[3], U1[3];
+    /* Sigma' = J W R S S R^T W^T J^T = N N^T with N = (T R) diag(s):
+     * n_ik = (T_i . R_col_k) s_k (Eq. 1 with Sigma = R S S^T R^T) */
+    dreal n0[3], n1[3];
     for (int k = 0; k < 3; ++k) {
-        U0[k] = (T0[0] * S[0 + k] + T0[1] * S[3 + k]) + T0[2] * S[6 + k];
-        U1[k] = (T1[0] * S[0 + k] + T1[1] * S[3 + k]) + T1[2] * S[6 + k];
+        n0[k] = ((T0[0] * R[k] + T0[1] * R[3 + k]) + T0[2] * R[6 + k]) * s3[k];
+        n1[k] = ((T1[0] * R[k] + T1[1] * R[3 + k]) + T1[2] * R[6 + k]) * s3[k];
     }
-    /* Sigma' = U T^T (Eq. 1) */
-    dreal P00 = (U0[0] * T0[0] + U0[1] * T0[1]) + U0[2] * T0[2];
-    dreal P01 = (U0[0] * T1[0] + U0[1] * T1[1]) + U0[2] * T1[2];
-    dreal P11 = (U1[0] * T1[0] + U1[1] * T1[1]) + U1[2] * T1[2];
-    dreal det = P00 * P11 - P01 * P01;
+    dreal P00 = (n0[0] * n0[0] + n0[1] * n0[1]) + n0[2] * n0[2];
+    dreal P01 = (n0[0] * n1[0] + n0[1] * n1[1]) + n0[2] * n1[2];
+    dreal P11 = (n1[0] * n1[0] + n1[1] * n1[1]) + n1[2] * n1[2];
+    /* det Sigma' = |n0 x n1|^2 (Lagrange) and n0 x n1 = s0 s1 s2 S^-1 R^T (T0 x T1):
+     * a sum of squares, free of the cancellation of P00 P11 - P01^2 */
+    dreal w0 = T0[1] * T1[2] - T0[2] * T1[1];
+    dreal w1 = T0[2] * T1[0] - T0[0] * T1[2];
+    dreal w2 = T0[0] * T1[1] - T0[1] * T1[0];
+    dreal c0 = (R[0] * w0 + R[3] * w1) + R[6] * w2;
+    dreal c1 = (R[1] * w0 + R[4] * w1) + R[7] * w2;
+    dreal c2 = (R[2] * w0 + R[5] * w1) + R[8] * w2;
+    dreal e0 = (s1 * s2) * c0;
+    dreal e1 = (s0 * s2) * c1;
+    dreal e2 = (s0 * s1) * c2;
+    dreal det = (e0 * e0 + e1 * e1) + e2 * e2;
     if (!(det > 0) || !(P00 > 0) || !(P11 > 0) || !finite_d(det)) return;
     dreal a = P11 / det;
     dreal b = -(P01 / det);
@@ -977,6 +973,163 @@ void ora_project_bwd(int64_t n, int sh_degree, const float* viewmat, const float
         }
         double dotd = dhat[0] * gd[0] + dhat[1] * gd[1] + dhat[2] * gd[2];
         for (int j = 0; j < 3; ++j) dm[j] += (gd[j] - dhat[j] * dotd) / len;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Exported: magnitudes of the projection backward (running error bound)     */
+/* ------------------------------------------------------------------------ */
+/*
+ * The chain rule of ora_project_bwd evaluated on magnitudes: every input
+ * gradient replaced by gmag[n][9] (>= |grad2d|), every factor by its absolute
+ * value and every sum or difference by the sum of its terms' magnitudes,
+ * stage by stage.  A floating-point evaluation of the chain has an error
+ * bounded by a small multiple of u times these values (u the unit roundoff).
+ */
+void ora_project_bwd_mag(int64_t n, int sh_degree, const float* viewmat, const float* intr,
+                         const float* means, const float* scales, const float* quats,
+                         const float* sh, const int32_t* tiles_touched, const double* gmag,
+                         double* mmeans, double* mscales, double* mquats, double* mopac,
+                         double* msh) {
+    int K = (sh_degree + 1) * (sh_degree + 1);
+    double V[12], aV[12];
+    for (int i = 0; i < 12; ++i) {
+        V[i] = viewmat[i];
+        aV[i] = fabs(V[i]);
+    }
+    double fx = intr[0], fy = intr[1];
+    double cw[3];
+    camera_centre(viewmat, cw);
+    for (int64_t i = 0; i < n; ++i) {
+        double* dm = mmeans + 3 * i;
+        double* ds = mscales + 3 * i;
+        double* dq = mquats + 4 * i;
+        double* dshi = msh + (int64_t)K * 3 * i;
+        dm[0] = dm[1] = dm[2] = 0;
+        ds[0] = ds[1] = ds[2] = 0;
+        dq[0] = dq[1] = dq[2] = dq[3] = 0;
+        mopac[i] = 0;
+        for (int k = 0; k < 3 * K; ++k) dshi[k] = 0;
+        if (tiles_touched[i] <= 0) continue;
+        const double* g2 = gmag + 9 * i;
+        double m[3] = {means[3 * i], means[3 * i + 1], means[3 * i + 2]};
+        double t[3];
+        for (int r = 0; r < 3; ++r)
+            t[r] = V[4 * r] * m[0] + V[4 * r + 1] * m[1] + V[4 * r + 2] * m[2] + V[4 * r + 3];
+        double qr[4] = {quats[4 * i], quats[4 * i + 1], quats[4 * i + 2], quats[4 * i + 3]};
+        double qn = sqrt(qr[0] * qr[0] + qr[1] * qr[1] + qr[2] * qr[2] + qr[3] * qr[3]);
+        double w = qr[0] / qn, x = qr[1] / qn, y = qr[2] / qn, z = qr[3] / qn;
+        double R[9] = {1 - 2 * (y * y + z * z), 2 * (x * y - w * z),     2 * (x * z + w * y),
+                       2 * (x * y + w * z),     1 - 2 * (x * x + z * z), 2 * (y * z - w * x),
+                       2 * (x * z - w * y),     2 * (y * z + w * x),     1 - 2 * (x * x + y * y)};
+        double s[3] = {scales[3 * i], scales[3 * i + 1], scales[3 * i + 2]};
+        double M[9], S[9], aM[9], aS[9];
+        for (int r = 0; r < 3; ++r)
+            for (int c = 0; c < 3; ++c) {
+                M[3 * r + c] = R[3 * r + c] * s[c];
+                aM[3 * r + c] = fabs(M[3 * r + c]);
+            }
+        for (int r = 0; r < 3; ++r)
+            for (int c = 0; c < 3; ++c) {
+                S[3 * r + c] = M[3 * r] * M[3 * c] + M[3 * r + 1] * M[3 * c + 1] +
+                               M[3 * r + 2] * M[3 * c + 2];
+                aS[3 * r + c] = aM[3 * r] * aM[3 * c] + aM[3 * r + 1] * aM[3 * c + 1] +
+                                aM[3 * r + 2] * aM[3 * c + 2];
+            }
+        double tx = t[0], ty = t[1], tz = t[2];
+        double j00 = fx / tz, j11 = fy / tz;
+        double j02 = -fx * tx / (tz * tz), j12 = -fy * ty / (tz * tz);
+        double Tm[2][3], aT[2][3];
+        for (int k = 0; k < 3; ++k) {
+            Tm[0][k] = j00 * V[k] + j02 * V[8 + k];
+            Tm[1][k] = j11 * V[4 + k] + j12 * V[8 + k];
+            aT[0][k] = fabs(j00) * aV[k] + fabs(j02) * aV[8 + k];
+            aT[1][k] = fabs(j11) * aV[4 + k] + fabs(j12) * aV[8 + k];
+        }
+        double P[2][2];
+        for (int a_ = 0; a_ < 2; ++a_)
+            for (int b_ = 0; b_ < 2; ++b_) {
+                double acc = 0;
+                for (int r = 0; r < 3; ++r)
+                    for (int c = 0; c < 3; ++c) acc += Tm[a_][r] * S[3 * r + c] * Tm[b_][c];
+                P[a_][b_] = acc;
+            }
+        double P00 = P[0][0], P01 = P[0][1], P11 = P[1][1];
+        double det = P00 * P11 - P01 * P01, det2 = det * det;
+        double aP01 = fabs(P01);
+        /* conic -> Sigma' */
+        double ga = g2[2], gb = g2[3], gc = g2[4];
+        double dP00 = ga * P11 * P11 / det2 + gb * aP01 * P11 / det2 + gc * (1.0 / det + P00 * P11 / det2);
+        double dP11 = ga * (1.0 / det + P11 * P00 / det2) + gb * aP01 * P00 / det2 + gc * P00 * P00 / det2;
+        double dP01 = ga * 2.0 * aP01 * P11 / det2 + gb * (1.0 / det + 2.0 * P01 * P01 / det2) +
+                      gc * 2.0 * P00 * aP01 / det2;
+        double dS[9], dT[2][3];
+        for (int r = 0; r < 3; ++r)
+            for (int c = 0; c < 3; ++c)
+                dS[3 * r + c] = dP00 * aT[0][r] * aT[0][c] + dP01 * aT[0][r] * aT[1][c] +
+                                dP11 * aT[1][r] * aT[1][c];
+        for (int r = 0; r < 3; ++r) {
+            double ST0 = aS[3 * r] * aT[0][0] + aS[3 * r + 1] * aT[0][1] + aS[3 * r + 2] * aT[0][2];
+            double ST1 = aS[3 * r] * aT[1][0] + aS[3 * r + 1] * aT[1][1] + aS[3 * r + 2] * aT[1][2];
+            dT[0][r] = 2.0 * dP00 * ST0 + dP01 * ST1;
+            dT[1][r] = dP01 * ST0 + 2.0 * dP11 * ST1;
+        }
+        double dj00 = 0, dj02 = 0, dj11 = 0, dj12 = 0;
+        for (int k = 0; k < 3; ++k) {
+            dj00 += dT[0][k] * aV[k];
+            dj02 += dT[0][k] * aV[8 + k];
+            dj11 += dT[1][k] * aV[4 + k];
+            dj12 += dT[1][k] * aV[8 + k];
+        }
+        double gmx = g2[0], gmy = g2[1];
+        double atx = fabs(tx), aty = fabs(ty);
+        double tz2 = tz * tz, tz3 = tz2 * tz;
+        double dt[3];
+        dt[0] = gmx * fabs(fx) / tz + dj02 * fabs(fx) / tz2;
+        dt[1] = gmy * fabs(fy) / tz + dj12 * fabs(fy) / tz2;
+        dt[2] = gmx * fabs(fx) * atx / tz2 + gmy * fabs(fy) * aty / tz2 + dj00 * fabs(fx) / tz2 +
+                dj02 * 2.0 * fabs(fx) * atx / tz3 + dj11 * fabs(fy) / tz2 +
+                dj12 * 2.0 * fabs(fy) * aty / tz3;
+        for (int c = 0; c < 3; ++c) dm[c] += aV[c] * dt[0] + aV[4 + c] * dt[1] + aV[8 + c] * dt[2];
+        double dM[9], dR[9];
+        for (int r = 0; r < 3; ++r)
+            for (int k = 0; k < 3; ++k) {
+                double acc = 0;
+                for (int j = 0; j < 3; ++j) acc += (dS[3 * r + j] + dS[3 * j + r]) * aM[3 * j + k];
+                dM[3 * r + k] = acc;
+            }
+        for (int r = 0; r < 3; ++r)
+            for (int k = 0; k < 3; ++k) {
+                ds[k] += dM[3 * r + k] * fabs(R[3 * r + k]);
+                dR[3 * r + k] = dM[3 * r + k] * fabs(s[k]);
+            }
+        double aw = fabs(w), ax = fabs(x), ay = fabs(y), az = fabs(z);
+        double dw = 2 * (az * dR[1] + ay * dR[2] + az * dR[3] + ax * dR[5] + ay * dR[6] + ax * dR[7]);
+        double dx = 2 * (ay * dR[1] + az * dR[2] + ay * dR[3] + 2 * ax * dR[4] + aw * dR[5] +
+                         az * dR[6] + aw * dR[7] + 2 * ax * dR[8]);
+        double dy = 2 * (2 * ay * dR[0] + ax * dR[1] + aw * dR[2] + ax * dR[3] + az * dR[5] +
+                         aw * dR[6] + az * dR[7] + 2 * ay * dR[8]);
+        double dz = 2 * (2 * az * dR[0] + aw * dR[1] + ax * dR[2] + aw * dR[3] + 2 * az * dR[4] +
+                         ay * dR[5] + ax * dR[6] + ay * dR[7]);
+        double qh[4] = {aw, ax, ay, az}, dqh[4] = {dw, dx, dy, dz};
+        double dotq = qh[0] * dqh[0] + qh[1] * dqh[1] + qh[2] * dqh[2] + qh[3] * dqh[3];
+        for (int k = 0; k < 4; ++k) dq[k] = (dqh[k] + qh[k] * dotq) / qn;
+        mopac[i] = g2[5];
+        double dhat[3], len, Y[16], dY[16][3];
+        view_dir(means + 3 * i, cw, dhat, &len);
+        sh_basis(dhat, Y, dY);
+        double gd[3] = {0, 0, 0};
+        for (int k = 0; k < K; ++k) {
+            double proj = 0;
+            for (int ch = 0; ch < 3; ++ch) {
+                dshi[3 * k + ch] = fabs(Y[k]) * g2[6 + ch];
+                proj += g2[6 + ch] * fabs((double)sh[(i * K + k) * 3 + ch]);
+            }
+            for (int j = 0; j < 3; ++j) gd[j] += proj * fabs(dY[k][j]);
+        }
+        double ad[3] = {fabs(dhat[0]), fabs(dhat[1]), fabs(dhat[2])};
+        double dotd = ad[0] * gd[0] + ad[1] * gd[1] + ad[2] * gd[2];
+        for (int j = 0; j < 3; ++j) dm[j] += (gd[j] + ad[j] * dotd) / len;
     }
 }
 

@@ -121,3 +121,13 @@ def test_parameter_gradients_match_finite_differences(seed):
                 assert abs(an - fd) <= 1e-6 + 1e-4 * abs(fd), (name, g, j, an, fd)
                 checked += 1
     assert checked >= 300
+
+
+def test_parameter_gradient_magnitudes_bound_the_gradients():
+    """The running-error magnitudes of the chain rule dominate |gradient| (the triangle
+    inequality applied stage by stage)."""
+    sc, cam, w, v = _scene(3, n=30)
+    L0, r0, g2, pg = oracle.loss_and_grads(sc, cam, w, v)
+    mag = oracle.project_bwd_magnitude(sc, cam, r0.proj, np.abs(g2))
+    for k in ("means", "scales", "quats", "opacities", "sh"):
+        assert np.all(getattr(mag, k) >= np.abs(getattr(pg, k)) * (1 - 1e-9) - 1e-15), k
