@@ -111,13 +111,13 @@ def _declare(lib: C.CDLL) -> None:
     lib.gs_bin_sort.argtypes = [C.POINTER(Camera), _I64, _P, _P, _P, _P, C.c_size_t, _P, _I64,
                                 _P, _P, _P, _P, _P]
     lib.gs_raster_workspace_bytes.restype = C.c_size_t
-    lib.gs_raster_workspace_bytes.argtypes = [C.c_int32, C.c_int32, C.POINTER(Settings)]
+    lib.gs_raster_workspace_bytes.argtypes = [C.c_int32, C.c_int32, _I64, C.POINTER(Settings)]
     lib.gs_rasterize_fwd.restype = st
-    lib.gs_rasterize_fwd.argtypes = [C.POINTER(Camera), C.POINTER(Settings), _I64, _P, _P, _P,
-                                     _P, _P, C.c_size_t, _P, _P, _P, _P, _P]
+    lib.gs_rasterize_fwd.argtypes = [C.POINTER(Camera), C.POINTER(Settings), _I64, _P, _P, _I64,
+                                     _P, _P, _P, C.c_size_t, _P, _P, _P, _P, _P]
     lib.gs_rasterize_bwd.restype = st
-    lib.gs_rasterize_bwd.argtypes = [C.POINTER(Camera), C.POINTER(Settings), _I64, _P, _P, _P,
-                                     _P, _P, C.c_size_t, _P, _P, _P, _P, _P, _P, _P]
+    lib.gs_rasterize_bwd.argtypes = [C.POINTER(Camera), C.POINTER(Settings), _I64, _P, _P, _I64,
+                                     _P, _P, _P, C.c_size_t, _P, _P, _P, _P, _P, _P, _P]
     lib.gs_project_bwd.restype = st
     lib.gs_project_bwd.argtypes = [C.POINTER(Camera), _I64, C.c_int32] + [_P] * 13 + [_P]
     lib.gs_raster_stats.restype = st
@@ -224,13 +224,14 @@ def gs_bin_sort(cam, n, splats, depths, tiles_touched, workspace, sorted_ids, ca
     return int(host.value) if sync_pairs else None
 
 
-def gs_raster_workspace_bytes(width, height, settings=None) -> int:
-    return int(library().gs_raster_workspace_bytes(int(width), int(height),
+def gs_raster_workspace_bytes(width, height, capacity, settings=None) -> int:
+    return int(library().gs_raster_workspace_bytes(int(width), int(height), int(capacity),
                                                    C.byref(_settings(settings))))
 
 
 def gs_rasterize_fwd(cam, n, splats, sorted_ids, tile_ranges, lpt_order, workspace, image,
                      t_final, n_contrib, last_idx, settings=None, stream=None):
+    """Forward blend (see gs.h); the pair capacity is sorted_ids' length."""
     import torch
 
     cam_c = Camera.of(cam)
@@ -238,7 +239,8 @@ def gs_rasterize_fwd(cam, n, splats, sorted_ids, tile_ranges, lpt_order, workspa
     st = library().gs_rasterize_fwd(
         C.byref(cam_c), C.byref(_settings(settings)), int(n),
         _ptr(splats, "splats", _f32(), SPLAT_FLOATS * n, optional=n == 0),
-        _ptr(sorted_ids, "sorted_ids", _i32()), _ptr(tile_ranges, "tile_ranges", _i32()),
+        _ptr(sorted_ids, "sorted_ids", _i32()), sorted_ids.numel(),
+        _ptr(tile_ranges, "tile_ranges", _i32()),
         _ptr(lpt_order, "lpt_order", _i32()), _ptr(workspace, "workspace", torch.uint8),
         workspace.numel(), _ptr(image, "image", _f32(), 3 * P), _ptr(t_final, "t_final", _f32(), P),
         _ptr(n_contrib, "n_contrib", _i32(), P), _ptr(last_idx, "last_idx", _i32(), P),
@@ -256,7 +258,8 @@ def gs_rasterize_bwd(cam, n, splats, sorted_ids, tile_ranges, lpt_order, workspa
     st = library().gs_rasterize_bwd(
         C.byref(cam_c), C.byref(_settings(settings)), int(n),
         _ptr(splats, "splats", _f32(), SPLAT_FLOATS * n, optional=n == 0),
-        _ptr(sorted_ids, "sorted_ids", _i32()), _ptr(tile_ranges, "tile_ranges", _i32()),
+        _ptr(sorted_ids, "sorted_ids", _i32()), sorted_ids.numel(),
+        _ptr(tile_ranges, "tile_ranges", _i32()),
         _ptr(lpt_order, "lpt_order", _i32()), _ptr(workspace, "workspace", torch.uint8),
         workspace.numel(), _ptr(t_final, "t_final", _f32(), P),
         _ptr(last_idx, "last_idx", _i32(), P), _ptr(dL_dimage, "dL_dimage", _f32(), 3 * P),
@@ -337,8 +340,6 @@ class Rasterizer:
         self.last_idx = torch.empty((H, W), dtype=i, device=dev)
         self.grad2d = torch.empty((self.n, GRAD2D), dtype=f, device=dev)
         self.touched = torch.empty(self.n, dtype=torch.uint8, device=dev)
-        self.raster_ws = torch.empty(gs_raster_workspace_bytes(W, H, self.settings),
-                                     dtype=torch.uint8, device=dev)
         self._alloc_pairs(capacity if capacity else max(4 * self.n, 1 << 16))
         self.n_pairs = None
         self._inputs = None
@@ -351,6 +352,9 @@ class Rasterizer:
         self.bin_ws = torch.empty(gs_bin_sort_workspace_bytes(self.n, self.capacity, self.cam.width,
                                                               self.cam.height),
                                   dtype=torch.uint8, device=self.device)
+        self.raster_ws = torch.empty(gs_raster_workspace_bytes(self.cam.width, self.cam.height,
+                                                               self.capacity, self.settings),
+                                     dtype=torch.uint8, device=self.device)
 
     def forward(self, means, scales, quats, opacities, sh, sync_pairs: bool = True):
         n = self.n

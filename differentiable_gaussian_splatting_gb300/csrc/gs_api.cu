@@ -183,25 +183,28 @@ gs_status gs_bin_sort(const gs_camera* cam, int64_t n, const float* splats, cons
     return GS_OK;
 }
 
-size_t gs_raster_workspace_bytes(int32_t width, int32_t height, const gs_settings* settings) {
+size_t gs_raster_workspace_bytes(int32_t width, int32_t height, int64_t capacity,
+                                 const gs_settings* settings) {
     gs_settings s = settings ? *settings : gs_default_settings();
-    if (width < 1 || height < 1 || !settings_ok(&s)) return 0;
-    return raster_layout(width, height, s.h_max).total;
+    if (width < 1 || height < 1 || capacity < 1 || capacity > kMaxIds || !settings_ok(&s)) return 0;
+    return raster_layout(width, height, s.h_max, capacity).total;
 }
 
 gs_status gs_rasterize_fwd(const gs_camera* cam, const gs_settings* settings, int64_t n,
-                           const float* splats, const int32_t* sorted_ids,
+                           const float* splats, const int32_t* sorted_ids, int64_t capacity,
                            const int32_t* tile_ranges, const int32_t* lpt_order, void* workspace,
                            size_t workspace_bytes, float* image, float* t_final,
                            int32_t* n_contrib, int32_t* last_idx, void* stream) {
     gs_settings s = settings ? *settings : gs_default_settings();
-    if (!camera_ok(cam) || !settings_ok(&s) || n < 0 || n > kMaxIds) return GS_ERR_INVALID_ARG;
+    if (!camera_ok(cam) || !settings_ok(&s) || n < 0 || n > kMaxIds || capacity < 1 ||
+        capacity > kMaxIds)
+        return GS_ERR_INVALID_ARG;
     const void* ptrs[] = {sorted_ids, tile_ranges, lpt_order, workspace, image, t_final,
                           n_contrib, last_idx};
     for (const void* p : ptrs)
         if (!p || !aligned16(p)) return GS_ERR_INVALID_ARG;
     if (n > 0 && (!splats || !aligned16(splats))) return GS_ERR_INVALID_ARG;
-    const RasterLayout L = raster_layout(cam->width, cam->height, s.h_max);
+    const RasterLayout L = raster_layout(cam->width, cam->height, s.h_max, capacity);
     if (workspace_bytes < L.total) return GS_ERR_WORKSPACE;
     return cuda_status(run_raster_fwd(cam_params(cam), raster_config(&s), splats, sorted_ids,
                                       tile_ranges, lpt_order, static_cast<char*>(workspace), L,
@@ -209,13 +212,15 @@ gs_status gs_rasterize_fwd(const gs_camera* cam, const gs_settings* settings, in
 }
 
 gs_status gs_rasterize_bwd(const gs_camera* cam, const gs_settings* settings, int64_t n,
-                           const float* splats, const int32_t* sorted_ids,
+                           const float* splats, const int32_t* sorted_ids, int64_t capacity,
                            const int32_t* tile_ranges, const int32_t* lpt_order, void* workspace,
                            size_t workspace_bytes, const float* t_final, const int32_t* last_idx,
                            const float* dL_dimage, const float* dL_dt_final, float* grad2d,
                            uint8_t* touched, void* stream) {
     gs_settings s = settings ? *settings : gs_default_settings();
-    if (!camera_ok(cam) || !settings_ok(&s) || n < 0 || n > kMaxIds) return GS_ERR_INVALID_ARG;
+    if (!camera_ok(cam) || !settings_ok(&s) || n < 0 || n > kMaxIds || capacity < 1 ||
+        capacity > kMaxIds)
+        return GS_ERR_INVALID_ARG;
     const void* ptrs[] = {sorted_ids, tile_ranges, lpt_order, workspace, t_final, last_idx,
                           dL_dimage};
     for (const void* p : ptrs)
@@ -223,7 +228,7 @@ gs_status gs_rasterize_bwd(const gs_camera* cam, const gs_settings* settings, in
     if (n > 0 && (!splats || !aligned16(splats) || !grad2d || !aligned16(grad2d)))
         return GS_ERR_INVALID_ARG;
     if (dL_dt_final && !aligned16(dL_dt_final)) return GS_ERR_INVALID_ARG;
-    const RasterLayout L = raster_layout(cam->width, cam->height, s.h_max);
+    const RasterLayout L = raster_layout(cam->width, cam->height, s.h_max, capacity);
     if (workspace_bytes < L.total) return GS_ERR_WORKSPACE;
     return cuda_status(run_raster_bwd(cam_params(cam), raster_config(&s), n, splats, sorted_ids,
                                       tile_ranges, lpt_order, static_cast<char*>(workspace), L,

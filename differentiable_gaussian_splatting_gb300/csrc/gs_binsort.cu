@@ -83,17 +83,35 @@ __global__ void __launch_bounds__(kRsBlock) rs_upsweep(const uint32_t* __restric
     const int64_t nblk = nblk_of(n);
     const int64_t b = blockIdx.x;
     if (b >= nblk) return;
-    __shared__ uint32_t cnt[256];
-    cnt[threadIdx.x] = 0;
+    __shared__ uint32_t cnt[kRsWarps][256];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int w = 0; w < kRsWarps; ++w) cnt[w][tid] = 0;
     __syncthreads();
-    const int64_t base = b * kRsTile;
-#pragma unroll 4
-    for (int i = threadIdx.x; i < kRsTile; i += kRsBlock) {
-        int64_t idx = base + i;
-        if (idx < n) atomicAdd(&cnt[(__ldg(keys + idx) >> shift) & 255u], 1u);
+    // each warp counts its own contiguous 512 keys; equal digits of a round are
+    // aggregated with __match_any_sync (one shared-memory add per distinct digit),
+    // so near-constant high key bytes do not serialise on one counter
+    const int64_t wbase = b * kRsTile + (int64_t)warp * (32 * kRsIpt);
+    uint32_t k[kRsIpt];
+#pragma unroll
+    for (int r = 0; r < kRsIpt; ++r) {
+        const int64_t idx = wbase + r * 32 + lane;
+        k[r] = idx < n ? __ldg(keys + idx) : 0u;
+    }
+#pragma unroll
+    for (int r = 0; r < kRsIpt; ++r) {
+        const int64_t idx = wbase + r * 32 + lane;
+        const bool valid = idx < n;
+        const uint32_t d = (k[r] >> shift) & 255u;
+        const uint32_t peers = __match_any_sync(0xffffffffu, valid ? d : 256u + lane);
+        if (valid && (peers & lanemask_lt()) == 0) cnt[warp][d] += __popc(peers);
+        __syncwarp();
     }
     __syncthreads();
-    hist[(int64_t)threadIdx.x * nblk + b] = cnt[threadIdx.x];
+    uint32_t tot = 0;
+#pragma unroll
+    for (int w = 0; w < kRsWarps; ++w) tot += cnt[w][tid];
+    hist[(int64_t)tid * nblk + b] = tot;
 }
 
 // one block per digit: exclusive scan of the digit's row of block counts
@@ -146,12 +164,18 @@ __global__ void __launch_bounds__(kRsBlock) rs_downsweep(
     uint32_t k[kRsIpt];
     int32_t v[kRsIpt];
     uint32_t loc[kRsIpt];
+    // issue every load of the warp's 512 keys before ranking them
 #pragma unroll
     for (int r = 0; r < kRsIpt; ++r) {
         const int64_t idx = wbase + r * 32 + lane;
         const bool valid = idx < n;
         k[r] = valid ? __ldg(keys_in + idx) : 0u;
         v[r] = valid ? __ldg(vals_in + idx) : 0;
+    }
+#pragma unroll
+    for (int r = 0; r < kRsIpt; ++r) {
+        const int64_t idx = wbase + r * 32 + lane;
+        const bool valid = idx < n;
         const uint32_t d = (k[r] >> shift) & 255u;
         const uint32_t peers = __match_any_sync(0xffffffffu, valid ? d : 256u + lane);
         const uint32_t rank = __popc(peers & lanemask_lt());
@@ -280,25 +304,33 @@ __global__ void __launch_bounds__(kRsBlock) vis_count(const int32_t* __restrict_
     if (threadIdx.x == 0) bsum[blockIdx.x] = total;
 }
 
-// visible Gaussians, in id order: (depth key, id)
+// visible Gaussians, in id order: (depth key, id).  Blocked: each thread owns 16
+// consecutive items, so one block-wide scan of per-thread counts suffices.
 __global__ void __launch_bounds__(kRsBlock) vis_write(const int32_t* __restrict__ tiles_touched,
                                                       const float* __restrict__ depths, int64_t n,
                                                       const int64_t* __restrict__ bsum,
                                                       uint32_t* __restrict__ keys,
                                                       int32_t* __restrict__ vals) {
     __shared__ int64_t s_warp[kRsWarps];
-    const int64_t base = (int64_t)blockIdx.x * kRsTile;
-    int64_t run = bsum[blockIdx.x];
+    const int64_t base = (int64_t)blockIdx.x * kRsTile + (int64_t)threadIdx.x * kRsIpt;
+    bool vis[kRsIpt];
+    int64_t c = 0;
+#pragma unroll
     for (int r = 0; r < kRsIpt; ++r) {
-        const int64_t idx = base + (int64_t)r * kRsBlock + threadIdx.x;
-        const bool vis = idx < n && tiles_touched[idx] > 0;
-        int64_t total;
-        int64_t off = block_exclusive_scan_256<int64_t>(vis ? 1 : 0, s_warp, &total);
-        if (vis) {
-            keys[run + off] = __float_as_uint(depths[idx]);  // depth > znear > 0: bits are ordered
-            vals[run + off] = (int32_t)idx;
+        const int64_t idx = base + r;
+        vis[r] = idx < n && tiles_touched[idx] > 0;
+        c += vis[r];
+    }
+    int64_t total;
+    int64_t pos = bsum[blockIdx.x] + block_exclusive_scan_256<int64_t>(c, s_warp, &total);
+#pragma unroll
+    for (int r = 0; r < kRsIpt; ++r) {
+        if (vis[r]) {
+            const int64_t idx = base + r;
+            keys[pos] = __float_as_uint(depths[idx]);  // depth > znear > 0: bits are ordered
+            vals[pos] = (int32_t)idx;
+            ++pos;
         }
-        run += total;
     }
 }
 
@@ -330,43 +362,106 @@ __global__ void __launch_bounds__(kRsBlock) pairs_offsets(const int32_t* __restr
     const int64_t m = *m_dev;
     if ((int64_t)blockIdx.x >= nblk_of(m)) return;
     __shared__ int64_t s_warp[kRsWarps];
-    const int64_t base = (int64_t)blockIdx.x * kRsTile;
-    int64_t run = bsum[blockIdx.x];
+    const int64_t base = (int64_t)blockIdx.x * kRsTile + (int64_t)threadIdx.x * kRsIpt;
+    int32_t c[kRsIpt];
+    int64_t sum = 0;
+#pragma unroll
     for (int r = 0; r < kRsIpt; ++r) {
-        const int64_t j = base + (int64_t)r * kRsBlock + threadIdx.x;
-        const int64_t c = j < m ? (int64_t)tiles_touched[order[j]] : 0;
-        int64_t total;
-        int64_t off = block_exclusive_scan_256<int64_t>(c, s_warp, &total);
-        if (j < m) poff[j] = run + off;
-        run += total;
+        const int64_t j = base + r;
+        c[r] = j < m ? tiles_touched[order[j]] : 0;
+        sum += c[r];
+    }
+    int64_t total;
+    int64_t pos = bsum[blockIdx.x] + block_exclusive_scan_256<int64_t>(sum, s_warp, &total);
+#pragma unroll
+    for (int r = 0; r < kRsIpt; ++r) {
+        const int64_t j = base + r;
+        if (j < m) poff[j] = pos;
+        pos += c[r];
     }
 }
 
-// emit (tile, Gaussian) pairs in depth order from the exact row spans
+// emit (tile, Gaussian) pairs in depth order from the exact row spans.  A warp
+// takes 32 consecutive splats; small ones are emitted by their own lane, large
+// ones (> kEmitLane tiles) by the whole warp, one tile row per lane.
+constexpr int kEmitLane = 16;
+
 __global__ void __launch_bounds__(256) emit_pairs(CamParams cam, const float4* __restrict__ splats,
                                                   const int32_t* __restrict__ order,
+                                                  const int32_t* __restrict__ tiles_touched,
                                                   const int64_t* __restrict__ poff,
                                                   const int64_t* __restrict__ m_dev,
                                                   int64_t capacity, uint32_t* __restrict__ pkeys,
                                                   int32_t* __restrict__ pvals) {
     const int64_t m = *m_dev;
-    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < m;
-         j += (int64_t)gridDim.x * blockDim.x) {
-        const int32_t g = order[j];
-        int64_t off = poff[j];
-        const float4 r0 = __ldg(splats + 3 * (int64_t)g), r1 = __ldg(splats + 3 * (int64_t)g + 1),
-                     r2 = __ldg(splats + 3 * (int64_t)g + 2);
-        const Ellipse e = ellipse_of(r0, r1, r2);
-        int ty0, ty1, tx0, tx1;
-        row_range(e, cam.nty, &ty0, &ty1);
-        for (int ty = ty0; ty < ty1; ++ty) {
-            if (!row_span(e, ty, cam.W, cam.H, cam.ntx, &tx0, &tx1)) continue;
-            const uint32_t rowkey = (uint32_t)ty * (uint32_t)cam.ntx;
-            for (int tx = tx0; tx < tx1; ++tx, ++off) {
-                if (off < capacity) {
-                    pkeys[off] = rowkey + (uint32_t)tx;
-                    pvals[off] = g;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t base = warp0 * 32; base < m; base += nwarps * 32) {
+        const int64_t j = base + lane;
+        const bool valid = j < m;
+        int32_t g = 0;
+        int64_t off = 0;
+        Ellipse e{};
+        int ty0 = 0, ty1 = 0;
+        bool big = false;
+        if (valid) {
+            g = order[j];
+            off = poff[j];
+            const float4 r0 = __ldg(splats + 3 * (int64_t)g), r1 = __ldg(splats + 3 * (int64_t)g + 1),
+                         r2 = __ldg(splats + 3 * (int64_t)g + 2);
+            e = ellipse_of(r0, r1, r2);
+            row_range(e, cam.nty, &ty0, &ty1);
+            big = tiles_touched[g] > kEmitLane;
+            if (!big) {
+                int tx0, tx1;
+                for (int ty = ty0; ty < ty1; ++ty) {
+                    if (!row_span(e, ty, cam.W, cam.H, cam.ntx, &tx0, &tx1)) continue;
+                    const uint32_t rowkey = (uint32_t)ty * (uint32_t)cam.ntx;
+                    for (int tx = tx0; tx < tx1; ++tx, ++off)
+                        if (off < capacity) {
+                            pkeys[off] = rowkey + (uint32_t)tx;
+                            pvals[off] = g;
+                        }
                 }
+            }
+        }
+        uint32_t todo = __ballot_sync(0xffffffffu, big);
+        while (todo) {
+            const int src = __ffs(todo) - 1;
+            todo &= todo - 1;
+            const unsigned F = 0xffffffffu;
+            Ellipse eb;
+            eb.mux = __shfl_sync(F, e.mux, src);
+            eb.muy = __shfl_sync(F, e.muy, src);
+            eb.l11 = __shfl_sync(F, e.l11, src);
+            eb.l12 = __shfl_sync(F, e.l12, src);
+            eb.l22 = __shfl_sync(F, e.l22, src);
+            eb.tau = __shfl_sync(F, e.tau, src);
+            eb.rx = __shfl_sync(F, e.rx, src);
+            eb.ry = __shfl_sync(F, e.ry, src);
+            const int32_t gb = __shfl_sync(F, g, src);
+            const int b0 = __shfl_sync(F, ty0, src), b1 = __shfl_sync(F, ty1, src);
+            int64_t ob = __shfl_sync(F, off, src);
+            for (int rb = b0; rb < b1; rb += 32) {
+                const int ty = rb + lane;
+                int tx0 = 0, tx1 = 0;
+                const bool has = ty < b1 && row_span(eb, ty, cam.W, cam.H, cam.ntx, &tx0, &tx1);
+                const int cnt = has ? tx1 - tx0 : 0;
+                int incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(F, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                int64_t o2 = ob + (incl - cnt);
+                const uint32_t rowkey = (uint32_t)ty * (uint32_t)cam.ntx;
+                for (int tx = tx0; tx < tx1; ++tx, ++o2)
+                    if (o2 < capacity) {
+                        pkeys[o2] = rowkey + (uint32_t)tx;
+                        pvals[o2] = gb;
+                    }
+                ob += __shfl_sync(F, incl, 31);
             }
         }
     }
@@ -426,14 +521,70 @@ __global__ void __launch_bounds__(kScanThreads) fill_empty_ranges(int2* __restri
     }
 }
 
-// LPT keys: descending pair count = ascending (maxk - count); stable -> ties by tile id
-__global__ void lpt_keys_kernel(const int2* __restrict__ ranges, int64_t nt, uint32_t maxk,
-                                uint32_t* __restrict__ keys, int32_t* __restrict__ vals) {
-    int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= nt) return;
-    int2 r = ranges[t];
-    keys[t] = maxk - (uint32_t)(r.y - r.x);
-    vals[t] = (int32_t)t;
+// LPT order ("Mitigating SM-Level Load Imbalance in 3D Gaussian Splatting on
+// GPUs", Sec. 4.1): tiles by descending pair count, ties by ascending tile id,
+// i.e. ascending unique 64-bit keys ((2^32 - 1 - count) << 32 | tile).  Runs of
+// 1024 keys are sorted in shared memory (bitonic), then every key's rank is its
+// position in its run plus, in every other run, the number of smaller keys.
+constexpr int kLptRun = 1024;
+
+__global__ void __launch_bounds__(kLptRun / 2) lpt_sort_runs(const int2* __restrict__ ranges,
+                                                            int64_t nt, uint64_t* __restrict__ runs) {
+    __shared__ uint64_t sk[kLptRun];
+    const int tid = threadIdx.x;
+    const int64_t base = (int64_t)blockIdx.x * kLptRun;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i = tid + h * (kLptRun / 2);
+        const int64_t t = base + i;
+        uint64_t key = ~0ull;
+        if (t < nt) {
+            const int2 r = ranges[t];
+            key = ((uint64_t)(0xffffffffu - (uint32_t)(r.y - r.x)) << 32) | (uint64_t)t;
+        }
+        sk[i] = key;
+    }
+    __syncthreads();
+    for (int size = 2; size <= kLptRun; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const int i = 2 * tid - (tid & (stride - 1));  // lower index of this thread's pair
+            const int jx = i + stride;
+            const bool up = (i & size) == 0;
+            const uint64_t a = sk[i], b = sk[jx];
+            if ((a > b) == up) {
+                sk[i] = b;
+                sk[jx] = a;
+            }
+            __syncthreads();
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i = tid + h * (kLptRun / 2);
+        runs[base + i] = sk[i];
+    }
+}
+
+__global__ void lpt_merge(const uint64_t* __restrict__ runs, int64_t nt, int32_t* __restrict__ lpt) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nruns = (nt + kLptRun - 1) / kLptRun;
+    if (i >= nruns * kLptRun) return;
+    const uint64_t key = runs[i];
+    if (key == ~0ull) return;  // padding
+    const int64_t r = i / kLptRun;
+    int64_t rank = i - r * kLptRun;
+    for (int64_t r2 = 0; r2 < nruns; ++r2) {
+        if (r2 == r) continue;
+        const uint64_t* run = runs + r2 * kLptRun;
+        int lo = 0, hi = kLptRun;  // number of keys < key
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (run[mid] < key) lo = mid + 1;
+            else hi = mid;
+        }
+        rank += lo;
+    }
+    lpt[rank] = (int32_t)(key & 0xffffffffu);
 }
 
 size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
@@ -470,10 +621,7 @@ BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles) {
     L.off_pvals1 = take((size_t)cap * 4);
     L.off_hist = take((size_t)256 * hist_blocks * 4);
     L.off_dtot = take(256 * 4);
-    L.off_lkeys0 = take((size_t)nt * 4);
-    L.off_lkeys1 = take((size_t)nt * 4);
-    L.off_lvals0 = take((size_t)nt * 4);
-    L.off_lvals1 = take((size_t)nt * 4);
+    L.off_lruns = take((size_t)((nt + kLptRun - 1) / kLptRun) * kLptRun * sizeof(uint64_t));
     L.total = off;
     return L;
 }
@@ -495,10 +643,7 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
     auto* pv1 = reinterpret_cast<int32_t*>(ws + L.off_pvals1);
     auto* hist = reinterpret_cast<uint32_t*>(ws + L.off_hist);
     auto* dtot = reinterpret_cast<uint32_t*>(ws + L.off_dtot);
-    auto* lk0 = reinterpret_cast<uint32_t*>(ws + L.off_lkeys0);
-    auto* lk1 = reinterpret_cast<uint32_t*>(ws + L.off_lkeys1);
-    auto* lv0 = reinterpret_cast<int32_t*>(ws + L.off_lvals0);
-    auto* lv1 = reinterpret_cast<int32_t*>(ws + L.off_lvals1);
+    auto* lruns = reinterpret_cast<uint64_t*>(ws + L.off_lruns);
     const int64_t nt = (int64_t)cam.ntx * cam.nty;
     cudaError_t err;
 
@@ -526,8 +671,8 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
         pairs_offsets<<<nb, kRsBlock, 0, st>>>(dvs, tiles_touched, counts + 0, bsum, poff);
         // 4. emit pairs in depth order
         const unsigned eg = (unsigned)std::min<int64_t>((n + 255) / 256, 65535);
-        emit_pairs<<<eg, 256, 0, st>>>(cam, reinterpret_cast<const float4*>(splats), dvs, poff,
-                                       counts + 0, capacity, pk0, pv0);
+        emit_pairs<<<eg, 256, 0, st>>>(cam, reinterpret_cast<const float4*>(splats), dvs,
+                                       tiles_touched, poff, counts + 0, capacity, pk0, pv0);
         // 5. stable sort by tile key; values land in sorted_ids
         uint32_t* pks = nullptr;
         err = radix_sort(pk0, pv0, pk1, pv1, sorted_ids, counts + 2, 0, capacity,
@@ -539,13 +684,11 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
     }
     // 7. LPT order: tiles by descending count, ties by tile id
     {
-        const int bits = bits_for(std::max<int64_t>(capacity, 1));
-        const uint32_t maxk = bits >= 32 ? 0xffffffffu : ((1u << bits) - 1u);
-        lpt_keys_kernel<<<(unsigned)((nt + 255) / 256), 256, 0, st>>>(
-            reinterpret_cast<const int2*>(tile_ranges), nt, maxk, lk0, lv0);
-        err = radix_sort(lk0, lv0, lk1, lv1, lpt_order, nullptr, nt, nt, bits, hist, dtot, st,
-                         nullptr, nullptr);
-        if (err != cudaSuccess) return err;
+        const unsigned nruns = (unsigned)((nt + kLptRun - 1) / kLptRun);
+        lpt_sort_runs<<<nruns, kLptRun / 2, 0, st>>>(reinterpret_cast<const int2*>(tile_ranges), nt,
+                                                     lruns);
+        lpt_merge<<<(unsigned)((nruns * (int64_t)kLptRun + 255) / 256), 256, 0, st>>>(lruns, nt,
+                                                                                   lpt_order);
     }
     return cudaGetLastError();
 }

@@ -150,24 +150,48 @@ __device__ __forceinline__ float quad_q(float l11, float l12, float l22, float d
 
 // ---------------------------------------------------------------------------
 // 8x4 sub-tile mask ("What the 3DGS Literature Left on the Table", Step 1 (c)):
-// bit w set iff the padded support meets the pixel-centre hull of the 8x4
+// bit w set if the padded support meets the pixel-centre hull of the 8x4
 // sub-tile of warp w (warp w covers columns 8 (w & 1) .. +7, rows 4 (w >> 1) .. +3
-// of the tile).  Conservative: every hit pixel of a warp has its bit set.
+// of the tile).  It only has to be conservative (every hit pixel of a warp has
+// its bit set), so it uses the SFU's approximate square root and reciprocal:
+// their few-ulp errors are far inside the 2^-8 r pad.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ float sqrt_approx(float x) {
+    float y;
+    asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t subtile_mask(const Ellipse& s, int tx, int ty, int W, int H) {
-    uint32_t m = 0;
+    const float inv_l11 = rcp_approx(s.l11);
+    const float h = sqrt_approx(fmaf(s.l12, s.l12, s.l22 * s.l22));
+    const float dyv = -(sqrt_approx(s.tau) * s.l12) * rcp_approx(s.l22 * h);
+    const float padx = fmaf(s.rx, kPadScale, kPadUnit);
+    const float ryp = s.ry + fmaf(s.ry, kPadScale, kPadUnit);
     const float xb = (float)(16 * tx);
-    const float xl0 = radd(xb, 0.5f), xl1 = radd(xb, 7.5f);
-    const float xr0 = radd(xb, 8.5f);
-    const float xr1 = smin(radd(xb, 15.5f), rsub((float)W, 0.5f));
-    const float ylim = rsub((float)H, 0.5f);
+    const float xl0 = xb + 0.5f, xl1 = xb + 7.5f;
+    const float xr0 = xb + 8.5f;
+    const float xr1 = fminf(xb + 15.5f, (float)W - 0.5f);
+    const float ylim = (float)H - 0.5f;
+    uint32_t m = 0;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        float y0 = radd((float)(16 * ty + 4 * r), 0.5f);
+        const float y0 = (float)(16 * ty + 4 * r) + 0.5f;
         if (y0 > ylim) break;
-        float y1 = smin(radd(y0, 3.0f), ylim);
-        float Xlo, Xhi;
-        if (!band_extent(s, y0, y1, &Xlo, &Xhi)) continue;
+        const float y1 = fminf(y0 + 3.f, ylim);
+        const float lo = fmaxf(y0 - s.muy, -ryp), hi = fminf(y1 - s.muy, ryp);
+        if (!(lo <= hi)) continue;
+        const float dh = fminf(fmaxf(fminf(fmaxf(dyv, lo), hi), -s.ry), s.ry);
+        const float dl = fminf(fmaxf(fminf(fmaxf(dyv, -hi), -lo), -s.ry), s.ry);
+        const float th = s.l22 * dh, tl = s.l22 * dl;
+        const float xh = (sqrt_approx(fmaxf(fmaf(-th, th, s.tau), 0.f)) - s.l12 * dh) * inv_l11;
+        const float xl = (sqrt_approx(fmaxf(fmaf(-tl, tl, s.tau), 0.f)) - s.l12 * dl) * inv_l11;
+        const float Xhi = s.mux + xh + padx, Xlo = s.mux - xl - padx;
         if (Xhi >= xl0 && Xlo <= xl1) m |= 1u << (2 * r);
         if (xr0 <= xr1 && Xhi >= xr0 && Xlo <= xr1) m |= 1u << (2 * r + 1);
     }

@@ -39,7 +39,7 @@ struct BinSortLayout {
     size_t off_pkeys0, off_pkeys1, off_pvals0, off_pvals1;  // [capacity]
     size_t off_hist;     // uint32[256 * nblk_max]
     size_t off_dtot;     // uint32[256] digit totals
-    size_t off_lkeys0, off_lkeys1, off_lvals0, off_lvals1;  // [n_tiles]
+    size_t off_lruns;    // uint64[n_tiles rounded up to 1024]: sorted runs of LPT keys
 };
 BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles);
 
@@ -62,8 +62,9 @@ struct RasterLayout {
     size_t off_part_c;   // float4[h_max][16][256]: chunk partial (C.rgb, T)
     size_t off_part_n;   // int2[h_max][16][256]: chunk partial (n, last)
     size_t off_bwd;      // float4[h_max][16][256]: (T after chunk, colour behind chunk)
+    size_t off_cmask;    // uint8[capacity]: warps that blended each pair
 };
-RasterLayout raster_layout(int W, int H, int h_max);
+RasterLayout raster_layout(int W, int H, int h_max, int64_t capacity);
 
 // control word indices
 enum : int {

@@ -55,6 +55,7 @@ struct RasterArgs {
     float4* part_c;
     int2* part_n;
     float4* bstate;
+    uint8_t* cmask;  // per pair: warps that blended it (forward writes, backward reads)
     // forward outputs
     float* image;
     float* t_final;
@@ -124,6 +125,7 @@ struct Smem {
     float4 r2[kBatch];
     int32_t gid[kBatch];
     uint8_t mask[kBatch];
+    uint32_t cm[8 * (kBatch / 32)];  // [warp][32-splat chunk] blended bits
     int item;
     int flag;
 };
@@ -131,9 +133,12 @@ struct Smem {
 // Front-to-back blend of list positions [s, e) for the calling thread's pixel.
 // All threads of the CTA must call it.  When sat_slot >= 0 the chunk stops
 // early once sat[sat_slot] < chunk (an earlier chunk saturated the tile).
-// Returns true if it stopped on that signal.
-__device__ bool blend_range(const RasterArgs& A, Smem& S, int tx, int ty, float px, float py,
-                            int64_t s, int64_t e, PixelState& st, int sat_slot, int chunk) {
+// With write_cmask, every position's 8-bit mask of the warps that blended it
+// is stored in A.cmask ("What the 3DGS Literature Left on the Table", Step 4.2).
+// Returns true if it stopped on the saturation signal.
+__device__ __forceinline__ bool blend_range(const RasterArgs& A, Smem& S, int tx, int ty, float px, float py,
+                            int64_t s, int64_t e, PixelState& st, int sat_slot, int chunk,
+                            bool write_cmask) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int64_t bs = s; bs < e; bs += kBatch) {
         if (tid == 0)
@@ -142,6 +147,7 @@ __device__ bool blend_range(const RasterArgs& A, Smem& S, int tx, int ty, float 
         if (!live) return false;
         if (S.flag) return true;
         const int64_t j = bs + tid;
+        if (tid < 8 * (kBatch / 32)) S.cm[tid] = 0u;
         if (j < e) {
             const int32_t g = __ldg(A.ids + j);
             const float4 r0 = __ldg(A.splats + 3 * (int64_t)g);
@@ -161,6 +167,7 @@ __device__ bool blend_range(const RasterArgs& A, Smem& S, int tx, int ty, float 
             const int jj = c + lane;
             const uint32_t bit = jj < nb ? (S.mask[jj] >> warp) & 1u : 0u;
             uint32_t work = __ballot_sync(0xffffffffu, bit);
+            uint32_t blended = 0u;  // this lane's blended splats of the chunk
             while (work) {
                 const int q = __ffs(work) - 1;
                 work &= work - 1;
@@ -180,11 +187,22 @@ __device__ bool blend_range(const RasterArgs& A, Smem& S, int tx, int ty, float 
                 if (hit) {
                     st.n += 1;
                     st.last = (int)(bs + idx);
+                    blended |= 1u << q;
                 }
                 st.done = st.done || (st.T < kTMin);
             }
+            if (write_cmask) {
+                blended = __reduce_or_sync(0xffffffffu, blended);
+                if (lane == 0) S.cm[warp * (kBatch / 32) + (c >> 5)] = blended;
+            }
         }
         __syncthreads();
+        if (write_cmask && j < e) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) m |= ((S.cm[w * (kBatch / 32) + (tid >> 5)] >> lane) & 1u) << w;
+            A.cmask[j] = (uint8_t)m;
+        }
     }
     return false;
 }
@@ -216,9 +234,13 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
         const int2 r = ranges[lpt[j]];
         return (double)(r.y - r.x);
     };
+    // Eq. 6 multiplied by K > 0 (same minimiser, no division), in round-to-nearest
+    // double with no contraction: K T(h, k) = max(N_total + lambda h k, K l) + beta K l,
+    // l = max(N_1 / k, N_{h+1}) (exact: k is a power of two)
     const double N1 = count_at(0);
-    const double lam = cfg.lambda, beta = cfg.beta;
-    const double base = fmax(tot / (double)K, N1) + beta * N1;
+    const double lam = cfg.lambda, beta = cfg.beta, Kd = (double)K;
+    const double KN1 = __dmul_rn(Kd, N1);
+    const double base = __dadd_rn(fmax(tot, KN1), __dmul_rn(beta, KN1));
     int bh = 0, bk = 1;
     if (cfg.split_mode == 2) {
         bh = min(min(cfg.force_h, cfg.h_max), nt);
@@ -232,7 +254,9 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
             const int h = 1 + cand / 4;
             const int k = ks[cand % 4];
             const double l = fmax(N1 / (double)k, count_at(h));
-            const double cost = fmax((tot + lam * (double)h * (double)k) / (double)K, l) + beta * l;
+            const double Kl = __dmul_rn(Kd, l);
+            const double work = __dadd_rn(tot, __dmul_rn(__dmul_rn(lam, (double)h), (double)k));
+            const double cost = __dadd_rn(fmax(work, Kl), __dmul_rn(beta, Kl));
             // lexicographic (cost, h, k): candidates are visited in increasing (h, k)
             if (cost < best) {
                 best = cost;
@@ -270,7 +294,7 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
                     k_best = s_k[w];
                 }
             }
-            if (h_best > 0 && !(best <= (1.0 - (double)cfg.eps) * base)) {
+            if (h_best > 0 && !(best <= __dmul_rn(__dsub_rn(1.0, (double)cfg.eps), base))) {
                 h_best = 0;
                 k_best = 1;
             }
@@ -299,7 +323,7 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
 // ---------------------------------------------------------------------------
 // forward: persistent kernel over whole tiles and depth chunks
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) raster_fwd_kernel(RasterArgs A) {
+__global__ void __launch_bounds__(kThreads, 4) raster_fwd_kernel(RasterArgs A) {
     __shared__ Smem S;
     const int tid = threadIdx.x;
     const int h = A.ctrl[kCtlH], k = A.ctrl[kCtlK], nitems = A.ctrl[kCtlItems];
@@ -318,7 +342,7 @@ __global__ void __launch_bounds__(kThreads) raster_fwd_kernel(RasterArgs A) {
         const float px = (float)x + 0.5f, py = (float)y + 0.5f;
         PixelState st{1.f, 0.f, 0.f, 0.f, 0, -1, !inside};
         if (it.slot < 0) {
-            blend_range(A, S, tx, ty, px, py, it.s, it.e, st, -1, 0);
+            blend_range(A, S, tx, ty, px, py, it.s, it.e, st, -1, 0, true);
             if (inside) {
                 const int64_t p = (int64_t)y * A.W + x;
                 A.image[3 * p] = st.cr;
@@ -331,7 +355,7 @@ __global__ void __launch_bounds__(kThreads) raster_fwd_kernel(RasterArgs A) {
             continue;
         }
         // ---- a depth chunk of a split tile: blend from T = 1 ----
-        blend_range(A, S, tx, ty, px, py, it.s, it.e, st, it.slot, it.chunk);
+        blend_range(A, S, tx, ty, px, py, it.s, it.e, st, it.slot, it.chunk, true);
         const int64_t pidx = ((int64_t)it.slot * kMaxChunks + it.chunk) * kThreads + tid;
         A.part_c[pidx] = make_float4(st.cr, st.cg, st.cb, st.T);
         A.part_n[pidx] = make_int2(st.n, st.last);
@@ -374,7 +398,7 @@ __global__ void __launch_bounds__(kThreads) raster_fwd_kernel(RasterArgs A) {
                 PixelState rs = acc;
                 rs.done = !replay;
                 blend_range(A, S, tx, ty, px, py, chunk_lo(rr.x, len, p, it.k),
-                            chunk_lo(rr.x, len, p + 1, it.k), rs, -1, 0);
+                            chunk_lo(rr.x, len, p + 1, it.k), rs, -1, 0, false);
                 if (replay) {
                     acc = rs;
                     acc.done = rs.T < kTMin;
@@ -528,15 +552,16 @@ __global__ void __launch_bounds__(kThreads) raster_bwd_kernel(RasterArgs A) {
             const int64_t bs = max64(it.s, be - kBatch);
             const int nb = (int)(be - bs);
             if (tid < nb) {
-                const int32_t g = __ldg(A.ids + bs + tid);
-                const float4 r0 = __ldg(A.splats + 3 * (int64_t)g);
-                const float4 r1 = __ldg(A.splats + 3 * (int64_t)g + 1);
-                const float4 r2 = __ldg(A.splats + 3 * (int64_t)g + 2);
-                S.r0[tid] = r0;
-                S.r1[tid] = r1;
-                S.r2[tid] = r2;
-                S.gid[tid] = g;
-                S.mask[tid] = (uint8_t)subtile_mask(ellipse_of(r0, r1, r2), tx, ty, A.W, A.H);
+                // the forward's contributor mask: warps that blended this splat
+                const uint8_t cm = A.cmask[bs + tid];
+                S.mask[tid] = cm;
+                if (cm) {
+                    const int32_t g = __ldg(A.ids + bs + tid);
+                    S.r0[tid] = __ldg(A.splats + 3 * (int64_t)g);
+                    S.r1[tid] = __ldg(A.splats + 3 * (int64_t)g + 1);
+                    S.r2[tid] = __ldg(A.splats + 3 * (int64_t)g + 2);
+                    S.gid[tid] = g;
+                }
             }
             __syncthreads();
             for (int c = ((nb - 1) >> 5) << 5; c >= 0; c -= 32) {
@@ -617,7 +642,7 @@ static int resident_bwd(int device) {
     return g_resident[device][1];
 }
 
-RasterLayout raster_layout(int W, int H, int h_max) {
+RasterLayout raster_layout(int W, int H, int h_max, int64_t capacity) {
     (void)W;
     (void)H;
     RasterLayout L{};
@@ -635,6 +660,7 @@ RasterLayout raster_layout(int W, int H, int h_max) {
     L.off_part_c = take(px * sizeof(float4));
     L.off_part_n = take(px * sizeof(int2));
     L.off_bwd = take(px * sizeof(float4));
+    L.off_cmask = take((size_t)max64(capacity, 1));
     L.total = off;
     return L;
 }
@@ -657,6 +683,7 @@ static RasterArgs make_args(const CamParams& cam, const float* splats, const int
     A.part_c = reinterpret_cast<float4*>(ws + L.off_part_c);
     A.part_n = reinterpret_cast<int2*>(ws + L.off_part_n);
     A.bstate = reinterpret_cast<float4*>(ws + L.off_bwd);
+    A.cmask = reinterpret_cast<uint8_t*>(ws + L.off_cmask);
     return A;
 }
 

@@ -167,9 +167,10 @@ gs_status gs_bin_sort(const gs_camera* cam, int64_t n, const float* splats, cons
                       int32_t* lpt_order, int64_t* counts_device, int64_t* n_pairs_host,
                       void* stream);
 
-/* Workspace bytes the two rasterize calls share for an image size and the
- * given settings (NULL = defaults). */
-size_t gs_raster_workspace_bytes(int32_t width, int32_t height, const gs_settings* settings);
+/* Workspace bytes the two rasterize calls share for an image size, the pair
+ * list capacity given to gs_bin_sort and the settings (NULL = defaults). */
+size_t gs_raster_workspace_bytes(int32_t width, int32_t height, int64_t capacity,
+                                 const gs_settings* settings);
 
 /*
  * gs_rasterize_fwd -- [RY] Eq. 2-5, Sec. 4.1-4.4; [K] Step 1 (c), Step 5, 6.
@@ -184,15 +185,20 @@ size_t gs_raster_workspace_bytes(int32_t width, int32_t height, const gs_setting
  * the result is the sequential one).
  *
  *   settings        NULL = gs_default_settings()
+ *   sorted_ids, capacity, tile_ranges, lpt_order   as given to / returned by
+ *                   gs_bin_sort
  *   workspace       >= gs_raster_workspace_bytes(...); it carries state to
  *                   gs_rasterize_bwd and must not change between the calls
+ *                   (split-tile state, and for every pair an 8-bit mask of the
+ *                   warps that blended it: the backward skips the rest,
+ *                   [K] Step 4.2)
  * Outputs:
  *   image [H][W][3], t_final [H][W] (final transmittance; no background),
  *   n_contrib [H][W] (blended splats), last_idx [H][W] (position in
  *   sorted_ids of the last blended splat, -1 if none)
  */
 gs_status gs_rasterize_fwd(const gs_camera* cam, const gs_settings* settings, int64_t n,
-                           const float* splats, const int32_t* sorted_ids,
+                           const float* splats, const int32_t* sorted_ids, int64_t capacity,
                            const int32_t* tile_ranges, const int32_t* lpt_order, void* workspace,
                            size_t workspace_bytes, float* image, float* t_final,
                            int32_t* n_contrib, int32_t* last_idx, void* stream);
@@ -220,7 +226,7 @@ gs_status gs_rasterize_fwd(const gs_camera* cam, const gs_settings* settings, in
  *   touched [n]     1 where a splat received a gradient (optional)
  */
 gs_status gs_rasterize_bwd(const gs_camera* cam, const gs_settings* settings, int64_t n,
-                           const float* splats, const int32_t* sorted_ids,
+                           const float* splats, const int32_t* sorted_ids, int64_t capacity,
                            const int32_t* tile_ranges, const int32_t* lpt_order, void* workspace,
                            size_t workspace_bytes, const float* t_final, const int32_t* last_idx,
                            const float* dL_dimage, const float* dL_dt_final, float* grad2d,

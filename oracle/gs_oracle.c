@@ -1143,16 +1143,19 @@ void ora_project_bwd_mag(int64_t n, int sh_degree, const float* viewmat, const f
  *   l(h, k) = max(N_1 / k, N_{h+1})  (l(0, k) = N_1; N_{nt+1} = 0)
  *   T(h, k) = max((N_total + lambda h k) / K, l) + beta l
  * The minimiser (lowest T; ties to the smaller h, then the smaller k) is
- * taken only if T <= (1 - eps) T(0); otherwise h = 0 (no chunking).
+ * taken only if T <= (1 - eps) T(0); otherwise h = 0 (no chunking).  The
+ * comparisons are made on K T (the same order, no division).
  * Writes (h*, k*) and returns T(h*, k*).
  */
 double ora_policy(int64_t nt, const int64_t* counts_desc, int64_t K, double lambda, double beta,
                   double eps, int64_t h_max, int64_t* h_out, int64_t* k_out) {
+    /* Eq. 6 multiplied by K > 0 (same minimiser, no division):
+     * K T(h, k) = max(N_total + lambda h k, K l) + beta K l;  l = max(N_1 / k, N_{h+1}) */
     double total = 0;
     for (int64_t t = 0; t < nt; ++t) total += (double)counts_desc[t];
+    double Kd = (double)K;
     double N1 = nt > 0 ? (double)counts_desc[0] : 0.0;
-    double base_l = N1;
-    double base = fmax(total / (double)K, base_l) + beta * base_l;
+    double base = fmax(total, Kd * N1) + beta * (Kd * N1);
     double best = base;
     int64_t bh = 0, bk = 1;
     int64_t hm = nt < h_max ? nt : h_max;
@@ -1162,7 +1165,8 @@ double ora_policy(int64_t nt, const int64_t* counts_desc, int64_t K, double lamb
             double k = ks[ki];
             double next = h < nt ? (double)counts_desc[h] : 0.0;
             double l = fmax(N1 / k, next);
-            double cost = fmax((total + lambda * (double)h * k) / (double)K, l) + beta * l;
+            double Kl = Kd * l;
+            double cost = fmax(total + lambda * (double)h * k, Kl) + beta * Kl;
             if (cost < best) {
                 best = cost;
                 bh = h;
@@ -1176,5 +1180,5 @@ double ora_policy(int64_t nt, const int64_t* counts_desc, int64_t K, double lamb
     }
     *h_out = bh;
     *k_out = bk;
-    return best;
+    return best / Kd;
 }

@@ -55,9 +55,10 @@ def test_host_queries(lib):
     assert lib.gs_status_string(3) == b"pair list capacity exceeded"
     assert gs.gs_bin_sort_workspace_bytes(1000, 4000, 128, 128) > 4000 * 16
     assert gs.gs_bin_sort_workspace_bytes(-1, 10, 128, 128) == 0
-    assert gs.gs_raster_workspace_bytes(64, 64) > 0
+    assert gs.gs_raster_workspace_bytes(64, 64, 1000) > 1000
+    assert gs.gs_raster_workspace_bytes(64, 64, 0) == 0
     bad = gs.Settings(7, 0, 0, 256, 256.0, 0.05, 0.1)
-    assert lib.gs_raster_workspace_bytes(64, 64, C.byref(bad)) == 0
+    assert lib.gs_raster_workspace_bytes(64, 64, 1000, C.byref(bad)) == 0
 
 
 def _cam(**kw):
@@ -101,5 +102,5 @@ def test_invalid_sizes_and_pointers_are_rejected_on_the_host(lib):
                 gs.Settings(0, 0, 4, 0, 256.0, 0.05, 0.1),      # h_max < 1
                 gs.Settings(0, 0, 4, 256, -1.0, 0.05, 0.1),     # lambda < 0
                 gs.Settings(0, 0, 4, 256, 256.0, 0.05, 1.5)):   # eps >= 1
-        assert lib.gs_rasterize_fwd(C.byref(cam), C.byref(bad), 10, *([fake] * 5), 1 << 30,
-                                    *([fake] * 4), None) == 1
+        assert lib.gs_rasterize_fwd(C.byref(cam), C.byref(bad), 10, fake, fake, 100, fake,
+                                    fake, fake, 1 << 30, *([fake] * 4), None) == 1
