@@ -122,6 +122,9 @@ def _declare(lib: C.CDLL) -> None:
     lib.gs_project_bwd.argtypes = [C.POINTER(Camera), _I64, C.c_int32] + [_P] * 13 + [_P]
     lib.gs_raster_stats.restype = st
     lib.gs_raster_stats.argtypes = [_P, C.c_size_t, _P, _P]
+    lib.gs_bin_sort_noalloc.restype = st
+    lib.gs_bin_sort_noalloc.argtypes = [C.POINTER(Camera), _I64, _P, _P, _P, _P, _I64, _P, _P, _P,
+                                        _P, _P]
 
 
 # ---------------------------------------------------------------------------
@@ -221,6 +224,26 @@ def gs_bin_sort(cam, n, splats, depths, tiles_touched, workspace, sorted_ids, ca
         _ptr(counts_device, "counts_device", torch.int64, 2, optional=True),
         C.byref(host) if sync_pairs else None, _stream(stream))
     _check("gs_bin_sort", st, f"; pairs needed: {host.value}" if st == 3 else "")
+    return int(host.value) if sync_pairs else None
+
+
+def gs_bin_sort_noalloc(cam, n, splats, depths, tiles_touched, sorted_ids, capacity, tile_ranges,
+                        lpt_order, counts_device=None, sync_pairs=True, stream=None):
+    """gs_bin_sort on the library's fixed scratch (allocates nothing; see gs.h for its limits)."""
+    import torch
+
+    cam_c = Camera.of(cam)
+    nt = library().gs_num_tiles(cam_c.width, cam_c.height)
+    host = C.c_int64(-1)
+    st = library().gs_bin_sort_noalloc(
+        C.byref(cam_c), int(n), _ptr(splats, "splats", _f32(), SPLAT_FLOATS * n, optional=n == 0),
+        _ptr(depths, "depths", _f32(), n, optional=n == 0),
+        _ptr(tiles_touched, "tiles_touched", _i32(), n, optional=n == 0),
+        _ptr(sorted_ids, "sorted_ids", _i32(), capacity), int(capacity),
+        _ptr(tile_ranges, "tile_ranges", _i32(), 2 * nt), _ptr(lpt_order, "lpt_order", _i32(), nt),
+        _ptr(counts_device, "counts_device", torch.int64, 2, optional=True),
+        C.byref(host) if sync_pairs else None, _stream(stream))
+    _check("gs_bin_sort_noalloc", st, f"; pairs needed: {host.value}" if st == 3 else "")
     return int(host.value) if sync_pairs else None
 
 

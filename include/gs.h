@@ -262,6 +262,33 @@ gs_status gs_project_bwd(const gs_camera* cam, int64_t n, int32_t sh_degree, con
 gs_status gs_raster_stats(const void* workspace, size_t workspace_bytes, int64_t* out,
                           void* stream);
 
+/*
+ * gs_bin_sort_noalloc -- gs_bin_sort for callers that may not allocate device
+ * memory.  The papers have no counterpart: it exists for hosts that own all
+ * of the GPU's memory (a plugin inside an application with its own
+ * allocator) or that cannot afford the synchronisation an allocation may
+ * cause.  Arguments, outputs and results are those of gs_bin_sort, minus
+ * the workspace: the scratch is one fixed 6 MiB device array inside this
+ * library (held on every device the library is loaded on until the process
+ * exits), so the call allocates nothing.
+ *
+ * Limits: n <= 65536 Gaussians, capacity <= 262144 pairs and at most 16384
+ * tiles (2048 x 2048 pixels); larger sizes return GS_ERR_WORKSPACE before
+ * anything is enqueued.  Use gs_bin_sort for more.
+ *
+ * The first call on a device looks up the array's address with that device
+ * current; make it before capturing the stream into a graph.  The array
+ * keeps the previous call's contents (the sort clears what must start at
+ * zero itself), and it is shared: calls whose GPU work overlaps (different
+ * streams or host threads without ordering between them) race on it and
+ * give undefined results.
+ */
+gs_status gs_bin_sort_noalloc(const gs_camera* cam, int64_t n, const float* splats,
+                              const float* depths, const int32_t* tiles_touched,
+                              int32_t* sorted_ids, int64_t capacity, int32_t* tile_ranges,
+                              int32_t* lpt_order, int64_t* counts_device, int64_t* n_pairs_host,
+                              void* stream);
+
 #ifdef __cplusplus
 }
 #endif
