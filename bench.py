@@ -20,6 +20,7 @@ sample of the same workload and prints the same line with "impl": "reference".
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -48,6 +49,10 @@ UNIT = "pairs/s"
 FLOPS_FWD_PER_E = 22
 FLOPS_BWD_PER_E = 48
 FP32_LANES_PER_SM = 128
+# SFU (ex2, rcp) operations per contributing pair: forward ex2; backward ex2 and 1/(1 - alpha)
+SFU_FWD_PER_E = 1
+SFU_BWD_PER_E = 2
+SFU_LANES_PER_SM = 16
 
 
 def parse():
@@ -229,9 +234,12 @@ def run_gpu(args):
     props = torch.cuda.get_device_properties(dev)
     sm_mhz = clocks["sm_mhz"] or peaks.get("clocks_under_load", {}).get("sm_mhz_median") or 1462.0
     dom = max(per_call, key=per_call.get)
-    roof = roofline(dom, per_call[dom], sc, n_pairs, E, H, W, peaks, props.multi_processor_count,
-                    sm_mhz)
+    M = int((r.tiles_touched > 0).sum().item())
+    roof = roofline(dom, per_call[dom], sc, M, n_pairs, E, H, W, peaks,
+                    props.multi_processor_count, sm_mhz)
     launches = kernel_launches(sc.n, r.capacity, W, H)
+    step_roof = step_roofline(ms_per_step, sc, M, n_pairs, E, H, W, peaks,
+                              props.multi_processor_count, sm_mhz)
 
     e2e = None if args.no_e2e else run_e2e(gs, r, sc, cam, w, dev, args, n_pairs)
     cpu = None
@@ -248,6 +256,7 @@ def run_gpu(args):
                        "l2": "inputs larger than L2 (354 MB parameters + 354 MB gradients)"},
             "per_call_ms": per_call,
             "roofline": roof,
+            "step_roofline": step_roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
@@ -259,7 +268,7 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def roofline(call, ms, sc, n_pairs, E, H, W, peaks, n_sm, sm_mhz):
+def roofline(call, ms, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz):
     """Algorithmic work of one launch / its average duration, against the binding peak."""
     if call in ("gs_rasterize_fwd", "gs_rasterize_bwd"):
         per = FLOPS_FWD_PER_E if call == "gs_rasterize_fwd" else FLOPS_BWD_PER_E
@@ -267,22 +276,89 @@ def roofline(call, ms, sc, n_pairs, E, H, W, peaks, n_sm, sm_mhz):
         peak = 2.0 * FP32_LANES_PER_SM * n_sm * sm_mhz * 1e6 / 1e12  # FMA = 2 flops
         achieved = flops / (ms * 1e-3) / 1e12
         return {"kernel": call, "bound": "alu", "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": profiled_traffic(call),
                 "peak_source": f"{n_sm} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 x {sm_mhz:.0f} MHz (sampled)",
                 "work": f"{per} flops x {E} contributing pairs"}
-    N = sc.n
-    K = (sc.sh_degree + 1) ** 2
+    N, G = sc.n, 44 + 12 * (sc.sh_degree + 1) ** 2  # G: parameter bytes per Gaussian
     if call == "gs_project":
-        byts = N * (12 + 12 + 16 + 4 + 48 + 4 + 8 + 4) + N * 12 * K
+        # geometry of every Gaussian, SH of the visible, record of the visible, radii
+        byts = 44 * N + (G - 44) * M + 64 * M + 8 * N
     elif call == "gs_project_bwd":
-        byts = N * (12 + 12 + 16 + 4 + 4 + 1 + 36) + N * 12 * K + N * (12 + 12 + 16 + 4 + 12 * K)
+        # grad2d and parameters of the visible, every gradient row written, the two flags
+        byts = 36 * M + G * M + G * N + 5 * N
     else:  # gs_bin_sort
-        byts = 8 * N * 8 + 8 * n_pairs * 5
+        byts = 8 * M * 8 + 8 * n_pairs * 5
     achieved = byts / (ms * 1e-3) / 1e9
     peak = float(peaks["hbm_gbs"])
     return {"kernel": call, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": None,
+            "frac": achieved / peak, "traffic": profiled_traffic(call),
             "peak_source": f"{peaks['source']} copy bandwidth"}
+
+
+# The kernel each single-kernel call runs, its sources, and its ncu summary.
+PROFILED = {
+    "gs_rasterize_fwd": ("raster_fwd_kernel", ["gs_raster.cu", "gs_device.cuh", "gs_internal.h"]),
+    "gs_rasterize_bwd": ("raster_bwd_kernel", ["gs_raster.cu", "gs_device.cuh", "gs_internal.h"]),
+    "gs_project": ("project_kernel", ["gs_project.cu", "gs_device.cuh", "gs_internal.h"]),
+    "gs_project_bwd": ("project_bwd_kernel", ["gs_project.cu", "gs_device.cuh", "gs_internal.h"]),
+}
+
+
+def sources_digest(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "differentiable_gaussian_splatting_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(call, workload="scene-1.5M-1297x840"):
+    """DRAM bytes (read + write) of one launch, from the committed ncu summary of the call's
+    kernel; None when there is none or the kernel's sources changed since it was taken."""
+    if call not in PROFILED:
+        return None
+    kernel, files = PROFILED[call]
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            for key in ("traffic_bytes_per_launch", "sources_sha256"):
+                if line.startswith(f"- {key}:"):
+                    fields[key] = line.split(":", 1)[1].split()[0].strip("`")
+    if fields.get("sources_sha256") != sources_digest(files):
+        return None
+    return int(fields["traffic_bytes_per_launch"]) if "traffic_bytes_per_launch" in fields else None
+
+
+def step_roofline(ms, sc, M, I, E, H, W, peaks, n_sm, sm_mhz):
+    """Whole-step roofline: per phase the largest of bytes / HBM, fp32 flops / fp32 peak and
+    SFU ops / SFU peak, summed over the phases; frac = that time / the measured step."""
+    N, P = sc.n, H * W
+    G = 44 + 12 * (sc.sh_degree + 1) ** 2  # parameter bytes per Gaussian
+    hbm = float(peaks["hbm_gbs"]) * 1e9
+    fp32 = 2.0 * FP32_LANES_PER_SM * n_sm * sm_mhz * 1e6
+    sfu = SFU_LANES_PER_SM * n_sm * sm_mhz * 1e6
+    phases = {
+        # 44 B of geometry per Gaussian, SH and the 64 B record only for the visible
+        "project": (44 * N + (G - 44) * M + 64 * M + 8 * N, 0, 0),
+        # depth sort of the M visible (8 B, 4 passes, read + write) and the pair list
+        # (emitted once, then 2 passes read + write)
+        "bin_sort": (8 * M * 8 + 8 * I * 5, 0, 0),
+        "forward": (48 * I + 24 * P, FLOPS_FWD_PER_E * E, SFU_FWD_PER_E * E),
+        # raster backward and the chain rule: records, pixel state and dL/dimage, grad2d,
+        # parameters of the visible, every gradient row written
+        "backward": (48 * I + 36 * P + 36 * M + G * M + G * N, FLOPS_BWD_PER_E * E,
+                     SFU_BWD_PER_E * E),
+    }
+    out, total = {}, 0.0
+    for k, (b, f, x) in phases.items():
+        t = max(b / hbm, f / fp32, x / sfu) * 1e3
+        out[k] = t
+        total += t
+    return {"ms": total, "frac": total / ms, "phases_ms": out,
+            "model": "per phase max(bytes/HBM, fp32 flops/fp32 peak, SFU ops/SFU peak), summed"}
 
 
 def kernel_launches(n, capacity, W, H) -> int:
@@ -293,8 +369,10 @@ def kernel_launches(n, capacity, W, H) -> int:
         return max(1, (bits + 7) // 8)
 
     tile_bits = max(1, int(nt - 1).bit_length())
-    cap_bits = max(1, int(capacity).bit_length())
-    bin_sort = 3 + 3 * passes(31) + 3 + 1 + 3 * passes(tile_bits) + 2 + 1 + 3 * passes(cap_bits)
+    # visible compaction 3, depth radix 3/pass, pair offsets 3, emit 1, tile radix 3/pass,
+    # tile ranges 2, LPT order 2
+    bin_sort = 3 + 3 * passes(31) + 3 + 1 + 3 * passes(tile_bits) + 2 + 2
+    # project 1, policy + forward 2, backward 1, project backward 1
     return 1 + bin_sort + 2 + 1 + 1
 
 
@@ -358,11 +436,12 @@ def oracle_sample_step(sc, cam, w, tile_stride: int):
     return int(b.counts[sel.astype(bool)].sum()), dt
 
 
-def cpu_baseline(sc, cam, w, stride: int = 8):
+def cpu_baseline(sc, cam, w, stride: int = 1):
     pairs, dt = oracle_sample_step(sc, cam, w, stride)
+    what = "every tile" if stride == 1 else f"every {stride}th tile in LPT order"
     return {"value": pairs / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"one view: all projections and tile counts, forward + backward of every "
-                      f"{stride}th tile in LPT order ({pairs} pairs), {dt:.1f} s"}
+            "sample": f"one view: all projections and tile counts, forward + backward of "
+                      f"{what} ({pairs} pairs), {dt:.1f} s"}
 
 
 def run_reference(args):
@@ -371,7 +450,7 @@ def run_reference(args):
         return
     sc, cam = ss.make_config(args.config)
     w = ss.loss_weights(args.config, cam.height, cam.width)
-    stride = 32
+    stride = 4
     for _ in range(args.warmup):
         oracle_sample_step(sc, cam, w, stride)
     tot_pairs, tot_s = 0, 0.0
