@@ -414,9 +414,10 @@ __global__ void __launch_bounds__(256) emit_pairs(CamParams cam, const float4* _
             row_range(e, cam.nty, &ty0, &ty1);
             big = tiles_touched[g] > kEmitLane;
             if (!big) {
+                const float dyv = vertex_dy(e);
                 int tx0, tx1;
                 for (int ty = ty0; ty < ty1; ++ty) {
-                    if (!row_span(e, ty, cam.W, cam.H, cam.ntx, &tx0, &tx1)) continue;
+                    if (!row_span(e, dyv, ty, cam.W, cam.H, cam.ntx, &tx0, &tx1)) continue;
                     const uint32_t rowkey = (uint32_t)ty * (uint32_t)cam.ntx;
                     for (int tx = tx0; tx < tx1; ++tx, ++off)
                         if (off < capacity) {
@@ -443,10 +444,11 @@ __global__ void __launch_bounds__(256) emit_pairs(CamParams cam, const float4* _
             const int32_t gb = __shfl_sync(F, g, src);
             const int b0 = __shfl_sync(F, ty0, src), b1 = __shfl_sync(F, ty1, src);
             int64_t ob = __shfl_sync(F, off, src);
+            const float dyv = vertex_dy(eb);
             for (int rb = b0; rb < b1; rb += 32) {
                 const int ty = rb + lane;
                 int tx0 = 0, tx1 = 0;
-                const bool has = ty < b1 && row_span(eb, ty, cam.W, cam.H, cam.ntx, &tx0, &tx1);
+                const bool has = ty < b1 && row_span(eb, dyv, ty, cam.W, cam.H, cam.ntx, &tx0, &tx1);
                 const int cnt = has ? tx1 - tx0 : 0;
                 int incl = cnt;
 #pragma unroll

@@ -94,14 +94,14 @@ __device__ __forceinline__ float pad_of(float r) { return radd(kPadUnit, rmul(r,
 
 // x-extent [*Xlo, *Xhi] of the padded support over the y band [y0, y1] (pixel
 // coordinates, y1 already clipped to the image); false if the band misses it.
-__device__ __forceinline__ bool band_extent(const Ellipse& s, float y0, float y1, float* Xlo,
-                                            float* Xhi) {
+// dyv is vertex_dy(s), computed once per splat by the caller.
+__device__ __forceinline__ bool band_extent(const Ellipse& s, float dyv, float y0, float y1,
+                                            float* Xlo, float* Xhi) {
     float padx = pad_of(s.rx);
     float ryp = radd(s.ry, pad_of(s.ry));
     float lo = smax(rsub(y0, s.muy), -ryp);
     float hi = smin(rsub(y1, s.muy), ryp);
     if (!(lo <= hi)) return false;
-    float dyv = vertex_dy(s);
     float dh = smin(smax(smin(smax(dyv, lo), hi), -s.ry), s.ry);
     float dl = smin(smax(smin(smax(dyv, -hi), -lo), -s.ry), s.ry);
     float xhi = radd(xr_at(s, dh), padx);
@@ -121,13 +121,14 @@ __device__ __forceinline__ void row_range(const Ellipse& s, int nty, int* ty0, i
 }
 
 // Tile columns [*tx0, *tx1) of row ty; false when empty.  A tile's region is
-// the closed hull of its pixel centres, clipped to the W x H image.
-__device__ __forceinline__ bool row_span(const Ellipse& s, int ty, int W, int H, int ntx, int* tx0,
-                                         int* tx1) {
+// the closed hull of its pixel centres, clipped to the W x H image.  dyv is
+// vertex_dy(s).
+__device__ __forceinline__ bool row_span(const Ellipse& s, float dyv, int ty, int W, int H, int ntx,
+                                         int* tx0, int* tx1) {
     float y0 = radd((float)(16 * ty), 0.5f);
     float y1 = smin(radd((float)(16 * ty), 15.5f), rsub((float)H, 0.5f));
     float Xlo, Xhi;
-    if (!band_extent(s, y0, y1, &Xlo, &Xhi)) return false;
+    if (!band_extent(s, dyv, y0, y1, &Xlo, &Xhi)) return false;
     if (Xlo > rsub((float)W, 0.5f) || Xhi < 0.5f) return false;
     float f0 = ceilf(rmul(rsub(Xlo, 15.5f), 0.0625f));
     float f1 = radd(floorf(rmul(rsub(Xhi, 0.5f), 0.0625f)), 1.0f);

@@ -177,8 +177,23 @@ __device__ __forceinline__ Projected project_chain(const CamParams& cam, float m
 // ---------------------------------------------------------------------------
 // forward projection kernel
 // ---------------------------------------------------------------------------
+// One thread per Gaussian for the chain and the colour.  The tile count is a
+// sum over the tile rows a splat's support may cover; rows per splat range
+// from 0 (culled) to the image height, so the block spreads all its
+// (Gaussian, row) pairs evenly over its threads instead of looping per thread.
+constexpr int kProjThreads = 256;
+
+struct ProjShared {
+    float e[8][kProjThreads];      // Ellipse fields, structure of arrays
+    float dyv[kProjThreads];       // vertex_dy of each splat
+    int ty0[kProjThreads];         // first row
+    int off[kProjThreads + 1];     // exclusive prefix of row counts
+    int cnt[kProjThreads];         // tile count
+    int wsum[kProjThreads / 32];
+};
+
 template <int K>
-__global__ void __launch_bounds__(256) project_kernel(CamParams cam, int64_t n,
+__global__ void __launch_bounds__(kProjThreads) project_kernel(CamParams cam, int64_t n,
                                                       const float* __restrict__ means,
                                                       const float* __restrict__ scales,
                                                       const float4* __restrict__ quats,
@@ -188,20 +203,76 @@ __global__ void __launch_bounds__(256) project_kernel(CamParams cam, int64_t n,
                                                       float* __restrict__ depths,
                                                       int2* __restrict__ radii,
                                                       int* __restrict__ tiles_touched) {
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    float mx = means[3 * i], my = means[3 * i + 1], mz = means[3 * i + 2];
-    float o = opac[i];
-    Projected P = project_chain(cam, mx, my, mz, scales[3 * i], scales[3 * i + 1],
-                                scales[3 * i + 2], quats[i], o);
-    int tiles = 0;
-    if (P.ok) {
-        Ellipse e{P.mux, P.muy, P.l11, P.l12, P.l22, P.tau, P.rx, P.ry};
-        int ty0, ty1, tx0, tx1;
-        row_range(e, cam.nty, &ty0, &ty1);
-        for (int ty = ty0; ty < ty1; ++ty)
-            if (row_span(e, ty, cam.W, cam.H, cam.ntx, &tx0, &tx1)) tiles += tx1 - tx0;
+    __shared__ ProjShared S;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t i = (int64_t)blockIdx.x * kProjThreads + tid;
+    const bool in = i < n;
+    float mx = 0.f, my = 0.f, mz = 0.f, o = 0.f;
+    Projected P;
+    P.ok = false;
+    if (in) {
+        mx = means[3 * i];
+        my = means[3 * i + 1];
+        mz = means[3 * i + 2];
+        o = opac[i];
+        P = project_chain(cam, mx, my, mz, scales[3 * i], scales[3 * i + 1], scales[3 * i + 2],
+                          quats[i], o);
     }
+    int nrows = 0;
+    if (P.ok) {
+        const Ellipse e{P.mux, P.muy, P.l11, P.l12, P.l22, P.tau, P.rx, P.ry};
+        int ty0, ty1;
+        row_range(e, cam.nty, &ty0, &ty1);
+        nrows = max(ty1 - ty0, 0);
+        S.e[0][tid] = e.mux;
+        S.e[1][tid] = e.muy;
+        S.e[2][tid] = e.l11;
+        S.e[3][tid] = e.l12;
+        S.e[4][tid] = e.l22;
+        S.e[5][tid] = e.tau;
+        S.e[6][tid] = e.rx;
+        S.e[7][tid] = e.ry;
+        S.dyv[tid] = nrows > 0 ? vertex_dy(e) : 0.f;
+        S.ty0[tid] = ty0;
+    }
+    S.cnt[tid] = 0;
+    // block exclusive scan of the row counts
+    int incl = nrows;
+#pragma unroll
+    for (int o2 = 1; o2 < 32; o2 <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o2);
+        if (lane >= o2) incl += v;
+    }
+    if (lane == 31) S.wsum[warp] = incl;
+    __syncthreads();
+    int wbase = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kProjThreads / 32; ++w) {
+        const int v = S.wsum[w];
+        wbase += w < warp ? v : 0;
+        total += v;
+    }
+    S.off[tid] = wbase + incl - nrows;
+    if (tid == 0) S.off[kProjThreads] = total;
+    __syncthreads();
+    for (int r = tid; r < total; r += kProjThreads) {
+        // owner: the last g with off[g] <= r (splats without rows share the next offset)
+        int lo = 0, hi = kProjThreads;  // off[lo] <= r < off[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (S.off[mid] <= r) lo = mid; else hi = mid;
+        }
+        const int g = lo;
+        const Ellipse e{S.e[0][g], S.e[1][g], S.e[2][g], S.e[3][g],
+                        S.e[4][g], S.e[5][g], S.e[6][g], S.e[7][g]};
+        const int ty = S.ty0[g] + (r - S.off[g]);
+        int tx0, tx1;
+        if (row_span(e, S.dyv[g], ty, cam.W, cam.H, cam.ntx, &tx0, &tx1))
+            atomicAdd(&S.cnt[g], tx1 - tx0);
+    }
+    __syncthreads();
+    if (!in) return;
+    const int tiles = S.cnt[tid];
     float4* rec = splats + 3 * i;
     if (!P.ok || tiles == 0) {
         float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -253,7 +324,7 @@ cudaError_t launch_project(const CamParams& cam, int64_t n, int sh_degree, const
                            const float* sh, float* splats, float* depths, int32_t* radii,
                            int32_t* tiles_touched, cudaStream_t st) {
     if (n == 0) return cudaSuccess;
-    dim3 block(256), grid((unsigned)((n + 255) / 256));
+    dim3 block(kProjThreads), grid((unsigned)((n + kProjThreads - 1) / kProjThreads));
     auto q4 = reinterpret_cast<const float4*>(quats);
     auto s4 = reinterpret_cast<float4*>(splats);
     auto r2 = reinterpret_cast<int2*>(radii);

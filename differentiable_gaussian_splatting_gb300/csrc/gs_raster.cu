@@ -210,25 +210,33 @@ __device__ __forceinline__ bool blend_range(const RasterArgs& A, Smem& S, int tx
 // ---------------------------------------------------------------------------
 // per-frame chunking policy (Ryu & Yoo, Eq. 6), one block
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ bool key_less(uint64_t ca, int ia, uint64_t cb, int ib) {
+    return ca < cb || (ca == cb && ia < ib);
+}
+
 __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* __restrict__ lpt,
                                                                 const int2* __restrict__ ranges,
                                                                 int nt, int K, RasterConfig cfg,
                                                                 int* ctrl, int* sat, int* done) {
-    __shared__ double s_tot[32];
-    __shared__ double s_cost[32];
-    __shared__ int s_h[32], s_k[32];
+    __shared__ long long s_tot[kPolicyThreads / 32];
+    __shared__ uint64_t s_cost[kPolicyThreads / 32];
+    __shared__ int s_cand[kPolicyThreads / 32];
+    __shared__ int s_hk[2];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    double tot = 0.0;
+    // N_total: an integer sum (exactly the double sum of the counts, all below 2^53)
+    long long part = 0;
     for (int t = tid; t < nt; t += kPolicyThreads) {
         const int2 r = ranges[t];
-        tot += (double)(r.y - r.x);
+        part += (long long)(r.y - r.x);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    if (lane == 0) s_tot[warp] = tot;
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) s_tot[warp] = part;
     __syncthreads();
-    tot = 0.0;
-    for (int w = 0; w < kPolicyThreads / 32; ++w) tot += s_tot[w];
+    long long itot = 0;
+#pragma unroll
+    for (int w = 0; w < kPolicyThreads / 32; ++w) itot += s_tot[w];
+    const double tot = (double)itot;
     auto count_at = [&](int j) -> double {
         if (j >= nt) return 0.0;
         const int2 r = ranges[lpt[j]];
@@ -236,7 +244,7 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
     };
     // Eq. 6 multiplied by K > 0 (same minimiser, no division), in round-to-nearest
     // double with no contraction: K T(h, k) = max(N_total + lambda h k, K l) + beta K l,
-    // l = max(N_1 / k, N_{h+1}) (exact: k is a power of two)
+    // l = max(N_1 / k, N_{h+1}); N_1 / k is an exact scaling by a power of two
     const double N1 = count_at(0);
     const double lam = cfg.lambda, beta = cfg.beta, Kd = (double)K;
     const double KN1 = __dmul_rn(Kd, N1);
@@ -247,63 +255,71 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
         bk = bh > 0 ? cfg.force_k : 1;
     } else if (cfg.split_mode == 0) {
         const int hm = min(nt, cfg.h_max);
-        const int ks[4] = {2, 4, 8, 16};
-        double best = base;
-        int h_best = 0, k_best = 1;
+        // candidate c = 4 (h - 1) + i, k = 2^(i + 1): increasing c is increasing (h, k), so
+        // the lexicographic minimum of (cost, h, k) is that of (cost, c).  Costs are
+        // non-negative, so their bit patterns order as unsigned integers.
+        uint64_t best = ~0ull;
+        int cand_best = INT_MAX;
         for (int cand = tid; cand < hm * 4; cand += kPolicyThreads) {
-            const int h = 1 + cand / 4;
-            const int k = ks[cand % 4];
-            const double l = fmax(N1 / (double)k, count_at(h));
+            const int h = 1 + (cand >> 2);
+            const int k = 2 << (cand & 3);
+            const double inv_k = 1.0 / (double)k;  // exact
+            const double l = fmax(__dmul_rn(N1, inv_k), count_at(h));
             const double Kl = __dmul_rn(Kd, l);
             const double work = __dadd_rn(tot, __dmul_rn(__dmul_rn(lam, (double)h), (double)k));
             const double cost = __dadd_rn(fmax(work, Kl), __dmul_rn(beta, Kl));
-            // lexicographic (cost, h, k): candidates are visited in increasing (h, k)
-            if (cost < best) {
-                best = cost;
-                h_best = h;
-                k_best = k;
+            const uint64_t cb = (uint64_t)__double_as_longlong(cost);
+            if (key_less(cb, cand, best, cand_best)) {
+                best = cb;
+                cand_best = cand;
             }
         }
-        // block argmin with the same order
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            const double oc = __shfl_xor_sync(0xffffffffu, best, o);
-            const int oh = __shfl_xor_sync(0xffffffffu, h_best, o);
-            const int ok = __shfl_xor_sync(0xffffffffu, k_best, o);
-            const bool take = oc < best || (oc == best && (oh < h_best || (oh == h_best && ok < k_best)));
-            if (take) {
+            const uint64_t oc = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, cand_best, o);
+            if (key_less(oc, oi, best, cand_best)) {
                 best = oc;
-                h_best = oh;
-                k_best = ok;
+                cand_best = oi;
             }
         }
         if (lane == 0) {
             s_cost[warp] = best;
-            s_h[warp] = h_best;
-            s_k[warp] = k_best;
+            s_cand[warp] = cand_best;
         }
         __syncthreads();
-        if (tid == 0) {
-            for (int w = 1; w < kPolicyThreads / 32; ++w) {
-                const bool take = s_cost[w] < best ||
-                                  (s_cost[w] == best &&
-                                   (s_h[w] < h_best || (s_h[w] == h_best && s_k[w] < k_best)));
-                if (take) {
-                    best = s_cost[w];
-                    h_best = s_h[w];
-                    k_best = s_k[w];
+        if (warp == 0) {
+            best = s_cost[lane];
+            cand_best = s_cand[lane];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const uint64_t oc = __shfl_xor_sync(0xffffffffu, best, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, cand_best, o);
+                if (key_less(oc, oi, best, cand_best)) {
+                    best = oc;
+                    cand_best = oi;
                 }
             }
-            if (h_best > 0 && !(best <= __dmul_rn(__dsub_rn(1.0, (double)cfg.eps), base))) {
-                h_best = 0;
-                k_best = 1;
+            if (lane == 0) {
+                int h_best = 0, k_best = 1;
+                // a split must cost strictly less than no split (h = 0 wins ties) ...
+                const double bc = __longlong_as_double((long long)best);
+                if (cand_best != INT_MAX && bc < base) {
+                    h_best = 1 + (cand_best >> 2);
+                    k_best = 2 << (cand_best & 3);
+                    // ... and save at least eps of it
+                    if (!(bc <= __dmul_rn(__dsub_rn(1.0, (double)cfg.eps), base))) {
+                        h_best = 0;
+                        k_best = 1;
+                    }
+                }
+                s_hk[0] = h_best;
+                s_hk[1] = k_best;
             }
-            s_h[0] = h_best;
-            s_k[0] = k_best;
         }
         __syncthreads();
-        bh = s_h[0];
-        bk = s_k[0];
+        bh = s_hk[0];
+        bk = s_hk[1];
     }
     for (int j = tid; j < bh; j += kPolicyThreads) {
         sat[j] = INT_MAX;
