@@ -76,100 +76,105 @@ __device__ __forceinline__ T block_exclusive_scan_256(T v, T* s_warp, T* total) 
 // ---------------------------------------------------------------------------
 // radix sort kernels
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kRsBlock) rs_upsweep(const uint32_t* __restrict__ keys,
-                                                       const int64_t* n_dev, int64_t n_static,
-                                                       int shift, uint32_t* __restrict__ hist) {
+// Look-back words: one per (block, digit), written once per pass.  Bits 63-62
+// hold the state (0 not ready, 1 the block's own digit count, 2 the inclusive
+// prefix over blocks 0..b), bits 61-56 the pass (1-based, so words left by an
+// earlier pass of the same sort read as not ready) and bits 55-0 the count.
+constexpr uint64_t kLbAgg = 1ull << 62;
+constexpr uint64_t kLbPrefix = 2ull << 62;
+constexpr uint64_t kLbCount = (1ull << 56) - 1;
+constexpr int kMaxPasses = 4;
+// polls of one look-back word before the block gives up and flags an error
+constexpr int kSpinLimit = 1 << 22;
+constexpr int kLbWindow = 8;
+
+__device__ __forceinline__ bool lb_ready(uint64_t w, uint64_t epoch) {
+    return (w >> 62) != 0 && (w & ~(kLbPrefix | kLbAgg | kLbCount)) == epoch;
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Digit counts of every pass in one read of the keys: ghist[pass][digit]
+// (zeroed beforehand).  Equal digits within a warp round are aggregated with
+// __match_any_sync, so near-constant high bytes do not serialise on one counter.
+__global__ void __launch_bounds__(kRsBlock) rs_global_hist(const uint32_t* __restrict__ keys,
+                                                           const int64_t* n_dev, int64_t n_static,
+                                                           int passes,
+                                                           uint32_t* __restrict__ ghist) {
     const int64_t n = count_of(n_dev, n_static);
-    const int64_t nblk = nblk_of(n);
-    const int64_t b = blockIdx.x;
-    if (b >= nblk) return;
-    __shared__ uint32_t cnt[kRsWarps][256];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    __shared__ uint32_t cnt[kMaxPasses][256];
+    const int tid = threadIdx.x, lane = tid & 31;
 #pragma unroll
-    for (int w = 0; w < kRsWarps; ++w) cnt[w][tid] = 0;
+    for (int p = 0; p < kMaxPasses; ++p) cnt[p][tid] = 0;
     __syncthreads();
-    // each warp counts its own contiguous 512 keys; equal digits of a round are
-    // aggregated with __match_any_sync (one shared-memory add per distinct digit),
-    // so near-constant high key bytes do not serialise on one counter
-    const int64_t wbase = b * kRsTile + (int64_t)warp * (32 * kRsIpt);
-    uint32_t k[kRsIpt];
-#pragma unroll
-    for (int r = 0; r < kRsIpt; ++r) {
-        const int64_t idx = wbase + r * 32 + lane;
-        k[r] = idx < n ? __ldg(keys + idx) : 0u;
-    }
-#pragma unroll
-    for (int r = 0; r < kRsIpt; ++r) {
-        const int64_t idx = wbase + r * 32 + lane;
+    const int64_t stride = (int64_t)gridDim.x * kRsBlock;
+    for (int64_t base = (int64_t)blockIdx.x * kRsBlock; base < n; base += stride) {
+        const int64_t idx = base + tid;
         const bool valid = idx < n;
-        const uint32_t d = (k[r] >> shift) & 255u;
-        const uint32_t peers = __match_any_sync(0xffffffffu, valid ? d : 256u + lane);
-        if (valid && (peers & lanemask_lt()) == 0) cnt[warp][d] += __popc(peers);
-        __syncwarp();
+        const uint32_t k = valid ? __ldg(keys + idx) : 0u;
+        for (int p = 0; p < passes; ++p) {
+            const uint32_t d = (k >> (8 * p)) & 255u;
+            const uint32_t peers = __match_any_sync(0xffffffffu, valid ? d : 256u + lane);
+            if (valid && (peers & lanemask_lt()) == 0) atomicAdd(&cnt[p][d], __popc(peers));
+        }
     }
     __syncthreads();
-    uint32_t tot = 0;
-#pragma unroll
-    for (int w = 0; w < kRsWarps; ++w) tot += cnt[w][tid];
-    hist[(int64_t)tid * nblk + b] = tot;
+    for (int p = 0; p < passes; ++p)
+        if (cnt[p][tid]) atomicAdd(ghist + p * 256 + tid, cnt[p][tid]);
 }
 
-// one block per digit: exclusive scan of the digit's row of block counts
-__global__ void __launch_bounds__(kRsBlock) rs_scan_rows(uint32_t* __restrict__ hist,
-                                                         const int64_t* n_dev, int64_t n_static,
-                                                         uint32_t* __restrict__ dtot) {
-    const int64_t n = count_of(n_dev, n_static);
-    const int64_t nblk = nblk_of(n);
-    const int d = blockIdx.x;
-    __shared__ uint32_t s_warp[kRsWarps];
-    uint32_t* row = hist + (int64_t)d * nblk;
-    const int64_t per = (nblk + kRsBlock - 1) / kRsBlock;
-    const int64_t lo = min64(nblk, per * threadIdx.x);
-    const int64_t hi = min64(nblk, lo + per);
-    uint32_t sum = 0;
-    for (int64_t j = lo; j < hi; ++j) sum += row[j];
-    uint32_t total;
-    uint32_t run = block_exclusive_scan_256<uint32_t>(sum, s_warp, &total);
-    for (int64_t j = lo; j < hi; ++j) {
-        uint32_t c = row[j];
-        row[j] = run;
-        run += c;
-    }
-    if (threadIdx.x == 0) dtot[d] = total;
-}
+// One pass of the stable LSD sort: blocks take consecutive 4096-key tiles in
+// ticket order, rank their keys by digit (warps with __match_any_sync, then
+// across warps), publish their digit counts, and add the counts of the tiles
+// before them by looking back through the published words (decoupled
+// look-back: a block only waits on tiles that started before it, so waits
+// end).  Keys are staged in shared memory in block-sorted order so that each
+// digit's run is written to global memory contiguously.
+struct OnesweepSmem {
+    uint32_t keys[kRsTile];
+    int32_t vals[kRsTile];
+    uint32_t wcnt[kRsWarps][256];
+    uint32_t dstart[256];
+    int64_t gbase[256];
+    uint32_t warp_sums[kRsWarps];
+    int ticket;
+};
 
-__global__ void __launch_bounds__(kRsBlock) rs_downsweep(
+__global__ void __launch_bounds__(kRsBlock, 2) rs_onesweep(
     const uint32_t* __restrict__ keys_in, const int32_t* __restrict__ vals_in,
     uint32_t* __restrict__ keys_out, int32_t* __restrict__ vals_out, const int64_t* n_dev,
-    int64_t n_static, int shift, const uint32_t* __restrict__ hist,
-    const uint32_t* __restrict__ dtot) {
+    int64_t n_static, int pass, const uint32_t* __restrict__ ghist, int* __restrict__ tickets,
+    uint64_t* __restrict__ lookback, unsigned long long* __restrict__ err) {
+    __shared__ OnesweepSmem S;
     const int64_t n = count_of(n_dev, n_static);
     const int64_t nblk = nblk_of(n);
-    const int64_t b = blockIdx.x;
-    if (b >= nblk) return;
-    __shared__ uint32_t s_base[256];
-    __shared__ uint32_t s_wcnt[kRsWarps][256];
-    __shared__ uint32_t s_warp[kRsWarps];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int shift = 8 * pass;
+    const uint64_t epoch = (uint64_t)(pass + 1) << 56;
+    if (tid == 0) S.ticket = atomicAdd(tickets + pass, 1);
 #pragma unroll
-    for (int w = 0; w < kRsWarps; ++w) s_wcnt[w][tid] = 0;
-    {
-        uint32_t total;
-        uint32_t dbase = block_exclusive_scan_256<uint32_t>(dtot[tid], s_warp, &total);
-        s_base[tid] = dbase + hist[(int64_t)tid * nblk + b];
-    }
+    for (int w = 0; w < kRsWarps; ++w) S.wcnt[w][tid] = 0;
     __syncthreads();
+    const int64_t b = S.ticket;
+    if (b >= nblk) return;
 
+    // ---- load (each warp owns 512 consecutive keys) and rank within the warp
     const int64_t wbase = b * kRsTile + (int64_t)warp * (32 * kRsIpt);
     uint32_t k[kRsIpt];
     int32_t v[kRsIpt];
     uint32_t loc[kRsIpt];
-    // issue every load of the warp's 512 keys before ranking them
 #pragma unroll
     for (int r = 0; r < kRsIpt; ++r) {
         const int64_t idx = wbase + r * 32 + lane;
         const bool valid = idx < n;
-        k[r] = valid ? __ldg(keys_in + idx) : 0u;
+        k[r] = valid ? __ldg(keys_in + idx) : 0xffffffffu;
         v[r] = valid ? __ldg(vals_in + idx) : 0;
     }
 #pragma unroll
@@ -179,58 +184,141 @@ __global__ void __launch_bounds__(kRsBlock) rs_downsweep(
         const uint32_t d = (k[r] >> shift) & 255u;
         const uint32_t peers = __match_any_sync(0xffffffffu, valid ? d : 256u + lane);
         const uint32_t rank = __popc(peers & lanemask_lt());
-        const uint32_t prev = s_wcnt[warp][d & 255u];
+        const uint32_t prev = S.wcnt[warp][d];
         loc[r] = prev + rank;
         __syncwarp();
-        if (valid && rank == 0) s_wcnt[warp][d] = prev + __popc(peers);
+        if (valid && rank == 0) S.wcnt[warp][d] = prev + __popc(peers);
         __syncwarp();
     }
     __syncthreads();
-    {
-        uint32_t run = 0;
+
+    // ---- per digit (thread = digit): warp prefixes, block count, publish
+    const int d = tid;
+    uint32_t cd = 0;
 #pragma unroll
-        for (int w = 0; w < kRsWarps; ++w) {
-            uint32_t c = s_wcnt[w][tid];
-            s_wcnt[w][tid] = run;
-            run += c;
-        }
+    for (int w = 0; w < kRsWarps; ++w) {
+        const uint32_t c = S.wcnt[w][d];
+        S.wcnt[w][d] = cd;
+        cd += c;
+    }
+    uint64_t* my = lookback + b * 256 + d;
+    st_relaxed(my, (b == 0 ? kLbPrefix : kLbAgg) | epoch | (uint64_t)cd);
+    // block-local start of each digit's run
+    uint32_t x = cd;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) S.warp_sums[warp] = x;
+    // global start of each digit: exclusive scan of the pass's digit counts
+    uint32_t gd = ghist[pass * 256 + d];
+    uint32_t gx = gd;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, gx, o);
+        if (lane >= o) gx += y;
     }
     __syncthreads();
+    uint32_t wpre = 0;
+#pragma unroll
+    for (int w = 0; w < kRsWarps; ++w) wpre += w < warp ? S.warp_sums[w] : 0u;
+    const uint32_t dstart = wpre + x - cd;
+    S.dstart[d] = dstart;
+    __syncthreads();
+    if (lane == 31) S.warp_sums[warp] = gx;
+    __syncthreads();
+    uint64_t gpre = 0;
+#pragma unroll
+    for (int w = 0; w < kRsWarps; ++w) gpre += w < warp ? S.warp_sums[w] : 0u;
+    const uint64_t gstart = gpre + gx - gd;
+
+    // ---- look back over the earlier tiles for this digit, kLbWindow words in
+    // flight at a time (nearest first), up to the first inclusive prefix
+    uint64_t excl = 0;
+    if (b > 0) {
+        bool found = false;
+        for (int64_t jb = b - 1; jb >= 0 && !found; jb -= kLbWindow) {
+            uint64_t wv[kLbWindow];
+#pragma unroll
+            for (int i = 0; i < kLbWindow; ++i)
+                wv[i] = jb - i >= 0 ? ld_relaxed(lookback + (jb - i) * 256 + d) : 0ull;
+#pragma unroll
+            for (int i = 0; i < kLbWindow; ++i) {
+                if (found || jb - i < 0) break;
+                const uint64_t* wp = lookback + (jb - i) * 256 + d;
+                int spins = 0;
+                while (!lb_ready(wv[i], epoch) && ++spins < kSpinLimit) wv[i] = ld_relaxed(wp);
+                if (spins >= kSpinLimit) {
+                    atomicOr(err, 1ull);  // the tile before never published: give up
+                    found = true;
+                    break;
+                }
+                excl += wv[i] & kLbCount;
+                found = (wv[i] >> 62) == 2;
+            }
+        }
+        st_relaxed(my, kLbPrefix | epoch | (excl + cd));
+    }
+    S.gbase[d] = (int64_t)(gstart + excl) - (int64_t)dstart;
+
+    // ---- stage in block-sorted order, then write each digit run contiguously
 #pragma unroll
     for (int r = 0; r < kRsIpt; ++r) {
         const int64_t idx = wbase + r * 32 + lane;
         if (idx < n) {
-            const uint32_t d = (k[r] >> shift) & 255u;
-            const uint32_t pos = s_base[d] + s_wcnt[warp][d] + loc[r];
-            keys_out[pos] = k[r];
-            vals_out[pos] = v[r];
+            const uint32_t dd = (k[r] >> shift) & 255u;
+            const uint32_t li = S.dstart[dd] + S.wcnt[warp][dd] + loc[r];
+            S.keys[li] = k[r];
+            S.vals[li] = v[r];
         }
+    }
+    __syncthreads();
+    const int cnt = (int)min64(kRsTile, n - b * kRsTile);
+    for (int i = tid; i < cnt; i += kRsBlock) {
+        const uint32_t key = S.keys[i];
+        const int64_t pos = S.gbase[(key >> shift) & 255u] + i;
+        keys_out[pos] = key;
+        vals_out[pos] = S.vals[i];
     }
 }
 
-// Stable LSD radix sort of (keys, vals) on bits [0, bits).  The count is read
-// from n_dev (device) when given, else n_static; n_max bounds it.  Passes
-// ping-pong between (k0, v0) and (k1, v1), starting from (k0, v0).  The last
-// pass writes its values to vf when given (a buffer distinct from v0, v1) and
-// its keys to the scratch buffer the pass did not read; *kres / *vres return
-// where the sorted keys and values are.
+// Stable LSD radix sort of (keys, vals) on bits [0, bits), bits <= 32.  The
+// count is read from n_dev (device) when given, else n_static; n_max bounds
+// it.  Passes ping-pong between (k0, v0) and (k1, v1), starting from (k0, v0).
+// The last pass writes its values to vf when given (a buffer distinct from v0,
+// v1) and its keys to the scratch buffer the pass did not read; *kres / *vres
+// return where the sorted keys and values are.  ctl is the sort's control
+// region (rs_ctl_bytes(n_max)), cleared here; err collects give-up flags.
+size_t rs_ctl_bytes(int64_t n_max) {
+    return 16 + kMaxPasses * 256 * 4 + (size_t)std::max<int64_t>(1, nblk_of(n_max)) * 256 * 8;
+}
+
 cudaError_t radix_sort(uint32_t* k0, int32_t* v0, uint32_t* k1, int32_t* v1, int32_t* vf,
-                       const int64_t* n_dev, int64_t n_static, int64_t n_max, int bits,
-                       uint32_t* hist, uint32_t* dtot, cudaStream_t st, uint32_t** kres,
+                       const int64_t* n_dev, int64_t n_static, int64_t n_max, int bits, char* ctl,
+                       unsigned long long* err, cudaStream_t st, uint32_t** kres,
                        int32_t** vres) {
     const int passes = std::max(1, (bits + 7) / 8);
     const unsigned grid = (unsigned)std::max<int64_t>(1, nblk_of(n_max));
+    int* tickets = reinterpret_cast<int*>(ctl);
+    uint32_t* ghist = reinterpret_cast<uint32_t*>(ctl + 16);
+    uint64_t* lookback = reinterpret_cast<uint64_t*>(ctl + 16 + kMaxPasses * 256 * 4);
+    cudaError_t e = cudaMemsetAsync(ctl, 0, rs_ctl_bytes(n_max), st);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const unsigned hgrid = (unsigned)std::max<int64_t>(
+        1, std::min<int64_t>((n_max + kRsBlock - 1) / kRsBlock, (int64_t)std::max(sms, 1)));
+    rs_global_hist<<<hgrid, kRsBlock, 0, st>>>(k0, n_dev, n_static, passes, ghist);
     uint32_t* kin = k0;
     int32_t* vin = v0;
     for (int p = 0; p < passes; ++p) {
         const bool last = p == passes - 1;
         uint32_t* kout = kin == k0 ? k1 : k0;
         int32_t* vout = (last && vf) ? vf : (vin == v0 ? v1 : v0);
-        const int shift = 8 * p;
-        rs_upsweep<<<grid, kRsBlock, 0, st>>>(kin, n_dev, n_static, shift, hist);
-        rs_scan_rows<<<256, kRsBlock, 0, st>>>(hist, n_dev, n_static, dtot);
-        rs_downsweep<<<grid, kRsBlock, 0, st>>>(kin, vin, kout, vout, n_dev, n_static, shift, hist,
-                                                dtot);
+        rs_onesweep<<<grid, kRsBlock, 0, st>>>(kin, vin, kout, vout, n_dev, n_static, p, ghist,
+                                               tickets, lookback, err);
         kin = kout;
         vin = vout;
     }
@@ -609,7 +697,6 @@ BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles) {
     };
     const int64_t nn = std::max<int64_t>(n, 1), cap = std::max<int64_t>(capacity, 1);
     const int64_t nt = std::max<int64_t>(n_tiles, 1);
-    const int64_t hist_blocks = nblk_of(std::max({nn, cap, nt}));
     L.off_counts = take(4 * sizeof(int64_t));
     L.off_bsum = take((size_t)(nblk_of(nn) + 1) * sizeof(int64_t));
     L.off_dkeys0 = take((size_t)nn * 4);
@@ -621,8 +708,7 @@ BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles) {
     L.off_pkeys1 = take((size_t)cap * 4);
     L.off_pvals0 = take((size_t)cap * 4);
     L.off_pvals1 = take((size_t)cap * 4);
-    L.off_hist = take((size_t)256 * hist_blocks * 4);
-    L.off_dtot = take(256 * 4);
+    L.off_hist = take(rs_ctl_bytes(std::max(nn, cap)));
     L.off_lruns = take((size_t)((nt + kLptRun - 1) / kLptRun) * kLptRun * sizeof(uint64_t));
     L.total = off;
     return L;
@@ -643,8 +729,8 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
     auto* pk1 = reinterpret_cast<uint32_t*>(ws + L.off_pkeys1);
     auto* pv0 = reinterpret_cast<int32_t*>(ws + L.off_pvals0);
     auto* pv1 = reinterpret_cast<int32_t*>(ws + L.off_pvals1);
-    auto* hist = reinterpret_cast<uint32_t*>(ws + L.off_hist);
-    auto* dtot = reinterpret_cast<uint32_t*>(ws + L.off_dtot);
+    char* rs_ctl = ws + L.off_hist;
+    auto* sort_err = reinterpret_cast<unsigned long long*>(ws + L.off_counts + 3 * sizeof(int64_t));
     auto* lruns = reinterpret_cast<uint64_t*>(ws + L.off_lruns);
     const int64_t nt = (int64_t)cam.ntx * cam.nty;
     cudaError_t err;
@@ -663,7 +749,7 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
         // 2. stable depth sort of the M visible (31 significant key bits)
         uint32_t* dks = nullptr;
         int32_t* dvs = nullptr;
-        err = radix_sort(dk0, dv0, dk1, dv1, nullptr, counts + 0, 0, n, 31, hist, dtot, st, &dks,
+        err = radix_sort(dk0, dv0, dk1, dv1, nullptr, counts + 0, 0, n, 31, rs_ctl, sort_err, st, &dks,
                          &dvs);
         if (err != cudaSuccess) return err;
         // 3. pair offsets in depth order, I = total, min(I, capacity)
@@ -678,7 +764,7 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
         // 5. stable sort by tile key; values land in sorted_ids
         uint32_t* pks = nullptr;
         err = radix_sort(pk0, pv0, pk1, pv1, sorted_ids, counts + 2, 0, capacity,
-                         bits_for(nt - 1), hist, dtot, st, &pks, nullptr);
+                         bits_for(nt - 1), rs_ctl, sort_err, st, &pks, nullptr);
         if (err != cudaSuccess) return err;
         // 6. tile ranges
         tile_ranges_kernel<<<1024, 256, 0, st>>>(pks, counts + 2, reinterpret_cast<int2*>(tile_ranges));

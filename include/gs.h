@@ -67,7 +67,7 @@ typedef enum {
     GS_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or setting */
     GS_ERR_CUDA = 2,        /* a CUDA runtime call or launch failed */
     GS_ERR_CAPACITY = 3,    /* the pair list does not fit: see gs_bin_sort */
-    GS_ERR_TIMEOUT = 4,     /* reserved: a bounded device wait gave up */
+    GS_ERR_TIMEOUT = 4,     /* a bounded device wait gave up (outputs invalid) */
     GS_ERR_WORKSPACE = 5    /* workspace smaller than the size query returned */
 } gs_status;
 
@@ -157,7 +157,10 @@ size_t gs_bin_sort_workspace_bytes(int64_t n, int64_t capacity, int32_t width, i
  *   n_pairs_host   optional host int64: if non-NULL the call synchronises
  *                  the stream and stores I; if I > capacity it returns
  *                  GS_ERR_CAPACITY (outputs are then invalid: retry with a
- *                  larger list).  With n_pairs_host NULL the call never
+ *                  larger list).  Each radix pass lets a block wait for the
+ *                  digit counts of the blocks before it; those waits are
+ *                  bounded, and if one gives up the synchronising call
+ *                  returns GS_ERR_TIMEOUT (outputs invalid).  With n_pairs_host NULL the call never
  *                  synchronises and the caller must ensure I <= capacity
  *                  (writes beyond capacity are always suppressed).
  */
