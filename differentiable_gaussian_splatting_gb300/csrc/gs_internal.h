@@ -32,12 +32,11 @@ cudaError_t launch_project_bwd(const CamParams& cam, int64_t n, int sh_degree, c
 // ---- binning + sort (gs_binsort.cu) ---------------------------------------
 struct BinSortLayout {
     size_t total;
-    size_t off_counts;   // int64[4]: M, I, min(I, capacity), sort give-up flags
-    size_t off_bsum;     // int64[nblk_n + 1] scan block sums
-    size_t off_dkeys0, off_dkeys1, off_dvals0, off_dvals1;  // uint32 / int32 [n]
-    size_t off_poff;     // int64[n + 1]: pair offsets in depth order
-    size_t off_pkeys0, off_pkeys1, off_pvals0, off_pvals1;  // [capacity]
-    size_t off_hist;     // radix sort control: pass tickets, digit counts, look-back words
+    size_t off_counts;   // int64[8]: M, I, min(I, capacity), raw pairs appended, pad
+    size_t off_raw;      // uint2[capacity]: raw (tile, Gaussian) pairs; later a merge buffer
+    size_t off_keys;     // uint64[capacity]: the tiles' slices of (depth bits << 32 | id)
+    size_t off_tcount;   // int32[n_tiles]: pairs per tile
+    size_t off_cursor;   // uint64[n_tiles]: bucket cursors
     size_t off_lruns;    // uint64[n_tiles rounded up to 1024]: sorted runs of LPT keys
 };
 BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles);

@@ -67,7 +67,7 @@ typedef enum {
     GS_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or setting */
     GS_ERR_CUDA = 2,        /* a CUDA runtime call or launch failed */
     GS_ERR_CAPACITY = 3,    /* the pair list does not fit: see gs_bin_sort */
-    GS_ERR_TIMEOUT = 4,     /* a bounded device wait gave up (outputs invalid) */
+    GS_ERR_TIMEOUT = 4,     /* reserved: a bounded device wait gave up */
     GS_ERR_WORKSPACE = 5    /* workspace smaller than the size query returned */
 } gs_status;
 
@@ -142,10 +142,11 @@ size_t gs_bin_sort_workspace_bytes(int64_t n, int64_t capacity, int32_t width, i
 
 /*
  * gs_bin_sort -- [K] Step 1 (b), (d); [RY] Sec. 4.1 (LPT ordering).
- * Two-stage sort: the visible Gaussians are radix-sorted by depth (stable, so
- * equal depths keep id order), every (tile, Gaussian) pair is emitted in that
- * order from the exact row spans, and the pairs are radix-sorted by tile
- * (stable).  The pair list is therefore ordered by (tile, depth, id).
+ * Per-tile buckets: every (tile, Gaussian) pair of the exact row spans is
+ * counted in its tile's counter, a prefix scan of the counts lays the tiles
+ * out, the pairs are scattered into their tiles' slices and every slice is
+ * sorted by (depth, id).  The pair list is therefore ordered by
+ * (tile, depth, id).
  *
  *   splats, depths, tiles_touched   outputs of gs_project
  *   workspace       device scratch of >= gs_bin_sort_workspace_bytes(...)
@@ -157,12 +158,10 @@ size_t gs_bin_sort_workspace_bytes(int64_t n, int64_t capacity, int32_t width, i
  *   n_pairs_host   optional host int64: if non-NULL the call synchronises
  *                  the stream and stores I; if I > capacity it returns
  *                  GS_ERR_CAPACITY (outputs are then invalid: retry with a
- *                  larger list).  Each radix pass lets a block wait for the
- *                  digit counts of the blocks before it; those waits are
- *                  bounded, and if one gives up the synchronising call
- *                  returns GS_ERR_TIMEOUT (outputs invalid).  With n_pairs_host NULL the call never
- *                  synchronises and the caller must ensure I <= capacity
- *                  (writes beyond capacity are always suppressed).
+ *                  larger list).  With n_pairs_host NULL the call never
+ *                  synchronises and the caller must ensure I <= capacity;
+ *                  when I > capacity every tile range is empty and nothing
+ *                  is written beyond capacity.
  */
 gs_status gs_bin_sort(const gs_camera* cam, int64_t n, const float* splats, const float* depths,
                       const int32_t* tiles_touched, void* workspace, size_t workspace_bytes,
