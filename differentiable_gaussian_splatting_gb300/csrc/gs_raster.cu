@@ -520,6 +520,9 @@ __global__ void __launch_bounds__(kThreads) raster_bwd_kernel(RasterArgs A) {
     const int h = A.ctrl[kCtlH], k = A.ctrl[kCtlK], nitems = A.ctrl[kCtlItems];
     const int my_comp = comp_of_lane(lane);
     const bool writer = !(lane & 1) && my_comp >= 0;
+    // the conic components are summed without their constant factors
+    // (-1/2 dx^2, -dx dy, -1/2 dy^2), applied once by the writing lane
+    const float comp_scale = (my_comp == 2 || my_comp == 4) ? -0.5f : (my_comp == 3 ? -1.f : 1.f);
     int lx, ly;
     tile_pixel(tid, &lx, &ly);
     while (true) {
@@ -577,6 +580,7 @@ __global__ void __launch_bounds__(kThreads) raster_bwd_kernel(RasterArgs A) {
                     S.r1[tid] = __ldg(A.splats + 3 * (int64_t)g + 1);
                     S.r2[tid] = __ldg(A.splats + 3 * (int64_t)g + 2);
                     S.gid[tid] = g;
+                    if (A.touched) A.touched[g] = 1;  // it blended into some pixel
                 }
             }
             __syncthreads();
@@ -585,16 +589,17 @@ __global__ void __launch_bounds__(kThreads) raster_bwd_kernel(RasterArgs A) {
                 uint32_t bit = jj < nb ? (S.mask[jj] >> warp) & 1u : 0u;
                 if (bs + jj > wlast) bit = 0;
                 uint32_t work = __ballot_sync(0xffffffffu, bit);
+                // list positions fit in 32 bits (the pair capacity is below 2^31)
+                const int rel_last = last - (int)bs;
                 while (work) {
                     const int q = 31 - __clz(work);
                     work &= ~(1u << q);
                     const int idx = c + q;
-                    const int64_t gpos = bs + idx;
                     const float4 r0 = S.r0[idx], r1 = S.r1[idx], r2 = S.r2[idx];
                     const float dx = rsub(px, r0.x), dy = rsub(py, r0.y);
                     float u1, u2;
                     const float qv = quad_q(r0.z, r0.w, r1.x, dx, dy, &u1, &u2);
-                    const bool act = (qv <= r1.y) && gpos <= (int64_t)last;
+                    const bool act = (qv <= r1.y) && idx <= rel_last;
                     const float araw = ex2_approx(fmaf(qv, kNegHalfLog2e, r1.z));
                     float alpha = fminf(araw, kAlphaMax);
                     alpha = act ? alpha : 0.f;
@@ -609,23 +614,24 @@ __global__ void __launch_bounds__(kThreads) raster_bwd_kernel(RasterArgs A) {
                     if (__ballot_sync(0xffffffffu, act) == 0) continue;
                     // conic of the evaluated quadratic: a = l11^2, b = l11 l12,
                     // c = l12^2 + l22^2, so a dx + b dy = l11 u1, b dx + c dy = l12 u1 + l22 u2
+                    const float gdx = gs * dx;
                     float v[9];
                     v[0] = gs * (r0.z * u1);
                     v[1] = gs * fmaf(r0.w, u1, r1.x * u2);
-                    v[2] = -0.5f * gs * dx * dx;
-                    v[3] = -gs * dx * dy;
-                    v[4] = -0.5f * gs * dy * dy;
+                    v[2] = gdx * dx;
+                    v[3] = gdx * dy;
+                    v[4] = (gs * dy) * dy;
                     v[5] = gs;
                     v[6] = wgt * Gr;
                     v[7] = wgt * Gg;
                     v[8] = wgt * Gb;
-                    float sum = reduce_scatter9(v, lane);
-                    const int32_t g = S.gid[idx];
+                    const float sum = reduce_scatter9(v, lane);
                     if (writer) {
-                        if (my_comp == 5) sum *= ex2_approx(-r1.z);  // / opacity
-                        atomicAdd(A.grad2d + 9 * (int64_t)g + my_comp, sum);
+                        const int32_t g = S.gid[idx];
+                        // component 5 is d/d(opacity): divide by o = 2^log2(o)
+                        const float f = my_comp == 5 ? ex2_approx(-r1.z) : comp_scale;
+                        atomicAdd(A.grad2d + 9 * (int64_t)g + my_comp, sum * f);
                     }
-                    if (lane == 0 && A.touched) A.touched[g] = 1;
                 }
             }
             __syncthreads();

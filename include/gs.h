@@ -225,7 +225,8 @@ gs_status gs_rasterize_fwd(const gs_camera* cam, const gs_settings* settings, in
  *   dL_dt_final [H][W]         optional (NULL = 0)
  * Outputs (zeroed by the call first):
  *   grad2d [n][9]   mux, muy, a, b, c, opacity, r, g, b
- *   touched [n]     1 where a splat received a gradient (optional)
+ *   touched [n]     1 where a splat blended into some pixel of the image
+ *                   (optional; its gradient may still be zero)
  */
 gs_status gs_rasterize_bwd(const gs_camera* cam, const gs_settings* settings, int64_t n,
                            const float* splats, const int32_t* sorted_ids, int64_t capacity,
