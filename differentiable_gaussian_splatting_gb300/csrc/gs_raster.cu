@@ -513,6 +513,107 @@ __device__ __forceinline__ int comp_of_lane(int lane) {
     }
 }
 
+// Two splats' nine values summed over the warp at once: lanes 0-15 keep
+// splat a, lanes 16-31 splat b (one exchange at xor 16), then each half
+// reduce-scatters its nine sums (xor 8, 4, 2, 1): 20 shuffles for both splats
+// instead of 24.  Afterwards lane l holds component comp16_of_lane(l & 15) of
+// splat (l < 16 ? a : b) (valid when >= 0).
+__device__ __forceinline__ float reduce_scatter9x2(const float a[9], const float b[9], int lane) {
+    const unsigned F = 0xffffffffu;
+    const bool lo16 = !(lane & 16);
+    float k[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+        const float r = __shfl_xor_sync(F, lo16 ? b[i] : a[i], 16);
+        k[i] = (lo16 ? a[i] : b[i]) + r;
+    }
+    const bool lo8 = !(lane & 8);
+    float u[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+        const float send = lo8 ? (i < 4 ? k[5 + i] : 0.f) : k[i];
+        const float r = __shfl_xor_sync(F, send, 8);
+        u[i] = lo8 ? k[i] + r : (i < 4 ? k[5 + i] + r : 0.f);
+    }
+    const bool lo4 = !(lane & 4);
+    float w[3];
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        const float send = lo4 ? (i < 2 ? u[3 + i] : 0.f) : u[i];
+        const float r = __shfl_xor_sync(F, send, 4);
+        w[i] = lo4 ? u[i] + r : (i < 2 ? u[3 + i] + r : 0.f);
+    }
+    const bool lo2 = !(lane & 2);
+    float x[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = lo2 ? (i < 1 ? w[2 + i] : 0.f) : w[i];
+        const float r = __shfl_xor_sync(F, send, 2);
+        x[i] = lo2 ? w[i] + r : (i < 1 ? w[2 + i] + r : 0.f);
+    }
+    const bool lo1 = !(lane & 1);
+    const float r = __shfl_xor_sync(F, lo1 ? x[1] : x[0], 1);
+    return (lo1 ? x[0] : x[1]) + r;
+}
+
+// component held by lane l (0..15 within its half) after reduce_scatter9x2, or -1
+__device__ __forceinline__ int comp16_of_lane(int l) {
+    switch (l) {
+        case 0: return 0;
+        case 1: return 1;
+        case 2: return 2;
+        case 4: return 3;
+        case 5: return 4;
+        case 8: return 5;
+        case 9: return 6;
+        case 10: return 7;
+        case 12: return 8;
+        default: return -1;
+    }
+}
+
+__device__ __forceinline__ float conic_scale(int comp) {
+    return (comp == 2 || comp == 4) ? -0.5f : (comp == 3 ? -1.f : 1.f);
+}
+
+// One splat of the back-to-front walk for the calling lane's pixel: recovers
+// the transmittance in front of it, updates the colour behind, and returns
+// whether the pixel blended it; v gets its nine screen-space terms (all zero
+// when it did not), the conic ones without their constant factors.
+__device__ __forceinline__ bool splat_terms(const Smem& S, int idx, float px, float py, int rel_last,
+                                            float Gr, float Gg, float Gb, float gTT, float& T,
+                                            float& accum, float v[9]) {
+    const float4 r0 = S.r0[idx], r1 = S.r1[idx], r2 = S.r2[idx];
+    const float dx = rsub(px, r0.x), dy = rsub(py, r0.y);
+    float u1, u2;
+    const float qv = quad_q(r0.z, r0.w, r1.x, dx, dy, &u1, &u2);
+    const bool act = (qv <= r1.y) && idx <= rel_last;
+    const float araw = ex2_approx(fmaf(qv, kNegHalfLog2e, r1.z));
+    float alpha = fminf(araw, kAlphaMax);
+    alpha = act ? alpha : 0.f;
+    const float inv = __fdividef(1.f, 1.f - alpha);
+    const float Tb = T * inv;
+    const float wgt = alpha * Tb;
+    const float cG = r2.x * Gr + r2.y * Gg + r2.z * Gb;
+    const float dalpha = Tb * cG - (accum + gTT) * inv;
+    accum = fmaf(cG, wgt, accum);
+    const float gs = (act && araw < kAlphaMax) ? araw * dalpha : 0.f;
+    T = act ? Tb : T;
+    // conic of the evaluated quadratic: a = l11^2, b = l11 l12, c = l12^2 + l22^2,
+    // so a dx + b dy = l11 u1 and b dx + c dy = l12 u1 + l22 u2
+    const float gdx = gs * dx;
+    v[0] = gs * (r0.z * u1);
+    v[1] = gs * fmaf(r0.w, u1, r1.x * u2);
+    v[2] = gdx * dx;
+    v[3] = gdx * dy;
+    v[4] = (gs * dy) * dy;
+    v[5] = gs;
+    v[6] = wgt * Gr;
+    v[7] = wgt * Gg;
+    v[8] = wgt * Gb;
+    return act;
+}
+
 __global__ void __launch_bounds__(kThreads) raster_bwd_kernel(RasterArgs A) {
     __shared__ Smem S;
     __shared__ int s_last;
@@ -520,9 +621,10 @@ __global__ void __launch_bounds__(kThreads) raster_bwd_kernel(RasterArgs A) {
     const int h = A.ctrl[kCtlH], k = A.ctrl[kCtlK], nitems = A.ctrl[kCtlItems];
     const int my_comp = comp_of_lane(lane);
     const bool writer = !(lane & 1) && my_comp >= 0;
+    const int my_comp2 = comp16_of_lane(lane & 15);
     // the conic components are summed without their constant factors
     // (-1/2 dx^2, -dx dy, -1/2 dy^2), applied once by the writing lane
-    const float comp_scale = (my_comp == 2 || my_comp == 4) ? -0.5f : (my_comp == 3 ? -1.f : 1.f);
+    const float comp_scale = conic_scale(my_comp), comp_scale2 = conic_scale(my_comp2);
     int lx, ly;
     tile_pixel(tid, &lx, &ly);
     while (true) {
@@ -592,45 +694,39 @@ __global__ void __launch_bounds__(kThreads) raster_bwd_kernel(RasterArgs A) {
                 // list positions fit in 32 bits (the pair capacity is below 2^31)
                 const int rel_last = last - (int)bs;
                 while (work) {
-                    const int q = 31 - __clz(work);
-                    work &= ~(1u << q);
-                    const int idx = c + q;
-                    const float4 r0 = S.r0[idx], r1 = S.r1[idx], r2 = S.r2[idx];
-                    const float dx = rsub(px, r0.x), dy = rsub(py, r0.y);
-                    float u1, u2;
-                    const float qv = quad_q(r0.z, r0.w, r1.x, dx, dy, &u1, &u2);
-                    const bool act = (qv <= r1.y) && idx <= rel_last;
-                    const float araw = ex2_approx(fmaf(qv, kNegHalfLog2e, r1.z));
-                    float alpha = fminf(araw, kAlphaMax);
-                    alpha = act ? alpha : 0.f;
-                    const float inv = __fdividef(1.f, 1.f - alpha);
-                    const float Tb = T * inv;
-                    const float wgt = alpha * Tb;
-                    const float cG = r2.x * Gr + r2.y * Gg + r2.z * Gb;
-                    const float dalpha = Tb * cG - (accum + gTT) * inv;
-                    accum = fmaf(cG, wgt, accum);
-                    const float gs = (act && araw < kAlphaMax) ? araw * dalpha : 0.f;
-                    T = act ? Tb : T;
-                    if (__ballot_sync(0xffffffffu, act) == 0) continue;
-                    // conic of the evaluated quadratic: a = l11^2, b = l11 l12,
-                    // c = l12^2 + l22^2, so a dx + b dy = l11 u1, b dx + c dy = l12 u1 + l22 u2
-                    const float gdx = gs * dx;
-                    float v[9];
-                    v[0] = gs * (r0.z * u1);
-                    v[1] = gs * fmaf(r0.w, u1, r1.x * u2);
-                    v[2] = gdx * dx;
-                    v[3] = gdx * dy;
-                    v[4] = (gs * dy) * dy;
-                    v[5] = gs;
-                    v[6] = wgt * Gr;
-                    v[7] = wgt * Gg;
-                    v[8] = wgt * Gb;
-                    const float sum = reduce_scatter9(v, lane);
-                    if (writer) {
-                        const int32_t g = S.gid[idx];
-                        // component 5 is d/d(opacity): divide by o = 2^log2(o)
-                        const float f = my_comp == 5 ? ex2_approx(-r1.z) : comp_scale;
-                        atomicAdd(A.grad2d + 9 * (int64_t)g + my_comp, sum * f);
+                    // splats two at a time, back to front: q1 behind q2
+                    const int q1 = 31 - __clz(work);
+                    work &= ~(1u << q1);
+                    float va[9];
+                    const bool act1 = splat_terms(S, c + q1, px, py, rel_last, Gr, Gg, Gb, gTT, T,
+                                                  accum, va);
+                    const uint32_t b1 = __ballot_sync(0xffffffffu, act1);
+                    if (work) {
+                        const int q2 = 31 - __clz(work);
+                        work &= ~(1u << q2);
+                        float vb[9];
+                        const bool act2 = splat_terms(S, c + q2, px, py, rel_last, Gr, Gg, Gb,
+                                                      gTT, T, accum, vb);
+                        const uint32_t b2 = __ballot_sync(0xffffffffu, act2);
+                        if ((b1 | b2) == 0) continue;
+                        const float sum = reduce_scatter9x2(va, vb, lane);
+                        const bool first = lane < 16;
+                        if (my_comp2 >= 0 && (first ? b1 : b2)) {
+                            const int idx = c + (first ? q1 : q2);
+                            const int32_t g = S.gid[idx];
+                            // component 5 is d/d(opacity): divide by o = 2^log2(o)
+                            const float f = my_comp2 == 5 ? ex2_approx(-S.r1[idx].z) : comp_scale2;
+                            atomicAdd(A.grad2d + 9 * (int64_t)g + my_comp2, sum * f);
+                        }
+                    } else {
+                        if (b1 == 0) continue;
+                        const float sum = reduce_scatter9(va, lane);
+                        if (writer) {
+                            const int idx = c + q1;
+                            const int32_t g = S.gid[idx];
+                            const float f = my_comp == 5 ? ex2_approx(-S.r1[idx].z) : comp_scale;
+                            atomicAdd(A.grad2d + 9 * (int64_t)g + my_comp, sum * f);
+                        }
                     }
                 }
             }
