@@ -340,197 +340,217 @@ cudaError_t launch_project(const CamParams& cam, int64_t n, int sh_degree, const
 // ---------------------------------------------------------------------------
 // backward: nine screen-space derivatives -> 59 parameter gradients
 // ---------------------------------------------------------------------------
+// One thread per Gaussian.  The SH rows (12 K bytes each) dominate the traffic:
+// each warp copies the rows of its live Gaussians into shared memory with
+// contiguous loads, every lane turns its row into the SH gradient in place, and
+// the warp writes its 32 consecutive gradient rows (zeros for the others) with
+// contiguous stores.
+constexpr int kPbThreads = 128;
+
 template <int K>
-__global__ void __launch_bounds__(256) project_bwd_kernel(
+__global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
     CamParams cam, int64_t n, const float* __restrict__ means, const float* __restrict__ scales,
     const float4* __restrict__ quats, const float* __restrict__ sh,
     const int* __restrict__ tiles_touched, const float* __restrict__ grad2d,
     const uint8_t* __restrict__ touched, float* __restrict__ dmeans, float* __restrict__ dscales,
     float4* __restrict__ dquats, float* __restrict__ dopac, float* __restrict__ dsh) {
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    float* dshrow = dsh + (int64_t)i * (K * 3);
-    bool live = tiles_touched[i] > 0 && (touched == nullptr || touched[i] != 0);
-    float g[9];
-    if (live) {
-#pragma unroll
-        for (int r = 0; r < 9; ++r) g[r] = grad2d[9 * i + r];
-    }
-    if (!live) {
-        dmeans[3 * i] = dmeans[3 * i + 1] = dmeans[3 * i + 2] = 0.f;
-        dscales[3 * i] = dscales[3 * i + 1] = dscales[3 * i + 2] = 0.f;
-        dquats[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        dopac[i] = 0.f;
-        if constexpr ((K * 3) % 4 == 0) {
-            float4* d4 = reinterpret_cast<float4*>(dshrow);
-#pragma unroll
-            for (int j = 0; j < K * 3 / 4; ++j) d4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        } else {
-#pragma unroll
-            for (int j = 0; j < K * 3; ++j) dshrow[j] = 0.f;
-        }
-        return;
-    }
-    const float* V = cam.V;
-    float m[3] = {means[3 * i], means[3 * i + 1], means[3 * i + 2]};
-    float s[3] = {scales[3 * i], scales[3 * i + 1], scales[3 * i + 2]};
-    float4 q4 = quats[i];
+    constexpr int RW = K * 3;                       // floats per SH row
+    constexpr bool kVec = (RW % 4) == 0;            // rows of whole float4
+    __shared__ float srow[kPbThreads / 32][32 * RW];
+    __shared__ int slive[kPbThreads / 32][32];  // rank among the live lanes -> lane
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t wbase = (int64_t)blockIdx.x * kPbThreads + warp * 32;
+    const int64_t i = wbase + lane;
+    const bool in = i < n;
+    const bool live = in && tiles_touched[i] > 0 && (touched == nullptr || touched[i] != 0);
+    float* my = srow[warp];
 
-    // ---- forward recomputation (fp32) ----
-    float t[3];
-#pragma unroll
-    for (int r = 0; r < 3; ++r) t[r] = V[4 * r] * m[0] + V[4 * r + 1] * m[1] + V[4 * r + 2] * m[2] + V[4 * r + 3];
-    float qn = sqrtf(q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w);
-    float iqn = 1.f / qn;
-    float w = q4.x * iqn, x = q4.y * iqn, y = q4.z * iqn, z = q4.w * iqn;
-    float R[9] = {1.f - 2.f * (y * y + z * z), 2.f * (x * y - w * z), 2.f * (x * z + w * y),
-                  2.f * (x * y + w * z), 1.f - 2.f * (x * x + z * z), 2.f * (y * z - w * x),
-                  2.f * (x * z - w * y), 2.f * (y * z + w * x), 1.f - 2.f * (x * x + y * y)};
-    float tz = t[2], iz = 1.f / tz;
-    float u = t[0] * iz, v = t[1] * iz;
-    float j00 = cam.fx * iz, j11 = cam.fy * iz, j02 = -j00 * u, j12 = -j11 * v;
-    float T0[3], T1[3];
-#pragma unroll
-    for (int k = 0; k < 3; ++k) {
-        T0[k] = j00 * V[k] + j02 * V[8 + k];
-        T1[k] = j11 * V[4 + k] + j12 * V[8 + k];
-    }
-    // Sigma' = N N^T, N = A diag(s), A = T R
-    float A0[3], A1[3], n0[3], n1[3];
-#pragma unroll
-    for (int k = 0; k < 3; ++k) {
-        A0[k] = T0[0] * R[k] + T0[1] * R[3 + k] + T0[2] * R[6 + k];
-        A1[k] = T1[0] * R[k] + T1[1] * R[3 + k] + T1[2] * R[6 + k];
-        n0[k] = A0[k] * s[k];
-        n1[k] = A1[k] * s[k];
-    }
-    // nu = n0 x n1 = s0 s1 s2 S^-1 R^T (T0 x T1) and det Sigma' = |nu|^2 (see the forward)
-    float w0 = T0[1] * T1[2] - T0[2] * T1[1];
-    float w1 = T0[2] * T1[0] - T0[0] * T1[2];
-    float w2 = T0[0] * T1[1] - T0[1] * T1[0];
-    float nu[3] = {s[1] * s[2] * (R[0] * w0 + R[3] * w1 + R[6] * w2),
-                   s[0] * s[2] * (R[1] * w0 + R[4] * w1 + R[7] * w2),
-                   s[0] * s[1] * (R[2] * w0 + R[5] * w1 + R[8] * w2)};
-    float idet = 1.f / (nu[0] * nu[0] + nu[1] * nu[1] + nu[2] * nu[2]);
-    // dual basis of N's rows, M = Lambda N: m0 = (n1 x nu) / det, m1 = (nu x n0) / det;
-    // Lambda = M M^T.  Forming Lambda a_k through adj(Sigma') cancels for thin splats.
-    float m0[3] = {(n1[1] * nu[2] - n1[2] * nu[1]) * idet, (n1[2] * nu[0] - n1[0] * nu[2]) * idet,
-                   (n1[0] * nu[1] - n1[1] * nu[0]) * idet};
-    float m1[3] = {(nu[1] * n0[2] - nu[2] * n0[1]) * idet, (nu[2] * n0[0] - nu[0] * n0[2]) * idet,
-                   (nu[0] * n0[1] - nu[1] * n0[0]) * idet};
-    float L00 = m0[0] * m0[0] + m0[1] * m0[1] + m0[2] * m0[2];
-    float L01 = m0[0] * m1[0] + m0[1] * m1[1] + m0[2] * m1[2];
-    float L11 = m1[0] * m1[0] + m1[1] * m1[1] + m1[2] * m1[2];
-
-    // ---- conic -> Sigma' = N N^T -> N: dL/dN = 2 dSigma' N = -2 Lambda G M,
-    //      G = [[ga, gb/2], [gb/2, gc]] ----
-    float ga = g[2], gbh = 0.5f * g[3], gc = g[4];
-    // ---- N = A diag(s) -> ds, dA; A = T R -> dT, dR ----
-    float dT0[3] = {0.f, 0.f, 0.f}, dT1[3] = {0.f, 0.f, 0.f};
-    float ds[3], dR[9];
-#pragma unroll
-    for (int k = 0; k < 3; ++k) {
-        const float gm0 = ga * m0[k] + gbh * m1[k];
-        const float gm1 = gbh * m0[k] + gc * m1[k];
-        const float dn0 = -2.f * (L00 * gm0 + L01 * gm1);
-        const float dn1 = -2.f * (L01 * gm0 + L11 * gm1);
-        ds[k] = dn0 * A0[k] + dn1 * A1[k];
-        const float dA0 = dn0 * s[k], dA1 = dn1 * s[k];
-#pragma unroll
-        for (int r = 0; r < 3; ++r) {
-            dT0[r] += R[3 * r + k] * dA0;
-            dT1[r] += R[3 * r + k] * dA1;
-            dR[3 * r + k] = T0[r] * dA0 + T1[r] * dA1;
-        }
-    }
-
-    // ---- T = J W -> dJ; (mu', J) -> dt -> dm ----
-    float dj00 = dT0[0] * V[0] + dT0[1] * V[1] + dT0[2] * V[2];
-    float dj02 = dT0[0] * V[8] + dT0[1] * V[9] + dT0[2] * V[10];
-    float dj11 = dT1[0] * V[4] + dT1[1] * V[5] + dT1[2] * V[6];
-    float dj12 = dT1[0] * V[8] + dT1[1] * V[9] + dT1[2] * V[10];
-    float gmx = g[0], gmy = g[1];
-    float dtx = (gmx - dj02 * iz) * j00;
-    float dty = (gmy - dj12 * iz) * j11;
-    float dtz = -(gmx * j00 * u + gmy * j11 * v) - (dj00 * j00 + dj11 * j11) * iz +
-                2.f * (dj02 * j00 * u + dj12 * j11 * v) * iz;
-    float dm[3];
-#pragma unroll
-    for (int c = 0; c < 3; ++c) dm[c] = V[c] * dtx + V[4 + c] * dty + V[8 + c] * dtz;
-
-    // ---- R(w, x, y, z) -> normalised quaternion -> raw quaternion ----
-    float dw = -2.f * z * dR[1] + 2.f * y * dR[2] + 2.f * z * dR[3] - 2.f * x * dR[5] -
-               2.f * y * dR[6] + 2.f * x * dR[7];
-    float dx_ = 2.f * y * dR[1] + 2.f * z * dR[2] + 2.f * y * dR[3] - 4.f * x * dR[4] -
-                2.f * w * dR[5] + 2.f * z * dR[6] + 2.f * w * dR[7] - 4.f * x * dR[8];
-    float dy_ = -4.f * y * dR[0] + 2.f * x * dR[1] + 2.f * w * dR[2] + 2.f * x * dR[3] +
-                2.f * z * dR[5] - 2.f * w * dR[6] + 2.f * z * dR[7] - 4.f * y * dR[8];
-    float dz_ = -4.f * z * dR[0] - 2.f * w * dR[1] + 2.f * x * dR[2] + 2.f * w * dR[3] -
-                4.f * z * dR[4] + 2.f * y * dR[5] + 2.f * x * dR[6] + 2.f * y * dR[7];
-    float dot = w * dw + x * dx_ + y * dy_ + z * dz_;
-    float4 dq = make_float4((dw - w * dot) * iqn, (dx_ - x * dot) * iqn, (dy_ - y * dot) * iqn,
-                            (dz_ - z * dot) * iqn);
-
-    // ---- colour -> SH coefficients and view direction ----
-    float ex = m[0] - cam.cw[0], ey = m[1] - cam.cw[1], ez = m[2] - cam.cw[2];
-    float ilen = rsqrtf(ex * ex + ey * ey + ez * ez);
-    float hx = ex * ilen, hy = ey * ilen, hz = ez * ilen;
-    float Y[16];
-    sh_values(hx, hy, hz, Y);
-    float gr = g[6], gg = g[7], gbl = g[8];
-    const float* row = sh + (int64_t)i * (K * 3);
-    float gdx = 0.f, gdy = 0.f, gdz = 0.f;
-    if constexpr ((K * 3) % 4 == 0) {
-        const float4* r4 = reinterpret_cast<const float4*>(row);
-        float4* d4 = reinterpret_cast<float4*>(dshrow);
-#pragma unroll
-        for (int gi = 0; gi < K / 4; ++gi) {
-            float4 v0 = __ldg(r4 + 3 * gi), v1 = __ldg(r4 + 3 * gi + 1), v2 = __ldg(r4 + 3 * gi + 2);
-            float c[12] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w, v2.x, v2.y, v2.z, v2.w};
-            float o[12];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                int k = 4 * gi + j;
-                o[3 * j] = Y[k] * gr;
-                o[3 * j + 1] = Y[k] * gg;
-                o[3 * j + 2] = Y[k] * gbl;
-                float p = gr * c[3 * j] + gg * c[3 * j + 1] + gbl * c[3 * j + 2];
-                float3 dY = sh_grad(k, hx, hy, hz);
-                gdx += p * dY.x;
-                gdy += p * dY.y;
-                gdz += p * dY.z;
-            }
-            d4[3 * gi] = make_float4(o[0], o[1], o[2], o[3]);
-            d4[3 * gi + 1] = make_float4(o[4], o[5], o[6], o[7]);
-            d4[3 * gi + 2] = make_float4(o[8], o[9], o[10], o[11]);
+    // ---- stage the live rows (others read as zero and are never used)
+    const uint32_t lmask = __ballot_sync(0xffffffffu, live);
+    if constexpr (kVec) {
+        constexpr int R4 = RW / 4;
+        const float4* sh4 = reinterpret_cast<const float4*>(sh);
+        float4* my4 = reinterpret_cast<float4*>(my);
+        const int nl = __popc(lmask);
+        if (live) slive[warp][__popc(lmask & ((1u << lane) - 1u))] = lane;
+        __syncwarp();
+        for (int f = lane; f < nl * R4; f += 32) {
+            const int rank = f / R4, col = f - rank * R4;
+            const int l = slive[warp][rank];
+            my4[l * R4 + col] = __ldg(sh4 + (wbase + l) * R4 + col);
         }
     } else {
+        if (live) {
+#pragma unroll
+            for (int j = 0; j < RW; ++j) my[lane * RW + j] = __ldg(sh + i * RW + j);
+        }
+    }
+    __syncwarp();
+
+    if (live) {
+        float g[9];
+#pragma unroll
+        for (int r = 0; r < 9; ++r) g[r] = grad2d[9 * i + r];
+        const float* V = cam.V;
+        float m[3] = {means[3 * i], means[3 * i + 1], means[3 * i + 2]};
+        float s[3] = {scales[3 * i], scales[3 * i + 1], scales[3 * i + 2]};
+        float4 q4 = quats[i];
+
+        // ---- forward recomputation (fp32) ----
+        float t[3];
+#pragma unroll
+        for (int r = 0; r < 3; ++r) t[r] = V[4 * r] * m[0] + V[4 * r + 1] * m[1] + V[4 * r + 2] * m[2] + V[4 * r + 3];
+        float qn = sqrtf(q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w);
+        float iqn = 1.f / qn;
+        float w = q4.x * iqn, x = q4.y * iqn, y = q4.z * iqn, z = q4.w * iqn;
+        float R[9] = {1.f - 2.f * (y * y + z * z), 2.f * (x * y - w * z), 2.f * (x * z + w * y),
+                      2.f * (x * y + w * z), 1.f - 2.f * (x * x + z * z), 2.f * (y * z - w * x),
+                      2.f * (x * z - w * y), 2.f * (y * z + w * x), 1.f - 2.f * (x * x + y * y)};
+        float tz = t[2], iz = 1.f / tz;
+        float u = t[0] * iz, v = t[1] * iz;
+        float j00 = cam.fx * iz, j11 = cam.fy * iz, j02 = -j00 * u, j12 = -j11 * v;
+        float T0[3], T1[3];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            T0[k] = j00 * V[k] + j02 * V[8 + k];
+            T1[k] = j11 * V[4 + k] + j12 * V[8 + k];
+        }
+        // Sigma' = N N^T, N = A diag(s), A = T R
+        float A0[3], A1[3], n0[3], n1[3];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            A0[k] = T0[0] * R[k] + T0[1] * R[3 + k] + T0[2] * R[6 + k];
+            A1[k] = T1[0] * R[k] + T1[1] * R[3 + k] + T1[2] * R[6 + k];
+            n0[k] = A0[k] * s[k];
+            n1[k] = A1[k] * s[k];
+        }
+        // nu = n0 x n1 = s0 s1 s2 S^-1 R^T (T0 x T1) and det Sigma' = |nu|^2 (see the forward)
+        float w0 = T0[1] * T1[2] - T0[2] * T1[1];
+        float w1 = T0[2] * T1[0] - T0[0] * T1[2];
+        float w2 = T0[0] * T1[1] - T0[1] * T1[0];
+        float nu[3] = {s[1] * s[2] * (R[0] * w0 + R[3] * w1 + R[6] * w2),
+                       s[0] * s[2] * (R[1] * w0 + R[4] * w1 + R[7] * w2),
+                       s[0] * s[1] * (R[2] * w0 + R[5] * w1 + R[8] * w2)};
+        float idet = 1.f / (nu[0] * nu[0] + nu[1] * nu[1] + nu[2] * nu[2]);
+        // dual basis of N's rows, M = Lambda N: m0 = (n1 x nu) / det, m1 = (nu x n0) / det;
+        // Lambda = M M^T.  Forming Lambda a_k through adj(Sigma') cancels for thin splats.
+        float m0[3] = {(n1[1] * nu[2] - n1[2] * nu[1]) * idet, (n1[2] * nu[0] - n1[0] * nu[2]) * idet,
+                       (n1[0] * nu[1] - n1[1] * nu[0]) * idet};
+        float m1[3] = {(nu[1] * n0[2] - nu[2] * n0[1]) * idet, (nu[2] * n0[0] - nu[0] * n0[2]) * idet,
+                       (nu[0] * n0[1] - nu[1] * n0[0]) * idet};
+        float L00 = m0[0] * m0[0] + m0[1] * m0[1] + m0[2] * m0[2];
+        float L01 = m0[0] * m1[0] + m0[1] * m1[1] + m0[2] * m1[2];
+        float L11 = m1[0] * m1[0] + m1[1] * m1[1] + m1[2] * m1[2];
+
+        // ---- conic -> Sigma' = N N^T -> N: dL/dN = 2 dSigma' N = -2 Lambda G M,
+        //      G = [[ga, gb/2], [gb/2, gc]] ----
+        float ga = g[2], gbh = 0.5f * g[3], gc = g[4];
+        // ---- N = A diag(s) -> ds, dA; A = T R -> dT, dR ----
+        float dT0[3] = {0.f, 0.f, 0.f}, dT1[3] = {0.f, 0.f, 0.f};
+        float ds[3], dR[9];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const float gm0 = ga * m0[k] + gbh * m1[k];
+            const float gm1 = gbh * m0[k] + gc * m1[k];
+            const float dn0 = -2.f * (L00 * gm0 + L01 * gm1);
+            const float dn1 = -2.f * (L01 * gm0 + L11 * gm1);
+            ds[k] = dn0 * A0[k] + dn1 * A1[k];
+            const float dA0 = dn0 * s[k], dA1 = dn1 * s[k];
+#pragma unroll
+            for (int r = 0; r < 3; ++r) {
+                dT0[r] += R[3 * r + k] * dA0;
+                dT1[r] += R[3 * r + k] * dA1;
+                dR[3 * r + k] = T0[r] * dA0 + T1[r] * dA1;
+            }
+        }
+
+        // ---- T = J W -> dJ; (mu', J) -> dt -> dm ----
+        float dj00 = dT0[0] * V[0] + dT0[1] * V[1] + dT0[2] * V[2];
+        float dj02 = dT0[0] * V[8] + dT0[1] * V[9] + dT0[2] * V[10];
+        float dj11 = dT1[0] * V[4] + dT1[1] * V[5] + dT1[2] * V[6];
+        float dj12 = dT1[0] * V[8] + dT1[1] * V[9] + dT1[2] * V[10];
+        float gmx = g[0], gmy = g[1];
+        float dtx = (gmx - dj02 * iz) * j00;
+        float dty = (gmy - dj12 * iz) * j11;
+        float dtz = -(gmx * j00 * u + gmy * j11 * v) - (dj00 * j00 + dj11 * j11) * iz +
+                    2.f * (dj02 * j00 * u + dj12 * j11 * v) * iz;
+        float dm[3];
+#pragma unroll
+        for (int c = 0; c < 3; ++c) dm[c] = V[c] * dtx + V[4 + c] * dty + V[8 + c] * dtz;
+
+        // ---- R(w, x, y, z) -> normalised quaternion -> raw quaternion ----
+        float dw = -2.f * z * dR[1] + 2.f * y * dR[2] + 2.f * z * dR[3] - 2.f * x * dR[5] -
+                   2.f * y * dR[6] + 2.f * x * dR[7];
+        float dx_ = 2.f * y * dR[1] + 2.f * z * dR[2] + 2.f * y * dR[3] - 4.f * x * dR[4] -
+                    2.f * w * dR[5] + 2.f * z * dR[6] + 2.f * w * dR[7] - 4.f * x * dR[8];
+        float dy_ = -4.f * y * dR[0] + 2.f * x * dR[1] + 2.f * w * dR[2] + 2.f * x * dR[3] +
+                    2.f * z * dR[5] - 2.f * w * dR[6] + 2.f * z * dR[7] - 4.f * y * dR[8];
+        float dz_ = -4.f * z * dR[0] - 2.f * w * dR[1] + 2.f * x * dR[2] + 2.f * w * dR[3] -
+                    4.f * z * dR[4] + 2.f * y * dR[5] + 2.f * x * dR[6] + 2.f * y * dR[7];
+        float dot = w * dw + x * dx_ + y * dy_ + z * dz_;
+        float4 dq = make_float4((dw - w * dot) * iqn, (dx_ - x * dot) * iqn, (dy_ - y * dot) * iqn,
+                                (dz_ - z * dot) * iqn);
+
+        // ---- colour -> SH coefficients (in place in the staged row) and view direction ----
+        float ex = m[0] - cam.cw[0], ey = m[1] - cam.cw[1], ez = m[2] - cam.cw[2];
+        float ilen = rsqrtf(ex * ex + ey * ey + ez * ez);
+        float hx = ex * ilen, hy = ey * ilen, hz = ez * ilen;
+        float Y[16];
+        sh_values(hx, hy, hz, Y);
+        float gr = g[6], gg = g[7], gbl = g[8];
+        float* row = my + lane * RW;
+        float gdx = 0.f, gdy = 0.f, gdz = 0.f;
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-            float c0 = __ldg(row + 3 * k), c1 = __ldg(row + 3 * k + 1), c2 = __ldg(row + 3 * k + 2);
-            dshrow[3 * k] = Y[k] * gr;
-            dshrow[3 * k + 1] = Y[k] * gg;
-            dshrow[3 * k + 2] = Y[k] * gbl;
-            float p = gr * c0 + gg * c1 + gbl * c2;
-            float3 dY = sh_grad(k, hx, hy, hz);
+            const float c0 = row[3 * k], c1 = row[3 * k + 1], c2 = row[3 * k + 2];
+            row[3 * k] = Y[k] * gr;
+            row[3 * k + 1] = Y[k] * gg;
+            row[3 * k + 2] = Y[k] * gbl;
+            const float p = gr * c0 + gg * c1 + gbl * c2;
+            const float3 dY = sh_grad(k, hx, hy, hz);
             gdx += p * dY.x;
             gdy += p * dY.y;
             gdz += p * dY.z;
         }
-    }
-    float dd = hx * gdx + hy * gdy + hz * gdz;
-    dm[0] += (gdx - hx * dd) * ilen;
-    dm[1] += (gdy - hy * dd) * ilen;
-    dm[2] += (gdz - hz * dd) * ilen;
+        float dd = hx * gdx + hy * gdy + hz * gdz;
+        dm[0] += (gdx - hx * dd) * ilen;
+        dm[1] += (gdy - hy * dd) * ilen;
+        dm[2] += (gdz - hz * dd) * ilen;
 
-    dmeans[3 * i] = dm[0];
-    dmeans[3 * i + 1] = dm[1];
-    dmeans[3 * i + 2] = dm[2];
-    dscales[3 * i] = ds[0];
-    dscales[3 * i + 1] = ds[1];
-    dscales[3 * i + 2] = ds[2];
-    dquats[i] = dq;
-    dopac[i] = g[5];
+        dmeans[3 * i] = dm[0];
+        dmeans[3 * i + 1] = dm[1];
+        dmeans[3 * i + 2] = dm[2];
+        dscales[3 * i] = ds[0];
+        dscales[3 * i + 1] = ds[1];
+        dscales[3 * i + 2] = ds[2];
+        dquats[i] = dq;
+        dopac[i] = g[5];
+    } else if (in) {
+        dmeans[3 * i] = dmeans[3 * i + 1] = dmeans[3 * i + 2] = 0.f;
+        dscales[3 * i] = dscales[3 * i + 1] = dscales[3 * i + 2] = 0.f;
+        dquats[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        dopac[i] = 0.f;
+    }
+    __syncwarp();
+
+    // ---- the warp's gradient rows, contiguous (zeros for the rows not live)
+    const int nrows = (int)min64(32, n - wbase);
+    if (nrows <= 0) return;
+    if constexpr (kVec) {
+        constexpr int R4 = RW / 4;
+        const float4* my4 = reinterpret_cast<const float4*>(my);
+        float4* d4 = reinterpret_cast<float4*>(dsh) + wbase * R4;
+        for (int f = lane; f < nrows * R4; f += 32) {
+            const int l = f / R4;
+            d4[f] = ((lmask >> l) & 1u) ? my4[f] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    } else {
+        float* d = dsh + wbase * RW;
+        for (int f = lane; f < nrows * RW; f += 32) {
+            const int l = f / RW;
+            d[f] = ((lmask >> l) & 1u) ? my[f] : 0.f;
+        }
+    }
 }
 
 cudaError_t launch_project_bwd(const CamParams& cam, int64_t n, int sh_degree, const float* means,
@@ -540,7 +560,7 @@ cudaError_t launch_project_bwd(const CamParams& cam, int64_t n, int sh_degree, c
                                float* dquats, float* dopacities, float* dsh, cudaStream_t st) {
     (void)opacities;
     if (n == 0) return cudaSuccess;
-    dim3 block(256), grid((unsigned)((n + 255) / 256));
+    dim3 block(kPbThreads), grid((unsigned)((n + kPbThreads - 1) / kPbThreads));
     auto q4 = reinterpret_cast<const float4*>(quats);
     auto dq4 = reinterpret_cast<float4*>(dquats);
     switch (sh_degree) {
