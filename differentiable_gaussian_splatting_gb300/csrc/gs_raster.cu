@@ -576,161 +576,187 @@ __device__ __forceinline__ float conic_scale(int comp) {
     return (comp == 2 || comp == 4) ? -0.5f : (comp == 3 ? -1.f : 1.f);
 }
 
-// One splat of the back-to-front walk for the calling lane's pixel: recovers
-// the transmittance in front of it, updates the colour behind, and returns
-// whether the pixel blended it; v gets its nine screen-space terms (all zero
-// when it did not), the conic ones without their constant factors.
-__device__ __forceinline__ bool splat_terms(const Smem& S, int idx, float px, float py, int rel_last,
-                                            float Gr, float Gg, float Gb, float gTT, float& T,
-                                            float& accum, float v[9]) {
-    const float4 r0 = S.r0[idx], r1 = S.r1[idx], r2 = S.r2[idx];
-    const float dx = rsub(px, r0.x), dy = rsub(py, r0.y);
-    float u1, u2;
-    const float qv = quad_q(r0.z, r0.w, r1.x, dx, dy, &u1, &u2);
-    const bool act = (qv <= r1.y) && idx <= rel_last;
+// ---------------------------------------------------------------------------
+// The backward kernel ("What the 3DGS Literature Left on the Table", Step 6.1,
+// 6.2): every warp owns one 8 x 8 quadrant of a tile, two vertically adjacent
+// pixels per lane (lane l: column l & 7, rows 2 (l >> 3) and 2 (l >> 3) + 1),
+// and walks the tile's list back to front on its own -- no block barrier --
+// from its last blended splat, staging in a private 32-splat slice only the
+// splats the forward's contributor mask marks for its quadrant.
+// ---------------------------------------------------------------------------
+constexpr int kBwdWarps = 4;
+constexpr int kBwdThreads = 32 * kBwdWarps;
+
+struct BwdSlice {
+    float4 r0[32], r1[32], r2[32];
+    int32_t gid[32];
+};
+
+// forward thread of tile pixel (lx, ly): the forward's warps cover 8 x 4 pixels
+__device__ __forceinline__ int fwd_thread(int lx, int ly) {
+    return 32 * ((lx >> 3) + 2 * (ly >> 2)) + (lx & 7) + 8 * (ly & 3);
+}
+
+// the back-to-front state of one pixel
+struct BwdPixel {
+    float T, accum, Gr, Gg, Gb, gTT;
+};
+
+// One row of one splat: recovers the transmittance in front of the splat,
+// updates the colour behind it; returns whether the pixel blended it and its
+// log-alpha derivative gs (zero when it did not or the clamp was active).
+__device__ __forceinline__ bool row_step(const float4& r0, const float4& r1, const float4& r2,
+                                         float dx, float dy, bool in_range, BwdPixel& P,
+                                         float* u1, float* u2, float* gs, float* wgt) {
+    const float qv = quad_q(r0.z, r0.w, r1.x, dx, dy, u1, u2);
+    const bool act = (qv <= r1.y) && in_range;
     const float araw = ex2_approx(fmaf(qv, kNegHalfLog2e, r1.z));
     float alpha = fminf(araw, kAlphaMax);
     alpha = act ? alpha : 0.f;
     const float inv = __fdividef(1.f, 1.f - alpha);
-    const float Tb = T * inv;
-    const float wgt = alpha * Tb;
-    const float cG = r2.x * Gr + r2.y * Gg + r2.z * Gb;
-    const float dalpha = Tb * cG - (accum + gTT) * inv;
-    accum = fmaf(cG, wgt, accum);
-    const float gs = (act && araw < kAlphaMax) ? araw * dalpha : 0.f;
-    T = act ? Tb : T;
-    // conic of the evaluated quadratic: a = l11^2, b = l11 l12, c = l12^2 + l22^2,
-    // so a dx + b dy = l11 u1 and b dx + c dy = l12 u1 + l22 u2
-    const float gdx = gs * dx;
-    v[0] = gs * (r0.z * u1);
-    v[1] = gs * fmaf(r0.w, u1, r1.x * u2);
-    v[2] = gdx * dx;
-    v[3] = gdx * dy;
-    v[4] = (gs * dy) * dy;
-    v[5] = gs;
-    v[6] = wgt * Gr;
-    v[7] = wgt * Gg;
-    v[8] = wgt * Gb;
+    const float Tb = P.T * inv;
+    const float w = alpha * Tb;
+    const float cG = r2.x * P.Gr + r2.y * P.Gg + r2.z * P.Gb;
+    const float dalpha = Tb * cG - (P.accum + P.gTT) * inv;
+    P.accum = fmaf(cG, w, P.accum);
+    *gs = (act && araw < kAlphaMax) ? araw * dalpha : 0.f;
+    *wgt = w;
+    P.T = act ? Tb : P.T;
     return act;
 }
 
-__global__ void __launch_bounds__(kThreads) raster_bwd_kernel(RasterArgs A) {
-    __shared__ Smem S;
-    __shared__ int s_last;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// One splat for the lane's two pixels; v gets the sum of their nine terms
+// (conic ones without their constant factors).  Conic of the evaluated
+// quadratic: a = l11^2, b = l11 l12, c = l12^2 + l22^2, so a dx + b dy = l11 u1
+// and b dx + c dy = l12 u1 + l22 u2.
+__device__ __forceinline__ bool splat_terms2(const BwdSlice& S, int q, float px, float py0,
+                                             float py1, int rel0, int rel1, BwdPixel& P0,
+                                             BwdPixel& P1, float v[9]) {
+    const float4 r0 = S.r0[q], r1 = S.r1[q], r2 = S.r2[q];
+    const float dx = rsub(px, r0.x);
+    const float dy0 = rsub(py0, r0.y), dy1 = rsub(py1, r0.y);
+    float a0, b0, a1, b1, g0, g1, w0, w1;
+    const bool act0 = row_step(r0, r1, r2, dx, dy0, q <= rel0, P0, &a0, &b0, &g0, &w0);
+    const bool act1 = row_step(r0, r1, r2, dx, dy1, q <= rel1, P1, &a1, &b1, &g1, &w1);
+    v[0] = fmaf(g1, r0.z * a1, g0 * (r0.z * a0));
+    v[1] = fmaf(g1, fmaf(r0.w, a1, r1.x * b1), g0 * fmaf(r0.w, a0, r1.x * b0));
+    const float gdx0 = g0 * dx, gdx1 = g1 * dx;
+    v[2] = fmaf(gdx1, dx, gdx0 * dx);
+    v[3] = fmaf(gdx1, dy1, gdx0 * dy0);
+    v[4] = fmaf(g1 * dy1, dy1, (g0 * dy0) * dy0);
+    v[5] = g0 + g1;
+    v[6] = fmaf(w1, P1.Gr, w0 * P0.Gr);
+    v[7] = fmaf(w1, P1.Gg, w0 * P0.Gg);
+    v[8] = fmaf(w1, P1.Gb, w0 * P0.Gb);
+    return act0 || act1;
+}
+
+__device__ __forceinline__ void load_bwd_pixel(const RasterArgs& A, const WorkItem& it, int x, int y,
+                                               int lx, int ly, BwdPixel& P, int& last) {
+    P = BwdPixel{1.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    last = -1;
+    if (x >= A.W || y >= A.H) return;
+    const int64_t p = (int64_t)y * A.W + x;
+    last = A.last_in[p];
+    const float Tfin = A.t_final_in[p];
+    P.Gr = A.dimg[3 * p];
+    P.Gg = A.dimg[3 * p + 1];
+    P.Gb = A.dimg[3 * p + 2];
+    P.gTT = A.dT ? A.dT[p] * Tfin : 0.f;
+    if (it.slot < 0) {
+        P.T = Tfin;
+    } else {
+        const int64_t slotp =
+            ((int64_t)it.slot * kMaxChunks + it.chunk) * kThreads + fwd_thread(lx, ly);
+        const float4 b = A.bstate[slotp];
+        P.T = b.x;
+        P.accum = b.y * P.Gr + b.z * P.Gg + b.w * P.Gb;
+    }
+}
+
+__global__ void __launch_bounds__(kBwdThreads) raster_bwd_kernel(RasterArgs A) {
+    __shared__ BwdSlice SL[kBwdWarps];
+    const unsigned F = 0xffffffffu;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    BwdSlice& S = SL[warp];
     const int h = A.ctrl[kCtlH], k = A.ctrl[kCtlK], nitems = A.ctrl[kCtlItems];
+    const int nunits = 4 * nitems;  // (work item, quadrant)
     const int my_comp = comp_of_lane(lane);
     const bool writer = !(lane & 1) && my_comp >= 0;
     const int my_comp2 = comp16_of_lane(lane & 15);
     // the conic components are summed without their constant factors
     // (-1/2 dx^2, -dx dy, -1/2 dy^2), applied once by the writing lane
     const float comp_scale = conic_scale(my_comp), comp_scale2 = conic_scale(my_comp2);
-    int lx, ly;
-    tile_pixel(tid, &lx, &ly);
+    const int col = lane & 7, rp = lane >> 3;
     while (true) {
-        if (tid == 0) {
-            S.item = atomicAdd(A.ctrl + kCtlQueueBwd, 1);
-            s_last = -1;
-        }
-        __syncthreads();
-        const int item = S.item;
-        if (item >= nitems) break;
-        const WorkItem it = decode_item(A, item, h, k);
+        int unit = 0;
+        if (lane == 0) unit = atomicAdd(A.ctrl + kCtlQueueBwd, 1);
+        unit = __shfl_sync(F, unit, 0);
+        if (unit >= nunits) break;
+        const int quad = unit & 3;
+        const WorkItem it = decode_item(A, unit >> 2, h, k);
         const int tx = it.tile % A.ntx, ty = it.tile / A.ntx;
-        const int x = tx * kTile + lx, y = ty * kTile + ly;
-        const bool inside = x < A.W && y < A.H;
-        const float px = (float)x + 0.5f, py = (float)y + 0.5f;
-        int last = -1;
-        float T = 1.f, accum = 0.f, Gr = 0.f, Gg = 0.f, Gb = 0.f, gTT = 0.f;
-        if (inside) {
-            const int64_t p = (int64_t)y * A.W + x;
-            last = A.last_in[p];
-            const float Tfin = A.t_final_in[p];
-            Gr = A.dimg[3 * p];
-            Gg = A.dimg[3 * p + 1];
-            Gb = A.dimg[3 * p + 2];
-            gTT = A.dT ? A.dT[p] * Tfin : 0.f;
-            if (it.slot < 0) {
-                T = Tfin;
-            } else {
-                const int64_t slotp =
-                    ((int64_t)it.slot * kMaxChunks + it.chunk) * kThreads + tid;
-                const float4 b = A.bstate[slotp];
-                T = b.x;
-                accum = b.y * Gr + b.z * Gg + b.w * Gb;
-            }
-        }
-        // last list position any pixel of this item needs
-        const int mylast = (int)min64((int64_t)last, it.e - 1);
-        int wlast = mylast;
+        const int lx = 8 * (quad & 1) + col, ly0 = 8 * (quad >> 1) + 2 * rp;
+        const int x = tx * kTile + lx, y0 = ty * kTile + ly0;
+        const float px = (float)x + 0.5f, py0 = (float)y0 + 0.5f, py1 = (float)(y0 + 1) + 0.5f;
+        BwdPixel P0, P1;
+        int last0, last1;
+        load_bwd_pixel(A, it, x, y0, lx, ly0, P0, last0);
+        load_bwd_pixel(A, it, x, y0 + 1, lx, ly0 + 1, P1, last1);
+        // the quadrant's two forward sub-tiles (8 x 4 each) in the contributor mask
+        const int w0 = (quad & 1) + 4 * (quad >> 1);
+        const uint32_t qmask = (1u << w0) | (1u << (w0 + 2));
+        int wlast = max((int)min64((int64_t)last0, it.e - 1), (int)min64((int64_t)last1, it.e - 1));
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) wlast = max(wlast, __shfl_xor_sync(0xffffffffu, wlast, o));
-        if (lane == 0 && wlast >= 0) atomicMax(&s_last, wlast);
-        __syncthreads();
-        const int64_t hi = (int64_t)s_last + 1;
-        __syncthreads();
-        for (int64_t be = hi; be > it.s; be -= kBatch) {
-            const int64_t bs = max64(it.s, be - kBatch);
-            const int nb = (int)(be - bs);
-            if (tid < nb) {
-                // the forward's contributor mask: warps that blended this splat
-                const uint8_t cm = A.cmask[bs + tid];
-                S.mask[tid] = cm;
-                if (cm) {
-                    const int32_t g = __ldg(A.ids + bs + tid);
-                    S.r0[tid] = __ldg(A.splats + 3 * (int64_t)g);
-                    S.r1[tid] = __ldg(A.splats + 3 * (int64_t)g + 1);
-                    S.r2[tid] = __ldg(A.splats + 3 * (int64_t)g + 2);
-                    S.gid[tid] = g;
-                    if (A.touched) A.touched[g] = 1;  // it blended into some pixel
-                }
+        for (int o = 16; o > 0; o >>= 1) wlast = max(wlast, __shfl_xor_sync(F, wlast, o));
+        for (int64_t ce = (int64_t)wlast + 1; ce > it.s; ce -= 32) {
+            const int64_t cs = max64(it.s, ce - 32);
+            const int n = (int)(ce - cs);
+            const bool bit = lane < n && (A.cmask[cs + lane] & qmask) != 0;
+            uint32_t work = __ballot_sync(F, bit);
+            if (bit) {
+                const int32_t g = __ldg(A.ids + cs + lane);
+                S.r0[lane] = __ldg(A.splats + 3 * (int64_t)g);
+                S.r1[lane] = __ldg(A.splats + 3 * (int64_t)g + 1);
+                S.r2[lane] = __ldg(A.splats + 3 * (int64_t)g + 2);
+                S.gid[lane] = g;
+                if (A.touched) A.touched[g] = 1;  // it blended into some pixel
             }
-            __syncthreads();
-            for (int c = ((nb - 1) >> 5) << 5; c >= 0; c -= 32) {
-                const int jj = c + lane;
-                uint32_t bit = jj < nb ? (S.mask[jj] >> warp) & 1u : 0u;
-                if (bs + jj > wlast) bit = 0;
-                uint32_t work = __ballot_sync(0xffffffffu, bit);
-                // list positions fit in 32 bits (the pair capacity is below 2^31)
-                const int rel_last = last - (int)bs;
-                while (work) {
-                    // splats two at a time, back to front: q1 behind q2
-                    const int q1 = 31 - __clz(work);
-                    work &= ~(1u << q1);
-                    float va[9];
-                    const bool act1 = splat_terms(S, c + q1, px, py, rel_last, Gr, Gg, Gb, gTT, T,
-                                                  accum, va);
-                    const uint32_t b1 = __ballot_sync(0xffffffffu, act1);
-                    if (work) {
-                        const int q2 = 31 - __clz(work);
-                        work &= ~(1u << q2);
-                        float vb[9];
-                        const bool act2 = splat_terms(S, c + q2, px, py, rel_last, Gr, Gg, Gb,
-                                                      gTT, T, accum, vb);
-                        const uint32_t b2 = __ballot_sync(0xffffffffu, act2);
-                        if ((b1 | b2) == 0) continue;
-                        const float sum = reduce_scatter9x2(va, vb, lane);
-                        const bool first = lane < 16;
-                        if (my_comp2 >= 0 && (first ? b1 : b2)) {
-                            const int idx = c + (first ? q1 : q2);
-                            const int32_t g = S.gid[idx];
-                            // component 5 is d/d(opacity): divide by o = 2^log2(o)
-                            const float f = my_comp2 == 5 ? ex2_approx(-S.r1[idx].z) : comp_scale2;
-                            atomicAdd(A.grad2d + 9 * (int64_t)g + my_comp2, sum * f);
-                        }
-                    } else {
-                        if (b1 == 0) continue;
-                        const float sum = reduce_scatter9(va, lane);
-                        if (writer) {
-                            const int idx = c + q1;
-                            const int32_t g = S.gid[idx];
-                            const float f = my_comp == 5 ? ex2_approx(-S.r1[idx].z) : comp_scale;
-                            atomicAdd(A.grad2d + 9 * (int64_t)g + my_comp, sum * f);
-                        }
+            __syncwarp();
+            // list positions fit in 32 bits (the pair capacity is below 2^31)
+            const int rel0 = last0 - (int)cs, rel1 = last1 - (int)cs;
+            while (work) {
+                // splats two at a time, back to front: q1 behind q2
+                const int q1 = 31 - __clz(work);
+                work &= ~(1u << q1);
+                float va[9];
+                const bool act1 = splat_terms2(S, q1, px, py0, py1, rel0, rel1, P0, P1, va);
+                const uint32_t b1 = __ballot_sync(F, act1);
+                if (work) {
+                    const int q2 = 31 - __clz(work);
+                    work &= ~(1u << q2);
+                    float vb[9];
+                    const bool act2 = splat_terms2(S, q2, px, py0, py1, rel0, rel1, P0, P1, vb);
+                    const uint32_t b2 = __ballot_sync(F, act2);
+                    if ((b1 | b2) == 0) continue;
+                    const float sum = reduce_scatter9x2(va, vb, lane);
+                    const bool first = lane < 16;
+                    if (my_comp2 >= 0 && (first ? b1 : b2)) {
+                        const int q = first ? q1 : q2;
+                        // component 5 is d/d(opacity): divide by o = 2^log2(o)
+                        const float f = my_comp2 == 5 ? ex2_approx(-S.r1[q].z) : comp_scale2;
+                        atomicAdd(A.grad2d + 9 * (int64_t)S.gid[q] + my_comp2, sum * f);
+                    }
+                } else {
+                    if (b1 == 0) continue;
+                    const float sum = reduce_scatter9(va, lane);
+                    if (writer) {
+                        const float f = my_comp == 5 ? ex2_approx(-S.r1[q1].z) : comp_scale;
+                        atomicAdd(A.grad2d + 9 * (int64_t)S.gid[q1] + my_comp, sum * f);
                     }
                 }
             }
-            __syncthreads();
+            __syncwarp();
         }
     }
 }
@@ -748,7 +774,7 @@ int raster_resident_ctas(int device) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, raster_fwd_kernel, kThreads, 0);
         g_resident[device][0] = std::max(1, sms * std::max(per, 1));
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, raster_bwd_kernel, kThreads, 0);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, raster_bwd_kernel, kBwdThreads, 0);
         g_resident[device][1] = std::max(1, sms * std::max(per, 1));
     }
     return g_resident[device][0];
@@ -852,7 +878,7 @@ cudaError_t run_raster_bwd(const CamParams& cam, const RasterConfig& cfg, int64_
     }
     err = cudaMemsetAsync(A.ctrl + kCtlQueueBwd, 0, sizeof(int), st);
     if (err != cudaSuccess) return err;
-    raster_bwd_kernel<<<K, kThreads, 0, st>>>(A);
+    raster_bwd_kernel<<<K, kBwdThreads, 0, st>>>(A);
     return cudaGetLastError();
 }
 
