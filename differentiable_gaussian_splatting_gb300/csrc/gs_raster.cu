@@ -592,6 +592,37 @@ struct BwdSlice {
     int32_t gid[32];
 };
 
+// 16-byte asynchronous global -> shared copies (completion by cp_async_wait)
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Start staging list positions [cs, cs + n) for a quadrant into slice B: the
+// splats whose contributor mask has a bit of qmask.  Returns the warp's work
+// mask (bit q: position cs + q is staged); the copies complete at the next
+// cp_async_wait that covers this group.
+__device__ __forceinline__ uint32_t stage_slice(const RasterArgs& A, BwdSlice& B, int64_t cs, int n,
+                                                uint32_t qmask, int lane) {
+    const bool bit = lane < n && (A.cmask[cs + lane] & qmask) != 0;
+    if (bit) {
+        const int32_t g = __ldg(A.ids + cs + lane);
+        const float4* src = A.splats + 3 * (int64_t)g;
+        cp_async16(&B.r0[lane], src);
+        cp_async16(&B.r1[lane], src + 1);
+        cp_async16(&B.r2[lane], src + 2);
+        B.gid[lane] = g;
+        if (A.touched) A.touched[g] = 1;  // it blended into some pixel
+    }
+    cp_async_commit();
+    return __ballot_sync(0xffffffffu, bit);
+}
+
 // forward thread of tile pixel (lx, ly): the forward's warps cover 8 x 4 pixels
 __device__ __forceinline__ int fwd_thread(int lx, int ly) {
     return 32 * ((lx >> 3) + 2 * (ly >> 2)) + (lx & 7) + 8 * (ly & 3);
@@ -675,10 +706,9 @@ __device__ __forceinline__ void load_bwd_pixel(const RasterArgs& A, const WorkIt
 }
 
 __global__ void __launch_bounds__(kBwdThreads) raster_bwd_kernel(RasterArgs A) {
-    __shared__ BwdSlice SL[kBwdWarps];
+    __shared__ BwdSlice SL[kBwdWarps][2];  // double-buffered per warp
     const unsigned F = 0xffffffffu;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    BwdSlice& S = SL[warp];
     const int h = A.ctrl[kCtlH], k = A.ctrl[kCtlK], nitems = A.ctrl[kCtlItems];
     const int nunits = 4 * nitems;  // (work item, quadrant)
     const int my_comp = comp_of_lane(lane);
@@ -709,20 +739,25 @@ __global__ void __launch_bounds__(kBwdThreads) raster_bwd_kernel(RasterArgs A) {
         int wlast = max((int)min64((int64_t)last0, it.e - 1), (int)min64((int64_t)last1, it.e - 1));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) wlast = max(wlast, __shfl_xor_sync(F, wlast, o));
-        for (int64_t ce = (int64_t)wlast + 1; ce > it.s; ce -= 32) {
-            const int64_t cs = max64(it.s, ce - 32);
-            const int n = (int)(ce - cs);
-            const bool bit = lane < n && (A.cmask[cs + lane] & qmask) != 0;
-            uint32_t work = __ballot_sync(F, bit);
-            if (bit) {
-                const int32_t g = __ldg(A.ids + cs + lane);
-                S.r0[lane] = __ldg(A.splats + 3 * (int64_t)g);
-                S.r1[lane] = __ldg(A.splats + 3 * (int64_t)g + 1);
-                S.r2[lane] = __ldg(A.splats + 3 * (int64_t)g + 2);
-                S.gid[lane] = g;
-                if (A.touched) A.touched[g] = 1;  // it blended into some pixel
+        if ((int64_t)wlast + 1 <= it.s) continue;
+        // 32-position slices back to front; the next slice is staged while
+        // the current one is processed
+        int cur = 0;
+        int64_t cs = max64(it.s, (int64_t)wlast + 1 - 32);
+        uint32_t work = stage_slice(A, SL[warp][0], cs, (int)((int64_t)wlast + 1 - cs), qmask, lane);
+        while (true) {
+            const bool more = cs > it.s;
+            int64_t cs2 = 0;
+            uint32_t work2 = 0;
+            if (more) {
+                cs2 = max64(it.s, cs - 32);
+                work2 = stage_slice(A, SL[warp][cur ^ 1], cs2, (int)(cs - cs2), qmask, lane);
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
             }
             __syncwarp();
+            const BwdSlice& S = SL[warp][cur];
             // list positions fit in 32 bits (the pair capacity is below 2^31)
             const int rel0 = last0 - (int)cs, rel1 = last1 - (int)cs;
             while (work) {
@@ -756,7 +791,11 @@ __global__ void __launch_bounds__(kBwdThreads) raster_bwd_kernel(RasterArgs A) {
                     }
                 }
             }
-            __syncwarp();
+            __syncwarp();  // the slice is restaged two steps later
+            if (!more) break;
+            cs = cs2;
+            work = work2;
+            cur ^= 1;
         }
     }
 }
