@@ -43,8 +43,11 @@ constexpr int kBlockSortMax = 4096;  // keys one block sorts in shared memory
 constexpr int kCountStride = 16;   // ints
 constexpr int kCursorStride = 8;   // uint64
 
-// counts words (int64): M, I, min(I, capacity), raw pairs appended
+// counts words (int64): M, I, min(I, capacity), raw pairs appended, tiles of
+// kWarpSortMax + 1 .. kBlockSortMax pairs, tiles of more
 constexpr int kCountRaw = 3;
+constexpr int kCountMedium = 4;
+constexpr int kCountLarge = 5;
 
 // ---------------------------------------------------------------------------
 // 1. one pass over the Gaussians: raw (tile, Gaussian) pairs and tile counts
@@ -158,18 +161,10 @@ __global__ void __launch_bounds__(kEmitThreads) bucket_emit(CamParams cam,
 // cursors, I and min(I, capacity).  When I > capacity the list cannot be
 // built; every range is then empty, so nothing downstream reads it.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kScanThreads) bucket_scan(const int* __restrict__ tile_count,
-                                                            int64_t nt, int64_t capacity,
-                                                            int2* __restrict__ ranges,
-                                                            unsigned long long* __restrict__ cursor,
-                                                            int64_t* __restrict__ counts) {
-    __shared__ int64_t s_part[kScanThreads / 32];
+// exclusive block scan (kScanThreads threads) of one int64 per thread
+__device__ __forceinline__ int64_t scan_block_1024(int64_t v, int64_t* s_part, int64_t* total) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t per = (nt + kScanThreads - 1) / kScanThreads;
-    const int64_t lo = min64(nt, per * tid), hi = min64(nt, lo + per);
-    int64_t sum = 0;
-    for (int64_t t = lo; t < hi; ++t) sum += tile_count[t * kCountStride];
-    int64_t x = sum;
+    int64_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
@@ -187,18 +182,48 @@ __global__ void __launch_bounds__(kScanThreads) bucket_scan(const int* __restric
         s_part[lane] = w;
     }
     __syncthreads();
-    int64_t run = (warp > 0 ? s_part[warp - 1] : 0) + x - sum;
-    const bool fits = s_part[31] <= capacity;
+    const int64_t ex = (warp > 0 ? s_part[warp - 1] : 0) + x - v;
+    *total = s_part[31];
+    __syncthreads();
+    return ex;
+}
+
+__global__ void __launch_bounds__(kScanThreads) bucket_scan(const int* __restrict__ tile_count,
+                                                            int64_t nt, int64_t capacity,
+                                                            int2* __restrict__ ranges,
+                                                            unsigned long long* __restrict__ cursor,
+                                                            int32_t* __restrict__ medium,
+                                                            int32_t* __restrict__ large,
+                                                            int64_t* __restrict__ counts) {
+    __shared__ int64_t s_part[kScanThreads / 32];
+    const int tid = threadIdx.x;
+    const int64_t per = (nt + kScanThreads - 1) / kScanThreads;
+    const int64_t lo = min64(nt, per * tid), hi = min64(nt, lo + per);
+    int64_t sum = 0, nm = 0, nl = 0;
+    for (int64_t t = lo; t < hi; ++t) {
+        const int c = tile_count[t * kCountStride];
+        sum += c;
+        nm += c > kWarpSortMax && c <= kBlockSortMax;
+        nl += c > kBlockSortMax;
+    }
+    int64_t total, tm, tl;
+    int64_t run = scan_block_1024(sum, s_part, &total);
+    int64_t om = scan_block_1024(nm, s_part, &tm);
+    int64_t ol = scan_block_1024(nl, s_part, &tl);
+    const bool fits = total <= capacity;
     for (int64_t t = lo; t < hi; ++t) {
         const int c = tile_count[t * kCountStride];
         ranges[t] = fits ? make_int2((int)run, (int)(run + c)) : make_int2(0, 0);
         cursor[t * kCursorStride] = (unsigned long long)run;
         run += c;
+        if (c > kWarpSortMax && c <= kBlockSortMax) medium[om++] = (int32_t)t;
+        if (c > kBlockSortMax) large[ol++] = (int32_t)t;
     }
     if (tid == 0) {
-        const int64_t total = s_part[31];
         counts[1] = total;
-        counts[2] = total < capacity ? total : capacity;
+        counts[2] = fits ? total : capacity;
+        counts[kCountMedium] = fits ? tm : 0;
+        counts[kCountLarge] = fits ? tl : 0;
     }
 }
 
@@ -357,58 +382,69 @@ __global__ void __launch_bounds__(32 * kSmallWarps, 4) bucket_sort_small(const i
     }
 }
 
-// slices of kWarpSortMax + 1 .. kBlockSortMax keys: one block each, in shared
-// memory: the warps sort 512-key chunks, then block-wide merge-path rounds
+// Block-wide merge-path rounds in shared memory: runs of length L0 .. P / 2 in
+// src are merged pairwise until one run of P keys remains; returns its buffer.
+__device__ __forceinline__ uint64_t* block_merge_rounds(uint64_t* src, uint64_t* dst, int L0, int P) {
+    const int tid = threadIdx.x;
+    const int per = P / kSortThreads;  // outputs per thread
+    for (int L = L0; L < P; L <<= 1) {
+        const int o0 = tid * per;
+        const int p0 = (o0 / (2 * L)) * (2 * L);
+        const int k = o0 - p0;
+        int i = merge_split_s(src, p0, L, p0 + L, L, k), j = k - i;
+        for (int q = 0; q < per; ++q) {
+            const uint64_t va = i < L ? src[sk_idx(p0 + i)] : ~0ull;
+            const uint64_t vb = j < L ? src[sk_idx(p0 + L + j)] : ~0ull;
+            const bool ta = va < vb;
+            dst[sk_idx(o0 + q)] = ta ? va : vb;
+            i += ta;
+            j += !ta;
+        }
+        __syncthreads();
+        uint64_t* tmp = src;
+        src = dst;
+        dst = tmp;
+    }
+    return src;
+}
+
+// Sort P keys (P = 8 * 32 E, padded) in A: every warp sorts one chunk of 32 E
+// (its result lands in B: five warp rounds), then block-wide rounds.
+template <int E>
+__device__ __forceinline__ uint64_t* block_sort_keys(uint64_t* A, uint64_t* B) {
+    constexpr int kWarps = kSortThreads / 32;
+    constexpr int C = 32 * E;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    static_assert(kWarps == 8, "eight warps");
+    // chunk offsets are multiples of 16, so sk_idx is affine across them
+    warp_merge_sort<E>(A + sk_idx(warp * C), B + sk_idx(warp * C), lane);
+    __syncthreads();
+    return block_merge_rounds(B, A, C, kWarps * C);
+}
+
+// slices of kWarpSortMax + 1 .. kBlockSortMax keys: one block each, in shared memory
 __global__ void __launch_bounds__(kSortThreads) bucket_sort_medium(const int2* __restrict__ ranges,
-                                                                   int64_t nt,
+                                                                   const int32_t* __restrict__ list,
                                                                    const uint64_t* __restrict__ keys,
-                                                                   int32_t* __restrict__ sorted_ids) {
+                                                                   int32_t* __restrict__ sorted_ids,
+                                                                   const int64_t* __restrict__ counts) {
     extern __shared__ uint64_t smem[];
     uint64_t* A = smem;                            // sk_len(kBlockSortMax)
     uint64_t* B = smem + sk_len(kBlockSortMax);    // sk_len(kBlockSortMax)
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int kWarps = kSortThreads / 32;
-    for (int64_t t = blockIdx.x; t < nt; t += gridDim.x) {
-        const int2 r = ranges[t];
+    const int tid = threadIdx.x;
+    const int64_t nm = counts[kCountMedium];
+    for (int64_t m = blockIdx.x; m < nm; m += gridDim.x) {
+        const int2 r = ranges[list[m]];
         const int cnt = r.y - r.x;
-        if (cnt <= kWarpSortMax || cnt > kBlockSortMax) continue;
-        int P = kWarpSortMax;
+        int P = 2 * kWarpSortMax;
         while (P < cnt) P <<= 1;
         for (int e = tid; e < P; e += kSortThreads) A[sk_idx(e)] = e < cnt ? keys[r.x + e] : ~0ull;
         __syncthreads();
-        // chunks of 512: sorted by one warp each; chunk c's result lands in A
-        // or B at the same offsets (the pass count is fixed, so all in B)
-        for (int c = warp; c < P / kWarpSortMax; c += kWarps) {
-            const int c0 = c * kWarpSortMax;
-            // run the warp sort on the chunk through offset views of A and B:
-            // sk_idx is affine per 16 keys, and chunk offsets are multiples of 16
-            warp_merge_sort<16>(A + sk_idx(c0), B + sk_idx(c0), lane);
-        }
-        __syncthreads();
-        // five warp merge rounds (an odd count) leave every chunk in B
-        uint64_t* src = B;
-        uint64_t* dst = A;
-        for (int L = kWarpSortMax; L < P; L <<= 1) {
-            const int per = P / kSortThreads;      // outputs per thread (2 .. 16)
-            const int o0 = tid * per;
-            const int p0 = (o0 / (2 * L)) * (2 * L);
-            const int k = o0 - p0;
-            int i = merge_split_s(src, p0, L, p0 + L, L, k), j = k - i;
-            for (int q = 0; q < per; ++q) {
-                const uint64_t va = i < L ? src[sk_idx(p0 + i)] : ~0ull;
-                const uint64_t vb = j < L ? src[sk_idx(p0 + L + j)] : ~0ull;
-                const bool ta = va < vb;
-                dst[sk_idx(o0 + q)] = ta ? va : vb;
-                i += ta;
-                j += !ta;
-            }
-            __syncthreads();
-            uint64_t* tmp = src;
-            src = dst;
-            dst = tmp;
-        }
+        const uint64_t* out = P == 1024 ? block_sort_keys<4>(A, B)
+                              : P == 2048 ? block_sort_keys<8>(A, B)
+                                          : block_sort_keys<16>(A, B);
         for (int e = tid; e < cnt; e += kSortThreads)
-            sorted_ids[r.x + e] = (int32_t)(uint32_t)src[sk_idx(e)];
+            sorted_ids[r.x + e] = (int32_t)(uint32_t)out[sk_idx(e)];
         __syncthreads();
     }
 }
@@ -429,19 +465,19 @@ __device__ __forceinline__ int merge_split_g(const uint64_t* a, int na, const ui
 }
 
 __global__ void __launch_bounds__(kSortThreads) bucket_sort_large(const int2* __restrict__ ranges,
-                                                                  int64_t nt,
+                                                                  const int32_t* __restrict__ list,
                                                                   uint64_t* __restrict__ buf0,
                                                                   uint64_t* __restrict__ buf1,
-                                                                  int32_t* __restrict__ sorted_ids) {
+                                                                  int32_t* __restrict__ sorted_ids,
+                                                                  const int64_t* __restrict__ counts) {
     extern __shared__ uint64_t smem[];
     uint64_t* A = smem;
     uint64_t* B = smem + sk_len(kBlockSortMax);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int kWarps = kSortThreads / 32;
-    for (int64_t t = blockIdx.x; t < nt; t += gridDim.x) {
-        const int2 r = ranges[t];
+    const int tid = threadIdx.x;
+    const int64_t nl = counts[kCountLarge];
+    for (int64_t m = blockIdx.x; m < nl; m += gridDim.x) {
+        const int2 r = ranges[list[m]];
         const int cnt = r.y - r.x;
-        if (cnt <= kBlockSortMax) continue;
         const int64_t s = r.x;
         // sort chunks of kBlockSortMax in shared memory, written back to buf0
         for (int c0 = 0; c0 < cnt; c0 += kBlockSortMax) {
@@ -449,33 +485,8 @@ __global__ void __launch_bounds__(kSortThreads) bucket_sort_large(const int2* __
             for (int e = tid; e < kBlockSortMax; e += kSortThreads)
                 A[sk_idx(e)] = e < n ? buf0[s + c0 + e] : ~0ull;
             __syncthreads();
-            for (int c = warp; c < kBlockSortMax / kWarpSortMax; c += kWarps) {
-                const int w0 = c * kWarpSortMax;
-                warp_merge_sort<16>(A + sk_idx(w0), B + sk_idx(w0), lane);
-            }
-            __syncthreads();
-            uint64_t* src = B;
-            uint64_t* dst = A;
-            for (int L = kWarpSortMax; L < kBlockSortMax; L <<= 1) {
-                const int per = kBlockSortMax / kSortThreads;
-                const int o0 = tid * per;
-                const int p0 = (o0 / (2 * L)) * (2 * L);
-                const int k = o0 - p0;
-                int i = merge_split_s(src, p0, L, p0 + L, L, k), j = k - i;
-                for (int q = 0; q < per; ++q) {
-                    const uint64_t va = i < L ? src[sk_idx(p0 + i)] : ~0ull;
-                    const uint64_t vb = j < L ? src[sk_idx(p0 + L + j)] : ~0ull;
-                    const bool ta = va < vb;
-                    dst[sk_idx(o0 + q)] = ta ? va : vb;
-                    i += ta;
-                    j += !ta;
-                }
-                __syncthreads();
-                uint64_t* tmp = src;
-                src = dst;
-                dst = tmp;
-            }
-            for (int e = tid; e < n; e += kSortThreads) buf0[s + c0 + e] = src[sk_idx(e)];
+            const uint64_t* out = block_sort_keys<16>(A, B);
+            for (int e = tid; e < n; e += kSortThreads) buf0[s + c0 + e] = out[sk_idx(e)];
             __syncthreads();
         }
         uint64_t* src = buf0;
@@ -552,17 +563,28 @@ __global__ void __launch_bounds__(kLptRun / 2) lpt_sort_runs(const int2* __restr
     }
 }
 
-__global__ void lpt_merge(const uint64_t* __restrict__ runs, int64_t nt, int32_t* __restrict__ lpt) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+// rank of every key = its position in its run + the keys smaller than it in the
+// other runs; the runs are searched in shared memory when they fit
+constexpr int kLptSmemRuns = 6;
+__global__ void __launch_bounds__(256) lpt_merge(const uint64_t* __restrict__ runs, int64_t nt,
+                                                 int32_t* __restrict__ lpt) {
+    __shared__ uint64_t sr[kLptSmemRuns * kLptRun];
     const int64_t nruns = (nt + kLptRun - 1) / kLptRun;
+    const bool in_smem = nruns <= kLptSmemRuns;
+    if (in_smem) {
+        for (int64_t e = threadIdx.x; e < nruns * kLptRun; e += blockDim.x) sr[e] = runs[e];
+        __syncthreads();
+    }
+    const uint64_t* R = in_smem ? sr : runs;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= nruns * kLptRun) return;
-    const uint64_t key = runs[i];
+    const uint64_t key = R[i];
     if (key == ~0ull) return;  // padding
     const int64_t r = i / kLptRun;
     int64_t rank = i - r * kLptRun;
     for (int64_t r2 = 0; r2 < nruns; ++r2) {
         if (r2 == r) continue;
-        const uint64_t* run = runs + r2 * kLptRun;
+        const uint64_t* run = R + r2 * kLptRun;
         int lo = 0, hi = kLptRun;  // number of keys < key
         while (lo < hi) {
             const int mid = (lo + hi) >> 1;
@@ -594,6 +616,7 @@ BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles) {
     L.off_keys = take((size_t)cap * sizeof(uint64_t));
     L.off_tcount = take((size_t)nt * kCountStride * sizeof(int));
     L.off_cursor = take((size_t)nt * kCursorStride * sizeof(unsigned long long));
+    L.off_lists = take((size_t)nt * 2 * sizeof(int32_t));
     L.off_lruns = take((size_t)((nt + kLptRun - 1) / kLptRun) * kLptRun * sizeof(uint64_t));
     L.total = off;
     return L;
@@ -608,8 +631,10 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
     auto* keys = reinterpret_cast<uint64_t*>(ws + L.off_keys);
     auto* tcount = reinterpret_cast<int*>(ws + L.off_tcount);
     auto* cursor = reinterpret_cast<unsigned long long*>(ws + L.off_cursor);
+    auto* medium = reinterpret_cast<int32_t*>(ws + L.off_lists);
     auto* lruns = reinterpret_cast<uint64_t*>(ws + L.off_lruns);
     const int64_t nt = (int64_t)cam.ntx * cam.nty;
+    auto* large = medium + nt;
     auto* ranges = reinterpret_cast<int2*>(tile_ranges);
     cudaError_t err;
 
@@ -625,7 +650,8 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
         bucket_emit<<<(unsigned)((n + kEmitThreads - 1) / kEmitThreads), kEmitThreads, 0, st>>>(
             cam, reinterpret_cast<const float4*>(splats), tiles_touched, n, capacity, tcount, raw,
             counts);
-    bucket_scan<<<1, kScanThreads, 0, st>>>(tcount, nt, capacity, ranges, cursor, counts);
+    bucket_scan<<<1, kScanThreads, 0, st>>>(tcount, nt, capacity, ranges, cursor, medium, large,
+                                            counts);
     if (n > 0) {
         const unsigned grid = (unsigned)std::max<int64_t>(
             1, std::min<int64_t>((capacity + 255) / 256, 8 * (int64_t)sms));
@@ -641,11 +667,12 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
                                    (int)sbytes);
         if (err != cudaSuccess) return err;
         const unsigned mg = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nt, 3 * (int64_t)sms));
-        bucket_sort_medium<<<mg, kSortThreads, sbytes, st>>>(ranges, nt, keys, sorted_ids);
+        bucket_sort_medium<<<mg, kSortThreads, sbytes, st>>>(ranges, medium, keys, sorted_ids, counts);
         // the raw list is free again: it is the long slices' second merge buffer
         bucket_sort_large<<<(unsigned)std::max<int64_t>(1, std::min<int64_t>(nt, 2 * (int64_t)sms)),
-                            kSortThreads, sbytes, st>>>(ranges, nt, keys,
-                                                        reinterpret_cast<uint64_t*>(raw), sorted_ids);
+                            kSortThreads, sbytes, st>>>(ranges, large, keys,
+                                                        reinterpret_cast<uint64_t*>(raw), sorted_ids,
+                                                        counts);
     }
     // 5. LPT order: tiles by descending count, ties by tile id
     {

@@ -32,11 +32,12 @@ cudaError_t launch_project_bwd(const CamParams& cam, int64_t n, int sh_degree, c
 // ---- binning + sort (gs_binsort.cu) ---------------------------------------
 struct BinSortLayout {
     size_t total;
-    size_t off_counts;   // int64[8]: M, I, min(I, capacity), raw pairs appended, pad
+    size_t off_counts;   // int64[8]: M, I, min(I, capacity), raw pairs, medium / large tiles
     size_t off_raw;      // uint2[capacity]: raw (tile, Gaussian) pairs; later a merge buffer
     size_t off_keys;     // uint64[capacity]: the tiles' slices of (depth bits << 32 | id)
     size_t off_tcount;   // int32[n_tiles]: pairs per tile
     size_t off_cursor;   // uint64[n_tiles]: bucket cursors
+    size_t off_lists;    // int32[2 n_tiles]: tiles sorted by a block, then by merge rounds
     size_t off_lruns;    // uint64[n_tiles rounded up to 1024]: sorted runs of LPT keys
 };
 BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles);
