@@ -363,15 +363,8 @@ def step_roofline(ms, sc, M, I, E, H, W, peaks, n_sm, sm_mhz):
 
 def kernel_launches(n, capacity, W, H) -> int:
     """Kernels one step launches (memsets excluded)."""
-    nt = ((W + 15) // 16) * ((H + 15) // 16)
-
-    def passes(bits):
-        return max(1, (bits + 7) // 8)
-
-    tile_bits = max(1, int(nt - 1).bit_length())
-    # visible compaction 3, depth radix 3/pass, pair offsets 3, emit 1, tile radix 3/pass,
-    # tile ranges 2, LPT order 2
-    bin_sort = 3 + 3 * passes(31) + 3 + 1 + 3 * passes(tile_bits) + 2 + 2
+    # binning: span pass, scan, scatter, three slice sorts, two LPT kernels
+    bin_sort = 1 + 1 + 1 + 3 + 2
     # project 1, policy + forward 2, backward 1, project backward 1
     return 1 + bin_sort + 2 + 1 + 1
 
