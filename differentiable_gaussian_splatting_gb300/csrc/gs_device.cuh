@@ -45,6 +45,18 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// 16-byte asynchronous global -> shared copies; complete for the calling
+// thread after cp_async_wait<N> (all but the N most recent groups)
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ int to_int_clamped(float f, int lo, int hi) {
     if (!(f >= (float)lo)) return lo;
     if (f > (float)hi) return hi;

@@ -364,6 +364,19 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
     const bool in = i < n;
     const bool live = in && tiles_touched[i] > 0 && (touched == nullptr || touched[i] != 0);
     float* my = srow[warp];
+    // this lane's inputs, requested before the SH rows are staged
+    float g[9], m[3], s[3];
+    float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live) {
+#pragma unroll
+        for (int r = 0; r < 9; ++r) g[r] = grad2d[9 * i + r];
+#pragma unroll
+        for (int r = 0; r < 3; ++r) {
+            m[r] = means[3 * i + r];
+            s[r] = scales[3 * i + r];
+        }
+        q4 = quats[i];
+    }
 
     // ---- stage the live rows (others read as zero and are never used)
     const uint32_t lmask = __ballot_sync(0xffffffffu, live);
@@ -377,24 +390,21 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
         for (int f = lane; f < nl * R4; f += 32) {
             const int rank = f / R4, col = f - rank * R4;
             const int l = slive[warp][rank];
-            my4[l * R4 + col] = __ldg(sh4 + (wbase + l) * R4 + col);
+            cp_async16(&my4[l * R4 + col], sh4 + (wbase + l) * R4 + col);
         }
+        cp_async_commit();  // waited for after the geometric part below
     } else {
         if (live) {
 #pragma unroll
             for (int j = 0; j < RW; ++j) my[lane * RW + j] = __ldg(sh + i * RW + j);
         }
     }
-    __syncwarp();
 
+    // ---- the geometric part (no SH needed), while the SH rows arrive
+    float dm[3] = {0.f, 0.f, 0.f}, ds[3] = {0.f, 0.f, 0.f};
+    float4 dq = make_float4(0.f, 0.f, 0.f, 0.f);
     if (live) {
-        float g[9];
-#pragma unroll
-        for (int r = 0; r < 9; ++r) g[r] = grad2d[9 * i + r];
         const float* V = cam.V;
-        float m[3] = {means[3 * i], means[3 * i + 1], means[3 * i + 2]};
-        float s[3] = {scales[3 * i], scales[3 * i + 1], scales[3 * i + 2]};
-        float4 q4 = quats[i];
 
         // ---- forward recomputation (fp32) ----
         float t[3];
@@ -447,7 +457,7 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
         float ga = g[2], gbh = 0.5f * g[3], gc = g[4];
         // ---- N = A diag(s) -> ds, dA; A = T R -> dT, dR ----
         float dT0[3] = {0.f, 0.f, 0.f}, dT1[3] = {0.f, 0.f, 0.f};
-        float ds[3], dR[9];
+        float dR[9];
 #pragma unroll
         for (int k = 0; k < 3; ++k) {
             const float gm0 = ga * m0[k] + gbh * m1[k];
@@ -474,7 +484,6 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
         float dty = (gmy - dj12 * iz) * j11;
         float dtz = -(gmx * j00 * u + gmy * j11 * v) - (dj00 * j00 + dj11 * j11) * iz +
                     2.f * (dj02 * j00 * u + dj12 * j11 * v) * iz;
-        float dm[3];
 #pragma unroll
         for (int c = 0; c < 3; ++c) dm[c] = V[c] * dtx + V[4 + c] * dty + V[8 + c] * dtz;
 
@@ -488,9 +497,13 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
         float dz_ = -4.f * z * dR[0] - 2.f * w * dR[1] + 2.f * x * dR[2] + 2.f * w * dR[3] -
                     4.f * z * dR[4] + 2.f * y * dR[5] + 2.f * x * dR[6] + 2.f * y * dR[7];
         float dot = w * dw + x * dx_ + y * dy_ + z * dz_;
-        float4 dq = make_float4((dw - w * dot) * iqn, (dx_ - x * dot) * iqn, (dy_ - y * dot) * iqn,
-                                (dz_ - z * dot) * iqn);
+        dq = make_float4((dw - w * dot) * iqn, (dx_ - x * dot) * iqn, (dy_ - y * dot) * iqn,
+                         (dz_ - z * dot) * iqn);
+    }
+    if constexpr (kVec) cp_async_wait<0>();
+    __syncwarp();
 
+    if (live) {
         // ---- colour -> SH coefficients (in place in the staged row) and view direction ----
         float ex = m[0] - cam.cw[0], ey = m[1] - cam.cw[1], ez = m[2] - cam.cw[2];
         float ilen = rsqrtf(ex * ex + ey * ey + ez * ez);

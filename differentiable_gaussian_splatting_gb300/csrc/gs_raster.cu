@@ -592,17 +592,6 @@ struct BwdSlice {
     int32_t gid[32];
 };
 
-// 16-byte asynchronous global -> shared copies (completion by cp_async_wait)
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // Start staging list positions [cs, cs + n) for a quadrant into slice B: the
 // splats whose contributor mask has a bit of qmask.  Returns the warp's work
 // mask (bit q: position cs + q is staged); the copies complete at the next
