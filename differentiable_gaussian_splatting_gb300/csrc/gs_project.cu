@@ -73,6 +73,101 @@ __device__ __forceinline__ float3 sh_grad(int k, float x, float y, float z) {
 }
 
 // ---------------------------------------------------------------------------
+// tau = fp32 rounding of 2 ln(255 o), in float-float arithmetic
+// ---------------------------------------------------------------------------
+// The threshold must be the correctly rounded fp32 value, which a double
+// evaluation gives; FP64 is slow on this part, so the value is computed in
+// float-float (a pair hi + lo of floats, about 44 bits) with ln x =
+// e ln 2 + 2 atanh((m - 1) / (m + 1)), x = 2^e m, m in [sqrt(1/2), sqrt(2))
+// (argument reduction by a power of two and the odd atanh series), and the
+// rounding to fp32 is accepted only when a bound on the error keeps the value
+// inside one fp32 rounding interval; otherwise (about one case in 10^4) the
+// caller evaluates it in double.  All operations are round-to-nearest and
+// uncontracted, as the error-free transformations require.
+struct FF {
+    float h, l;
+};
+__device__ __forceinline__ FF two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    return FF{s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+__device__ __forceinline__ FF fast_two_sum(float a, float b) {  // |a| >= |b|
+    const float s = __fadd_rn(a, b);
+    return FF{s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ FF two_prod(float a, float b) {
+    const float p = __fmul_rn(a, b);
+    return FF{p, __fmaf_rn(a, b, -p)};
+}
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+    const FF s = two_sum(a.h, b.h);
+    return fast_two_sum(s.h, __fadd_rn(__fadd_rn(a.l, b.l), s.l));
+}
+__device__ __forceinline__ FF ff_mul(FF a, FF b) {
+    const FF p = two_prod(a.h, b.h);
+    return fast_two_sum(p.h, __fmaf_rn(a.h, b.l, __fmaf_rn(a.l, b.h, p.l)));
+}
+
+// *tau and true when the fp32 rounding is certain, false otherwise
+__device__ __forceinline__ bool tau_float_float(float o, float* tau) {
+    if (!(o > 0.f) || !(o < 1.0e30f)) return false;
+    // x = 255 o exactly, as xh + xl
+    const float xh = __fmul_rn(255.f, o);
+    const float xl = __fmaf_rn(255.f, o, -xh);
+    if (!(xh > 1.f || (xh == 1.f && xl > 0.f))) {
+        *tau = 0.f;  // 255 o <= 1: tau <= 0 (culled either way)
+        return true;
+    }
+    // x = 2^e (mh + ml), mh in [sqrt(1/2), sqrt(2)); the scalings are exact
+    const int bits = __float_as_int(xh);
+    int e = ((bits >> 23) & 0xff) - 127;
+    float mh = __int_as_float((bits & 0x7fffff) | 0x3f800000);
+    if (mh > 0x1.6a09e6p+0f) {
+        mh = __fmul_rn(mh, 0.5f);
+        e += 1;
+    }
+    const float ml = __fmul_rn(xl, __int_as_float((127 - e) << 23));
+    // s = (M - 1) / (M + 1), M = mh + ml (mh - 1 is exact)
+    const FF num = two_sum(__fsub_rn(mh, 1.f), ml);
+    const FF d0 = two_sum(mh, 1.f);
+    const FF den = fast_two_sum(d0.h, __fadd_rn(d0.l, ml));
+    const float sh = __fdiv_rn(num.h, den.h);
+    float r = __fmaf_rn(-sh, den.h, num.h);  // exact remainder
+    r = __fmaf_rn(-sh, den.l, __fadd_rn(r, num.l));
+    const FF s = fast_two_sum(sh, __fdiv_rn(r, den.h));
+    // ln M = 2 s (1 + z P(z)), z = s^2 <= 0.0295, P = 1/3 + z/5 + z^2/7 + ...
+    const FF z = ff_mul(s, s);
+    float R = 0x1.af286cp-5f;                  // 1/19
+    R = __fmaf_rn(R, z.h, 0x1.e1e1e2p-5f);     // 1/17
+    R = __fmaf_rn(R, z.h, 0x1.111112p-4f);     // 1/15
+    R = __fmaf_rn(R, z.h, 0x1.3b13b2p-4f);     // 1/13
+    R = __fmaf_rn(R, z.h, 0x1.745d18p-4f);     // 1/11
+    R = __fmaf_rn(R, z.h, 0x1.c71c72p-4f);     // 1/9
+    FF P = ff_add(FF{0x1.24924ap-3f, -0x1.b6db6ep-28f}, two_prod(z.h, R));     // 1/7 + z R
+    P = ff_add(FF{0x1.99999ap-3f, -0x1.99999ap-29f}, ff_mul(z, P));             // 1/5 + z P
+    P = ff_add(FF{0x1.555556p-2f, -0x1.555556p-27f}, ff_mul(z, P));             // 1/3 + z P
+    const FF u = ff_mul(z, P);
+    const FF w = fast_two_sum(1.f, u.h);
+    const FF lnM = ff_mul(s, fast_two_sum(w.h, __fadd_rn(w.l, u.l)));          // ln M / 2
+    // ln x / 2 = e ln2 / 2 + ln M / 2; ln 2 = hi (15 bits, so e hi is exact) + lo + lo2
+    const float fe = (float)e;
+    const FF eln2 = fast_two_sum(__fmul_rn(fe, 0x1.62e4p-1f),
+                                 __fmaf_rn(fe, 0x1.7f7d1cp-20f, __fmul_rn(fe, 0x1.ef357ap-45f)));
+    const FF half_e = FF{__fmul_rn(eln2.h, 0.5f), __fmul_rn(eln2.l, 0.5f)};
+    const FF L = ff_add(half_e, lnM);          // ln(x) / 2
+    // tau = 4 L (exact scaling); accept the fp32 rounding if the error bound
+    // (2^-36 relative) cannot cross the half gap to a neighbouring float
+    const float Th = __fmul_rn(L.h, 4.f), Tl = __fmul_rn(L.l, 4.f);
+    const int tb = __float_as_int(Th);
+    const float gap = Tl >= 0.f ? __fsub_rn(__int_as_float(tb + 1), Th)
+                                : __fsub_rn(Th, __int_as_float(tb - 1));
+    if (!(__fadd_rn(fabsf(Tl), __fmul_rn(Th, 0x1p-36f)) < __fmul_rn(gap, 0.5f))) return false;
+    *tau = Th;
+    return true;
+}
+
+// ---------------------------------------------------------------------------
 // the fp32 projection chain (fixed order, round-to-nearest)
 // ---------------------------------------------------------------------------
 struct Projected {
@@ -153,9 +248,9 @@ __device__ __forceinline__ Projected project_chain(const CamParams& cam, float m
     float l22 = rdiv(1.f, rsqrt_exact(P11));
     float l11 = rsqrt_exact(rdiv(P11, det));
     float l12 = -rmul(rdiv(P01, P11), l11);
-    // tau = fp32 rounding of 2 ln(255 o), evaluated in double
-    double td = 2.0 * log(255.0 * (double)opac);
-    float tau = __double2float_rn(td);
+    // tau = fp32 rounding of 2 ln(255 o): float-float, in double when undecided
+    float tau;
+    if (!tau_float_float(opac, &tau)) tau = __double2float_rn(2.0 * log(255.0 * (double)opac));
     if (!(tau > 0.f)) return P;
     float rx = rsqrt_exact(rmul(tau, P00));
     float ry = rsqrt_exact(rmul(tau, P11));
