@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
 // ---------------------------------------------------------------------------
 // forward: persistent kernel over whole tiles and depth chunks
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 4) raster_fwd_kernel(RasterArgs A) {
+__global__ void __launch_bounds__(kThreads, 5) raster_fwd_kernel(RasterArgs A) {
     __shared__ Smem S;
     const int tid = threadIdx.x;
     const int h = A.ctrl[kCtlH], k = A.ctrl[kCtlK], nitems = A.ctrl[kCtlItems];
