@@ -263,7 +263,8 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
         for (int cand = tid; cand < hm * 4; cand += kPolicyThreads) {
             const int h = 1 + (cand >> 2);
             const int k = 2 << (cand & 3);
-            const double inv_k = 1.0 / (double)k;  // exact
+            // 1 / k = 2^-((cand & 3) + 1), built from its exponent bits (exact, no division)
+            const double inv_k = __longlong_as_double((long long)(1022 - (cand & 3)) << 52);
             const double l = fmax(__dmul_rn(N1, inv_k), count_at(h));
             const double Kl = __dmul_rn(Kd, l);
             const double work = __dadd_rn(tot, __dmul_rn(__dmul_rn(lam, (double)h), (double)k));
