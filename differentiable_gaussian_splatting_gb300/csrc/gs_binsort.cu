@@ -353,7 +353,7 @@ __device__ __forceinline__ void warp_sort_tile(const uint64_t* __restrict__ keys
 
 // slices of 1 .. kWarpSortMax keys: one warp each
 constexpr int kSmallWarps = 4;
-__global__ void __launch_bounds__(32 * kSmallWarps, 4) bucket_sort_small(const int2* __restrict__ ranges,
+__global__ void __launch_bounds__(32 * kSmallWarps, 6) bucket_sort_small(const int2* __restrict__ ranges,
                                                                       int64_t nt,
                                                                       const uint64_t* __restrict__ keys,
                                                                       int32_t* __restrict__ sorted_ids) {
