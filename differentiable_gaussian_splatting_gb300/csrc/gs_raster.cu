@@ -162,6 +162,7 @@ __device__ __forceinline__ bool blend_range(const RasterArgs& A, Smem& S, int tx
         }
         __syncthreads();
         const int nb = (int)min64(kBatch, e - bs);
+        const int pos0 = (int)bs;  // list positions fit in 32 bits (capacity < 2^31)
         for (int c = 0; c < nb; c += 32) {
             if (__ballot_sync(0xffffffffu, !st.done) == 0) break;
             const int jj = c + lane;
@@ -184,11 +185,10 @@ __device__ __forceinline__ bool blend_range(const RasterArgs& A, Smem& S, int tx
                 st.cg = fmaf(w, r2.y, st.cg);
                 st.cb = fmaf(w, r2.z, st.cb);
                 st.T = st.T * (1.f - alpha);
-                if (hit) {
-                    st.n += 1;
-                    st.last = (int)(bs + idx);
-                    blended |= 1u << q;
-                }
+                // branch-free bookkeeping (no reconvergence point in the loop)
+                st.n += hit ? 1 : 0;
+                st.last = hit ? pos0 + idx : st.last;
+                blended |= (hit ? 1u : 0u) << q;
                 st.done = st.done || (st.T < kTMin);
             }
             if (write_cmask) {
