@@ -766,19 +766,18 @@ __global__ void __launch_bounds__(kBwdThreads) raster_bwd_kernel(RasterArgs A) {
                     if ((b1 | b2) == 0) continue;
                     const float sum = reduce_scatter9x2(va, vb, lane);
                     const bool first = lane < 16;
-                    if (my_comp2 >= 0 && (first ? b1 : b2)) {
-                        const int q = first ? q1 : q2;
-                        // component 5 is d/d(opacity): divide by o = 2^log2(o)
-                        const float f = my_comp2 == 5 ? ex2_approx(-S.r1[q].z) : comp_scale2;
-                        atomicAdd(A.grad2d + 9 * (int64_t)S.gid[q] + my_comp2, sum * f);
-                    }
+                    // every lane forms its write; only the atomic is predicated
+                    const int q = first ? q1 : q2;
+                    // component 5 is d/d(opacity): divide by o = 2^log2(o)
+                    const float f = my_comp2 == 5 ? ex2_approx(-S.r1[q].z) : comp_scale2;
+                    float* dst = A.grad2d + 9 * (int64_t)S.gid[q] + my_comp2;
+                    if (my_comp2 >= 0 && (first ? b1 : b2)) atomicAdd(dst, sum * f);
                 } else {
                     if (b1 == 0) continue;
                     const float sum = reduce_scatter9(va, lane);
-                    if (writer) {
-                        const float f = my_comp == 5 ? ex2_approx(-S.r1[q1].z) : comp_scale;
-                        atomicAdd(A.grad2d + 9 * (int64_t)S.gid[q1] + my_comp, sum * f);
-                    }
+                    const float f = my_comp == 5 ? ex2_approx(-S.r1[q1].z) : comp_scale;
+                    float* dst = A.grad2d + 9 * (int64_t)S.gid[q1] + my_comp;
+                    if (writer) atomicAdd(dst, sum * f);
                 }
             }
             __syncwarp();  // the slice is restaged two steps later
