@@ -329,6 +329,16 @@ __global__ void __launch_bounds__(kProjThreads) project_kernel(CamParams cam, in
         S.e[7][tid] = e.ry;
         S.dyv[tid] = nrows > 0 ? vertex_dy(e) : 0.f;
         S.ty0[tid] = ty0;
+        // the colour needs the SH row of every visible Gaussian: bring the rows of
+        // those whose padded box meets the image into L2 while the rows are walked
+        const float px = radd(P.rx, pad_of(P.rx));
+        if (nrows > 0 && P.mux + px >= 0.5f && P.mux - px <= (float)cam.W - 0.5f) {
+            const char* row = reinterpret_cast<const char*>(sh + i * (K * 3));
+#pragma unroll
+            for (int b = 0; b < K * 12; b += 128)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(row + b));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(row + K * 12 - 1));
+        }
     }
     S.cnt[tid] = 0;
     // block exclusive scan of the row counts
