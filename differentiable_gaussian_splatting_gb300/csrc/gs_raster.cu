@@ -618,9 +618,10 @@ __device__ __forceinline__ int fwd_thread(int lx, int ly) {
     return 32 * ((lx >> 3) + 2 * (ly >> 2)) + (lx & 7) + 8 * (ly & 3);
 }
 
-// the back-to-front state of one pixel
+// the back-to-front state of one pixel; accg is the colour behind (dotted
+// with dL/dC) plus dL/dT_final * T_final, the two always appear summed
 struct BwdPixel {
-    float T, accum, Gr, Gg, Gb, gTT;
+    float T, accg, Gr, Gg, Gb;
 };
 
 // One row of one splat: recovers the transmittance in front of the splat,
@@ -631,18 +632,19 @@ __device__ __forceinline__ bool row_step(const float4& r0, const float4& r1, con
                                          float* u1, float* u2, float* gs, float* wgt) {
     const float qv = quad_q(r0.z, r0.w, r1.x, dx, dy, u1, u2);
     const bool act = (qv <= r1.y) && in_range;
-    const float araw = ex2_approx(fmaf(qv, kNegHalfLog2e, r1.z));
-    float alpha = fminf(araw, kAlphaMax);
+    float alpha = fminf(ex2_approx(fmaf(qv, kNegHalfLog2e, r1.z)), kAlphaMax);
     alpha = act ? alpha : 0.f;
+    // alpha = 0 gives inv = 1 exactly, so T is unchanged without a select
     const float inv = __fdividef(1.f, 1.f - alpha);
     const float Tb = P.T * inv;
     const float w = alpha * Tb;
     const float cG = r2.x * P.Gr + r2.y * P.Gg + r2.z * P.Gb;
-    const float dalpha = Tb * cG - (P.accum + P.gTT) * inv;
-    P.accum = fmaf(cG, w, P.accum);
-    *gs = (act && araw < kAlphaMax) ? araw * dalpha : 0.f;
+    const float dalpha = Tb * cG - P.accg * inv;
+    P.accg = fmaf(cG, w, P.accg);
+    // zero when the pixel did not blend (alpha = 0) or the clamp was active
+    *gs = alpha < kAlphaMax ? alpha * dalpha : 0.f;
     *wgt = w;
-    P.T = act ? Tb : P.T;
+    P.T = Tb;
     return act;
 }
 
@@ -674,7 +676,7 @@ __device__ __forceinline__ bool splat_terms2(const BwdSlice& S, int q, float px,
 
 __device__ __forceinline__ void load_bwd_pixel(const RasterArgs& A, const WorkItem& it, int x, int y,
                                                int lx, int ly, BwdPixel& P, int& last) {
-    P = BwdPixel{1.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    P = BwdPixel{1.f, 0.f, 0.f, 0.f, 0.f};
     last = -1;
     if (x >= A.W || y >= A.H) return;
     const int64_t p = (int64_t)y * A.W + x;
@@ -683,7 +685,7 @@ __device__ __forceinline__ void load_bwd_pixel(const RasterArgs& A, const WorkIt
     P.Gr = A.dimg[3 * p];
     P.Gg = A.dimg[3 * p + 1];
     P.Gb = A.dimg[3 * p + 2];
-    P.gTT = A.dT ? A.dT[p] * Tfin : 0.f;
+    P.accg = A.dT ? A.dT[p] * Tfin : 0.f;
     if (it.slot < 0) {
         P.T = Tfin;
     } else {
@@ -691,11 +693,11 @@ __device__ __forceinline__ void load_bwd_pixel(const RasterArgs& A, const WorkIt
             ((int64_t)it.slot * kMaxChunks + it.chunk) * kThreads + fwd_thread(lx, ly);
         const float4 b = A.bstate[slotp];
         P.T = b.x;
-        P.accum = b.y * P.Gr + b.z * P.Gg + b.w * P.Gb;
+        P.accg += b.y * P.Gr + b.z * P.Gg + b.w * P.Gb;
     }
 }
 
-__global__ void __launch_bounds__(kBwdThreads) raster_bwd_kernel(RasterArgs A) {
+__global__ void __launch_bounds__(kBwdThreads, 6) raster_bwd_kernel(RasterArgs A) {
     __shared__ BwdSlice SL[kBwdWarps][2];  // double-buffered per warp
     const unsigned F = 0xffffffffu;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
