@@ -2,12 +2,15 @@
 //
 // Host side only: argument validation (synchronous, before anything is
 // enqueued), workspace carving and kernel launches on the caller's stream.
-// The library allocates no device memory.
+// The library allocates no device memory.  gs_bin_sort keeps one side stream
+// and two events per device, created on its first call there, for work that
+// overlaps the main sequence and is joined back into the caller's stream.
 #include <cuda_runtime.h>
 
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/gs.h"
 #include "gs_internal.h"
@@ -35,6 +38,31 @@ bool camera_ok(const gs_camera* cam) {
         return false;
     if (!(cam->znear > 0.f) || !finite_f(cam->znear)) return false;
     return true;
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_side_mu;  // guards g_side and orders the enqueues that use it
+SideStream g_side[kMaxDevices];
+bool g_side_ready[kMaxDevices];
+
+// The side stream of the current device; call with g_side_mu held.
+cudaError_t side_stream(const SideStream** out) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!g_side_ready[dev]) {
+        SideStream s{};
+        err = cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking);
+        if (err != cudaSuccess) return err;
+        err = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
+        if (err == cudaSuccess) err = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
+        if (err != cudaSuccess) return err;
+        g_side[dev] = s;
+        g_side_ready[dev] = true;
+    }
+    *out = &g_side[dev];
+    return cudaSuccess;
 }
 
 CamParams cam_params(const gs_camera* cam) {
@@ -88,6 +116,63 @@ RasterConfig raster_config(const gs_settings* s) {
 gs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GS_OK : GS_ERR_CUDA; }
 
 }  // namespace
+
+namespace gs {
+
+gs_status bin_sort_entry(const gs_camera* cam, int64_t n, const float* splats,
+                         const float* depths, const int32_t* tiles_touched, void* workspace,
+                         size_t workspace_bytes, int32_t* sorted_ids, int64_t capacity,
+                         int32_t* tile_ranges, int32_t* lpt_order, int64_t* counts_device,
+                         int64_t* n_pairs_host, void* stream, bool overlap) {
+    if (!camera_ok(cam) || n < 0 || n > kMaxIds || capacity < 1 || capacity > kMaxIds)
+        return GS_ERR_INVALID_ARG;
+    if (n > 0) {
+        const void* ptrs[] = {splats, depths, tiles_touched};
+        for (const void* p : ptrs)
+            if (!p || !aligned16(p)) return GS_ERR_INVALID_ARG;
+    }
+    const void* outs[] = {workspace, sorted_ids, tile_ranges, lpt_order};
+    for (const void* p : outs)
+        if (!p || !aligned16(p)) return GS_ERR_INVALID_ARG;
+    if (counts_device && (reinterpret_cast<uintptr_t>(counts_device) & 7u)) return GS_ERR_INVALID_ARG;
+    const int64_t nt = gs_num_tiles(cam->width, cam->height);
+    const BinSortLayout L = binsort_layout(n, capacity, nt);
+    if (workspace_bytes < L.total) return GS_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    char* ws = static_cast<char*>(workspace);
+    cudaError_t err;
+    {
+        // the whole sequence is enqueued under the lock, so that the join event
+        // still marks this call's side work when the caller's stream waits on it
+        std::unique_lock<std::mutex> lk(g_side_mu, std::defer_lock);
+        const SideStream* side = nullptr;
+        if (overlap) {
+            lk.lock();
+            err = side_stream(&side);
+            if (err != cudaSuccess) return GS_ERR_CUDA;
+        }
+        err = run_bin_sort(cam_params(cam), n, splats, depths, tiles_touched, ws, L, sorted_ids,
+                           capacity, tile_ranges, lpt_order, st, side);
+    }
+    if (err != cudaSuccess) return GS_ERR_CUDA;
+    const int64_t* counts = reinterpret_cast<const int64_t*>(ws + L.off_counts);
+    if (counts_device) {
+        err = cudaMemcpyAsync(counts_device, counts, 2 * sizeof(int64_t), cudaMemcpyDeviceToDevice, st);
+        if (err != cudaSuccess) return GS_ERR_CUDA;
+    }
+    if (n_pairs_host) {
+        int64_t host_counts[2] = {0, 0};
+        err = cudaMemcpyAsync(host_counts, counts, 2 * sizeof(int64_t), cudaMemcpyDeviceToHost, st);
+        if (err != cudaSuccess) return GS_ERR_CUDA;
+        err = cudaStreamSynchronize(st);
+        if (err != cudaSuccess) return GS_ERR_CUDA;
+        *n_pairs_host = host_counts[1];
+        if (host_counts[1] > capacity) return GS_ERR_CAPACITY;
+    }
+    return GS_OK;
+}
+
+}  // namespace gs
 
 extern "C" {
 
@@ -147,41 +232,11 @@ gs_status gs_bin_sort(const gs_camera* cam, int64_t n, const float* splats, cons
                       int32_t* sorted_ids, int64_t capacity, int32_t* tile_ranges,
                       int32_t* lpt_order, int64_t* counts_device, int64_t* n_pairs_host,
                       void* stream) {
-    if (!camera_ok(cam) || n < 0 || n > kMaxIds || capacity < 1 || capacity > kMaxIds)
-        return GS_ERR_INVALID_ARG;
-    if (n > 0) {
-        const void* ptrs[] = {splats, depths, tiles_touched};
-        for (const void* p : ptrs)
-            if (!p || !aligned16(p)) return GS_ERR_INVALID_ARG;
-    }
-    const void* outs[] = {workspace, sorted_ids, tile_ranges, lpt_order};
-    for (const void* p : outs)
-        if (!p || !aligned16(p)) return GS_ERR_INVALID_ARG;
-    if (counts_device && (reinterpret_cast<uintptr_t>(counts_device) & 7u)) return GS_ERR_INVALID_ARG;
-    const int64_t nt = gs_num_tiles(cam->width, cam->height);
-    const BinSortLayout L = binsort_layout(n, capacity, nt);
-    if (workspace_bytes < L.total) return GS_ERR_WORKSPACE;
-    cudaStream_t st = (cudaStream_t)stream;
-    char* ws = static_cast<char*>(workspace);
-    cudaError_t err = run_bin_sort(cam_params(cam), n, splats, depths, tiles_touched, ws, L,
-                                   sorted_ids, capacity, tile_ranges, lpt_order, st);
-    if (err != cudaSuccess) return GS_ERR_CUDA;
-    const int64_t* counts = reinterpret_cast<const int64_t*>(ws + L.off_counts);
-    if (counts_device) {
-        err = cudaMemcpyAsync(counts_device, counts, 2 * sizeof(int64_t), cudaMemcpyDeviceToDevice, st);
-        if (err != cudaSuccess) return GS_ERR_CUDA;
-    }
-    if (n_pairs_host) {
-        int64_t host_counts[2] = {0, 0};
-        err = cudaMemcpyAsync(host_counts, counts, 2 * sizeof(int64_t), cudaMemcpyDeviceToHost, st);
-        if (err != cudaSuccess) return GS_ERR_CUDA;
-        err = cudaStreamSynchronize(st);
-        if (err != cudaSuccess) return GS_ERR_CUDA;
-        *n_pairs_host = host_counts[1];
-        if (host_counts[1] > capacity) return GS_ERR_CAPACITY;
-    }
-    return GS_OK;
+    return gs::bin_sort_entry(cam, n, splats, depths, tiles_touched, workspace, workspace_bytes,
+                              sorted_ids, capacity, tile_ranges, lpt_order, counts_device,
+                              n_pairs_host, stream, true);
 }
+
 
 size_t gs_raster_workspace_bytes(int32_t width, int32_t height, int64_t capacity,
                                  const gs_settings* settings) {

@@ -625,7 +625,7 @@ BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles) {
 cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, const float* depths,
                          const int32_t* tiles_touched, char* ws, const BinSortLayout& L,
                          int32_t* sorted_ids, int64_t capacity, int32_t* tile_ranges,
-                         int32_t* lpt_order, cudaStream_t st) {
+                         int32_t* lpt_order, cudaStream_t st, const SideStream* side) {
     auto* counts = reinterpret_cast<int64_t*>(ws + L.off_counts);
     auto* raw = reinterpret_cast<uint2*>(ws + L.off_raw);
     auto* keys = reinterpret_cast<uint64_t*>(ws + L.off_keys);
@@ -652,6 +652,27 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
             counts);
     bucket_scan<<<1, kScanThreads, 0, st>>>(tcount, nt, capacity, ranges, cursor, medium, large,
                                             counts);
+    // LPT order (tiles by descending count, ties by tile id) needs only the
+    // ranges: on the side stream, when given, it runs beside the scatter and sorts
+    cudaStream_t ls = st;
+    if (side) {
+        err = cudaEventRecord(side->fork, st);
+        if (err != cudaSuccess) return err;
+        err = cudaStreamWaitEvent(side->stream, side->fork, 0);
+        if (err != cudaSuccess) return err;
+        ls = side->stream;
+    }
+    {
+        const unsigned nruns = (unsigned)((nt + kLptRun - 1) / kLptRun);
+        lpt_sort_runs<<<nruns, kLptRun / 2, 0, ls>>>(reinterpret_cast<const int2*>(tile_ranges), nt,
+                                                     lruns);
+        lpt_merge<<<(unsigned)((nruns * (int64_t)kLptRun + 255) / 256), 256, 0, ls>>>(lruns, nt,
+                                                                                   lpt_order);
+    }
+    if (side) {
+        err = cudaEventRecord(side->join, side->stream);
+        if (err != cudaSuccess) return err;
+    }
     if (n > 0) {
         const unsigned grid = (unsigned)std::max<int64_t>(
             1, std::min<int64_t>((capacity + 255) / 256, 8 * (int64_t)sms));
@@ -674,13 +695,9 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
                                                         reinterpret_cast<uint64_t*>(raw), sorted_ids,
                                                         counts);
     }
-    // 5. LPT order: tiles by descending count, ties by tile id
-    {
-        const unsigned nruns = (unsigned)((nt + kLptRun - 1) / kLptRun);
-        lpt_sort_runs<<<nruns, kLptRun / 2, 0, st>>>(reinterpret_cast<const int2*>(tile_ranges), nt,
-                                                     lruns);
-        lpt_merge<<<(unsigned)((nruns * (int64_t)kLptRun + 255) / 256), 256, 0, st>>>(lruns, nt,
-                                                                                   lpt_order);
+    if (side) {
+        err = cudaStreamWaitEvent(st, side->join, 0);  // the LPT order is ready
+        if (err != cudaSuccess) return err;
     }
     return cudaGetLastError();
 }

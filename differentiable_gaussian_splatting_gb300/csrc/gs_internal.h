@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "../../include/gs.h"
+
 namespace gs {
 
 // Camera as the kernels see it: rows 0..2 of the view matrix, intrinsics,
@@ -42,10 +44,26 @@ struct BinSortLayout {
 };
 BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles);
 
+// A second stream with fork / join events: work that depends only on an
+// earlier step runs on it beside the main sequence and is joined back.
+struct SideStream {
+    cudaStream_t stream;
+    cudaEvent_t fork, join;
+};
+
+// gs_bin_sort with its argument checks; overlap = false keeps every launch in
+// order on the caller's stream and creates no side stream.
+gs_status bin_sort_entry(const gs_camera* cam, int64_t n, const float* splats,
+                         const float* depths, const int32_t* tiles_touched, void* workspace,
+                         size_t workspace_bytes, int32_t* sorted_ids, int64_t capacity,
+                         int32_t* tile_ranges, int32_t* lpt_order, int64_t* counts_device,
+                         int64_t* n_pairs_host, void* stream, bool overlap);
+
+// side may be null (everything in order on st)
 cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, const float* depths,
                          const int32_t* tiles_touched, char* ws, const BinSortLayout& L,
                          int32_t* sorted_ids, int64_t capacity, int32_t* tile_ranges,
-                         int32_t* lpt_order, cudaStream_t st);
+                         int32_t* lpt_order, cudaStream_t st, const SideStream* side);
 
 // ---- rasterization (gs_raster.cu) ------------------------------------------
 struct RasterConfig {

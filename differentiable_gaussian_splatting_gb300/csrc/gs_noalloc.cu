@@ -66,6 +66,8 @@ extern "C" gs_status gs_bin_sort_noalloc(const gs_camera* cam, int64_t n, const 
         return GS_ERR_WORKSPACE;
     void* scratch = nullptr;
     if (scratch_address(&scratch) != cudaSuccess) return GS_ERR_CUDA;
-    return gs_bin_sort(cam, n, splats, depths, tiles_touched, scratch, kScratchBytes, sorted_ids,
-                       capacity, tile_ranges, lpt_order, counts_device, n_pairs_host, stream);
+    // in order on the caller's stream: no side stream or events are created here
+    return gs::bin_sort_entry(cam, n, splats, depths, tiles_touched, scratch, kScratchBytes,
+                              sorted_ids, capacity, tile_ranges, lpt_order, counts_device,
+                              n_pairs_host, stream, false);
 }

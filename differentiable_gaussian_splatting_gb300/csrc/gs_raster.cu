@@ -223,6 +223,16 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
     __shared__ int s_cand[kPolicyThreads / 32];
     __shared__ int s_hk[2];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    auto count_at = [&](int j) -> double {
+        if (j >= nt) return 0.0;
+        const int2 r = ranges[lpt[j]];
+        return (double)(r.y - r.x);
+    };
+    // the loads that do not depend on N_total are issued before its reduction:
+    // N_1 and N_{h+1} of this thread's first candidate
+    const int hm = cfg.split_mode == 0 ? min(nt, cfg.h_max) : 0;
+    const double N1 = count_at(0);
+    const double n_first = tid < hm * 4 ? count_at(1 + (tid >> 2)) : 0.0;
     // N_total: an integer sum (exactly the double sum of the counts, all below 2^53)
     long long part = 0;
     for (int t = tid; t < nt; t += kPolicyThreads) {
@@ -237,15 +247,9 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
 #pragma unroll
     for (int w = 0; w < kPolicyThreads / 32; ++w) itot += s_tot[w];
     const double tot = (double)itot;
-    auto count_at = [&](int j) -> double {
-        if (j >= nt) return 0.0;
-        const int2 r = ranges[lpt[j]];
-        return (double)(r.y - r.x);
-    };
     // Eq. 6 multiplied by K > 0 (same minimiser, no division), in round-to-nearest
     // double with no contraction: K T(h, k) = max(N_total + lambda h k, K l) + beta K l,
     // l = max(N_1 / k, N_{h+1}); N_1 / k is an exact scaling by a power of two
-    const double N1 = count_at(0);
     const double lam = cfg.lambda, beta = cfg.beta, Kd = (double)K;
     const double KN1 = __dmul_rn(Kd, N1);
     const double base = __dadd_rn(fmax(tot, KN1), __dmul_rn(beta, KN1));
@@ -254,7 +258,6 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
         bh = min(min(cfg.force_h, cfg.h_max), nt);
         bk = bh > 0 ? cfg.force_k : 1;
     } else if (cfg.split_mode == 0) {
-        const int hm = min(nt, cfg.h_max);
         // candidate c = 4 (h - 1) + i, k = 2^(i + 1): increasing c is increasing (h, k), so
         // the lexicographic minimum of (cost, h, k) is that of (cost, c).  Costs are
         // non-negative, so their bit patterns order as unsigned integers.
@@ -265,7 +268,7 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
             const int k = 2 << (cand & 3);
             // 1 / k = 2^-((cand & 3) + 1), built from its exponent bits (exact, no division)
             const double inv_k = __longlong_as_double((long long)(1022 - (cand & 3)) << 52);
-            const double l = fmax(__dmul_rn(N1, inv_k), count_at(h));
+            const double l = fmax(__dmul_rn(N1, inv_k), cand == tid ? n_first : count_at(h));
             const double Kl = __dmul_rn(Kd, l);
             const double work = __dadd_rn(tot, __dmul_rn(__dmul_rn(lam, (double)h), (double)k));
             const double cost = __dadd_rn(fmax(work, Kl), __dmul_rn(beta, Kl));
