@@ -56,6 +56,7 @@ cudaError_t side_stream(const SideStream** out) {
         err = cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking);
         if (err != cudaSuccess) return err;
         err = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
+        if (err == cudaSuccess) err = cudaEventCreateWithFlags(&s.fork2, cudaEventDisableTiming);
         if (err == cudaSuccess) err = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
         if (err != cudaSuccess) return err;
         g_side[dev] = s;
@@ -152,14 +153,10 @@ gs_status bin_sort_entry(const gs_camera* cam, int64_t n, const float* splats,
             if (err != cudaSuccess) return GS_ERR_CUDA;
         }
         err = run_bin_sort(cam_params(cam), n, splats, depths, tiles_touched, ws, L, sorted_ids,
-                           capacity, tile_ranges, lpt_order, st, side);
+                           capacity, tile_ranges, lpt_order, counts_device, st, side);
     }
     if (err != cudaSuccess) return GS_ERR_CUDA;
     const int64_t* counts = reinterpret_cast<const int64_t*>(ws + L.off_counts);
-    if (counts_device) {
-        err = cudaMemcpyAsync(counts_device, counts, 2 * sizeof(int64_t), cudaMemcpyDeviceToDevice, st);
-        if (err != cudaSuccess) return GS_ERR_CUDA;
-    }
     if (n_pairs_host) {
         int64_t host_counts[2] = {0, 0};
         err = cudaMemcpyAsync(host_counts, counts, 2 * sizeof(int64_t), cudaMemcpyDeviceToHost, st);

@@ -50,6 +50,17 @@ constexpr int kCountMedium = 4;
 constexpr int kCountLarge = 5;
 
 // ---------------------------------------------------------------------------
+// 0. the call's counters and the tile counters to zero
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) bin_zero(int64_t* __restrict__ counts,
+                                                int* __restrict__ tile_count, int64_t nt) {
+    grid_dep_sync();
+    const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i0 < 8) counts[i0] = 0;
+    for (int64_t t = i0; t < nt; t += (int64_t)gridDim.x * blockDim.x) tile_count[t * kCountStride] = 0;
+}
+
+// ---------------------------------------------------------------------------
 // 1. one pass over the Gaussians: raw (tile, Gaussian) pairs and tile counts
 // ---------------------------------------------------------------------------
 struct EmitShared {
@@ -71,6 +82,7 @@ __global__ void __launch_bounds__(kEmitThreads) bucket_emit(CamParams cam,
                                                             int* __restrict__ tile_count,
                                                             uint2* __restrict__ raw,
                                                             int64_t* __restrict__ counts) {
+    grid_dep_sync();
     __shared__ EmitShared S;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t g = (int64_t)blockIdx.x * kEmitThreads + tid;
@@ -161,31 +173,50 @@ __global__ void __launch_bounds__(kEmitThreads) bucket_emit(CamParams cam,
 // cursors, I and min(I, capacity).  When I > capacity the list cannot be
 // built; every range is then empty, so nothing downstream reads it.
 // ---------------------------------------------------------------------------
-// exclusive block scan (kScanThreads threads) of one int64 per thread
-__device__ __forceinline__ int64_t scan_block_1024(int64_t v, int64_t* s_part, int64_t* total) {
+// exclusive block scan (kScanThreads threads) of two int64 per thread at once
+__device__ __forceinline__ void scan_block2(int64_t& a, int64_t& b, int64_t* s_a, int64_t* s_b,
+                                            int64_t* ta, int64_t* tb) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    int64_t x = v;
+    const int64_t a0 = a, b0 = b;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+        const int64_t ya = __shfl_up_sync(0xffffffffu, a, o);
+        const int64_t yb = __shfl_up_sync(0xffffffffu, b, o);
+        if (lane >= o) {
+            a += ya;
+            b += yb;
+        }
     }
-    if (lane == 31) s_part[warp] = x;
+    if (lane == 31) {
+        s_a[warp] = a;
+        s_b[warp] = b;
+    }
     __syncthreads();
     if (warp == 0) {
-        int64_t w = s_part[lane];
+        int64_t wa = s_a[lane], wb = s_b[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += y;
+            const int64_t ya = __shfl_up_sync(0xffffffffu, wa, o);
+            const int64_t yb = __shfl_up_sync(0xffffffffu, wb, o);
+            if (lane >= o) {
+                wa += ya;
+                wb += yb;
+            }
         }
-        s_part[lane] = w;
+        s_a[lane] = wa;
+        s_b[lane] = wb;
     }
     __syncthreads();
-    const int64_t ex = (warp > 0 ? s_part[warp - 1] : 0) + x - v;
-    *total = s_part[31];
-    __syncthreads();
-    return ex;
+    a += (warp > 0 ? s_a[warp - 1] : 0) - a0;
+    b += (warp > 0 ? s_b[warp - 1] : 0) - b0;
+    *ta = s_a[31];
+    *tb = s_b[31];
+}
+
+constexpr int kScanRegs = 8;  // tiles per thread held in registers (nt <= 8192)
+
+__device__ __forceinline__ int size_class(int c) {
+    return c > kBlockSortMax ? 2 : (c > kWarpSortMax ? 1 : 0);
 }
 
 __global__ void __launch_bounds__(kScanThreads) bucket_scan(const int* __restrict__ tile_count,
@@ -194,36 +225,63 @@ __global__ void __launch_bounds__(kScanThreads) bucket_scan(const int* __restric
                                                             unsigned long long* __restrict__ cursor,
                                                             int32_t* __restrict__ medium,
                                                             int32_t* __restrict__ large,
-                                                            int64_t* __restrict__ counts) {
-    __shared__ int64_t s_part[kScanThreads / 32];
+                                                            int64_t* __restrict__ counts,
+                                                            int64_t* __restrict__ counts_out) {
+    grid_dep_sync();
+    __shared__ int64_t s_a[kScanThreads / 32], s_b[kScanThreads / 32];
     const int tid = threadIdx.x;
     const int64_t per = (nt + kScanThreads - 1) / kScanThreads;
     const int64_t lo = min64(nt, per * tid), hi = min64(nt, lo + per);
-    int64_t sum = 0, nm = 0, nl = 0;
-    for (int64_t t = lo; t < hi; ++t) {
-        const int c = tile_count[t * kCountStride];
-        sum += c;
-        nm += c > kWarpSortMax && c <= kBlockSortMax;
-        nl += c > kBlockSortMax;
+    // per thread: its pair count and, packed, its medium (low word) and large
+    // (high word) tile counts -- each below 2^32, as nt is
+    int64_t run = 0, cls = 0;
+    int c[kScanRegs];
+    if (per <= kScanRegs) {
+#pragma unroll
+        for (int i = 0; i < kScanRegs; ++i)
+            c[i] = lo + i < hi ? tile_count[(lo + i) * kCountStride] : 0;
+#pragma unroll
+        for (int i = 0; i < kScanRegs; ++i) {
+            run += c[i];
+            const int k = size_class(c[i]);
+            cls += k == 1 ? 1ll : (k == 2 ? (1ll << 32) : 0ll);
+        }
+    } else {
+        for (int64_t t = lo; t < hi; ++t) {
+            const int ct = tile_count[t * kCountStride];
+            run += ct;
+            const int k = size_class(ct);
+            cls += k == 1 ? 1ll : (k == 2 ? (1ll << 32) : 0ll);
+        }
     }
-    int64_t total, tm, tl;
-    int64_t run = scan_block_1024(sum, s_part, &total);
-    int64_t om = scan_block_1024(nm, s_part, &tm);
-    int64_t ol = scan_block_1024(nl, s_part, &tl);
+    int64_t total, tcls;
+    scan_block2(run, cls, s_a, s_b, &total, &tcls);
     const bool fits = total <= capacity;
-    for (int64_t t = lo; t < hi; ++t) {
-        const int c = tile_count[t * kCountStride];
-        ranges[t] = fits ? make_int2((int)run, (int)(run + c)) : make_int2(0, 0);
+    int64_t om = cls & 0xffffffffll, ol = cls >> 32;
+    auto emit = [&](int64_t t, int ct) {
+        ranges[t] = fits ? make_int2((int)run, (int)(run + ct)) : make_int2(0, 0);
         cursor[t * kCursorStride] = (unsigned long long)run;
-        run += c;
-        if (c > kWarpSortMax && c <= kBlockSortMax) medium[om++] = (int32_t)t;
-        if (c > kBlockSortMax) large[ol++] = (int32_t)t;
+        run += ct;
+        const int k = size_class(ct);
+        if (k == 1) medium[om++] = (int32_t)t;
+        if (k == 2) large[ol++] = (int32_t)t;
+    };
+    if (per <= kScanRegs) {
+#pragma unroll
+        for (int i = 0; i < kScanRegs; ++i)
+            if (lo + i < hi) emit(lo + i, c[i]);
+    } else {
+        for (int64_t t = lo; t < hi; ++t) emit(t, tile_count[t * kCountStride]);
     }
     if (tid == 0) {
         counts[1] = total;
         counts[2] = fits ? total : capacity;
-        counts[kCountMedium] = fits ? tm : 0;
-        counts[kCountLarge] = fits ? tl : 0;
+        counts[kCountMedium] = fits ? (tcls & 0xffffffffll) : 0;
+        counts[kCountLarge] = fits ? (tcls >> 32) : 0;
+        if (counts_out) {
+            counts_out[0] = counts[0];  // M: complete, the span pass has finished
+            counts_out[1] = total;
+        }
     }
 }
 
@@ -235,6 +293,7 @@ __global__ void __launch_bounds__(256) bucket_scatter(const uint2* __restrict__ 
                                                       unsigned long long* __restrict__ cursor,
                                                       int64_t capacity, uint64_t* __restrict__ keys,
                                                       const int64_t* __restrict__ counts) {
+    grid_dep_sync();
     constexpr int kIlp = 4;
     const int64_t m = min64(counts[kCountRaw], capacity);
     const int64_t step = (int64_t)gridDim.x * blockDim.x;
@@ -357,6 +416,7 @@ __global__ void __launch_bounds__(32 * kSmallWarps, 6) bucket_sort_small(const i
                                                                       int64_t nt,
                                                                       const uint64_t* __restrict__ keys,
                                                                       int32_t* __restrict__ sorted_ids) {
+    grid_dep_sync();
     __shared__ uint64_t sbuf[kSmallWarps][2][sk_len(kWarpSortMax)];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint64_t* b0 = sbuf[warp][0];
@@ -428,6 +488,7 @@ __global__ void __launch_bounds__(kSortThreads) bucket_sort_medium(const int2* _
                                                                    const uint64_t* __restrict__ keys,
                                                                    int32_t* __restrict__ sorted_ids,
                                                                    const int64_t* __restrict__ counts) {
+    grid_dep_sync();
     extern __shared__ uint64_t smem[];
     uint64_t* A = smem;                            // sk_len(kBlockSortMax)
     uint64_t* B = smem + sk_len(kBlockSortMax);    // sk_len(kBlockSortMax)
@@ -470,6 +531,7 @@ __global__ void __launch_bounds__(kSortThreads) bucket_sort_large(const int2* __
                                                                   uint64_t* __restrict__ buf1,
                                                                   int32_t* __restrict__ sorted_ids,
                                                                   const int64_t* __restrict__ counts) {
+    grid_dep_sync();
     extern __shared__ uint64_t smem[];
     uint64_t* A = smem;
     uint64_t* B = smem + sk_len(kBlockSortMax);
@@ -528,6 +590,7 @@ constexpr int kLptRun = 1024;
 
 __global__ void __launch_bounds__(kLptRun / 2) lpt_sort_runs(const int2* __restrict__ ranges,
                                                             int64_t nt, uint64_t* __restrict__ runs) {
+    grid_dep_sync();
     __shared__ uint64_t sk[kLptRun];
     const int tid = threadIdx.x;
     const int64_t base = (int64_t)blockIdx.x * kLptRun;
@@ -568,6 +631,7 @@ __global__ void __launch_bounds__(kLptRun / 2) lpt_sort_runs(const int2* __restr
 constexpr int kLptSmemRuns = 6;
 __global__ void __launch_bounds__(256) lpt_merge(const uint64_t* __restrict__ runs, int64_t nt,
                                                  int32_t* __restrict__ lpt) {
+    grid_dep_sync();
     __shared__ uint64_t sr[kLptSmemRuns * kLptRun];
     const int64_t nruns = (nt + kLptRun - 1) / kLptRun;
     const bool in_smem = nruns <= kLptSmemRuns;
@@ -625,7 +689,8 @@ BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles) {
 cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, const float* depths,
                          const int32_t* tiles_touched, char* ws, const BinSortLayout& L,
                          int32_t* sorted_ids, int64_t capacity, int32_t* tile_ranges,
-                         int32_t* lpt_order, cudaStream_t st, const SideStream* side) {
+                         int32_t* lpt_order, int64_t* counts_out, cudaStream_t st,
+                         const SideStream* side) {
     auto* counts = reinterpret_cast<int64_t*>(ws + L.off_counts);
     auto* raw = reinterpret_cast<uint2*>(ws + L.off_raw);
     auto* keys = reinterpret_cast<uint64_t*>(ws + L.off_keys);
@@ -637,23 +702,27 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
     auto* large = medium + nt;
     auto* ranges = reinterpret_cast<int2*>(tile_ranges);
     cudaError_t err;
-
-    err = cudaMemsetAsync(counts, 0, 8 * sizeof(int64_t), st);
-    if (err != cudaSuccess) return err;
-    err = cudaMemsetAsync(tcount, 0, (size_t)nt * kCountStride * sizeof(int), st);
-    if (err != cudaSuccess) return err;
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     sms = std::max(sms, 1);
-    if (n > 0)
-        bucket_emit<<<(unsigned)((n + kEmitThreads - 1) / kEmitThreads), kEmitThreads, 0, st>>>(
-            cam, reinterpret_cast<const float4*>(splats), tiles_touched, n, capacity, tcount, raw,
-            counts);
-    bucket_scan<<<1, kScanThreads, 0, st>>>(tcount, nt, capacity, ranges, cursor, medium, large,
-                                            counts);
-    // LPT order (tiles by descending count, ties by tile id) needs only the
-    // ranges: on the side stream, when given, it runs beside the scatter and sorts
+
+    // 0. the counters start at zero
+    err = launch(bin_zero, (unsigned)std::min<int64_t>((nt + 255) / 256, 4 * (int64_t)sms), 256, 0,
+                 st, counts, tcount, nt);
+    if (err != cudaSuccess) return err;
+    // 1.-2. pairs and tile counts; tile ranges
+    if (n > 0) {
+        err = launch(bucket_emit, (unsigned)((n + kEmitThreads - 1) / kEmitThreads), kEmitThreads, 0,
+                     st, cam, reinterpret_cast<const float4*>(splats), tiles_touched, n, capacity,
+                     tcount, raw, counts);
+        if (err != cudaSuccess) return err;
+    }
+    err = launch(bucket_scan, 1, kScanThreads, 0, st, (const int*)tcount, nt, capacity, ranges,
+                 cursor, medium, large, counts, counts_out);
+    if (err != cudaSuccess) return err;
+    // 5. LPT order (tiles by descending count, ties by tile id) needs only the
+    // ranges: on the side stream, when given, it runs beside steps 3 and 4
     cudaStream_t ls = st;
     if (side) {
         err = cudaEventRecord(side->fork, st);
@@ -664,22 +733,34 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
     }
     {
         const unsigned nruns = (unsigned)((nt + kLptRun - 1) / kLptRun);
-        lpt_sort_runs<<<nruns, kLptRun / 2, 0, ls>>>(reinterpret_cast<const int2*>(tile_ranges), nt,
-                                                     lruns);
-        lpt_merge<<<(unsigned)((nruns * (int64_t)kLptRun + 255) / 256), 256, 0, ls>>>(lruns, nt,
-                                                                                   lpt_order);
-    }
-    if (side) {
-        err = cudaEventRecord(side->join, side->stream);
+        err = launch(lpt_sort_runs, nruns, kLptRun / 2, 0, ls, (const int2*)ranges, nt, lruns);
+        if (err != cudaSuccess) return err;
+        err = launch(lpt_merge, (unsigned)((nruns * (int64_t)kLptRun + 255) / 256), 256, 0, ls,
+                     (const uint64_t*)lruns, nt, lpt_order);
         if (err != cudaSuccess) return err;
     }
     if (n > 0) {
+        // 3. the pairs into their tiles' slices
         const unsigned grid = (unsigned)std::max<int64_t>(
             1, std::min<int64_t>((capacity + 255) / 256, 8 * (int64_t)sms));
-        bucket_scatter<<<grid, 256, 0, st>>>(raw, depths, cursor, capacity, keys, counts);
+        err = launch(bucket_scatter, grid, 256, 0, st, (const uint2*)raw, depths, cursor, capacity,
+                     keys, (const int64_t*)counts);
+        if (err != cudaSuccess) return err;
+        // 4. the short slices on st; the medium and long ones (other tiles, other
+        // parts of the key and id lists) beside them on the side stream
+        cudaStream_t ms = st;
+        if (side) {
+            err = cudaEventRecord(side->fork2, st);
+            if (err != cudaSuccess) return err;
+            err = cudaStreamWaitEvent(side->stream, side->fork2, 0);
+            if (err != cudaSuccess) return err;
+            ms = side->stream;
+        }
         const unsigned sg = (unsigned)std::max<int64_t>(
             1, std::min<int64_t>((nt + kSmallWarps - 1) / kSmallWarps, 16 * (int64_t)sms));
-        bucket_sort_small<<<sg, 32 * kSmallWarps, 0, st>>>(ranges, nt, keys, sorted_ids);
+        err = launch(bucket_sort_small, sg, 32 * kSmallWarps, 0, st, (const int2*)ranges, nt,
+                     (const uint64_t*)keys, sorted_ids);
+        if (err != cudaSuccess) return err;
         const size_t sbytes = 2 * sk_len(kBlockSortMax) * sizeof(uint64_t);
         err = cudaFuncSetAttribute(bucket_sort_medium, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)sbytes);
@@ -688,18 +769,25 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
                                    (int)sbytes);
         if (err != cudaSuccess) return err;
         const unsigned mg = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nt, 3 * (int64_t)sms));
-        bucket_sort_medium<<<mg, kSortThreads, sbytes, st>>>(ranges, medium, keys, sorted_ids, counts);
+        err = launch(bucket_sort_medium, mg, kSortThreads, sbytes, ms, (const int2*)ranges,
+                     (const int32_t*)medium, (const uint64_t*)keys, sorted_ids,
+                     (const int64_t*)counts);
+        if (err != cudaSuccess) return err;
         // the raw list is free again: it is the long slices' second merge buffer
-        bucket_sort_large<<<(unsigned)std::max<int64_t>(1, std::min<int64_t>(nt, 2 * (int64_t)sms)),
-                            kSortThreads, sbytes, st>>>(ranges, large, keys,
-                                                        reinterpret_cast<uint64_t*>(raw), sorted_ids,
-                                                        counts);
-    }
-    if (side) {
-        err = cudaStreamWaitEvent(st, side->join, 0);  // the LPT order is ready
+        const unsigned lg = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nt, 2 * (int64_t)sms));
+        err = launch(bucket_sort_large, lg, kSortThreads, sbytes, ms, (const int2*)ranges,
+                     (const int32_t*)large, keys, reinterpret_cast<uint64_t*>(raw), sorted_ids,
+                     (const int64_t*)counts);
         if (err != cudaSuccess) return err;
     }
-    return cudaGetLastError();
+    if (side) {
+        // the LPT order and the medium and long slices are done
+        err = cudaEventRecord(side->join, side->stream);
+        if (err != cudaSuccess) return err;
+        err = cudaStreamWaitEvent(st, side->join, 0);
+        if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace gs

@@ -45,6 +45,16 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Programmatic dependent launch: every kernel starts with this.  It waits
+// until the kernel launched before it on the stream has completed and its
+// writes are visible (immediately, when it was launched without the
+// programmatic-serialisation attribute), then lets the next kernel on the
+// stream begin launching while this one runs.
+__device__ __forceinline__ void grid_dep_sync() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 16-byte asynchronous global -> shared copies; complete for the calling
 // thread after cp_async_wait<N> (all but the N most recent groups)
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {

@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "../../include/gs.h"
 
 namespace gs {
@@ -44,11 +46,30 @@ struct BinSortLayout {
 };
 BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles);
 
+// Launch a kernel on st with programmatic stream serialisation: it may begin
+// launching while the kernel before it on st still runs, and waits for that
+// kernel's completion in its first statement (grid_dep_sync).
+template <typename... P, typename... A>
+inline cudaError_t launch(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, A&&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
+
 // A second stream with fork / join events: work that depends only on an
 // earlier step runs on it beside the main sequence and is joined back.
 struct SideStream {
     cudaStream_t stream;
-    cudaEvent_t fork, join;
+    cudaEvent_t fork, fork2, join;
 };
 
 // gs_bin_sort with its argument checks; overlap = false keeps every launch in
@@ -63,7 +84,8 @@ gs_status bin_sort_entry(const gs_camera* cam, int64_t n, const float* splats,
 cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, const float* depths,
                          const int32_t* tiles_touched, char* ws, const BinSortLayout& L,
                          int32_t* sorted_ids, int64_t capacity, int32_t* tile_ranges,
-                         int32_t* lpt_order, cudaStream_t st, const SideStream* side);
+                         int32_t* lpt_order, int64_t* counts_out, cudaStream_t st,
+                         const SideStream* side);
 
 // ---- rasterization (gs_raster.cu) ------------------------------------------
 struct RasterConfig {

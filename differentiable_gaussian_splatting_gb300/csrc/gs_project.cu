@@ -298,6 +298,7 @@ __global__ void __launch_bounds__(kProjThreads) project_kernel(CamParams cam, in
                                                       float* __restrict__ depths,
                                                       int2* __restrict__ radii,
                                                       int* __restrict__ tiles_touched) {
+    grid_dep_sync();
     __shared__ ProjShared S;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t i = (int64_t)blockIdx.x * kProjThreads + tid;
@@ -433,13 +434,16 @@ cudaError_t launch_project(const CamParams& cam, int64_t n, int sh_degree, const
     auto q4 = reinterpret_cast<const float4*>(quats);
     auto s4 = reinterpret_cast<float4*>(splats);
     auto r2 = reinterpret_cast<int2*>(radii);
+    auto go = [&](auto kernel) {
+        return launch(kernel, grid, block, 0, st, cam, n, means, scales, q4, opacities, sh, s4,
+                      depths, r2, tiles_touched);
+    };
     switch (sh_degree) {
-        case 0: project_kernel<1><<<grid, block, 0, st>>>(cam, n, means, scales, q4, opacities, sh, s4, depths, r2, tiles_touched); break;
-        case 1: project_kernel<4><<<grid, block, 0, st>>>(cam, n, means, scales, q4, opacities, sh, s4, depths, r2, tiles_touched); break;
-        case 2: project_kernel<9><<<grid, block, 0, st>>>(cam, n, means, scales, q4, opacities, sh, s4, depths, r2, tiles_touched); break;
-        default: project_kernel<16><<<grid, block, 0, st>>>(cam, n, means, scales, q4, opacities, sh, s4, depths, r2, tiles_touched); break;
+        case 0: return go(project_kernel<1>);
+        case 1: return go(project_kernel<4>);
+        case 2: return go(project_kernel<9>);
+        default: return go(project_kernel<16>);
     }
-    return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
@@ -459,6 +463,7 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
     const int* __restrict__ tiles_touched, const float* __restrict__ grad2d,
     const uint8_t* __restrict__ touched, float* __restrict__ dmeans, float* __restrict__ dscales,
     float4* __restrict__ dquats, float* __restrict__ dopac, float* __restrict__ dsh) {
+    grid_dep_sync();
     constexpr int RW = K * 3;                       // floats per SH row
     constexpr bool kVec = (RW % 4) == 0;            // rows of whole float4
     __shared__ float srow[kPbThreads / 32][32 * RW];
@@ -681,13 +686,16 @@ cudaError_t launch_project_bwd(const CamParams& cam, int64_t n, int sh_degree, c
     dim3 block(kPbThreads), grid((unsigned)((n + kPbThreads - 1) / kPbThreads));
     auto q4 = reinterpret_cast<const float4*>(quats);
     auto dq4 = reinterpret_cast<float4*>(dquats);
+    auto go = [&](auto kernel) {
+        return launch(kernel, grid, block, 0, st, cam, n, means, scales, q4, sh, tiles_touched,
+                      grad2d, touched, dmeans, dscales, dq4, dopacities, dsh);
+    };
     switch (sh_degree) {
-        case 0: project_bwd_kernel<1><<<grid, block, 0, st>>>(cam, n, means, scales, q4, sh, tiles_touched, grad2d, touched, dmeans, dscales, dq4, dopacities, dsh); break;
-        case 1: project_bwd_kernel<4><<<grid, block, 0, st>>>(cam, n, means, scales, q4, sh, tiles_touched, grad2d, touched, dmeans, dscales, dq4, dopacities, dsh); break;
-        case 2: project_bwd_kernel<9><<<grid, block, 0, st>>>(cam, n, means, scales, q4, sh, tiles_touched, grad2d, touched, dmeans, dscales, dq4, dopacities, dsh); break;
-        default: project_bwd_kernel<16><<<grid, block, 0, st>>>(cam, n, means, scales, q4, sh, tiles_touched, grad2d, touched, dmeans, dscales, dq4, dopacities, dsh); break;
+        case 0: return go(project_bwd_kernel<1>);
+        case 1: return go(project_bwd_kernel<4>);
+        case 2: return go(project_bwd_kernel<9>);
+        default: return go(project_bwd_kernel<16>);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace gs

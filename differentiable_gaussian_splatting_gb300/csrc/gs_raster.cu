@@ -218,6 +218,7 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
                                                                 const int2* __restrict__ ranges,
                                                                 int nt, int K, RasterConfig cfg,
                                                                 int* ctrl, int* sat, int* done) {
+    grid_dep_sync();
     __shared__ long long s_tot[kPolicyThreads / 32];
     __shared__ uint64_t s_cost[kPolicyThreads / 32];
     __shared__ int s_cand[kPolicyThreads / 32];
@@ -344,6 +345,7 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
 // forward: persistent kernel over whole tiles and depth chunks
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 5) raster_fwd_kernel(RasterArgs A) {
+    grid_dep_sync();
     __shared__ Smem S;
     const int tid = threadIdx.x;
     const int h = A.ctrl[kCtlH], k = A.ctrl[kCtlK], nitems = A.ctrl[kCtlItems];
@@ -700,7 +702,33 @@ __device__ __forceinline__ void load_bwd_pixel(const RasterArgs& A, const WorkIt
     }
 }
 
+// The accumulators of the backward to zero: grad2d (nf floats, 16-byte
+// aligned), the touched flags (n bytes, any alignment; may be null) and the
+// work-queue counter.
+__global__ void __launch_bounds__(256) bwd_zero(float* __restrict__ grad2d, int64_t nf,
+                                                uint8_t* __restrict__ touched, int64_t n,
+                                                int* __restrict__ queue) {
+    grid_dep_sync();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t n4 = nf / 4;
+    float4* g4 = reinterpret_cast<float4*>(grad2d);
+    for (int64_t i = i0; i < n4; i += stride) g4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t i = 4 * n4 + i0; i < nf; i += stride) grad2d[i] = 0.f;
+    if (touched) {
+        // bytes up to the first 16-byte boundary, 16-byte words, the tail
+        const int64_t head = min64(n, (int64_t)((16u - (reinterpret_cast<uintptr_t>(touched) & 15u)) & 15u));
+        const int64_t n16 = (n - head) / 16;
+        uint4* t16 = reinterpret_cast<uint4*>(touched + head);
+        if (i0 < head) touched[i0] = 0;
+        for (int64_t i = i0; i < n16; i += stride) t16[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int64_t i = head + 16 * n16 + i0; i < n; i += stride) touched[i] = 0;
+    }
+    if (i0 == 0) *queue = 0;
+}
+
 __global__ void __launch_bounds__(kBwdThreads, 6) raster_bwd_kernel(RasterArgs A) {
+    grid_dep_sync();
     __shared__ BwdSlice SL[kBwdWarps][2];  // double-buffered per warp
     const unsigned F = 0xffffffffu;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -877,10 +905,10 @@ cudaError_t run_raster_fwd(const CamParams& cam, const RasterConfig& cfg, const 
     A.n_contrib = n_contrib;
     A.last_idx = last_idx;
     const int nt = cam.ntx * cam.nty;
-    policy_kernel<<<1, kPolicyThreads, 0, st>>>(lpt_order, A.ranges, nt, K, cfg, A.ctrl, A.sat,
-                                                A.done);
-    raster_fwd_kernel<<<K, kThreads, 0, st>>>(A);
-    return cudaGetLastError();
+    cudaError_t err = launch(policy_kernel, 1, kPolicyThreads, 0, st, lpt_order,
+                             (const int2*)A.ranges, nt, K, cfg, A.ctrl, A.sat, A.done);
+    if (err != cudaSuccess) return err;
+    return launch(raster_fwd_kernel, K, kThreads, 0, st, A);
 }
 
 cudaError_t run_raster_bwd(const CamParams& cam, const RasterConfig& cfg, int64_t n,
@@ -900,19 +928,15 @@ cudaError_t run_raster_bwd(const CamParams& cam, const RasterConfig& cfg, int64_
     A.dT = dL_dt;
     A.grad2d = grad2d;
     A.touched = touched;
-    cudaError_t err;
-    if (n > 0) {
-        err = cudaMemsetAsync(grad2d, 0, (size_t)n * 9 * sizeof(float), st);
-        if (err != cudaSuccess) return err;
-        if (touched) {
-            err = cudaMemsetAsync(touched, 0, (size_t)n, st);
-            if (err != cudaSuccess) return err;
-        }
-    }
-    err = cudaMemsetAsync(A.ctrl + kCtlQueueBwd, 0, sizeof(int), st);
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t nf = n * 9;
+    const int64_t zb = std::max<int64_t>(1, std::min<int64_t>((nf / 4 + 255) / 256,
+                                                               8 * (int64_t)std::max(sms, 1)));
+    cudaError_t err = launch(bwd_zero, (unsigned)zb, 256, 0, st, grad2d, nf, touched, n,
+                             A.ctrl + kCtlQueueBwd);
     if (err != cudaSuccess) return err;
-    raster_bwd_kernel<<<K, kBwdThreads, 0, st>>>(A);
-    return cudaGetLastError();
+    return launch(raster_bwd_kernel, K, kBwdThreads, 0, st, A);
 }
 
 }  // namespace gs
