@@ -482,38 +482,8 @@ __device__ __forceinline__ uint64_t* block_sort_keys(uint64_t* A, uint64_t* B) {
     return block_merge_rounds(B, A, C, kWarps * C);
 }
 
-// slices of kWarpSortMax + 1 .. kBlockSortMax keys: one block each, in shared memory
-__global__ void __launch_bounds__(kSortThreads) bucket_sort_medium(const int2* __restrict__ ranges,
-                                                                   const int32_t* __restrict__ list,
-                                                                   const uint64_t* __restrict__ keys,
-                                                                   int32_t* __restrict__ sorted_ids,
-                                                                   const int64_t* __restrict__ counts) {
-    grid_dep_sync();
-    extern __shared__ uint64_t smem[];
-    uint64_t* A = smem;                            // sk_len(kBlockSortMax)
-    uint64_t* B = smem + sk_len(kBlockSortMax);    // sk_len(kBlockSortMax)
-    const int tid = threadIdx.x;
-    const int64_t nm = counts[kCountMedium];
-    for (int64_t m = blockIdx.x; m < nm; m += gridDim.x) {
-        const int2 r = ranges[list[m]];
-        const int cnt = r.y - r.x;
-        int P = 2 * kWarpSortMax;
-        while (P < cnt) P <<= 1;
-        for (int e = tid; e < P; e += kSortThreads) A[sk_idx(e)] = e < cnt ? keys[r.x + e] : ~0ull;
-        __syncthreads();
-        const uint64_t* out = P == 1024 ? block_sort_keys<4>(A, B)
-                              : P == 2048 ? block_sort_keys<8>(A, B)
-                                          : block_sort_keys<16>(A, B);
-        for (int e = tid; e < cnt; e += kSortThreads)
-            sorted_ids[r.x + e] = (int32_t)(uint32_t)out[sk_idx(e)];
-        __syncthreads();
-    }
-}
-
-// slices longer than kBlockSortMax: one block each, through global memory.
-// Chunks of kBlockSortMax are sorted in shared memory as above into buf0, then
-// runs are merged pairwise (merge path) between buf0 and buf1 until one run
-// remains; the ids are written by the last pass.
+// number of elements of run a among the first k of merge(a[0, na), b[0, nb)),
+// both in global memory (keys are unique)
 __device__ __forceinline__ int merge_split_g(const uint64_t* a, int na, const uint64_t* b, int nb,
                                              int k) {
     int lo = max(0, k - nb), hi = min(k, na);
@@ -525,59 +495,91 @@ __device__ __forceinline__ int merge_split_g(const uint64_t* a, int na, const ui
     return lo;
 }
 
-__global__ void __launch_bounds__(kSortThreads) bucket_sort_large(const int2* __restrict__ ranges,
-                                                                  const int32_t* __restrict__ list,
-                                                                  uint64_t* __restrict__ buf0,
-                                                                  uint64_t* __restrict__ buf1,
-                                                                  int32_t* __restrict__ sorted_ids,
-                                                                  const int64_t* __restrict__ counts) {
-    grid_dep_sync();
-    extern __shared__ uint64_t smem[];
-    uint64_t* A = smem;
-    uint64_t* B = smem + sk_len(kBlockSortMax);
+// One block sorts a slice of kWarpSortMax + 1 .. kBlockSortMax keys in shared
+// memory (A, B: sk_len(kBlockSortMax) words each) and writes its ids.
+__device__ __forceinline__ void sort_medium_slice(int2 r, const uint64_t* __restrict__ keys,
+                                                  int32_t* __restrict__ sorted_ids, uint64_t* A,
+                                                  uint64_t* B) {
     const int tid = threadIdx.x;
-    const int64_t nl = counts[kCountLarge];
-    for (int64_t m = blockIdx.x; m < nl; m += gridDim.x) {
-        const int2 r = ranges[list[m]];
-        const int cnt = r.y - r.x;
-        const int64_t s = r.x;
-        // sort chunks of kBlockSortMax in shared memory, written back to buf0
-        for (int c0 = 0; c0 < cnt; c0 += kBlockSortMax) {
-            const int n = min(kBlockSortMax, cnt - c0);
-            for (int e = tid; e < kBlockSortMax; e += kSortThreads)
-                A[sk_idx(e)] = e < n ? buf0[s + c0 + e] : ~0ull;
-            __syncthreads();
-            const uint64_t* out = block_sort_keys<16>(A, B);
-            for (int e = tid; e < n; e += kSortThreads) buf0[s + c0 + e] = out[sk_idx(e)];
-            __syncthreads();
-        }
-        uint64_t* src = buf0;
-        uint64_t* dst = buf1;
-        for (int width = kBlockSortMax; width < cnt; width <<= 1) {
-            const bool last = 2 * width >= cnt;
-            for (int p0 = 0; p0 < cnt; p0 += 2 * width) {
-                const int na = min(width, cnt - p0);
-                const int nb = min(width, cnt - p0 - na);
-                const uint64_t* Ag = src + s + p0;
-                const uint64_t* Bg = Ag + na;
-                const int tot = na + nb;
-                const int per = (tot + kSortThreads - 1) / kSortThreads;
-                const int k0 = min(tid * per, tot), k1 = min(k0 + per, tot);
-                if (k0 < k1) {
-                    int i = merge_split_g(Ag, na, Bg, nb, k0), j = k0 - i;
-                    for (int k = k0; k < k1; ++k) {
-                        const bool takeA = j >= nb || (i < na && Ag[i] < Bg[j]);
-                        const uint64_t v = takeA ? Ag[i++] : Bg[j++];
-                        if (last) sorted_ids[s + p0 + k] = (int32_t)(uint32_t)v;
-                        else dst[s + p0 + k] = v;
-                    }
+    const int cnt = r.y - r.x;
+    int P = 2 * kWarpSortMax;
+    while (P < cnt) P <<= 1;
+    for (int e = tid; e < P; e += kSortThreads) A[sk_idx(e)] = e < cnt ? keys[r.x + e] : ~0ull;
+    __syncthreads();
+    const uint64_t* out = P == 1024 ? block_sort_keys<4>(A, B)
+                          : P == 2048 ? block_sort_keys<8>(A, B)
+                                      : block_sort_keys<16>(A, B);
+    for (int e = tid; e < cnt; e += kSortThreads)
+        sorted_ids[r.x + e] = (int32_t)(uint32_t)out[sk_idx(e)];
+    __syncthreads();
+}
+
+// One block sorts a slice of more than kBlockSortMax keys: chunks of
+// kBlockSortMax in shared memory, then merge-path rounds between buf0 and buf1
+// in global memory; the last round writes the ids.
+__device__ __forceinline__ void sort_large_slice(int2 r, uint64_t* __restrict__ buf0,
+                                                 uint64_t* __restrict__ buf1,
+                                                 int32_t* __restrict__ sorted_ids, uint64_t* A,
+                                                 uint64_t* B) {
+    const int tid = threadIdx.x;
+    const int cnt = r.y - r.x;
+    const int64_t s = r.x;
+    for (int c0 = 0; c0 < cnt; c0 += kBlockSortMax) {
+        const int n = min(kBlockSortMax, cnt - c0);
+        for (int e = tid; e < kBlockSortMax; e += kSortThreads)
+            A[sk_idx(e)] = e < n ? buf0[s + c0 + e] : ~0ull;
+        __syncthreads();
+        const uint64_t* out = block_sort_keys<16>(A, B);
+        for (int e = tid; e < n; e += kSortThreads) buf0[s + c0 + e] = out[sk_idx(e)];
+        __syncthreads();
+    }
+    uint64_t* src = buf0;
+    uint64_t* dst = buf1;
+    for (int width = kBlockSortMax; width < cnt; width <<= 1) {
+        const bool last = 2 * width >= cnt;
+        for (int p0 = 0; p0 < cnt; p0 += 2 * width) {
+            const int na = min(width, cnt - p0);
+            const int nb = min(width, cnt - p0 - na);
+            const uint64_t* Ag = src + s + p0;
+            const uint64_t* Bg = Ag + na;
+            const int tot = na + nb;
+            const int per = (tot + kSortThreads - 1) / kSortThreads;
+            const int k0 = min(tid * per, tot), k1 = min(k0 + per, tot);
+            if (k0 < k1) {
+                int i = merge_split_g(Ag, na, Bg, nb, k0), j = k0 - i;
+                for (int k = k0; k < k1; ++k) {
+                    const bool takeA = j >= nb || (i < na && Ag[i] < Bg[j]);
+                    const uint64_t v = takeA ? Ag[i++] : Bg[j++];
+                    if (last) sorted_ids[s + p0 + k] = (int32_t)(uint32_t)v;
+                    else dst[s + p0 + k] = v;
                 }
             }
-            __syncthreads();
-            uint64_t* tmp = src;
-            src = dst;
-            dst = tmp;
         }
+        __syncthreads();
+        uint64_t* tmp = src;
+        src = dst;
+        dst = tmp;
+    }
+}
+
+// The slices the warps do not take, one block each: the long ones first (they
+// take longest), then the medium ones.  keys doubles as the long slices' first
+// merge buffer and buf1 (the raw list, free by now) as their second.
+__global__ void __launch_bounds__(kSortThreads) bucket_sort_blocks(const int2* __restrict__ ranges,
+                                                                   const int32_t* __restrict__ medium,
+                                                                   const int32_t* __restrict__ large,
+                                                                   uint64_t* __restrict__ keys,
+                                                                   uint64_t* __restrict__ buf1,
+                                                                   int32_t* __restrict__ sorted_ids,
+                                                                   const int64_t* __restrict__ counts) {
+    grid_dep_sync();
+    extern __shared__ uint64_t smem[];
+    uint64_t* A = smem;                            // sk_len(kBlockSortMax)
+    uint64_t* B = smem + sk_len(kBlockSortMax);    // sk_len(kBlockSortMax)
+    const int64_t nm = counts[kCountMedium], nl = counts[kCountLarge];
+    for (int64_t m = blockIdx.x; m < nl + nm; m += gridDim.x) {
+        if (m < nl) sort_large_slice(ranges[large[m]], keys, buf1, sorted_ids, A, B);
+        else sort_medium_slice(ranges[medium[m - nl]], keys, sorted_ids, A, B);
     }
 }
 
@@ -762,22 +764,14 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
                      (const uint64_t*)keys, sorted_ids);
         if (err != cudaSuccess) return err;
         const size_t sbytes = 2 * sk_len(kBlockSortMax) * sizeof(uint64_t);
-        err = cudaFuncSetAttribute(bucket_sort_medium, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        err = cudaFuncSetAttribute(bucket_sort_blocks, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)sbytes);
-        if (err != cudaSuccess) return err;
-        err = cudaFuncSetAttribute(bucket_sort_large, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)sbytes);
-        if (err != cudaSuccess) return err;
-        const unsigned mg = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nt, 3 * (int64_t)sms));
-        err = launch(bucket_sort_medium, mg, kSortThreads, sbytes, ms, (const int2*)ranges,
-                     (const int32_t*)medium, (const uint64_t*)keys, sorted_ids,
-                     (const int64_t*)counts);
         if (err != cudaSuccess) return err;
         // the raw list is free again: it is the long slices' second merge buffer
-        const unsigned lg = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nt, 2 * (int64_t)sms));
-        err = launch(bucket_sort_large, lg, kSortThreads, sbytes, ms, (const int2*)ranges,
-                     (const int32_t*)large, keys, reinterpret_cast<uint64_t*>(raw), sorted_ids,
-                     (const int64_t*)counts);
+        const unsigned mg = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nt, 3 * (int64_t)sms));
+        err = launch(bucket_sort_blocks, mg, kSortThreads, sbytes, ms, (const int2*)ranges,
+                     (const int32_t*)medium, (const int32_t*)large, keys,
+                     reinterpret_cast<uint64_t*>(raw), sorted_ids, (const int64_t*)counts);
         if (err != cudaSuccess) return err;
     }
     if (side) {

@@ -186,11 +186,12 @@ __device__ __forceinline__ bool blend_range(const RasterArgs& A, Smem& S, int tx
                 st.cb = fmaf(w, r2.z, st.cb);
                 st.T = st.T * (1.f - alpha);
                 // branch-free bookkeeping (no reconvergence point in the loop)
-                st.n += hit ? 1 : 0;
-                st.last = hit ? pos0 + idx : st.last;
                 blended |= (hit ? 1u : 0u) << q;
                 st.done = st.done || (st.T < kTMin);
             }
+            // the chunk's hits, in order: their count, and the last one
+            st.n += __popc(blended);
+            st.last = blended ? pos0 + c + 31 - __clz(blended) : st.last;
             if (write_cmask) {
                 blended = __reduce_or_sync(0xffffffffu, blended);
                 if (lane == 0) S.cm[warp * (kBatch / 32) + (c >> 5)] = blended;
