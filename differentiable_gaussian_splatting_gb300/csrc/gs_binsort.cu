@@ -26,6 +26,8 @@
 
 #include <algorithm>
 
+#include <cooperative_groups.h>
+
 #include "gs_device.cuh"
 #include "gs_internal.h"
 
@@ -169,7 +171,7 @@ __global__ void __launch_bounds__(kEmitThreads) bucket_emit(CamParams cam,
 }
 
 // ---------------------------------------------------------------------------
-// 2. one block: tile ranges from the exclusive scan of the counts, the bucket
+// 2. one cluster: tile ranges from the exclusive scan of the counts, the bucket
 // cursors, I and min(I, capacity).  When I > capacity the list cannot be
 // built; every range is then empty, so nothing downstream reads it.
 // ---------------------------------------------------------------------------
@@ -219,6 +221,12 @@ __device__ __forceinline__ int size_class(int c) {
     return c > kBlockSortMax ? 2 : (c > kWarpSortMax ? 1 : 0);
 }
 
+// The scan runs on a cluster of kScanCluster blocks (one per SM), each over a
+// contiguous share of the tiles; the blocks' totals are exchanged through
+// distributed shared memory, so the strided counter reads and the range and
+// start writes spread over kScanCluster SMs.
+constexpr int kScanCluster = 8;
+
 __global__ void __launch_bounds__(kScanThreads) bucket_scan(const int* __restrict__ tile_count,
                                                             int64_t nt, int64_t capacity,
                                                             int2* __restrict__ ranges,
@@ -228,52 +236,100 @@ __global__ void __launch_bounds__(kScanThreads) bucket_scan(const int* __restric
                                                             int64_t* __restrict__ counts,
                                                             int64_t* __restrict__ counts_out) {
     grid_dep_sync();
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
     __shared__ int64_t s_a[kScanThreads / 32], s_b[kScanThreads / 32];
-    const int tid = threadIdx.x;
-    const int64_t per = (nt + kScanThreads - 1) / kScanThreads;
-    const int64_t lo = min64(nt, per * tid), hi = min64(nt, lo + per);
-    // per thread: its pair count and, packed, its medium (low word) and large
-    // (high word) tile counts -- each below 2^32, as nt is
-    int64_t run = 0, cls = 0;
-    int c[kScanRegs];
-    if (per <= kScanRegs) {
-#pragma unroll
-        for (int i = 0; i < kScanRegs; ++i)
-            c[i] = lo + i < hi ? tile_count[(lo + i) * kCountStride] : 0;
-#pragma unroll
-        for (int i = 0; i < kScanRegs; ++i) {
-            run += c[i];
-            const int k = size_class(c[i]);
-            cls += k == 1 ? 1ll : (k == 2 ? (1ll << 32) : 0ll);
-        }
-    } else {
-        for (int64_t t = lo; t < hi; ++t) {
-            const int ct = tile_count[t * kCountStride];
-            run += ct;
-            const int k = size_class(ct);
-            cls += k == 1 ? 1ll : (k == 2 ? (1ll << 32) : 0ll);
-        }
-    }
-    int64_t total, tcls;
-    scan_block2(run, cls, s_a, s_b, &total, &tcls);
-    const bool fits = total <= capacity;
-    int64_t om = cls & 0xffffffffll, ol = cls >> 32;
-    auto emit = [&](int64_t t, int ct) {
-        ranges[t] = fits ? make_int2((int)run, (int)(run + ct)) : make_int2(0, 0);
-        cursor[t * kCursorStride] = (unsigned long long)run;
-        run += ct;
-        const int k = size_class(ct);
-        if (k == 1) medium[om++] = (int32_t)t;
-        if (k == 2) large[ol++] = (int32_t)t;
+    __shared__ int64_t s_tot[2];  // this block's pair count and packed class counts
+    __shared__ int64_t s_off[4];  // offsets from the lower blocks; totals of all
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int rank = (int)cluster.block_rank();
+    const int64_t share = (nt + kScanCluster - 1) / kScanCluster;
+    const int64_t b0 = min64(nt, share * rank), b1 = min64(nt, b0 + share);
+    const int64_t per = (b1 - b0 + kScanThreads - 1) / kScanThreads;
+    // consecutive threads take consecutive tiles: step k covers tiles
+    // b0 + k kScanThreads + tid.  A tile's size class is packed into one int64
+    // (medium: low word, large: high word; both counts are below 2^32, as nt is)
+    auto cls_of = [](int ct) -> int64_t {
+        const int z = size_class(ct);
+        return z == 1 ? 1ll : (z == 2 ? (1ll << 32) : 0ll);
     };
-    if (per <= kScanRegs) {
+    const bool in_regs = per <= kScanRegs;
+    int c[kScanRegs];
+    int64_t tr = 0, tc = 0;  // this thread's pair count and packed class counts
+    if (in_regs) {
 #pragma unroll
-        for (int i = 0; i < kScanRegs; ++i)
-            if (lo + i < hi) emit(lo + i, c[i]);
+        for (int k = 0; k < kScanRegs; ++k) {
+            const int64_t t = b0 + (int64_t)k * kScanThreads + tid;
+            c[k] = k < per && t < b1 ? tile_count[t * kCountStride] : 0;
+            tr += c[k];
+            tc += cls_of(c[k]);
+        }
     } else {
-        for (int64_t t = lo; t < hi; ++t) emit(t, tile_count[t * kCountStride]);
+        for (int64_t t = b0 + tid; t < b1; t += kScanThreads) {
+            const int ct = tile_count[t * kCountStride];
+            tr += ct;
+            tc += cls_of(ct);
+        }
     }
+    int64_t blk_run, blk_cls;  // this block's totals
+    scan_block2(tr, tc, s_a, s_b, &blk_run, &blk_cls);
     if (tid == 0) {
+        s_tot[0] = blk_run;
+        s_tot[1] = blk_cls;
+    }
+    cluster.sync();
+    if (tid < 32) {
+        int64_t a = 0, b = 0;
+        if (lane < kScanCluster) {
+            const int64_t* t = cluster.map_shared_rank(s_tot, lane);
+            a = t[0];
+            b = t[1];
+        }
+        int64_t ea = lane < rank ? a : 0, eb = lane < rank ? b : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            ea += __shfl_xor_sync(0xffffffffu, ea, o);
+            eb += __shfl_xor_sync(0xffffffffu, eb, o);
+            a += __shfl_xor_sync(0xffffffffu, a, o);
+            b += __shfl_xor_sync(0xffffffffu, b, o);
+        }
+        if (lane == 0) {
+            s_off[0] = ea;
+            s_off[1] = eb;
+            s_off[2] = a;
+            s_off[3] = b;
+        }
+    }
+    __syncthreads();
+    const int64_t total = s_off[2], tcls = s_off[3];
+    const bool fits = total <= capacity;
+    int64_t carry_run = s_off[0], carry_cls = s_off[1];  // pairs / classes before this step
+    for (int64_t k = 0; k < per; ++k) {
+        __syncthreads();  // s_a / s_b are free again
+        const int64_t t = b0 + k * kScanThreads + tid;
+        int ct = 0;
+        if (in_regs) {
+#pragma unroll
+            for (int q = 0; q < kScanRegs; ++q)
+                if (q == k) ct = c[q];
+        } else if (t < b1) {
+            ct = tile_count[t * kCountStride];
+        }
+        int64_t r = ct, q = cls_of(ct), sr, sq;
+        scan_block2(r, q, s_a, s_b, &sr, &sq);
+        r += carry_run;
+        q += carry_cls;
+        if (t < b1) {
+            ranges[t] = fits ? make_int2((int)r, (int)(r + ct)) : make_int2(0, 0);
+            cursor[t * kCursorStride] = (unsigned long long)r;
+            const int z = size_class(ct);
+            if (z == 1) medium[q & 0xffffffffll] = (int32_t)t;
+            if (z == 2) large[q >> 32] = (int32_t)t;
+        }
+        carry_run += sr;
+        carry_cls += sq;
+    }
+    if (rank == 0 && tid == 0) {
         counts[1] = total;
         counts[2] = fits ? total : capacity;
         counts[kCountMedium] = fits ? (tcls & 0xffffffffll) : 0;
@@ -283,6 +339,7 @@ __global__ void __launch_bounds__(kScanThreads) bucket_scan(const int* __restric
             counts_out[1] = total;
         }
     }
+    cluster.sync();  // s_tot stays readable until every block has read it
 }
 
 // ---------------------------------------------------------------------------
@@ -720,8 +777,9 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
                      tcount, raw, counts);
         if (err != cudaSuccess) return err;
     }
-    err = launch(bucket_scan, 1, kScanThreads, 0, st, (const int*)tcount, nt, capacity, ranges,
-                 cursor, medium, large, counts, counts_out);
+    err = launch_clustered(bucket_scan, kScanCluster, kScanCluster, kScanThreads, 0, st,
+                           (const int*)tcount, nt, capacity, ranges, cursor, medium, large, counts,
+                           counts_out);
     if (err != cudaSuccess) return err;
     // 5. LPT order (tiles by descending count, ties by tile id) needs only the
     // ranges: on the side stream, when given, it runs beside steps 3 and 4

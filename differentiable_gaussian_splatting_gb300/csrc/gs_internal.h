@@ -48,21 +48,32 @@ BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles);
 
 // Launch a kernel on st with programmatic stream serialisation: it may begin
 // launching while the kernel before it on st still runs, and waits for that
-// kernel's completion in its first statement (grid_dep_sync).
+// kernel's completion in its first statement (grid_dep_sync).  cluster > 1
+// groups the blocks into thread-block clusters of that many blocks.
 template <typename... P, typename... A>
-inline cudaError_t launch(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
-                          cudaStream_t st, A&&... args) {
-    cudaLaunchAttribute attr[1];
+inline cudaError_t launch_clustered(void (*kernel)(P...), unsigned cluster, dim3 grid, dim3 block,
+                                    size_t smem, cudaStream_t st, A&&... args) {
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = cluster > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
+
+template <typename... P, typename... A>
+inline cudaError_t launch(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, A&&... args) {
+    return launch_clustered(kernel, 1, grid, block, smem, st, std::forward<A>(args)...);
 }
 
 // A second stream with fork / join events: work that depends only on an

@@ -173,6 +173,17 @@ def test_edge_cases():
     assert g.n_pairs == 0 and np.all(g.T == 1)
 
 
+def test_binning_on_a_large_tile_grid():
+    # 275 x 263 = 72325 tiles: more than the tile-count scan keeps in registers, so
+    # its looping path runs; many tiles are empty
+    rng = np.random.default_rng(11)
+    sc, cam = ss.random_scene(rng, 20_000, 4400, 4200, sh_degree=0, log_scale=(-5.0, 0.5))
+    g = run_forward(sc, cam)
+    proj = oracle.project(sc, cam)
+    check_projection(g, proj, sc)
+    check_binning(g, oracle.bin_sort(cam, proj))
+
+
 def test_repeatable_integer_outputs():
     sc, cam = ss.make_config(2, n=50_000)
     a = run_forward(sc, cam)
