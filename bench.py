@@ -369,8 +369,8 @@ def step_roofline(ms, sc, M, I, E, H, W, peaks, n_sm, sm_mhz):
 
 def kernel_launches(n, capacity, W, H) -> int:
     """Kernels one step launches."""
-    # binning: counter reset, span pass, scan, scatter, three slice sorts, two LPT kernels
-    bin_sort = 1 + 1 + 1 + 1 + 3 + 2
+    # binning: counter reset, span pass, scan, scatter, two slice sorts, two LPT kernels
+    bin_sort = 1 + 1 + 1 + 1 + 2 + 2
     # project 1, policy + forward 2, accumulator reset + backward 2, project backward 1
     return 1 + bin_sort + 2 + 2 + 1
 
