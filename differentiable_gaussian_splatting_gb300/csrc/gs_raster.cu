@@ -667,13 +667,15 @@ __device__ __forceinline__ bool splat_terms2(const BwdSlice& S, int q, float px,
     float a0, b0, a1, b1, g0, g1, w0, w1;
     const bool act0 = row_step(r0, r1, r2, dx, dy0, q <= rel0, P0, &a0, &b0, &g0, &w0);
     const bool act1 = row_step(r0, r1, r2, dx, dy1, q <= rel1, P1, &a1, &b1, &g1, &w1);
-    v[0] = fmaf(g1, r0.z * a1, g0 * (r0.z * a0));
-    v[1] = fmaf(g1, fmaf(r0.w, a1, r1.x * b1), g0 * fmaf(r0.w, a0, r1.x * b0));
-    const float gdx0 = g0 * dx, gdx1 = g1 * dx;
-    v[2] = fmaf(gdx1, dx, gdx0 * dx);
-    v[3] = fmaf(gdx1, dy1, gdx0 * dy0);
-    v[4] = fmaf(g1 * dy1, dy1, (g0 * dy0) * dy0);
+    // the two rows share dx and the splat's factors: sum over the rows first
+    const float ga = fmaf(g1, a1, g0 * a0), gb = fmaf(g1, b1, g0 * b0);
+    v[0] = r0.z * ga;
+    v[1] = fmaf(r0.w, ga, r1.x * gb);
     v[5] = g0 + g1;
+    v[2] = (v[5] * dx) * dx;
+    const float gdy0 = g0 * dy0, gdy1 = g1 * dy1;
+    v[3] = (gdy0 + gdy1) * dx;
+    v[4] = fmaf(gdy1, dy1, gdy0 * dy0);
     v[6] = fmaf(w1, P1.Gr, w0 * P0.Gr);
     v[7] = fmaf(w1, P1.Gg, w0 * P0.Gg);
     v[8] = fmaf(w1, P1.Gb, w0 * P0.Gb);
