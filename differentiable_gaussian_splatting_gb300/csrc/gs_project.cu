@@ -466,7 +466,11 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
     grid_dep_sync();
     constexpr int RW = K * 3;                       // floats per SH row
     constexpr bool kVec = (RW % 4) == 0;            // rows of whole float4
-    __shared__ float srow[kPbThreads / 32][32 * RW];
+    // staged rows of whole float4 sit an odd number of float4 apart, so that the
+    // lanes' 16-byte accesses to their own rows fall in distinct bank groups
+    constexpr int R4 = kVec ? RW / 4 : 1;           // float4 per row
+    constexpr int RS = kVec ? 4 * (R4 | 1) : RW;    // floats from one staged row to the next
+    __shared__ __align__(16) float srow[kPbThreads / 32][32 * RS];
     __shared__ int slive[kPbThreads / 32][32];  // rank among the live lanes -> lane
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t wbase = (int64_t)blockIdx.x * kPbThreads + warp * 32;
@@ -491,7 +495,6 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
     // ---- stage the live rows (others read as zero and are never used)
     const uint32_t lmask = __ballot_sync(0xffffffffu, live);
     if constexpr (kVec) {
-        constexpr int R4 = RW / 4;
         const float4* sh4 = reinterpret_cast<const float4*>(sh);
         float4* my4 = reinterpret_cast<float4*>(my);
         const int nl = __popc(lmask);
@@ -500,7 +503,7 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
         for (int f = lane; f < nl * R4; f += 32) {
             const int rank = f / R4, col = f - rank * R4;
             const int l = slive[warp][rank];
-            cp_async16(&my4[l * R4 + col], sh4 + (wbase + l) * R4 + col);
+            cp_async16(&my4[l * (RS / 4) + col], sh4 + (wbase + l) * R4 + col);
         }
         cp_async_commit();  // waited for after the geometric part below
     } else {
@@ -621,19 +624,39 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
         float Y[16];
         sh_values(hx, hy, hz, Y);
         float gr = g[6], gg = g[7], gbl = g[8];
-        float* row = my + lane * RW;
+        float* row = my + lane * RS;
         float gdx = 0.f, gdy = 0.f, gdz = 0.f;
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-            const float c0 = row[3 * k], c1 = row[3 * k + 1], c2 = row[3 * k + 2];
-            row[3 * k] = Y[k] * gr;
-            row[3 * k + 1] = Y[k] * gg;
-            row[3 * k + 2] = Y[k] * gbl;
+        auto basis = [&](int k, float c0, float c1, float c2) {
             const float p = gr * c0 + gg * c1 + gbl * c2;
             const float3 dY = sh_grad(k, hx, hy, hz);
             gdx += p * dY.x;
             gdy += p * dY.y;
             gdz += p * dY.z;
+        };
+        if constexpr (kVec) {
+            // groups of four basis functions = three float4 of the row
+            float4* r4 = reinterpret_cast<float4*>(row);
+#pragma unroll
+            for (int q = 0; q < K / 4; ++q) {
+                const float4 v0 = r4[3 * q], v1 = r4[3 * q + 1], v2 = r4[3 * q + 2];
+                const float y0 = Y[4 * q], y1 = Y[4 * q + 1], y2 = Y[4 * q + 2], y3 = Y[4 * q + 3];
+                r4[3 * q] = make_float4(y0 * gr, y0 * gg, y0 * gbl, y1 * gr);
+                r4[3 * q + 1] = make_float4(y1 * gg, y1 * gbl, y2 * gr, y2 * gg);
+                r4[3 * q + 2] = make_float4(y2 * gbl, y3 * gr, y3 * gg, y3 * gbl);
+                basis(4 * q, v0.x, v0.y, v0.z);
+                basis(4 * q + 1, v0.w, v1.x, v1.y);
+                basis(4 * q + 2, v1.z, v1.w, v2.x);
+                basis(4 * q + 3, v2.y, v2.z, v2.w);
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const float c0 = row[3 * k], c1 = row[3 * k + 1], c2 = row[3 * k + 2];
+                row[3 * k] = Y[k] * gr;
+                row[3 * k + 1] = Y[k] * gg;
+                row[3 * k + 2] = Y[k] * gbl;
+                basis(k, c0, c1, c2);
+            }
         }
         float dd = hx * gdx + hy * gdy + hz * gdz;
         dm[0] += (gdx - hx * dd) * ilen;
@@ -660,12 +683,11 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
     const int nrows = (int)min64(32, n - wbase);
     if (nrows <= 0) return;
     if constexpr (kVec) {
-        constexpr int R4 = RW / 4;
         const float4* my4 = reinterpret_cast<const float4*>(my);
         float4* d4 = reinterpret_cast<float4*>(dsh) + wbase * R4;
         for (int f = lane; f < nrows * R4; f += 32) {
-            const int l = f / R4;
-            d4[f] = ((lmask >> l) & 1u) ? my4[f] : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int l = f / R4, col = f - l * R4;
+            d4[f] = ((lmask >> l) & 1u) ? my4[l * (RS / 4) + col] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     } else {
         float* d = dsh + wbase * RW;
