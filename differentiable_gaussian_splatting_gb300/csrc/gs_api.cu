@@ -3,7 +3,7 @@
 // Host side only: argument validation (synchronous, before anything is
 // enqueued), workspace carving and kernel launches on the caller's stream.
 // The library allocates no device memory.  gs_bin_sort keeps one side stream
-// and two events per device, created on its first call there, for work that
+// and three events per device, created on its first call there, for work that
 // overlaps the main sequence and is joined back into the caller's stream.
 #include <cuda_runtime.h>
 

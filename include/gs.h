@@ -34,6 +34,13 @@
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
  *     enqueued on it and the call returns without waiting, except
  *     gs_bin_sort when `n_pairs_host` is non-NULL (one stream sync).
+ *     gs_bin_sort forks part of its work onto a side stream the library
+ *     keeps per device (created with three events on the first call there)
+ *     and joins it back into `stream` before it returns, so its outputs are
+ *     ordered on `stream` like every other call's.  Kernels are launched
+ *     with programmatic stream serialisation: each may start launching
+ *     while the previous kernel on the stream runs, and waits for that
+ *     kernel's completion before touching memory.
  *   - Argument errors are detected synchronously on the host and returned
  *     as GS_ERR_INVALID_ARG before anything is enqueued.  A failed launch
  *     returns GS_ERR_CUDA.
