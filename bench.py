@@ -137,6 +137,23 @@ def measured_peaks() -> dict:
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+def max_over_ranks(ms: float, device) -> float:
+    """The slowest rank's time (every rank gets it); ms itself outside a process group."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, pairs_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job pairs/s: every rank renders its own replica of the view (weak scaling)."""
+    return world * pairs_per_rank / (ms_per_step * 1e-3)
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -227,12 +244,9 @@ def run_gpu(args):
     calls = ["gs_project", "gs_bin_sort", "gs_rasterize_fwd", "gs_rasterize_bwd", "gs_project_bwd"]
     per_call = {c: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
                 for j, c in enumerate(calls)}
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
-    value = world * n_pairs / (ms_per_step * 1e-3)
+    value = job_value(world, n_pairs, ms_per_step)
 
     # roofline of the dominant call (all its work is one kernel launch after small set-up)
     peaks = measured_peaks()
