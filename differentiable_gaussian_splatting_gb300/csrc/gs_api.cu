@@ -2,8 +2,8 @@
 //
 // Host side only: argument validation (synchronous, before anything is
 // enqueued), workspace carving and kernel launches on the caller's stream.
-// The library allocates no device memory.  gs_bin_sort keeps one side stream
-// and three events per device, created on its first call there, for work that
+// The library allocates no device memory.  gs_bin_sort keeps two side streams
+// and four events per device, created on its first call there, for work that
 // overlaps the main sequence and is joined back into the caller's stream.
 #include <cuda_runtime.h>
 
@@ -54,10 +54,12 @@ cudaError_t side_stream(const SideStream** out) {
     if (!g_side_ready[dev]) {
         SideStream s{};
         err = cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking);
+        if (err == cudaSuccess) err = cudaStreamCreateWithFlags(&s.stream2, cudaStreamNonBlocking);
         if (err != cudaSuccess) return err;
         err = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
         if (err == cudaSuccess) err = cudaEventCreateWithFlags(&s.fork2, cudaEventDisableTiming);
         if (err == cudaSuccess) err = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
+        if (err == cudaSuccess) err = cudaEventCreateWithFlags(&s.join2, cudaEventDisableTiming);
         if (err != cudaSuccess) return err;
         g_side[dev] = s;
         g_side_ready[dev] = true;

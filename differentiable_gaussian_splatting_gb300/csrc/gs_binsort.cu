@@ -17,10 +17,12 @@
 //   3. bucket_scatter  stream the raw list into the tiles' slices as 64-bit keys
 //                      (depth bits << 32 | id); depth > 0, so the key order is
 //                      the (depth, id) order
-//   4. bucket_sort_*   sort every slice: up to 512 keys in one warp's registers
-//                      (bitonic network, no barriers); longer slices by one
-//                      block: 512-key chunks sorted by warps, then merge-path
-//                      rounds through global memory
+//   4. slice sorts     up to 512 keys: one warp, in registers and shared memory
+//                      (bucket_sort_small); up to 4096: one block in shared memory
+//                      (bucket_sort_blocks); longer slices: a merge sort over the
+//                      whole grid (long_plan, long_chunks, long_round), 4096-key
+//                      chunks sorted in shared memory, then merge rounds whose
+//                      4096-key output pieces are each merged by one block
 //   5. LPT order of the tiles.
 #include <cuda_runtime.h>
 
@@ -50,6 +52,8 @@ constexpr int kCursorStride = 8;   // uint64
 constexpr int kCountRaw = 3;
 constexpr int kCountMedium = 4;
 constexpr int kCountLarge = 5;
+constexpr int kCountLongChunks = 6;  // chunks of kBlockSortMax keys in the long slices
+constexpr int kCountLongest = 7;     // keys of the longest slice
 
 // ---------------------------------------------------------------------------
 // 0. the call's counters and the tile counters to zero
@@ -571,72 +575,202 @@ __device__ __forceinline__ void sort_medium_slice(int2 r, const uint64_t* __rest
     __syncthreads();
 }
 
-// One block sorts a slice of more than kBlockSortMax keys: chunks of
-// kBlockSortMax in shared memory, then merge-path rounds between buf0 and buf1
-// in global memory; the last round writes the ids.
-__device__ __forceinline__ void sort_large_slice(int2 r, uint64_t* __restrict__ buf0,
-                                                 uint64_t* __restrict__ buf1,
-                                                 int32_t* __restrict__ sorted_ids, uint64_t* A,
-                                                 uint64_t* B) {
-    const int tid = threadIdx.x;
-    const int cnt = r.y - r.x;
-    const int64_t s = r.x;
-    for (int c0 = 0; c0 < cnt; c0 += kBlockSortMax) {
-        const int n = min(kBlockSortMax, cnt - c0);
-        for (int e = tid; e < kBlockSortMax; e += kSortThreads)
-            A[sk_idx(e)] = e < n ? buf0[s + c0 + e] : ~0ull;
-        __syncthreads();
-        const uint64_t* out = block_sort_keys<16>(A, B);
-        for (int e = tid; e < n; e += kSortThreads) buf0[s + c0 + e] = out[sk_idx(e)];
-        __syncthreads();
-    }
-    uint64_t* src = buf0;
-    uint64_t* dst = buf1;
-    for (int width = kBlockSortMax; width < cnt; width <<= 1) {
-        const bool last = 2 * width >= cnt;
-        for (int p0 = 0; p0 < cnt; p0 += 2 * width) {
-            const int na = min(width, cnt - p0);
-            const int nb = min(width, cnt - p0 - na);
-            const uint64_t* Ag = src + s + p0;
-            const uint64_t* Bg = Ag + na;
-            const int tot = na + nb;
-            const int per = (tot + kSortThreads - 1) / kSortThreads;
-            const int k0 = min(tid * per, tot), k1 = min(k0 + per, tot);
-            if (k0 < k1) {
-                int i = merge_split_g(Ag, na, Bg, nb, k0), j = k0 - i;
-                for (int k = k0; k < k1; ++k) {
-                    const bool takeA = j >= nb || (i < na && Ag[i] < Bg[j]);
-                    const uint64_t v = takeA ? Ag[i++] : Bg[j++];
-                    if (last) sorted_ids[s + p0 + k] = (int32_t)(uint32_t)v;
-                    else dst[s + p0 + k] = v;
-                }
-            }
-        }
-        __syncthreads();
-        uint64_t* tmp = src;
-        src = dst;
-        dst = tmp;
-    }
-}
-
-// The slices the warps do not take, one block each: the long ones first (they
-// take longest), then the medium ones.  keys doubles as the long slices' first
-// merge buffer and buf1 (the raw list, free by now) as their second.
+// The medium slices (kWarpSortMax + 1 .. kBlockSortMax keys), one block each.
 __global__ void __launch_bounds__(kSortThreads) bucket_sort_blocks(const int2* __restrict__ ranges,
                                                                    const int32_t* __restrict__ medium,
-                                                                   const int32_t* __restrict__ large,
-                                                                   uint64_t* __restrict__ keys,
-                                                                   uint64_t* __restrict__ buf1,
+                                                                   const uint64_t* __restrict__ keys,
                                                                    int32_t* __restrict__ sorted_ids,
                                                                    const int64_t* __restrict__ counts) {
     grid_dep_sync();
     extern __shared__ uint64_t smem[];
     uint64_t* A = smem;                            // sk_len(kBlockSortMax)
     uint64_t* B = smem + sk_len(kBlockSortMax);    // sk_len(kBlockSortMax)
-    const int64_t nm = counts[kCountMedium], nl = counts[kCountLarge];
-    for (int64_t m = blockIdx.x; m < nl + nm; m += gridDim.x) {
-        if (m < nl) sort_large_slice(ranges[large[m]], keys, buf1, sorted_ids, A, B);
-        else sort_medium_slice(ranges[medium[m - nl]], keys, sorted_ids, A, B);
+    const int64_t nm = counts[kCountMedium];
+    for (int64_t m = blockIdx.x; m < nm; m += gridDim.x)
+        sort_medium_slice(ranges[medium[m]], keys, sorted_ids, A, B);
+}
+
+// ---------------------------------------------------------------------------
+// the long slices (more than kBlockSortMax keys): a merge sort over the whole
+// grid.  Every slice is cut into chunks of kBlockSortMax keys, each chunk is
+// sorted by one block in shared memory, and merge rounds double the sorted
+// runs: in a round every kBlockSortMax-key piece of every slice's output is
+// merged by one block from the two runs it falls between (the run split found
+// by merge path in global memory, the piece merged in shared memory).  The
+// round in which a slice becomes one run writes its ids.
+// ---------------------------------------------------------------------------
+constexpr int kLongChunk = kBlockSortMax;
+
+// One block: chunk offsets of the long slices (exclusive prefix of their chunk
+// counts, chunk_off[nl] = the total), the total and the longest slice.
+__global__ void __launch_bounds__(kScanThreads) long_plan(const int2* __restrict__ ranges,
+                                                          const int32_t* __restrict__ large,
+                                                          int32_t* __restrict__ chunk_off,
+                                                          int64_t* __restrict__ counts) {
+    grid_dep_sync();
+    __shared__ int64_t s_a[kScanThreads / 32], s_b[kScanThreads / 32];
+    const int tid = threadIdx.x;
+    const int64_t nl = counts[kCountLarge];
+    int64_t carry = 0, longest = 0;
+    for (int64_t b = 0; b < nl; b += kScanThreads) {
+        const int64_t m = b + tid;
+        int64_t ch = 0, len = 0;
+        if (m < nl) {
+            const int2 r = ranges[large[m]];
+            len = r.y - r.x;
+            ch = (len + kLongChunk - 1) / kLongChunk;
+        }
+        int64_t ex = ch, mx = len, tot, unused;
+        scan_block2(ex, mx, s_a, s_b, &tot, &unused);
+        if (m < nl) chunk_off[m] = (int32_t)(carry + ex);
+        carry += tot;
+        // the longest: a max over the block (mx was scanned as a sum; redo as a max)
+        int64_t v = len;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+        __syncthreads();
+        if ((tid & 31) == 0) s_a[tid >> 5] = v;
+        __syncthreads();
+        if (tid < 32) {
+            int64_t w = s_a[tid];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) w = max(w, __shfl_xor_sync(0xffffffffu, w, o));
+            if (tid == 0) s_b[0] = w;
+        }
+        __syncthreads();
+        longest = max(longest, s_b[0]);
+        __syncthreads();
+    }
+    if (tid == 0) {
+        chunk_off[nl] = (int32_t)carry;
+        counts[kCountLongChunks] = carry;
+        counts[kCountLongest] = longest;
+    }
+}
+
+// the long slice m holding global chunk c: chunk_off[m] <= c < chunk_off[m + 1]
+__device__ __forceinline__ int64_t long_owner(const int32_t* __restrict__ chunk_off, int64_t nl,
+                                              int64_t c) {
+    int64_t lo = 0, hi = nl;  // chunk_off[lo] <= c < chunk_off[hi]
+    while (hi - lo > 1) {
+        const int64_t mid = (lo + hi) >> 1;
+        if (chunk_off[mid] <= c) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(kSortThreads) long_chunks(const int2* __restrict__ ranges,
+                                                            const int32_t* __restrict__ large,
+                                                            const int32_t* __restrict__ chunk_off,
+                                                            uint64_t* __restrict__ keys,
+                                                            const int64_t* __restrict__ counts) {
+    grid_dep_sync();
+    extern __shared__ uint64_t smem[];
+    uint64_t* A = smem;
+    uint64_t* B = smem + sk_len(kBlockSortMax);
+    const int tid = threadIdx.x;
+    const int64_t nl = counts[kCountLarge], T = counts[kCountLongChunks];
+    for (int64_t c = blockIdx.x; c < T; c += gridDim.x) {
+        const int64_t m = long_owner(chunk_off, nl, c);
+        const int2 r = ranges[large[m]];
+        const int64_t s = (int64_t)r.x + (c - chunk_off[m]) * kLongChunk;
+        const int n = (int)min64(kLongChunk, (int64_t)r.y - s);
+        for (int e = tid; e < kLongChunk; e += kSortThreads) A[sk_idx(e)] = e < n ? keys[s + e] : ~0ull;
+        __syncthreads();
+        const uint64_t* out = block_sort_keys<16>(A, B);
+        for (int e = tid; e < n; e += kSortThreads) keys[s + e] = out[sk_idx(e)];
+        __syncthreads();
+    }
+}
+
+// Merge path in global memory by one warp: the number of elements of a[0, na)
+// among the first k of merge(a, b) (keys are unique).  Each step tests 32
+// evenly spaced candidates, so a search over 2^17 takes four steps.
+__device__ __forceinline__ int64_t merge_split_warp(const uint64_t* __restrict__ a, int64_t na,
+                                                    const uint64_t* __restrict__ b, int64_t nb,
+                                                    int64_t k, int lane) {
+    int64_t lo = max64(0, k - nb), hi = min64(k, na);  // the answer lies in [lo, hi]
+    while (lo < hi) {
+        const int64_t span = hi - lo;
+        const int64_t step = (span + 31) / 32;
+        const int64_t i = lo + (int64_t)lane * step;
+        // true for i below the answer (a[i] precedes the (k - i)-th element of b)
+        const bool p = i < hi && a[i] < b[k - 1 - i];
+        const int t = __popc(__ballot_sync(0xffffffffu, p));
+        if (step == 1) return lo + t;
+        // samples 0 .. t-1 are below the answer, sample t (if any) is not
+        const int64_t nlo = t > 0 ? lo + (int64_t)(t - 1) * step + 1 : lo;
+        const int64_t nhi = min64(hi, lo + (int64_t)t * step);
+        lo = nlo;
+        hi = nhi;
+    }
+    return lo;
+}
+
+// One merge round of width w: the runs [p0, p0 + w) and [p0 + w, p0 + 2w) of
+// every long slice still longer than w are merged from src into dst, or into
+// the ids when the merged run is the whole slice.
+__global__ void __launch_bounds__(kSortThreads) long_round(const int2* __restrict__ ranges,
+                                                           const int32_t* __restrict__ large,
+                                                           const int32_t* __restrict__ chunk_off,
+                                                           const uint64_t* __restrict__ src,
+                                                           uint64_t* __restrict__ dst,
+                                                           int32_t* __restrict__ sorted_ids,
+                                                           int64_t w,
+                                                           const int64_t* __restrict__ counts) {
+    grid_dep_sync();
+    extern __shared__ uint64_t smem[];      // kLongChunk keys: the piece's inputs
+    __shared__ int64_t s_split[2];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t nl = counts[kCountLarge], T = counts[kCountLongChunks];
+    if (counts[kCountLongest] <= w) return;  // every slice is one run already
+    constexpr int kPer = kLongChunk / kSortThreads;  // outputs per thread
+    for (int64_t c = blockIdx.x; c < T; c += gridDim.x) {
+        const int64_t m = long_owner(chunk_off, nl, c);
+        const int2 r = ranges[large[m]];
+        const int64_t n = (int64_t)r.y - r.x;
+        if (n <= w) continue;  // this slice finished in an earlier round
+        const int64_t o0 = (c - chunk_off[m]) * kLongChunk, o1 = min64(o0 + kLongChunk, n);
+        const int64_t p0 = (o0 / (2 * w)) * (2 * w);
+        const int64_t na = min64(w, n - p0), nb = min64(w, n - p0 - na);
+        const bool last = 2 * w >= n;
+        const uint64_t* a = src + r.x + p0;
+        const uint64_t* b = a + na;
+        if (warp < 2) {
+            const int64_t k = (warp == 0 ? o0 : o1) - p0;
+            const int64_t i = merge_split_warp(a, na, b, nb, k, lane);
+            if (lane == 0) s_split[warp] = i;
+        }
+        __syncthreads();
+        const int64_t i0 = s_split[0], i1 = s_split[1];
+        const int64_t j0 = (o0 - p0) - i0, j1 = (o1 - p0) - i1;
+        const int la = (int)(i1 - i0), lb = (int)(j1 - j0);
+        for (int e = tid; e < la; e += kSortThreads) smem[e] = a[i0 + e];
+        for (int e = tid; e < lb; e += kSortThreads) smem[la + e] = b[j0 + e];
+        __syncthreads();
+        // this thread's outputs [kPer tid, kPer tid + kPer) of the piece
+        const int q0 = tid * kPer, q1 = min(q0 + kPer, la + lb);
+        if (q0 < q1) {
+            int lo = max(0, q0 - lb), hi = min(q0, la);
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (smem[mid] < smem[la + q0 - 1 - mid]) lo = mid + 1;
+                else hi = mid;
+            }
+            int x = lo, y = q0 - lo;
+            const int64_t out = r.x + o0;
+            for (int q = q0; q < q1; ++q) {
+                const uint64_t va = x < la ? smem[x] : ~0ull;
+                const uint64_t vb = y < lb ? smem[la + y] : ~0ull;
+                const bool ta = va < vb;
+                const uint64_t v = ta ? va : vb;
+                x += ta;
+                y += !ta;
+                if (last) sorted_ids[out + q] = (int32_t)(uint32_t)v;
+                else dst[out + q] = v;
+            }
+        }
+        __syncthreads();  // smem and s_split are reused by the next piece
     }
 }
 
@@ -740,6 +874,7 @@ BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles) {
     L.off_tcount = take((size_t)nt * kCountStride * sizeof(int));
     L.off_cursor = take((size_t)nt * kCursorStride * sizeof(unsigned long long));
     L.off_lists = take((size_t)nt * 2 * sizeof(int32_t));
+    L.off_lchunk = take((size_t)(nt + 1) * sizeof(int32_t));
     L.off_lruns = take((size_t)((nt + kLptRun - 1) / kLptRun) * kLptRun * sizeof(uint64_t));
     L.total = off;
     return L;
@@ -825,12 +960,47 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
         err = cudaFuncSetAttribute(bucket_sort_blocks, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)sbytes);
         if (err != cudaSuccess) return err;
-        // the raw list is free again: it is the long slices' second merge buffer
         const unsigned mg = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nt, 3 * (int64_t)sms));
         err = launch(bucket_sort_blocks, mg, kSortThreads, sbytes, ms, (const int2*)ranges,
-                     (const int32_t*)medium, (const int32_t*)large, keys,
-                     reinterpret_cast<uint64_t*>(raw), sorted_ids, (const int64_t*)counts);
+                     (const int32_t*)medium, (const uint64_t*)keys, sorted_ids,
+                     (const int64_t*)counts);
         if (err != cudaSuccess) return err;
+        // the long slices: chunk sorts, then merge rounds between the key list and
+        // the raw list (free again) -- on a second side stream when given.  A tile
+        // holds at most one pair per Gaussian, so min(n, capacity) bounds a slice
+        // and fixes the number of rounds; rounds past the longest slice return at once.
+        cudaStream_t gs = side ? side->stream2 : st;
+        if (side) {
+            err = cudaStreamWaitEvent(gs, side->fork2, 0);
+            if (err != cudaSuccess) return err;
+        }
+        auto* chunk_off = reinterpret_cast<int32_t*>(ws + L.off_lchunk);
+        err = launch(long_plan, 1, kScanThreads, 0, gs, (const int2*)ranges, (const int32_t*)large,
+                     chunk_off, counts);
+        if (err != cudaSuccess) return err;
+        err = cudaFuncSetAttribute(long_chunks, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)sbytes);
+        if (err != cudaSuccess) return err;
+        err = launch(long_chunks, (unsigned)(3 * sms), kSortThreads, sbytes, gs, (const int2*)ranges,
+                     (const int32_t*)large, (const int32_t*)chunk_off, keys, (const int64_t*)counts);
+        if (err != cudaSuccess) return err;
+        const int64_t bound = std::min<int64_t>(n, capacity);
+        const size_t rbytes = (size_t)kLongChunk * sizeof(uint64_t);
+        uint64_t* bufs[2] = {keys, reinterpret_cast<uint64_t*>(raw)};
+        int r = 0;
+        for (int64_t w = kLongChunk; w < bound; w *= 2, ++r) {
+            err = launch(long_round, (unsigned)(6 * sms), kSortThreads, rbytes, gs,
+                         (const int2*)ranges, (const int32_t*)large, (const int32_t*)chunk_off,
+                         (const uint64_t*)bufs[r & 1], bufs[(r & 1) ^ 1], sorted_ids, w,
+                         (const int64_t*)counts);
+            if (err != cudaSuccess) return err;
+        }
+        if (side) {
+            err = cudaEventRecord(side->join2, gs);
+            if (err != cudaSuccess) return err;
+            err = cudaStreamWaitEvent(st, side->join2, 0);
+            if (err != cudaSuccess) return err;
+        }
     }
     if (side) {
         // the LPT order and the medium and long slices are done

@@ -41,7 +41,8 @@ struct BinSortLayout {
     size_t off_keys;     // uint64[capacity]: the tiles' slices of (depth bits << 32 | id)
     size_t off_tcount;   // int32[n_tiles]: pairs per tile
     size_t off_cursor;   // uint64[n_tiles]: bucket cursors
-    size_t off_lists;    // int32[2 n_tiles]: tiles sorted by a block, then by merge rounds
+    size_t off_lists;    // int32[2 n_tiles]: tiles sorted by a block, tiles sorted by merge rounds
+    size_t off_lchunk;   // int32[n_tiles + 1]: chunk offsets of the long slices
     size_t off_lruns;    // uint64[n_tiles rounded up to 1024]: sorted runs of LPT keys
 };
 BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles);
@@ -79,8 +80,8 @@ inline cudaError_t launch(void (*kernel)(P...), dim3 grid, dim3 block, size_t sm
 // A second stream with fork / join events: work that depends only on an
 // earlier step runs on it beside the main sequence and is joined back.
 struct SideStream {
-    cudaStream_t stream;
-    cudaEvent_t fork, fork2, join;
+    cudaStream_t stream, stream2;
+    cudaEvent_t fork, fork2, join, join2;
 };
 
 // gs_bin_sort with its argument checks; overlap = false keeps every launch in

@@ -34,9 +34,9 @@
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
  *     enqueued on it and the call returns without waiting, except
  *     gs_bin_sort when `n_pairs_host` is non-NULL (one stream sync).
- *     gs_bin_sort forks part of its work onto a side stream the library
- *     keeps per device (created with three events on the first call there)
- *     and joins it back into `stream` before it returns, so its outputs are
+ *     gs_bin_sort forks part of its work onto two side streams the library
+ *     keeps per device (created with four events on the first call there)
+ *     and joins them back into `stream` before it returns, so its outputs are
  *     ordered on `stream` like every other call's.  Kernels are launched
  *     with programmatic stream serialisation: each may start launching
  *     while the previous kernel on the stream runs, and waits for that
