@@ -139,11 +139,33 @@ gs_status bin_sort_entry(const gs_camera* cam, int64_t n, const float* splats,
         if (!p || !aligned16(p)) return GS_ERR_INVALID_ARG;
     if (counts_device && (reinterpret_cast<uintptr_t>(counts_device) & 7u)) return GS_ERR_INVALID_ARG;
     const int64_t nt = gs_num_tiles(cam->width, cam->height);
-    const BinSortLayout L = binsort_layout(n, capacity, nt);
-    if (workspace_bytes < L.total) return GS_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
     char* ws = static_cast<char*>(workspace);
     cudaError_t err;
+    // long pair lists: the two-stage radix sort (no per-tile atomics); the choice
+    // depends on the capacity alone, so the workspace query agrees with it
+    const bool radix = capacity >= kRadixMinPairs;
+    if (radix) {
+        const RadixBinLayout R = radix_bin_layout(n, capacity, nt);
+        if (workspace_bytes < R.total) return GS_ERR_WORKSPACE;
+        err = run_bin_sort_radix(cam_params(cam), n, splats, depths, tiles_touched, ws, R,
+                                 sorted_ids, capacity, tile_ranges, lpt_order, counts_device, st);
+        if (err != cudaSuccess) return GS_ERR_CUDA;
+        if (n_pairs_host) {
+            const int64_t* counts = reinterpret_cast<const int64_t*>(ws + R.off_counts);
+            int64_t host_counts[8] = {0};
+            err = cudaMemcpyAsync(host_counts, counts, sizeof(host_counts), cudaMemcpyDeviceToHost, st);
+            if (err != cudaSuccess) return GS_ERR_CUDA;
+            err = cudaStreamSynchronize(st);
+            if (err != cudaSuccess) return GS_ERR_CUDA;
+            *n_pairs_host = host_counts[1];
+            if (host_counts[kRadixErrWord] != 0) return GS_ERR_TIMEOUT;
+            if (host_counts[1] > capacity) return GS_ERR_CAPACITY;
+        }
+        return GS_OK;
+    }
+    const BinSortLayout L = binsort_layout(n, capacity, nt);
+    if (workspace_bytes < L.total) return GS_ERR_WORKSPACE;
     {
         // the whole sequence is enqueued under the lock, so that the join event
         // still marks this call's side work when the caller's stream waits on it
@@ -223,7 +245,9 @@ size_t gs_bin_sort_workspace_bytes(int64_t n, int64_t capacity, int32_t width, i
     if (n < 0 || n > kMaxIds || capacity < 1 || capacity > kMaxIds || width < 1 || height < 1 ||
         width > kMaxImageSide || height > kMaxImageSide)
         return 0;
-    return binsort_layout(n, capacity, gs_num_tiles(width, height)).total;
+    const int64_t nt = gs_num_tiles(width, height);
+    return capacity >= kRadixMinPairs ? radix_bin_layout(n, capacity, nt).total
+                                      : binsort_layout(n, capacity, nt).total;
 }
 
 gs_status gs_bin_sort(const gs_camera* cam, int64_t n, const float* splats, const float* depths,

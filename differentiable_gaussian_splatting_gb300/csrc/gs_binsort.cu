@@ -857,6 +857,20 @@ size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
 
+size_t lpt_runs_bytes(int64_t nt) {
+    nt = std::max<int64_t>(nt, 1);
+    return (size_t)((nt + kLptRun - 1) / kLptRun) * kLptRun * sizeof(uint64_t);
+}
+
+cudaError_t launch_lpt(const int2* ranges, int64_t nt, uint64_t* runs, int32_t* lpt_order,
+                       cudaStream_t st) {
+    const unsigned nruns = (unsigned)((nt + kLptRun - 1) / kLptRun);
+    cudaError_t err = launch(lpt_sort_runs, nruns, kLptRun / 2, 0, st, ranges, nt, runs);
+    if (err != cudaSuccess) return err;
+    return launch(lpt_merge, (unsigned)((nruns * (int64_t)kLptRun + 255) / 256), 256, 0, st,
+                  (const uint64_t*)runs, nt, lpt_order);
+}
+
 BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles) {
     BinSortLayout L{};
     size_t off = 0;
@@ -875,7 +889,7 @@ BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles) {
     L.off_cursor = take((size_t)nt * kCursorStride * sizeof(unsigned long long));
     L.off_lists = take((size_t)nt * 2 * sizeof(int32_t));
     L.off_lchunk = take((size_t)(nt + 1) * sizeof(int32_t));
-    L.off_lruns = take((size_t)((nt + kLptRun - 1) / kLptRun) * kLptRun * sizeof(uint64_t));
+    L.off_lruns = take(lpt_runs_bytes(nt));
     L.total = off;
     return L;
 }
@@ -926,14 +940,8 @@ cudaError_t run_bin_sort(const CamParams& cam, int64_t n, const float* splats, c
         if (err != cudaSuccess) return err;
         ls = side->stream;
     }
-    {
-        const unsigned nruns = (unsigned)((nt + kLptRun - 1) / kLptRun);
-        err = launch(lpt_sort_runs, nruns, kLptRun / 2, 0, ls, (const int2*)ranges, nt, lruns);
-        if (err != cudaSuccess) return err;
-        err = launch(lpt_merge, (unsigned)((nruns * (int64_t)kLptRun + 255) / 256), 256, 0, ls,
-                     (const uint64_t*)lruns, nt, lpt_order);
-        if (err != cudaSuccess) return err;
-    }
+    err = launch_lpt(ranges, nt, lruns, lpt_order, ls);
+    if (err != cudaSuccess) return err;
     if (n > 0) {
         // 3. the pairs into their tiles' slices
         const unsigned grid = (unsigned)std::max<int64_t>(

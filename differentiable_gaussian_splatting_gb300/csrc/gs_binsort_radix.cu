@@ -1,0 +1,800 @@
+// gs_binsort_radix.cu -- tile binning for long pair lists: the two-stage
+// radix sort.
+//
+// "What the 3DGS Literature Left on the Table" (Kopanas), Step 1 (b), (d): the
+// visible Gaussians are sorted once by a 32-bit depth key, their (tile,
+// Gaussian) pairs are emitted in that depth order from the exact row spans, and
+// the pairs are then sorted by the tile key with a stable LSD radix sort, so the
+// list is ordered by (tile, depth, id).  "Mitigating SM-Level Load Imbalance in
+// 3D Gaussian Splatting on GPUs" (Ryu & Yoo), Sec. 4.1: LPT order of the tiles.
+//
+// gs_bin_sort takes this path when the pair capacity is large (millions of
+// pairs): every pass is then a stream over the keys at memory speed, where the
+// per-tile buckets of gs_binsort.cu contend on the counters of dense tiles.
+// Same outputs, bit for bit.
+//
+// Radix sort: LSD, 8-bit digits, one kernel per pass; the digit counts of every
+// pass are taken by the kernel that writes the keys (the visible-Gaussian
+// compaction, the pair emission).  Blocks take 4096-key tiles in ticket order,
+// rank keys within warps with __match_any_sync, publish their digit counts and
+// add those of earlier tiles by decoupled look-back (every wait is bounded and
+// sets a give-up flag).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "gs_device.cuh"
+#include "gs_internal.h"
+
+namespace gs {
+
+namespace {
+
+constexpr int kRsBlock = 256;
+constexpr int kRsIpt = 16;
+constexpr int kRsTile = kRsBlock * kRsIpt;  // 4096 keys per block
+constexpr int kRsWarps = kRsBlock / 32;
+constexpr int kScanThreads = 1024;
+
+__host__ __device__ inline int64_t nblk_of(int64_t n) { return (n + kRsTile - 1) / kRsTile; }
+
+__device__ __forceinline__ int64_t count_of(const int64_t* n_dev, int64_t n_static) {
+    return n_dev ? *n_dev : n_static;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// exclusive scan of one value per thread over a block of kRsBlock threads
+template <typename T>
+__device__ __forceinline__ T block_exclusive_scan_256(T v, T* s_warp, T* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    T x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        T y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        T w = lane < kRsWarps ? s_warp[lane] : T(0);
+#pragma unroll
+        for (int o = 1; o < kRsWarps; o <<= 1) {
+            T y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < kRsWarps) s_warp[lane] = w;  // inclusive warp prefix
+    }
+    __syncthreads();
+    T warp_excl = warp > 0 ? s_warp[warp - 1] : T(0);
+    *total = s_warp[kRsWarps - 1];
+    __syncthreads();
+    return warp_excl + x - v;
+}
+
+// ---------------------------------------------------------------------------
+// radix sort kernels
+// ---------------------------------------------------------------------------
+// Look-back words: one per (block, digit), written once per pass.  Bits 63-62
+// hold the state (0 not ready, 1 the block's own digit count, 2 the inclusive
+// prefix over blocks 0..b), bits 61-56 the pass (1-based, so words left by an
+// earlier pass of the same sort read as not ready) and bits 55-0 the count.
+constexpr uint64_t kLbAgg = 1ull << 62;
+constexpr uint64_t kLbPrefix = 2ull << 62;
+constexpr uint64_t kLbCount = (1ull << 56) - 1;
+constexpr int kMaxPasses = 4;
+// polls of one look-back word before the block gives up and flags an error
+constexpr int kSpinLimit = 1 << 22;
+constexpr int kLbWindow = 8;
+
+__device__ __forceinline__ bool lb_ready(uint64_t w, uint64_t epoch) {
+    return (w >> 62) != 0 && (w & ~(kLbPrefix | kLbAgg | kLbCount)) == epoch;
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// One pass of the stable LSD sort: blocks take consecutive 4096-key tiles in
+// ticket order, rank their keys by digit (warps with __match_any_sync, then
+// across warps), publish their digit counts, and add the counts of the tiles
+// before them by looking back through the published words (decoupled
+// look-back: a block only waits on tiles that started before it, so waits
+// end).  Keys are staged in shared memory in block-sorted order so that each
+// digit's run is written to global memory contiguously.
+struct OnesweepSmem {
+    uint32_t keys[kRsTile];
+    int32_t vals[kRsTile];
+    uint32_t wcnt[kRsWarps][256];
+    uint32_t dstart[256];
+    int64_t gbase[256];
+    uint32_t warp_sums[kRsWarps];
+    int ticket;
+};
+
+__global__ void __launch_bounds__(kRsBlock, 2) rs_onesweep(
+    const uint32_t* __restrict__ keys_in, const int32_t* __restrict__ vals_in,
+    uint32_t* __restrict__ keys_out, int32_t* __restrict__ vals_out, const int64_t* n_dev,
+    int64_t n_static, int pass, const uint32_t* __restrict__ ghist, int* __restrict__ tickets,
+    uint64_t* __restrict__ lookback, unsigned long long* __restrict__ err) {
+    grid_dep_sync();
+    __shared__ OnesweepSmem S;
+    const int64_t n = count_of(n_dev, n_static);
+    const int64_t nblk = nblk_of(n);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int shift = 8 * pass;
+    const uint64_t epoch = (uint64_t)(pass + 1) << 56;
+    if (tid == 0) S.ticket = atomicAdd(tickets + pass, 1);
+#pragma unroll
+    for (int w = 0; w < kRsWarps; ++w) S.wcnt[w][tid] = 0;
+    __syncthreads();
+    const int64_t b = S.ticket;
+    if (b >= nblk) return;
+
+    // ---- load (each warp owns 512 consecutive keys) and rank within the warp
+    const int64_t wbase = b * kRsTile + (int64_t)warp * (32 * kRsIpt);
+    uint32_t k[kRsIpt];
+    int32_t v[kRsIpt];
+    uint32_t loc[kRsIpt];
+#pragma unroll
+    for (int r = 0; r < kRsIpt; ++r) {
+        const int64_t idx = wbase + r * 32 + lane;
+        const bool valid = idx < n;
+        k[r] = valid ? __ldg(keys_in + idx) : 0xffffffffu;
+        v[r] = valid ? __ldg(vals_in + idx) : 0;
+    }
+#pragma unroll
+    for (int r = 0; r < kRsIpt; ++r) {
+        const int64_t idx = wbase + r * 32 + lane;
+        const bool valid = idx < n;
+        const uint32_t d = (k[r] >> shift) & 255u;
+        const uint32_t peers = __match_any_sync(0xffffffffu, valid ? d : 256u + lane);
+        const uint32_t rank = __popc(peers & lanemask_lt());
+        const uint32_t prev = S.wcnt[warp][d];
+        loc[r] = prev + rank;
+        __syncwarp();
+        if (valid && rank == 0) S.wcnt[warp][d] = prev + __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // ---- per digit (thread = digit): warp prefixes, block count, publish
+    const int d = tid;
+    uint32_t cd = 0;
+#pragma unroll
+    for (int w = 0; w < kRsWarps; ++w) {
+        const uint32_t c = S.wcnt[w][d];
+        S.wcnt[w][d] = cd;
+        cd += c;
+    }
+    uint64_t* my = lookback + b * 256 + d;
+    st_relaxed(my, (b == 0 ? kLbPrefix : kLbAgg) | epoch | (uint64_t)cd);
+    // block-local start of each digit's run
+    uint32_t x = cd;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) S.warp_sums[warp] = x;
+    // global start of each digit: exclusive scan of the pass's digit counts
+    uint32_t gd = ghist[pass * 256 + d];
+    uint32_t gx = gd;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, gx, o);
+        if (lane >= o) gx += y;
+    }
+    __syncthreads();
+    uint32_t wpre = 0;
+#pragma unroll
+    for (int w = 0; w < kRsWarps; ++w) wpre += w < warp ? S.warp_sums[w] : 0u;
+    const uint32_t dstart = wpre + x - cd;
+    S.dstart[d] = dstart;
+    __syncthreads();
+    if (lane == 31) S.warp_sums[warp] = gx;
+    __syncthreads();
+    uint64_t gpre = 0;
+#pragma unroll
+    for (int w = 0; w < kRsWarps; ++w) gpre += w < warp ? S.warp_sums[w] : 0u;
+    const uint64_t gstart = gpre + gx - gd;
+
+    // ---- look back over the earlier tiles for this digit, kLbWindow words in
+    // flight at a time (nearest first), up to the first inclusive prefix
+    uint64_t excl = 0;
+    if (b > 0) {
+        bool found = false;
+        for (int64_t jb = b - 1; jb >= 0 && !found; jb -= kLbWindow) {
+            uint64_t wv[kLbWindow];
+#pragma unroll
+            for (int i = 0; i < kLbWindow; ++i)
+                wv[i] = jb - i >= 0 ? ld_relaxed(lookback + (jb - i) * 256 + d) : 0ull;
+#pragma unroll
+            for (int i = 0; i < kLbWindow; ++i) {
+                if (found || jb - i < 0) break;
+                const uint64_t* wp = lookback + (jb - i) * 256 + d;
+                int spins = 0;
+                while (!lb_ready(wv[i], epoch) && ++spins < kSpinLimit) wv[i] = ld_relaxed(wp);
+                if (spins >= kSpinLimit) {
+                    atomicOr(err, 1ull);  // the tile before never published: give up
+                    found = true;
+                    break;
+                }
+                excl += wv[i] & kLbCount;
+                found = (wv[i] >> 62) == 2;
+            }
+        }
+        st_relaxed(my, kLbPrefix | epoch | (excl + cd));
+    }
+    S.gbase[d] = (int64_t)(gstart + excl) - (int64_t)dstart;
+
+    // ---- stage in block-sorted order, then write each digit run contiguously
+#pragma unroll
+    for (int r = 0; r < kRsIpt; ++r) {
+        const int64_t idx = wbase + r * 32 + lane;
+        if (idx < n) {
+            const uint32_t dd = (k[r] >> shift) & 255u;
+            const uint32_t li = S.dstart[dd] + S.wcnt[warp][dd] + loc[r];
+            S.keys[li] = k[r];
+            S.vals[li] = v[r];
+        }
+    }
+    __syncthreads();
+    const int cnt = (int)min64(kRsTile, n - b * kRsTile);
+    for (int i = tid; i < cnt; i += kRsBlock) {
+        const uint32_t key = S.keys[i];
+        const int64_t pos = S.gbase[(key >> shift) & 255u] + i;
+        keys_out[pos] = key;
+        vals_out[pos] = S.vals[i];
+    }
+}
+
+// Stable LSD radix sort of (keys, vals) on bits [0, bits), bits <= 32.  The
+// count is read from n_dev (device) when given, else n_static; n_max bounds
+// it.  Passes ping-pong between (k0, v0) and (k1, v1), starting from (k0, v0).
+// The last pass writes its values to vf when given (a buffer distinct from v0,
+// v1) and its keys to the scratch buffer the pass did not read; *kres / *vres
+// return where the sorted keys and values are.  ghist holds the digit counts of
+// every pass ([pass][digit], taken when the keys were written).  ctl is the
+// sort's control region (rs_ctl_bytes(n_max)), cleared here; err collects
+// give-up flags.
+size_t rs_ctl_bytes(int64_t n_max) {
+    return 16 + kMaxPasses * 256 * 4 + (size_t)std::max<int64_t>(1, nblk_of(n_max)) * 256 * 8;
+}
+
+cudaError_t radix_sort(uint32_t* k0, int32_t* v0, uint32_t* k1, int32_t* v1, int32_t* vf,
+                       const int64_t* n_dev, int64_t n_static, int64_t n_max, int bits, char* ctl,
+                       const uint32_t* ghist_given, unsigned long long* err, cudaStream_t st,
+                       uint32_t** kres, int32_t** vres) {
+    const int passes = std::max(1, (bits + 7) / 8);
+    const unsigned grid = (unsigned)std::max<int64_t>(1, nblk_of(n_max));
+    int* tickets = reinterpret_cast<int*>(ctl);
+    const uint32_t* ghist = ghist_given;  // taken by the kernel that wrote the keys
+    uint64_t* lookback = reinterpret_cast<uint64_t*>(ctl + 16 + kMaxPasses * 256 * 4);
+    cudaError_t e = cudaMemsetAsync(ctl, 0, rs_ctl_bytes(n_max), st);
+    if (e != cudaSuccess) return e;
+    uint32_t* kin = k0;
+    int32_t* vin = v0;
+    for (int p = 0; p < passes; ++p) {
+        const bool last = p == passes - 1;
+        uint32_t* kout = kin == k0 ? k1 : k0;
+        int32_t* vout = (last && vf) ? vf : (vin == v0 ? v1 : v0);
+        e = launch(rs_onesweep, grid, kRsBlock, 0, st, (const uint32_t*)kin, (const int32_t*)vin, kout,
+                   vout, n_dev, n_static, p, ghist, tickets, lookback, err);
+        if (e != cudaSuccess) return e;
+        kin = kout;
+        vin = vout;
+    }
+    if (kres) *kres = kin;
+    if (vres) *vres = vin;
+    return cudaSuccess;
+}
+
+// ---------------------------------------------------------------------------
+// scans: per-block sums, a single-block scan of the sums, per-block writes
+// ---------------------------------------------------------------------------
+// exclusive scan in place of bsum[0 .. nb), nb = ceil(count / kRsTile);
+// count = *count_dev (or count_static).  Writes the grand total to *total_out
+// and min(total, cap) to *capped_out (if given).
+__global__ void __launch_bounds__(kScanThreads) scan_block_sums(int64_t* __restrict__ bsum,
+                                                                const int64_t* count_dev,
+                                                                int64_t count_static,
+                                                                int64_t* total_out,
+                                                                int64_t cap, int64_t* capped_out) {
+    grid_dep_sync();
+    const int64_t nb = nblk_of(count_of(count_dev, count_static));
+    __shared__ int64_t s_part[kScanThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t per = (nb + kScanThreads - 1) / kScanThreads;
+    const int64_t lo = min64(nb, per * tid), hi = min64(nb, lo + per);
+    int64_t sum = 0;
+    for (int64_t j = lo; j < hi; ++j) sum += bsum[j];
+    int64_t x = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_part[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t w = s_part[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        s_part[lane] = w;
+    }
+    __syncthreads();
+    int64_t run = (warp > 0 ? s_part[warp - 1] : 0) + x - sum;
+    for (int64_t j = lo; j < hi; ++j) {
+        int64_t c = bsum[j];
+        bsum[j] = run;
+        run += c;
+    }
+    if (tid == kScanThreads - 1) {
+        int64_t total = s_part[31];
+        *total_out = total;
+        if (capped_out) *capped_out = total < cap ? total : cap;
+    }
+}
+
+// visible Gaussians: per-block counts
+__global__ void __launch_bounds__(kRsBlock) vis_count(const int32_t* __restrict__ tiles_touched,
+                                                      int64_t n, int64_t* __restrict__ bsum) {
+    grid_dep_sync();
+    __shared__ int64_t s_warp[kRsWarps];
+    const int64_t base = (int64_t)blockIdx.x * kRsTile;
+    int64_t c = 0;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < kRsTile; i += kRsBlock) {
+        int64_t idx = base + i;
+        if (idx < n && tiles_touched[idx] > 0) ++c;
+    }
+    int64_t total;
+    block_exclusive_scan_256<int64_t>(c, s_warp, &total);
+    if (threadIdx.x == 0) bsum[blockIdx.x] = total;
+}
+
+// visible Gaussians, in id order: (depth key, id).  Blocked: each thread owns 16
+// consecutive items, so one block-wide scan of per-thread counts suffices.
+__global__ void __launch_bounds__(kRsBlock) vis_write(const int32_t* __restrict__ tiles_touched,
+                                                      const float* __restrict__ depths, int64_t n,
+                                                      const int64_t* __restrict__ bsum,
+                                                      uint32_t* __restrict__ keys,
+                                                      int32_t* __restrict__ vals,
+                                                      uint32_t* __restrict__ dhist) {
+    grid_dep_sync();
+    __shared__ int64_t s_warp[kRsWarps];
+    __shared__ uint32_t hist[kMaxPasses][256];
+#pragma unroll
+    for (int p = 0; p < kMaxPasses; ++p) hist[p][threadIdx.x] = 0;
+    const int64_t base = (int64_t)blockIdx.x * kRsTile + (int64_t)threadIdx.x * kRsIpt;
+    bool vis[kRsIpt];
+    int64_t c = 0;
+#pragma unroll
+    for (int r = 0; r < kRsIpt; ++r) {
+        const int64_t idx = base + r;
+        vis[r] = idx < n && tiles_touched[idx] > 0;
+        c += vis[r];
+    }
+    int64_t total;
+    int64_t pos = bsum[blockIdx.x] + block_exclusive_scan_256<int64_t>(c, s_warp, &total);
+#pragma unroll
+    for (int r = 0; r < kRsIpt; ++r) {
+        if (vis[r]) {
+            const int64_t idx = base + r;
+            const uint32_t k = __float_as_uint(depths[idx]);  // depth > znear > 0: bits are ordered
+            keys[pos] = k;
+            vals[pos] = (int32_t)idx;
+            ++pos;
+#pragma unroll
+            for (int p = 0; p < kMaxPasses; ++p) atomicAdd(&hist[p][(k >> (8 * p)) & 255u], 1u);
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int p = 0; p < kMaxPasses; ++p)
+        if (hist[p][threadIdx.x]) atomicAdd(dhist + p * 256 + threadIdx.x, hist[p][threadIdx.x]);
+}
+
+// pairs per visible Gaussian in depth order: per-block sums
+__global__ void __launch_bounds__(kRsBlock) pairs_count(const int32_t* __restrict__ order,
+                                                        const int32_t* __restrict__ tiles_touched,
+                                                        const int64_t* __restrict__ m_dev,
+                                                        int64_t* __restrict__ bsum) {
+    grid_dep_sync();
+    const int64_t m = *m_dev;
+    if ((int64_t)blockIdx.x >= nblk_of(m)) return;
+    __shared__ int64_t s_warp[kRsWarps];
+    const int64_t base = (int64_t)blockIdx.x * kRsTile;
+    int64_t c = 0;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < kRsTile; i += kRsBlock) {
+        int64_t j = base + i;
+        if (j < m) c += tiles_touched[order[j]];
+    }
+    int64_t total;
+    block_exclusive_scan_256<int64_t>(c, s_warp, &total);
+    if (threadIdx.x == 0) bsum[blockIdx.x] = total;
+}
+
+__global__ void __launch_bounds__(kRsBlock) pairs_offsets(const int32_t* __restrict__ order,
+                                                          const int32_t* __restrict__ tiles_touched,
+                                                          const int64_t* __restrict__ m_dev,
+                                                          const int64_t* __restrict__ bsum,
+                                                          int64_t* __restrict__ poff) {
+    grid_dep_sync();
+    const int64_t m = *m_dev;
+    if ((int64_t)blockIdx.x >= nblk_of(m)) return;
+    __shared__ int64_t s_warp[kRsWarps];
+    const int64_t base = (int64_t)blockIdx.x * kRsTile + (int64_t)threadIdx.x * kRsIpt;
+    int32_t c[kRsIpt];
+    int64_t sum = 0;
+    int32_t g[kRsIpt];
+#pragma unroll
+    for (int r = 0; r < kRsIpt; ++r) {
+        const int64_t j = base + r;
+        g[r] = j < m ? order[j] : 0;
+        c[r] = j < m ? tiles_touched[g[r]] : 0;
+        sum += c[r];
+    }
+    int64_t total;
+    int64_t pos = bsum[blockIdx.x] + block_exclusive_scan_256<int64_t>(sum, s_warp, &total);
+    // indexed by Gaussian id: the emission walks the Gaussians in id order
+#pragma unroll
+    for (int r = 0; r < kRsIpt; ++r) {
+        const int64_t j = base + r;
+        if (j < m) poff[g[r]] = pos;
+        pos += c[r];
+    }
+}
+
+// emit (tile, Gaussian) pairs into their depth-order places from the exact row
+// spans.  A block takes 256 consecutive Gaussian ids (in id order the large,
+// near splats are spread over the blocks; in depth order they would crowd the
+// first ones); the (splat, tile row) entries of its visible splats are spread
+// evenly over the block's threads (a scan of the row counts and a search for
+// each entry's owner).  A splat's pairs go to its own offset range poff[id], in
+// any order within it (they lie in distinct tiles, and the tile sort is stable
+// across splats).  The digit counts of the tile sort's passes are counted here.
+constexpr int kEmitThreads = 256;
+struct EmitRows {
+    float e[8][kEmitThreads];    // Ellipse fields, structure of arrays
+    float dyv[kEmitThreads];
+    int ty0[kEmitThreads];
+    int off[kEmitThreads + 1];   // exclusive prefix of row counts
+    int pcur[kEmitThreads];      // pairs placed so far per splat
+    int64_t pb[kEmitThreads];    // the splat's first pair
+    int32_t gid[kEmitThreads];
+    int wsum[kEmitThreads / 32];
+    uint32_t hist[kMaxPasses][256];
+    int diff0[257];              // pass 0 digit counts as a circular difference array
+    uint32_t base0;              // + whole cycles of 256 consecutive tiles
+};
+
+// Digit counts of the tile keys [a, a + w) (consecutive tiles of one row) for
+// every pass, by ranges instead of per key: pass 0 (the low byte) through the
+// circular difference array, higher passes per digit the range overlaps.
+__device__ __forceinline__ void count_tile_range(EmitRows& S, uint32_t a, int w, int passes) {
+    atomicAdd(&S.base0, (uint32_t)(w >> 8));
+    const int r = w & 255, s0 = (int)(a & 255u);
+    if (r > 0) {
+        atomicAdd(&S.diff0[s0], 1);
+        if (s0 + r <= 256) {
+            atomicSub(&S.diff0[s0 + r], 1);
+        } else {
+            atomicSub(&S.diff0[256], 1);
+            atomicAdd(&S.diff0[0], 1);
+            atomicSub(&S.diff0[s0 + r - 256], 1);
+        }
+    }
+    const uint64_t b = (uint64_t)a + (uint64_t)w;  // one past the last key
+    for (int p = 1; p < passes; ++p) {
+        const int sh = 8 * p;
+        const uint64_t lo = (uint64_t)a >> sh, hi = (b - 1) >> sh;
+        for (uint64_t h = lo; h <= hi; ++h) {
+            const uint64_t c0 = max((uint64_t)a, h << sh), c1 = min(b, (h + 1) << sh);
+            atomicAdd(&S.hist[p][h & 255u], (uint32_t)(c1 - c0));
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kEmitThreads) emit_pairs(
+    CamParams cam, const float4* __restrict__ splats, const int32_t* __restrict__ tiles_touched,
+    const int64_t* __restrict__ poff, int64_t n, int64_t capacity, uint32_t* __restrict__ pkeys,
+    int32_t* __restrict__ pvals, int passes, uint32_t* __restrict__ thist) {
+    grid_dep_sync();
+    __shared__ EmitRows S;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t j = (int64_t)blockIdx.x * kEmitThreads + tid;  // Gaussian id
+    int nrows = 0;
+    if (j < n && tiles_touched[j] > 0) {
+        const int32_t g = (int32_t)j;
+        const float4 r0 = __ldg(splats + 3 * (int64_t)g), r1 = __ldg(splats + 3 * (int64_t)g + 1),
+                     r2 = __ldg(splats + 3 * (int64_t)g + 2);
+        const Ellipse e = ellipse_of(r0, r1, r2);
+        int ty0, ty1;
+        row_range(e, cam.nty, &ty0, &ty1);
+        nrows = max(ty1 - ty0, 0);
+        S.e[0][tid] = e.mux;
+        S.e[1][tid] = e.muy;
+        S.e[2][tid] = e.l11;
+        S.e[3][tid] = e.l12;
+        S.e[4][tid] = e.l22;
+        S.e[5][tid] = e.tau;
+        S.e[6][tid] = e.rx;
+        S.e[7][tid] = e.ry;
+        S.dyv[tid] = vertex_dy(e);
+        S.ty0[tid] = ty0;
+        S.pb[tid] = poff[j];
+        S.gid[tid] = g;
+    }
+    S.pcur[tid] = 0;
+#pragma unroll
+    for (int p = 0; p < kMaxPasses; ++p) S.hist[p][tid] = 0;
+    S.diff0[tid] = 0;
+    if (tid == 0) {
+        S.diff0[256] = 0;
+        S.base0 = 0;
+    }
+    int ri = nrows;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int rv = __shfl_up_sync(0xffffffffu, ri, o);
+        if (lane >= o) ri += rv;
+    }
+    if (lane == 31) S.wsum[warp] = ri;
+    __syncthreads();
+    int rbase = 0, rtotal = 0;
+#pragma unroll
+    for (int w = 0; w < kEmitThreads / 32; ++w) {
+        const int rv = S.wsum[w];
+        rbase += w < warp ? rv : 0;
+        rtotal += rv;
+    }
+    S.off[tid] = rbase + ri - nrows;
+    if (tid == 0) S.off[kEmitThreads] = rtotal;
+    __syncthreads();
+    for (int r = tid; r < rtotal; r += kEmitThreads) {
+        int lo = 0, hi = kEmitThreads;  // the last owner with off[owner] <= r
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (S.off[mid] <= r) lo = mid; else hi = mid;
+        }
+        const Ellipse e{S.e[0][lo], S.e[1][lo], S.e[2][lo], S.e[3][lo],
+                        S.e[4][lo], S.e[5][lo], S.e[6][lo], S.e[7][lo]};
+        const int ty = S.ty0[lo] + (r - S.off[lo]);
+        int tx0, tx1;
+        if (!row_span(e, S.dyv[lo], ty, cam.W, cam.H, cam.ntx, &tx0, &tx1)) continue;
+        const int w = tx1 - tx0;
+        const int64_t at = S.pb[lo] + atomicAdd(&S.pcur[lo], w);
+        const uint32_t a = (uint32_t)ty * (uint32_t)cam.ntx + (uint32_t)tx0;
+        const int32_t gid = S.gid[lo];
+        const int wv = (int)max64(0, min64(w, capacity - at));  // the pairs that fit
+        for (int i = 0; i < wv; ++i) {
+            pkeys[at + i] = a + (uint32_t)i;
+            pvals[at + i] = gid;
+        }
+        if (wv > 0) count_tile_range(S, a, wv, passes);
+    }
+    __syncthreads();
+    // pass 0: the running sum of the difference array, plus the whole cycles
+    {
+        int x = S.diff0[tid];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        __syncthreads();
+        if (lane == 31) S.wsum[warp] = x;
+        __syncthreads();
+        int pre = 0;
+#pragma unroll
+        for (int w = 0; w < kEmitThreads / 32; ++w) pre += w < warp ? S.wsum[w] : 0;
+        S.hist[0][tid] = S.base0 + (uint32_t)(pre + x);
+    }
+    __syncthreads();
+    for (int p = 0; p < passes; ++p)
+        if (S.hist[p][tid]) atomicAdd(thist + p * 256 + tid, S.hist[p][tid]);
+}
+
+// tile ranges [start, end) from the sorted keys (ranges zeroed beforehand);
+// none when the pair list did not fit (counts[1] > capacity)
+__global__ void __launch_bounds__(256) tile_ranges_kernel(const uint32_t* __restrict__ keys,
+                                                          const int64_t* __restrict__ counts,
+                                                          int64_t capacity,
+                                                          int2* __restrict__ ranges) {
+    grid_dep_sync();
+    if (counts[1] > capacity) return;
+    const int64_t n = counts[2];
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint32_t t = keys[i];
+        if (i == 0 || keys[i - 1] != t) ranges[t].x = (int)i;
+        if (i == n - 1 || keys[i + 1] != t) ranges[t].y = (int)(i + 1);
+    }
+}
+
+// empty tiles get [p, p) with p the end of the last non-empty tile before them
+// (so that starts are the exclusive prefix sum of the counts); one block
+__global__ void __launch_bounds__(kScanThreads) fill_empty_ranges(int2* __restrict__ ranges,
+                                                                  int64_t nt,
+                                                                  const int64_t* __restrict__ counts,
+                                                                  int64_t* __restrict__ counts_out) {
+    grid_dep_sync();
+    if (threadIdx.x == 0 && counts_out) {
+        counts_out[0] = counts[0];
+        counts_out[1] = counts[1];
+    }
+    __shared__ int s_part[kScanThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t per = (nt + kScanThreads - 1) / kScanThreads;
+    const int64_t lo = min64(nt, per * tid), hi = min64(nt, lo + per);
+    int m = 0;
+    for (int64_t t = lo; t < hi; ++t) m = max(m, ranges[t].y);
+    int x = m;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x = max(x, y);
+    }
+    if (lane == 31) s_part[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = s_part[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w = max(w, y);
+        }
+        s_part[lane] = w;
+    }
+    __syncthreads();
+    // exclusive running max of the ends before this thread's segment
+    int run = warp > 0 ? s_part[warp - 1] : 0;
+    int prev_lane = __shfl_up_sync(0xffffffffu, x, 1);
+    if (lane > 0) run = max(run, prev_lane);
+    for (int64_t t = lo; t < hi; ++t) {
+        int2 r = ranges[t];
+        if (r.y == 0) {
+            ranges[t] = make_int2(run, run);
+        } else {
+            run = max(run, r.y);
+        }
+    }
+}
+
+
+size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+int bits_for(int64_t v) {
+    int b = 0;
+    while (b < 62 && (int64_t(1) << b) <= v) ++b;
+    return std::max(b, 1);
+}
+
+
+}  // namespace
+
+RadixBinLayout radix_bin_layout(int64_t n, int64_t capacity, int64_t n_tiles) {
+    RadixBinLayout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off = align_up(off + bytes);
+        return o;
+    };
+    const int64_t nn = std::max<int64_t>(n, 1), cap = std::max<int64_t>(capacity, 1);
+    const int64_t nt = std::max<int64_t>(n_tiles, 1);
+    L.off_counts = take(8 * sizeof(int64_t) + 2 * kMaxPasses * 256 * sizeof(uint32_t));
+    L.off_bsum = take((size_t)(nblk_of(nn) + 1) * sizeof(int64_t));
+    L.off_dkeys0 = take((size_t)nn * 4);
+    L.off_dkeys1 = take((size_t)nn * 4);
+    L.off_dvals0 = take((size_t)nn * 4);
+    L.off_dvals1 = take((size_t)nn * 4);
+    L.off_poff = take((size_t)(nn + 1) * sizeof(int64_t));
+    L.off_pkeys0 = take((size_t)cap * 4);
+    L.off_pkeys1 = take((size_t)cap * 4);
+    L.off_pvals0 = take((size_t)cap * 4);
+    L.off_pvals1 = take((size_t)cap * 4);
+    L.off_hist = take(rs_ctl_bytes(std::max(nn, cap)));
+    L.off_lruns = take(lpt_runs_bytes(nt));
+    L.total = off;
+    return L;
+}
+
+cudaError_t run_bin_sort_radix(const CamParams& cam, int64_t n, const float* splats,
+                               const float* depths, const int32_t* tiles_touched, char* ws,
+                               const RadixBinLayout& L, int32_t* sorted_ids, int64_t capacity,
+                               int32_t* tile_ranges, int32_t* lpt_order, int64_t* counts_out,
+                               cudaStream_t st) {
+    auto* counts = reinterpret_cast<int64_t*>(ws + L.off_counts);
+    auto* bsum = reinterpret_cast<int64_t*>(ws + L.off_bsum);
+    auto* dk0 = reinterpret_cast<uint32_t*>(ws + L.off_dkeys0);
+    auto* dk1 = reinterpret_cast<uint32_t*>(ws + L.off_dkeys1);
+    auto* dv0 = reinterpret_cast<int32_t*>(ws + L.off_dvals0);
+    auto* dv1 = reinterpret_cast<int32_t*>(ws + L.off_dvals1);
+    auto* poff = reinterpret_cast<int64_t*>(ws + L.off_poff);
+    auto* pk0 = reinterpret_cast<uint32_t*>(ws + L.off_pkeys0);
+    auto* pk1 = reinterpret_cast<uint32_t*>(ws + L.off_pkeys1);
+    auto* pv0 = reinterpret_cast<int32_t*>(ws + L.off_pvals0);
+    auto* pv1 = reinterpret_cast<int32_t*>(ws + L.off_pvals1);
+    char* rs_ctl = ws + L.off_hist;
+    auto* sort_err = reinterpret_cast<unsigned long long*>(counts + kRadixErrWord);
+    auto* lruns = reinterpret_cast<uint64_t*>(ws + L.off_lruns);
+    const int64_t nt = (int64_t)cam.ntx * cam.nty;
+    auto* ranges = reinterpret_cast<int2*>(tile_ranges);
+    cudaError_t err;
+
+    // counts, then the digit counts of the depth sort and of the tile sort
+    auto* dhist = reinterpret_cast<uint32_t*>(counts + 8);
+    auto* thist = dhist + kMaxPasses * 256;
+    err = cudaMemsetAsync(counts, 0, 8 * sizeof(int64_t) + 2 * kMaxPasses * 256 * sizeof(uint32_t),
+                          st);
+    if (err != cudaSuccess) return err;
+    err = cudaMemsetAsync(tile_ranges, 0, (size_t)nt * 2 * sizeof(int32_t), st);
+    if (err != cudaSuccess) return err;
+
+    if (n > 0) {
+        const unsigned nb = (unsigned)nblk_of(n);
+        // 1. compact the visible Gaussians (id order) into (depth key, id)
+        err = launch(vis_count, nb, kRsBlock, 0, st, tiles_touched, n, bsum);
+        if (err != cudaSuccess) return err;
+        err = launch(scan_block_sums, 1, kScanThreads, 0, st, bsum, (const int64_t*)nullptr, n,
+                     counts + 0, (int64_t)0, (int64_t*)nullptr);
+        if (err != cudaSuccess) return err;
+        err = launch(vis_write, nb, kRsBlock, 0, st, tiles_touched, depths, n, (const int64_t*)bsum,
+                     dk0, dv0, dhist);
+        if (err != cudaSuccess) return err;
+        // 2. stable depth sort of the M visible (31 significant key bits)
+        uint32_t* dks = nullptr;
+        int32_t* dvs = nullptr;
+        err = radix_sort(dk0, dv0, dk1, dv1, nullptr, counts + 0, 0, n, 31, rs_ctl, dhist, sort_err,
+                         st, &dks, &dvs);
+        if (err != cudaSuccess) return err;
+        // 3. pair offsets in depth order, I = total, min(I, capacity)
+        err = launch(pairs_count, nb, kRsBlock, 0, st, (const int32_t*)dvs, tiles_touched,
+                     (const int64_t*)(counts + 0), bsum);
+        if (err != cudaSuccess) return err;
+        err = launch(scan_block_sums, 1, kScanThreads, 0, st, bsum, (const int64_t*)(counts + 0),
+                     (int64_t)0, counts + 1, capacity, counts + 2);
+        if (err != cudaSuccess) return err;
+        err = launch(pairs_offsets, nb, kRsBlock, 0, st, (const int32_t*)dvs, tiles_touched,
+                     (const int64_t*)(counts + 0), (const int64_t*)bsum, poff);
+        if (err != cudaSuccess) return err;
+        // 4. emit pairs in depth order
+        const int tbits = bits_for(nt - 1);
+        err = launch(emit_pairs, (unsigned)((n + kEmitThreads - 1) / kEmitThreads), kEmitThreads, 0,
+                     st, cam, reinterpret_cast<const float4*>(splats), tiles_touched,
+                     (const int64_t*)poff, n, capacity, pk0, pv0, (tbits + 7) / 8, thist);
+        if (err != cudaSuccess) return err;
+        // 5. stable sort by tile key; values land in sorted_ids
+        uint32_t* pks = nullptr;
+        err = radix_sort(pk0, pv0, pk1, pv1, sorted_ids, counts + 2, 0, capacity, tbits, rs_ctl,
+                         thist, sort_err, st, &pks, nullptr);
+        if (err != cudaSuccess) return err;
+        // 6. tile ranges
+        err = launch(tile_ranges_kernel, 1024, 256, 0, st, (const uint32_t*)pks,
+                     (const int64_t*)counts, capacity, ranges);
+        if (err != cudaSuccess) return err;
+    }
+    err = launch(fill_empty_ranges, 1, kScanThreads, 0, st, ranges, nt, (const int64_t*)counts,
+                 counts_out);
+    if (err != cudaSuccess) return err;
+    // 7. LPT order: tiles by descending count, ties by tile id
+    return launch_lpt(ranges, nt, lruns, lpt_order, st);
+}
+
+}  // namespace gs

@@ -47,6 +47,34 @@ struct BinSortLayout {
 };
 BinSortLayout binsort_layout(int64_t n, int64_t capacity, int64_t n_tiles);
 
+// The two-stage radix sort (gs_binsort_radix.cu), taken for pair capacities of
+// at least kRadixMinPairs; its counts words are M, I, min(I, capacity) and, at
+// kRadixErrWord, a flag that a look-back wait gave up.
+constexpr int64_t kRadixMinPairs = int64_t(8) << 20;
+constexpr int kRadixErrWord = 4;
+struct RadixBinLayout {
+    size_t total;
+    size_t off_counts;   // int64[8]
+    size_t off_bsum;     // int64[nblk_n + 1] scan block sums
+    size_t off_dkeys0, off_dkeys1, off_dvals0, off_dvals1;  // uint32 / int32 [n]
+    size_t off_poff;     // int64[n + 1]: each visible Gaussian's first pair (by id)
+    size_t off_pkeys0, off_pkeys1, off_pvals0, off_pvals1;  // [capacity]
+    size_t off_hist;     // radix sort control: pass tickets, digit counts, look-back words
+    size_t off_lruns;    // sorted runs of LPT keys
+};
+RadixBinLayout radix_bin_layout(int64_t n, int64_t capacity, int64_t n_tiles);
+cudaError_t run_bin_sort_radix(const CamParams& cam, int64_t n, const float* splats,
+                               const float* depths, const int32_t* tiles_touched, char* ws,
+                               const RadixBinLayout& L, int32_t* sorted_ids, int64_t capacity,
+                               int32_t* tile_ranges, int32_t* lpt_order, int64_t* counts_out,
+                               cudaStream_t st);
+
+// LPT order of the tiles from their ranges (gs_binsort.cu); runs is scratch of
+// lpt_runs_bytes(nt) bytes
+size_t lpt_runs_bytes(int64_t nt);
+cudaError_t launch_lpt(const int2* ranges, int64_t nt, uint64_t* runs, int32_t* lpt_order,
+                       cudaStream_t st);
+
 // Launch a kernel on st with programmatic stream serialisation: it may begin
 // launching while the kernel before it on st still runs, and waits for that
 // kernel's completion in its first statement (grid_dep_sync).  cluster > 1

@@ -74,7 +74,8 @@ typedef enum {
     GS_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or setting */
     GS_ERR_CUDA = 2,        /* a CUDA runtime call or launch failed */
     GS_ERR_CAPACITY = 3,    /* the pair list does not fit: see gs_bin_sort */
-    GS_ERR_TIMEOUT = 4,     /* reserved: a bounded device wait gave up */
+    GS_ERR_TIMEOUT = 4,     /* a bounded device wait gave up (gs_bin_sort's radix sort;
+                               reported when the call synchronises) */
     GS_ERR_WORKSPACE = 5    /* workspace smaller than the size query returned */
 } gs_status;
 
@@ -152,8 +153,11 @@ size_t gs_bin_sort_workspace_bytes(int64_t n, int64_t capacity, int32_t width, i
  * Per-tile buckets: every (tile, Gaussian) pair of the exact row spans is
  * counted in its tile's counter, a prefix scan of the counts lays the tiles
  * out, the pairs are scattered into their tiles' slices and every slice is
- * sorted by (depth, id).  The pair list is therefore ordered by
- * (tile, depth, id).
+ * sorted by (depth, id).  For capacities of 8 Mi pairs and more the call
+ * takes the two-stage radix sort instead ([K] Step 1 (d)): the visible
+ * Gaussians sorted by depth, their pairs emitted in that order and sorted
+ * stably by tile.  Either way the pair list is ordered by (tile, depth, id),
+ * and the outputs are the same bit for bit.
  *
  *   splats, depths, tiles_touched   outputs of gs_project
  *   workspace       device scratch of >= gs_bin_sort_workspace_bytes(...)

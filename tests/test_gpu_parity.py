@@ -50,8 +50,8 @@ def _check_project_bwd_alone(sc, cam, proj, r2):
         assert_grads_close(o.cpu().numpy(), getattr(rp, k), "alone:" + k, getattr(pm, k))
 
 
-def _full_parity(sc, cam, w, v=None, settings=None):
-    g = run_forward(sc, cam, settings=settings)
+def _full_parity(sc, cam, w, v=None, settings=None, capacity=None):
+    g = run_forward(sc, cam, settings=settings, capacity=capacity)
     ref = oracle.render(sc, cam)
     check_projection(g, ref.proj, sc)
     check_binning(g, ref.binning)
@@ -182,6 +182,47 @@ def test_binning_on_a_large_tile_grid():
     proj = oracle.project(sc, cam)
     check_projection(g, proj, sc)
     check_binning(g, oracle.bin_sort(cam, proj))
+
+
+# pair capacities from this size on take gs_bin_sort's two-stage radix sort
+RADIX_CAPACITY = 8 << 20
+
+
+@pytest.mark.parametrize("seed,W,H,n,deg", [(1, 150, 97, 900, 3), (2, 200, 120, 3000, 1)])
+def test_radix_path_full_parity(seed, W, H, n, deg):
+    rng = np.random.default_rng(seed)
+    sc, cam = ss.random_scene(rng, n, W, H, sh_degree=deg, log_scale=(-2.8, 0.8), logit_std=2.5)
+    w = rng.standard_normal((H, W, 3))
+    _full_parity(sc, cam, w, capacity=RADIX_CAPACITY)
+
+
+def test_radix_and_bucket_paths_agree():
+    sc, cam = ss.make_config(2)
+    a = run_forward(sc, cam)
+    b = run_forward(sc, cam, capacity=RADIX_CAPACITY)
+    assert a.n_pairs == b.n_pairs
+    for f in ("sorted_ids", "ranges", "lpt", "n_contrib", "last_idx"):
+        np.testing.assert_array_equal(getattr(a, f), getattr(b, f), err_msg=f)
+    np.testing.assert_array_equal(a.img, b.img)
+
+
+def test_radix_path_capacity_overflow():
+    import torch
+
+    import differentiable_gaussian_splatting_gb300 as gs
+    from gpu_util import t
+
+    # the heavy-tailed 3M scene has about 30M pairs: more than the capacity
+    sc, cam = ss.make_config(4)
+    r = gs.Rasterizer(cam, sc.sh_degree, sc.n, capacity=RADIX_CAPACITY)
+    gs.gs_project(r.cam, sc.n, sc.sh_degree, t(sc.means), t(sc.scales), t(sc.quats),
+                  t(sc.opacities), t(sc.sh), r.splats, r.depths, r.radii, r.tiles_touched)
+    with pytest.raises(gs.GSError):
+        gs.gs_bin_sort(r.cam, sc.n, r.splats, r.depths, r.tiles_touched, r.bin_ws, r.sorted_ids,
+                       r.capacity, r.tile_ranges, r.lpt_order)
+    torch.cuda.synchronize()
+    rg = r.tile_ranges.cpu().numpy()
+    assert np.all(rg == 0), "every tile range is empty when the list does not fit"
 
 
 def test_repeatable_integer_outputs():
