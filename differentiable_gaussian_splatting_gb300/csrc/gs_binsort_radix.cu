@@ -121,7 +121,7 @@ struct OnesweepSmem {
     int ticket;
 };
 
-__global__ void __launch_bounds__(kRsBlock, 2) rs_onesweep(
+__global__ void __launch_bounds__(kRsBlock, 4) rs_onesweep(
     const uint32_t* __restrict__ keys_in, const int32_t* __restrict__ vals_in,
     uint32_t* __restrict__ keys_out, int32_t* __restrict__ vals_out, const int64_t* n_dev,
     int64_t n_static, int pass, const uint32_t* __restrict__ ghist, int* __restrict__ tickets,
