@@ -383,8 +383,19 @@ def step_roofline(ms, sc, M, I, E, H, W, peaks, n_sm, sm_mhz):
 
 def kernel_launches(n, capacity, W, H) -> int:
     """Kernels one step launches."""
-    # binning: counter reset, span pass, scan, scatter, two slice sorts, two LPT kernels
-    bin_sort = 1 + 1 + 1 + 1 + 2 + 2
+    if capacity >= 8 << 20:
+        # long lists, two-stage radix sort: compaction count / scan / write, 4 depth passes,
+        # pair count / scan / offsets, emission, 1-3 tile passes, ranges, empty ranges, 2 LPT
+        tiles = ((W + 15) // 16) * ((H + 15) // 16)
+        tile_passes = (max(1, (tiles - 1).bit_length()) + 7) // 8
+        bin_sort = 3 + 4 + 3 + 1 + tile_passes + 2 + 2
+    else:
+        # buckets: counter reset, span pass, scan, scatter, two slice sorts, two LPT kernels,
+        # the long-slice plan and chunk sort, and one merge round per doubling up to min(n, capacity)
+        rounds, w = 0, 4096
+        while w < min(n, capacity):
+            rounds, w = rounds + 1, 2 * w
+        bin_sort = 1 + 1 + 1 + 1 + 2 + 2 + 2 + rounds
     # project 1, policy + forward 2, accumulator reset + backward 2, project backward 1
     return 1 + bin_sort + 2 + 2 + 1
 
