@@ -64,6 +64,8 @@ def parse():
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--sh-bf16", action="store_true",
+                   help="SH coefficients stored as bfloat16 (gs_project_sh16, gs_project_bwd_sh16)")
     return p.parse_args()
 
 
@@ -176,6 +178,10 @@ def run_gpu(args):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
     inputs = [to_dev(x) for x in (sc.means, sc.scales, sc.quats, sc.opacities, sc.sh)]
+    if args.sh_bf16:
+        inputs[4] = inputs[4].to(torch.bfloat16)
+    project = gs.gs_project_sh16 if args.sh_bf16 else gs.gs_project
+    project_bwd = gs.gs_project_bwd_sh16 if args.sh_bf16 else gs.gs_project_bwd
     dimg = to_dev(w)
     r = gs.Rasterizer(cam, sc.sh_degree, sc.n, device=dev)
     r.forward(*inputs)  # sizes the pair list (one host sync, outside the timed region)
@@ -191,7 +197,7 @@ def run_gpu(args):
         n = r.n
         if ev:
             ev[0].record(stream)
-        gs.gs_project(r.cam, n, r.sh_degree, *inputs, r.splats, r.depths, r.radii, r.tiles_touched)
+        project(r.cam, n, r.sh_degree, *inputs, r.splats, r.depths, r.radii, r.tiles_touched)
         if ev:
             ev[1].record(stream)
         gs.gs_bin_sort(r.cam, n, r.splats, r.depths, r.tiles_touched, r.bin_ws, r.sorted_ids,
@@ -207,8 +213,7 @@ def run_gpu(args):
                             r.settings)
         if ev:
             ev[4].record(stream)
-        gs.gs_project_bwd(r.cam, n, r.sh_degree, *inputs, r.tiles_touched, r.grad2d, r.touched,
-                          *grads)
+        project_bwd(r.cam, n, r.sh_degree, *inputs, r.tiles_touched, r.grad2d, r.touched, *grads)
         if ev:
             ev[5].record(stream)
 
@@ -272,7 +277,8 @@ def run_gpu(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": ss.CONFIG_NAMES[args.config], "gaussians": sc.n,
                        "image": f"{W}x{H}", "sh_degree": sc.sh_degree, "tile_pairs": n_pairs,
-                       "contributing_pairs": E, "parallelism": "replicas" if world > 1 else "single",
+                       "contributing_pairs": E, "sh_storage": "bf16" if args.sh_bf16 else "f32",
+                       "parallelism": "replicas" if world > 1 else "single",
                        "l2": "inputs larger than L2 (354 MB parameters + 354 MB gradients)"},
             "per_call_ms": per_call,
             "roofline": roof,
@@ -411,6 +417,8 @@ def run_e2e(gs, r, sc, cam, w, dev, args, n_pairs):
 
     host_in = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
                for a in (sc.means, sc.scales, sc.quats, sc.opacities, sc.sh, w)]
+    if args.sh_bf16:
+        host_in[4] = host_in[4].to(torch.bfloat16).pin_memory()
     dev_in = [[torch.empty(h.shape, dtype=h.dtype, device=dev) for h in host_in] for _ in range(2)]
     host_img = torch.empty((cam.height, cam.width, 3), dtype=torch.float32).pin_memory()
     bi = sum(h.numel() * h.element_size() for h in host_in)

@@ -26,6 +26,7 @@ from . import build as _build
 
 __all__ = [
     "gs_project", "gs_bin_sort", "gs_rasterize_fwd", "gs_rasterize_bwd", "gs_project_bwd",
+    "gs_project_sh16", "gs_project_bwd_sh16",
     "gs_raster_stats", "gs_default_settings", "Camera", "Settings", "Rasterizer", "library",
     "GSError", "TILE", "GRAD2D", "SPLAT_FLOATS",
 ]
@@ -122,6 +123,10 @@ def _declare(lib: C.CDLL) -> None:
     lib.gs_project_bwd.argtypes = [C.POINTER(Camera), _I64, C.c_int32] + [_P] * 13 + [_P]
     lib.gs_raster_stats.restype = st
     lib.gs_raster_stats.argtypes = [_P, C.c_size_t, _P, _P]
+    lib.gs_project_sh16.restype = st
+    lib.gs_project_sh16.argtypes = [C.POINTER(Camera), _I64, C.c_int32] + [_P] * 9 + [_P]
+    lib.gs_project_bwd_sh16.restype = st
+    lib.gs_project_bwd_sh16.argtypes = [C.POINTER(Camera), _I64, C.c_int32] + [_P] * 13 + [_P]
     lib.gs_bin_sort_noalloc.restype = st
     lib.gs_bin_sort_noalloc.argtypes = [C.POINTER(Camera), _I64, _P, _P, _P, _P, _I64, _P, _P, _P,
                                         _P, _P]
@@ -130,6 +135,12 @@ def _declare(lib: C.CDLL) -> None:
 # ---------------------------------------------------------------------------
 # argument marshalling
 # ---------------------------------------------------------------------------
+def _is_bf16(t) -> bool:
+    import torch
+
+    return isinstance(t, torch.Tensor) and t.dtype == torch.bfloat16
+
+
 def _ptr(t, name, dtype=None, numel=None, optional=False):
     """Device address of a tensor (checked), an int address, or None."""
     if t is None:
@@ -200,6 +211,22 @@ def gs_project(cam, n, sh_degree, means, scales, quats, opacities, sh, splats, d
         _ptr(splats, "splats", f, SPLAT_FLOATS * n), _ptr(depths, "depths", f, n),
         _ptr(radii, "radii", i, 2 * n), _ptr(tiles_touched, "tiles_touched", i, n), _stream(stream))
     _check("gs_project", st)
+
+
+def gs_project_sh16(cam, n, sh_degree, means, scales, quats, opacities, sh, splats, depths, radii,
+                    tiles_touched, stream=None):
+    """gs_project with the SH coefficients as a torch.bfloat16 tensor (see gs.h)."""
+    import torch
+
+    K = (int(sh_degree) + 1) ** 2
+    f, i = _f32(), _i32()
+    st = library().gs_project_sh16(
+        C.byref(Camera.of(cam)), int(n), int(sh_degree), _ptr(means, "means", f, 3 * n),
+        _ptr(scales, "scales", f, 3 * n), _ptr(quats, "quats", f, 4 * n),
+        _ptr(opacities, "opacities", f, n), _ptr(sh, "sh", torch.bfloat16, 3 * K * n),
+        _ptr(splats, "splats", f, SPLAT_FLOATS * n), _ptr(depths, "depths", f, n),
+        _ptr(radii, "radii", i, 2 * n), _ptr(tiles_touched, "tiles_touched", i, n), _stream(stream))
+    _check("gs_project_sh16", st)
 
 
 def gs_bin_sort_workspace_bytes(n, capacity, width, height) -> int:
@@ -309,6 +336,25 @@ def gs_project_bwd(cam, n, sh_degree, means, scales, quats, opacities, sh, tiles
     _check("gs_project_bwd", st)
 
 
+def gs_project_bwd_sh16(cam, n, sh_degree, means, scales, quats, opacities, sh, tiles_touched,
+                        grad2d, touched, dmeans, dscales, dquats, dopacities, dsh, stream=None):
+    """gs_project_bwd with the SH coefficients as a torch.bfloat16 tensor; dsh is fp32."""
+    import torch
+
+    K = (int(sh_degree) + 1) ** 2
+    f, i = _f32(), _i32()
+    st = library().gs_project_bwd_sh16(
+        C.byref(Camera.of(cam)), int(n), int(sh_degree), _ptr(means, "means", f, 3 * n),
+        _ptr(scales, "scales", f, 3 * n), _ptr(quats, "quats", f, 4 * n),
+        _ptr(opacities, "opacities", f, n, optional=True),
+        _ptr(sh, "sh", torch.bfloat16, 3 * K * n),
+        _ptr(tiles_touched, "tiles_touched", i, n), _ptr(grad2d, "grad2d", f, GRAD2D * n),
+        _ptr(touched, "touched", torch.uint8, n, optional=True), _ptr(dmeans, "dmeans", f, 3 * n),
+        _ptr(dscales, "dscales", f, 3 * n), _ptr(dquats, "dquats", f, 4 * n),
+        _ptr(dopacities, "dopacities", f, n), _ptr(dsh, "dsh", f, 3 * K * n), _stream(stream))
+    _check("gs_project_bwd_sh16", st)
+
+
 def gs_raster_stats(workspace, stream=None) -> dict:
     out = (C.c_int64 * 8)()
     st = library().gs_raster_stats(_ptr(workspace, "workspace"), workspace.numel(), out,
@@ -381,8 +427,10 @@ class Rasterizer:
 
     def forward(self, means, scales, quats, opacities, sh, sync_pairs: bool = True):
         n = self.n
-        gs_project(self.cam, n, self.sh_degree, means, scales, quats, opacities, sh, self.splats,
-                   self.depths, self.radii, self.tiles_touched)
+        # SH coefficients as torch.bfloat16 take the bfloat16-storage calls
+        project = gs_project_sh16 if _is_bf16(sh) else gs_project
+        project(self.cam, n, self.sh_degree, means, scales, quats, opacities, sh, self.splats,
+                self.depths, self.radii, self.tiles_touched)
         while True:
             try:
                 self.n_pairs = gs_bin_sort(self.cam, n, self.splats, self.depths,
@@ -416,9 +464,10 @@ class Rasterizer:
         g = Grads(torch.empty((n, 3), dtype=f, device=dev), torch.empty((n, 3), dtype=f, device=dev),
                   torch.empty((n, 4), dtype=f, device=dev), torch.empty(n, dtype=f, device=dev),
                   torch.empty((n, K, 3), dtype=f, device=dev))
-        gs_project_bwd(self.cam, n, self.sh_degree, means, scales, quats, opacities, sh,
-                       self.tiles_touched, self.grad2d, self.touched, g.means, g.scales, g.quats,
-                       g.opacities, g.sh)
+        project_bwd = gs_project_bwd_sh16 if _is_bf16(sh) else gs_project_bwd
+        project_bwd(self.cam, n, self.sh_degree, means, scales, quats, opacities, sh,
+                    self.tiles_touched, self.grad2d, self.touched, g.means, g.scales, g.quats,
+                    g.opacities, g.sh)
         return g
 
     def stats(self) -> dict:

@@ -14,6 +14,7 @@
 
 #include "../../include/gs.h"
 #include "gs_internal.h"
+#include "gs_sh16.h"
 
 using namespace gs;
 
@@ -312,6 +313,40 @@ gs_status gs_rasterize_bwd(const gs_camera* cam, const gs_settings* settings, in
                                       tile_ranges, lpt_order, static_cast<char*>(workspace), L,
                                       t_final, last_idx, dL_dimage, dL_dt_final, grad2d, touched,
                                       (cudaStream_t)stream));
+}
+
+gs_status gs_project_sh16(const gs_camera* cam, int64_t n, int32_t sh_degree, const float* means,
+                          const float* scales, const float* quats, const float* opacities,
+                          const uint16_t* sh, float* splats, float* depths, int32_t* radii,
+                          int32_t* tiles_touched, void* stream) {
+    if (!camera_ok(cam) || n < 0 || n > kMaxIds || sh_degree < 0 || sh_degree > 3)
+        return GS_ERR_INVALID_ARG;
+    if (n == 0) return GS_OK;
+    const void* ptrs[] = {means, scales, quats, opacities, sh, splats, depths, radii, tiles_touched};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return GS_ERR_INVALID_ARG;
+    return cuda_status(launch_project_sh16(cam_params(cam), n, sh_degree, means, scales, quats,
+                                           opacities, sh, splats, depths, radii, tiles_touched,
+                                           (cudaStream_t)stream));
+}
+
+gs_status gs_project_bwd_sh16(const gs_camera* cam, int64_t n, int32_t sh_degree,
+                              const float* means, const float* scales, const float* quats,
+                              const float* opacities, const uint16_t* sh,
+                              const int32_t* tiles_touched, const float* grad2d,
+                              const uint8_t* touched, float* dmeans, float* dscales,
+                              float* dquats, float* dopacities, float* dsh, void* stream) {
+    if (!camera_ok(cam) || n < 0 || n > kMaxIds || sh_degree < 0 || sh_degree > 3)
+        return GS_ERR_INVALID_ARG;
+    if (n == 0) return GS_OK;
+    const void* ptrs[] = {means, scales, quats, sh, tiles_touched, grad2d,
+                          dmeans, dscales, dquats, dopacities, dsh};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return GS_ERR_INVALID_ARG;
+    return cuda_status(launch_project_bwd_sh16(cam_params(cam), n, sh_degree, means, scales,
+                                               quats, opacities, sh, tiles_touched, grad2d,
+                                               touched, dmeans, dscales, dquats, dopacities, dsh,
+                                               (cudaStream_t)stream));
 }
 
 gs_status gs_project_bwd(const gs_camera* cam, int64_t n, int32_t sh_degree, const float* means,

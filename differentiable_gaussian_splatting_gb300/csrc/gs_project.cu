@@ -12,6 +12,7 @@
 
 #include "gs_device.cuh"
 #include "gs_internal.h"
+#include "gs_sh16.h"
 
 namespace gs {
 
@@ -29,6 +30,15 @@ constexpr float kY3b = 2.8906114426405538f;   // sqrt(105 / 4pi)
 constexpr float kY3c = 0.45704579946446572f;  // sqrt(21 / 32pi)
 constexpr float kY3d = 0.37317633259011540f;  // sqrt(7 / 16pi)
 constexpr float kY3e = 1.4453057213202769f;   // sqrt(105 / 16pi)
+
+// SH coefficients are fp32, or bfloat16 (the upper half of an fp32, as raw
+// 16-bit patterns; widening is exact)
+__device__ __forceinline__ float sh_at(const float* p, int64_t j) { return __ldg(p + j); }
+__device__ __forceinline__ float sh_at(const uint16_t* p, int64_t j) {
+    return __uint_as_float((uint32_t)__ldg(p + j) << 16);
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 __device__ __forceinline__ void sh_values(float x, float y, float z, float Y[16]) {
     float xx = x * x, yy = y * y, zz = z * z;
@@ -287,13 +297,13 @@ struct ProjShared {
     int wsum[kProjThreads / 32];
 };
 
-template <int K>
+template <int K, typename ShT>
 __global__ void __launch_bounds__(kProjThreads) project_kernel(CamParams cam, int64_t n,
                                                       const float* __restrict__ means,
                                                       const float* __restrict__ scales,
                                                       const float4* __restrict__ quats,
                                                       const float* __restrict__ opac,
-                                                      const float* __restrict__ sh,
+                                                      const ShT* __restrict__ sh,
                                                       float4* __restrict__ splats,
                                                       float* __restrict__ depths,
                                                       int2* __restrict__ radii,
@@ -334,11 +344,12 @@ __global__ void __launch_bounds__(kProjThreads) project_kernel(CamParams cam, in
         // those whose padded box meets the image into L2 while the rows are walked
         const float px = radd(P.rx, pad_of(P.rx));
         if (nrows > 0 && P.mux + px >= 0.5f && P.mux - px <= (float)cam.W - 0.5f) {
+            constexpr int kRowBytes = K * 3 * (int)sizeof(ShT);
             const char* row = reinterpret_cast<const char*>(sh + i * (K * 3));
 #pragma unroll
-            for (int b = 0; b < K * 12; b += 128)
+            for (int b = 0; b < kRowBytes; b += 128)
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(row + b));
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(row + K * 12 - 1));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(row + kRowBytes - 1));
         }
     }
     S.cnt[tid] = 0;
@@ -396,8 +407,35 @@ __global__ void __launch_bounds__(kProjThreads) project_kernel(CamParams cam, in
     float Y[16];
     sh_values(dx * inv, dy * inv, dz * inv, Y);
     float cr = 0.f, cg = 0.f, cb = 0.f;
-    const float* row = sh + (int64_t)i * (K * 3);
-    if constexpr ((K * 3) % 4 == 0) {
+    const ShT* row = sh + (int64_t)i * (K * 3);
+    if constexpr (sizeof(ShT) == 2 && (K * 3) % 24 == 0) {
+        // bfloat16: groups of eight basis functions = three 16-byte loads
+        const uint4* r4 = reinterpret_cast<const uint4*>(row);
+#pragma unroll
+        for (int g = 0; g < K / 8; ++g) {
+            const uint4 a = __ldg(r4 + 3 * g), b = __ldg(r4 + 3 * g + 1), c = __ldg(r4 + 3 * g + 2);
+            const uint32_t w[12] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                // coefficients 3q, 3q + 1, 3q + 2 of the group (two per 32-bit word)
+                const int e0 = 3 * q, e1 = 3 * q + 1, e2 = 3 * q + 2;
+                const float v0 = (e0 & 1) ? bf16_hi(w[e0 >> 1]) : bf16_lo(w[e0 >> 1]);
+                const float v1 = (e1 & 1) ? bf16_hi(w[e1 >> 1]) : bf16_lo(w[e1 >> 1]);
+                const float v2 = (e2 & 1) ? bf16_hi(w[e2 >> 1]) : bf16_lo(w[e2 >> 1]);
+                const float y = Y[8 * g + q];
+                cr += y * v0;
+                cg += y * v1;
+                cb += y * v2;
+            }
+        }
+    } else if constexpr (sizeof(ShT) == 2) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            cr += Y[k] * sh_at(row, 3 * k);
+            cg += Y[k] * sh_at(row, 3 * k + 1);
+            cb += Y[k] * sh_at(row, 3 * k + 2);
+        }
+    } else if constexpr ((K * 3) % 4 == 0) {
         // groups of four basis functions = three float4 (Kopanas, Step 3)
         const float4* r4 = reinterpret_cast<const float4*>(row);
 #pragma unroll
@@ -425,10 +463,11 @@ __global__ void __launch_bounds__(kProjThreads) project_kernel(CamParams cam, in
     tiles_touched[i] = tiles;
 }
 
-cudaError_t launch_project(const CamParams& cam, int64_t n, int sh_degree, const float* means,
-                           const float* scales, const float* quats, const float* opacities,
-                           const float* sh, float* splats, float* depths, int32_t* radii,
-                           int32_t* tiles_touched, cudaStream_t st) {
+template <typename ShT>
+cudaError_t launch_project_t(const CamParams& cam, int64_t n, int sh_degree, const float* means,
+                             const float* scales, const float* quats, const float* opacities,
+                             const ShT* sh, float* splats, float* depths, int32_t* radii,
+                             int32_t* tiles_touched, cudaStream_t st) {
     if (n == 0) return cudaSuccess;
     dim3 block(kProjThreads), grid((unsigned)((n + kProjThreads - 1) / kProjThreads));
     auto q4 = reinterpret_cast<const float4*>(quats);
@@ -439,11 +478,27 @@ cudaError_t launch_project(const CamParams& cam, int64_t n, int sh_degree, const
                       depths, r2, tiles_touched);
     };
     switch (sh_degree) {
-        case 0: return go(project_kernel<1>);
-        case 1: return go(project_kernel<4>);
-        case 2: return go(project_kernel<9>);
-        default: return go(project_kernel<16>);
+        case 0: return go(project_kernel<1, ShT>);
+        case 1: return go(project_kernel<4, ShT>);
+        case 2: return go(project_kernel<9, ShT>);
+        default: return go(project_kernel<16, ShT>);
     }
+}
+
+cudaError_t launch_project(const CamParams& cam, int64_t n, int sh_degree, const float* means,
+                           const float* scales, const float* quats, const float* opacities,
+                           const float* sh, float* splats, float* depths, int32_t* radii,
+                           int32_t* tiles_touched, cudaStream_t st) {
+    return launch_project_t(cam, n, sh_degree, means, scales, quats, opacities, sh, splats,
+                            depths, radii, tiles_touched, st);
+}
+
+cudaError_t launch_project_sh16(const CamParams& cam, int64_t n, int sh_degree, const float* means,
+                                const float* scales, const float* quats, const float* opacities,
+                                const uint16_t* sh, float* splats, float* depths, int32_t* radii,
+                                int32_t* tiles_touched, cudaStream_t st) {
+    return launch_project_t(cam, n, sh_degree, means, scales, quats, opacities, sh, splats,
+                            depths, radii, tiles_touched, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -456,10 +511,10 @@ cudaError_t launch_project(const CamParams& cam, int64_t n, int sh_degree, const
 // contiguous stores.
 constexpr int kPbThreads = 128;
 
-template <int K>
+template <int K, typename ShT>
 __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
     CamParams cam, int64_t n, const float* __restrict__ means, const float* __restrict__ scales,
-    const float4* __restrict__ quats, const float* __restrict__ sh,
+    const float4* __restrict__ quats, const ShT* __restrict__ sh,
     const int* __restrict__ tiles_touched, const float* __restrict__ grad2d,
     const uint8_t* __restrict__ touched, float* __restrict__ dmeans, float* __restrict__ dscales,
     float4* __restrict__ dquats, float* __restrict__ dopac, float* __restrict__ dsh) {
@@ -472,6 +527,12 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
     constexpr int RS = kVec ? 4 * (R4 | 1) : RW;    // floats from one staged row to the next
     __shared__ __align__(16) float srow[kPbThreads / 32][32 * RS];
     __shared__ int slive[kPbThreads / 32][32];  // rank among the live lanes -> lane
+    // bfloat16 rows of whole 16-byte words are staged in the upper part of the
+    // lane's fp32 row, whose gradients are written from its start: a group's
+    // coefficients are read before its gradients overwrite them
+    constexpr bool kVec16 = sizeof(ShT) == 2 && (RW % 8) == 0;
+    constexpr int R8 = kVec16 ? RW / 8 : 1;         // 16-byte words per bfloat16 row
+    constexpr int kOff16 = RS / 4 - R8;             // its first word within the row
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t wbase = (int64_t)blockIdx.x * kPbThreads + warp * 32;
     const int64_t i = wbase + lane;
@@ -494,7 +555,24 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
 
     // ---- stage the live rows (others read as zero and are never used)
     const uint32_t lmask = __ballot_sync(0xffffffffu, live);
-    if constexpr (kVec) {
+    if constexpr (kVec16) {
+        const uint4* sh16 = reinterpret_cast<const uint4*>(sh);
+        uint4* my16 = reinterpret_cast<uint4*>(my);
+        const int nl = __popc(lmask);
+        if (live) slive[warp][__popc(lmask & ((1u << lane) - 1u))] = lane;
+        __syncwarp();
+        for (int f = lane; f < nl * R8; f += 32) {
+            const int rank = f / R8, col = f - rank * R8;
+            const int l = slive[warp][rank];
+            cp_async16(&my16[l * (RS / 4) + kOff16 + col], sh16 + (wbase + l) * R8 + col);
+        }
+        cp_async_commit();  // waited for after the geometric part below
+    } else if constexpr (sizeof(ShT) == 2) {
+        if (live) {
+#pragma unroll
+            for (int j = 0; j < RW; ++j) my[lane * RS + j] = sh_at(sh, i * RW + j);
+        }
+    } else if constexpr (kVec) {
         const float4* sh4 = reinterpret_cast<const float4*>(sh);
         float4* my4 = reinterpret_cast<float4*>(my);
         const int nl = __popc(lmask);
@@ -613,7 +691,7 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
         dq = make_float4((dw - w * dot) * iqn, (dx_ - x * dot) * iqn, (dy_ - y * dot) * iqn,
                          (dz_ - z * dot) * iqn);
     }
-    if constexpr (kVec) cp_async_wait<0>();
+    if constexpr (kVec || kVec16) cp_async_wait<0>();
     __syncwarp();
 
     if (live) {
@@ -633,7 +711,33 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
             gdy += p * dY.y;
             gdz += p * dY.z;
         };
-        if constexpr (kVec) {
+        if constexpr (kVec16) {
+            // bfloat16 coefficients from the staged row, eight basis functions
+            // (three 16-byte words) at a time; their gradients into the fp32 row
+            const uint4* s16 = reinterpret_cast<const uint4*>(row) + kOff16;
+            float4* r4 = reinterpret_cast<float4*>(row);
+#pragma unroll
+            for (int q8 = 0; q8 < K / 8; ++q8) {
+                const uint4 a = s16[3 * q8], b = s16[3 * q8 + 1], c = s16[3 * q8 + 2];
+                const uint32_t wd[12] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w};
+                float o[24];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int e = 3 * q;
+                    const float c0 = (e & 1) ? bf16_hi(wd[e >> 1]) : bf16_lo(wd[e >> 1]);
+                    const float c1 = ((e + 1) & 1) ? bf16_hi(wd[(e + 1) >> 1]) : bf16_lo(wd[(e + 1) >> 1]);
+                    const float c2 = ((e + 2) & 1) ? bf16_hi(wd[(e + 2) >> 1]) : bf16_lo(wd[(e + 2) >> 1]);
+                    const float y = Y[8 * q8 + q];
+                    o[e] = y * gr;
+                    o[e + 1] = y * gg;
+                    o[e + 2] = y * gbl;
+                    basis(8 * q8 + q, c0, c1, c2);
+                }
+#pragma unroll
+                for (int f = 0; f < 6; ++f)
+                    r4[6 * q8 + f] = make_float4(o[4 * f], o[4 * f + 1], o[4 * f + 2], o[4 * f + 3]);
+            }
+        } else if constexpr (kVec) {
             // groups of four basis functions = three float4 of the row
             float4* r4 = reinterpret_cast<float4*>(row);
 #pragma unroll
@@ -698,12 +802,12 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
     }
 }
 
-cudaError_t launch_project_bwd(const CamParams& cam, int64_t n, int sh_degree, const float* means,
-                               const float* scales, const float* quats, const float* opacities,
-                               const float* sh, const int32_t* tiles_touched, const float* grad2d,
-                               const uint8_t* touched, float* dmeans, float* dscales,
-                               float* dquats, float* dopacities, float* dsh, cudaStream_t st) {
-    (void)opacities;
+template <typename ShT>
+cudaError_t launch_project_bwd_t(const CamParams& cam, int64_t n, int sh_degree,
+                                 const float* means, const float* scales, const float* quats,
+                                 const ShT* sh, const int32_t* tiles_touched, const float* grad2d,
+                                 const uint8_t* touched, float* dmeans, float* dscales,
+                                 float* dquats, float* dopacities, float* dsh, cudaStream_t st) {
     if (n == 0) return cudaSuccess;
     dim3 block(kPbThreads), grid((unsigned)((n + kPbThreads - 1) / kPbThreads));
     auto q4 = reinterpret_cast<const float4*>(quats);
@@ -713,11 +817,32 @@ cudaError_t launch_project_bwd(const CamParams& cam, int64_t n, int sh_degree, c
                       grad2d, touched, dmeans, dscales, dq4, dopacities, dsh);
     };
     switch (sh_degree) {
-        case 0: return go(project_bwd_kernel<1>);
-        case 1: return go(project_bwd_kernel<4>);
-        case 2: return go(project_bwd_kernel<9>);
-        default: return go(project_bwd_kernel<16>);
+        case 0: return go(project_bwd_kernel<1, ShT>);
+        case 1: return go(project_bwd_kernel<4, ShT>);
+        case 2: return go(project_bwd_kernel<9, ShT>);
+        default: return go(project_bwd_kernel<16, ShT>);
     }
+}
+
+cudaError_t launch_project_bwd(const CamParams& cam, int64_t n, int sh_degree, const float* means,
+                               const float* scales, const float* quats, const float* opacities,
+                               const float* sh, const int32_t* tiles_touched, const float* grad2d,
+                               const uint8_t* touched, float* dmeans, float* dscales,
+                               float* dquats, float* dopacities, float* dsh, cudaStream_t st) {
+    (void)opacities;
+    return launch_project_bwd_t(cam, n, sh_degree, means, scales, quats, sh, tiles_touched,
+                                grad2d, touched, dmeans, dscales, dquats, dopacities, dsh, st);
+}
+
+cudaError_t launch_project_bwd_sh16(const CamParams& cam, int64_t n, int sh_degree,
+                                    const float* means, const float* scales, const float* quats,
+                                    const float* opacities, const uint16_t* sh,
+                                    const int32_t* tiles_touched, const float* grad2d,
+                                    const uint8_t* touched, float* dmeans, float* dscales,
+                                    float* dquats, float* dopacities, float* dsh, cudaStream_t st) {
+    (void)opacities;
+    return launch_project_bwd_t(cam, n, sh_degree, means, scales, quats, sh, tiles_touched,
+                                grad2d, touched, dmeans, dscales, dquats, dopacities, dsh, st);
 }
 
 }  // namespace gs

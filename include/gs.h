@@ -277,6 +277,25 @@ gs_status gs_raster_stats(const void* workspace, size_t workspace_bytes, int64_t
                           void* stream);
 
 /*
+ * gs_project_sh16, gs_project_bwd_sh16 -- gs_project and gs_project_bwd with the
+ * SH coefficients stored as bfloat16 ([K] Step 6: bfloat16 SH halves the bytes
+ * the two calls read for them).  `sh` holds the raw 16-bit patterns (the upper
+ * half of each fp32 value; widening is exact), same layout [n][K][3], 16-byte
+ * aligned.  Everything else -- arguments, outputs (dsh is fp32), errors -- is as
+ * for the fp32 calls; the arithmetic is fp32 on the widened values.
+ */
+gs_status gs_project_sh16(const gs_camera* cam, int64_t n, int32_t sh_degree, const float* means,
+                          const float* scales, const float* quats, const float* opacities,
+                          const uint16_t* sh, float* splats, float* depths, int32_t* radii,
+                          int32_t* tiles_touched, void* stream);
+gs_status gs_project_bwd_sh16(const gs_camera* cam, int64_t n, int32_t sh_degree,
+                              const float* means, const float* scales, const float* quats,
+                              const float* opacities, const uint16_t* sh,
+                              const int32_t* tiles_touched, const float* grad2d,
+                              const uint8_t* touched, float* dmeans, float* dscales,
+                              float* dquats, float* dopacities, float* dsh, void* stream);
+
+/*
  * gs_bin_sort_noalloc -- gs_bin_sort for callers that may not allocate device
  * memory.  The papers have no counterpart: it exists for hosts that own all
  * of the GPU's memory (a plugin inside an application with its own

@@ -42,13 +42,17 @@ class GpuRun:
     last_idx: np.ndarray
 
 
-def run_forward(sc, cam, settings=None, capacity=None):
+def run_forward(sc, cam, settings=None, capacity=None, sh_bf16=False):
     import torch
 
     import differentiable_gaussian_splatting_gb300 as gs
 
     r = gs.Rasterizer(cam, sc.sh_degree, sc.n, capacity=capacity, settings=settings)
-    r.forward(t(sc.means), t(sc.scales), t(sc.quats), t(sc.opacities), t(sc.sh))
+    sh = t(sc.sh)
+    if sh_bf16:
+        sh = sh.to(torch.bfloat16)  # the scene's SH must be bfloat16 values already
+        assert torch.equal(sh.float(), t(sc.sh).float())
+    r.forward(t(sc.means), t(sc.scales), t(sc.quats), t(sc.opacities), sh)
     torch.cuda.synchronize()
     I = r.n_pairs
     return GpuRun(r, r.splats.cpu().numpy(), r.depths.cpu().numpy(), r.radii.cpu().numpy(),

@@ -50,8 +50,8 @@ def _check_project_bwd_alone(sc, cam, proj, r2):
         assert_grads_close(o.cpu().numpy(), getattr(rp, k), "alone:" + k, getattr(pm, k))
 
 
-def _full_parity(sc, cam, w, v=None, settings=None, capacity=None):
-    g = run_forward(sc, cam, settings=settings, capacity=capacity)
+def _full_parity(sc, cam, w, v=None, settings=None, capacity=None, sh_bf16=False):
+    g = run_forward(sc, cam, settings=settings, capacity=capacity, sh_bf16=sh_bf16)
     ref = oracle.render(sc, cam)
     check_projection(g, ref.proj, sc)
     check_binning(g, ref.binning)
@@ -223,6 +223,33 @@ def test_radix_path_capacity_overflow():
     torch.cuda.synchronize()
     rg = r.tile_ranges.cpu().numpy()
     assert np.all(rg == 0), "every tile range is empty when the list does not fit"
+
+
+def _bf16_values(a):
+    """a rounded to bfloat16 (round to nearest even), as float32 values."""
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).float().numpy()
+
+
+@pytest.mark.parametrize("seed,W,H,n,deg", [(0, 37, 53, 300, 0), (5, 80, 60, 700, 1),
+                                            (3, 64, 40, 600, 2), (1, 150, 97, 900, 3)])
+def test_bf16_sh_full_parity(seed, W, H, n, deg):
+    # SH stored as bfloat16: the oracle gets the same (widened) values, so the
+    # tolerances are those of the fp32 path
+    rng = np.random.default_rng(seed)
+    sc, cam = ss.random_scene(rng, n, W, H, sh_degree=deg, log_scale=(-2.8, 0.8), logit_std=2.5)
+    sc.sh = _bf16_values(sc.sh).astype(sc.sh.dtype)
+    w = rng.standard_normal((H, W, 3))
+    v = rng.standard_normal((H, W))
+    _full_parity(sc, cam, w, v, sh_bf16=True)
+
+
+def test_bf16_sh_config2_full():
+    sc, cam = ss.make_config(2, n=20_000)
+    sc.sh = _bf16_values(sc.sh).astype(sc.sh.dtype)
+    w = ss.loss_weights(2, cam.height, cam.width)
+    _full_parity(sc, cam, w, sh_bf16=True)
 
 
 def test_repeatable_integer_outputs():
