@@ -20,6 +20,9 @@ The arithmetic lives in ``gs_oracle.c`` (plain C, compiled with
 Every function here is argument marshalling around the C entry points; the
 docstrings of ``gs_oracle.c`` cite the passages each one follows.
 
+The training step after the chain rule (``raw_grads``, ``adam_step``) sits here
+too: the GPU's fused chain rule + Adam call is compared with it.
+
 Parity pins: every function is pinned by a ``-m "not gpu"`` test under
 ``tests/`` (closed forms, library special cases, brute force, finite
 differences); see the test names in ``tests/test_oracle_*.py``.  The chunking
@@ -98,6 +101,11 @@ def _declare(lib: C.CDLL) -> None:
     lib.ora_project_bwd_mag.argtypes = [_I64, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                         _P, _P]
     lib.ora_policy.argtypes = [_I64, _P, _I64, C.c_double, C.c_double, C.c_double, _I64, _P, _P]
+    lib.ora_raw_grads.restype = None
+    lib.ora_raw_grads.argtypes = [_I64, _P, _P, _P, _P, _P, _P]
+    lib.ora_adam_step.restype = None
+    lib.ora_adam_step.argtypes = [_I64, _P, _P, _P, _P, C.c_double, C.c_double, C.c_double,
+                                  C.c_double, _I64]
     lib.ora_policy.restype = C.c_double
 
 
@@ -325,6 +333,30 @@ def policy(counts_desc, K: int, lam: float = 256.0, beta: float = 0.05, eps: flo
     k = C.c_int64(0)
     cost = lib.ora_policy(len(c), _p(c), int(K), lam, beta, eps, int(h_max), C.byref(h), C.byref(k))
     return int(h.value), int(k.value), float(cost)
+
+
+def raw_grads(scales: np.ndarray, opacities: np.ndarray, pg: ParamGrads):
+    """Gradients w.r.t. log-scales and opacity logits from those w.r.t. the activated
+    scales and opacities (the training step after the chain rule)."""
+    lib = _lib("f64")
+    s = np.ascontiguousarray(scales, np.float64)
+    o = np.ascontiguousarray(opacities, np.float64).reshape(-1)
+    ds = np.ascontiguousarray(pg.scales, np.float64)
+    do = np.ascontiguousarray(pg.opacities, np.float64).reshape(-1)
+    dls = np.empty_like(ds)
+    dlo = np.empty_like(do)
+    lib.ora_raw_grads(len(o), _p(s), _p(o), _p(ds), _p(do), _p(dls), _p(dlo))
+    return dls, dlo
+
+
+def adam_step(p: np.ndarray, m: np.ndarray, v: np.ndarray, g: np.ndarray, lr: float,
+              b1: float, b2: float, eps: float, t: int) -> None:
+    """One Adam step t >= 1 on float64 arrays, in place (p, m, v)."""
+    for a in (p, m, v):
+        assert a.dtype == np.float64 and a.flags.c_contiguous
+    gg = np.ascontiguousarray(g, np.float64)
+    assert gg.size == p.size == m.size == v.size
+    _lib("f64").ora_adam_step(p.size, _p(p), _p(m), _p(v), _p(gg), lr, b1, b2, eps, int(t))
 
 
 def sh_basis(dirs: np.ndarray) -> tuple[np.ndarray, np.ndarray]:

@@ -1182,3 +1182,32 @@ double ora_policy(int64_t nt, const int64_t* counts_desc, int64_t K, double lamb
     *k_out = bk;
     return best / Kd;
 }
+
+/*
+ * The training step after the chain rule ("proj_sh_bwd_adam" of the pages' Metal
+ * port, where the projection backward and the Adam step are one pass): the
+ * gradients of the raw parameters a training loop optimises, then one Adam step.
+ *
+ * Raw gradients: scales are exp(log-scales) and opacities sigmoid(logits), so
+ * dL/dlog s = s dL/ds and dL/dlogit = o (1 - o) dL/do.
+ */
+void ora_raw_grads(int64_t n, const double* scales, const double* opac, const double* dscales,
+                   const double* dopac, double* dlog_scales, double* dlogits) {
+    for (int64_t i = 0; i < 3 * n; ++i) dlog_scales[i] = scales[i] * dscales[i];
+    for (int64_t i = 0; i < n; ++i) dlogits[i] = opac[i] * (1.0 - opac[i]) * dopac[i];
+}
+
+/*
+ * Adam (Kingma & Ba), one step t >= 1 on count elements, in place:
+ *   m <- b1 m + (1 - b1) g,  v <- b2 v + (1 - b2) g^2,
+ *   p <- p - lr (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps)
+ */
+void ora_adam_step(int64_t count, double* p, double* m, double* v, const double* g, double lr,
+                   double b1, double b2, double eps, int64_t t) {
+    double c1 = 1.0 - pow(b1, (double)t), c2 = 1.0 - pow(b2, (double)t);
+    for (int64_t i = 0; i < count; ++i) {
+        m[i] = b1 * m[i] + (1.0 - b1) * g[i];
+        v[i] = b2 * v[i] + (1.0 - b2) * g[i] * g[i];
+        p[i] -= lr * (m[i] / c1) / (sqrt(v[i] / c2) + eps);
+    }
+}
