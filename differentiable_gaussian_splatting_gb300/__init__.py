@@ -26,7 +26,7 @@ from . import build as _build
 
 __all__ = [
     "gs_project", "gs_bin_sort", "gs_rasterize_fwd", "gs_rasterize_bwd", "gs_project_bwd",
-    "gs_project_sh16", "gs_project_bwd_sh16",
+    "gs_project_sh16", "gs_project_bwd_sh16", "gs_project_bwd_adam", "AdamSettings",
     "gs_raster_stats", "gs_default_settings", "Camera", "Settings", "Rasterizer", "library",
     "GSError", "TILE", "GRAD2D", "SPLAT_FLOATS",
 ]
@@ -73,6 +73,20 @@ class Settings(C.Structure):
     _fields_ = [("split_mode", C.c_int32), ("force_h", C.c_int32), ("force_k", C.c_int32),
                 ("h_max", C.c_int32), ("policy_lambda", C.c_float), ("policy_beta", C.c_float),
                 ("policy_eps", C.c_float)]
+
+
+class AdamSettings(C.Structure):
+    """gs_adam_settings: learning rates per parameter group, Adam's betas and eps, step t."""
+    _fields_ = [("lr_means", C.c_float), ("lr_scales", C.c_float), ("lr_quats", C.c_float),
+                ("lr_opacities", C.c_float), ("lr_sh0", C.c_float), ("lr_shN", C.c_float),
+                ("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float),
+                ("step", C.c_int32)]
+
+
+class AdamMoments(C.Structure):
+    """gs_adam_moments: device pointers of the first and second moments, one per
+    parameter (means, log-scales, quaternions, opacity logits, SH)."""
+    _fields_ = [("m", C.c_void_p * 5), ("v", C.c_void_p * 5)]
 
 
 _lib = None
@@ -127,6 +141,9 @@ def _declare(lib: C.CDLL) -> None:
     lib.gs_project_sh16.argtypes = [C.POINTER(Camera), _I64, C.c_int32] + [_P] * 9 + [_P]
     lib.gs_project_bwd_sh16.restype = st
     lib.gs_project_bwd_sh16.argtypes = [C.POINTER(Camera), _I64, C.c_int32] + [_P] * 13 + [_P]
+    lib.gs_project_bwd_adam.restype = st
+    lib.gs_project_bwd_adam.argtypes = ([C.POINTER(Camera), _I64, C.c_int32] + [_P] * 8 +
+                                        [C.POINTER(AdamMoments), C.POINTER(AdamSettings), _P])
     lib.gs_bin_sort_noalloc.restype = st
     lib.gs_bin_sort_noalloc.argtypes = [C.POINTER(Camera), _I64, _P, _P, _P, _P, _I64, _P, _P, _P,
                                         _P, _P]
@@ -353,6 +370,33 @@ def gs_project_bwd_sh16(cam, n, sh_degree, means, scales, quats, opacities, sh, 
         _ptr(dscales, "dscales", f, 3 * n), _ptr(dquats, "dquats", f, 4 * n),
         _ptr(dopacities, "dopacities", f, n), _ptr(dsh, "dsh", f, 3 * K * n), _stream(stream))
     _check("gs_project_bwd_sh16", st)
+
+
+def gs_project_bwd_adam(cam, n, sh_degree, means, log_scales, quats, opacity_logits, sh,
+                        tiles_touched, grad2d, touched, m, v, settings: AdamSettings,
+                        stream=None):
+    """gs_project_bwd fused with one Adam step on the raw parameters, in place (see gs.h).
+    m and v: five tensors each, shaped like (means, log_scales, quats, opacity_logits, sh)."""
+    import torch
+
+    K = (int(sh_degree) + 1) ** 2
+    f, i = _f32(), _i32()
+    sizes = (3 * n, 3 * n, 4 * n, n, 3 * K * n)
+    names = ("means", "log_scales", "quats", "opacity_logits", "sh")
+    if len(m) != 5 or len(v) != 5:
+        raise ValueError("m and v need five tensors each")
+    mom = AdamMoments()
+    for k in range(5):
+        mom.m[k] = _ptr(m[k], "m." + names[k], f, sizes[k])
+        mom.v[k] = _ptr(v[k], "v." + names[k], f, sizes[k])
+    params = (means, log_scales, quats, opacity_logits, sh)
+    st = library().gs_project_bwd_adam(
+        C.byref(Camera.of(cam)), int(n), int(sh_degree),
+        *[_ptr(t, names[k], f, sizes[k]) for k, t in enumerate(params)],
+        _ptr(tiles_touched, "tiles_touched", i, n), _ptr(grad2d, "grad2d", f, GRAD2D * n),
+        _ptr(touched, "touched", torch.uint8, n, optional=True), C.byref(mom),
+        C.byref(settings), _stream(stream))
+    _check("gs_project_bwd_adam", st)
 
 
 def gs_raster_stats(workspace, stream=None) -> dict:

@@ -14,7 +14,7 @@
 
 #include "../../include/gs.h"
 #include "gs_internal.h"
-#include "gs_sh16.h"
+#include "gs_project_variants.h"
 
 using namespace gs;
 
@@ -347,6 +347,44 @@ gs_status gs_project_bwd_sh16(const gs_camera* cam, int64_t n, int32_t sh_degree
                                                quats, opacities, sh, tiles_touched, grad2d,
                                                touched, dmeans, dscales, dquats, dopacities, dsh,
                                                (cudaStream_t)stream));
+}
+
+gs_status gs_project_bwd_adam(const gs_camera* cam, int64_t n, int32_t sh_degree, float* means,
+                              float* log_scales, float* quats, float* opacity_logits, float* sh,
+                              const int32_t* tiles_touched, const float* grad2d,
+                              const uint8_t* touched, const gs_adam_moments* moments,
+                              const gs_adam_settings* adam, void* stream) {
+    if (!camera_ok(cam) || n < 0 || n > kMaxIds || sh_degree < 0 || sh_degree > 3 || !moments ||
+        !adam)
+        return GS_ERR_INVALID_ARG;
+    const float lrs[6] = {adam->lr_means, adam->lr_scales, adam->lr_quats, adam->lr_opacities,
+                          adam->lr_sh0, adam->lr_shN};
+    for (float lr : lrs)
+        if (!finite_f(lr) || lr < 0.f) return GS_ERR_INVALID_ARG;
+    if (!(adam->beta1 >= 0.f && adam->beta1 < 1.f) || !(adam->beta2 >= 0.f && adam->beta2 < 1.f) ||
+        !(adam->eps > 0.f) || !finite_f(adam->eps) || adam->step < 1)
+        return GS_ERR_INVALID_ARG;
+    if (n == 0) return GS_OK;
+    const void* ptrs[] = {means, log_scales, quats, opacity_logits, sh, tiles_touched, grad2d,
+                          moments->m[0], moments->m[1], moments->m[2], moments->m[3], moments->m[4],
+                          moments->v[0], moments->v[1], moments->v[2], moments->v[3], moments->v[4]};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return GS_ERR_INVALID_ARG;
+    AdamArgs a{};
+    float* params[5] = {means, log_scales, quats, opacity_logits, sh};
+    for (int k = 0; k < 5; ++k) {
+        a.p[k] = params[k];
+        a.m[k] = moments->m[k];
+        a.v[k] = moments->v[k];
+    }
+    for (int k = 0; k < 6; ++k) a.lr[k] = lrs[k];
+    a.b1 = adam->beta1;
+    a.b2 = adam->beta2;
+    a.eps = adam->eps;
+    a.c1 = (float)(1.0 / (1.0 - std::pow((double)adam->beta1, (double)adam->step)));
+    a.c2 = (float)(1.0 / (1.0 - std::pow((double)adam->beta2, (double)adam->step)));
+    return cuda_status(launch_project_bwd_adam(cam_params(cam), n, sh_degree, tiles_touched,
+                                               grad2d, touched, a, (cudaStream_t)stream));
 }
 
 gs_status gs_project_bwd(const gs_camera* cam, int64_t n, int32_t sh_degree, const float* means,

@@ -12,7 +12,7 @@
 
 #include "gs_device.cuh"
 #include "gs_internal.h"
-#include "gs_sh16.h"
+#include "gs_project_variants.h"
 
 namespace gs {
 
@@ -511,13 +511,40 @@ cudaError_t launch_project_sh16(const CamParams& cam, int64_t n, int sh_degree, 
 // contiguous stores.
 constexpr int kPbThreads = 128;
 
-template <int K, typename ShT>
+// A parameter read: through the read-only path, except when the kernel updates
+// the parameters in place (the fused Adam step)
+template <bool kInPlace, typename T>
+__device__ __forceinline__ T ld_param(const T* p) {
+    if constexpr (kInPlace) return *p;
+    else return __ldg(p);
+}
+
+// One Adam step of one parameter (fp32): the moments are updated in place and
+// the new parameter value is returned
+__device__ __forceinline__ float adam1(float p, float& m, float& v, float g, float lr,
+                                       const AdamArgs& a) {
+    m = fmaf(a.b1, m, (1.f - a.b1) * g);
+    v = fmaf(a.b2, v, (1.f - a.b2) * (g * g));
+    return p - lr * (m * a.c1) / (sqrtf(v * a.c2) + a.eps);
+}
+
+__device__ __forceinline__ void adam_at(float* p, float* m, float* v, int64_t j, float g, float lr,
+                                        const AdamArgs& a) {
+    float mj = m[j], vj = v[j];
+    p[j] = adam1(p[j], mj, vj, g, lr, a);
+    m[j] = mj;
+    v[j] = vj;
+}
+
+// kAdam: the parameters are the raw ones (means, log-scales, quaternions,
+// opacity logits, SH in ad.p[]); instead of writing gradients the kernel takes
+// one Adam step on them (scales = exp(log-scales), opacities = sigmoid(logits)).
+template <int K, typename ShT, bool kAdam>
 __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
-    CamParams cam, int64_t n, const float* __restrict__ means, const float* __restrict__ scales,
-    const float4* __restrict__ quats, const ShT* __restrict__ sh,
-    const int* __restrict__ tiles_touched, const float* __restrict__ grad2d,
+    CamParams cam, int64_t n, const float* means, const float* scales, const float4* quats,
+    const ShT* sh, const int* __restrict__ tiles_touched, const float* __restrict__ grad2d,
     const uint8_t* __restrict__ touched, float* __restrict__ dmeans, float* __restrict__ dscales,
-    float4* __restrict__ dquats, float* __restrict__ dopac, float* __restrict__ dsh) {
+    float4* __restrict__ dquats, float* __restrict__ dopac, float* __restrict__ dsh, AdamArgs ad) {
     grid_dep_sync();
     constexpr int RW = K * 3;                       // floats per SH row
     constexpr bool kVec = (RW % 4) == 0;            // rows of whole float4
@@ -542,15 +569,18 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
     // this lane's inputs, requested before the SH rows are staged
     float g[9], m[3], s[3];
     float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    float sig = 0.f;  // the opacity, for the logit's chain rule (fused Adam)
     if (live) {
 #pragma unroll
         for (int r = 0; r < 9; ++r) g[r] = grad2d[9 * i + r];
 #pragma unroll
         for (int r = 0; r < 3; ++r) {
-            m[r] = means[3 * i + r];
-            s[r] = scales[3 * i + r];
+            m[r] = ld_param<kAdam>(means + 3 * i + r);
+            s[r] = ld_param<kAdam>(scales + 3 * i + r);
+            if constexpr (kAdam) s[r] = expf(s[r]);
         }
-        q4 = quats[i];
+        q4 = ld_param<kAdam>(quats + i);
+        if constexpr (kAdam) sig = 1.f / (1.f + expf(-ad.p[3][i]));
     }
 
     // ---- stage the live rows (others read as zero and are never used)
@@ -587,7 +617,7 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
     } else {
         if (live) {
 #pragma unroll
-            for (int j = 0; j < RW; ++j) my[lane * RW + j] = __ldg(sh + i * RW + j);
+            for (int j = 0; j < RW; ++j) my[lane * RW + j] = ld_param<kAdam>(sh + i * RW + j);
         }
     }
 
@@ -767,26 +797,105 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
         dm[1] += (gdy - hy * dd) * ilen;
         dm[2] += (gdz - hz * dd) * ilen;
 
-        dmeans[3 * i] = dm[0];
-        dmeans[3 * i + 1] = dm[1];
-        dmeans[3 * i + 2] = dm[2];
-        dscales[3 * i] = ds[0];
-        dscales[3 * i + 1] = ds[1];
-        dscales[3 * i + 2] = ds[2];
-        dquats[i] = dq;
-        dopac[i] = g[5];
+        if constexpr (!kAdam) {
+            dmeans[3 * i] = dm[0];
+            dmeans[3 * i + 1] = dm[1];
+            dmeans[3 * i + 2] = dm[2];
+            dscales[3 * i] = ds[0];
+            dscales[3 * i + 1] = ds[1];
+            dscales[3 * i + 2] = ds[2];
+            dquats[i] = dq;
+            dopac[i] = g[5];
+        }
     } else if (in) {
-        dmeans[3 * i] = dmeans[3 * i + 1] = dmeans[3 * i + 2] = 0.f;
-        dscales[3 * i] = dscales[3 * i + 1] = dscales[3 * i + 2] = 0.f;
-        dquats[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        dopac[i] = 0.f;
+        if constexpr (!kAdam) {
+            dmeans[3 * i] = dmeans[3 * i + 1] = dmeans[3 * i + 2] = 0.f;
+            dscales[3 * i] = dscales[3 * i + 1] = dscales[3 * i + 2] = 0.f;
+            dquats[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            dopac[i] = 0.f;
+        }
+    }
+    if constexpr (kAdam) {
+        // every Gaussian takes the step (zero gradients where not live): the raw
+        // gradients are dL/dlog s = s dL/ds and dL/dlogit = o (1 - o) dL/do
+        if (in) {
+            // the eleven geometric values: every load first, then the steps, then
+            // every store (the compiler cannot reorder them across the stores)
+            const int grp[11] = {0, 0, 0, 1, 1, 1, 2, 2, 2, 2, 3};
+            const int64_t idx[11] = {3 * i, 3 * i + 1, 3 * i + 2, 3 * i, 3 * i + 1, 3 * i + 2,
+                                     4 * i, 4 * i + 1, 4 * i + 2, 4 * i + 3, i};
+            const float gv[11] = {dm[0], dm[1], dm[2], ds[0] * s[0], ds[1] * s[1], ds[2] * s[2],
+                                  dq.x, dq.y, dq.z, dq.w, g[5] * sig * (1.f - sig)};
+            float pv[11], mv[11], vv[11];
+#pragma unroll
+            for (int e = 0; e < 11; ++e) {
+                pv[e] = ad.p[grp[e]][idx[e]];
+                mv[e] = ad.m[grp[e]][idx[e]];
+                vv[e] = ad.v[grp[e]][idx[e]];
+            }
+#pragma unroll
+            for (int e = 0; e < 11; ++e)
+                pv[e] = adam1(pv[e], mv[e], vv[e], live ? gv[e] : 0.f, ad.lr[grp[e]], ad);
+#pragma unroll
+            for (int e = 0; e < 11; ++e) {
+                ad.p[grp[e]][idx[e]] = pv[e];
+                ad.m[grp[e]][idx[e]] = mv[e];
+                ad.v[grp[e]][idx[e]] = vv[e];
+            }
+        }
     }
     __syncwarp();
 
     // ---- the warp's gradient rows, contiguous (zeros for the rows not live)
     const int nrows = (int)min64(32, n - wbase);
     if (nrows <= 0) return;
-    if constexpr (kVec) {
+    if constexpr (kAdam && kVec) {
+        // the SH rows' Adam step over the warp's rows in 16-byte words, four words
+        // a lane in flight (band 0 is the first three values of a row)
+        float4* P = reinterpret_cast<float4*>(ad.p[4]) + wbase * R4;
+        float4* M = reinterpret_cast<float4*>(ad.m[4]) + wbase * R4;
+        float4* Vv = reinterpret_cast<float4*>(ad.v[4]) + wbase * R4;
+        const float4* my4 = reinterpret_cast<const float4*>(my);
+        const int nf = nrows * R4;
+        for (int f0 = lane; f0 < nf; f0 += 4 * 32) {
+            float4 pw[4], mw[4], vw[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int f = f0 + 32 * u;
+                if (f < nf) {
+                    pw[u] = P[f];
+                    mw[u] = M[f];
+                    vw[u] = Vv[f];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int f = f0 + 32 * u;
+                if (f < nf) {
+                    const int l = f / R4, col = f - l * R4;
+                    const float4 gw = ((lmask >> l) & 1u) ? my4[l * (RS / 4) + col]
+                                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float l0 = ad.lr[5], lb = col == 0 ? ad.lr[4] : ad.lr[5];
+                    pw[u].x = adam1(pw[u].x, mw[u].x, vw[u].x, gw.x, lb, ad);
+                    pw[u].y = adam1(pw[u].y, mw[u].y, vw[u].y, gw.y, lb, ad);
+                    pw[u].z = adam1(pw[u].z, mw[u].z, vw[u].z, gw.z, lb, ad);
+                    pw[u].w = adam1(pw[u].w, mw[u].w, vw[u].w, gw.w, l0, ad);
+                    P[f] = pw[u];
+                    M[f] = mw[u];
+                    Vv[f] = vw[u];
+                }
+            }
+        }
+    } else if constexpr (kAdam) {
+        float* P = ad.p[4] + wbase * RW;
+        float* M = ad.m[4] + wbase * RW;
+        float* Vv = ad.v[4] + wbase * RW;
+        for (int f = lane; f < nrows * RW; f += 32) {
+            const int l = f / RW, j = f - l * RW;
+            const float gv = ((lmask >> l) & 1u) ? my[l * RS + j] : 0.f;
+            adam_at(P, M, Vv, f, gv, j < 3 ? ad.lr[4] : ad.lr[5], ad);
+        }
+    } else if constexpr (kVec) {
         const float4* my4 = reinterpret_cast<const float4*>(my);
         float4* d4 = reinterpret_cast<float4*>(dsh) + wbase * R4;
         for (int f = lane; f < nrows * R4; f += 32) {
@@ -814,13 +923,13 @@ cudaError_t launch_project_bwd_t(const CamParams& cam, int64_t n, int sh_degree,
     auto dq4 = reinterpret_cast<float4*>(dquats);
     auto go = [&](auto kernel) {
         return launch(kernel, grid, block, 0, st, cam, n, means, scales, q4, sh, tiles_touched,
-                      grad2d, touched, dmeans, dscales, dq4, dopacities, dsh);
+                      grad2d, touched, dmeans, dscales, dq4, dopacities, dsh, AdamArgs{});
     };
     switch (sh_degree) {
-        case 0: return go(project_bwd_kernel<1, ShT>);
-        case 1: return go(project_bwd_kernel<4, ShT>);
-        case 2: return go(project_bwd_kernel<9, ShT>);
-        default: return go(project_bwd_kernel<16, ShT>);
+        case 0: return go(project_bwd_kernel<1, ShT, false>);
+        case 1: return go(project_bwd_kernel<4, ShT, false>);
+        case 2: return go(project_bwd_kernel<9, ShT, false>);
+        default: return go(project_bwd_kernel<16, ShT, false>);
     }
 }
 
@@ -843,6 +952,28 @@ cudaError_t launch_project_bwd_sh16(const CamParams& cam, int64_t n, int sh_degr
     (void)opacities;
     return launch_project_bwd_t(cam, n, sh_degree, means, scales, quats, sh, tiles_touched,
                                 grad2d, touched, dmeans, dscales, dquats, dopacities, dsh, st);
+}
+
+cudaError_t launch_project_bwd_adam(const CamParams& cam, int64_t n, int sh_degree,
+                                    const int32_t* tiles_touched, const float* grad2d,
+                                    const uint8_t* touched, const AdamArgs& adam, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    dim3 block(kPbThreads), grid((unsigned)((n + kPbThreads - 1) / kPbThreads));
+    const float* means = adam.p[0];
+    const float* log_scales = adam.p[1];
+    auto q4 = reinterpret_cast<const float4*>(adam.p[2]);
+    const float* sh = adam.p[4];
+    auto go = [&](auto kernel) {
+        return launch(kernel, grid, block, 0, st, cam, n, means, log_scales, q4, sh, tiles_touched,
+                      grad2d, touched, (float*)nullptr, (float*)nullptr, (float4*)nullptr,
+                      (float*)nullptr, (float*)nullptr, adam);
+    };
+    switch (sh_degree) {
+        case 0: return go(project_bwd_kernel<1, float, true>);
+        case 1: return go(project_bwd_kernel<4, float, true>);
+        case 2: return go(project_bwd_kernel<9, float, true>);
+        default: return go(project_bwd_kernel<16, float, true>);
+    }
 }
 
 }  // namespace gs

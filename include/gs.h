@@ -296,6 +296,42 @@ gs_status gs_project_bwd_sh16(const gs_camera* cam, int64_t n, int32_t sh_degree
                               float* dquats, float* dopacities, float* dsh, void* stream);
 
 /*
+ * gs_project_bwd_adam -- gs_project_bwd fused with one Adam step ("proj_sh_bwd_adam"
+ * of the pages' Metal port: the chain rule's gradients are never written, the step
+ * reads and writes the parameters and moments instead).  The parameters are the
+ * RAW ones a training loop optimises -- means [n][3], log-scales [n][3],
+ * quaternions [n][4] (w, x, y, z; not normalised), opacity logits [n], SH
+ * [n][K][3] -- and are updated in place; the forward of the same step must have
+ * been given scales = exp(log-scales) and opacities = sigmoid(logits).  Gradients
+ * of the raw parameters: dL/dlog s = s dL/ds, dL/dlogit = o (1 - o) dL/do, the
+ * rest as gs_project_bwd.  Every Gaussian takes the step (culled or untouched ones
+ * with a zero gradient: their moments decay and their parameters still move).
+ *
+ *   Adam, per element:  m <- b1 m + (1 - b1) g;  v <- b2 v + (1 - b2) g^2;
+ *                       p <- p - lr (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps)
+ *   moments         device m[5], v[5], each of the layout of its parameter, in the
+ *                   order above; updated in place
+ *   adam            learning rates per group (SH band 0 = the first 3 values of a
+ *                   row, bands 1-3 the rest), b1, b2 in [0, 1), eps > 0, step t >= 1
+ */
+typedef struct {
+    float lr_means, lr_scales, lr_quats, lr_opacities, lr_sh0, lr_shN;
+    float beta1, beta2, eps;
+    int32_t step;
+} gs_adam_settings;
+
+typedef struct {
+    float* m[5];
+    float* v[5];
+} gs_adam_moments;
+
+gs_status gs_project_bwd_adam(const gs_camera* cam, int64_t n, int32_t sh_degree, float* means,
+                              float* log_scales, float* quats, float* opacity_logits, float* sh,
+                              const int32_t* tiles_touched, const float* grad2d,
+                              const uint8_t* touched, const gs_adam_moments* moments,
+                              const gs_adam_settings* adam, void* stream);
+
+/*
  * gs_bin_sort_noalloc -- gs_bin_sort for callers that may not allocate device
  * memory.  The papers have no counterpart: it exists for hosts that own all
  * of the GPU's memory (a plugin inside an application with its own
