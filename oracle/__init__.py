@@ -21,7 +21,8 @@ Every function here is argument marshalling around the C entry points; the
 docstrings of ``gs_oracle.c`` cite the passages each one follows.
 
 The training step after the chain rule (``raw_grads``, ``adam_step``) sits here
-too: the GPU's fused chain rule + Adam call is compared with it.
+too: the GPU's fused chain rule + Adam call is compared with it; so does the
+L1 + SSIM loss before the backward (``loss_l1_ssim``).
 
 Parity pins: every function is pinned by a ``-m "not gpu"`` test under
 ``tests/`` (closed forms, library special cases, brute force, finite
@@ -107,6 +108,9 @@ def _declare(lib: C.CDLL) -> None:
     lib.ora_adam_step.argtypes = [_I64, _P, _P, _P, _P, C.c_double, C.c_double, C.c_double,
                                   C.c_double, _I64]
     lib.ora_policy.restype = C.c_double
+    lib.ora_loss_l1_ssim.restype = None
+    lib.ora_loss_l1_ssim.argtypes = [_I32, _I32, _P, _P, C.c_double, C.c_double, C.c_double,
+                                     C.c_double, _P, _P, _P]
 
 
 def _p(a: np.ndarray | None):
@@ -357,6 +361,36 @@ def adam_step(p: np.ndarray, m: np.ndarray, v: np.ndarray, g: np.ndarray, lr: fl
     gg = np.ascontiguousarray(g, np.float64)
     assert gg.size == p.size == m.size == v.size
     _lib("f64").ora_adam_step(p.size, _p(p), _p(m), _p(v), _p(gg), lr, b1, b2, eps, int(t))
+
+
+SSIM_C1 = 0.01 ** 2
+SSIM_C2 = 0.03 ** 2
+SSIM_SIGMA = 1.5
+
+
+@dataclass
+class Loss:
+    loss: float        # (1 - lambda) mean|x - y| + lambda (1 - mean SSIM)
+    l1: float          # mean |x - y|
+    ssim: float        # mean SSIM
+    dL_dimg: np.ndarray  # [H, W, 3] float64
+    ssim_map: np.ndarray | None  # [H, W, 3] float64 per-pixel SSIM (when asked for)
+
+
+def loss_l1_ssim(img: np.ndarray, target: np.ndarray, lam: float = 0.2, c1: float = SSIM_C1,
+                 c2: float = SSIM_C2, sigma: float = SSIM_SIGMA, want_map: bool = False) -> Loss:
+    """The L1 + SSIM training loss of two [H, W, 3] float32 images and its gradient
+    w.r.t. the first (11 x 11 Gaussian window, zero outside the image)."""
+    x = _f32(img)
+    y = _f32(target)
+    assert x.shape == y.shape and x.ndim == 3 and x.shape[2] == 3
+    H, W = x.shape[:2]
+    out = np.zeros(3, np.float64)
+    g = np.empty((H, W, 3), np.float64)
+    smap = np.empty((H, W, 3), np.float64) if want_map else None
+    _lib("f64").ora_loss_l1_ssim(W, H, _p(x), _p(y), lam, c1, c2, sigma, _p(out), _p(g),
+                                 _p(smap))
+    return Loss(float(out[0]), float(out[1]), float(out[2]), g, smap)
 
 
 def sh_basis(dirs: np.ndarray) -> tuple[np.ndarray, np.ndarray]:

@@ -23,7 +23,11 @@
  *   - the nine screen-space derivatives per splat (Kopanas, Step 1 (a)) and
  *     the chain rule back to means, scales, quaternions, opacities and SH
  *     coefficients (calculus; pinned by finite differences in the tests);
- *   - the per-frame chunking cost model (Ryu & Yoo, Sec. 4.4, Eq. 6).
+ *   - the per-frame chunking cost model (Ryu & Yoo, Sec. 4.4, Eq. 6);
+ *   - the steps either side of the path in a training step (the pages' Metal
+ *     port, "perf: rasterizer and pipeline optimizations", Breakdown and
+ *     Queue): the raw-parameter gradients and one Adam step, and the
+ *     L1 + SSIM photometric loss with its gradient.
  *
  * Precision.  The pages fix fp32 for the rasterizer and require the quadratic
  * to be evaluated with explicit round-to-nearest operations so that every
@@ -1210,4 +1214,116 @@ void ora_adam_step(int64_t count, double* p, double* m, double* v, const double*
         v[i] = b2 * v[i] + (1.0 - b2) * g[i] * g[i];
         p[i] -= lr * (m[i] / c1) / (sqrt(v[i] / c2) + eps);
     }
+}
+
+/*
+ * The photometric loss of a training step ("loss_fwd_bwd" of the pages' Metal
+ * port, whose intermediates are five windowed moments for each of the three
+ * colour channels), read as the usual 3DGS objective
+ *
+ *   L = (1 - lambda) mean |x - y| + lambda (1 - mean SSIM(x, y))
+ *
+ * over the H x W x 3 values of the rendered image x and the target y, with the
+ * structural similarity of Wang et al. (2004) per pixel and channel:
+ *
+ *   mu_x = w * x,  mu_y = w * y,  e_xx = w * x^2,  e_yy = w * y^2,  e_xy = w * xy
+ *   var_x = e_xx - mu_x^2,  var_y = e_yy - mu_y^2,  cov = e_xy - mu_x mu_y
+ *   SSIM = (2 mu_x mu_y + c1)(2 cov + c2) / ((mu_x^2 + mu_y^2 + c1)(var_x + var_y + c2))
+ *
+ * "w *" is the weighted sum over the 11 x 11 window centred on the pixel with
+ * weights g(a) g(b), g(k) = exp(-k^2 / (2 sigma^2)) normalised over k = -5..5,
+ * and pixels outside the image count as zero.  Written as that 2D sum, not as
+ * two 1D passes.
+ *
+ * The gradient dL/dx is the chain rule through those definitions.  Per pixel q
+ * and channel the SSIM depends on x only through mu_x, e_xx and e_xy; with
+ * A1 = 2 mu_x mu_y + c1, A2 = 2 cov + c2, B1 = mu_x^2 + mu_y^2 + c1,
+ * B2 = var_x + var_y + c2 and D = B1 B2:
+ *
+ *   dS/dmu_x = (2 mu_y (A2 - A1) - 2 mu_x S (B2 - B1)) / D
+ *   dS/de_xx = -S / B2
+ *   dS/de_xy = 2 A1 / D
+ *
+ * and a pixel p enters mu_x(q), e_xx(q), e_xy(q) with weights w(q - p),
+ * w(q - p) 2 x(p) and w(q - p) y(p), for every q of the image within the
+ * window.  The L1 term's derivative is sign(x - y) (0 where x = y).
+ *
+ * out[0] = L, out[1] = mean |x - y|, out[2] = mean SSIM; dL_dx [H][W][3];
+ * ssim_map [H][W][3] (optional, NULL = not written) the per-pixel SSIM.
+ */
+#define SSIM_R 5 /* window radius: 11 taps */
+
+static void ssim_window(double sigma, double* g) {
+    double s = 0.0;
+    for (int k = -SSIM_R; k <= SSIM_R; ++k) {
+        g[k + SSIM_R] = exp(-(double)(k * k) / (2.0 * sigma * sigma));
+        s += g[k + SSIM_R];
+    }
+    for (int k = 0; k <= 2 * SSIM_R; ++k) g[k] /= s;
+}
+
+void ora_loss_l1_ssim(int W, int H, const float* x, const float* y, double lambda, double c1,
+                      double c2, double sigma, double* out, double* dL_dx, double* ssim_map) {
+    double g[2 * SSIM_R + 1];
+    ssim_window(sigma, g);
+    int64_t np = (int64_t)W * H;
+    double inv = 1.0 / (double)(3 * np);
+    /* per pixel and channel: dS/dmu_x, dS/de_xx, dS/de_xy */
+    double* dmu = (double*)malloc(sizeof(double) * 3 * np);
+    double* dxx = (double*)malloc(sizeof(double) * 3 * np);
+    double* dxy = (double*)malloc(sizeof(double) * 3 * np);
+    double l1 = 0.0, ssim = 0.0;
+    for (int r = 0; r < H; ++r)
+        for (int c = 0; c < W; ++c)
+            for (int ch = 0; ch < 3; ++ch) {
+                double mx = 0, my = 0, exx = 0, eyy = 0, exy = 0;
+                for (int a = -SSIM_R; a <= SSIM_R; ++a)
+                    for (int b = -SSIM_R; b <= SSIM_R; ++b) {
+                        int rr = r + a, cc = c + b;
+                        if (rr < 0 || rr >= H || cc < 0 || cc >= W) continue;
+                        double w = g[a + SSIM_R] * g[b + SSIM_R];
+                        double xv = x[((int64_t)rr * W + cc) * 3 + ch];
+                        double yv = y[((int64_t)rr * W + cc) * 3 + ch];
+                        mx += w * xv;
+                        my += w * yv;
+                        exx += w * xv * xv;
+                        eyy += w * yv * yv;
+                        exy += w * xv * yv;
+                    }
+                double vx = exx - mx * mx, vy = eyy - my * my, cov = exy - mx * my;
+                double A1 = 2.0 * mx * my + c1, A2 = 2.0 * cov + c2;
+                double B1 = mx * mx + my * my + c1, B2 = vx + vy + c2;
+                double D = B1 * B2;
+                double s = A1 * A2 / D;
+                int64_t i = ((int64_t)r * W + c) * 3 + ch;
+                if (ssim_map) ssim_map[i] = s;
+                dmu[i] = (2.0 * my * (A2 - A1) - 2.0 * mx * s * (B2 - B1)) / D;
+                dxx[i] = -s / B2;
+                dxy[i] = 2.0 * A1 / D;
+                ssim += s;
+                l1 += fabs((double)x[i] - (double)y[i]);
+            }
+    out[1] = l1 * inv;
+    out[2] = ssim * inv;
+    out[0] = (1.0 - lambda) * out[1] + lambda * (1.0 - out[2]);
+    for (int r = 0; r < H; ++r)
+        for (int c = 0; c < W; ++c)
+            for (int ch = 0; ch < 3; ++ch) {
+                int64_t i = ((int64_t)r * W + c) * 3 + ch;
+                double xv = x[i], yv = y[i];
+                double ds = 0.0;
+                for (int a = -SSIM_R; a <= SSIM_R; ++a)
+                    for (int b = -SSIM_R; b <= SSIM_R; ++b) {
+                        int rr = r + a, cc = c + b;
+                        if (rr < 0 || rr >= H || cc < 0 || cc >= W) continue;
+                        double w = g[a + SSIM_R] * g[b + SSIM_R];
+                        int64_t q = ((int64_t)rr * W + cc) * 3 + ch;
+                        ds += w * (dmu[q] + 2.0 * xv * dxx[q] + yv * dxy[q]);
+                    }
+                double sg = xv > yv ? 1.0 : (xv < yv ? -1.0 : 0.0);
+                dL_dx[i] = (1.0 - lambda) * inv * sg - lambda * inv * ds;
+            }
+    free(dmu);
+    free(dxx);
+    free(dxy);
 }
