@@ -15,6 +15,10 @@ time is the max over ranks and `value` counts the pairs of all ranks.
 
 --impl reference times the CPU oracle (oracle/, plain C, one core) on a bounded
 sample of the same workload and prints the same line with "impl": "reference".
+
+--train-step times a whole training step instead: the same calls with the L1 + SSIM
+loss against a synthetic target between forward and backward (gs_loss_l1_ssim), and
+the chain rule fused with an Adam step on the raw parameters (gs_project_bwd_adam).
 """
 
 from __future__ import annotations
@@ -53,6 +57,10 @@ FP32_LANES_PER_SM = 128
 SFU_FWD_PER_E = 1
 SFU_BWD_PER_E = 2
 SFU_LANES_PER_SM = 16
+# The L1 + SSIM loss per pixel: per channel, the window's 11 taps along rows and then
+# columns for five moments (x, y, x^2, y^2, xy) and again for the three derivative
+# maps of SSIM, 16 x 11 FMA = 352 flops; three channels
+LOSS_FLOPS_PER_PIXEL = 3 * 16 * 11 * 2
 
 
 def parse():
@@ -66,6 +74,10 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--sh-bf16", action="store_true",
                    help="SH coefficients stored as bfloat16 (gs_project_sh16, gs_project_bwd_sh16)")
+    p.add_argument("--train-step", action="store_true",
+                   help="a whole training step: the hot path with the L1 + SSIM loss against a "
+                        "target image between forward and backward, and the chain rule fused "
+                        "with an Adam step on the raw parameters (gs_project_bwd_adam)")
     return p.parse_args()
 
 
@@ -305,7 +317,24 @@ def roofline(call, ms, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz):
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": profiled_traffic(call),
                 "peak_source": f"{n_sm} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 x {sm_mhz:.0f} MHz (sampled)",
                 "work": f"{per} flops x {E} contributing pairs"}
+    if call == "gs_loss_l1_ssim":
+        flops = LOSS_FLOPS_PER_PIXEL * H * W
+        peak = 2.0 * FP32_LANES_PER_SM * n_sm * sm_mhz * 1e6 / 1e12
+        achieved = flops / (ms * 1e-3) / 1e12
+        return {"kernel": call, "bound": "alu", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": profiled_traffic(call),
+                "peak_source": f"{n_sm} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 x {sm_mhz:.0f} MHz (sampled)",
+                "work": f"{LOSS_FLOPS_PER_PIXEL} flops x {H * W} pixels"}
     N, G = sc.n, 44 + 12 * (sc.sh_degree + 1) ** 2  # G: parameter bytes per Gaussian
+    if call == "gs_project_bwd_adam":
+        # grad2d of the visible, the two flags, parameters and both moments read and
+        # written, the activated scales and opacities written
+        byts = 36 * M + 5 * N + 6 * G * N + 16 * N
+        achieved = byts / (ms * 1e-3) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        return {"kernel": call, "bound": "hbm", "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "traffic": profiled_traffic(call),
+                "peak_source": f"{peaks['source']} copy bandwidth"}
     if call == "gs_project":
         # geometry of every Gaussian, SH of the visible, record of the visible, radii
         byts = 44 * N + (G - 44) * M + 64 * M + 8 * N
@@ -327,6 +356,9 @@ PROFILED = {
     "gs_rasterize_bwd": ("raster_bwd_kernel", ["gs_raster.cu", "gs_device.cuh", "gs_internal.h"]),
     "gs_project": ("project_kernel", ["gs_project.cu", "gs_device.cuh", "gs_internal.h"]),
     "gs_project_bwd": ("project_bwd_kernel", ["gs_project.cu", "gs_device.cuh", "gs_internal.h"]),
+    "gs_loss_l1_ssim": ("loss_ssim_kernel", ["gs_loss.cu", "gs_device.cuh", "gs_internal.h"]),
+    "gs_project_bwd_adam": ("project_bwd_adam", ["gs_project.cu", "gs_device.cuh",
+                                                 "gs_internal.h", "gs_project_variants.h"]),
 }
 
 
@@ -358,9 +390,11 @@ def profiled_traffic(call, workload="scene-1.5M-1297x840"):
     return int(fields["traffic_bytes_per_launch"]) if "traffic_bytes_per_launch" in fields else None
 
 
-def step_roofline(ms, sc, M, I, E, H, W, peaks, n_sm, sm_mhz):
+def step_roofline(ms, sc, M, I, E, H, W, peaks, n_sm, sm_mhz, train=False):
     """Whole-step roofline: per phase the largest of bytes / HBM, fp32 flops / fp32 peak and
-    SFU ops / SFU peak, summed over the phases; frac = that time / the measured step."""
+    SFU ops / SFU peak, summed over the phases; frac = that time / the measured step.
+    train: the training step (loss phase; Adam on parameters and moments in place of the
+    gradient rows)."""
     N, P = sc.n, H * W
     G = 44 + 12 * (sc.sh_degree + 1) ** 2  # parameter bytes per Gaussian
     hbm = float(peaks["hbm_gbs"]) * 1e9
@@ -378,6 +412,10 @@ def step_roofline(ms, sc, M, I, E, H, W, peaks, n_sm, sm_mhz):
         "backward": (48 * I + 36 * P + 36 * M + G * M + G * N, FLOPS_BWD_PER_E * E,
                      SFU_BWD_PER_E * E),
     }
+    if train:
+        phases["loss"] = (36 * P, LOSS_FLOPS_PER_PIXEL * P, 0)
+        phases["backward"] = (48 * I + 36 * P + 36 * M + 5 * N + 6 * G * N + 16 * N,
+                              FLOPS_BWD_PER_E * E, SFU_BWD_PER_E * E)
     out, total = {}, 0.0
     for k, (b, f, x) in phases.items():
         t = max(b / hbm, f / fp32, x / sfu) * 1e3
@@ -499,6 +537,164 @@ def cpu_baseline(sc, cam, w, stride: int = 1):
                       f"{what} ({pairs} pairs), {dt:.1f} s"}
 
 
+# Adam settings of the training step: the learning rates 3DGS trains with (means, scales,
+# rotations, opacities, SH band 0, SH bands 1-3), beta1 0.9, beta2 0.999, eps 1e-15
+TRAIN_LR = dict(lr_means=1.6e-4, lr_scales=5e-3, lr_quats=1e-3, lr_opacities=5e-2,
+                lr_sh0=2.5e-3, lr_shN=1.25e-4)
+
+
+def run_train(args):
+    """A whole training step per timed step: gs_project on the activated parameters,
+    gs_bin_sort, gs_rasterize_fwd, gs_loss_l1_ssim against a synthetic target image,
+    gs_rasterize_bwd of the loss's gradient and gs_project_bwd_adam, which steps the raw
+    parameters and both moments in place and writes the activated scales and opacities
+    the next step's projection reads."""
+    import torch
+    import torch.distributed as dist
+
+    import differentiable_gaussian_splatting_gb300 as gs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    sc, cam = ss.make_config(args.config)
+    H, W = cam.height, cam.width
+    _, target = ss.image_pair(np.random.default_rng(200 + args.config), H, W)
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+
+    log_s = np.log(sc.scales.astype(np.float64))
+    o = sc.opacities.astype(np.float64).reshape(-1)
+    raw = [to_dev(sc.means), to_dev(log_s), to_dev(sc.quats), to_dev(np.log(o / (1 - o))),
+           to_dev(sc.sh)]
+    act_s, act_o = to_dev(sc.scales), to_dev(o)
+    mom_m = [torch.zeros_like(t) for t in raw]
+    mom_v = [torch.zeros_like(t) for t in raw]
+    tgt = to_dev(target)
+    dimg = torch.empty_like(tgt)
+    loss_out = torch.zeros(4, dtype=torch.float32, device=dev)
+    loss_ws = torch.empty(gs.gs_loss_workspace_bytes(W, H), dtype=torch.uint8, device=dev)
+    adam = gs.AdamSettings(**TRAIN_LR, beta1=0.9, beta2=0.999, eps=1e-15, step=1)
+
+    r = gs.Rasterizer(cam, sc.sh_degree, sc.n, device=dev)
+    r.forward(raw[0], act_s, raw[2], act_o, raw[4])  # sizes the pair list (one host sync)
+    n_pairs = r.n_pairs
+    r._alloc_pairs(int(n_pairs * 1.25) + 1024)
+    stream = torch.cuda.current_stream()
+    t_step = [0]
+
+    def step(ev=None):
+        n = r.n
+        t_step[0] += 1
+        adam.step = t_step[0]
+        marks = iter(ev) if ev else None
+
+        def mark():
+            if marks:
+                next(marks).record(stream)
+
+        mark()
+        gs.gs_project(r.cam, n, r.sh_degree, raw[0], act_s, raw[2], act_o, raw[4], r.splats,
+                      r.depths, r.radii, r.tiles_touched)
+        mark()
+        gs.gs_bin_sort(r.cam, n, r.splats, r.depths, r.tiles_touched, r.bin_ws, r.sorted_ids,
+                       r.capacity, r.tile_ranges, r.lpt_order, r.counts, sync_pairs=False)
+        mark()
+        gs.gs_rasterize_fwd(r.cam, n, r.splats, r.sorted_ids, r.tile_ranges, r.lpt_order,
+                            r.raster_ws, r.image, r.t_final, r.n_contrib, r.last_idx, r.settings)
+        mark()
+        gs.gs_loss_l1_ssim(W, H, r.image, tgt, dimg, loss_out, loss_ws)
+        mark()
+        gs.gs_rasterize_bwd(r.cam, n, r.splats, r.sorted_ids, r.tile_ranges, r.lpt_order,
+                            r.raster_ws, r.t_final, r.last_idx, dimg, None, r.grad2d, r.touched,
+                            r.settings)
+        mark()
+        gs.gs_project_bwd_adam(r.cam, n, r.sh_degree, *raw, r.tiles_touched, r.grad2d,
+                               r.touched, mom_m, mom_v, adam, scales_out=act_s,
+                               opacities_out=act_o)
+        mark()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    loss0 = float(loss_out[0].item())
+    pairs0 = int(r.counts[1].item())
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(stop)
+    loss1 = float(loss_out[0].item())
+    counts = r.counts.cpu().numpy()
+    if counts[1] > r.capacity:
+        raise RuntimeError(f"pair list outgrew its capacity during training: {counts[1]}")
+    pairs1 = int(counts[1])
+    calls = ["gs_project", "gs_bin_sort", "gs_rasterize_fwd", "gs_loss_l1_ssim",
+             "gs_rasterize_bwd", "gs_project_bwd_adam"]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    per_call = {c: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
+                for j, c in enumerate(calls)}
+    total_ms = max_over_ranks(total_ms, dev)
+    ms_per_step = total_ms / args.steps
+    # pairs of the timed steps: the count moves a little as the parameters train
+    pairs = 0.5 * (pairs0 + pairs1)
+    value = world * pairs / (ms_per_step * 1e-3)
+    peaks = measured_peaks()
+    clocks = clk.summary()
+    props = torch.cuda.get_device_properties(dev)
+    sm_mhz = clocks["sm_mhz"] or peaks.get("clocks_under_load", {}).get("sm_mhz_median") or 1462.0
+    dom = max(per_call, key=per_call.get)
+    M = int((r.tiles_touched > 0).sum().item())
+    E = int(r.n_contrib.sum().item())
+    roof = roofline(dom, per_call[dom], sc, M, pairs1, E, H, W, peaks,
+                    props.multi_processor_count, sm_mhz)
+    step_roof = step_roofline(ms_per_step, sc, M, pairs1, E, H, W, peaks,
+                              props.multi_processor_count, sm_mhz, train=True)
+    launches = kernel_launches(sc.n, r.capacity, W, H) + 2  # the loss: tiles + final sum
+    if rank == 0:
+        print(json.dumps({
+            "metric": "training step (hot path + L1/SSIM loss + fused chain rule and Adam), "
+                      "tile-Gaussian pairs/s",
+            "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": ss.CONFIG_NAMES[args.config], "gaussians": sc.n,
+                       "image": f"{W}x{H}", "sh_degree": sc.sh_degree,
+                       "tile_pairs": [pairs0, pairs1], "contributing_pairs": E,
+                       "loss": [loss0, loss1], "adam": TRAIN_LR,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (354 MB parameters + 708 MB moments)"},
+            "per_call_ms": per_call,
+            "roofline": roof,
+            "step_roofline": step_roof,
+            "cpu_baseline": None,
+            "e2e": None,
+            "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
+                       "reasons": clocks["reasons"]},
+            "gpu_launches": launches * args.steps,
+        }))
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -531,5 +727,7 @@ if __name__ == "__main__":
     a = parse()
     if a.impl == "reference":
         run_reference(a)
+    elif a.train_step:
+        run_train(a)
     else:
         run_gpu(a)

@@ -27,6 +27,7 @@ from . import build as _build
 __all__ = [
     "gs_project", "gs_bin_sort", "gs_rasterize_fwd", "gs_rasterize_bwd", "gs_project_bwd",
     "gs_project_sh16", "gs_project_bwd_sh16", "gs_project_bwd_adam", "AdamSettings",
+    "gs_loss_l1_ssim", "gs_loss_workspace_bytes", "LossSettings",
     "gs_raster_stats", "gs_default_settings", "Camera", "Settings", "Rasterizer", "library",
     "GSError", "TILE", "GRAD2D", "SPLAT_FLOATS",
 ]
@@ -89,6 +90,16 @@ class AdamMoments(C.Structure):
     _fields_ = [("m", C.c_void_p * 5), ("v", C.c_void_p * 5)]
 
 
+class LossSettings(C.Structure):
+    """gs_loss_settings: weight of the SSIM term, the SSIM constants, the window's sigma."""
+    _fields_ = [("lambda_", C.c_float), ("c1", C.c_float), ("c2", C.c_float),
+                ("sigma", C.c_float)]
+
+    @classmethod
+    def default(cls) -> "LossSettings":
+        return cls(0.2, 0.01 ** 2, 0.03 ** 2, 1.5)
+
+
 _lib = None
 _lib_lock = threading.Lock()
 _P = C.c_void_p
@@ -143,7 +154,13 @@ def _declare(lib: C.CDLL) -> None:
     lib.gs_project_bwd_sh16.argtypes = [C.POINTER(Camera), _I64, C.c_int32] + [_P] * 13 + [_P]
     lib.gs_project_bwd_adam.restype = st
     lib.gs_project_bwd_adam.argtypes = ([C.POINTER(Camera), _I64, C.c_int32] + [_P] * 8 +
-                                        [C.POINTER(AdamMoments), C.POINTER(AdamSettings), _P])
+                                        [C.POINTER(AdamMoments), C.POINTER(AdamSettings), _P,
+                                         _P, _P])
+    lib.gs_loss_workspace_bytes.restype = C.c_size_t
+    lib.gs_loss_workspace_bytes.argtypes = [C.c_int32, C.c_int32]
+    lib.gs_loss_l1_ssim.restype = st
+    lib.gs_loss_l1_ssim.argtypes = [C.c_int32, C.c_int32, _P, _P, C.POINTER(LossSettings), _P, _P,
+                                    _P, C.c_size_t, _P]
     lib.gs_bin_sort_noalloc.restype = st
     lib.gs_bin_sort_noalloc.argtypes = [C.POINTER(Camera), _I64, _P, _P, _P, _P, _I64, _P, _P, _P,
                                         _P, _P]
@@ -374,9 +391,11 @@ def gs_project_bwd_sh16(cam, n, sh_degree, means, scales, quats, opacities, sh, 
 
 def gs_project_bwd_adam(cam, n, sh_degree, means, log_scales, quats, opacity_logits, sh,
                         tiles_touched, grad2d, touched, m, v, settings: AdamSettings,
-                        stream=None):
+                        scales_out=None, opacities_out=None, stream=None):
     """gs_project_bwd fused with one Adam step on the raw parameters, in place (see gs.h).
-    m and v: five tensors each, shaped like (means, log_scales, quats, opacity_logits, sh)."""
+    m and v: five tensors each, shaped like (means, log_scales, quats, opacity_logits, sh).
+    scales_out / opacities_out (optional) receive exp(log_scales) and sigmoid(logits)
+    after the step."""
     import torch
 
     K = (int(sh_degree) + 1) ** 2
@@ -395,8 +414,29 @@ def gs_project_bwd_adam(cam, n, sh_degree, means, log_scales, quats, opacity_log
         *[_ptr(t, names[k], f, sizes[k]) for k, t in enumerate(params)],
         _ptr(tiles_touched, "tiles_touched", i, n), _ptr(grad2d, "grad2d", f, GRAD2D * n),
         _ptr(touched, "touched", torch.uint8, n, optional=True), C.byref(mom),
-        C.byref(settings), _stream(stream))
+        C.byref(settings), _ptr(scales_out, "scales_out", f, 3 * n, optional=True),
+        _ptr(opacities_out, "opacities_out", f, n, optional=True), _stream(stream))
     _check("gs_project_bwd_adam", st)
+
+
+def gs_loss_workspace_bytes(width, height) -> int:
+    return int(library().gs_loss_workspace_bytes(int(width), int(height)))
+
+
+def gs_loss_l1_ssim(width, height, image, target, dL_dimage, loss_out, workspace,
+                    settings: LossSettings | None = None, stream=None):
+    """The L1 + SSIM loss of image against target and its gradient (see gs.h).
+    loss_out: device float32[3] = (L, mean |x - y|, mean SSIM)."""
+    import torch
+
+    P = 3 * int(width) * int(height)
+    f = _f32()
+    ls = settings if settings is not None else LossSettings.default()
+    st = library().gs_loss_l1_ssim(
+        int(width), int(height), _ptr(image, "image", f, P), _ptr(target, "target", f, P),
+        C.byref(ls), _ptr(dL_dimage, "dL_dimage", f, P), _ptr(loss_out, "loss_out", f, 3),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check("gs_loss_l1_ssim", st)
 
 
 def gs_raster_stats(workspace, stream=None) -> dict:

@@ -353,7 +353,8 @@ gs_status gs_project_bwd_adam(const gs_camera* cam, int64_t n, int32_t sh_degree
                               float* log_scales, float* quats, float* opacity_logits, float* sh,
                               const int32_t* tiles_touched, const float* grad2d,
                               const uint8_t* touched, const gs_adam_moments* moments,
-                              const gs_adam_settings* adam, void* stream) {
+                              const gs_adam_settings* adam, float* scales_out,
+                              float* opacities_out, void* stream) {
     if (!camera_ok(cam) || n < 0 || n > kMaxIds || sh_degree < 0 || sh_degree > 3 || !moments ||
         !adam)
         return GS_ERR_INVALID_ARG;
@@ -383,6 +384,10 @@ gs_status gs_project_bwd_adam(const gs_camera* cam, int64_t n, int32_t sh_degree
     a.eps = adam->eps;
     a.c1 = (float)(1.0 / (1.0 - std::pow((double)adam->beta1, (double)adam->step)));
     a.c2 = (float)(1.0 / (1.0 - std::pow((double)adam->beta2, (double)adam->step)));
+    if ((scales_out && !aligned16(scales_out)) || (opacities_out && !aligned16(opacities_out)))
+        return GS_ERR_INVALID_ARG;
+    a.act_scales = scales_out;
+    a.act_opacities = opacities_out;
     return cuda_status(launch_project_bwd_adam(cam_params(cam), n, sh_degree, tiles_touched,
                                                grad2d, touched, a, (cudaStream_t)stream));
 }
@@ -402,6 +407,35 @@ gs_status gs_project_bwd(const gs_camera* cam, int64_t n, int32_t sh_degree, con
     return cuda_status(launch_project_bwd(cam_params(cam), n, sh_degree, means, scales, quats,
                                           opacities, sh, tiles_touched, grad2d, touched, dmeans,
                                           dscales, dquats, dopacities, dsh, (cudaStream_t)stream));
+}
+
+size_t gs_loss_workspace_bytes(int32_t width, int32_t height) {
+    if (width < 1 || height < 1) return 0;
+    return (size_t)loss_tiles(width, height) * 2 * sizeof(float);
+}
+
+gs_status gs_loss_l1_ssim(int32_t width, int32_t height, const float* image, const float* target,
+                          const gs_loss_settings* settings, float* dL_dimage, float* loss_out,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+    if (width < 1 || height < 1 || width > (1 << 20) || height > (1 << 20) || !settings)
+        return GS_ERR_INVALID_ARG;
+    const gs_loss_settings& ls = *settings;
+    if (!(ls.lambda >= 0.f && ls.lambda <= 1.f) || !(ls.c1 > 0.f) || !finite_f(ls.c1) ||
+        !(ls.c2 > 0.f) || !finite_f(ls.c2) || !(ls.sigma > 0.f) || !finite_f(ls.sigma))
+        return GS_ERR_INVALID_ARG;
+    const void* ptrs[] = {image, target, dL_dimage, loss_out, workspace};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return GS_ERR_INVALID_ARG;
+    const size_t bytes = (size_t)width * height * 3 * sizeof(float);
+    const char* d = (const char*)dL_dimage;
+    for (const void* p : {(const void*)image, (const void*)target}) {
+        const char* q = (const char*)p;
+        if (d < q + bytes && q < d + bytes) return GS_ERR_INVALID_ARG;
+    }
+    if (workspace_bytes < gs_loss_workspace_bytes(width, height)) return GS_ERR_WORKSPACE;
+    return cuda_status(launch_loss_l1_ssim(width, height, image, target, ls.lambda, ls.c1, ls.c2,
+                                           ls.sigma, dL_dimage, loss_out, workspace,
+                                           (cudaStream_t)stream));
 }
 
 gs_status gs_raster_stats(const void* workspace, size_t workspace_bytes, int64_t* out,

@@ -69,6 +69,13 @@ cudaError_t run_bin_sort_radix(const CamParams& cam, int64_t n, const float* spl
                                int32_t* tile_ranges, int32_t* lpt_order, int64_t* counts_out,
                                cudaStream_t st);
 
+// L1 + SSIM loss and its gradient (gs_loss.cu): per-tile partial sums in ws
+// (loss_tiles(W, H) float2), loss_out = (L, mean |x - y|, mean SSIM)
+int64_t loss_tiles(int W, int H);
+cudaError_t launch_loss_l1_ssim(int W, int H, const float* img, const float* tgt, double lambda,
+                                float c1, float c2, double sigma, float* dimg, float* loss_out,
+                                void* ws, cudaStream_t st);
+
 // LPT order of the tiles from their ranges (gs_binsort.cu); runs is scratch of
 // lpt_runs_bytes(nt) bytes
 size_t lpt_runs_bytes(int64_t nt);

@@ -842,6 +842,11 @@ __global__ void __launch_bounds__(kPbThreads) project_bwd_kernel(
                 ad.m[grp[e]][idx[e]] = mv[e];
                 ad.v[grp[e]][idx[e]] = vv[e];
             }
+            if (ad.act_scales) {
+#pragma unroll
+                for (int r = 0; r < 3; ++r) ad.act_scales[3 * i + r] = expf(pv[3 + r]);
+            }
+            if (ad.act_opacities) ad.act_opacities[i] = 1.f / (1.f + expf(-pv[10]));
         }
     }
     __syncwarp();

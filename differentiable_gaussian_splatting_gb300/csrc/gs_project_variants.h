@@ -25,13 +25,16 @@ cudaError_t launch_project_bwd_sh16(const CamParams& cam, int64_t n, int sh_degr
 // One Adam step on the raw parameters, fused into the chain rule: p[] are
 // updated in place, m[] / v[] are the moments (same layouts as the parameters:
 // means, log-scales, quaternions, opacity logits, SH).  c1 = 1 / (1 - beta1^t),
-// c2 = 1 / (1 - beta2^t).
+// c2 = 1 / (1 - beta2^t).  act_scales / act_opacities, when set, receive the
+// activated values of the updated parameters (the next forward's inputs).
 struct AdamArgs {
     float* p[5];
     float* m[5];
     float* v[5];
     float lr[6];  // means, scales, quaternions, opacities, SH band 0, SH bands 1-3
     float b1, b2, eps, c1, c2;
+    float* act_scales;     // optional: exp(log-scales) after the step
+    float* act_opacities;  // optional: sigmoid(logits) after the step
 };
 
 cudaError_t launch_project_bwd_adam(const CamParams& cam, int64_t n, int sh_degree,

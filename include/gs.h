@@ -14,6 +14,11 @@
  *   gs_project_bwd    chain rule back to means, scales, quaternions,
  *                     opacities and SH coefficients
  *
+ * Around them: gs_loss_l1_ssim (the L1 + SSIM loss between the forward and
+ * the backward), gs_project_bwd_adam (the chain rule fused with one Adam
+ * step), bfloat16-SH variants of the projection and its chain rule, and
+ * gs_bin_sort_noalloc.
+ *
  * Sources (page title, section / equation):
  *   [RY]  Ryu & Yoo, "Mitigating SM-Level Load Imbalance in 3D Gaussian
  *         Splatting on GPUs": Sec. 2.1 Eq. 1 (projection), Eq. 2 (alpha),
@@ -313,6 +318,9 @@ gs_status gs_project_bwd_sh16(const gs_camera* cam, int64_t n, int32_t sh_degree
  *                   order above; updated in place
  *   adam            learning rates per group (SH band 0 = the first 3 values of a
  *                   row, bands 1-3 the rest), b1, b2 in [0, 1), eps > 0, step t >= 1
+ *   scales_out      optional [n][3] (NULL = not written): exp(log-scales) after the
+ *                   step, the next forward's scales
+ *   opacities_out   optional [n]: sigmoid(logits) after the step
  */
 typedef struct {
     float lr_means, lr_scales, lr_quats, lr_opacities, lr_sh0, lr_shN;
@@ -329,7 +337,45 @@ gs_status gs_project_bwd_adam(const gs_camera* cam, int64_t n, int32_t sh_degree
                               float* log_scales, float* quats, float* opacity_logits, float* sh,
                               const int32_t* tiles_touched, const float* grad2d,
                               const uint8_t* touched, const gs_adam_moments* moments,
-                              const gs_adam_settings* adam, void* stream);
+                              const gs_adam_settings* adam, float* scales_out,
+                              float* opacities_out, void* stream);
+
+/*
+ * gs_loss_l1_ssim -- the photometric loss of a training step and its gradient, the
+ * step between gs_rasterize_fwd and gs_rasterize_bwd ("loss_fwd_bwd" of the pages'
+ * Metal port, "perf: rasterizer and pipeline optimizations", Breakdown and Queue,
+ * which keeps five windowed moments per colour channel; the formula is the usual
+ * 3DGS objective, which the pages do not print):
+ *
+ *   L = (1 - lambda) mean |x - y| + lambda (1 - mean SSIM(x, y))
+ *
+ * over the width * height * 3 values of the rendered image x and the target y.
+ * SSIM per pixel and channel is that of Wang et al. (2004):
+ *   (2 mu_x mu_y + c1)(2 cov + c2) / ((mu_x^2 + mu_y^2 + c1)(var_x + var_y + c2)),
+ * the means, variances and covariance taken over the 11 x 11 window centred on
+ * the pixel with weights g(a) g(b), g(k) ~ exp(-k^2 / (2 sigma^2)) normalised
+ * over k = -5..5, and pixels outside the image counting as zero.  The L1 term's
+ * derivative is sign(x - y), 0 where x = y.
+ *
+ *   image, target   [height][width][3] (the layout gs_rasterize_fwd writes)
+ *   settings        lambda in [0, 1] (3DGS uses 0.2); c1, c2 > 0 (0.01^2 and
+ *                   0.03^2 for values in [0, 1]); sigma > 0 (1.5)
+ *   dL_dimage       out [height][width][3], the gradient w.r.t. image (the input
+ *                   gs_rasterize_bwd takes); must not overlap image or target
+ *   loss_out        out, device float[3] = (L, mean |x - y|, mean SSIM)
+ *   workspace       device scratch of gs_loss_workspace_bytes(width, height) bytes
+ *
+ * Two launches; deterministic (fixed summation order).  width, height >= 1.
+ */
+typedef struct {
+    float lambda, c1, c2, sigma;
+} gs_loss_settings;
+
+size_t gs_loss_workspace_bytes(int32_t width, int32_t height);
+
+gs_status gs_loss_l1_ssim(int32_t width, int32_t height, const float* image, const float* target,
+                          const gs_loss_settings* settings, float* dL_dimage, float* loss_out,
+                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * gs_bin_sort_noalloc -- gs_bin_sort for callers that may not allocate device

@@ -110,7 +110,7 @@ def _declare(lib: C.CDLL) -> None:
     lib.ora_policy.restype = C.c_double
     lib.ora_loss_l1_ssim.restype = None
     lib.ora_loss_l1_ssim.argtypes = [_I32, _I32, _P, _P, C.c_double, C.c_double, C.c_double,
-                                     C.c_double, _P, _P, _P]
+                                     C.c_double, _P, _P, _P, _P]
 
 
 def _p(a: np.ndarray | None):
@@ -375,6 +375,7 @@ class Loss:
     ssim: float        # mean SSIM
     dL_dimg: np.ndarray  # [H, W, 3] float64
     ssim_map: np.ndarray | None  # [H, W, 3] float64 per-pixel SSIM (when asked for)
+    mag: np.ndarray | None  # [H, W, 3] the gradient's terms summed in absolute value (when asked for)
 
 
 def loss_l1_ssim(img: np.ndarray, target: np.ndarray, lam: float = 0.2, c1: float = SSIM_C1,
@@ -388,9 +389,10 @@ def loss_l1_ssim(img: np.ndarray, target: np.ndarray, lam: float = 0.2, c1: floa
     out = np.zeros(3, np.float64)
     g = np.empty((H, W, 3), np.float64)
     smap = np.empty((H, W, 3), np.float64) if want_map else None
+    mag = np.empty((H, W, 3), np.float64) if want_map else None
     _lib("f64").ora_loss_l1_ssim(W, H, _p(x), _p(y), lam, c1, c2, sigma, _p(out), _p(g),
-                                 _p(smap))
-    return Loss(float(out[0]), float(out[1]), float(out[2]), g, smap)
+                                 _p(smap), _p(mag))
+    return Loss(float(out[0]), float(out[1]), float(out[2]), g, smap, mag)
 
 
 def sh_basis(dirs: np.ndarray) -> tuple[np.ndarray, np.ndarray]:

@@ -1249,7 +1249,11 @@ void ora_adam_step(int64_t count, double* p, double* m, double* v, const double*
  * window.  The L1 term's derivative is sign(x - y) (0 where x = y).
  *
  * out[0] = L, out[1] = mean |x - y|, out[2] = mean SSIM; dL_dx [H][W][3];
- * ssim_map [H][W][3] (optional, NULL = not written) the per-pixel SSIM.
+ * ssim_map [H][W][3] (optional, NULL = not written) the per-pixel SSIM; mag
+ * [H][W][3] (optional) the same sums over absolute values of every term,
+ * (1 - lambda) / (3HW) + lambda / (3HW) sum_q w(q - p) (|dS/dmu_x| +
+ * 2 |x(p)| |dS/de_xx| + |y(p)| |dS/de_xy|): the scale that rounding errors of
+ * an fp32 evaluation are proportional to.
  */
 #define SSIM_R 5 /* window radius: 11 taps */
 
@@ -1263,7 +1267,8 @@ static void ssim_window(double sigma, double* g) {
 }
 
 void ora_loss_l1_ssim(int W, int H, const float* x, const float* y, double lambda, double c1,
-                      double c2, double sigma, double* out, double* dL_dx, double* ssim_map) {
+                      double c2, double sigma, double* out, double* dL_dx, double* ssim_map,
+                      double* mag) {
     double g[2 * SSIM_R + 1];
     ssim_window(sigma, g);
     int64_t np = (int64_t)W * H;
@@ -1311,7 +1316,7 @@ void ora_loss_l1_ssim(int W, int H, const float* x, const float* y, double lambd
             for (int ch = 0; ch < 3; ++ch) {
                 int64_t i = ((int64_t)r * W + c) * 3 + ch;
                 double xv = x[i], yv = y[i];
-                double ds = 0.0;
+                double ds = 0.0, da = 0.0;
                 for (int a = -SSIM_R; a <= SSIM_R; ++a)
                     for (int b = -SSIM_R; b <= SSIM_R; ++b) {
                         int rr = r + a, cc = c + b;
@@ -1319,9 +1324,12 @@ void ora_loss_l1_ssim(int W, int H, const float* x, const float* y, double lambd
                         double w = g[a + SSIM_R] * g[b + SSIM_R];
                         int64_t q = ((int64_t)rr * W + cc) * 3 + ch;
                         ds += w * (dmu[q] + 2.0 * xv * dxx[q] + yv * dxy[q]);
+                        da += w * (fabs(dmu[q]) + 2.0 * fabs(xv) * fabs(dxx[q]) +
+                                   fabs(yv) * fabs(dxy[q]));
                     }
                 double sg = xv > yv ? 1.0 : (xv < yv ? -1.0 : 0.0);
                 dL_dx[i] = (1.0 - lambda) * inv * sg - lambda * inv * ds;
+                if (mag) mag[i] = (1.0 - lambda) * inv + lambda * inv * da;
             }
     free(dmu);
     free(dxx);

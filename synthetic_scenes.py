@@ -238,3 +238,46 @@ def random_scene(rng, n, width, height, f=None, sh_degree=3, depth=(2.0, 6.0),
     sh[:, 0, :] = rng.uniform(0.0, 1.0, (n, 3)) * (2.0 * math.sqrt(math.pi))
     cam = pinhole(np.eye(4), f, width, height)
     return _pack(means, log_scales, quats, logits, sh, sh_degree), cam
+
+
+def _smooth_field(rng, height, width, cell):
+    """Random values on a coarse grid, bilinearly interpolated to height x width x 3."""
+    gh, gw = height // cell + 2, width // cell + 2
+    g = rng.random((gh, gw, 3))
+    ys = np.arange(height) / cell
+    xs = np.arange(width) / cell
+    y0 = np.floor(ys).astype(int)
+    x0 = np.floor(xs).astype(int)
+    fy = (ys - y0)[:, None, None]
+    fx = (xs - x0)[None, :, None]
+    a = g[y0][:, x0]
+    b = g[y0][:, x0 + 1]
+    c = g[y0 + 1][:, x0]
+    d = g[y0 + 1][:, x0 + 1]
+    return (a * (1 - fx) + b * fx) * (1 - fy) + (c * (1 - fx) + d * fx) * fy
+
+
+def image_pair(rng, height, width) -> tuple[np.ndarray, np.ndarray]:
+    """A rendered image and its target for the photometric loss, [H, W, 3] float32 in
+    [0, 1]: smooth content at two scales with sharp-edged rectangles and a black
+    region (where a render without background shows nothing); the target is the
+    same content with a shifted edge, added texture and noise."""
+    base = 0.6 * _smooth_field(rng, height, width, 24) + 0.4 * _smooth_field(rng, height, width, 5)
+    img = base.copy()
+    tgt = base.copy()
+    for _ in range(max(1, (height * width) // 4000)):
+        h = int(rng.integers(2, max(3, height // 3)))
+        w = int(rng.integers(2, max(3, width // 3)))
+        y = int(rng.integers(0, height))
+        x = int(rng.integers(0, width))
+        col = rng.random(3)
+        img[y:y + h, x:x + w] = col
+        dy, dx = rng.integers(-2, 3, size=2)
+        tgt[max(0, y + dy):y + dy + h, max(0, x + dx):x + dx + w] = col
+    tgt = tgt + 0.15 * (_smooth_field(rng, height, width, 3) - 0.5)
+    tgt = tgt + 0.03 * rng.standard_normal(tgt.shape)
+    # black where nothing is rendered: a band along the top
+    band = int(0.15 * height)
+    img[:band] = 0.0
+    tgt[: band // 2] = 0.0
+    return (np.clip(img, 0, 1).astype(np.float32), np.clip(tgt, 0, 1).astype(np.float32))

@@ -52,8 +52,10 @@ def test_fused_adam_step_matches_oracle(seed, W, H, n, deg):
     M = [t(a.copy()) for a in m0]
     Vv = [t(a.copy()) for a in v0]
     s = gs.AdamSettings(**LR, beta1=B1, beta2=B2, eps=EPS, step=STEP)
+    act_s = torch.full((sc.n, 3), float("nan"), device="cuda")
+    act_o = torch.full((sc.n,), float("nan"), device="cuda")
     gs.gs_project_bwd_adam(r.cam, sc.n, sc.sh_degree, *P, r.tiles_touched, r.grad2d, r.touched,
-                           M, Vv, s)
+                           M, Vv, s, scales_out=act_s, opacities_out=act_o)
     torch.cuda.synchronize()
     # oracle: gradients of the activated parameters, carried to the raw ones, then Adam
     r2, mag = oracle.blend_bwd(cam, ref.proj, ref.binning, wm, None)
@@ -99,3 +101,10 @@ def test_fused_adam_step_matches_oracle(seed, W, H, n, deg):
         lim = 1e-3 * lr_el + 2e-7 * np.maximum(1.0, np.abs(p_ref))
         bad = np.abs(p_gpu - p_ref) > lim
         assert not bad.any(), (names[k], int(bad.sum()), float((np.abs(p_gpu - p_ref) / lim).max()))
+        if k == 1:  # the next forward's scales: exp of the updated log-scales
+            np.testing.assert_allclose(act_s.cpu().numpy(), np.exp(p_gpu), rtol=1e-6)
+            np.testing.assert_allclose(act_s.cpu().numpy(), np.exp(p_ref),
+                                       rtol=2e-6 + float(lim.max()))
+        if k == 3:  # and opacities: sigmoid of the updated logits
+            sg = 1 / (1 + np.exp(-p_gpu))
+            np.testing.assert_allclose(act_o.cpu().numpy(), sg, rtol=1e-6, atol=1e-7)
