@@ -81,6 +81,15 @@ struct LossArgs {
     float l1w, ssw;     // (1 - lambda) / (3 H W), lambda / (3 H W)
 };
 
+// 4-byte asynchronous global -> shared copy; writes 0 instead when !valid (the
+// source address is then not read)
+__device__ __forceinline__ void cp_async4_zfill(float* smem, const float* gmem, bool valid) {
+    const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+    const int n = valid ? 4 : 0;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(sa), "l"(gmem), "r"(n)
+                 : "memory");
+}
+
 __global__ void __launch_bounds__(kLossThreads, 2)
     loss_ssim_kernel(int W, int H, const float* __restrict__ img, const float* __restrict__ tgt,
                      LossArgs la, float* __restrict__ dimg, float2* __restrict__ part) {
@@ -96,20 +105,24 @@ __global__ void __launch_bounds__(kLossThreads, 2)
     const int tx0 = blockIdx.x * kLT, ty0 = blockIdx.y * kLT;
     float l1_sum = 0.f, ssim_sum = 0.f;
 
-    for (int ch = 0; ch < 3; ++ch) {
-        // stage channel ch of x and y over the tile and a 10-pixel halo (0 outside)
+    // stage channel ch of x and y over the tile and a 10-pixel halo (0 outside) as
+    // asynchronous copies; channel ch + 1 is staged while channel ch's derivative
+    // maps are summed, once nothing reads the staged values any more
+    auto stage = [&](int ch) {
         for (int i = tid; i < kIn * kIn; i += kLossThreads) {
             const int r = i / kIn, c = i - r * kIn;
             const int gy = ty0 - 2 * kLR + r, gx = tx0 - 2 * kLR + c;
-            float xv = 0.f, yv = 0.f;
-            if (gy >= 0 && gy < H && gx >= 0 && gx < W) {
-                const int64_t o = ((int64_t)gy * W + gx) * 3 + ch;
-                xv = __ldg(img + o);
-                yv = __ldg(tgt + o);
-            }
-            xs[r * kInPitch + c] = xv;
-            ys[r * kInPitch + c] = yv;
+            const bool in = gy >= 0 && gy < H && gx >= 0 && gx < W;
+            const int64_t o = in ? ((int64_t)gy * W + gx) * 3 + ch : 0;
+            cp_async4_zfill(xs + r * kInPitch + c, img + o, in);
+            cp_async4_zfill(ys + r * kInPitch + c, tgt + o, in);
         }
+        cp_async_commit();
+    };
+    stage(0);
+
+    for (int ch = 0; ch < 3; ++ch) {
+        cp_async_wait<0>();
         __syncthreads();
 
         // along rows: x, y, x^2, y^2, xy summed with the window, 42 columns
@@ -177,7 +190,8 @@ __global__ void __launch_bounds__(kLossThreads, 2)
                     const float cov = acc[4][j] - mx * my;
                     const float A1 = 2.f * mx * my + la.c1, A2 = 2.f * cov + la.c2;
                     const float B1 = mx * mx + my * my + la.c1, B2 = vx + vy + la.c2;
-                    const float rD = 1.f / (B1 * B2);
+                    const float rD = rcp_approx(B1 * B2);  // ~1 ulp: far below the
+                                                           // cancellation error of B2
                     const float S = A1 * A2 * rD;
                     a = (2.f * my * (A2 - A1) - 2.f * mx * S * (B2 - B1)) * rD;
                     b = -S * B1 * rD;
@@ -194,6 +208,7 @@ __global__ void __launch_bounds__(kLossThreads, 2)
             }
         }
         __syncthreads();
+        if (ch < 2) stage(ch + 1);
 
         // along rows: a, b, c summed with the window, the tile's 32 columns
         if (tid < kMom * (kLT / kH2)) {
@@ -247,13 +262,22 @@ __global__ void __launch_bounds__(kLossThreads, 2)
                     }
                 }
             }
+            // the pixel's own x and y (the staging room holds the next channel by now;
+            // pixels outside the image are never written)
+            float xv[kV2], yv[kV2];
+#pragma unroll
+            for (int j = 0; j < kV2; ++j) {
+                const int gy = ty0 + s * kV2 + j, gx = tx0 + c;
+                const bool in = gy < H && gx < W;
+                const int64_t o = in ? ((int64_t)gy * W + gx) * 3 + ch : 0;
+                xv[j] = in ? __ldg(img + o) : 0.f;
+                yv[j] = in ? __ldg(tgt + o) : 0.f;
+            }
 #pragma unroll
             for (int j = 0; j < kV2; ++j) {
                 const int r = s * kV2 + j;
-                const int o = (r + 2 * kLR) * kInPitch + c + 2 * kLR;
-                const float xv = xs[o], yv = ys[o];
-                const float sg = xv > yv ? 1.f : (xv < yv ? -1.f : 0.f);
-                const float ds = acc[0][j] + 2.f * xv * acc[1][j] + yv * acc[2][j];
+                const float sg = xv[j] > yv[j] ? 1.f : (xv[j] < yv[j] ? -1.f : 0.f);
+                const float ds = acc[0][j] + 2.f * xv[j] * acc[1][j] + yv[j] * acc[2][j];
                 grad[(r * kLT + c) * 3 + ch] = la.l1w * sg - la.ssw * ds;
             }
         }

@@ -520,12 +520,15 @@ __device__ __forceinline__ T ld_param(const T* p) {
 }
 
 // One Adam step of one parameter (fp32): the moments are updated in place and
-// the new parameter value is returned
+// the new parameter value is returned.  The step's square root and reciprocal
+// are the hardware approximations (about one unit in the last place each): the
+// step size needs no correct rounding, and the exact forms cost most of the
+// kernel's instructions
 __device__ __forceinline__ float adam1(float p, float& m, float& v, float g, float lr,
                                        const AdamArgs& a) {
     m = fmaf(a.b1, m, (1.f - a.b1) * g);
     v = fmaf(a.b2, v, (1.f - a.b2) * (g * g));
-    return p - lr * (m * a.c1) / (sqrtf(v * a.c2) + a.eps);
+    return p - lr * (m * a.c1) * rcp_approx(sqrt_approx(v * a.c2) + a.eps);
 }
 
 __device__ __forceinline__ void adam_at(float* p, float* m, float* v, int64_t j, float g, float lr,
