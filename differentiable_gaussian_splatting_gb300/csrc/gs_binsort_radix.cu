@@ -208,8 +208,23 @@ __global__ void __launch_bounds__(kRsBlock, 4) rs_onesweep(
     for (int w = 0; w < kRsWarps; ++w) gpre += w < warp ? S.warp_sums[w] : 0u;
     const uint64_t gstart = gpre + gx - gd;
 
+    // ---- stage in block-sorted order (before the look-back: the keys' registers
+    // are free while it waits)
+#pragma unroll
+    for (int r = 0; r < kRsIpt; ++r) {
+        const int64_t idx = wbase + r * 32 + lane;
+        if (idx < n) {
+            const uint32_t dd = (k[r] >> shift) & 255u;
+            const uint32_t li = S.dstart[dd] + S.wcnt[warp][dd] + loc[r];
+            S.keys[li] = k[r];
+            S.vals[li] = v[r];
+        }
+    }
+
     // ---- look back over the earlier tiles for this digit, kLbWindow words in
-    // flight at a time (nearest first), up to the first inclusive prefix
+    // flight at a time (nearest first), up to the first inclusive prefix (8, 16
+    // and 32 words measured alike on 29.7M keys: the walk is not what bounds
+    // the pass)
     uint64_t excl = 0;
     if (b > 0) {
         bool found = false;
@@ -237,17 +252,7 @@ __global__ void __launch_bounds__(kRsBlock, 4) rs_onesweep(
     }
     S.gbase[d] = (int64_t)(gstart + excl) - (int64_t)dstart;
 
-    // ---- stage in block-sorted order, then write each digit run contiguously
-#pragma unroll
-    for (int r = 0; r < kRsIpt; ++r) {
-        const int64_t idx = wbase + r * 32 + lane;
-        if (idx < n) {
-            const uint32_t dd = (k[r] >> shift) & 255u;
-            const uint32_t li = S.dstart[dd] + S.wcnt[warp][dd] + loc[r];
-            S.keys[li] = k[r];
-            S.vals[li] = v[r];
-        }
-    }
+    // ---- write each digit run contiguously
     __syncthreads();
     const int cnt = (int)min64(kRsTile, n - b * kRsTile);
     for (int i = tid; i < cnt; i += kRsBlock) {
