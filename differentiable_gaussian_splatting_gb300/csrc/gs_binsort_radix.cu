@@ -152,18 +152,28 @@ __global__ void __launch_bounds__(kRsBlock, 4) rs_onesweep(
         k[r] = valid ? __ldg(keys_in + idx) : 0xffffffffu;
         v[r] = valid ? __ldg(vals_in + idx) : 0;
     }
+    // The lanes holding the same digit come from eight ballots; the lowest of them
+    // adds their number to the warp's count of that digit and hands the old count
+    // to the others.  A warp's shared-memory atomics take effect in program
+    // order, so item r's offsets follow item r - 1's and the ranking is stable,
+    // while the items' atomics need not wait for one another.
+    const uint32_t lt = lanemask_lt();
 #pragma unroll
     for (int r = 0; r < kRsIpt; ++r) {
         const int64_t idx = wbase + r * 32 + lane;
         const bool valid = idx < n;
         const uint32_t d = (k[r] >> shift) & 255u;
-        const uint32_t peers = __match_any_sync(0xffffffffu, valid ? d : 256u + lane);
-        const uint32_t rank = __popc(peers & lanemask_lt());
-        const uint32_t prev = S.wcnt[warp][d];
-        loc[r] = prev + rank;
-        __syncwarp();
-        if (valid && rank == 0) S.wcnt[warp][d] = prev + __popc(peers);
-        __syncwarp();
+        uint32_t peers = __ballot_sync(0xffffffffu, valid);
+#pragma unroll
+        for (int bit = 0; bit < 8; ++bit) {
+            const uint32_t m = __ballot_sync(0xffffffffu, (d >> bit) & 1u);
+            peers &= ((d >> bit) & 1u) ? m : ~m;
+        }
+        if (!valid) peers = 1u << lane;
+        const int leader = __ffs(peers) - 1;
+        uint32_t old = 0;
+        if (valid && leader == lane) old = atomicAdd(&S.wcnt[warp][d], (uint32_t)__popc(peers));
+        loc[r] = __shfl_sync(0xffffffffu, old, leader) + __popc(peers & lt);
     }
     __syncthreads();
 
