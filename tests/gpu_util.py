@@ -1,5 +1,5 @@
 """Helpers for the GPU parity tests: run the C-ABI path on the device and compare it with
-the CPU oracle.  Tolerances (north star of the method): bit-exact integers; RGB and final
+the CPU oracle.  Tolerances: bit-exact integers; RGB and final
 transmittance within 1e-5 relative / 1e-6 absolute; gradients within 1e-4 relative /
 1e-6 absolute, relative to the magnitude of what each gradient sums (the oracle's sum of
 the absolute values of every product and addend; it equals |gradient| when nothing
