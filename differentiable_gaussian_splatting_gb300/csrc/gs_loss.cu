@@ -63,16 +63,25 @@ static_assert(kIn * (kMom / kH1) <= kLossThreads && kMom * (kMom / kV1) <= kLoss
                   kMom * (kLT / kH2) <= kLossThreads && kLT * (kLT / kV2) <= kLossThreads,
               "one strip per thread in every pass");
 
-// shared memory, in floats
+// shared memory, in floats.  The moments of x and of y share a pass and sit in
+// float2 pairs, summed with the packed FMA (two lanes of fp32 per instruction,
+// each rounded as fmaf); so do SSIM's derivatives by mu_x and E[x^2]
 constexpr int kXs = 0;                                // x: [kIn][kInPitch]
 constexpr int kYs = kXs + kIn * kInPitch;             // y
-constexpr int kRow1 = kYs + kIn * kInPitch;           // 5 row sums: [5][kIn][kMomPitch]
-constexpr int kCoef = kRow1 + 5 * kIn * kMomPitch;    // a, b, c: [3][kMom][kMomPitch]
-constexpr int kRow2 = kRow1;                          // their row sums: [3][kMom][kOutPitch]
-constexpr int kGrad = kCoef + 3 * kMom * kMomPitch;   // dL/dx: [kLT][kLT][3]
+constexpr int kRow1 = kYs + kIn * kInPitch;           // row sums of
+constexpr int kRowM = kRow1;                          //   (x, y): float2 [kIn][kMomPitch]
+constexpr int kRowE = kRowM + 2 * kIn * kMomPitch;    //   (x^2, y^2): float2 [kIn][kMomPitch]
+constexpr int kRowC = kRowE + 2 * kIn * kMomPitch;    //   xy: [kIn][kMomPitch]
+constexpr int kCoef = kRowC + kIn * kMomPitch;        // (a, b): float2 [kMom][kMomPitch]
+constexpr int kCoefC = kCoef + 2 * kMom * kMomPitch;  // c: [kMom][kMomPitch]
+constexpr int kRow2 = kRow1;                          // their row sums: (a, b) float2
+constexpr int kRow2C = kRow2 + 2 * kMom * kOutPitch;  //   [kMom][kOutPitch], c
+constexpr int kGrad = kCoefC + kMom * kMomPitch;      // dL/dx: [kLT][kLT][3]
 constexpr int kRed = kGrad + kLT * kLT * 3;           // 2 x 8 warp partials
 constexpr int kLossSmemFloats = kRed + 2 * (kLossThreads / 32);
 static_assert(3 * kMom * kOutPitch <= 5 * kIn * kMomPitch, "second row sums fit the first's room");
+static_assert(kRowM % 2 == 0 && kRowE % 2 == 0 && kCoef % 2 == 0 && kRow2 % 2 == 0,
+              "float2 arrays on 8-byte boundaries");
 constexpr size_t kLossSmem = sizeof(float) * kLossSmemFloats;
 
 struct LossArgs {
@@ -97,10 +106,16 @@ __global__ void __launch_bounds__(kLossThreads, 2)
     extern __shared__ float sm[];
     float* xs = sm + kXs;
     float* ys = sm + kYs;
-    float* row1 = sm + kRow1;
-    float* coef = sm + kCoef;
-    float* row2 = sm + kRow2;
+    float2* rowm = reinterpret_cast<float2*>(sm + kRowM);
+    float2* rowe = reinterpret_cast<float2*>(sm + kRowE);
+    float* rowc = sm + kRowC;
+    float2* coef = reinterpret_cast<float2*>(sm + kCoef);
+    float* coefc = sm + kCoefC;
+    float2* row2 = reinterpret_cast<float2*>(sm + kRow2);
+    float* row2c = sm + kRow2C;
     float* grad = sm + kGrad;
+    // the window's taps as (g, g) pairs
+    auto g2 = [&](int k) { return make_float2(la.g[k], la.g[k]); };
     const int tid = threadIdx.x;
     const int tx0 = blockIdx.x * kLT, ty0 = blockIdx.y * kLT;
     float l1_sum = 0.f, ssim_sum = 0.f;
@@ -130,51 +145,60 @@ __global__ void __launch_bounds__(kLossThreads, 2)
             const int r = tid % kIn, s = tid / kIn;
             const float* xr = xs + r * kInPitch + s * kH1;
             const float* yr = ys + r * kInPitch + s * kH1;
-            float acc[5][kH1];
+            float2 am[kH1], ae[kH1];
+            float ac[kH1];
 #pragma unroll
-            for (int q = 0; q < 5; ++q)
-#pragma unroll
-                for (int j = 0; j < kH1; ++j) acc[q][j] = 0.f;
+            for (int j = 0; j < kH1; ++j) {
+                am[j] = ae[j] = make_float2(0.f, 0.f);
+                ac[j] = 0.f;
+            }
 #pragma unroll
             for (int i = 0; i < kH1 + 2 * kLR; ++i) {
-                const float xv = xr[i], yv = yr[i];
-                const float v[5] = {xv, yv, xv * xv, yv * yv, xv * yv};
+                const float2 v = make_float2(xr[i], yr[i]);
+                const float2 v2 = __fmul2_rn(v, v);
+                const float vc = v.x * v.y;
 #pragma unroll
                 for (int j = 0; j < kH1; ++j) {
                     const int k = i - j;
                     if (k >= 0 && k < kTaps) {
-#pragma unroll
-                        for (int q = 0; q < 5; ++q) acc[q][j] = fmaf(la.g[k], v[q], acc[q][j]);
+                        am[j] = __ffma2_rn(g2(k), v, am[j]);
+                        ae[j] = __ffma2_rn(g2(k), v2, ae[j]);
+                        ac[j] = fmaf(la.g[k], vc, ac[j]);
                     }
                 }
             }
 #pragma unroll
-            for (int q = 0; q < 5; ++q)
-#pragma unroll
-                for (int j = 0; j < kH1; ++j)
-                    row1[(q * kIn + r) * kMomPitch + s * kH1 + j] = acc[q][j];
+            for (int j = 0; j < kH1; ++j) {
+                const int o = r * kMomPitch + s * kH1 + j;
+                rowm[o] = am[j];
+                rowe[o] = ae[j];
+                rowc[o] = ac[j];
+            }
         }
         __syncthreads();
 
         // along columns: the five moments on the tile + 5, then S, a, b, c
         if (tid < kMom * (kMom / kV1)) {
             const int c = tid % kMom, s = tid / kMom;
-            float acc[5][kV1];
+            float2 am[kV1], ae[kV1];
+            float ac[kV1];
 #pragma unroll
-            for (int q = 0; q < 5; ++q)
-#pragma unroll
-                for (int j = 0; j < kV1; ++j) acc[q][j] = 0.f;
+            for (int j = 0; j < kV1; ++j) {
+                am[j] = ae[j] = make_float2(0.f, 0.f);
+                ac[j] = 0.f;
+            }
 #pragma unroll
             for (int i = 0; i < kV1 + 2 * kLR; ++i) {
-                float v[5];
-#pragma unroll
-                for (int q = 0; q < 5; ++q) v[q] = row1[(q * kIn + s * kV1 + i) * kMomPitch + c];
+                const int o = (s * kV1 + i) * kMomPitch + c;
+                const float2 vm = rowm[o], ve = rowe[o];
+                const float vc = rowc[o];
 #pragma unroll
                 for (int j = 0; j < kV1; ++j) {
                     const int k = i - j;
                     if (k >= 0 && k < kTaps) {
-#pragma unroll
-                        for (int q = 0; q < 5; ++q) acc[q][j] = fmaf(la.g[k], v[q], acc[q][j]);
+                        am[j] = __ffma2_rn(g2(k), vm, am[j]);
+                        ae[j] = __ffma2_rn(g2(k), ve, ae[j]);
+                        ac[j] = fmaf(la.g[k], vc, ac[j]);
                     }
                 }
             }
@@ -185,9 +209,9 @@ __global__ void __launch_bounds__(kLossThreads, 2)
                 const int gy = ty0 - kLR + r;
                 float a = 0.f, b = 0.f, cc = 0.f;
                 if (gy >= 0 && gy < H && gx >= 0 && gx < W) {
-                    const float mx = acc[0][j], my = acc[1][j];
-                    const float vx = acc[2][j] - mx * mx, vy = acc[3][j] - my * my;
-                    const float cov = acc[4][j] - mx * my;
+                    const float mx = am[j].x, my = am[j].y;
+                    const float vx = ae[j].x - mx * mx, vy = ae[j].y - my * my;
+                    const float cov = ac[j] - mx * my;
                     const float A1 = 2.f * mx * my + la.c1, A2 = 2.f * cov + la.c2;
                     const float B1 = mx * mx + my * my + la.c1, B2 = vx + vy + la.c2;
                     const float rD = rcp_approx(B1 * B2);  // ~1 ulp: far below the
@@ -202,9 +226,8 @@ __global__ void __launch_bounds__(kLossThreads, 2)
                         l1_sum += fabsf(xs[o] - ys[o]);
                     }
                 }
-                coef[(0 * kMom + r) * kMomPitch + c] = a;
-                coef[(1 * kMom + r) * kMomPitch + c] = b;
-                coef[(2 * kMom + r) * kMomPitch + c] = cc;
+                coef[r * kMomPitch + c] = make_float2(a, b);
+                coefc[r * kMomPitch + c] = cc;
             }
         }
         __syncthreads();
@@ -213,52 +236,56 @@ __global__ void __launch_bounds__(kLossThreads, 2)
         // along rows: a, b, c summed with the window, the tile's 32 columns
         if (tid < kMom * (kLT / kH2)) {
             const int r = tid % kMom, s = tid / kMom;
-            float acc[3][kH2];
+            float2 aab[kH2];
+            float acc_c[kH2];
 #pragma unroll
-            for (int q = 0; q < 3; ++q)
-#pragma unroll
-                for (int j = 0; j < kH2; ++j) acc[q][j] = 0.f;
+            for (int j = 0; j < kH2; ++j) {
+                aab[j] = make_float2(0.f, 0.f);
+                acc_c[j] = 0.f;
+            }
 #pragma unroll
             for (int i = 0; i < kH2 + 2 * kLR; ++i) {
-                float v[3];
-#pragma unroll
-                for (int q = 0; q < 3; ++q) v[q] = coef[(q * kMom + r) * kMomPitch + s * kH2 + i];
+                const int o = r * kMomPitch + s * kH2 + i;
+                const float2 vab = coef[o];
+                const float vc = coefc[o];
 #pragma unroll
                 for (int j = 0; j < kH2; ++j) {
                     const int k = i - j;
                     if (k >= 0 && k < kTaps) {
-#pragma unroll
-                        for (int q = 0; q < 3; ++q) acc[q][j] = fmaf(la.g[k], v[q], acc[q][j]);
+                        aab[j] = __ffma2_rn(g2(k), vab, aab[j]);
+                        acc_c[j] = fmaf(la.g[k], vc, acc_c[j]);
                     }
                 }
             }
 #pragma unroll
-            for (int q = 0; q < 3; ++q)
-#pragma unroll
-                for (int j = 0; j < kH2; ++j)
-                    row2[(q * kMom + r) * kOutPitch + s * kH2 + j] = acc[q][j];
+            for (int j = 0; j < kH2; ++j) {
+                row2[r * kOutPitch + s * kH2 + j] = aab[j];
+                row2c[r * kOutPitch + s * kH2 + j] = acc_c[j];
+            }
         }
         __syncthreads();
 
         // along columns, then dL/dx of the tile's pixels for this channel
         {
             const int c = tid % kLT, s = tid / kLT;
-            float acc[3][kV2];
+            float2 aab[kV2];
+            float acc_c[kV2];
 #pragma unroll
-            for (int q = 0; q < 3; ++q)
-#pragma unroll
-                for (int j = 0; j < kV2; ++j) acc[q][j] = 0.f;
+            for (int j = 0; j < kV2; ++j) {
+                aab[j] = make_float2(0.f, 0.f);
+                acc_c[j] = 0.f;
+            }
 #pragma unroll
             for (int i = 0; i < kV2 + 2 * kLR; ++i) {
-                float v[3];
-#pragma unroll
-                for (int q = 0; q < 3; ++q) v[q] = row2[(q * kMom + s * kV2 + i) * kOutPitch + c];
+                const int o = (s * kV2 + i) * kOutPitch + c;
+                const float2 vab = row2[o];
+                const float vc = row2c[o];
 #pragma unroll
                 for (int j = 0; j < kV2; ++j) {
                     const int k = i - j;
                     if (k >= 0 && k < kTaps) {
-#pragma unroll
-                        for (int q = 0; q < 3; ++q) acc[q][j] = fmaf(la.g[k], v[q], acc[q][j]);
+                        aab[j] = __ffma2_rn(g2(k), vab, aab[j]);
+                        acc_c[j] = fmaf(la.g[k], vc, acc_c[j]);
                     }
                 }
             }
@@ -277,7 +304,7 @@ __global__ void __launch_bounds__(kLossThreads, 2)
             for (int j = 0; j < kV2; ++j) {
                 const int r = s * kV2 + j;
                 const float sg = xv[j] > yv[j] ? 1.f : (xv[j] < yv[j] ? -1.f : 0.f);
-                const float ds = acc[0][j] + 2.f * xv[j] * acc[1][j] + yv[j] * acc[2][j];
+                const float ds = aab[j].x + 2.f * xv[j] * aab[j].y + yv[j] * acc_c[j];
                 grad[(r * kLT + c) * 3 + ch] = la.l1w * sg - la.ssw * ds;
             }
         }
