@@ -493,12 +493,6 @@ struct EmitRows {
     int64_t pb[kEmitThreads];    // the splat's first pair
     int32_t gid[kEmitThreads];
     int wsum[kEmitThreads / 32];
-    // one chunk of rows: each row's run of pairs (first place, first key, id) and
-    // the exclusive prefix of the runs' lengths
-    int64_t rat[kEmitThreads];
-    uint32_t ra[kEmitThreads];
-    int32_t rgid[kEmitThreads];
-    int roff[kEmitThreads + 1];
     uint32_t hist[kMaxPasses][256];
     int diff0[257];              // pass 0 digit counts as a circular difference array
     uint32_t base0;              // + whole cycles of 256 consecutive tiles
@@ -587,15 +581,20 @@ __global__ void __launch_bounds__(kEmitThreads) emit_pairs(
     S.off[tid] = rbase + ri - nrows;
     if (tid == 0) S.off[kEmitThreads] = rtotal;
     __syncthreads();
-    // rows in chunks of one per thread: each thread finds its row's span, then the
-    // whole block writes the chunk's runs of pairs, consecutive threads to
-    // consecutive places: a wide splat's long rows no longer hold up one thread,
-    // and the stores coalesce within runs (short runs written by their own
-    // thread, a store per lane to its own place, measured slower: 323 us
-    // against 280 on 29.7M pairs)
-    for (int r0 = 0; r0 < rtotal; r0 += kEmitThreads) {
-        const int r = r0 + tid;
+    // rows in chunks of one per lane, each warp on its own: a lane finds one row's
+    // span, the warp scans its 32 runs' lengths in registers, and all 32 lanes
+    // write the runs' pairs, consecutive lanes to consecutive places; a pair's run
+    // is found by a 5-step shuffle search.  A wide splat's long rows no longer
+    // hold up one thread, the stores coalesce within runs, and no block barrier
+    // stops the other warps (one thread per row took 324 us on 29.7M pairs, the
+    // block writing each chunk together 280 us)
+    const unsigned F = 0xffffffffu;
+    for (int r0 = warp * 32; r0 < rtotal; r0 += kEmitThreads) {
+        const int r = r0 + lane;
         int wv = 0;
+        int64_t at = 0;
+        uint32_t a = 0;
+        int32_t gid = 0;
         if (r < rtotal) {
             int lo = 0, hi = kEmitThreads;  // the last owner with off[owner] <= r
             while (hi - lo > 1) {
@@ -608,46 +607,39 @@ __global__ void __launch_bounds__(kEmitThreads) emit_pairs(
             int tx0, tx1;
             if (row_span(e, S.dyv[lo], ty, cam.W, cam.H, cam.ntx, &tx0, &tx1)) {
                 const int w = tx1 - tx0;
-                const int64_t at = S.pb[lo] + atomicAdd(&S.pcur[lo], w);
-                const uint32_t a = (uint32_t)ty * (uint32_t)cam.ntx + (uint32_t)tx0;
+                at = S.pb[lo] + atomicAdd(&S.pcur[lo], w);
+                a = (uint32_t)ty * (uint32_t)cam.ntx + (uint32_t)tx0;
+                gid = S.gid[lo];
                 wv = (int)max64(0, min64(w, capacity - at));  // the pairs that fit
-                S.rat[tid] = at;
-                S.ra[tid] = a;
-                S.rgid[tid] = S.gid[lo];
                 if (wv > 0) count_tile_range(S, a, wv, passes);
             }
         }
-        // exclusive prefix of the runs' lengths over the block
+        // exclusive prefix of the warp's runs' lengths
         int x = wv;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            const int y = __shfl_up_sync(F, x, o);
             if (lane >= o) x += y;
         }
-        if (lane == 31) S.wsum[warp] = x;
-        __syncthreads();
-        int pre = 0, total = 0;
+        const int excl = x - wv;
+        const int total = __shfl_sync(F, x, 31);
+        for (int p0 = 0; p0 < total; p0 += 32) {
+            const int p = p0 + lane;
+            int src = 0;  // the last lane whose run starts at or before p
 #pragma unroll
-        for (int w = 0; w < kEmitThreads / 32; ++w) {
-            const int v = S.wsum[w];
-            pre += w < warp ? v : 0;
-            total += v;
-        }
-        S.roff[tid] = pre + x - wv;
-        if (tid == 0) S.roff[kEmitThreads] = total;
-        __syncthreads();
-        for (int p = tid; p < total; p += kEmitThreads) {
-            int lo = 0, hi = kEmitThreads;  // the last run with roff[run] <= p
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (S.roff[mid] <= p) lo = mid; else hi = mid;
+            for (int step = 16; step > 0; step >>= 1)
+                if (__shfl_sync(F, excl, src + step) <= p) src += step;
+            const int64_t at_s = __shfl_sync(F, at, src);
+            const uint32_t a_s = __shfl_sync(F, a, src);
+            const int32_t gid_s = __shfl_sync(F, gid, src);
+            const int i = p - __shfl_sync(F, excl, src);
+            if (p < total) {
+                pkeys[at_s + i] = a_s + (uint32_t)i;
+                pvals[at_s + i] = gid_s;
             }
-            const int i = p - S.roff[lo];
-            pkeys[S.rat[lo] + i] = S.ra[lo] + (uint32_t)i;
-            pvals[S.rat[lo] + i] = S.rgid[lo];
         }
-        __syncthreads();  // the runs are read; the next chunk may overwrite them
     }
+    __syncthreads();
     // pass 0: the running sum of the difference array, plus the whole cycles
     {
         int x = S.diff0[tid];
