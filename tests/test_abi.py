@@ -104,3 +104,58 @@ def test_invalid_sizes_and_pointers_are_rejected_on_the_host(lib):
                 gs.Settings(0, 0, 4, 256, 256.0, 0.05, 1.5)):   # eps >= 1
         assert lib.gs_rasterize_fwd(C.byref(cam), C.byref(bad), 10, fake, fake, 100, fake,
                                     fake, fake, 1 << 30, *([fake] * 4), None) == 1
+
+
+def test_loss_arguments_are_checked_on_the_host(lib):
+    import differentiable_gaussian_splatting_gb300 as gs
+
+    fake = C.c_void_p(0x100000)
+    mis = C.c_void_p(0x100004)
+    ok = gs.LossSettings.default()
+    ws = lib.gs_loss_workspace_bytes(100, 60)
+    assert ws == 4 * 2 * 8  # one float2 per 32x32 tile: 4 x 2 tiles
+    assert lib.gs_loss_workspace_bytes(0, 60) == 0
+
+    def call(w=100, h=60, img=fake, tgt=fake, s=ok, d=C.c_void_p(0x200000), out=fake,
+             wsp=fake, wsb=ws):
+        return lib.gs_loss_l1_ssim(w, h, img, tgt, C.byref(s) if s is not None else None, d, out,
+                                   wsp, wsb, None)
+
+    assert call(w=0) == 1 and call(h=-3) == 1
+    assert call(s=None) == 1
+    for field, value in (("lambda_", -0.1), ("lambda_", 1.5), ("c1", 0.0), ("c2", -1.0),
+                         ("sigma", 0.0), ("sigma", float("inf"))):
+        bad = gs.LossSettings.default()
+        setattr(bad, field, value)
+        assert call(s=bad) == 1, field
+    assert call(img=None) == 1 and call(out=mis) == 1
+    # the gradient may not overlap either image
+    assert call(d=C.c_void_p(0x100000 + 16)) == 1
+    assert call(wsb=ws - 1) == 5  # workspace too small
+
+
+def test_adam_arguments_are_checked_on_the_host(lib):
+    import differentiable_gaussian_splatting_gb300 as gs
+
+    cam = _cam()
+    fake = C.c_void_p(0x100000)
+    mom = gs.AdamMoments()
+    for k in range(5):
+        mom.m[k] = 0x100000
+        mom.v[k] = 0x100000
+    good = dict(lr_means=1e-4, lr_scales=5e-3, lr_quats=1e-3, lr_opacities=5e-2, lr_sh0=2.5e-3,
+                lr_shN=1.25e-4, beta1=0.9, beta2=0.999, eps=1e-15, step=1)
+
+    def call(s, moments=mom, n=10, act=None):
+        return lib.gs_project_bwd_adam(C.byref(cam), n, 3, *([fake] * 8),
+                                       C.byref(moments) if moments is not None else None,
+                                       C.byref(gs.AdamSettings(**s)), act, None, None)
+
+    for field, value in (("beta1", 1.0), ("beta2", -0.1), ("eps", 0.0), ("step", 0),
+                         ("lr_sh0", -1.0), ("lr_means", float("nan"))):
+        assert call({**good, field: value}) == 1, field
+    assert call(good, moments=None) == 1
+    assert call(good, act=C.c_void_p(0x100004)) == 1  # activated scales misaligned
+    assert call(good, n=-1) == 1
+    empty = gs.AdamMoments()
+    assert call(good, moments=empty) == 1  # null moment pointers
