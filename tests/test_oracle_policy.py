@@ -41,3 +41,29 @@ def test_h_max_limits_the_search():
     assert h_all >= 2
     h1, _, _ = oracle.policy(counts, K=64, h_max=1)
     assert h1 <= 1
+
+
+def _golden_cases():
+    import os
+
+    path = os.path.join(os.path.dirname(__file__), "golden", "policy_eq6_cases.txt")
+    for line in open(path):
+        line = line.split("#", 1)[0].strip()
+        if not line:
+            continue
+        f = [x.strip() for x in line.split(";")]
+        counts = []
+        for part in f[0].split(","):
+            v, _, r = part.partition("x")
+            counts += [int(v)] * int(r or 1)
+        yield (counts, int(f[1]), float(f[2]), float(f[3]), float(f[4]), int(f[5]), int(f[6]),
+               float(f[7]))
+
+
+def test_golden_hand_worked_cases():
+    cases = list(_golden_cases())
+    assert len(cases) == 7
+    for counts, K, lam, beta, eps, h, k, cost in cases:
+        got = oracle.policy(counts, K=K, lam=lam, beta=beta, eps=eps)
+        assert got[:2] == (h, k), (counts[:3], K, got)
+        assert abs(got[2] - cost) <= 1e-9 * cost, (counts[:3], K, got)
