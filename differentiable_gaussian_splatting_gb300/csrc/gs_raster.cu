@@ -5,7 +5,7 @@
 // resident CTAs takes work from a queue in LPT order (one atomicAdd per fetch);
 // Sec. 4.2 the heaviest tiles are split into k depth-contiguous chunks that
 // blend from unit transmittance, signal saturation through a per-tile
-// atomicMin flag that later chunks check once per batch of staged splats, and are
+// atomicMin flag that later chunks check once per 256-splat batch, and are
 // composed with Eq. 5; Sec. 4.3-4.4 the per-frame policy of Eq. 6 picks how
 // many tiles to split and how deeply.  Chunk items and whole-tile items share
 // one queue (heavy chunks first), which is the fused form of the selective
@@ -40,9 +40,7 @@ namespace gs {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kBatch = 512;              // splats staged per block barrier
-constexpr int kPer = kBatch / kThreads;  // staged by each thread
-static_assert(kBatch % kThreads == 0, "whole splats per thread");
+constexpr int kBatch = 256;
 constexpr int kPolicyThreads = 1024;
 
 struct RasterArgs {
@@ -125,6 +123,7 @@ struct Smem {
     float4 r0[kBatch];
     float4 r1[kBatch];
     float4 r2[kBatch];
+    int32_t gid[kBatch];
     uint8_t mask[kBatch];
     uint32_t cm[8 * (kBatch / 32)];  // [warp][32-splat chunk] blended bits
     int item;
@@ -147,23 +146,19 @@ __device__ __forceinline__ bool blend_range(const RasterArgs& A, Smem& S, int tx
         const int live = __syncthreads_or(!st.done);
         if (!live) return false;
         if (S.flag) return true;
-        for (int q = tid; q < 8 * (kBatch / 32); q += kThreads) S.cm[q] = 0u;
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int slot = tid + u * kThreads;
-            const int64_t j = bs + slot;
-            if (j < e) {
-                const int32_t g = __ldg(A.ids + j);
-                const float4 r0 = __ldg(A.splats + 3 * (int64_t)g);
-                const float4 r1 = __ldg(A.splats + 3 * (int64_t)g + 1);
-                const float4 r2 = __ldg(A.splats + 3 * (int64_t)g + 2);
-                S.r0[slot] = r0;
-                S.r1[slot] = r1;
-                S.r2[slot] = r2;
-                S.mask[slot] = (uint8_t)subtile_mask(ellipse_of(r0, r1, r2), tx, ty, A.W, A.H);
-            } else {
-                S.mask[slot] = 0;
-            }
+        const int64_t j = bs + tid;
+        if (tid < 8 * (kBatch / 32)) S.cm[tid] = 0u;
+        if (j < e) {
+            const int32_t g = __ldg(A.ids + j);
+            const float4 r0 = __ldg(A.splats + 3 * (int64_t)g);
+            const float4 r1 = __ldg(A.splats + 3 * (int64_t)g + 1);
+            const float4 r2 = __ldg(A.splats + 3 * (int64_t)g + 2);
+            S.r0[tid] = r0;
+            S.r1[tid] = r1;
+            S.r2[tid] = r2;
+            S.mask[tid] = (uint8_t)subtile_mask(ellipse_of(r0, r1, r2), tx, ty, A.W, A.H);
+        } else {
+            S.mask[tid] = 0;
         }
         __syncthreads();
         const int nb = (int)min64(kBatch, e - bs);
@@ -203,19 +198,11 @@ __device__ __forceinline__ bool blend_range(const RasterArgs& A, Smem& S, int tx
             }
         }
         __syncthreads();
-        if (write_cmask) {
+        if (write_cmask && j < e) {
+            uint32_t m = 0;
 #pragma unroll
-            for (int u = 0; u < kPer; ++u) {
-                const int slot = tid + u * kThreads;
-                const int64_t j = bs + slot;
-                if (j < e) {
-                    uint32_t m = 0;
-#pragma unroll
-                    for (int w = 0; w < 8; ++w)
-                        m |= ((S.cm[w * (kBatch / 32) + (slot >> 5)] >> lane) & 1u) << w;
-                    A.cmask[j] = (uint8_t)m;
-                }
-            }
+            for (int w = 0; w < 8; ++w) m |= ((S.cm[w * (kBatch / 32) + (tid >> 5)] >> lane) & 1u) << w;
+            A.cmask[j] = (uint8_t)m;
         }
     }
     return false;
