@@ -1,0 +1,100 @@
+"""The benchmark's host logic on CPU: the roofline figures it reports (algorithmic work per
+launch over time, against the stated peak), the whole-step model, the kernel-launch
+count it claims, and the rule that a profile's DRAM traffic is reported only while the
+kernel's sources still hash to what was captured."""
+
+import os
+import sys
+from types import SimpleNamespace
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+PEAKS = {"hbm_gbs": 6000.0, "source": "measured"}
+SC = SimpleNamespace(n=1000, sh_degree=3)  # 236 parameter bytes per Gaussian
+N_SM, MHZ = 152, 2000.0
+FP32_TFLOPS = 2.0 * 128 * N_SM * MHZ * 1e6 / 1e12
+
+
+def test_alu_roofline_of_the_raster_calls():
+    E = 10_000_000
+    r = bench.roofline("gs_rasterize_bwd", 0.5, SC, 700, 3000, E, 100, 200, PEAKS, N_SM, MHZ)
+    assert r["bound"] == "alu" and r["unit"] == "TFLOP/s"
+    assert r["peak"] == pytest.approx(FP32_TFLOPS)
+    assert r["achieved"] == pytest.approx(bench.FLOPS_BWD_PER_E * E / 0.5e-3 / 1e12)
+    assert r["frac"] == pytest.approx(r["achieved"] / r["peak"])
+    f = bench.roofline("gs_rasterize_fwd", 0.25, SC, 700, 3000, E, 100, 200, PEAKS, N_SM, MHZ)
+    assert f["achieved"] == pytest.approx(bench.FLOPS_FWD_PER_E * E / 0.25e-3 / 1e12)
+
+
+def test_loss_roofline_counts_window_fmas_per_pixel():
+    H, W = 840, 1297
+    assert bench.LOSS_FLOPS_PER_PIXEL == 3 * (5 + 3) * 2 * 11 * 2
+    r = bench.roofline("gs_loss_l1_ssim", 0.1, SC, 0, 0, 0, H, W, PEAKS, N_SM, MHZ)
+    assert r["bound"] == "alu"
+    assert r["achieved"] == pytest.approx(bench.LOSS_FLOPS_PER_PIXEL * H * W / 0.1e-3 / 1e12)
+
+
+@pytest.mark.parametrize("call,expected", [
+    # visible: M = 600 of N = 1000; G = 44 + 12 * 16 = 236 bytes of parameters
+    ("gs_project", 44 * 1000 + 192 * 600 + 64 * 600 + 8 * 1000),
+    ("gs_project_bwd", 36 * 600 + 236 * 600 + 236 * 1000 + 5 * 1000),
+    ("gs_project_bwd_adam", 36 * 600 + 5 * 1000 + 6 * 236 * 1000 + 16 * 1000),
+    ("gs_bin_sort", 8 * 600 * 8 + 8 * 5000 * 5),
+])
+def test_hbm_roofline_bytes(call, expected):
+    r = bench.roofline(call, 0.01, SC, 600, 5000, 0, 100, 100, PEAKS, N_SM, MHZ)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 6000.0
+    assert r["achieved"] == pytest.approx(expected / 0.01e-3 / 1e9)
+
+
+def test_step_roofline_sums_the_binding_term_of_each_phase():
+    M, I, E, H, W = 600, 5000, 2_000_000, 100, 100
+    out = bench.step_roofline(1.0, SC, M, I, E, H, W, PEAKS, N_SM, MHZ)
+    assert set(out["phases_ms"]) == {"project", "bin_sort", "forward", "backward"}
+    assert out["ms"] == pytest.approx(sum(out["phases_ms"].values()))
+    assert out["frac"] == pytest.approx(out["ms"] / 1.0)
+    fwd_flops = bench.FLOPS_FWD_PER_E * E / (FP32_TFLOPS * 1e12) * 1e3
+    assert out["phases_ms"]["forward"] >= fwd_flops * (1 - 1e-12)
+    # with few contributing pairs the backward is bound by its bytes, which Adam raises
+    # (parameters and both moments read and written instead of one gradient row)
+    plain = bench.step_roofline(1.0, SC, M, I, 0, H, W, PEAKS, N_SM, MHZ)
+    train = bench.step_roofline(1.0, SC, M, I, 0, H, W, PEAKS, N_SM, MHZ, train=True)
+    assert "loss" in train["phases_ms"] and "loss" not in plain["phases_ms"]
+    assert train["phases_ms"]["backward"] > plain["phases_ms"]["backward"]
+
+
+def test_kernel_launch_count_of_both_binning_paths():
+    # project, policy + forward, reset + backward, chain rule: 6 kernels around the sort
+    # bucket path: 10 binning kernels plus one merge round per doubling of 4096 up to
+    # min(n, capacity) -- 9 rounds on the 1.5M scene, 25 launches per step as the ncu
+    # launch list of that scene counts them
+    assert bench.kernel_launches(1000, 4000, 128, 128) == 10 + 6
+    assert bench.kernel_launches(1_500_000, 1_900_000, 1297, 840) == 10 + 9 + 6 == 25
+    # long lists: the two-stage radix sort, one tile pass per 8 bits of the tile index
+    # (8160 tiles at 1920 x 1080: 13 bits, 2 passes)
+    assert ((120 * 68) - 1).bit_length() == 13
+    assert bench.kernel_launches(3_000_000, 9 << 20, 1920, 1080) == (3 + 4 + 3 + 1 + 2 + 2 + 2) + 6
+
+
+def test_profile_traffic_only_while_sources_match(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    csrc = tmp_path / "differentiable_gaussian_splatting_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in ("gs_raster.cu", "gs_device.cuh", "gs_internal.h"):
+        (csrc / f).write_text(f"// {f}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    digest = bench.sources_digest(["gs_raster.cu", "gs_device.cuh", "gs_internal.h"])
+    page = prof / "raster_bwd_kernel_scene-1.5M-1297x840.md"
+    page.write_text(f"- sources_sha256: `{digest}` (as captured)\n"
+                    "- traffic_bytes_per_launch: 123456\n")
+    assert bench.profiled_traffic("gs_rasterize_bwd") == 123456
+    (csrc / "gs_raster.cu").write_text("// changed since the capture\n")
+    assert bench.profiled_traffic("gs_rasterize_bwd") is None
+    assert bench.profiled_traffic("gs_bin_sort") is None  # several kernels: no single profile
