@@ -287,11 +287,9 @@ def run_gpu(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": ss.CONFIG_NAMES[args.config], "gaussians": sc.n,
-                       "image": f"{W}x{H}", "sh_degree": sc.sh_degree, "tile_pairs": n_pairs,
-                       "contributing_pairs": E, "sh_storage": "bf16" if args.sh_bf16 else "f32",
-                       "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "inputs larger than L2 (354 MB parameters + 354 MB gradients)"},
+            "config": workload_config(args, sc, W, H, n_pairs,
+                                      "replicas" if world > 1 else "single"),
+            "contributing_pairs": E,
             "per_call_ms": per_call,
             "roofline": roof,
             "step_roofline": step_roof,
@@ -509,10 +507,31 @@ def run_e2e(gs, r, sc, cam, w, dev, args, n_pairs):
 # ---------------------------------------------------------------------------
 # CPU oracle (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
+L2_BYTES = 129e6  # the GB300's L2
+
+
+def l2_note(sc, second: str, factor: int) -> str:
+    """How the timed steps avoid a warm L2: whether the parameters and the arrays of the
+    same size that each step writes (gradients, or the two Adam moments) exceed it."""
+    mb = sum(a.nbytes for a in (sc.means, sc.scales, sc.quats, sc.opacities, sc.sh)) / 1e6
+    fits = "larger than" if (1 + factor) * mb * 1e6 > L2_BYTES else "smaller than"
+    return f"inputs {fits} L2 ({mb:.3g} MB parameters + {factor * mb:.3g} MB {second})"
+
+
+def workload_config(args, sc, W, H, n_pairs, parallelism):
+    """The workload both arms time: scene, image, SH storage and the view's tile-Gaussian
+    pair count (an integer both sides reproduce bit for bit)."""
+    return {"workload": ss.CONFIG_NAMES[args.config], "gaussians": sc.n, "image": f"{W}x{H}",
+            "sh_degree": sc.sh_degree, "tile_pairs": int(n_pairs),
+            "sh_storage": "bf16" if args.sh_bf16 else "f32", "parallelism": parallelism,
+            "l2": l2_note(sc, "gradients", 1)}
+
+
 def oracle_sample_step(sc, cam, w, tile_stride: int):
     """One bounded oracle step: projection and binning of the whole view, then the
     forward and backward blend of every tile_stride-th tile (in LPT order, so the
-    sample spans heavy and light tiles).  Returns (pairs processed, seconds)."""
+    sample spans heavy and light tiles).  Returns (pairs processed, seconds, pairs of the
+    whole view)."""
     import oracle
 
     t0 = time.perf_counter()
@@ -526,11 +545,11 @@ def oracle_sample_step(sc, cam, w, tile_stride: int):
     g2, _ = oracle.blend_bwd(cam, proj, b, w)
     oracle.project_bwd(sc, cam, proj, g2)
     dt = time.perf_counter() - t0
-    return int(b.counts[sel.astype(bool)].sum()), dt
+    return int(b.counts[sel.astype(bool)].sum()), dt, int(counts.counts.sum())
 
 
 def cpu_baseline(sc, cam, w, stride: int = 1):
-    pairs, dt = oracle_sample_step(sc, cam, w, stride)
+    pairs, dt, _ = oracle_sample_step(sc, cam, w, stride)
     what = "every tile" if stride == 1 else f"every {stride}th tile in LPT order"
     return {"value": pairs / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"one view: all projections and tile counts, forward + backward of "
@@ -681,7 +700,7 @@ def run_train(args):
                        "tile_pairs": [pairs0, pairs1], "contributing_pairs": E,
                        "loss": [loss0, loss1], "adam": TRAIN_LR,
                        "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "inputs larger than L2 (354 MB parameters + 708 MB moments)"},
+                       "l2": l2_note(sc, "moments", 2)},
             "per_call_ms": per_call,
             "roofline": roof,
             "step_roofline": step_roof,
@@ -700,13 +719,20 @@ def run_reference(args):
     if rank != 0:
         return
     sc, cam = ss.make_config(args.config)
+    if args.sh_bf16:
+        # the oracle reads the same coefficients the bfloat16 path stores, widened to float
+        import dataclasses
+
+        import torch
+        sh = torch.from_numpy(np.ascontiguousarray(sc.sh, np.float32))
+        sc = dataclasses.replace(sc, sh=sh.to(torch.bfloat16).float().numpy())
     w = ss.loss_weights(args.config, cam.height, cam.width)
     stride = 4
     for _ in range(args.warmup):
         oracle_sample_step(sc, cam, w, stride)
     tot_pairs, tot_s = 0, 0.0
     for _ in range(args.steps):
-        p, dt = oracle_sample_step(sc, cam, w, stride)
+        p, dt, view_pairs = oracle_sample_step(sc, cam, w, stride)
         tot_pairs += p
         tot_s += dt
     value = tot_pairs / tot_s
@@ -716,7 +742,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": ss.CONFIG_NAMES[args.config]},
+        "data": "synthetic",
+        "config": workload_config(args, sc, cam.width, cam.height, view_pairs, "single"),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

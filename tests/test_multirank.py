@@ -83,3 +83,17 @@ def test_reference_arm_line_on_rank_zero():
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    # the same workload description as the GPU arm's line, with the view's pair count
+    # taken from the oracle's own binning
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    import synthetic_scenes as ss
+
+    sc, cam = ss.make_config(1)
+    counts = oracle.bin_sort(cam, oracle.project(sc, cam), None)
+    expect = {"workload": ss.CONFIG_NAMES[1], "gaussians": sc.n,
+              "image": f"{cam.width}x{cam.height}", "sh_degree": sc.sh_degree,
+              "tile_pairs": int(counts.counts.sum()), "sh_storage": "f32",
+              "parallelism": "single", "l2": bench.l2_note(sc, "gradients", 1)}
+    assert line["config"] == expect
