@@ -61,7 +61,13 @@ cudaError_t side_stream(const SideStream** out) {
         if (err == cudaSuccess) err = cudaEventCreateWithFlags(&s.fork2, cudaEventDisableTiming);
         if (err == cudaSuccess) err = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
         if (err == cudaSuccess) err = cudaEventCreateWithFlags(&s.join2, cudaEventDisableTiming);
-        if (err != cudaSuccess) return err;
+        if (err != cudaSuccess) {  // release what was made, so a retry starts clean
+            for (cudaStream_t st : {s.stream, s.stream2})
+                if (st) cudaStreamDestroy(st);
+            for (cudaEvent_t ev : {s.fork, s.fork2, s.join, s.join2})
+                if (ev) cudaEventDestroy(ev);
+            return err;
+        }
         g_side[dev] = s;
         g_side_ready[dev] = true;
     }
