@@ -1,0 +1,214 @@
+"""Mutation check of the oracle's pins: each entry below plants one plausible mistake
+in a copy of ``oracle/gs_oracle.c`` (a flipped sign, a dropped term or factor, a wrong
+or transposed index, a reversed order) and runs the oracle's own pin tests
+(``tests/test_oracle_*.py``) against that copy.  A mutant that no pin rejects marks
+arithmetic the pins do not fix.
+
+The table is checked against the source on every CPU run (each planted text must occur
+exactly once, so the table follows the source as it changes).  Running the mutants
+themselves takes a minute or two on eight cores and is opt-in:
+
+    GS_ORACLE_MUTANTS=1 python -m pytest tests/test_mutation_oracle.py -n 8 -q
+
+Everything happens on the CPU, in a temporary copy: the repository's oracle is never
+modified.
+"""
+
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "gs_oracle.c")
+
+# (name, text in gs_oracle.c, replacement)
+MUTANTS = [
+    # ---- projection: camera transform, rotation, Jacobian, Eq. 1, conic, tau, extents
+    ("camera_row_index", "dreal ty = ((V[4] * mx + V[5] * my) + V[6] * mz) + V[7];",
+     "dreal ty = ((V[4] * mx + V[5] * my) + V[2] * mz) + V[7];"),
+    ("rotation_sign_r01", "R[1] = 2 * (x * y - w * z);", "R[1] = 2 * (x * y + w * z);"),
+    ("rotation_index_r12", "R[5] = 2 * (y * z - w * x);", "R[5] = 2 * (y * z - w * y);"),
+    ("jacobian_sign_j02", "dreal j02 = -(j00 * u);", "dreal j02 = (j00 * u);"),
+    ("jacobian_row_t1", "T1[k] = j11 * V[4 + k] + j12 * V[8 + k];",
+     "T1[k] = j11 * V[4 + k] + j12 * V[4 + k];"),
+    ("scale_index_n1", "T1[2] * R[6 + k]) * s3[k];", "T1[2] * R[6 + k]) * s3[(k + 1) % 3];"),
+    ("determinant_scale_e0", "dreal e0 = (s1 * s2) * c0;", "dreal e0 = (s0 * s2) * c0;"),
+    ("conic_sign_b", "dreal b = -(P01 / det);", "dreal b = (P01 / det);"),
+    ("cholesky_sign_l12", "dreal l12 = -((P01 / P11) * l11);", "dreal l12 = ((P01 / P11) * l11);"),
+    ("tau_factor_two", "double t = 2.0 * log(CUTOFF_INV * (double)o);",
+     "double t = log(CUTOFF_INV * (double)o);"),
+    ("extent_rx_uses_p11", "dreal rx = sqrt(tau * P00);", "dreal rx = sqrt(tau * P11);"),
+    ("near_plane_ignored", "if (!(tz > cam->znear) ||", "if (!(tz > 0) ||"),
+    # ---- exact row spans and tile rows
+    ("span_boundary_sign", "return (sqrt(disc) - s->l12 * dy) / s->l11;",
+     "return (sqrt(disc) + s->l12 * dy) / s->l11;"),
+    ("span_vertex_sign", "return -((sqrt(s->tau) * s->l12) / (s->l22 * h));",
+     "return ((sqrt(s->tau) * s->l12) / (s->l22 * h));"),
+    ("span_left_not_mirrored", "dmax(dyv, -hi), -lo)", "dmax(dyv, lo), hi)"),
+    ("span_last_column_dropped", "dreal f1 = floor((Xhi - (dreal)0.5) * (dreal)0.0625) + 1;",
+     "dreal f1 = floor((Xhi - (dreal)0.5) * (dreal)0.0625);"),
+    ("rows_first_row_late", "ceil(((s->muy - ryp) - (dreal)15.5)",
+     "ceil(((s->muy - ryp) - (dreal)0.5)"),
+    ("tile_band_not_clipped",
+     "dmin((dreal)(16 * ty) + (dreal)15.5, (dreal)cam->H - (dreal)0.5)",
+     "((dreal)(16 * ty) + (dreal)15.5)"),
+    # ---- spherical harmonics and the view direction
+    ("sh_sign_y2", "Y[2] = k1 * z;", "Y[2] = -k1 * z;"),
+    ("sh_gradient_y9", "dY[9][1] = k3a * (3 * x * x - 3 * y * y);",
+     "dY[9][1] = k3a * (3 * x * x - y * y);"),
+    ("sh_normalisation_k2b", "double k2b = sqrt(5.0 / (16 * PI));",
+     "double k2b = sqrt(5.0 / (4 * PI));"),
+    ("camera_centre_sign", "cw[j] = -((double)viewmat[0 + j] * viewmat[3]",
+     "cw[j] = ((double)viewmat[0 + j] * viewmat[3]"),
+    ("camera_centre_transposed",
+     "(double)viewmat[4 + j] * viewmat[7] +", "(double)viewmat[1 + 4 * j] * viewmat[7] +"),
+    ("colour_channel_dropped", "acc += Y[k] * (double)sh[(i * K + k) * 3 + ch];",
+     "acc += Y[k] * (double)sh[(i * K + k) * 3];"),
+]
+MUTANTS += [
+    # ---- binning, (tile, depth, id) order, ranges, LPT order
+    ("sort_depth_reversed", "if (x->depth_d != y->depth_d) return x->depth_d < y->depth_d ? -1 : 1;",
+     "if (x->depth_d != y->depth_d) return x->depth_d > y->depth_d ? -1 : 1;"),
+    ("sort_tie_break_reversed", "if (x->id != y->id) return x->id < y->id ? -1 : 1;",
+     "if (x->id != y->id) return x->id > y->id ? -1 : 1;"),
+    ("lpt_ascending", "if (x->count != y->count) return x->count > y->count ? -1 : 1;",
+     "if (x->count != y->count) return x->count < y->count ? -1 : 1;"),
+    ("range_end_off_by_one", "        ranges[2 * t + 1] = acc;\n",
+     "        ranges[2 * t + 1] = acc - (acc > 0);\n"),
+    # ---- forward blend
+    ("pixel_centre_dropped", "dreal dx = ((dreal)px + (dreal)0.5) - mux;",
+     "dreal dx = ((dreal)px) - mux;"),
+    ("quadratic_form_term", "dreal q = fma(u1, u1, u2 * u2);", "dreal q = fma(u1, u1, u2);"),
+    ("termination_threshold",
+     "if (fabs(T - T_MIN) <= 2.0 * err * T) fl |= 1;\n                        if (T < T_MIN) break;",
+     "if (fabs(T - T_MIN) <= 2.0 * err * T) fl |= 1;\n                        if (T < 1e-3) break;"),
+    ("alpha_clamp_dropped",
+     "double alpha = araw < ALPHA_MAX ? araw : ALPHA_MAX;\n                        for (int ch",
+     "double alpha = araw;\n                        for (int ch"),
+    ("colour_without_transmittance", "C[ch] += rgb[3 * (int64_t)g + ch] * alpha * T;",
+     "C[ch] += rgb[3 * (int64_t)g + ch] * alpha;"),
+    ("transmittance_update", "T *= (1.0 - alpha);\n                        err +=",
+     "T *= (1.0 - alpha) * (1.0 - alpha);\n                        err +="),
+    ("contributors_not_counted", "                        n++;\n", ""),
+    ("last_index_relative", "last = (int32_t)k;", "last = (int32_t)(k - s0);"),
+    # ---- backward of the blend: the nine screen-space derivatives
+    ("dalpha_behind_sign", "double dalpha = e->T * cG - bG / (1.0 - e->alpha) -",
+     "double dalpha = e->T * cG + bG / (1.0 - e->alpha) -"),
+    ("dalpha_final_t_factor", " gT * Tfin / (1.0 - e->alpha);", " gT * Tfin;"),
+    ("behind_without_transmittance", "behind[ch] += col[ch] * w;",
+     "behind[ch] += col[ch] * e->alpha;"),
+    ("dq_alpha_dropped", "double dq = -0.5 * e->alpha * dalpha;", "double dq = -0.5 * dalpha;"),
+    ("dopacity_factor", "term[5] = exp(-0.5 * e->q) * dalpha;", "term[5] = e->alpha * dalpha;"),
+    ("dmux_conic_index", "term[0] = -2.0 * (a * e->dx + b * e->dy) * dq;",
+     "term[0] = -2.0 * (a * e->dx + c * e->dy) * dq;"),
+    ("dmuy_sign", "term[1] = -2.0 * (b * e->dx + c * e->dy) * dq;",
+     "term[1] = 2.0 * (b * e->dx + c * e->dy) * dq;"),
+    ("dconic_b_factor", "term[3] = 2.0 * e->dx * e->dy * dq;", "term[3] = e->dx * e->dy * dq;"),
+    ("conic_c_from_factor", "c = l12 * l12 + l22 * l22;", "c = l22 * l22;"),
+    ("clamp_gate_dropped", "if (!e->clamped) {", "if (1) {"),
+    ("dcolour_factor", "term[6 + ch] = w * G[ch];", "term[6 + ch] = e->alpha * G[ch];"),
+    # ---- projection backward (chain rule)
+    ("dP00_sign", "double dP00 = ga * (-P11 * P11 / det2) + gb * (P01 * P11 / det2) +",
+     "double dP00 = ga * (-P11 * P11 / det2) + gb * (-P01 * P11 / det2) +"),
+    ("dP01_sign", "gb * (-1.0 / det - 2.0 * P01 * P01 / det2)",
+     "gb * (1.0 / det - 2.0 * P01 * P01 / det2)"),
+    ("dT_operand",
+     "S[3 * r + 2] * Tm[1][2];\n            dT[0][r] = 2.0 * dP00 * ST0 + dP01 * ST1;",
+     "S[3 * r + 2] * Tm[1][2];\n            dT[0][r] = 2.0 * dP00 * ST0 + dP01 * ST0;"),
+    ("dJ_index", "dj02 += dT[0][k] * V[8 + k];", "dj02 += dT[0][k] * V[k];"),
+    ("dt_second_derivative", "dt[2] += dj02 * (2.0 * fx * tx / tz3);",
+     "dt[2] += dj02 * (fx * tx / tz3);"),
+    ("dt_mean_sign", "dt[2] += gmx * (-fx * tx / tz2);", "dt[2] += gmx * (fx * tx / tz2);"),
+    ("dmeans_transposed", "dm[c] += V[c] * dt[0] + V[4 + c] * dt[1] + V[8 + c] * dt[2];",
+     "dm[c] += V[4 * c] * dt[0] + V[4 * c + 1] * dt[1] + V[4 * c + 2] * dt[2];"),
+    ("dM_not_symmetrised", "acc += (dS[3 * r + j] + dS[3 * j + r]) * M[3 * j + k];",
+     "acc += 2.0 * dS[3 * r + j] * M[3 * j + k];"),
+    ("dscale_transposed", "ds[k] += dM[3 * r + k] * R[3 * r + k];",
+     "ds[k] += dM[3 * r + k] * R[3 * k + r];"),
+    ("dquat_sign_w", "dw += dR[1] * (-2 * z);", "dw += dR[1] * (2 * z);"),
+    ("dquat_sign_x", "dx += dR[5] * (-2 * w);", "dx += dR[5] * (2 * w);"),
+    ("dquat_not_projected", "dq[k] = (dqh[k] - qh[k] * dotq) / qn;", "dq[k] = dqh[k] / qn;"),
+    ("dopacity_scaled", "dopac[i] = g2[5];", "dopac[i] = 0.5 * g2[5];"),
+    ("dsh_channel", "dshi[3 * k + ch] = Y[k] * gcol[ch];", "dshi[3 * k + ch] = Y[k] * gcol[0];"),
+    ("dmeans_sh_not_projected", "dm[j] += (gd[j] - dhat[j] * dotd) / len;",
+     "dm[j] += gd[j] / len;"),
+    # ---- chunking policy (Eq. 6)
+    ("policy_chunk_cost_k", "double cost = fmax(total + lambda * (double)h * k, Kl) + beta * Kl;",
+     "double cost = fmax(total + lambda * (double)h, Kl) + beta * Kl;"),
+    ("policy_margin_dropped", "!(best <= (1.0 - eps) * base)", "!(best <= base)"),
+    ("policy_next_tile_ignored", "double l = fmax(N1 / k, next);", "double l = N1 / k;"),
+    ("policy_next_index", "double next = h < nt ? (double)counts_desc[h] : 0.0;",
+     "double next = h < nt ? (double)counts_desc[h - 1] : 0.0;"),
+    # ---- raw gradients and Adam
+    ("adam_second_moment", "v[i] = b2 * v[i] + (1.0 - b2) * g[i] * g[i];",
+     "v[i] = b2 * v[i] + (1.0 - b2) * g[i];"),
+    ("adam_bias_correction", "p[i] -= lr * (m[i] / c1) / (sqrt(v[i] / c2) + eps);",
+     "p[i] -= lr * m[i] / (sqrt(v[i]) + eps);"),
+    ("raw_logit_factor", "dlogits[i] = opac[i] * (1.0 - opac[i]) * dopac[i];",
+     "dlogits[i] = opac[i] * dopac[i];"),
+    ("raw_log_scale_factor", "dlog_scales[i] = scales[i] * dscales[i];",
+     "dlog_scales[i] = dscales[i];"),
+    # ---- L1 + SSIM loss
+    ("ssim_variance_term", "double vx = exx - mx * mx,", "double vx = exx,"),
+    ("ssim_dmu_sign", "dmu[i] = (2.0 * my * (A2 - A1) - 2.0 * mx * s * (B2 - B1)) / D;",
+     "dmu[i] = (2.0 * my * (A2 - A1) + 2.0 * mx * s * (B2 - B1)) / D;"),
+    ("ssim_dxx_sign", "dxx[i] = -s / B2;", "dxx[i] = s / B2;"),
+    ("ssim_chain_factor", "ds += w * (dmu[q] + 2.0 * xv * dxx[q] + yv * dxy[q]);",
+     "ds += w * (dmu[q] + xv * dxx[q] + yv * dxy[q]);"),
+    ("ssim_window_width", "g[k + SSIM_R] = exp(-(double)(k * k) / (2.0 * sigma * sigma));",
+     "g[k + SSIM_R] = exp(-(double)(k * k) / (sigma * sigma));"),
+    ("l1_sign", "double sg = xv > yv ? 1.0 : (xv < yv ? -1.0 : 0.0);", "double sg = 1.0;"),
+]
+
+
+def _source() -> str:
+    with open(SRC) as f:
+        return f.read()
+
+
+def test_mutant_table_matches_the_source():
+    src = _source()
+    names = [m[0] for m in MUTANTS]
+    assert len(set(names)) == len(names)
+    for name, old, new in MUTANTS:
+        assert src.count(old) == 1, f"{name}: planted text must occur exactly once"
+        assert old != new, name
+
+
+def _copy_tree(dst: str) -> None:
+    os.makedirs(os.path.join(dst, "oracle"))
+    for f in ("__init__.py", "definitional.py", "gs_oracle.c"):
+        shutil.copy(os.path.join(ROOT, "oracle", f), os.path.join(dst, "oracle", f))
+    for f in ("synthetic_scenes.py", "pytest.ini"):
+        shutil.copy(os.path.join(ROOT, f), os.path.join(dst, f))
+    os.makedirs(os.path.join(dst, "tests"))
+    for f in os.listdir(os.path.join(ROOT, "tests")):
+        if f == "conftest.py" or (f.startswith("test_oracle_") and f.endswith(".py")):
+            shutil.copy(os.path.join(ROOT, "tests", f), os.path.join(dst, "tests", f))
+    shutil.copytree(os.path.join(ROOT, "tests", "golden"), os.path.join(dst, "tests", "golden"))
+
+
+@pytest.mark.skipif(os.environ.get("GS_ORACLE_MUTANTS") != "1",
+                    reason="mutation run is opt-in: GS_ORACLE_MUTANTS=1")
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_every_mutant_fails_a_pin(tmp_path, name, old, new):
+    dst = str(tmp_path / "copy")
+    _copy_tree(dst)
+    path = os.path.join(dst, "oracle", "gs_oracle.c")
+    with open(path) as f:
+        src = f.read()
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    env = dict(os.environ, PYTHONPATH=dst, PYTHONDONTWRITEBYTECODE="1")
+    env.pop("GS_ORACLE_MUTANTS")
+    # the mutant must build: a planted mistake, not a syntax error
+    b = subprocess.run([sys.executable, "-c", "import oracle; oracle.build(force=True)"],
+                       cwd=dst, env=env, capture_output=True, text=True, timeout=300)
+    assert b.returncode == 0, f"{name} does not compile:\n{b.stderr[-2000:]}"
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:xdist", "tests"],
+                       cwd=dst, env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 1, (
+        f"mutant {name} survived every pin (pytest exit {r.returncode}):\n{r.stdout[-1500:]}")

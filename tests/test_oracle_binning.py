@@ -179,3 +179,23 @@ def test_completeness_for_ground_splats_under_the_camera():
         need = set(np.unique(tile_of[q <= np.float32(r[6])]).tolist())
         assert need <= set(oracle.splat_tiles(cam, r).tolist()), g
     assert thin > 50 and far > 200, (thin, far)
+
+
+def test_equal_depths_are_listed_by_ascending_id():
+    """Splats at exactly the same depth keep ascending Gaussian id within each tile: the id
+    is the tie-break of the (tile, depth, id) order, which a stable depth sort of the
+    id-ordered splats followed by a stable tile sort gives (Kopanas, Step 1 (d))."""
+    rng = np.random.default_rng(7)
+    sc, cam = ss.random_scene(rng, 300, 64, 48, sh_degree=0, log_scale=(-2.0, 0.3))
+    # the identity camera makes each depth t_z equal to the mean's z: all exactly 3
+    sc.means[:, 2] = np.float32(3.0)
+    proj = oracle.project(sc, cam)
+    assert np.all(proj.splat[proj.visible, 7] == 3.0)
+    b = oracle.bin_sort(cam, proj, None)
+    crowded = 0
+    for t in range(len(b.counts)):
+        s, e = b.ranges[t]
+        ids = b.ids[s:e]
+        assert np.all(np.diff(ids) > 0), t
+        crowded += len(ids) >= 5
+    assert crowded >= 10  # of the 12 tiles

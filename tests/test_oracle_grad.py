@@ -40,19 +40,14 @@ def _loss_from_records(cam, proj, b, w, v):
     return float((w * im.img).sum() + (v * im.T).sum()), im
 
 
-@pytest.mark.parametrize("seed", [0, 1])
-def test_screen_space_gradients_match_finite_differences(seed):
-    sc, cam, w, v = _scene(seed)
-    proj = oracle.project(sc, cam, V64)
-    b = oracle.bin_sort(cam, proj, None, V64)
-    _, im0 = _loss_from_records(cam, proj, b, w, v)
-    g2, _ = oracle.blend_bwd(cam, proj, b, w, v, V64)
-    gs = np.nonzero(np.abs(g2).sum(1) > 0)[0]
-    assert len(gs) >= 10
+def _fd_screen_space(cam, proj, b, w, v, im0, g2, splats):
+    """Central differences of the loss in each record entry of the given splats, against
+    the analytic nine derivatives; returns the number of entries checked (an entry is
+    skipped when a perturbation changes a hit or stop decision)."""
     # record columns: 0 mux, 1 muy, 2 a, 3 b, 4 c, 5 opacity; rgb separately
     cols = [(0, 0), (1, 1), (2, 2), (3, 3), (4, 4), (5, 5)]
     checked = 0
-    for g in gs[:15]:
+    for g in splats:
         for col, gi in cols + [("rgb", 6), ("rgb", 7), ("rgb", 8)]:
             p_hi, p_lo = copy.deepcopy(proj), copy.deepcopy(proj)
             if col == "rgb":
@@ -77,7 +72,60 @@ def test_screen_space_gradients_match_finite_differences(seed):
             fd = (L1 - L2) / (2 * h)
             assert abs(g2[g, gi] - fd) <= 1e-6 + 2e-6 * abs(fd), (g, gi, g2[g, gi], fd)
             checked += 1
-    assert checked >= 100
+    return checked
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_screen_space_gradients_match_finite_differences(seed):
+    sc, cam, w, v = _scene(seed)
+    proj = oracle.project(sc, cam, V64)
+    b = oracle.bin_sort(cam, proj, None, V64)
+    _, im0 = _loss_from_records(cam, proj, b, w, v)
+    g2, _ = oracle.blend_bwd(cam, proj, b, w, v, V64)
+    gs = np.nonzero(np.abs(g2).sum(1) > 0)[0]
+    assert len(gs) >= 10
+    assert _fd_screen_space(cam, proj, b, w, v, im0, g2, gs[:15]) >= 100
+
+
+def _front_clamped(cam, proj):
+    """Splats whose alpha reaches the 0.99 clamp at a pixel where they are the front-most
+    hit (so they blend there at T = 1), from the records' conics in numpy."""
+    ys, xs = np.mgrid[0:cam.height, 0:cam.width]
+    px, py = xs + 0.5, ys + 0.5
+    front = np.full((cam.height, cam.width), np.inf)
+    who = np.full((cam.height, cam.width), -1)
+    raw = np.zeros((cam.height, cam.width))
+    for g in np.nonzero(proj.visible)[0]:
+        mx, my, a, bb, c, o, tau, z = proj.splat[g, :8]
+        dx, dy = px - mx, py - my
+        q = a * dx * dx + 2 * bb * dx * dy + c * dy * dy
+        hit = (q <= tau) & (z < front)
+        front[hit], who[hit], raw[hit] = z, g, o * np.exp(-0.5 * q[hit])
+    return np.unique(who[(who >= 0) & (raw > 0.99 * (1 + 1e-4))])
+
+
+def test_clamped_alphas_carry_no_geometry_or_opacity_gradient():
+    """Where o exp(-q/2) exceeds 0.99 the alpha is the constant 0.99, so that pixel adds
+    nothing to the derivatives of the splat's mean, conic and opacity; only its colour
+    term remains. Large splats of opacity 0.995-0.999 are clamped near their centres,
+    and central differences, which see the clamp, must agree with the backward."""
+    for seed in range(20, 40):
+        rng = np.random.default_rng(seed)
+        sc, cam, w, v = _scene(seed, n=10)
+        sc.scales *= np.float32(4.0)
+        sc.opacities[:] = rng.uniform(0.995, 0.999, sc.n).astype(np.float32)
+        proj = oracle.project(sc, cam, V64)
+        b = oracle.bin_sort(cam, proj, None, V64)
+        _, im0 = _loss_from_records(cam, proj, b, w, v)
+        if np.any(im0.flags & 2):  # an alpha within rounding of the clamp: resample
+            continue
+        clamped = _front_clamped(cam, proj)
+        if len(clamped) >= 3:
+            break
+    else:
+        pytest.fail("no scene with clamped splats and no alpha near the clamp")
+    g2, _ = oracle.blend_bwd(cam, proj, b, w, v, V64)
+    assert _fd_screen_space(cam, proj, b, w, v, im0, g2, clamped[:6]) >= 25
 
 
 def _perturbed(sc, field, idx, delta):

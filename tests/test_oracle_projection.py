@@ -193,3 +193,28 @@ def test_sh_degree0_is_constant_colour():
     v = p.visible
     # degree-0 colour = Y_00 s_0 with Y_00 = 1 / (2 sqrt(pi))
     np.testing.assert_allclose(p.rgb[v], sc.sh[v, 0, :] / (2 * np.sqrt(np.pi)), rtol=1e-6)
+
+
+def test_colour_follows_the_direction_from_the_camera_centre():
+    """A camera placed at C and turned by R has the view matrix [R | -R C]. Each colour is
+    then sum_k Y_k(d) s_k with d the unit vector from C to the mean (Kopanas, Step 3),
+    here built from C itself rather than recovered from the view matrix."""
+    rng = np.random.default_rng(11)
+    sc, cam = ss.random_scene(rng, 60, 64, 48, sh_degree=3)
+    R = Rotation.random(random_state=5).as_matrix()
+    C = np.array([0.7, -1.3, 2.1])
+    means_cam = sc.means.astype(np.float64)
+    sc.means = (means_cam @ R + C).astype(np.float32)  # world = R^T m_cam + C
+    V = np.eye(4)
+    V[:3, :3] = R
+    V[:3, 3] = -R @ C
+    cam = ss.pinhole(V.astype(np.float32), cam.fx, cam.width, cam.height)
+    proj = oracle.project(sc, cam)
+    vis = proj.visible
+    assert vis.sum() >= 30
+    d = sc.means.astype(np.float64) - C
+    d /= np.linalg.norm(d, axis=1, keepdims=True)
+    Y, _ = oracle.sh_basis(d)
+    expect = np.einsum("nk,nkc->nc", Y, sc.sh.astype(np.float64))
+    np.testing.assert_allclose(proj.rgb[vis], expect[vis], rtol=1e-5, atol=1e-6)
+    assert np.all(proj.rgb[~vis] == 0)
