@@ -196,6 +196,18 @@ def test_radix_path_full_parity(seed, W, H, n, deg):
     _full_parity(sc, cam, w, capacity=RADIX_CAPACITY)
 
 
+@pytest.mark.parametrize("capacity", [None, RADIX_CAPACITY], ids=["buckets", "radix"])
+def test_equal_depths_full_parity(capacity):
+    # every splat at exactly the same depth (identity camera, z = 3): only the id
+    # tie-break orders each tile's list, and overlapping splats blend in id order
+    rng = np.random.default_rng(9)
+    sc, cam = ss.random_scene(rng, 800, 100, 70, sh_degree=1, log_scale=(-2.6, 0.6),
+                              logit_std=2.0)
+    sc.means[:, 2] = np.float32(3.0)
+    w = rng.standard_normal((70, 100, 3))
+    _full_parity(sc, cam, w, capacity=capacity)
+
+
 def test_radix_and_bucket_paths_agree():
     sc, cam = ss.make_config(2)
     a = run_forward(sc, cam)
