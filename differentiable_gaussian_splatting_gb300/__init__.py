@@ -28,7 +28,9 @@ __all__ = [
     "gs_project", "gs_bin_sort", "gs_rasterize_fwd", "gs_rasterize_bwd", "gs_project_bwd",
     "gs_project_sh16", "gs_project_bwd_sh16", "gs_project_bwd_adam", "AdamSettings",
     "gs_loss_l1_ssim", "gs_loss_workspace_bytes", "LossSettings",
-    "gs_raster_stats", "gs_default_settings", "Camera", "Settings", "Rasterizer", "library",
+    "gs_bin_sort_workspace_bytes", "gs_raster_workspace_bytes", "gs_bin_sort_noalloc",
+    "gs_raster_stats", "gs_default_settings", "gs_status_string", "gs_num_tiles",
+    "Camera", "Settings", "Rasterizer", "library",
     "GSError", "TILE", "GRAD2D", "SPLAT_FLOATS",
 ]
 
@@ -219,6 +221,16 @@ def _settings(settings) -> Settings:
 
 def gs_default_settings() -> Settings:
     return library().gs_default_settings()
+
+
+def gs_status_string(status: int) -> str:
+    """The library's text for a gs_status code."""
+    return library().gs_status_string(int(status)).decode()
+
+
+def gs_num_tiles(width: int, height: int) -> int:
+    """Number of 16 x 16 tiles covering a width x height image (0 for an empty image)."""
+    return int(library().gs_num_tiles(int(width), int(height)))
 
 
 def _f32():

@@ -38,9 +38,11 @@ def test_every_declared_symbol_is_exported(lib):
 def test_python_binding_has_the_c_names():
     import differentiable_gaussian_splatting_gb300 as gs
 
-    for name in ("gs_project", "gs_bin_sort", "gs_rasterize_fwd", "gs_rasterize_bwd",
-                 "gs_project_bwd"):
-        assert callable(getattr(gs, name))
+    for name in _declared():
+        assert callable(getattr(gs, name, None)), name
+        assert name in gs.__all__, name
+    assert gs.gs_num_tiles(1297, 840) == 82 * 53 and gs.gs_num_tiles(0, 5) == 0
+    assert gs.gs_status_string(3) == gs.STATUS[3]
 
 
 def test_host_queries(lib):
