@@ -98,3 +98,20 @@ def test_profile_traffic_only_while_sources_match(tmp_path, monkeypatch):
     (csrc / "gs_raster.cu").write_text("// changed since the capture\n")
     assert bench.profiled_traffic("gs_rasterize_bwd") is None
     assert bench.profiled_traffic("gs_bin_sort") is None  # several kernels: no single profile
+
+
+def test_l2_note_and_workload_config_follow_the_scene():
+    import synthetic_scenes as ss
+
+    small, _ = ss.make_config(1)
+    big, _ = ss.make_config(3, n=300_000)  # 70.8 MB of parameters
+    assert bench.l2_note(small, "gradients", 1).startswith("inputs smaller than L2")
+    # 2 x 70.8 MB of parameters and gradients exceed the 129 MB L2; 1 x alone would not
+    assert bench.l2_note(big, "gradients", 1).startswith("inputs larger than L2 (70.8 MB")
+    assert bench.l2_note(big, "moments", 2).endswith("+ 142 MB moments)")
+    args = SimpleNamespace(config=1, sh_bf16=False)
+    cfg = bench.workload_config(args, small, 128, 128, 5713, "single")
+    assert cfg["workload"] == ss.CONFIG_NAMES[1] and cfg["tile_pairs"] == 5713
+    assert cfg["gaussians"] == small.n and cfg["image"] == "128x128"
+    assert bench.workload_config(SimpleNamespace(config=1, sh_bf16=True), small, 128, 128, 5713,
+                                 "single")["sh_storage"] == "bf16"
