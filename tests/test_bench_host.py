@@ -115,3 +115,24 @@ def test_l2_note_and_workload_config_follow_the_scene():
     assert cfg["gaussians"] == small.n and cfg["image"] == "128x128"
     assert bench.workload_config(SimpleNamespace(config=1, sh_bf16=True), small, 128, 128, 5713,
                                  "single")["sh_storage"] == "bf16"
+
+
+def test_clock_summary_reads_nvidia_smi_lines():
+    """The clocks record of a bench line: median SM clock under load, the maximum, and every
+    throttle reason seen Active in any sample (lines as nvidia-smi prints them with
+    --format=csv,noheader,nounits); unreadable or short lines are skipped."""
+    s = bench.ClockSampler(0)
+    s.lines = [
+        "2070, 2070, 812.50, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "1980, 2070, 1395.10, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "2055, 2070, 990.00, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "[N/A], [N/A], [N/A], [N/A], [N/A], [N/A], [N/A], [N/A]",
+        "2070, 2070",
+    ]
+    out = s.summary()
+    assert out == {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
+                   "samples": 3}
+    s.lines = ["1500, 2070, 700.0, 0x88, Active, Not Active, Active, Not Active"]
+    assert s.summary()["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+    s.lines = []
+    assert s.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
