@@ -281,7 +281,9 @@ def gs_bin_sort_workspace_bytes(n, capacity, width, height) -> int:
 
 def gs_bin_sort(cam, n, splats, depths, tiles_touched, workspace, sorted_ids, capacity,
                 tile_ranges, lpt_order, counts_device=None, sync_pairs=True, stream=None):
-    """Two-stage radix sort into (tile, depth, id) order; returns I when sync_pairs."""
+    """Tile binning and sort into (tile, depth, id) order, with tile ranges and LPT order
+    (per-tile buckets below 8 Mi pairs of capacity, a two-stage radix sort from there);
+    returns the pair count I when sync_pairs (GSError status 3 names the count needed)."""
     import torch
 
     cam_c = Camera.of(cam)

@@ -161,3 +161,15 @@ def test_adam_arguments_are_checked_on_the_host(lib):
     assert call(good, n=-1) == 1
     empty = gs.AdamMoments()
     assert call(good, moments=empty) == 1  # null moment pointers
+
+
+def test_capacity_error_carries_the_pairs_needed():
+    """A pair list too short for the view raises GSError status 3 naming the pairs needed,
+    which the Rasterizer reads to re-allocate before it retries the sort."""
+    import differentiable_gaussian_splatting_gb300 as gs
+
+    with pytest.raises(gs.GSError) as e:
+        gs._check("gs_bin_sort", 3, "; pairs needed: 1234567")
+    assert e.value.status == 3
+    assert gs.Rasterizer._needed(e.value) == 1234567
+    gs._check("gs_bin_sort", 0)  # GS_OK raises nothing
