@@ -129,6 +129,8 @@ gs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GS_OK : GS_ERR_
 
 namespace gs {
 
+bool camera_valid(const gs_camera* cam) { return camera_ok(cam); }
+
 gs_status bin_sort_entry(const gs_camera* cam, int64_t n, const float* splats,
                          const float* depths, const int32_t* tiles_touched, void* workspace,
                          size_t workspace_bytes, int32_t* sorted_ids, int64_t capacity,
@@ -230,7 +232,8 @@ const char* gs_status_string(gs_status status) {
 
 int64_t gs_num_tiles(int32_t width, int32_t height) {
     if (width < 1 || height < 1) return 0;
-    return (int64_t)((width + GS_TILE - 1) / GS_TILE) * ((height + GS_TILE - 1) / GS_TILE);
+    // in 64 bits: width + 15 overflows int32 for widths near INT32_MAX
+    return (((int64_t)width + GS_TILE - 1) / GS_TILE) * (((int64_t)height + GS_TILE - 1) / GS_TILE);
 }
 
 gs_status gs_project(const gs_camera* cam, int64_t n, int32_t sh_degree, const float* means,

@@ -119,6 +119,10 @@ struct SideStream {
     cudaEvent_t fork, fork2, join, join2;
 };
 
+// the camera checks every call makes (finite matrix and intrinsics, image
+// sides 1..32768, znear > 0)
+bool camera_valid(const gs_camera* cam);
+
 // gs_bin_sort with its argument checks; overlap = false keeps every launch in
 // order on the caller's stream and creates no side stream.
 gs_status bin_sort_entry(const gs_camera* cam, int64_t n, const float* splats,

@@ -8,44 +8,37 @@
 // here instead, in one statically sized device array that every GPU which
 // loads this library holds until the process exits.
 //
-// The first call on a device looks up the array's device address (with that
-// device current) and caches it; make that first call before any stream
-// capture.  All calls share the array and it keeps the previous call's
+// Every call looks up the array's device address on the current device (a
+// host-side lookup; the first one on a device may load the library's device
+// code there, so make the first call on each device before any stream
+// capture).  All calls share the array and it keeps the previous call's
 // contents: the sort clears what must start at zero itself, and calls whose
 // work overlaps on the GPU (other streams, other threads) race on it.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "../../include/gs.h"
 #include "gs_internal.h"
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(6) << 20;  // 6 MiB
+// The limits below need 6,619,648 bytes of scratch when all three are at
+// their maximum (the layout grows with each of them); 7 MiB leaves a margin.
+constexpr size_t kScratchBytes = size_t(7) << 20;  // 7 MiB
 constexpr int64_t kMaxGaussians = int64_t(1) << 16;
 constexpr int64_t kMaxCapacity = int64_t(1) << 18;
 constexpr int64_t kMaxTiles = int64_t(1) << 14;
 
 __device__ __align__(256) char g_scratch[kScratchBytes];
 
-std::mutex g_mu;
-void* g_addr[64];
-
-// Device address of g_scratch on the current device (looked up once per device).
+// Device address of g_scratch in the current device's context.  It is looked
+// up on every call, not cached: a cached address would go stale if the
+// context were destroyed and recreated (cudaDeviceReset) while the library
+// stays loaded.
 cudaError_t scratch_address(void** out) {
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
+    void* p = nullptr;
+    const cudaError_t err = cudaGetSymbolAddress(&p, g_scratch);
     if (err != cudaSuccess) return err;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_addr[dev]) {
-        void* p = nullptr;
-        err = cudaGetSymbolAddress(&p, g_scratch);
-        if (err != cudaSuccess) return err;
-        g_addr[dev] = p;
-    }
-    *out = g_addr[dev];
+    *out = p;
     return cudaSuccess;
 }
 
@@ -57,8 +50,7 @@ extern "C" gs_status gs_bin_sort_noalloc(const gs_camera* cam, int64_t n, const 
                                          int32_t* tile_ranges, int32_t* lpt_order,
                                          int64_t* counts_device, int64_t* n_pairs_host,
                                          void* stream) {
-    if (!cam || cam->width < 1 || cam->height < 1 || n < 0 || capacity < 1)
-        return GS_ERR_INVALID_ARG;
+    if (!gs::camera_valid(cam) || n < 0 || capacity < 1) return GS_ERR_INVALID_ARG;
     // sizes the fixed scratch cannot hold: a caller error, reported before any GPU work
     const int64_t nt = gs_num_tiles(cam->width, cam->height);
     if (n > kMaxGaussians || capacity > kMaxCapacity || nt > kMaxTiles) return GS_ERR_WORKSPACE;

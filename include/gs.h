@@ -383,7 +383,7 @@ gs_status gs_loss_l1_ssim(int32_t width, int32_t height, const float* image, con
  * of the GPU's memory (a plugin inside an application with its own
  * allocator) or that cannot afford the synchronisation an allocation may
  * cause.  Arguments, outputs and results are those of gs_bin_sort, minus
- * the workspace: the scratch is one fixed 6 MiB device array inside this
+ * the workspace: the scratch is one fixed 7 MiB device array inside this
  * library (held on every device the library is loaded on until the process
  * exits), so the call allocates nothing.
  *
@@ -391,8 +391,9 @@ gs_status gs_loss_l1_ssim(int32_t width, int32_t height, const float* image, con
  * tiles (2048 x 2048 pixels); larger sizes return GS_ERR_WORKSPACE before
  * anything is enqueued.  Use gs_bin_sort for more.
  *
- * The first call on a device looks up the array's address with that device
- * current; make it before capturing the stream into a graph.  The array
+ * Every call looks up the array's address with the calling thread's current
+ * device; the first call on a device may load the library's device code
+ * there, so make it before capturing the stream into a graph.  The array
  * keeps the previous call's contents (the sort clears what must start at
  * zero itself), and it is shared: calls whose GPU work overlaps (different
  * streams or host threads without ordering between them) race on it and

@@ -12,6 +12,7 @@ import pytest
 import synthetic_scenes as ss
 
 LIMIT_N, LIMIT_CAP = 1 << 16, 1 << 18
+SCRATCH_BYTES = 7 << 20  # the library's fixed scratch array
 
 
 def _cam(width=64, height=64):
@@ -40,6 +41,18 @@ def test_sizes_beyond_the_fixed_scratch_are_rejected_on_the_host():
     assert call(_cam(), 1000, 0) == 1
     assert call(_cam(0, 64), 1000, 1000) == 1
     assert call(_cam(), -1, 1000) == 1
+    # the camera is checked before the sizes: a width far beyond the image limit is an
+    # invalid argument, not a size the scratch cannot hold
+    assert call(_cam(2_000_000_000, 64), 1000, 1000) == 1
+
+
+def test_every_limit_at_once_fits_the_fixed_scratch():
+    import differentiable_gaussian_splatting_gb300 as gs
+
+    # 2048 x 2048 is 16384 tiles, the tile limit; the layout grows with each size
+    need = gs.gs_bin_sort_workspace_bytes(LIMIT_N, LIMIT_CAP, 2048, 2048)
+    assert 0 < need <= SCRATCH_BYTES
+    assert gs.gs_bin_sort_workspace_bytes(LIMIT_N, LIMIT_CAP, 16384, 256) <= SCRATCH_BYTES
 
 
 def _project(sc, cam):
@@ -121,6 +134,23 @@ def test_noalloc_sort_matches_gs_bin_sort_on_consecutive_calls():
         got = _sort_noalloc(cam, n, splats, depths, tt, cap)
         torch.cuda.synchronize()
         assert 0 < got[0] <= cap
+        _same(want, got)
+
+
+@pytest.mark.gpu
+def test_noalloc_sort_with_every_limit_at_its_maximum():
+    import torch
+
+    # 65536 Gaussians, a 262144-pair capacity and 16384 tiles in one call (about 161k
+    # pairs), twice in a row
+    rng = np.random.default_rng(14)
+    sc, cam = ss.random_scene(rng, LIMIT_N, 2048, 2048, sh_degree=0, log_scale=(-6.0, 0.5))
+    splats, depths, tt = _project(sc, cam)
+    for _ in range(2):
+        want = _sort_with_workspace(cam, sc.n, splats, depths, tt, LIMIT_CAP)
+        got = _sort_noalloc(cam, sc.n, splats, depths, tt, LIMIT_CAP)
+        torch.cuda.synchronize()
+        assert 100_000 < got[0] <= LIMIT_CAP
         _same(want, got)
 
 
