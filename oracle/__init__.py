@@ -96,7 +96,10 @@ def _declare(lib: C.CDLL) -> None:
                             _P, _P, _P, _P, _P, _I64]
     lib.ora_bin.restype = _I64
     lib.ora_blend.argtypes = [_I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+    lib.ora_blend2.argtypes = [_I32, _I32, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P]
     lib.ora_blend_bwd.argtypes = [_I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+    lib.ora_blend_bwd2.argtypes = [_I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                   _P]
     lib.ora_project_bwd.argtypes = [_I64, _I32, _P, _P, _I32, _I32, C.c_float,
                                     _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
     lib.ora_project_bwd_mag.argtypes = [_I64, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -247,8 +250,20 @@ def _pixel_mask(cam, sel: np.ndarray | None) -> np.ndarray:
     return np.repeat(np.repeat(m, TILE, 0), TILE, 1)[:H, :W]
 
 
-def blend(cam, proj: Projection, b: Binning, variant: str = "f32") -> Image:
-    """Front-to-back blending of the selected tiles (Ryu & Yoo Eq. 2-3)."""
+RULE = -(1 << 31)  # stop_last entry: apply the stop rule at this pixel
+FLAG_NOT_ADMISSIBLE = 4
+
+
+def blend(cam, proj: Projection, b: Binning, variant: str = "f32",
+          stop_last: np.ndarray | None = None, clamp_flip: bool = False) -> Image:
+    """Front-to-back blending of the selected tiles (Ryu & Yoo Eq. 2-3).
+
+    The other admissible outcomes of fp32 near-ties: stop_last [H, W] int32 holds, per
+    pixel, RULE (apply the 1e-4 stop rule) or the list position of the last splat a
+    renderer blended (-1 for none); that pixel then blends every hit up to it and its
+    flags get FLAG_NOT_ADMISSIBLE when the stop rule does not admit the outcome.
+    clamp_flip takes the other decision at every alpha within the band of the 0.99
+    clamp (FLAG_CLAMP_TIE pixels)."""
     lib = _lib(variant)
     W, H = int(cam.width), int(cam.height)
     img = np.zeros((H, W, 3), np.float64)
@@ -256,9 +271,19 @@ def blend(cam, proj: Projection, b: Binning, variant: str = "f32") -> Image:
     nc = np.zeros((H, W), np.int32)
     last = np.full((H, W), -1, np.int32)
     flags = np.zeros((H, W), np.uint8)
-    lib.ora_blend(W, H, _p(proj.splat), _p(proj.rgb), _p(b.ranges), _p(b.sel_off), _p(b.ids),
-                  _p(b.sel), _p(img), _p(T), _p(nc), _p(last), _p(flags))
+    sl = None if stop_last is None else np.ascontiguousarray(stop_last, np.int32).reshape(H, W)
+    lib.ora_blend2(W, H, _p(proj.splat), _p(proj.rgb), _p(b.ranges), _p(b.sel_off), _p(b.ids),
+                   _p(b.sel), _p(sl), int(bool(clamp_flip)), _p(img), _p(T), _p(nc), _p(last),
+                   _p(flags))
     return Image(img, T, nc, last, flags, _pixel_mask(cam, b.sel))
+
+
+@dataclass
+class BlendGrads:
+    grad2d: np.ndarray  # [N, 9] (mux, muy, a, b, c, opacity, r, g, b)
+    gabs: np.ndarray    # [N, 9] magnitude: every term in absolute value, down to the inputs
+    grho: np.ndarray    # [N, 9] the terms' magnitudes weighted by their pixel's fp32 error bound
+    galt: np.ndarray    # [N, 9] spread of the admissible results at clamp near-ties
 
 
 def blend_bwd(cam, proj: Projection, b: Binning, dL_dimg: np.ndarray,
@@ -266,18 +291,87 @@ def blend_bwd(cam, proj: Projection, b: Binning, dL_dimg: np.ndarray,
     """Nine screen-space derivatives per splat, summed over the selected tiles.
 
     Returns (grad2d [N, 9], gmag [N, 9]) with columns (mux, muy, a, b, c, opacity, r, g, b);
-    gmag is the magnitude of what each element sums (every product and every addend of
-    dL/dalpha in absolute value); it equals |grad2d| when nothing cancels."""
+    gmag is the magnitude of what each element sums (every product and every addend, down
+    to the inputs, in absolute value); it equals |grad2d| when nothing cancels."""
+    r = blend_bwd_bounds(cam, proj, b, dL_dimg, dL_dT, variant=variant)
+    return r.grad2d, r.gabs
+
+
+def blend_bwd_bounds(cam, proj: Projection, b: Binning, dL_dimg: np.ndarray,
+                     dL_dT: np.ndarray | None = None, stop_last: np.ndarray | None = None,
+                     variant: str = "f32") -> BlendGrads:
+    """blend_bwd with the outcome a renderer took at stop near-ties (stop_last as for
+    blend) and the quantities that bound an fp32 evaluation's error (BlendGrads)."""
     lib = _lib(variant)
     W, H = int(cam.width), int(cam.height)
     n = int(proj.splat.shape[0])
-    g = np.zeros((n, 9), np.float64)
-    ga = np.zeros((n, 9), np.float64)
+    out = BlendGrads(*(np.zeros((n, 9), np.float64) for _ in range(4)))
     dimg = np.ascontiguousarray(dL_dimg, dtype=np.float64).reshape(H, W, 3)
     dT = None if dL_dT is None else np.ascontiguousarray(dL_dT, dtype=np.float64).reshape(H, W)
-    lib.ora_blend_bwd(W, H, _p(proj.splat), _p(proj.rgb), _p(b.ranges), _p(b.sel_off), _p(b.ids),
-                      _p(b.sel), _p(dimg), _p(dT), _p(g), _p(ga))
-    return g, ga
+    sl = None if stop_last is None else np.ascontiguousarray(stop_last, np.int32).reshape(H, W)
+    lib.ora_blend_bwd2(W, H, _p(proj.splat), _p(proj.rgb), _p(b.ranges), _p(b.sel_off),
+                       _p(b.ids), _p(b.sel), _p(sl), _p(dimg), _p(dT), _p(out.grad2d),
+                       _p(out.gabs), _p(out.grho), _p(out.galt))
+    return out
+
+
+# --------------------------------------------------------------------------
+# the same calls over disjoint tile sets on several host threads
+# --------------------------------------------------------------------------
+def tile_parts(b: Binning, parts: int) -> list[Binning]:
+    """Split the selected tiles of b into up to `parts` disjoint sets of similar pair
+    counts (largest tiles first, each to the lightest set).  Each part is b with its own
+    selection mask: the calls below then blend only that part's tiles."""
+    tiles = np.nonzero(b.sel)[0] if b.sel is not None else np.arange(len(b.counts))
+    parts = max(1, min(int(parts), len(tiles)))
+    order = tiles[np.argsort(-b.counts[tiles], kind="stable")]
+    load = np.zeros(parts)
+    masks = np.zeros((parts, len(b.counts)), np.uint8)
+    for t in order:
+        j = int(np.argmin(load))
+        masks[j, t] = 1
+        load[j] += 256 + b.counts[t]
+    return [Binning(b.counts, b.ranges, b.lpt_order, m, b.sel_off, b.ids) for m in masks]
+
+
+def _threads(fn, items, workers):
+    from concurrent.futures import ThreadPoolExecutor
+
+    # the C calls release the GIL (ctypes), so the parts run on separate cores
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        return list(ex.map(fn, items))
+
+
+def blend_parallel(cam, proj: Projection, b: Binning, workers: int | None = None,
+                   stop_last: np.ndarray | None = None, clamp_flip: bool = False) -> Image:
+    """blend() of b's tiles split over `workers` host threads; every pixel's result comes
+    from the one part that holds its tile, so the outputs equal blend()'s."""
+    workers = workers or os.cpu_count() or 1
+    outs = _threads(lambda p: blend(cam, proj, p, stop_last=stop_last, clamp_flip=clamp_flip),
+                    tile_parts(b, workers), workers)
+    res = outs[0]
+    for o in outs[1:]:
+        m = o.tile_mask
+        for f in ("img", "T", "n_contrib", "last_idx", "flags"):
+            getattr(res, f)[m] = getattr(o, f)[m]
+        res.tile_mask = res.tile_mask | m
+    return res
+
+
+def blend_bwd_parallel(cam, proj: Projection, b: Binning, dL_dimg: np.ndarray,
+                       dL_dT: np.ndarray | None = None, stop_last: np.ndarray | None = None,
+                       workers: int | None = None) -> BlendGrads:
+    """blend_bwd_bounds() of b's tiles split over `workers` host threads; each part's
+    per-Gaussian sums (float64) are added, so the result equals the single call's up to
+    the order of those additions."""
+    workers = workers or os.cpu_count() or 1
+    outs = _threads(lambda p: blend_bwd_bounds(cam, proj, p, dL_dimg, dL_dT, stop_last),
+                    tile_parts(b, workers), workers)
+    res = outs[0]
+    for o in outs[1:]:
+        for f in ("grad2d", "gabs", "grho", "galt"):
+            getattr(res, f).__iadd__(getattr(o, f))
+    return res
 
 
 @dataclass

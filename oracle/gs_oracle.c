@@ -604,8 +604,22 @@ int64_t ora_bin(int64_t n, const float* viewmat, const float* intr, int W, int H
  * The relative error of T after k blends is then bounded by
  * sum_j (E_ALPHA alpha_j / (1 - alpha_j) + 2^-23); a decision is flagged when
  * T is within twice that bound of 1e-4.
+ *
+ * The other admissible outcomes of such near-ties are rendered on request:
+ *   stop_last (may be NULL): per pixel ORA_RULE to apply the stop rule, or the
+ *     list position of the last splat a renderer blended (-1 for none).  The
+ *     pixel then blends every hit up to that position and stops, and flags
+ *     bit 2 is set when the stop rule does not admit that outcome: a hit
+ *     blended after T fell below 1e-4 outside the band, a stop before a hit
+ *     with T at or above 1e-4 outside the band, or a position that is not a
+ *     hit of the list.
+ *   clamp_flip: nonzero takes the other clamp decision at every splat whose
+ *     alpha lies within the band of 0.99 (bit 1): alpha = 0.99 where the rule
+ *     leaves it unclamped, the unclamped o exp(-q/2) where the rule clamps.
  */
 #define E_ALPHA 7.62939453125e-06 /* 2^-17 */
+#define ORA_RULE INT32_MIN
+#define U32 5.9604644775390625e-08 /* 2^-24, unit roundoff of fp32 */
 
 typedef struct {
     int W, H, ntx;
@@ -632,47 +646,128 @@ static int hit_test(const double* rec, int px, int py, dreal* q_out, double* dx_
     return q <= tau;
 }
 
-void ora_blend(int W, int H, const double* splat, const double* rgb, const int64_t* ranges,
-               const int64_t* sel_off, const int32_t* ids, const uint8_t* sel, double* img,
-               double* T_final, int32_t* n_contrib, int32_t* last_idx, uint8_t* flags) {
+/* alpha of a hit with the clamp decision; *near_clamp: alpha within the band */
+static double alpha_of(const double* rec, double q, int clamp_flip, int* clamped,
+                       int* near_clamp, double* araw_out) {
+    double araw = rec[5] * exp(-0.5 * q);
+    int near = fabs(araw - ALPHA_MAX) <= 2.0 * E_ALPHA * ALPHA_MAX;
+    int c = !(araw < ALPHA_MAX);
+    if (clamp_flip && near) c = !c;
+    *clamped = c;
+    *near_clamp = near;
+    *araw_out = araw;
+    return c ? ALPHA_MAX : araw;
+}
+
+/* One blended splat of a pixel (front to back), as the backward needs it. */
+typedef struct {
+    int32_t g;
+    int64_t k;
+    double alpha, araw, T, dx, dy, q;
+    int clamped, near_clamp;
+} blended_t;
+
+/*
+ * The splats a pixel blends, front to back, under the stop rule or the forced
+ * outcome stop (ORA_RULE or a list position); returns their number, grows
+ * *list as needed, writes the final transmittance and the flags (bits as
+ * ora_blend's) and the fp32 band err of the stop decisions.
+ */
+static int64_t pixel_blend(const blend_ctx_t* c, int64_t t, int px, int py, int32_t stop,
+                           int clamp_flip, blended_t** list, int64_t* cap, double* T_out,
+                           uint8_t* flags_out) {
+    int64_t s0 = c->ranges[2 * t], s1 = c->ranges[2 * t + 1];
+    int forced = stop != ORA_RULE;
+    double T = 1.0, err = 0;
+    int64_t nb = 0, last = -1;
+    uint8_t fl = 0;
+    for (int64_t k = s0; k < s1; ++k) {
+        int near = fabs(T - T_MIN) <= 2.0 * err * T;
+        if (near) fl |= 1;
+        if (!forced && T < T_MIN) break;
+        int32_t g = c->ids[c->sel_off[t] + (k - s0)];
+        const double* rec = c->splat + REC * (int64_t)g;
+        dreal q;
+        double dx, dy;
+        if (!hit_test(rec, px, py, &q, &dx, &dy)) continue;
+        if (forced) {
+            if (k > (int64_t)stop) {
+                if (!(T < T_MIN || near)) fl |= 4; /* stopped before a hit the rule blends */
+                break;
+            }
+            if (T < T_MIN && !near) fl |= 4; /* blended past a stop outside the band */
+        }
+        int clamped, near_clamp;
+        double araw;
+        double alpha = alpha_of(rec, (double)q, clamp_flip, &clamped, &near_clamp, &araw);
+        if (near_clamp) fl |= 2;
+        if (nb == *cap) {
+            *cap *= 2;
+            *list = (blended_t*)realloc(*list, sizeof(blended_t) * (size_t)*cap);
+        }
+        blended_t* e = &(*list)[nb++];
+        e->g = g;
+        e->k = k;
+        e->alpha = alpha;
+        e->araw = araw;
+        e->T = T;
+        e->dx = dx;
+        e->dy = dy;
+        e->q = (double)q;
+        e->clamped = clamped;
+        e->near_clamp = near_clamp;
+        T *= (1.0 - alpha);
+        err += E_ALPHA * alpha / (1.0 - alpha) + 1.1920928955078125e-07;
+        last = k;
+    }
+    if (forced && last != (int64_t)stop) fl |= 4; /* the given position is not a blended hit */
+    *T_out = T;
+    *flags_out = fl;
+    return nb;
+}
+
+void ora_blend2(int W, int H, const double* splat, const double* rgb, const int64_t* ranges,
+                const int64_t* sel_off, const int32_t* ids, const uint8_t* sel,
+                const int32_t* stop_last, int clamp_flip, double* img, double* T_final,
+                int32_t* n_contrib, int32_t* last_idx, uint8_t* flags) {
     int ntx = (W + TILE - 1) / TILE, nty = (H + TILE - 1) / TILE;
+    blend_ctx_t c = {W, H, ntx, splat, rgb, ranges, sel_off, ids};
+    int64_t cap = 64;
+    blended_t* list = (blended_t*)malloc(sizeof(blended_t) * (size_t)cap);
     for (int ty = 0; ty < nty; ++ty)
         for (int tx = 0; tx < ntx; ++tx) {
             int64_t t = (int64_t)ty * ntx + tx;
             if (sel && !sel[t]) continue;
-            int64_t s0 = ranges[2 * t], s1 = ranges[2 * t + 1];
             for (int py = ty * TILE; py < ty * TILE + TILE && py < H; ++py)
                 for (int px = tx * TILE; px < tx * TILE + TILE && px < W; ++px) {
-                    double T = 1.0, C[3] = {0, 0, 0}, err = 0;
-                    int32_t n = 0, last = -1;
-                    uint8_t fl = 0;
-                    for (int64_t k = s0; k < s1; ++k) {
-                        if (fabs(T - T_MIN) <= 2.0 * err * T) fl |= 1;
-                        if (T < T_MIN) break;
-                        int32_t g = ids[sel_off[t] + (k - s0)];
-                        const double* rec = splat + REC * (int64_t)g;
-                        dreal q;
-                        double dx, dy;
-                        if (!hit_test(rec, px, py, &q, &dx, &dy)) continue;
-                        double araw = rec[5] * exp(-0.5 * (double)q);
-                        if (fabs(araw - ALPHA_MAX) <= 2.0 * E_ALPHA * ALPHA_MAX) fl |= 2;
-                        double alpha = araw < ALPHA_MAX ? araw : ALPHA_MAX;
-                        for (int ch = 0; ch < 3; ++ch) C[ch] += rgb[3 * (int64_t)g + ch] * alpha * T;
-                        T *= (1.0 - alpha);
-                        err += E_ALPHA * alpha / (1.0 - alpha) + 1.1920928955078125e-07;
-                        n++;
-                        last = (int32_t)k;
-                    }
                     int64_t p = (int64_t)py * W + px;
+                    double T;
+                    uint8_t fl;
+                    int32_t stop = stop_last ? stop_last[p] : ORA_RULE;
+                    int64_t nb = pixel_blend(&c, t, px, py, stop, clamp_flip, &list, &cap, &T, &fl);
+                    double C[3] = {0, 0, 0};
+                    for (int64_t j = 0; j < nb; ++j) {
+                        const blended_t* e = &list[j];
+                        for (int ch = 0; ch < 3; ++ch)
+                            C[ch] += rgb[3 * (int64_t)e->g + ch] * e->alpha * e->T;
+                    }
                     img[3 * p] = C[0];
                     img[3 * p + 1] = C[1];
                     img[3 * p + 2] = C[2];
                     T_final[p] = T;
-                    n_contrib[p] = n;
-                    last_idx[p] = last;
+                    n_contrib[p] = (int32_t)nb;
+                    last_idx[p] = nb ? (int32_t)list[nb - 1].k : -1;
                     flags[p] = fl;
                 }
         }
+    free(list);
+}
+
+void ora_blend(int W, int H, const double* splat, const double* rgb, const int64_t* ranges,
+               const int64_t* sel_off, const int32_t* ids, const uint8_t* sel, double* img,
+               double* T_final, int32_t* n_contrib, int32_t* last_idx, uint8_t* flags) {
+    ora_blend2(W, H, splat, rgb, ranges, sel_off, ids, sel, NULL, 0, img, T_final, n_contrib,
+               last_idx, flags);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -689,117 +784,155 @@ void ora_blend(int W, int H, const double* splat, const double* rgb, const int64
  *   dL/dmux = -2 (a dx + b dy) dL/dq,  dL/dmuy = -2 (b dx + c dy) dL/dq,
  *   dL/da = dx^2 dL/dq,  dL/db = 2 dx dy dL/dq,  dL/dc = dy^2 dL/dq.
  * grad2d[g][0..8] = (mux, muy, a, b, c, opacity, r, g, b), accumulated in
- * double over every selected tile.  gabs[g][0..8] accumulates the magnitude
- * of each term: the same product with every factor, and every addend of
- * dL/dalpha (T_k |c.G|, sum_{j>k} |c_j.G| alpha_j T_j / (1 - alpha_k),
- * |gT| T_final / (1 - alpha_k)), taken in absolute value.  It bounds the sum
- * of absolute values of what a floating-point evaluation adds up, and equals
- * |grad2d| when nothing cancels.
+ * double over every selected tile.
+ *
+ * Magnitudes (the scale of an fp32 evaluation's error), all optional:
+ *   gabs[g][r]: every term above evaluated with each input replaced by its
+ *     absolute value and every difference by a sum, down to the inputs (the
+ *     dot products c . G and B . G as sums over channels of |c_ch G_ch|); it
+ *     bounds the sum of absolute values of everything an evaluation adds and
+ *     equals |grad2d| when nothing cancels.
+ *   grho[g][r]: the same terms, each weighted by the relative error bound
+ *     eps_p of its pixel's fp32 evaluation,
+ *       eps_p = 2 sum_j (E_ALPHA alpha_j / (1 - alpha_j) + 8 u) + 2 E_ALPHA + 32 u,
+ *     u = 2^-24, over the pixel's blended splats j: the transmittance in
+ *     front of a splat and the colour behind it carry each alpha's error
+ *     amplified by 1 / (1 - alpha) and a few roundings per blend (forward
+ *     products, backward division and running sums); alpha itself (and the
+ *     opacity it is divided by) carries E_ALPHA; a term's own products a few
+ *     roundings.
+ *   galt[g][r]: the spread of the admissible results at near-ties of the
+ *     clamp: per pixel with an alpha in the band of 0.99 (ora_blend's bit 1),
+ *     |terms with every such clamp decision taken the other way - terms as the
+ *     rule takes them|, summed.
+ * stop_last: as for ora_blend2 (NULL or per pixel ORA_RULE / a forced last
+ *   position): the backward of the outcome a renderer took at a stop near-tie.
  */
-typedef struct {
-    int32_t g;
-    int64_t k;
-    double alpha, araw, T, dx, dy, q;
-    int clamped;
-} blended_t;
+static void pixel_terms(const blend_ctx_t* c, const blended_t* list, int64_t nb, double Tfin,
+                        const double G[3], double gT, double* term, double* mag) {
+    double behind[3] = {0, 0, 0};
+    double behind_mag = 0;
+    for (int64_t j = nb - 1; j >= 0; --j) {
+        const blended_t* e = &list[j];
+        const double* rec = c->splat + REC * (int64_t)e->g;
+        const double* col = c->rgb + 3 * (int64_t)e->g;
+        double* tm = term + 9 * j;
+        double* mg = mag + 9 * j;
+        for (int r = 0; r < 9; ++r) tm[r] = mg[r] = 0;
+        double w = e->alpha * e->T;
+        for (int ch = 0; ch < 3; ++ch) {
+            tm[6 + ch] = w * G[ch];
+            mg[6 + ch] = fabs(tm[6 + ch]);
+        }
+        double cG = col[0] * G[0] + col[1] * G[1] + col[2] * G[2];
+        double cG_mag = fabs(col[0] * G[0]) + fabs(col[1] * G[1]) + fabs(col[2] * G[2]);
+        double bG = behind[0] * G[0] + behind[1] * G[1] + behind[2] * G[2];
+        double dalpha = e->T * cG - bG / (1.0 - e->alpha) - gT * Tfin / (1.0 - e->alpha);
+        double dalpha_mag = e->T * cG_mag + behind_mag / (1.0 - e->alpha) +
+                            fabs(gT) * Tfin / (1.0 - e->alpha);
+        for (int ch = 0; ch < 3; ++ch) behind[ch] += col[ch] * w;
+        behind_mag += cG_mag * w;
+        if (!e->clamped) {
+            double dq = -0.5 * e->alpha * dalpha;
+            /* conic of the evaluated quadratic: a = l11^2, b = l11 l12,
+             * c = l12^2 + l22^2 */
+            double l11 = rec[13], l12 = rec[14], l22 = rec[15];
+            double a = l11 * l11, b = l11 * l12, cc = l12 * l12 + l22 * l22;
+            tm[5] = exp(-0.5 * e->q) * dalpha;
+            tm[0] = -2.0 * (a * e->dx + b * e->dy) * dq;
+            tm[1] = -2.0 * (b * e->dx + cc * e->dy) * dq;
+            tm[2] = e->dx * e->dx * dq;
+            tm[3] = 2.0 * e->dx * e->dy * dq;
+            tm[4] = e->dy * e->dy * dq;
+            double dq_mag = 0.5 * e->alpha * dalpha_mag;
+            mg[5] = exp(-0.5 * e->q) * dalpha_mag;
+            mg[0] = 2.0 * (fabs(a * e->dx) + fabs(b * e->dy)) * dq_mag;
+            mg[1] = 2.0 * (fabs(b * e->dx) + fabs(cc * e->dy)) * dq_mag;
+            mg[2] = e->dx * e->dx * dq_mag;
+            mg[3] = 2.0 * fabs(e->dx * e->dy) * dq_mag;
+            mg[4] = e->dy * e->dy * dq_mag;
+        }
+    }
+}
 
-void ora_blend_bwd(int W, int H, const double* splat, const double* rgb, const int64_t* ranges,
-                   const int64_t* sel_off, const int32_t* ids, const uint8_t* sel,
-                   const double* dL_dimg, const double* dL_dT, double* grad2d, double* gabs) {
+void ora_blend_bwd2(int W, int H, const double* splat, const double* rgb, const int64_t* ranges,
+                    const int64_t* sel_off, const int32_t* ids, const uint8_t* sel,
+                    const int32_t* stop_last, const double* dL_dimg, const double* dL_dT,
+                    double* grad2d, double* gabs, double* grho, double* galt) {
     int ntx = (W + TILE - 1) / TILE, nty = (H + TILE - 1) / TILE;
-    int64_t cap = 64;
+    blend_ctx_t c = {W, H, ntx, splat, rgb, ranges, sel_off, ids};
+    int64_t cap = 64, tcap = 0;
     blended_t* list = (blended_t*)malloc(sizeof(blended_t) * (size_t)cap);
+    double *term = NULL, *mag = NULL, *term2 = NULL, *mag2 = NULL;
     for (int ty = 0; ty < nty; ++ty)
         for (int tx = 0; tx < ntx; ++tx) {
             int64_t t = (int64_t)ty * ntx + tx;
             if (sel && !sel[t]) continue;
-            int64_t s0 = ranges[2 * t], s1 = ranges[2 * t + 1];
             for (int py = ty * TILE; py < ty * TILE + TILE && py < H; ++py)
                 for (int px = tx * TILE; px < tx * TILE + TILE && px < W; ++px) {
-                    /* forward recomputation */
-                    double T = 1.0;
-                    int64_t nb = 0;
-                    for (int64_t k = s0; k < s1; ++k) {
-                        if (T < T_MIN) break;
-                        int32_t g = ids[sel_off[t] + (k - s0)];
-                        const double* rec = splat + REC * (int64_t)g;
-                        dreal q;
-                        double dx, dy;
-                        if (!hit_test(rec, px, py, &q, &dx, &dy)) continue;
-                        double araw = rec[5] * exp(-0.5 * (double)q);
-                        double alpha = araw < ALPHA_MAX ? araw : ALPHA_MAX;
-                        if (nb == cap) {
-                            cap *= 2;
-                            list = (blended_t*)realloc(list, sizeof(blended_t) * (size_t)cap);
-                        }
-                        blended_t* e = &list[nb++];
-                        e->g = g;
-                        e->k = k;
-                        e->alpha = alpha;
-                        e->araw = araw;
-                        e->T = T;
-                        e->dx = dx;
-                        e->dy = dy;
-                        e->q = (double)q;
-                        e->clamped = !(araw < ALPHA_MAX);
-                        T *= (1.0 - alpha);
-                    }
                     int64_t p = (int64_t)py * W + px;
+                    double Tfin;
+                    uint8_t fl;
+                    int32_t stop = stop_last ? stop_last[p] : ORA_RULE;
+                    int64_t nb = pixel_blend(&c, t, px, py, stop, 0, &list, &cap, &Tfin, &fl);
+                    if (nb == 0) continue;
+                    if (nb > tcap) {
+                        tcap = cap;
+                        term = (double*)realloc(term, sizeof(double) * 9 * (size_t)tcap);
+                        mag = (double*)realloc(mag, sizeof(double) * 9 * (size_t)tcap);
+                        term2 = (double*)realloc(term2, sizeof(double) * 9 * (size_t)tcap);
+                        mag2 = (double*)realloc(mag2, sizeof(double) * 9 * (size_t)tcap);
+                    }
                     double G[3] = {dL_dimg[3 * p], dL_dimg[3 * p + 1], dL_dimg[3 * p + 2]};
                     double gT = dL_dT ? dL_dT[p] : 0.0;
-                    double Tfin = T;
-                    double behind[3] = {0, 0, 0};
-                    double behind_abs = 0;
-                    for (int64_t j = nb - 1; j >= 0; --j) {
-                        blended_t* e = &list[j];
-                        const double* rec = splat + REC * (int64_t)e->g;
-                        const double* col = rgb + 3 * (int64_t)e->g;
-                        double* gr = grad2d + 9 * (int64_t)e->g;
-                        double* ga = gabs + 9 * (int64_t)e->g;
-                        double term[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
-                        double mag[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
-                        double w = e->alpha * e->T;
-                        for (int ch = 0; ch < 3; ++ch) {
-                            term[6 + ch] = w * G[ch];
-                            mag[6 + ch] = fabs(term[6 + ch]);
-                        }
-                        double cG = col[0] * G[0] + col[1] * G[1] + col[2] * G[2];
-                        double bG = behind[0] * G[0] + behind[1] * G[1] + behind[2] * G[2];
-                        double dalpha = e->T * cG - bG / (1.0 - e->alpha) -
-                                        gT * Tfin / (1.0 - e->alpha);
-                        double dalpha_mag = e->T * fabs(cG) + behind_abs / (1.0 - e->alpha) +
-                                            fabs(gT) * Tfin / (1.0 - e->alpha);
-                        for (int ch = 0; ch < 3; ++ch) behind[ch] += col[ch] * w;
-                        behind_abs += fabs(cG) * w;
-                        if (!e->clamped) {
-                            double dq = -0.5 * e->alpha * dalpha;
-                            /* conic of the evaluated quadratic: a = l11^2,
-                             * b = l11 l12, c = l12^2 + l22^2 */
-                            double l11 = rec[13], l12 = rec[14], l22 = rec[15];
-                            double a = l11 * l11, b = l11 * l12, c = l12 * l12 + l22 * l22;
-                            term[5] = exp(-0.5 * e->q) * dalpha;
-                            term[0] = -2.0 * (a * e->dx + b * e->dy) * dq;
-                            term[1] = -2.0 * (b * e->dx + c * e->dy) * dq;
-                            term[2] = e->dx * e->dx * dq;
-                            term[3] = 2.0 * e->dx * e->dy * dq;
-                            term[4] = e->dy * e->dy * dq;
-                            double dq_mag = 0.5 * e->alpha * dalpha_mag;
-                            double u1 = fabs(l11 * e->dx) + fabs(l12 * e->dy);
-                            mag[5] = exp(-0.5 * e->q) * dalpha_mag;
-                            mag[0] = 2.0 * fabs(l11) * u1 * dq_mag;
-                            mag[1] = 2.0 * (fabs(l12) * u1 + l22 * l22 * fabs(e->dy)) * dq_mag;
-                            mag[2] = e->dx * e->dx * dq_mag;
-                            mag[3] = 2.0 * fabs(e->dx * e->dy) * dq_mag;
-                            mag[4] = e->dy * e->dy * dq_mag;
-                        }
+                    pixel_terms(&c, list, nb, Tfin, G, gT, term, mag);
+                    double eps = 2.0 * E_ALPHA + 32.0 * U32;
+                    int any_near_clamp = 0;
+                    for (int64_t j = 0; j < nb; ++j) {
+                        eps += 2.0 * (E_ALPHA * list[j].alpha / (1.0 - list[j].alpha) + 8.0 * U32);
+                        any_near_clamp |= list[j].near_clamp;
+                    }
+                    for (int64_t j = 0; j < nb; ++j) {
+                        int64_t g = list[j].g;
                         for (int r = 0; r < 9; ++r) {
-                            gr[r] += term[r];
-                            ga[r] += mag[r];
+                            grad2d[9 * g + r] += term[9 * j + r];
+                            if (gabs) gabs[9 * g + r] += mag[9 * j + r];
+                            if (grho) grho[9 * g + r] += eps * mag[9 * j + r];
+                        }
+                    }
+                    if (galt && any_near_clamp) {
+                        /* the same splats with every near-tie clamp decision flipped */
+                        double T = 1.0;
+                        for (int64_t j = 0; j < nb; ++j) {
+                            blended_t* e = &list[j];
+                            if (e->near_clamp) {
+                                e->clamped = !e->clamped;
+                                e->alpha = e->clamped ? ALPHA_MAX : e->araw;
+                            }
+                            e->T = T;
+                            T *= (1.0 - e->alpha);
+                        }
+                        pixel_terms(&c, list, nb, T, G, gT, term2, mag2);
+                        for (int64_t j = 0; j < nb; ++j) {
+                            int64_t g = list[j].g;
+                            for (int r = 0; r < 9; ++r)
+                                galt[9 * g + r] += fabs(term2[9 * j + r] - term[9 * j + r]);
                         }
                     }
                 }
         }
     free(list);
+    free(term);
+    free(mag);
+    free(term2);
+    free(mag2);
+}
+
+void ora_blend_bwd(int W, int H, const double* splat, const double* rgb, const int64_t* ranges,
+                   const int64_t* sel_off, const int32_t* ids, const uint8_t* sel,
+                   const double* dL_dimg, const double* dL_dT, double* grad2d, double* gabs) {
+    ora_blend_bwd2(W, H, splat, rgb, ranges, sel_off, ids, sel, NULL, dL_dimg, dL_dT, grad2d, gabs,
+                   NULL, NULL);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -82,18 +82,17 @@ MUTANTS += [
     ("pixel_centre_dropped", "dreal dx = ((dreal)px + (dreal)0.5) - mux;",
      "dreal dx = ((dreal)px) - mux;"),
     ("quadratic_form_term", "dreal q = fma(u1, u1, u2 * u2);", "dreal q = fma(u1, u1, u2);"),
-    ("termination_threshold",
-     "if (fabs(T - T_MIN) <= 2.0 * err * T) fl |= 1;\n                        if (T < T_MIN) break;",
-     "if (fabs(T - T_MIN) <= 2.0 * err * T) fl |= 1;\n                        if (T < 1e-3) break;"),
-    ("alpha_clamp_dropped",
-     "double alpha = araw < ALPHA_MAX ? araw : ALPHA_MAX;\n                        for (int ch",
-     "double alpha = araw;\n                        for (int ch"),
-    ("colour_without_transmittance", "C[ch] += rgb[3 * (int64_t)g + ch] * alpha * T;",
-     "C[ch] += rgb[3 * (int64_t)g + ch] * alpha;"),
-    ("transmittance_update", "T *= (1.0 - alpha);\n                        err +=",
-     "T *= (1.0 - alpha) * (1.0 - alpha);\n                        err +="),
-    ("contributors_not_counted", "                        n++;\n", ""),
-    ("last_index_relative", "last = (int32_t)k;", "last = (int32_t)(k - s0);"),
+    ("termination_threshold", "if (!forced && T < T_MIN) break;",
+     "if (!forced && T < 1e-3) break;"),
+    ("alpha_clamp_dropped", "return c ? ALPHA_MAX : araw;", "return araw;"),
+    ("colour_without_transmittance",
+     "C[ch] += rgb[3 * (int64_t)e->g + ch] * e->alpha * e->T;",
+     "C[ch] += rgb[3 * (int64_t)e->g + ch] * e->alpha;"),
+    ("transmittance_update", "T *= (1.0 - alpha);\n        err +=",
+     "T *= (1.0 - alpha) * (1.0 - alpha);\n        err +="),
+    ("contributors_not_counted", "n_contrib[p] = (int32_t)nb;", "n_contrib[p] = 0;"),
+    ("last_index_relative", "last_idx[p] = nb ? (int32_t)list[nb - 1].k : -1;",
+     "last_idx[p] = nb ? (int32_t)(list[nb - 1].k - ranges[2 * t]) : -1;"),
     # ---- backward of the blend: the nine screen-space derivatives
     ("dalpha_behind_sign", "double dalpha = e->T * cG - bG / (1.0 - e->alpha) -",
      "double dalpha = e->T * cG + bG / (1.0 - e->alpha) -"),
@@ -101,15 +100,30 @@ MUTANTS += [
     ("behind_without_transmittance", "behind[ch] += col[ch] * w;",
      "behind[ch] += col[ch] * e->alpha;"),
     ("dq_alpha_dropped", "double dq = -0.5 * e->alpha * dalpha;", "double dq = -0.5 * dalpha;"),
-    ("dopacity_factor", "term[5] = exp(-0.5 * e->q) * dalpha;", "term[5] = e->alpha * dalpha;"),
-    ("dmux_conic_index", "term[0] = -2.0 * (a * e->dx + b * e->dy) * dq;",
-     "term[0] = -2.0 * (a * e->dx + c * e->dy) * dq;"),
-    ("dmuy_sign", "term[1] = -2.0 * (b * e->dx + c * e->dy) * dq;",
-     "term[1] = 2.0 * (b * e->dx + c * e->dy) * dq;"),
-    ("dconic_b_factor", "term[3] = 2.0 * e->dx * e->dy * dq;", "term[3] = e->dx * e->dy * dq;"),
-    ("conic_c_from_factor", "c = l12 * l12 + l22 * l22;", "c = l22 * l22;"),
+    ("dopacity_factor", "tm[5] = exp(-0.5 * e->q) * dalpha;", "tm[5] = e->alpha * dalpha;"),
+    ("dmux_conic_index", "tm[0] = -2.0 * (a * e->dx + b * e->dy) * dq;",
+     "tm[0] = -2.0 * (a * e->dx + cc * e->dy) * dq;"),
+    ("dmuy_sign", "tm[1] = -2.0 * (b * e->dx + cc * e->dy) * dq;",
+     "tm[1] = 2.0 * (b * e->dx + cc * e->dy) * dq;"),
+    ("dconic_b_factor", "tm[3] = 2.0 * e->dx * e->dy * dq;", "tm[3] = e->dx * e->dy * dq;"),
+    ("conic_c_from_factor", "cc = l12 * l12 + l22 * l22;", "cc = l22 * l22;"),
     ("clamp_gate_dropped", "if (!e->clamped) {", "if (1) {"),
-    ("dcolour_factor", "term[6 + ch] = w * G[ch];", "term[6 + ch] = e->alpha * G[ch];"),
+    ("dcolour_factor", "tm[6 + ch] = w * G[ch];", "tm[6 + ch] = e->alpha * G[ch];"),
+    # ---- magnitudes and error bounds that set the GPU gradient tolerance
+    ("magnitude_behind_doubled", "behind_mag += cG_mag * w;", "behind_mag += 2.0 * cG_mag * w;"),
+    ("magnitude_conic_b_factor", "mg[3] = 2.0 * fabs(e->dx * e->dy) * dq_mag;",
+     "mg[3] = 4.0 * fabs(e->dx * e->dy) * dq_mag;"),
+    ("error_bound_alpha_weight",
+     "eps += 2.0 * (E_ALPHA * list[j].alpha / (1.0 - list[j].alpha) + 8.0 * U32);",
+     "eps += 2.0 * (E_ALPHA / (1.0 - list[j].alpha) + 8.0 * U32);"),
+    ("clamp_spread_not_a_difference",
+     "galt[9 * g + r] += fabs(term2[9 * j + r] - term[9 * j + r]);",
+     "galt[9 * g + r] += fabs(term2[9 * j + r]) + fabs(term[9 * j + r]);"),
+    ("forced_stop_not_checked", "if (T < T_MIN && !near) fl |= 4;", "if (0) fl |= 4;"),
+    ("param_magnitude_quat_doubled", "double dw = 2 * (az * dR[1] + ay * dR[2]",
+     "double dw = 4 * (az * dR[1] + ay * dR[2]"),
+    ("param_magnitude_view_dir", "dm[j] += (gd[j] + ad[j] * dotd) / len;",
+     "dm[j] += (2.0 * gd[j] + ad[j] * dotd) / len;"),
     # ---- projection backward (chain rule)
     ("dP00_sign", "double dP00 = ga * (-P11 * P11 / det2) + gb * (P01 * P11 / det2) +",
      "double dP00 = ga * (-P11 * P11 / det2) + gb * (-P01 * P11 / det2) +"),
