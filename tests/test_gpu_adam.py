@@ -1,14 +1,16 @@
 """The chain rule fused with one Adam step (gs_project_bwd_adam) against the oracle: the
 oracle's parameter gradients carried to the raw parameters (log-scales, opacity logits)
 and its Adam step, from the same parameters and moments.  The gradients are compared
-through the first moment, m_new = b1 m + (1 - b1) g, at the gradient tolerances."""
+through the first moment, m_new = b1 m + (1 - b1) g, at the gradient tolerances (1e-4
+relative, or the derived fp32 bound where that is larger; gpu_util)."""
 
 import numpy as np
 import pytest
 
 import oracle
 import synthetic_scenes as ss
-from gpu_util import GRAD_ATOL, GRAD_RTOL, assert_grads_close, masked_weights, t
+from gpu_util import (GRAD_ATOL, GRAD_RTOL, assert_grads_tiered, grad2d_bounds, param_bounds,
+                      t)
 
 pytestmark = pytest.mark.gpu
 
@@ -39,11 +41,14 @@ def test_fused_adam_step_matches_oracle(seed, W, H, n, deg):
 
     sc, cam, log_s, logit, rng = _raw_scene(seed, W, H, n, deg)
     ref = oracle.render(sc, cam)
-    wm = masked_weights(rng.standard_normal((H, W, 3)), ref.image)
+    wm = rng.standard_normal((H, W, 3)).astype(np.float32)
     # GPU: forward on the activated values, the raster backward, then the fused step
     r = gs.Rasterizer(cam, sc.sh_degree, sc.n)
     r.forward(t(sc.means), t(sc.scales), t(sc.quats), t(sc.opacities), t(sc.sh))
     r.backward(t(wm))
+    # the oracle takes the GPU's stop where the oracle flags it as a fp32 near-tie
+    tie = (ref.image.flags & oracle.FLAG_STOP_TIE) != 0
+    stop_last = np.where(tie, r.last_idx.cpu().numpy(), oracle.RULE).astype(np.int32)
     raw = [sc.means.astype(np.float32), log_s, sc.quats.astype(np.float32), logit,
            sc.sh.astype(np.float32)]
     m0 = [rng.standard_normal(a.shape).astype(np.float32) * 1e-3 for a in raw]
@@ -58,15 +63,18 @@ def test_fused_adam_step_matches_oracle(seed, W, H, n, deg):
                            M, Vv, s, scales_out=act_s, opacities_out=act_o)
     torch.cuda.synchronize()
     # oracle: gradients of the activated parameters, carried to the raw ones, then Adam
-    r2, mag = oracle.blend_bwd(cam, ref.proj, ref.binning, wm, None)
-    pg = oracle.project_bwd(sc, cam, ref.proj, r2)
-    pm = oracle.project_bwd_magnitude(sc, cam, ref.proj, mag)
+    rb, bound = grad2d_bounds(cam, ref.proj, ref.binning, wm, None, stop_last)
+    pg = oracle.project_bwd(sc, cam, ref.proj, rb.grad2d)
+    pb, pm = param_bounds(sc, cam, ref.proj, bound, rb.gabs)
     dls, dlo = oracle.raw_grads(sc.scales, sc.opacities, pg)
-    mls = np.abs(sc.scales.astype(np.float64)) * pm.scales
+    s_abs = np.abs(sc.scales.astype(np.float64))
     o = sc.opacities.astype(np.float64).reshape(-1)
-    mlo = o * (1 - o) * np.abs(pm.opacities.reshape(-1))
     grads = [pg.means, dls, pg.quats, dlo, pg.sh]
-    mags = [pm.means, mls, pm.quats, mlo, pm.sh]
+    mags = [pm.means, s_abs * pm.scales, pm.quats, o * (1 - o) * np.abs(pm.opacities.reshape(-1)),
+            pm.sh]
+    # the raw gradients are exact scalings of the activated ones: so are their bounds
+    bounds = [pb["means"], s_abs * pb["scales"], pb["quats"],
+              o * (1 - o) * pb["opacities"].reshape(-1), pb["sh"]]
     lrs = [LR["lr_means"], LR["lr_scales"], LR["lr_quats"], LR["lr_opacities"]]
     names = ["means", "log_scales", "quats", "logits", "sh"]
     for k in range(5):
@@ -94,8 +102,9 @@ def test_fused_adam_step_matches_oracle(seed, W, H, n, deg):
         v_gpu = Vv[k].cpu().numpy().astype(np.float64)
         # the gradient the step used, read back from the first moment
         g_gpu = (m_gpu - B1 * m0[k].astype(np.float64)) / (1 - B1)
-        assert_grads_close(g_gpu, g, names[k], np.asarray(mags[k]).reshape(g.shape),
-                           rtol=GRAD_RTOL, atol=GRAD_ATOL + 4e-7 * np.abs(m0[k]).max())
+        assert_grads_tiered(g_gpu, g, "adam:" + names[k], np.asarray(bounds[k]).reshape(g.shape),
+                            np.asarray(mags[k]).reshape(g.shape), rtol=GRAD_RTOL,
+                            atol=GRAD_ATOL + 4e-7 * np.abs(m0[k]).max())
         np.testing.assert_allclose(v_gpu, v_ref, rtol=1e-3, atol=1e-12, err_msg=names[k])
         # the step itself: within a thousandth of its rate, plus the parameter's rounding
         lim = 1e-3 * lr_el + 2e-7 * np.maximum(1.0, np.abs(p_ref))
