@@ -18,7 +18,11 @@ constexpr float kTMin = 1e-4f;
 constexpr float kAlphaMax = 0.99f;
 constexpr float kNegHalfLog2e = -0.72134752044448170368f;  // -log2(e) / 2
 constexpr float kPadUnit = 0.00390625f;                     // 2^-8 px
-constexpr float kPadScale = 0.00390625f;                    // 2^-8
+constexpr float kPadScale = 9.5367431640625e-07f;           // 2^-20
+constexpr float kDiscPad = 4.76837158203125e-07f;           // 2^-21 (of tau)
+// the sub-tile mask's approximate square root and reciprocal: a wider margin
+constexpr float kMaskPadScale = 1.52587890625e-05f;         // 2^-16
+constexpr float kMaskDiscPad = 1.9073486328125e-06f;        // 2^-19 (of tau)
 constexpr int kRadiusMax = 1 << 30;
 constexpr int kMaxChunks = 16;  // largest k of the chunking policy
 
@@ -95,15 +99,19 @@ __device__ __forceinline__ Ellipse ellipse_of(const float4& r0, const float4& r1
 // The support ellipse q(d) <= tau has right boundary
 //   x_r(dy) = (sqrt(tau - (l22 dy)^2) - l12 dy) / l11,
 // concave in dy with its vertex at dy = -sqrt(tau) l12 / (l22 h),
-// h = sqrt(l12^2 + l22^2); the left boundary is x_l(dy) = -x_r(-dy).  Bands
-// are widened by pady and extents by padx, pad = 2^-8 px + r 2^-8, so that
-// every pixel whose fp32 hit test passes lies in an emitted tile: near the
-// tips of the ellipse the fp32 boundary is uncertain by about sqrt(u) times
-// the half-width (u = 2^-24), which the r 2^-8 term covers.
+// h = sqrt(l12^2 + l22^2); the left boundary is x_l(dy) = -x_r(-dy).  The
+// fp32 evaluation is widened just enough that every pixel whose fp32 hit test
+// passes lies in an emitted tile (u = 2^-24): the discriminant, whose
+// absolute error of about 4 u tau moves the boundary by about sqrt(u) r near
+// the tips, gets + 2^-21 tau before the root; the other roundings of the span
+// and of the hit test are a few u of the extent, covered by
+// pad = 2^-8 px + r 2^-20 on the extents and bands (the 2^-8 px for the
+// rounding of mu' + x_r in pixel coordinates up to a 32768-pixel image).
 __device__ __forceinline__ float xr_at(const Ellipse& s, float dy) {
     float t = rmul(s.l22, dy);
     float disc = rsub(s.tau, rmul(t, t));
     if (!(disc > 0.f)) disc = 0.f;
+    disc = radd(disc, rmul(s.tau, kDiscPad));
     return rdiv(rsub(rsqrt_exact(disc), rmul(s.l12, dy)), s.l11);
 }
 
@@ -176,8 +184,9 @@ __device__ __forceinline__ float quad_q(float l11, float l12, float l22, float d
 // bit w set if the padded support meets the pixel-centre hull of the 8x4
 // sub-tile of warp w (warp w covers columns 8 (w & 1) .. +7, rows 4 (w >> 1) .. +3
 // of the tile).  It only has to be conservative (every hit pixel of a warp has
-// its bit set), so it uses the SFU's approximate square root and reciprocal:
-// their few-ulp errors are far inside the 2^-8 r pad.
+// its bit set), so it uses the SFU's approximate square root and reciprocal
+// with wider margins than the spans (2^-19 tau on the discriminant, r 2^-16 on
+// the extents): their few-ulp errors are well inside those.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float sqrt_approx(float x) {
     float y;
@@ -194,8 +203,9 @@ __device__ __forceinline__ uint32_t subtile_mask(const Ellipse& s, int tx, int t
     const float inv_l11 = rcp_approx(s.l11);
     const float h = sqrt_approx(fmaf(s.l12, s.l12, s.l22 * s.l22));
     const float dyv = -(sqrt_approx(s.tau) * s.l12) * rcp_approx(s.l22 * h);
-    const float padx = fmaf(s.rx, kPadScale, kPadUnit);
-    const float ryp = s.ry + fmaf(s.ry, kPadScale, kPadUnit);
+    const float padx = fmaf(s.rx, kMaskPadScale, kPadUnit);
+    const float ryp = s.ry + fmaf(s.ry, kMaskPadScale, kPadUnit);
+    const float dpad = s.tau * kMaskDiscPad;
     const float xb = (float)(16 * tx);
     const float xl0 = xb + 0.5f, xl1 = xb + 7.5f;
     const float xr0 = xb + 8.5f;
@@ -212,8 +222,8 @@ __device__ __forceinline__ uint32_t subtile_mask(const Ellipse& s, int tx, int t
         const float dh = fminf(fmaxf(fminf(fmaxf(dyv, lo), hi), -s.ry), s.ry);
         const float dl = fminf(fmaxf(fminf(fmaxf(dyv, -hi), -lo), -s.ry), s.ry);
         const float th = s.l22 * dh, tl = s.l22 * dl;
-        const float xh = (sqrt_approx(fmaxf(fmaf(-th, th, s.tau), 0.f)) - s.l12 * dh) * inv_l11;
-        const float xl = (sqrt_approx(fmaxf(fmaf(-tl, tl, s.tau), 0.f)) - s.l12 * dl) * inv_l11;
+        const float xh = (sqrt_approx(fmaxf(fmaf(-th, th, s.tau), 0.f) + dpad) - s.l12 * dh) * inv_l11;
+        const float xl = (sqrt_approx(fmaxf(fmaf(-tl, tl, s.tau), 0.f) + dpad) - s.l12 * dl) * inv_l11;
         const float Xhi = s.mux + xh + padx, Xlo = s.mux - xl - padx;
         if (Xhi >= xl0 && Xlo <= xl1) m |= 1u << (2 * r);
         if (xr0 <= xr1 && Xhi >= xr0 && Xlo <= xr1) m |= 1u << (2 * r + 1);

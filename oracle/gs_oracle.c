@@ -223,22 +223,32 @@ static void project_one(const camera_t* cam, const float* m3, const float* s3, c
 /* ------------------------------------------------------------------------ */
 /*
  * A tile's region is the closed hull of its pixel centres (x + 0.5, y + 0.5)
- * clipped to the image.  For each tile row, the support ellipse
- * q(d) <= tau, inflated by pad = 2^-8 px + r * 2^-8, is intersected with the
- * row's band and the covered tile columns [tx0, tx1) follow in closed form.
- * With q = (l11 dx + l12 dy)^2 + (l22 dy)^2 the right boundary is
- * x_r(dy) = (sqrt(tau - (l22 dy)^2) - l12 dy) / l11, concave in dy with its
- * vertex at dy = -sqrt(tau) l12 / (l22 h), h = sqrt(l12^2 + l22^2); the left
- * boundary is x_l(dy) = -x_r(-dy).  The band is widened by pady; x_r is
- * evaluated at the band point nearest its vertex, clamped to |dy| <= ry, and
- * the result widened by padx.  Near the ellipse's tips the fp32 boundary is
- * uncertain by about sqrt(u) r (u = 2^-24); the r 2^-8 term covers that.
+ * clipped to the image.  For each tile row, the support ellipse q(d) <= tau is
+ * intersected with the row's band and the covered tile columns [tx0, tx1)
+ * follow in closed form.  With q = (l11 dx + l12 dy)^2 + (l22 dy)^2 the right
+ * boundary is x_r(dy) = (sqrt(tau - (l22 dy)^2) - l12 dy) / l11, concave in
+ * dy with its vertex at dy = -sqrt(tau) l12 / (l22 h), h = sqrt(l12^2 +
+ * l22^2); the left boundary is x_l(dy) = -x_r(-dy).  x_r is evaluated at the
+ * band point nearest its vertex, clamped to |dy| <= ry.
+ *
+ * The fp32 evaluation is widened just enough that every pixel whose fp32 hit
+ * test passes lies in an emitted tile (u = 2^-24):
+ *   - the discriminant tau - (l22 dy)^2 carries an absolute error of about
+ *     4 u tau, which near the tips (discriminant -> 0) moves the boundary by
+ *     about sqrt(u) r; it is widened by 2^-21 tau = 8 u tau before the root,
+ *     so the widening is about sqrt(8 u tau) / l11 at a tip and u-sized
+ *     elsewhere;
+ *   - the remaining roundings of the span and of the hit test's quadratic
+ *     are a few u of the extent: padx = 2^-8 px + rx 2^-20 (and pady alike
+ *     for the band), the 2^-8 px covering the rounding of mu' + x_r in
+ *     pixel coordinates up to the 32768-pixel image limit.
  */
 
 static dreal xr_at(const splat_t* s, dreal dy) {
     dreal t = s->l22 * dy;
     dreal disc = s->tau - t * t;
     if (!(disc > 0)) disc = 0;
+    disc = disc + s->tau * (dreal)4.76837158203125e-07; /* + 2^-21 tau */
     return (sqrt(disc) - s->l12 * dy) / s->l11;
 }
 
@@ -259,8 +269,8 @@ static int to_int_clamped(dreal f, int lo, int hi) {
 
 /* rows [*ty0, *ty1) that the padded ellipse may cover */
 static void row_range(const camera_t* cam, const splat_t* s, int* ty0, int* ty1) {
-    const dreal pad_unit = (dreal)0.00390625;  /* 2^-8 */
-    const dreal pad_scale = (dreal)0.00390625; /* 2^-8 */
+    const dreal pad_unit = (dreal)0.00390625;        /* 2^-8 */
+    const dreal pad_scale = (dreal)9.5367431640625e-07; /* 2^-20 */
     dreal pady = pad_unit + s->ry * pad_scale;
     dreal ryp = s->ry + pady;
     dreal f0 = ceil(((s->muy - ryp) - (dreal)15.5) * (dreal)0.0625);
@@ -271,8 +281,8 @@ static void row_range(const camera_t* cam, const splat_t* s, int* ty0, int* ty1)
 
 /* span of tile columns [*tx0, *tx1) in row ty; returns 0 when empty */
 static int row_span(const camera_t* cam, const splat_t* s, int ty, int* tx0, int* tx1) {
-    const dreal pad_unit = (dreal)0.00390625;  /* 2^-8 */
-    const dreal pad_scale = (dreal)0.00390625; /* 2^-8 */
+    const dreal pad_unit = (dreal)0.00390625;        /* 2^-8 */
+    const dreal pad_scale = (dreal)9.5367431640625e-07; /* 2^-20 */
     dreal padx = pad_unit + s->rx * pad_scale;
     dreal pady = pad_unit + s->ry * pad_scale;
     dreal ryp = s->ry + pady;

@@ -174,7 +174,8 @@ def assert_grads_tiered(gpu, ref, name, bound, mag=None, rtol=GRAD_RTOL, atol=GR
                         max_share=TIER2_MAX_SHARE):
     """|gpu - ref| <= atol + max(rtol |ref|, bound) element by element; the elements that
     pass only under the bound (the second tier) may be at most max_share of them.  The
-    worst err / magnitude is taken over the elements whose error exceeds atol."""
+    worst err / magnitude is taken over the elements whose error exceeds atol, the worst
+    err / |ref| over the second tier with |ref| floored at atol."""
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
     bound = np.broadcast_to(np.asarray(bound, np.float64), ref.shape)
@@ -189,7 +190,7 @@ def assert_grads_tiered(gpu, ref, name, bound, mag=None, rtol=GRAD_RTOL, atol=GR
                              f"{bound.flat[i]:.4g} (|err| / tolerance {(err / lim).flat[i]:.3g})")
     t2 = ~tier1
     st = dict(check=name, kind="elements", n=int(err.size), tier2=int(t2.sum()),
-              worst_rel=float((err / np.maximum(np.abs(ref), 1e-300))[t2].max()) if t2.any() else 0.0,
+              worst_rel=float((err / np.maximum(np.abs(ref), atol))[t2].max()) if t2.any() else 0.0,
               worst_err_over_bound=float((err / np.maximum(bound, 1e-300))[t2].max()) if t2.any()
               else 0.0)
     if mag is not None:
