@@ -13,8 +13,9 @@ Rank 0 prints ONE JSON line.  Under torchrun (N > 1) every rank renders its own
 replica of the view (the path does not shard across GPUs: replicas only), the
 time is the max over ranks and `value` counts the pairs of all ranks.
 
---impl reference times the CPU oracle (oracle/, plain C, one core) on a bounded
-sample of the same workload and prints the same line with "impl": "reference".
+--impl reference times the CPU oracle (oracle/, plain C; its unmodified calls on every
+host core, over disjoint tiles and Gaussians) on the same workload (a bounded sample of
+the larger scenes) and prints the same line with "impl": "reference".
 
 --train-step times a whole training step instead: the same calls with the L1 + SSIM
 loss against a synthetic target between forward and backward (gs_loss_l1_ssim), and
@@ -44,19 +45,25 @@ import synthetic_scenes as ss  # noqa: E402
 METRIC = "raster fwd+bwd ms/iter & tile-Gaussian pairs/s, 1.5M Gaussians @1297×840"
 UNIT = "pairs/s"
 
-# Algorithmic work per contributing pixel-splat pair E (counted from the
-# oracle's scalar formulas, an FMA counted as 2 flops; exponentials and
-# reciprocals run on the SFU and are not counted):
-#   forward : dx, dy 2; A 2; B 2; q 4; exponent 2; clamp 1; w 1; C 6; T 2   = 22
-#   backward: the 13 of the quadratic / exponent / clamp; 1 - alpha 1; T_k 1;
-#             w 1; c.G 5; dL/dalpha 4; colour-behind 2; g 1; nine outputs 20 = 48
-FLOPS_FWD_PER_E = 22
-FLOPS_BWD_PER_E = 48
-FP32_LANES_PER_SM = 128
-# SFU (ex2, rcp) operations per contributing pair: forward ex2; backward ex2 and 1/(1 - alpha)
+# Algorithmic work per contributing pixel-splat pair E, counted from the oracle's scalar
+# formulas.  The roofline is the op model of the hot-path table: fp32 ops (an FMA is one
+# op, one lane-cycle) against SMs x 128 lanes x the SM clock, and SFU ops (ex2, rcp)
+# against SMs x 16 x the clock:
+#   forward : dx, dy 2; the quadratic 5 (u1, u2, q); exponent 1; clamp 1; w 1; C 3; T 1 = 14
+#             fp32 ops + 1 SFU (ex2)
+#   backward: per pixel the quadratic, exponent and clamp 8; 1 - alpha, T_k, w 3; c.G 3;
+#             dL/dalpha 2; colour behind 1; the nine outputs and their sums 23 = 40 fp32
+#             ops + 2 SFU (ex2, 1 / (1 - alpha))
+OPS_FWD_PER_E = 14
+OPS_BWD_PER_E = 40
 SFU_FWD_PER_E = 1
 SFU_BWD_PER_E = 2
+FP32_LANES_PER_SM = 128
 SFU_LANES_PER_SM = 16
+# The same work as flops (an FMA counted as 2; the SFU not counted), reported beside the
+# op model: forward 22, backward 48
+FLOPS_FWD_PER_E = 22
+FLOPS_BWD_PER_E = 48
 # The L1 + SSIM loss per pixel: per channel, the window's 11 taps along rows and then
 # columns for five moments (x, y, x^2, y^2, xy) and again for the three derivative
 # maps of SSIM, 16 x 11 FMA = 352 flops; three channels
@@ -277,6 +284,8 @@ def run_gpu(args):
     launches = kernel_launches(sc.n, r.capacity, W, H)
     step_roof = step_roofline(ms_per_step, sc, M, n_pairs, E, H, W, peaks,
                               props.multi_processor_count, sm_mhz)
+    roof["per_call"] = per_call_fractions(per_call, sc, M, n_pairs, E, H, W, peaks,
+                                          props.multi_processor_count, sm_mhz)
 
     e2e = None if args.no_e2e else run_e2e(gs, r, sc, cam, w, dev, args, n_pairs)
     cpu = None
@@ -305,16 +314,27 @@ def run_gpu(args):
 
 
 def roofline(call, ms, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz):
-    """Algorithmic work of one launch / its average duration, against the binding peak."""
+    """Algorithmic work of one launch / its average duration, against the binding peak.
+    The blend kernels: fp32 ops of the op model against SMs x 128 lanes x the sampled SM
+    clock (Tops/s, reported in the TFLOP/s unit), with the SFU fraction and the flop-model
+    fraction beside it."""
     if call in ("gs_rasterize_fwd", "gs_rasterize_bwd"):
-        per = FLOPS_FWD_PER_E if call == "gs_rasterize_fwd" else FLOPS_BWD_PER_E
-        flops = per * E
-        peak = 2.0 * FP32_LANES_PER_SM * n_sm * sm_mhz * 1e6 / 1e12  # FMA = 2 flops
-        achieved = flops / (ms * 1e-3) / 1e12
+        fwd = call == "gs_rasterize_fwd"
+        ops = (OPS_FWD_PER_E if fwd else OPS_BWD_PER_E) * E
+        sfu = (SFU_FWD_PER_E if fwd else SFU_BWD_PER_E) * E
+        flops = (FLOPS_FWD_PER_E if fwd else FLOPS_BWD_PER_E) * E
+        hz = n_sm * sm_mhz * 1e6
+        peak = FP32_LANES_PER_SM * hz / 1e12
+        achieved = ops / (ms * 1e-3) / 1e12
         return {"kernel": call, "bound": "alu", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": profiled_traffic(call),
-                "peak_source": f"{n_sm} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 x {sm_mhz:.0f} MHz (sampled)",
-                "work": f"{per} flops x {E} contributing pairs"}
+                "peak_source": f"{n_sm} SMs x {FP32_LANES_PER_SM} fp32 lanes x {sm_mhz:.0f} MHz "
+                               f"(sampled), one op per lane per cycle",
+                "work": f"{ops // E} fp32 ops (an FMA is one op) x {E} contributing pairs",
+                "sfu_frac": sfu / (ms * 1e-3) / (SFU_LANES_PER_SM * hz),
+                "flop_model": {"frac": flops / (ms * 1e-3) / (2 * FP32_LANES_PER_SM * hz),
+                               "work": f"{flops // E} flops (an FMA is two) x {E} pairs, "
+                                       f"against 2 x the fp32 lanes"}}
     if call == "gs_loss_l1_ssim":
         flops = LOSS_FLOPS_PER_PIXEL * H * W
         peak = 2.0 * FP32_LANES_PER_SM * n_sm * sm_mhz * 1e6 / 1e12
@@ -346,6 +366,15 @@ def roofline(call, ms, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz):
     return {"kernel": call, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "traffic": profiled_traffic(call),
             "peak_source": f"{peaks['source']} copy bandwidth"}
+
+
+def per_call_fractions(per_call, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz) -> dict:
+    """Each call's roofline fraction (bound and frac) from its own event time."""
+    out = {}
+    for call, ms in per_call.items():
+        r = roofline(call, ms, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz)
+        out[call] = {"bound": r["bound"], "frac": r["frac"], "ms": ms}
+    return out
 
 
 # The kernel each single-kernel call runs, its sources, and its ncu summary.
@@ -396,7 +425,7 @@ def step_roofline(ms, sc, M, I, E, H, W, peaks, n_sm, sm_mhz, train=False):
     N, P = sc.n, H * W
     G = 44 + 12 * (sc.sh_degree + 1) ** 2  # parameter bytes per Gaussian
     hbm = float(peaks["hbm_gbs"]) * 1e9
-    fp32 = 2.0 * FP32_LANES_PER_SM * n_sm * sm_mhz * 1e6
+    fp32 = FP32_LANES_PER_SM * n_sm * sm_mhz * 1e6  # fp32 ops (an FMA is one)
     sfu = SFU_LANES_PER_SM * n_sm * sm_mhz * 1e6
     phases = {
         # 44 B of geometry per Gaussian, SH and the 64 B record only for the visible
@@ -404,23 +433,24 @@ def step_roofline(ms, sc, M, I, E, H, W, peaks, n_sm, sm_mhz, train=False):
         # depth sort of the M visible (8 B, 4 passes, read + write) and the pair list
         # (emitted once, then 2 passes read + write)
         "bin_sort": (8 * M * 8 + 8 * I * 5, 0, 0),
-        "forward": (48 * I + 24 * P, FLOPS_FWD_PER_E * E, SFU_FWD_PER_E * E),
+        "forward": (48 * I + 24 * P, OPS_FWD_PER_E * E, SFU_FWD_PER_E * E),
         # raster backward and the chain rule: records, pixel state and dL/dimage, grad2d,
         # parameters of the visible, every gradient row written
-        "backward": (48 * I + 36 * P + 36 * M + G * M + G * N, FLOPS_BWD_PER_E * E,
+        "backward": (48 * I + 36 * P + 36 * M + G * M + G * N, OPS_BWD_PER_E * E,
                      SFU_BWD_PER_E * E),
     }
     if train:
-        phases["loss"] = (36 * P, LOSS_FLOPS_PER_PIXEL * P, 0)
+        phases["loss"] = (36 * P, LOSS_FLOPS_PER_PIXEL * P // 2, 0)  # its FMAs
         phases["backward"] = (48 * I + 36 * P + 36 * M + 5 * N + 6 * G * N + 16 * N,
-                              FLOPS_BWD_PER_E * E, SFU_BWD_PER_E * E)
+                              OPS_BWD_PER_E * E, SFU_BWD_PER_E * E)
     out, total = {}, 0.0
     for k, (b, f, x) in phases.items():
         t = max(b / hbm, f / fp32, x / sfu) * 1e3
         out[k] = t
         total += t
     return {"ms": total, "frac": total / ms, "phases_ms": out,
-            "model": "per phase max(bytes/HBM, fp32 flops/fp32 peak, SFU ops/SFU peak), summed"}
+            "model": "per phase max(bytes/HBM, fp32 ops/(SMs x 128 x clock), SFU ops/(SMs x 16 "
+                     "x clock)), summed; an FMA is one op"}
 
 
 def kernel_launches(n, capacity, W, H) -> int:
@@ -527,33 +557,79 @@ def workload_config(args, sc, W, H, n_pairs, parallelism):
             "l2": l2_note(sc, "gradients", 1)}
 
 
-def oracle_sample_step(sc, cam, w, tile_stride: int):
+def _row_chunks(n: int, parts: int):
+    step = max(1, -(-n // max(1, parts)))
+    return [np.arange(i, min(n, i + step)) for i in range(0, n, step)]
+
+
+def _threads(fn, items, workers):
+    from concurrent.futures import ThreadPoolExecutor
+
+    # the oracle's C calls release the GIL (ctypes): the items run on separate cores
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        return list(ex.map(fn, items))
+
+
+def oracle_sample_step(sc, cam, w, tile_stride: int, workers: int = 1):
     """One bounded oracle step: projection and binning of the whole view, then the
     forward and backward blend of every tile_stride-th tile (in LPT order, so the
-    sample spans heavy and light tiles).  Returns (pairs processed, seconds, pairs of the
-    whole view)."""
+    sample spans heavy and light tiles), then the chain rule.  With workers > 1 the
+    unmodified oracle calls run on that many host threads: the projection and the chain
+    rule over disjoint ranges of Gaussians, the blends over disjoint sets of tiles (the
+    oracle's tile_parts), per-Gaussian float64 sums added at the end.  Returns (pairs
+    processed, seconds, pairs of the whole view)."""
     import oracle
 
     t0 = time.perf_counter()
-    proj = oracle.project(sc, cam)
+    if workers > 1:
+        chunks = _row_chunks(sc.n, 4 * workers)
+        ps = _threads(lambda rows: oracle.project(sc.subset(rows), cam), chunks, workers)
+        proj = oracle.Projection(*(np.concatenate([getattr(p, f) for p in ps])
+                                   for f in ("splat", "rgb", "radii", "tiles_touched")))
+    else:
+        proj = oracle.project(sc, cam)
     ntx, nty = oracle.n_tiles(cam)
     counts = oracle.bin_sort(cam, proj, np.zeros(ntx * nty, np.uint8))
     sel = np.zeros(ntx * nty, np.uint8)
     sel[counts.lpt_order[::tile_stride]] = 1
     b = oracle.bin_sort(cam, proj, sel)
-    oracle.blend(cam, proj, b)
-    g2, _ = oracle.blend_bwd(cam, proj, b, w)
-    oracle.project_bwd(sc, cam, proj, g2)
+    if workers > 1:
+        oracle.blend_parallel(cam, proj, b, workers=workers)
+        g2 = oracle.blend_bwd_parallel(cam, proj, b, w, workers=workers).grad2d
+
+        def chain(rows):
+            p = oracle.Projection(proj.splat[rows], proj.rgb[rows], proj.radii[rows],
+                                  proj.tiles_touched[rows])
+            return oracle.project_bwd(sc.subset(rows), cam, p, g2[rows])
+
+        _threads(chain, _row_chunks(sc.n, 4 * workers), workers)
+    else:
+        oracle.blend(cam, proj, b)
+        g2, _ = oracle.blend_bwd(cam, proj, b, w)
+        oracle.project_bwd(sc, cam, proj, g2)
     dt = time.perf_counter() - t0
     return int(b.counts[sel.astype(bool)].sum()), dt, int(counts.counts.sum())
 
 
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def cpu_baseline(sc, cam, w, stride: int = 1):
-    pairs, dt, _ = oracle_sample_step(sc, cam, w, stride)
+    """The oracle over the whole view, on every host core (the headline) and on one."""
+    cores = host_cores()
     what = "every tile" if stride == 1 else f"every {stride}th tile in LPT order"
-    return {"value": pairs / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+    pairs, dt, _ = oracle_sample_step(sc, cam, w, stride, workers=cores)
+    pairs1, dt1, _ = oracle_sample_step(sc, cam, w, stride, workers=1)
+    return {"value": pairs / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"one view: all projections and tile counts, forward + backward of "
-                      f"{what} ({pairs} pairs), {dt:.1f} s"}
+                      f"{what} ({pairs} pairs) and the chain rule, the unmodified oracle calls "
+                      f"on {cores} host threads (disjoint tiles / Gaussians), {dt:.2f} s",
+            "single_core": {"value": pairs1 / dt1, "unit": UNIT, "cores": 1,
+                            "sample": f"the same view on one thread, {dt1:.1f} s"}}
 
 
 # Adam settings of the training step: the learning rates 3DGS trains with (means, scales,
@@ -687,6 +763,8 @@ def run_train(args):
                     props.multi_processor_count, sm_mhz)
     step_roof = step_roofline(ms_per_step, sc, M, pairs1, E, H, W, peaks,
                               props.multi_processor_count, sm_mhz, train=True)
+    roof["per_call"] = per_call_fractions(per_call, sc, M, pairs1, E, H, W, peaks,
+                                          props.multi_processor_count, sm_mhz)
     launches = kernel_launches(sc.n, r.capacity, W, H) + 2  # the loss: tiles + final sum
     if rank == 0:
         print(json.dumps({
@@ -727,24 +805,27 @@ def run_reference(args):
         sh = torch.from_numpy(np.ascontiguousarray(sc.sh, np.float32))
         sc = dataclasses.replace(sc, sh=sh.to(torch.bfloat16).float().numpy())
     w = ss.loss_weights(args.config, cam.height, cam.width)
-    stride = 4
+    # the whole view up to the 1.5M scene; every 4th tile (in LPT order) of the larger ones
+    stride = 1 if args.config <= 3 else 4
+    cores = host_cores()
     for _ in range(args.warmup):
-        oracle_sample_step(sc, cam, w, stride)
+        oracle_sample_step(sc, cam, w, stride, workers=cores)
     tot_pairs, tot_s = 0, 0.0
     for _ in range(args.steps):
-        p, dt, view_pairs = oracle_sample_step(sc, cam, w, stride)
+        p, dt, view_pairs = oracle_sample_step(sc, cam, w, stride, workers=cores)
         tot_pairs += p
         tot_s += dt
     value = tot_pairs / tot_s
-    sample = (f"each step: all projections and tile counts, forward + backward of every "
-              f"{stride}th tile in LPT order ({tot_pairs // args.steps} pairs)")
+    what = "every tile" if stride == 1 else f"every {stride}th tile in LPT order"
+    sample = (f"each step: all projections and tile counts, forward + backward of {what} "
+              f"({tot_pairs // args.steps} pairs) and the chain rule, on {cores} host threads")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": workload_config(args, sc, cam.width, cam.height, view_pairs, "single"),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))

@@ -19,17 +19,37 @@ PEAKS = {"hbm_gbs": 6000.0, "source": "measured"}
 SC = SimpleNamespace(n=1000, sh_degree=3)  # 236 parameter bytes per Gaussian
 N_SM, MHZ = 152, 2000.0
 FP32_TFLOPS = 2.0 * 128 * N_SM * MHZ * 1e6 / 1e12
+FP32_TOPS = 128 * N_SM * MHZ * 1e6 / 1e12    # an FMA is one op
+SFU_OPS = 16 * N_SM * MHZ * 1e6
 
 
 def test_alu_roofline_of_the_raster_calls():
+    # the op model: 40 fp32 ops + 2 SFU per contributing pair backward, 14 + 1 forward,
+    # against SMs x 128 lanes (x 16 for the SFU) x the clock; flops reported beside it
+    assert (bench.OPS_BWD_PER_E, bench.SFU_BWD_PER_E) == (40, 2)
+    assert (bench.OPS_FWD_PER_E, bench.SFU_FWD_PER_E) == (14, 1)
     E = 10_000_000
     r = bench.roofline("gs_rasterize_bwd", 0.5, SC, 700, 3000, E, 100, 200, PEAKS, N_SM, MHZ)
     assert r["bound"] == "alu" and r["unit"] == "TFLOP/s"
-    assert r["peak"] == pytest.approx(FP32_TFLOPS)
-    assert r["achieved"] == pytest.approx(bench.FLOPS_BWD_PER_E * E / 0.5e-3 / 1e12)
+    assert r["peak"] == pytest.approx(FP32_TOPS)
+    assert r["achieved"] == pytest.approx(40 * E / 0.5e-3 / 1e12)
     assert r["frac"] == pytest.approx(r["achieved"] / r["peak"])
+    assert r["sfu_frac"] == pytest.approx(2 * E / 0.5e-3 / SFU_OPS)
+    assert r["flop_model"]["frac"] == pytest.approx(48 * E / 0.5e-3 / 1e12 / FP32_TFLOPS)
     f = bench.roofline("gs_rasterize_fwd", 0.25, SC, 700, 3000, E, 100, 200, PEAKS, N_SM, MHZ)
-    assert f["achieved"] == pytest.approx(bench.FLOPS_FWD_PER_E * E / 0.25e-3 / 1e12)
+    assert f["achieved"] == pytest.approx(14 * E / 0.25e-3 / 1e12)
+    assert f["flop_model"]["frac"] == pytest.approx(22 * E / 0.25e-3 / 1e12 / FP32_TFLOPS)
+
+
+def test_per_call_fractions_cover_every_call():
+    E = 10_000_000
+    per_call = {"gs_project": 0.08, "gs_bin_sort": 0.1, "gs_rasterize_fwd": 0.2,
+                "gs_rasterize_bwd": 0.4, "gs_project_bwd": 0.09}
+    out = bench.per_call_fractions(per_call, SC, 600, 5000, E, 100, 100, PEAKS, N_SM, MHZ)
+    assert set(out) == set(per_call)
+    for call, ms in per_call.items():
+        r = bench.roofline(call, ms, SC, 600, 5000, E, 100, 100, PEAKS, N_SM, MHZ)
+        assert out[call] == {"bound": r["bound"], "frac": r["frac"], "ms": ms}
 
 
 def test_loss_roofline_counts_window_fmas_per_pixel():
@@ -59,8 +79,12 @@ def test_step_roofline_sums_the_binding_term_of_each_phase():
     assert set(out["phases_ms"]) == {"project", "bin_sort", "forward", "backward"}
     assert out["ms"] == pytest.approx(sum(out["phases_ms"].values()))
     assert out["frac"] == pytest.approx(out["ms"] / 1.0)
-    fwd_flops = bench.FLOPS_FWD_PER_E * E / (FP32_TFLOPS * 1e12) * 1e3
-    assert out["phases_ms"]["forward"] >= fwd_flops * (1 - 1e-12)
+    fwd_ops = bench.OPS_FWD_PER_E * E / (FP32_TOPS * 1e12) * 1e3
+    assert out["phases_ms"]["forward"] >= fwd_ops * (1 - 1e-12)
+    assert out["phases_ms"]["backward"] == pytest.approx(
+        max(bench.OPS_BWD_PER_E * E / (FP32_TOPS * 1e12),
+            bench.SFU_BWD_PER_E * E / SFU_OPS,
+            (48 * I + 36 * H * W + 36 * M + 236 * M + 236 * SC.n) / 6000e9) * 1e3)
     # with few contributing pairs the backward is bound by its bytes, which Adam raises
     # (parameters and both moments read and written instead of one gradient row)
     plain = bench.step_roofline(1.0, SC, M, I, 0, H, W, PEAKS, N_SM, MHZ)
