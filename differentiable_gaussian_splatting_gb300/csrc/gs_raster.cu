@@ -459,128 +459,93 @@ __global__ void __launch_bounds__(kThreads, 5) raster_fwd_kernel(RasterArgs A) {
 // ---------------------------------------------------------------------------
 // backward
 // ---------------------------------------------------------------------------
-// Halving reduce-scatter of nine values over a warp (5 + 3 + 2 + 1 + 1 = 12
-// shuffles).  Afterwards the even lane 2j' of each pair holds the warp sum of
-// component comp_of_lane(lane) (valid when >= 0).
-__device__ __forceinline__ float reduce_scatter9(float v[9], int lane) {
-    const unsigned F = 0xffffffffu;
-    // xor 16: lower half keeps components 0..4, upper half 5..8
-    const bool lo16 = !(lane & 16);
-    float u[5];
-#pragma unroll
-    for (int i = 0; i < 5; ++i) {
-        const float send = lo16 ? (i < 4 ? v[5 + i] : 0.f) : v[i];
-        const float r = __shfl_xor_sync(F, send, 16);
-        u[i] = lo16 ? v[i] + r : (i < 4 ? v[5 + i] + r : 0.f);
-    }
-    // xor 8: 5 -> 3 (lower) / 2 (upper)
-    const bool lo8 = !(lane & 8);
-    float w3[3];
-#pragma unroll
-    for (int i = 0; i < 3; ++i) {
-        const float send = lo8 ? (i < 2 ? u[3 + i] : 0.f) : u[i];
-        const float r = __shfl_xor_sync(F, send, 8);
-        w3[i] = lo8 ? u[i] + r : (i < 2 ? u[3 + i] + r : 0.f);
-    }
-    // xor 4: 3 -> 2 / 1
-    const bool lo4 = !(lane & 4);
-    float w2[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float send = lo4 ? (i == 0 ? w3[2] : 0.f) : w3[i];
-        const float r = __shfl_xor_sync(F, send, 4);
-        w2[i] = lo4 ? w3[i] + r : (i == 0 ? w3[2] + r : 0.f);
-    }
-    // xor 2: 2 -> 1 / 1
-    const bool lo2 = !(lane & 2);
-    const float send = lo2 ? w2[1] : w2[0];
-    const float r = __shfl_xor_sync(F, send, 2);
-    float x = lo2 ? w2[0] + r : w2[1] + r;
-    // xor 1: sum the pair
-    x += __shfl_xor_sync(F, x, 1);
-    return x;
-}
-
-// component held by `lane` after reduce_scatter9, or -1 (a padding slot).
-// Lane bits 4, 3, 2, 1 pick the half kept at the xor-16, 8, 4, 2 steps:
-//   xor 16: {0..4} | {5..8, pad};  xor 8: first three | last two of those;
-//   xor 4: first two | third;  xor 2: first | second.
-__device__ __forceinline__ int comp_of_lane(int lane) {
-    switch (lane >> 1) {
-        case 0: return 0;   // lanes 0, 1
-        case 1: return 1;   // lanes 2, 3
-        case 2: return 2;   // lanes 4, 5
-        case 4: return 3;   // lanes 8, 9
-        case 5: return 4;   // lanes 10, 11
-        case 8: return 5;   // lanes 16, 17
-        case 9: return 6;   // lanes 18, 19
-        case 10: return 7;  // lanes 20, 21
-        case 12: return 8;  // lanes 24, 25
-        default: return -1;
-    }
-}
-
-// Two splats' nine values summed over the warp at once: lanes 0-15 keep
-// splat a, lanes 16-31 splat b (one exchange at xor 16), then each half
-// reduce-scatters its nine sums (xor 8, 4, 2, 1): 20 shuffles for both splats
-// instead of 24.  Afterwards lane l holds component comp16_of_lane(l & 15) of
-// splat (l < 16 ? a : b) (valid when >= 0).
-__device__ __forceinline__ float reduce_scatter9x2(const float a[9], const float b[9], int lane) {
+// Two splats' column moments summed over the warp ("What the 3DGS Literature
+// Left on the Table", Step 2 and Step 6.4).  Every lane holds, per splat, six
+// values of its two pixels: the log-alpha derivative sums m = g0 + g1,
+// sy = g0 dy0 + g1 dy1, syy = g0 dy0^2 + g1 dy1^2 and the colour terms
+// w0 G0 + w1 G1 (r, g, b).  Lanes l, l ^ 8, l ^ 16, l ^ 24 share a pixel
+// column, hence dx:
+//   xor 16  lanes 0-15 keep splat a, lanes 16-31 splat b (6 shuffles);
+//   xor 8   each column's four lanes summed; geometry (m, sy, syy) stays on
+//           the lanes with bit 3 clear, colour on the others (3 shuffles);
+//           the geometry lanes form the column's dx-weighted terms once per
+//           column instead of per pixel: dx^2 m, dx sy and, with the splat's
+//           conic factor, the mean derivatives l11 s and l12 s + l22^2 sy,
+//           s = l11 dx m + l12 sy the column's sum of g u1;
+//   xor 4, 2, 1  the columns summed (3 + 2 + 1 shuffles).
+// Afterwards lane l holds, for the splat of its half, the quantity
+// moment_of_lane(l & 15).  15 shuffles for two splats.
+__device__ __forceinline__ float reduce_moments2(const float a[6], const float b[6], float dxa,
+                                                 float dxb, float l11, float l12, float l22,
+                                                 int lane) {
     const unsigned F = 0xffffffffu;
     const bool lo16 = !(lane & 16);
-    float k[9];
+    float k[6];
 #pragma unroll
-    for (int i = 0; i < 9; ++i) {
+    for (int i = 0; i < 6; ++i) {
         const float r = __shfl_xor_sync(F, lo16 ? b[i] : a[i], 16);
         k[i] = (lo16 ? a[i] : b[i]) + r;
     }
     const bool lo8 = !(lane & 8);
-    float u[5];
+    float v[6];
 #pragma unroll
-    for (int i = 0; i < 5; ++i) {
-        const float send = lo8 ? (i < 4 ? k[5 + i] : 0.f) : k[i];
-        const float r = __shfl_xor_sync(F, send, 8);
-        u[i] = lo8 ? k[i] + r : (i < 4 ? k[5 + i] + r : 0.f);
+    for (int i = 0; i < 3; ++i) {
+        const float r = __shfl_xor_sync(F, lo8 ? k[3 + i] : k[i], 8);
+        v[i] = (lo8 ? k[i] : k[3 + i]) + r;
     }
+    // geometry lanes: (m, d/dmuy, syy, d/dmux, dx^2 m, dx sy) of the column, with
+    // sum g u1 = l11 dx m + l12 sy (u1 = l11 dx + l12 dy); colour lanes: (r, g, b, unused)
+    const float dx = lo16 ? dxa : dxb;
+    const float dxm = dx * v[0];
+    const float su1 = fmaf(l11, dxm, l12 * v[1]);
+    v[3] = l11 * su1;
+    v[4] = dx * dxm;
+    v[5] = dx * v[1];
+    // (slot 1 holds green on the colour lanes)
+    v[1] = lo8 ? fmaf(l12, su1, l22 * (l22 * v[1])) : v[1];
     const bool lo4 = !(lane & 4);
     float w[3];
 #pragma unroll
     for (int i = 0; i < 3; ++i) {
-        const float send = lo4 ? (i < 2 ? u[3 + i] : 0.f) : u[i];
-        const float r = __shfl_xor_sync(F, send, 4);
-        w[i] = lo4 ? u[i] + r : (i < 2 ? u[3 + i] + r : 0.f);
+        const float r = __shfl_xor_sync(F, lo4 ? v[3 + i] : v[i], 4);
+        w[i] = (lo4 ? v[i] : v[3 + i]) + r;
     }
     const bool lo2 = !(lane & 2);
-    float x[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float send = lo2 ? (i < 1 ? w[2 + i] : 0.f) : w[i];
-        const float r = __shfl_xor_sync(F, send, 2);
-        x[i] = lo2 ? w[i] + r : (i < 1 ? w[2 + i] + r : 0.f);
-    }
+    const float r0 = __shfl_xor_sync(F, lo2 ? w[2] : w[0], 2);
+    const float x0 = (lo2 ? w[0] : w[2]) + r0;
+    const float r1 = __shfl_xor_sync(F, lo2 ? 0.f : w[1], 2);
+    const float x1 = (lo2 ? w[1] : 0.f) + r1;
     const bool lo1 = !(lane & 1);
-    const float r = __shfl_xor_sync(F, lo1 ? x[1] : x[0], 1);
-    return (lo1 ? x[0] : x[1]) + r;
+    const float r = __shfl_xor_sync(F, lo1 ? x1 : x0, 1);
+    return (lo1 ? x0 : x1) + r;
 }
 
-// component held by lane l (0..15 within its half) after reduce_scatter9x2, or -1
-__device__ __forceinline__ int comp16_of_lane(int l) {
+// What lane l (0..15 within its half) holds after reduce_moments2, as the
+// grad2d component it feeds (mux, muy, a, b, c, opacity, r, g, b), or -1:
+//   0: sum g           -> opacity (times 1 / o)
+//   1: d/dmuy
+//   2: sum g dy^2      -> c (times -1/2)
+//   4: d/dmux
+//   5: sum g dx^2      -> a (times -1/2)
+//   6: sum g dx dy     -> b (times -1)
+//   8, 9, 10: sum w G  -> r, g, b
+__device__ __forceinline__ int moment_comp_of_lane(int l) {
     switch (l) {
-        case 0: return 0;
+        case 0: return 5;
         case 1: return 1;
-        case 2: return 2;
-        case 4: return 3;
-        case 5: return 4;
-        case 8: return 5;
-        case 9: return 6;
-        case 10: return 7;
-        case 12: return 8;
+        case 2: return 4;
+        case 4: return 0;
+        case 5: return 2;
+        case 6: return 3;
+        case 8: return 6;
+        case 9: return 7;
+        case 10: return 8;
         default: return -1;
     }
 }
 
-__device__ __forceinline__ float conic_scale(int comp) {
-    return (comp == 2 || comp == 4) ? -0.5f : (comp == 3 ? -1.f : 1.f);
+__device__ __forceinline__ float moment_scale(int l) {
+    return (l == 2 || l == 5) ? -0.5f : (l == 6 ? -1.f : 1.f);
 }
 
 // ---------------------------------------------------------------------------
@@ -654,31 +619,29 @@ __device__ __forceinline__ bool row_step(const float4& r0, const float4& r1, con
     return act;
 }
 
-// One splat for the lane's two pixels; v gets the sum of their nine terms
-// (conic ones without their constant factors).  Conic of the evaluated
-// quadratic: a = l11^2, b = l11 l12, c = l12^2 + l22^2, so a dx + b dy = l11 u1
-// and b dx + c dy = l12 u1 + l22 u2.
-__device__ __forceinline__ bool splat_terms2(const BwdSlice& S, int q, float px, float py0,
-                                             float py1, int rel0, int rel1, BwdPixel& P0,
-                                             BwdPixel& P1, float v[9]) {
+// One splat for the lane's two pixels: its six moments (reduce_moments2) in v
+// and its dx.  Returns whether either pixel blended it.  The conic and mean
+// derivatives are formed from the moments inside the reduction: with the
+// evaluated quadratic's conic a = l11^2, b = l11 l12, c = l12^2 + l22^2,
+// dL/dmux = l11 (l11 sum g dx + l12 sum g dy) and
+// dL/dmuy = l12 (l11 sum g dx + l12 sum g dy) + l22^2 sum g dy.
+__device__ __forceinline__ bool splat_moments2(const BwdSlice& S, int q, float px, float py0,
+                                               float py1, int rel0, int rel1, BwdPixel& P0,
+                                               BwdPixel& P1, float v[6], float* dx_out) {
     const float4 r0 = S.r0[q], r1 = S.r1[q], r2 = S.r2[q];
     const float dx = rsub(px, r0.x);
     const float dy0 = rsub(py0, r0.y), dy1 = rsub(py1, r0.y);
     float a0, b0, a1, b1, g0, g1, w0, w1;
     const bool act0 = row_step(r0, r1, r2, dx, dy0, q <= rel0, P0, &a0, &b0, &g0, &w0);
     const bool act1 = row_step(r0, r1, r2, dx, dy1, q <= rel1, P1, &a1, &b1, &g1, &w1);
-    // the two rows share dx and the splat's factors: sum over the rows first
-    const float ga = fmaf(g1, a1, g0 * a0), gb = fmaf(g1, b1, g0 * b0);
-    v[0] = r0.z * ga;
-    v[1] = fmaf(r0.w, ga, r1.x * gb);
-    v[5] = g0 + g1;
-    v[2] = (v[5] * dx) * dx;
     const float gdy0 = g0 * dy0, gdy1 = g1 * dy1;
-    v[3] = (gdy0 + gdy1) * dx;
-    v[4] = fmaf(gdy1, dy1, gdy0 * dy0);
-    v[6] = fmaf(w1, P1.Gr, w0 * P0.Gr);
-    v[7] = fmaf(w1, P1.Gg, w0 * P0.Gg);
-    v[8] = fmaf(w1, P1.Gb, w0 * P0.Gb);
+    v[0] = g0 + g1;
+    v[1] = gdy0 + gdy1;
+    v[2] = fmaf(gdy1, dy1, gdy0 * dy0);
+    v[3] = fmaf(w1, P1.Gr, w0 * P0.Gr);
+    v[4] = fmaf(w1, P1.Gg, w0 * P0.Gg);
+    v[5] = fmaf(w1, P1.Gb, w0 * P0.Gb);
+    *dx_out = dx;
     return act0 || act1;
 }
 
@@ -737,12 +700,12 @@ __global__ void __launch_bounds__(kBwdThreads, 6) raster_bwd_kernel(RasterArgs A
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int h = A.ctrl[kCtlH], k = A.ctrl[kCtlK], nitems = A.ctrl[kCtlItems];
     const int nunits = 4 * nitems;  // (work item, quadrant)
-    const int my_comp = comp_of_lane(lane);
-    const bool writer = !(lane & 1) && my_comp >= 0;
-    const int my_comp2 = comp16_of_lane(lane & 15);
-    // the conic components are summed without their constant factors
-    // (-1/2 dx^2, -dx dy, -1/2 dy^2), applied once by the writing lane
-    const float comp_scale = conic_scale(my_comp), comp_scale2 = conic_scale(my_comp2);
+    // the writing lanes (reduce_moments2): their component, constant factor and role
+    const int sl = lane & 15;
+    const int my_comp = moment_comp_of_lane(sl);
+    const float my_scale = moment_scale(sl);
+    const bool is_opac = sl == 0;
+    const bool first = lane < 16;
     const int col = lane & 7, rp = lane >> 3;
     while (true) {
         int unit = 0;
@@ -790,31 +753,38 @@ __global__ void __launch_bounds__(kBwdThreads, 6) raster_bwd_kernel(RasterArgs A
                 // splats two at a time, back to front: q1 behind q2
                 const int q1 = 31 - __clz(work);
                 work &= ~(1u << q1);
-                float va[9];
-                const bool act1 = splat_terms2(S, q1, px, py0, py1, rel0, rel1, P0, P1, va);
+                float va[6], dxa;
+                const bool act1 = splat_moments2(S, q1, px, py0, py1, rel0, rel1, P0, P1, va, &dxa);
                 const uint32_t b1 = __ballot_sync(F, act1);
+                float sum;
+                int q;
+                bool wr;
                 if (work) {
                     const int q2 = 31 - __clz(work);
                     work &= ~(1u << q2);
-                    float vb[9];
-                    const bool act2 = splat_terms2(S, q2, px, py0, py1, rel0, rel1, P0, P1, vb);
+                    float vb[6], dxb;
+                    const bool act2 =
+                        splat_moments2(S, q2, px, py0, py1, rel0, rel1, P0, P1, vb, &dxb);
                     const uint32_t b2 = __ballot_sync(F, act2);
                     if ((b1 | b2) == 0) continue;
-                    const float sum = reduce_scatter9x2(va, vb, lane);
-                    const bool first = lane < 16;
-                    // every lane forms its write; only the atomic is predicated
-                    const int q = first ? q1 : q2;
-                    // component 5 is d/d(opacity): divide by o = 2^log2(o)
-                    const float f = my_comp2 == 5 ? ex2_approx(-S.r1[q].z) : comp_scale2;
-                    float* dst = A.grad2d + 9 * (int64_t)S.gid[q] + my_comp2;
-                    if (my_comp2 >= 0 && (first ? b1 : b2)) atomicAdd(dst, sum * f);
+                    q = first ? q1 : q2;
+                    wr = (first ? b1 : b2) != 0;
+                    const float4 r0 = S.r0[q];
+                    sum = reduce_moments2(va, vb, dxa, dxb, r0.z, r0.w, S.r1[q].x, lane);
                 } else {
+                    // a lone last splat: paired with zeros
                     if (b1 == 0) continue;
-                    const float sum = reduce_scatter9(va, lane);
-                    const float f = my_comp == 5 ? ex2_approx(-S.r1[q1].z) : comp_scale;
-                    float* dst = A.grad2d + 9 * (int64_t)S.gid[q1] + my_comp;
-                    if (writer) atomicAdd(dst, sum * f);
+                    const float vz[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    q = q1;
+                    wr = first;
+                    const float4 r0 = S.r0[q];
+                    sum = reduce_moments2(va, vz, dxa, 0.f, r0.z, r0.w, S.r1[q].x, lane);
                 }
+                // every lane forms its write; only the atomic is predicated.  The
+                // opacity lane divides o back out, o = 2^log2(o)
+                const float f = is_opac ? ex2_approx(-S.r1[q].z) : my_scale;
+                float* dst = A.grad2d + 9 * (int64_t)S.gid[q] + my_comp;
+                if (my_comp >= 0 && wr) atomicAdd(dst, sum * f);
             }
             __syncwarp();  // the slice is restaged two steps later
             if (!more) break;
