@@ -16,9 +16,9 @@
 // Radix sort: LSD, 8-bit digits, one kernel per pass; the digit counts of every
 // pass are taken by the kernel that writes the keys (the visible-Gaussian
 // compaction, the pair emission).  Blocks take 4096-key tiles in ticket order,
-// rank keys within warps with __match_any_sync, publish their digit counts and
-// add those of earlier tiles by decoupled look-back (every wait is bounded and
-// sets a give-up flag).
+// rank keys within warps from eight ballots and one shared atomic per digit
+// and warp, publish their digit counts and add those of earlier tiles by
+// decoupled look-back (every wait is bounded and sets a give-up flag).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -105,7 +105,7 @@ __device__ __forceinline__ void st_relaxed(uint64_t* p, uint64_t v) {
 }
 
 // One pass of the stable LSD sort: blocks take consecutive 4096-key tiles in
-// ticket order, rank their keys by digit (warps with __match_any_sync, then
+// ticket order, rank their keys by digit (within warps from ballots, then
 // across warps), publish their digit counts, and add the counts of the tiles
 // before them by looking back through the published words (decoupled
 // look-back: a block only waits on tiles that started before it, so waits
@@ -154,9 +154,11 @@ __global__ void __launch_bounds__(kRsBlock, 4) rs_onesweep(
     }
     // The lanes holding the same digit come from eight ballots; the lowest of them
     // adds their number to the warp's count of that digit and hands the old count
-    // to the others.  A warp's shared-memory atomics take effect in program
-    // order, so item r's offsets follow item r - 1's and the ranking is stable,
-    // while the items' atomics need not wait for one another.
+    // to the others.  Items are ranked in order r = 0, 1, ...: the leaders of
+    // item r may be other lanes than those of item r - 1, and __syncwarp() orders
+    // the two items' shared-memory updates among the warp's lanes (the CUDA
+    // programming guide's memory-ordering guarantee of __syncwarp), so item r's
+    // offsets follow item r - 1's and the ranking is stable.
     const uint32_t lt = lanemask_lt();
 #pragma unroll
     for (int r = 0; r < kRsIpt; ++r) {
@@ -174,6 +176,7 @@ __global__ void __launch_bounds__(kRsBlock, 4) rs_onesweep(
         uint32_t old = 0;
         if (valid && leader == lane) old = atomicAdd(&S.wcnt[warp][d], (uint32_t)__popc(peers));
         loc[r] = __shfl_sync(0xffffffffu, old, leader) + __popc(peers & lt);
+        __syncwarp();
     }
     __syncthreads();
 
@@ -849,3 +852,56 @@ cudaError_t run_bin_sort_radix(const CamParams& cam, int64_t n, const float* spl
 }
 
 }  // namespace gs
+
+// ---------------------------------------------------------------------------
+// Test hook (not part of the C ABI in gs.h): makes the look-back's bounded wait
+// run out with the unmodified one-sweep kernel.  One pass over n keys (n >
+// 4096, so that there are at least two 4096-key tiles) runs with the pass's
+// ticket counter set to 1 before the launch: the block that draws ticket 1
+// waits on tile 0's published counts, which no block writes, gives up after
+// its poll limit and sets the give-up flag; every access stays inside the
+// buffers.  ws must hold gs_test_lookback_timeout_ws_bytes(n) bytes; keys_out
+// and vals_out receive meaningless values.  Returns GS_ERR_TIMEOUT when the
+// flag was set (the status gs_bin_sort returns then), GS_OK if not.
+// ---------------------------------------------------------------------------
+namespace {
+size_t lookback_test_ws_layout(int64_t n, size_t* off_ghist, size_t* off_err) {
+    const size_t ctl = gs::rs_ctl_bytes(n);
+    *off_ghist = (ctl + 255) & ~size_t(255);
+    *off_err = *off_ghist + 4 * 256 * sizeof(uint32_t);
+    return *off_err + 256;
+}
+}  // namespace
+
+extern "C" size_t gs_test_lookback_timeout_ws_bytes(int64_t n) {
+    size_t a, b;
+    return n > 0 ? lookback_test_ws_layout(n, &a, &b) : 0;
+}
+
+extern "C" gs_status gs_test_lookback_timeout(const uint32_t* keys_in, const int32_t* vals_in,
+                                              uint32_t* keys_out, int32_t* vals_out, int64_t n,
+                                              void* ws, size_t ws_bytes, void* stream) {
+    using namespace gs;
+    if (!keys_in || !vals_in || !keys_out || !vals_out || !ws || n <= kRsTile || n > (1 << 24))
+        return GS_ERR_INVALID_ARG;
+    size_t off_ghist, off_err;
+    if (ws_bytes < lookback_test_ws_layout(n, &off_ghist, &off_err)) return GS_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    char* w = static_cast<char*>(ws);
+    if (cudaMemsetAsync(w, 0, ws_bytes, st) != cudaSuccess) return GS_ERR_CUDA;
+    // ticket counter of pass 0 (the first int of the control region) := 1
+    if (cudaMemsetAsync(w, 1, 1, st) != cudaSuccess) return GS_ERR_CUDA;
+    int* tickets = reinterpret_cast<int*>(w);
+    uint64_t* lookback = reinterpret_cast<uint64_t*>(w + 16 + kMaxPasses * 256 * 4);
+    auto* ghist = reinterpret_cast<const uint32_t*>(w + off_ghist);
+    auto* err = reinterpret_cast<unsigned long long*>(w + off_err);
+    const unsigned grid = (unsigned)nblk_of(n);
+    if (launch(rs_onesweep, grid, kRsBlock, 0, st, keys_in, vals_in, keys_out, vals_out,
+               (const int64_t*)nullptr, n, 0, ghist, tickets, lookback, err) != cudaSuccess)
+        return GS_ERR_CUDA;
+    unsigned long long flag = 0;
+    if (cudaMemcpyAsync(&flag, err, sizeof(flag), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return GS_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return GS_ERR_CUDA;
+    return flag ? GS_ERR_TIMEOUT : GS_OK;
+}
