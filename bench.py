@@ -286,6 +286,7 @@ def run_gpu(args):
                               props.multi_processor_count, sm_mhz)
     roof["per_call"] = per_call_fractions(per_call, sc, M, n_pairs, E, H, W, peaks,
                                           props.multi_processor_count, sm_mhz)
+    load = imbalance(r.stats(), r.n_tiles)  # the last forward's frame (synchronises)
 
     e2e = None if args.no_e2e else run_e2e(gs, r, sc, cam, w, dev, args, n_pairs)
     cpu = None
@@ -302,6 +303,7 @@ def run_gpu(args):
             "per_call_ms": per_call,
             "roofline": roof,
             "step_roofline": step_roof,
+            "imbalance": load,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
@@ -366,6 +368,22 @@ def roofline(call, ms, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz):
     return {"kernel": call, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "traffic": profiled_traffic(call),
             "peak_source": f"{peaks['source']} copy bandwidth"}
+
+
+def imbalance(stats: dict, n_tiles: int) -> dict:
+    """Per-frame tile load (Ryu & Yoo, Sec. 3.1): the heaviest tile against the mean, the
+    lightest non-empty tile and the per-CTA share N_total / K; the split policy's choice
+    (Eq. 6) and what the forward did with the 256-splat batches of split tiles."""
+    K = max(int(stats["resident_ctas"]), 1)
+    tot, nmax = int(stats["n_total"]), int(stats["n_max"])
+    nz, nmin = int(stats["nonempty_tiles"]), int(stats["n_min_nonempty"])
+    return {"tiles": n_tiles, "nonempty_tiles": nz, "n_max": nmax,
+            "n_mean": tot / max(n_tiles, 1), "n_mean_nonempty": tot / max(nz, 1),
+            "n_min_nonempty": nmin, "max_over_min": nmax / max(nmin, 1),
+            "max_over_share": nmax / (tot / K) if tot else 0.0, "resident_ctas": K,
+            "h": int(stats["h"]), "k": int(stats["k"]),
+            "batches": {k: int(stats["batches_" + k]) for k in
+                        ("tiles", "chunks", "skipped_on_flag", "skipped_done", "discarded")}}
 
 
 def per_call_fractions(per_call, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz) -> dict:

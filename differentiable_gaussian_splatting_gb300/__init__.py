@@ -454,12 +454,15 @@ def gs_loss_l1_ssim(width, height, image, target, dL_dimage, loss_out, workspace
 
 
 def gs_raster_stats(workspace, stream=None) -> dict:
-    out = (C.c_int64 * 8)()
+    out = (C.c_int64 * 16)()
     st = library().gs_raster_stats(_ptr(workspace, "workspace"), workspace.numel(), out,
                                    _stream(stream))
     _check("gs_raster_stats", st)
     return {"h": out[0], "k": out[1], "resident_ctas": out[2], "work_items": out[3],
-            "device_error": out[4]}
+            "device_error": out[4], "n_max": out[5], "n_min_nonempty": out[6],
+            "n_total": out[7], "nonempty_tiles": out[8], "batches_tiles": out[9],
+            "batches_chunks": out[10], "batches_skipped_on_flag": out[11],
+            "batches_skipped_done": out[12], "batches_discarded": out[13]}
 
 
 # ---------------------------------------------------------------------------

@@ -455,12 +455,21 @@ gs_status gs_raster_stats(const void* workspace, size_t workspace_bytes, int64_t
     cudaError_t err = cudaMemcpyAsync(ctrl, workspace, sizeof(ctrl), cudaMemcpyDeviceToHost, st);
     if (err == cudaSuccess) err = cudaStreamSynchronize(st);
     if (err != cudaSuccess) return GS_ERR_CUDA;
-    for (int i = 0; i < 8; ++i) out[i] = 0;
+    for (int i = 0; i < 16; ++i) out[i] = 0;
     out[0] = ctrl[kCtlH];
     out[1] = ctrl[kCtlK];
     out[2] = ctrl[kCtlResident];
     out[3] = ctrl[kCtlItems];
     out[4] = ctrl[kCtlError];
+    out[5] = ctrl[kCtlNMax];
+    out[6] = ctrl[kCtlNMinNz];
+    out[7] = ctrl[kCtlNTotal];
+    out[8] = ctrl[kCtlNonEmpty];
+    out[9] = ctrl[kCtlBatchTile];
+    out[10] = ctrl[kCtlBatchChunk];
+    out[11] = ctrl[kCtlSkipFlag];
+    out[12] = ctrl[kCtlSkipDone];
+    out[13] = ctrl[kCtlDiscard];
     return GS_OK;
 }
 

@@ -149,6 +149,7 @@ struct RasterLayout {
     size_t off_ctrl;     // int32[16] control words
     size_t off_sat;      // int32[h_max] saturation flags
     size_t off_done;     // int32[h_max] finished-chunk counters
+    size_t off_cbatch;   // int32[h_max][16]: batches each chunk blended
     size_t off_part_c;   // float4[h_max][16][256]: chunk partial (C.rgb, T)
     size_t off_part_n;   // int2[h_max][16][256]: chunk partial (n, last)
     size_t off_bwd;      // float4[h_max][16][256]: (T after chunk, colour behind chunk)
@@ -165,6 +166,21 @@ enum : int {
     kCtlItems = 4,
     kCtlResident = 5,
     kCtlError = 6,
+    // per-frame tile load (the policy kernel): pairs of the heaviest tile, of the
+    // lightest non-empty tile, of all tiles, and the number of non-empty tiles
+    kCtlNMax = 7,
+    kCtlNMinNz = 8,
+    kCtlNTotal = 9,
+    kCtlNonEmpty = 10,
+    // 256-splat batches of the forward: blended by whole tiles, blended by depth
+    // chunks, left unread by chunks that saw the saturation flag, left unread by
+    // chunks whose own pixels had all stopped, and blended by chunks whose result
+    // the composition discarded (every pixel had stopped before them)
+    kCtlBatchTile = 11,
+    kCtlBatchChunk = 12,
+    kCtlSkipFlag = 13,
+    kCtlSkipDone = 14,
+    kCtlDiscard = 15,
     kCtlWords = 16
 };
 

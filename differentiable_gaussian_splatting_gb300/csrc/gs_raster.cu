@@ -52,6 +52,7 @@ struct RasterArgs {
     int* ctrl;
     int* sat;
     int* done;
+    int* cbatch;
     float4* part_c;
     int2* part_n;
     float4* bstate;
@@ -130,6 +131,12 @@ struct Smem {
     int flag;
 };
 
+// Batches of one blend_range call (block-uniform): blended, and left unread
+// because an earlier chunk saturated the tile or because every pixel had stopped.
+struct BatchCount {
+    int blended, skip_flag, skip_done;
+};
+
 // Front-to-back blend of list positions [s, e) for the calling thread's pixel.
 // All threads of the CTA must call it.  When sat_slot >= 0 the chunk stops
 // early once sat[sat_slot] < chunk (an earlier chunk saturated the tile).
@@ -138,14 +145,23 @@ struct Smem {
 // Returns true if it stopped on the saturation signal.
 __device__ __forceinline__ bool blend_range(const RasterArgs& A, Smem& S, int tx, int ty, float px, float py,
                             int64_t s, int64_t e, PixelState& st, int sat_slot, int chunk,
-                            bool write_cmask) {
+                            bool write_cmask, BatchCount& bc) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    bc = BatchCount{0, 0, 0};
     for (int64_t bs = s; bs < e; bs += kBatch) {
         if (tid == 0)
             S.flag = (sat_slot >= 0 && chunk > 0) ? (*(volatile int*)(A.sat + sat_slot) < chunk) : 0;
         const int live = __syncthreads_or(!st.done);
-        if (!live) return false;
-        if (S.flag) return true;
+        const int left = (int)((e - bs + kBatch - 1) / kBatch);
+        if (!live) {
+            bc.skip_done = left;
+            return false;
+        }
+        if (S.flag) {
+            bc.skip_flag = left;
+            return true;
+        }
+        ++bc.blended;
         const int64_t j = bs + tid;
         if (tid < 8 * (kBatch / 32)) S.cm[tid] = 0u;
         if (j < e) {
@@ -224,6 +240,7 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
     __shared__ uint64_t s_cost[kPolicyThreads / 32];
     __shared__ int s_cand[kPolicyThreads / 32];
     __shared__ int s_hk[2];
+    __shared__ int s_nz[kPolicyThreads / 32], s_nmin[kPolicyThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     auto count_at = [&](int j) -> double {
         if (j >= nt) return 0.0;
@@ -235,19 +252,39 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
     const int hm = cfg.split_mode == 0 ? min(nt, cfg.h_max) : 0;
     const double N1 = count_at(0);
     const double n_first = tid < hm * 4 ? count_at(1 + (tid >> 2)) : 0.0;
-    // N_total: an integer sum (exactly the double sum of the counts, all below 2^53)
+    // N_total: an integer sum (exactly the double sum of the counts, all below 2^53);
+    // beside it the lightest non-empty tile and the number of non-empty tiles
     long long part = 0;
+    int nz = 0, nmin = INT_MAX;
     for (int t = tid; t < nt; t += kPolicyThreads) {
         const int2 r = ranges[t];
-        part += (long long)(r.y - r.x);
+        const int c = r.y - r.x;
+        part += (long long)c;
+        if (c > 0) {
+            ++nz;
+            nmin = min(nmin, c);
+        }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    if (lane == 0) s_tot[warp] = part;
+    for (int o = 16; o > 0; o >>= 1) {
+        part += __shfl_xor_sync(0xffffffffu, part, o);
+        nz += __shfl_xor_sync(0xffffffffu, nz, o);
+        nmin = min(nmin, __shfl_xor_sync(0xffffffffu, nmin, o));
+    }
+    if (lane == 0) {
+        s_tot[warp] = part;
+        s_nz[warp] = nz;
+        s_nmin[warp] = nmin;
+    }
     __syncthreads();
     long long itot = 0;
+    int inz = 0, imin = INT_MAX;
 #pragma unroll
-    for (int w = 0; w < kPolicyThreads / 32; ++w) itot += s_tot[w];
+    for (int w = 0; w < kPolicyThreads / 32; ++w) {
+        itot += s_tot[w];
+        inz += s_nz[w];
+        imin = min(imin, s_nmin[w]);
+    }
     const double tot = (double)itot;
     // Eq. 6 multiplied by K > 0 (same minimiser, no division), in round-to-nearest
     // double with no contraction: K T(h, k) = max(N_total + lambda h k, K l) + beta K l,
@@ -339,6 +376,11 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
         ctrl[kCtlQueueFwd] = 0;
         ctrl[kCtlQueueBwd] = 0;
         ctrl[kCtlError] = 0;
+        ctrl[kCtlNMax] = (int)N1;
+        ctrl[kCtlNMinNz] = inz > 0 ? imin : 0;
+        ctrl[kCtlNTotal] = (int)itot;  // pair counts stay below 2^31
+        ctrl[kCtlNonEmpty] = inz;
+        for (int w = kCtlBatchTile; w <= kCtlDiscard; ++w) ctrl[w] = 0;
     }
 }
 
@@ -364,8 +406,10 @@ __global__ void __launch_bounds__(kThreads, 5) raster_fwd_kernel(RasterArgs A) {
         const bool inside = x < A.W && y < A.H;
         const float px = (float)x + 0.5f, py = (float)y + 0.5f;
         PixelState st{1.f, 0.f, 0.f, 0.f, 0, -1, !inside};
+        BatchCount bc;
         if (it.slot < 0) {
-            blend_range(A, S, tx, ty, px, py, it.s, it.e, st, -1, 0, true);
+            blend_range(A, S, tx, ty, px, py, it.s, it.e, st, -1, 0, true, bc);
+            if (tid == 0) atomicAdd(A.ctrl + kCtlBatchTile, bc.blended);
             if (inside) {
                 const int64_t p = (int64_t)y * A.W + x;
                 A.image[3 * p] = st.cr;
@@ -378,7 +422,13 @@ __global__ void __launch_bounds__(kThreads, 5) raster_fwd_kernel(RasterArgs A) {
             continue;
         }
         // ---- a depth chunk of a split tile: blend from T = 1 ----
-        blend_range(A, S, tx, ty, px, py, it.s, it.e, st, it.slot, it.chunk, true);
+        blend_range(A, S, tx, ty, px, py, it.s, it.e, st, it.slot, it.chunk, true, bc);
+        if (tid == 0) {
+            A.cbatch[it.slot * kMaxChunks + it.chunk] = bc.blended;
+            atomicAdd(A.ctrl + kCtlBatchChunk, bc.blended);
+            atomicAdd(A.ctrl + kCtlSkipFlag, bc.skip_flag);
+            atomicAdd(A.ctrl + kCtlSkipDone, bc.skip_done);
+        }
         const int64_t pidx = ((int64_t)it.slot * kMaxChunks + it.chunk) * kThreads + tid;
         A.part_c[pidx] = make_float4(st.cr, st.cg, st.cb, st.T);
         A.part_n[pidx] = make_int2(st.n, st.last);
@@ -394,8 +444,11 @@ __global__ void __launch_bounds__(kThreads, 5) raster_fwd_kernel(RasterArgs A) {
         PixelState acc{1.f, 0.f, 0.f, 0.f, 0, -1, !inside};
         const int2 rr = A.ranges[it.tile];
         const int64_t len = (int64_t)rr.y - rr.x;
+        int discard = 0;
         for (int p = 0; p < it.k; ++p) {
             const int64_t slotp = ((int64_t)it.slot * kMaxChunks + p) * kThreads + tid;
+            // every pixel stopped before chunk p: its blended batches were wasted
+            if (__syncthreads_and(acc.done)) discard += __ldcg(A.cbatch + it.slot * kMaxChunks + p);
             const float Tb = acc.T;
             const float cr0 = acc.cr, cg0 = acc.cg, cb0 = acc.cb;
             bool replay = false;
@@ -420,8 +473,9 @@ __global__ void __launch_bounds__(kThreads, 5) raster_fwd_kernel(RasterArgs A) {
                 // pixels whose stop lies in it
                 PixelState rs = acc;
                 rs.done = !replay;
+                BatchCount rc;
                 blend_range(A, S, tx, ty, px, py, chunk_lo(rr.x, len, p, it.k),
-                            chunk_lo(rr.x, len, p + 1, it.k), rs, -1, 0, false);
+                            chunk_lo(rr.x, len, p + 1, it.k), rs, -1, 0, false, rc);
                 if (replay) {
                     acc = rs;
                     acc.done = rs.T < kTMin;
@@ -431,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, 5) raster_fwd_kernel(RasterArgs A) {
             A.bstate[slotp] = make_float4(acc.T, acc.cr - cr0, acc.cg - cg0, acc.cb - cb0);
             (void)Tb;
         }
+        if (tid == 0 && discard) atomicAdd(A.ctrl + kCtlDiscard, discard);
         // colour added by chunks q > p ("colour behind" chunk p)
         {
             float br = 0.f, bg = 0.f, bb = 0.f;
@@ -835,6 +890,7 @@ RasterLayout raster_layout(int W, int H, int h_max, int64_t capacity) {
     L.off_ctrl = take(kCtlWords * sizeof(int));
     L.off_sat = take(hm * sizeof(int));
     L.off_done = take(hm * sizeof(int));
+    L.off_cbatch = take(hm * kMaxChunks * sizeof(int));
     L.off_part_c = take(px * sizeof(float4));
     L.off_part_n = take(px * sizeof(int2));
     L.off_bwd = take(px * sizeof(float4));
@@ -858,6 +914,7 @@ static RasterArgs make_args(const CamParams& cam, const float* splats, const int
     A.ctrl = reinterpret_cast<int*>(ws + L.off_ctrl);
     A.sat = reinterpret_cast<int*>(ws + L.off_sat);
     A.done = reinterpret_cast<int*>(ws + L.off_done);
+    A.cbatch = reinterpret_cast<int*>(ws + L.off_cbatch);
     A.part_c = reinterpret_cast<float4*>(ws + L.off_part_c);
     A.part_n = reinterpret_cast<int2*>(ws + L.off_part_n);
     A.bstate = reinterpret_cast<float4*>(ws + L.off_bwd);

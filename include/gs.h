@@ -273,10 +273,18 @@ gs_status gs_project_bwd(const gs_camera* cam, int64_t n, int32_t sh_degree, con
 
 /*
  * gs_raster_stats -- diagnostics of the last gs_rasterize_fwd on a workspace.
- * Synchronises the stream and copies to host out[8]:
+ * Synchronises the stream and copies to host out[16]:
  *   out[0] h*  (tiles split)        out[1] k*  (chunks per split tile)
  *   out[2] K   (resident CTAs)      out[3] work items of the persistent kernel
  *   out[4] device error word (0 = none)
+ *   per-frame tile load ("Mitigating SM-Level Load Imbalance...", Sec. 3.1):
+ *   out[5] pairs of the heaviest tile   out[6] of the lightest non-empty tile
+ *   out[7] pairs of all tiles           out[8] non-empty tiles
+ *   256-splat batches of the forward (Sec. 4.2): out[9] blended by whole tiles,
+ *   out[10] blended by depth chunks, out[11] left unread by chunks that saw
+ *   the saturation flag, out[12] left unread by chunks whose pixels had all
+ *   stopped, out[13] blended by chunks the composition discarded (every pixel
+ *   had stopped before them)
  */
 gs_status gs_raster_stats(const void* workspace, size_t workspace_bytes, int64_t* out,
                           void* stream);

@@ -160,3 +160,15 @@ def test_clock_summary_reads_nvidia_smi_lines():
     assert s.summary()["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
     s.lines = []
     assert s.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+
+def test_imbalance_reports_the_tile_load_against_the_per_cta_share():
+    st = {"resident_ctas": 760, "n_total": 1_520_000, "n_max": 10_000, "nonempty_tiles": 4000,
+          "n_min_nonempty": 2, "h": 3, "k": 4, "batches_tiles": 9000, "batches_chunks": 120,
+          "batches_skipped_on_flag": 30, "batches_skipped_done": 5, "batches_discarded": 7}
+    out = bench.imbalance(st, 4346)
+    assert out["max_over_share"] == pytest.approx(10_000 / (1_520_000 / 760))
+    assert out["max_over_min"] == pytest.approx(5000)
+    assert out["n_mean"] == pytest.approx(1_520_000 / 4346)
+    assert out["n_mean_nonempty"] == pytest.approx(380)
+    assert (out["h"], out["k"], out["batches"]["discarded"]) == (3, 4, 7)

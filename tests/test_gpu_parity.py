@@ -103,6 +103,17 @@ def test_forced_split_tiles_match_sequential():
         g, ref = _full_parity(sc, cam, w, settings=s, name=f"split{h}x{k}:")
         st = g.r.stats()
         assert (st["h"], st["k"]) == (h, k)
+        # every 256-splat batch of every chunk is blended or skipped, and counted once
+        counts = (g.ranges[:, 1] - g.ranges[:, 0])[g.lpt].astype(np.int64)
+        want = 0
+        for t in range(h):
+            lo = [(int(counts[t]) * p) // k for p in range(k + 1)]
+            want += sum(-(-(lo[p + 1] - lo[p]) // 256) for p in range(k))
+        got = (st["batches_chunks"] + st["batches_skipped_on_flag"] +
+               st["batches_skipped_done"])
+        assert got == want, (st, want)
+        assert 0 <= st["batches_discarded"] <= st["batches_chunks"]
+        assert st["batches_tiles"] <= sum(-(-int(c) // 256) for c in counts[h:])
 
 
 def test_policy_matches_oracle_eq6():
@@ -117,6 +128,10 @@ def test_policy_matches_oracle_eq6():
                             beta=float(np.float32(s.policy_beta)),
                             eps=float(np.float32(s.policy_eps)), h_max=s.h_max)
     assert (st["h"], st["k"]) == (h, k)
+    # the per-frame tile load the policy saw
+    nz = counts[counts > 0]
+    assert (st["n_max"], st["n_total"]) == (int(counts.max()), int(counts.sum()))
+    assert (st["n_min_nonempty"], st["nonempty_tiles"]) == (int(nz.min()), len(nz))
 
 
 def test_config2_full():
