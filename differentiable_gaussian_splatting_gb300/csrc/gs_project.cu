@@ -237,6 +237,19 @@ __device__ __forceinline__ Projected project_chain(const CamParams& cam, float m
     float P00 = radd(radd(rmul(n0[0], n0[0]), rmul(n0[1], n0[1])), rmul(n0[2], n0[2]));
     float P01 = radd(radd(rmul(n0[0], n1[0]), rmul(n0[1], n1[1])), rmul(n0[2], n1[2]));
     float P11 = radd(radd(rmul(n1[0], n1[0]), rmul(n1[1], n1[1])), rmul(n1[2], n1[2]));
+    // A support that cannot reach the image gets no tile from the spans: cull it
+    // before the threshold, the conic factor and the extents.  o < 1 gives
+    // tau < 2 ln 255 < 11.1, so the padded half extents (the spans' widening
+    // included) stay below sqrt(11.1 Sigma'xx) * 1.001 + 0.02 and likewise in y;
+    // a box that misses the pixel-centre hull of the image by those bounds has
+    // no tile, which the full chain would also find (the outputs are the same).
+    if (P00 >= 0.f && P11 >= 0.f) {
+        const float bx = fmaf(sqrt_approx(11.1f * P00), 1.001f, 0.02f);
+        const float by = fmaf(sqrt_approx(11.1f * P11), 1.001f, 0.02f);
+        if (mux + bx < 0.5f || mux - bx > (float)cam.W - 0.5f || muy + by < 0.5f ||
+            muy - by > (float)cam.H - 0.5f)
+            return P;
+    }
     // det Sigma' = |n0 x n1|^2 (Lagrange's identity) with n0 x n1 = s0 s1 s2 S^-1 R^T (T0 x T1):
     // a sum of squares, free of the cancellation of P00 P11 - P01^2 for thin splats
     float w0 = rsub(rmul(T0[1], T1[2]), rmul(T0[2], T1[1]));
@@ -346,10 +359,18 @@ __global__ void __launch_bounds__(kProjThreads) project_kernel(CamParams cam, in
         if (nrows > 0 && P.mux + px >= 0.5f && P.mux - px <= (float)cam.W - 0.5f) {
             constexpr int kRowBytes = K * 3 * (int)sizeof(ShT);
             const char* row = reinterpret_cast<const char*>(sh + i * (K * 3));
+            if constexpr (kRowBytes % 16 == 0) {
+                // exactly the row's bytes (whole 128-byte lines would fetch a third
+                // more for a 192-byte row); rows start on 16-byte boundaries
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(row),
+                             "r"(kRowBytes)
+                             : "memory");
+            } else {
 #pragma unroll
-            for (int b = 0; b < kRowBytes; b += 128)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(row + b));
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(row + kRowBytes - 1));
+                for (int b = 0; b < kRowBytes; b += 128)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(row + b));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(row + kRowBytes - 1));
+            }
         }
     }
     S.cnt[tid] = 0;
