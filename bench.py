@@ -356,8 +356,9 @@ def roofline(call, ms, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz):
                 "unit": "GB/s", "frac": achieved / peak, "traffic": profiled_traffic(call),
                 "peak_source": f"{peaks['source']} copy bandwidth"}
     if call == "gs_project":
-        # geometry of every Gaussian, SH of the visible, record of the visible, radii
-        byts = 44 * N + (G - 44) * M + 64 * M + 8 * N
+        # geometry of every Gaussian, SH of the visible; every row of the outputs
+        # (record, depth, radii, tile count: 64 B) is written, culled rows as zeros
+        byts = 44 * N + (G - 44) * M + 64 * N
     elif call == "gs_project_bwd":
         # grad2d and parameters of the visible, every gradient row written, the two flags
         byts = 36 * M + G * M + G * N + 5 * N
@@ -446,8 +447,9 @@ def step_roofline(ms, sc, M, I, E, H, W, peaks, n_sm, sm_mhz, train=False):
     fp32 = FP32_LANES_PER_SM * n_sm * sm_mhz * 1e6  # fp32 ops (an FMA is one)
     sfu = SFU_LANES_PER_SM * n_sm * sm_mhz * 1e6
     phases = {
-        # 44 B of geometry per Gaussian, SH and the 64 B record only for the visible
-        "project": (44 * N + (G - 44) * M + 64 * M + 8 * N, 0, 0),
+        # 44 B of geometry per Gaussian, SH only for the visible, 64 B of outputs per
+        # Gaussian (culled rows are written as zeros)
+        "project": (44 * N + (G - 44) * M + 64 * N, 0, 0),
         # depth sort of the M visible (8 B, 4 passes, read + write) and the pair list
         # (emitted once, then 2 passes read + write)
         "bin_sort": (8 * M * 8 + 8 * I * 5, 0, 0),
