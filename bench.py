@@ -279,19 +279,21 @@ def run_gpu(args):
     sm_mhz = clocks["sm_mhz"] or peaks.get("clocks_under_load", {}).get("sm_mhz_median") or 1462.0
     dom = max(per_call, key=per_call.get)
     M = int((r.tiles_touched > 0).sum().item())
+    T = int((r.touched != 0).sum().item())
     roof = roofline(dom, per_call[dom], sc, M, n_pairs, E, H, W, peaks,
-                    props.multi_processor_count, sm_mhz)
+                    props.multi_processor_count, sm_mhz, T)
     launches = kernel_launches(sc.n, r.capacity, W, H)
     step_roof = step_roofline(ms_per_step, sc, M, n_pairs, E, H, W, peaks,
-                              props.multi_processor_count, sm_mhz)
+                              props.multi_processor_count, sm_mhz, T=T)
     roof["per_call"] = per_call_fractions(per_call, sc, M, n_pairs, E, H, W, peaks,
-                                          props.multi_processor_count, sm_mhz)
+                                          props.multi_processor_count, sm_mhz, T)
     load = imbalance(r.stats(), r.n_tiles)  # the last forward's frame (synchronises)
 
     e2e = None if args.no_e2e else run_e2e(gs, r, sc, cam, w, dev, args, n_pairs)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(sc, cam, w)
+        # the whole view up to the 1.5M scene, every 16th tile of the larger ones
+        cpu = cpu_baseline(sc, cam, w, stride=1 if args.config <= 3 else 16)
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -315,8 +317,10 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def roofline(call, ms, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz):
+def roofline(call, ms, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz, T=None):
     """Algorithmic work of one launch / its average duration, against the binding peak.
+    M: visible Gaussians; T: Gaussians the backward touched (its chain rule reads the
+    parameters and grad2d of those only; M when not given).
     The blend kernels: fp32 ops of the op model against SMs x 128 lanes x the sampled SM
     clock (Tops/s, reported in the TFLOP/s unit), with the SFU fraction and the flop-model
     fraction beside it."""
@@ -346,10 +350,11 @@ def roofline(call, ms, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz):
                 "peak_source": f"{n_sm} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 x {sm_mhz:.0f} MHz (sampled)",
                 "work": f"{LOSS_FLOPS_PER_PIXEL} flops x {H * W} pixels"}
     N, G = sc.n, 44 + 12 * (sc.sh_degree + 1) ** 2  # G: parameter bytes per Gaussian
+    T = M if T is None else T
     if call == "gs_project_bwd_adam":
-        # grad2d of the visible, the two flags, parameters and both moments read and
+        # grad2d of the touched, the two flags, parameters and both moments read and
         # written, the activated scales and opacities written
-        byts = 36 * M + 5 * N + 6 * G * N + 16 * N
+        byts = 36 * T + 5 * N + 6 * G * N + 16 * N
         achieved = byts / (ms * 1e-3) / 1e9
         peak = float(peaks["hbm_gbs"])
         return {"kernel": call, "bound": "hbm", "achieved": achieved, "peak": peak,
@@ -360,8 +365,8 @@ def roofline(call, ms, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz):
         # (record, depth, radii, tile count: 64 B) is written, culled rows as zeros
         byts = 44 * N + (G - 44) * M + 64 * N
     elif call == "gs_project_bwd":
-        # grad2d and parameters of the visible, every gradient row written, the two flags
-        byts = 36 * M + G * M + G * N + 5 * N
+        # grad2d and parameters of the touched, every gradient row written, the two flags
+        byts = 36 * T + G * T + G * N + 5 * N
     else:  # gs_bin_sort
         byts = 8 * M * 8 + 8 * n_pairs * 5
     achieved = byts / (ms * 1e-3) / 1e9
@@ -387,11 +392,11 @@ def imbalance(stats: dict, n_tiles: int) -> dict:
                         ("tiles", "chunks", "skipped_on_flag", "skipped_done", "discarded")}}
 
 
-def per_call_fractions(per_call, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz) -> dict:
+def per_call_fractions(per_call, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz, T=None) -> dict:
     """Each call's roofline fraction (bound and frac) from its own event time."""
     out = {}
     for call, ms in per_call.items():
-        r = roofline(call, ms, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz)
+        r = roofline(call, ms, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz, T)
         out[call] = {"bound": r["bound"], "frac": r["frac"], "ms": ms}
     return out
 
@@ -436,12 +441,13 @@ def profiled_traffic(call, workload="scene-1.5M-1297x840"):
     return int(fields["traffic_bytes_per_launch"]) if "traffic_bytes_per_launch" in fields else None
 
 
-def step_roofline(ms, sc, M, I, E, H, W, peaks, n_sm, sm_mhz, train=False):
+def step_roofline(ms, sc, M, I, E, H, W, peaks, n_sm, sm_mhz, train=False, T=None):
     """Whole-step roofline: per phase the largest of bytes / HBM, fp32 flops / fp32 peak and
     SFU ops / SFU peak, summed over the phases; frac = that time / the measured step.
     train: the training step (loss phase; Adam on parameters and moments in place of the
     gradient rows)."""
     N, P = sc.n, H * W
+    T = M if T is None else T  # Gaussians the backward touched
     G = 44 + 12 * (sc.sh_degree + 1) ** 2  # parameter bytes per Gaussian
     hbm = float(peaks["hbm_gbs"]) * 1e9
     fp32 = FP32_LANES_PER_SM * n_sm * sm_mhz * 1e6  # fp32 ops (an FMA is one)
@@ -455,13 +461,13 @@ def step_roofline(ms, sc, M, I, E, H, W, peaks, n_sm, sm_mhz, train=False):
         "bin_sort": (8 * M * 8 + 8 * I * 5, 0, 0),
         "forward": (48 * I + 24 * P, OPS_FWD_PER_E * E, SFU_FWD_PER_E * E),
         # raster backward and the chain rule: records, pixel state and dL/dimage, grad2d,
-        # parameters of the visible, every gradient row written
-        "backward": (48 * I + 36 * P + 36 * M + G * M + G * N, OPS_BWD_PER_E * E,
+        # parameters of the touched, every gradient row written
+        "backward": (48 * I + 36 * P + 36 * T + G * T + G * N, OPS_BWD_PER_E * E,
                      SFU_BWD_PER_E * E),
     }
     if train:
         phases["loss"] = (36 * P, LOSS_FLOPS_PER_PIXEL * P // 2, 0)  # its FMAs
-        phases["backward"] = (48 * I + 36 * P + 36 * M + 5 * N + 6 * G * N + 16 * N,
+        phases["backward"] = (48 * I + 36 * P + 36 * T + 5 * N + 6 * G * N + 16 * N,
                               OPS_BWD_PER_E * E, SFU_BWD_PER_E * E)
     out, total = {}, 0.0
     for k, (b, f, x) in phases.items():
@@ -642,8 +648,12 @@ def cpu_baseline(sc, cam, w, stride: int = 1):
     """The oracle over the whole view, on every host core (the headline) and on one."""
     cores = host_cores()
     what = "every tile" if stride == 1 else f"every {stride}th tile in LPT order"
-    pairs, dt, _ = oracle_sample_step(sc, cam, w, stride, workers=cores)
+    if stride > 1:
+        # the sampled step is short beside the first touch of the large scenes' arrays:
+        # one untimed pass first, so that neither variant pays it
+        oracle_sample_step(sc, cam, w, stride, workers=cores)
     pairs1, dt1, _ = oracle_sample_step(sc, cam, w, stride, workers=1)
+    pairs, dt, _ = oracle_sample_step(sc, cam, w, stride, workers=cores)
     return {"value": pairs / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"one view: all projections and tile counts, forward + backward of "
                       f"{what} ({pairs} pairs) and the chain rule, the unmodified oracle calls "
@@ -778,13 +788,14 @@ def run_train(args):
     sm_mhz = clocks["sm_mhz"] or peaks.get("clocks_under_load", {}).get("sm_mhz_median") or 1462.0
     dom = max(per_call, key=per_call.get)
     M = int((r.tiles_touched > 0).sum().item())
+    T = int((r.touched != 0).sum().item())
     E = int(r.n_contrib.sum().item())
     roof = roofline(dom, per_call[dom], sc, M, pairs1, E, H, W, peaks,
-                    props.multi_processor_count, sm_mhz)
+                    props.multi_processor_count, sm_mhz, T)
     step_roof = step_roofline(ms_per_step, sc, M, pairs1, E, H, W, peaks,
-                              props.multi_processor_count, sm_mhz, train=True)
+                              props.multi_processor_count, sm_mhz, train=True, T=T)
     roof["per_call"] = per_call_fractions(per_call, sc, M, pairs1, E, H, W, peaks,
-                                          props.multi_processor_count, sm_mhz)
+                                          props.multi_processor_count, sm_mhz, T)
     launches = kernel_launches(sc.n, r.capacity, W, H) + 2  # the loss: tiles + final sum
     if rank == 0:
         print(json.dumps({

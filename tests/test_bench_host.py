@@ -172,3 +172,11 @@ def test_imbalance_reports_the_tile_load_against_the_per_cta_share():
     assert out["n_mean"] == pytest.approx(1_520_000 / 4346)
     assert out["n_mean_nonempty"] == pytest.approx(380)
     assert (out["h"], out["k"], out["batches"]["discarded"]) == (3, 4, 7)
+
+
+def test_chain_rule_bytes_count_the_touched_gaussians():
+    # the chain rule reads grad2d and the parameters of the Gaussians the backward
+    # touched (T <= M), and writes every gradient row
+    r = bench.roofline("gs_project_bwd", 0.01, SC, 600, 5000, 0, 100, 100, PEAKS, N_SM, MHZ, T=250)
+    assert r["achieved"] == pytest.approx((36 * 250 + 236 * 250 + 236 * 1000 + 5 * 1000)
+                                          / 0.01e-3 / 1e9)
