@@ -326,9 +326,11 @@ def roofline(call, ms, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz, T=None):
     fraction beside it."""
     if call in ("gs_rasterize_fwd", "gs_rasterize_bwd"):
         fwd = call == "gs_rasterize_fwd"
-        ops = (OPS_FWD_PER_E if fwd else OPS_BWD_PER_E) * E
+        ops_e = OPS_FWD_PER_E if fwd else OPS_BWD_PER_E
+        flops_e = FLOPS_FWD_PER_E if fwd else FLOPS_BWD_PER_E
+        ops = ops_e * E
         sfu = (SFU_FWD_PER_E if fwd else SFU_BWD_PER_E) * E
-        flops = (FLOPS_FWD_PER_E if fwd else FLOPS_BWD_PER_E) * E
+        flops = flops_e * E
         hz = n_sm * sm_mhz * 1e6
         peak = FP32_LANES_PER_SM * hz / 1e12
         achieved = ops / (ms * 1e-3) / 1e12
@@ -336,10 +338,10 @@ def roofline(call, ms, sc, M, n_pairs, E, H, W, peaks, n_sm, sm_mhz, T=None):
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": profiled_traffic(call),
                 "peak_source": f"{n_sm} SMs x {FP32_LANES_PER_SM} fp32 lanes x {sm_mhz:.0f} MHz "
                                f"(sampled), one op per lane per cycle",
-                "work": f"{ops // E} fp32 ops (an FMA is one op) x {E} contributing pairs",
+                "work": f"{ops_e} fp32 ops (an FMA is one op) x {E} contributing pairs",
                 "sfu_frac": sfu / (ms * 1e-3) / (SFU_LANES_PER_SM * hz),
                 "flop_model": {"frac": flops / (ms * 1e-3) / (2 * FP32_LANES_PER_SM * hz),
-                               "work": f"{flops // E} flops (an FMA is two) x {E} pairs, "
+                               "work": f"{flops_e} flops (an FMA is two) x {E} pairs, "
                                        f"against 2 x the fp32 lanes"}}
     if call == "gs_loss_l1_ssim":
         flops = LOSS_FLOPS_PER_PIXEL * H * W

@@ -180,3 +180,9 @@ def test_chain_rule_bytes_count_the_touched_gaussians():
     r = bench.roofline("gs_project_bwd", 0.01, SC, 600, 5000, 0, 100, 100, PEAKS, N_SM, MHZ, T=250)
     assert r["achieved"] == pytest.approx((36 * 250 + 236 * 250 + 236 * 1000 + 5 * 1000)
                                           / 0.01e-3 / 1e9)
+
+
+def test_raster_roofline_without_contributing_pairs():
+    # an empty view (no pixel blends anything) reports zero, not a division error
+    r = bench.roofline("gs_rasterize_bwd", 0.1, SC, 0, 0, 0, 100, 100, PEAKS, N_SM, MHZ)
+    assert r["achieved"] == 0 and r["frac"] == 0
