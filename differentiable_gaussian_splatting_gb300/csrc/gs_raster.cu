@@ -26,6 +26,7 @@
 // last blended splat, T recovered by division by (1 - alpha); the nine
 // per-splat derivatives of a warp are summed by a halving reduce-scatter of
 // 12 shuffles, after which nine lanes add them atomically.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -225,8 +226,14 @@ __device__ __forceinline__ bool blend_range(const RasterArgs& A, Smem& S, int tx
 }
 
 // ---------------------------------------------------------------------------
-// per-frame chunking policy (Ryu & Yoo, Eq. 6), one block
+// per-frame chunking policy (Ryu & Yoo, Eq. 6), one cluster of kPolicyCluster
+// blocks: every block sums the tile counts, block r evaluates the candidates
+// c = r mod kPolicyCluster (the float64 arithmetic spread over as many SMs),
+// and block 0 takes the least of the blocks' best through distributed shared
+// memory and writes the choice
 // ---------------------------------------------------------------------------
+constexpr int kPolicyCluster = 8;
+
 __device__ __forceinline__ bool key_less(uint64_t ca, int ia, uint64_t cb, int ib) {
     return ca < cb || (ca == cb && ia < ib);
 }
@@ -236,7 +243,12 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
                                                                 int nt, int K, RasterConfig cfg,
                                                                 int* ctrl, int* sat, int* done) {
     grid_dep_sync();
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
     __shared__ long long s_tot[kPolicyThreads / 32];
+    __shared__ uint64_t s_best;  // this block's least (cost, candidate)
+    __shared__ int s_best_cand;
     __shared__ uint64_t s_cost[kPolicyThreads / 32];
     __shared__ int s_cand[kPolicyThreads / 32];
     __shared__ int s_hk[2];
@@ -251,7 +263,8 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
     // N_1 and N_{h+1} of this thread's first candidate
     const int hm = cfg.split_mode == 0 ? min(nt, cfg.h_max) : 0;
     const double N1 = count_at(0);
-    const double n_first = tid < hm * 4 ? count_at(1 + (tid >> 2)) : 0.0;
+    const int cand0 = rank + kPolicyCluster * tid;
+    const double n_first = cand0 < hm * 4 ? count_at(1 + (cand0 >> 2)) : 0.0;
     // N_total: an integer sum (exactly the double sum of the counts, all below 2^53);
     // beside it the lightest non-empty tile and the number of non-empty tiles
     long long part = 0;
@@ -302,12 +315,12 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
         // non-negative, so their bit patterns order as unsigned integers.
         uint64_t best = ~0ull;
         int cand_best = INT_MAX;
-        for (int cand = tid; cand < hm * 4; cand += kPolicyThreads) {
+        for (int cand = cand0; cand < hm * 4; cand += kPolicyCluster * kPolicyThreads) {
             const int h = 1 + (cand >> 2);
             const int k = 2 << (cand & 3);
             // 1 / k = 2^-((cand & 3) + 1), built from its exponent bits (exact, no division)
             const double inv_k = __longlong_as_double((long long)(1022 - (cand & 3)) << 52);
-            const double l = fmax(__dmul_rn(N1, inv_k), cand == tid ? n_first : count_at(h));
+            const double l = fmax(__dmul_rn(N1, inv_k), cand == cand0 ? n_first : count_at(h));
             const double Kl = __dmul_rn(Kd, l);
             const double work = __dadd_rn(tot, __dmul_rn(__dmul_rn(lam, (double)h), (double)k));
             const double cost = __dadd_rn(fmax(work, Kl), __dmul_rn(beta, Kl));
@@ -344,6 +357,28 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
                 }
             }
             if (lane == 0) {
+                s_best = best;
+                s_best_cand = cand_best;
+            }
+        }
+        cluster.sync();
+        if (rank == 0 && warp == 0) {
+            best = ~0ull;
+            cand_best = INT_MAX;
+            if (lane < kPolicyCluster) {
+                best = *cluster.map_shared_rank(&s_best, lane);
+                cand_best = *cluster.map_shared_rank(&s_best_cand, lane);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const uint64_t oc = __shfl_xor_sync(0xffffffffu, best, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, cand_best, o);
+                if (key_less(oc, oi, best, cand_best)) {
+                    best = oc;
+                    cand_best = oi;
+                }
+            }
+            if (lane == 0) {
                 int h_best = 0, k_best = 1;
                 // a split must cost strictly less than no split (h = 0 wins ties) ...
                 const double bc = __longlong_as_double((long long)best);
@@ -360,10 +395,13 @@ __global__ void __launch_bounds__(kPolicyThreads) policy_kernel(const int32_t* _
                 s_hk[1] = k_best;
             }
         }
+        // the other blocks' shared memory stays readable until block 0 has read it
+        cluster.sync();
         __syncthreads();
         bh = s_hk[0];
         bk = s_hk[1];
     }
+    if (rank != 0) return;
     for (int j = tid; j < bh; j += kPolicyThreads) {
         sat[j] = INT_MAX;
         done[j] = 0;
@@ -935,7 +973,8 @@ cudaError_t run_raster_fwd(const CamParams& cam, const RasterConfig& cfg, const 
     A.n_contrib = n_contrib;
     A.last_idx = last_idx;
     const int nt = cam.ntx * cam.nty;
-    cudaError_t err = launch(policy_kernel, 1, kPolicyThreads, 0, st, lpt_order,
+    cudaError_t err = launch_clustered(policy_kernel, kPolicyCluster, kPolicyCluster,
+                                       kPolicyThreads, 0, st, lpt_order,
                              (const int2*)A.ranges, nt, K, cfg, A.ctrl, A.sat, A.done);
     if (err != cudaSuccess) return err;
     return launch(raster_fwd_kernel, K, kThreads, 0, st, A);
