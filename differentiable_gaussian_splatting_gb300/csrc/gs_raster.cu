@@ -914,8 +914,6 @@ static int resident_bwd(int device) {
 }
 
 RasterLayout raster_layout(int W, int H, int h_max, int64_t capacity) {
-    (void)W;
-    (void)H;
     RasterLayout L{};
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -923,7 +921,9 @@ RasterLayout raster_layout(int W, int H, int h_max, int64_t capacity) {
         off = (off + bytes + 255) & ~size_t(255);
         return o;
     };
-    const size_t hm = (size_t)std::max(h_max, 1);
+    // at most min(h_max, tiles) tiles are split (the policy's candidates)
+    const int64_t nt = (((int64_t)W + kTile - 1) / kTile) * (((int64_t)H + kTile - 1) / kTile);
+    const size_t hm = (size_t)std::max<int64_t>(std::min<int64_t>(h_max, nt), 1);
     const size_t px = hm * kMaxChunks * kThreads;
     L.off_ctrl = take(kCtlWords * sizeof(int));
     L.off_sat = take(hm * sizeof(int));

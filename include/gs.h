@@ -101,7 +101,7 @@ typedef struct gs_settings {
                             2: split the force_h heaviest tiles into force_k chunks */
     int32_t force_h;     /* split_mode 2: number of tiles to split (<= h_max) */
     int32_t force_k;     /* split_mode 2: chunks per split tile, 2..GS_MAX_CHUNKS */
-    int32_t h_max;       /* most tiles that may be split (sizes the workspace) */
+    int32_t h_max;       /* most tiles that may be split; min(h_max, tiles) sizes the workspace */
     float policy_lambda; /* per-chunk overhead in Gaussian-equivalents (Eq. 6) */
     float policy_beta;   /* residual-imbalance penalty (Eq. 6) */
     float policy_eps;    /* split only if the estimate improves by this fraction */

@@ -116,14 +116,19 @@ def test_forced_split_tiles_match_sequential():
         assert st["batches_tiles"] <= sum(-(-int(c) // 256) for c in counts[h:])
 
 
-def test_policy_matches_oracle_eq6():
+@pytest.mark.parametrize("h_max", [256, 4096, 65536])
+def test_policy_matches_oracle_eq6(h_max):
+    """(h, k) of the 8-block policy search equals the oracle's Eq. 6 on the same counts;
+    h_max 4096 and 65536 (every one of the 8,160 tiles a candidate: 32,640 candidates,
+    several per thread) exercise the search loop and its cross-block minimum."""
     import differentiable_gaussian_splatting_gb300 as gs
 
     sc, cam = ss.make_config(4, n=300_000)
-    g = run_forward(sc, cam)
+    s = gs.gs_default_settings()
+    s.h_max = h_max
+    g = run_forward(sc, cam, settings=s)
     st = g.r.stats()
     counts = (g.ranges[:, 1] - g.ranges[:, 0])[g.lpt].astype(np.int64)
-    s = gs.gs_default_settings()
     h, k, _ = oracle.policy(counts, st["resident_ctas"], lam=float(np.float32(s.policy_lambda)),
                             beta=float(np.float32(s.policy_beta)),
                             eps=float(np.float32(s.policy_eps)), h_max=s.h_max)
