@@ -617,13 +617,19 @@ def oracle_sample_step(sc, cam, w, tile_stride: int, workers: int = 1):
     else:
         proj = oracle.project(sc, cam)
     ntx, nty = oracle.n_tiles(cam)
-    counts = oracle.bin_sort(cam, proj, np.zeros(ntx * nty, np.uint8))
-    sel = np.zeros(ntx * nty, np.uint8)
-    sel[counts.lpt_order[::tile_stride]] = 1
-    b = oracle.bin_sort(cam, proj, sel)
+    if tile_stride == 1:
+        b = oracle.bin_sort(cam, proj)
+        sel = np.ones(ntx * nty, np.uint8)
+        counts = b
+    else:
+        counts = oracle.bin_sort(cam, proj, np.zeros(ntx * nty, np.uint8))
+        sel = np.zeros(ntx * nty, np.uint8)
+        sel[counts.lpt_order[::tile_stride]] = 1
+        b = oracle.bin_sort(cam, proj, sel)
+    # the method's gradient only (the error-bound sums the parity tests use are not formed)
     if workers > 1:
         oracle.blend_parallel(cam, proj, b, workers=workers)
-        g2 = oracle.blend_bwd_parallel(cam, proj, b, w, workers=workers).grad2d
+        g2 = oracle.blend_bwd_parallel(cam, proj, b, w, workers=workers, bounds=False).grad2d
 
         def chain(rows):
             p = oracle.Projection(proj.splat[rows], proj.rgb[rows], proj.radii[rows],
@@ -633,7 +639,7 @@ def oracle_sample_step(sc, cam, w, tile_stride: int, workers: int = 1):
         _threads(chain, _row_chunks(sc.n, 4 * workers), workers)
     else:
         oracle.blend(cam, proj, b)
-        g2, _ = oracle.blend_bwd(cam, proj, b, w)
+        g2 = oracle.blend_bwd_bounds(cam, proj, b, w, bounds=False).grad2d
         oracle.project_bwd(sc, cam, proj, g2)
     dt = time.perf_counter() - t0
     return int(b.counts[sel.astype(bool)].sum()), dt, int(counts.counts.sum())

@@ -218,9 +218,13 @@ def bin_sort(cam, proj: Projection, sel: np.ndarray | None = None, variant: str 
     sel_a = None if sel is None else np.ascontiguousarray(sel, dtype=np.uint8)
     args = (n, _p(vm), _p(intr), W, H, zn, _p(proj.splat), _p(proj.tiles_touched), _p(sel_a),
             _p(counts), _p(ranges), _p(lpt), _p(sel_off))
-    need = lib.ora_bin(*args, None, 0)
-    ids = np.zeros(max(need, 1), np.int32)
-    lib.ora_bin(*args, _p(ids), need)
+    # every Gaussian gives at most tiles_touched pairs, so one call usually suffices
+    cap = int(np.clip(np.asarray(proj.tiles_touched, np.int64), 0, None).sum())
+    ids = np.zeros(max(cap, 1), np.int32)
+    need = lib.ora_bin(*args, _p(ids), cap)
+    if need > cap:
+        ids = np.zeros(need, np.int32)
+        lib.ora_bin(*args, _p(ids), need)
     return Binning(counts, ranges, lpt, sel_a, sel_off, ids[:need])
 
 
@@ -299,13 +303,15 @@ def blend_bwd(cam, proj: Projection, b: Binning, dL_dimg: np.ndarray,
 
 def blend_bwd_bounds(cam, proj: Projection, b: Binning, dL_dimg: np.ndarray,
                      dL_dT: np.ndarray | None = None, stop_last: np.ndarray | None = None,
-                     variant: str = "f32") -> BlendGrads:
+                     variant: str = "f32", bounds: bool = True) -> BlendGrads:
     """blend_bwd with the outcome a renderer took at stop near-ties (stop_last as for
-    blend) and the quantities that bound an fp32 evaluation's error (BlendGrads)."""
+    blend) and the quantities that bound an fp32 evaluation's error (BlendGrads; with
+    bounds=False only grad2d is formed, the other fields are None)."""
     lib = _lib(variant)
     W, H = int(cam.width), int(cam.height)
     n = int(proj.splat.shape[0])
-    out = BlendGrads(*(np.zeros((n, 9), np.float64) for _ in range(4)))
+    out = BlendGrads(*(np.zeros((n, 9), np.float64) if bounds or i == 0 else None
+                       for i in range(4)))
     dimg = np.ascontiguousarray(dL_dimg, dtype=np.float64).reshape(H, W, 3)
     dT = None if dL_dT is None else np.ascontiguousarray(dL_dT, dtype=np.float64).reshape(H, W)
     sl = None if stop_last is None else np.ascontiguousarray(stop_last, np.int32).reshape(H, W)
@@ -360,17 +366,19 @@ def blend_parallel(cam, proj: Projection, b: Binning, workers: int | None = None
 
 def blend_bwd_parallel(cam, proj: Projection, b: Binning, dL_dimg: np.ndarray,
                        dL_dT: np.ndarray | None = None, stop_last: np.ndarray | None = None,
-                       workers: int | None = None) -> BlendGrads:
+                       workers: int | None = None, bounds: bool = True) -> BlendGrads:
     """blend_bwd_bounds() of b's tiles split over `workers` host threads; each part's
     per-Gaussian sums (float64) are added, so the result equals the single call's up to
     the order of those additions."""
     workers = workers or os.cpu_count() or 1
-    outs = _threads(lambda p: blend_bwd_bounds(cam, proj, p, dL_dimg, dL_dT, stop_last),
+    outs = _threads(lambda p: blend_bwd_bounds(cam, proj, p, dL_dimg, dL_dT, stop_last,
+                                               bounds=bounds),
                     tile_parts(b, workers), workers)
     res = outs[0]
     for o in outs[1:]:
         for f in ("grad2d", "gabs", "grho", "galt"):
-            getattr(res, f).__iadd__(getattr(o, f))
+            if getattr(res, f) is not None:
+                getattr(res, f).__iadd__(getattr(o, f))
     return res
 
 
