@@ -384,8 +384,10 @@ __global__ void __launch_bounds__(kRsBlock) vis_count(const int32_t* __restrict_
     if (threadIdx.x == 0) bsum[blockIdx.x] = total;
 }
 
-// visible Gaussians, in id order: (depth key, id).  Blocked: each thread owns 16
-// consecutive items, so one block-wide scan of per-thread counts suffices.
+// visible Gaussians, in id order: (depth key, id).  Warp w of a block owns its
+// 512 consecutive ids in 16 sweeps of 32 (lane l takes id 32 r + l of sweep r),
+// so loads and stores are coalesced; a ballot per sweep ranks the visible ones,
+// and one scan of the 8 warps' counts places each warp's run.
 __global__ void __launch_bounds__(kRsBlock) vis_write(const int32_t* __restrict__ tiles_touched,
                                                       const float* __restrict__ depths, int64_t n,
                                                       const int64_t* __restrict__ bsum,
@@ -393,32 +395,38 @@ __global__ void __launch_bounds__(kRsBlock) vis_write(const int32_t* __restrict_
                                                       int32_t* __restrict__ vals,
                                                       uint32_t* __restrict__ dhist) {
     grid_dep_sync();
-    __shared__ int64_t s_warp[kRsWarps];
+    __shared__ int s_cnt[kRsWarps];
     __shared__ uint32_t hist[kMaxPasses][256];
 #pragma unroll
     for (int p = 0; p < kMaxPasses; ++p) hist[p][threadIdx.x] = 0;
-    const int64_t base = (int64_t)blockIdx.x * kRsTile + (int64_t)threadIdx.x * kRsIpt;
-    bool vis[kRsIpt];
-    int64_t c = 0;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t wbase = (int64_t)blockIdx.x * kRsTile + (int64_t)warp * (32 * kRsIpt);
+    uint32_t m[kRsIpt];
+    int cnt = 0;
 #pragma unroll
     for (int r = 0; r < kRsIpt; ++r) {
-        const int64_t idx = base + r;
-        vis[r] = idx < n && tiles_touched[idx] > 0;
-        c += vis[r];
+        const int64_t idx = wbase + 32 * r + lane;
+        m[r] = __ballot_sync(0xffffffffu, idx < n && tiles_touched[idx] > 0);
+        cnt += __popc(m[r]);
     }
-    int64_t total;
-    int64_t pos = bsum[blockIdx.x] + block_exclusive_scan_256<int64_t>(c, s_warp, &total);
+    if (lane == 0) s_cnt[warp] = cnt;
+    __syncthreads();
+    int64_t pos = bsum[blockIdx.x];
+#pragma unroll
+    for (int w = 0; w < kRsWarps; ++w) pos += w < warp ? s_cnt[w] : 0;
+    const uint32_t lt = lanemask_lt();
 #pragma unroll
     for (int r = 0; r < kRsIpt; ++r) {
-        if (vis[r]) {
-            const int64_t idx = base + r;
+        if ((m[r] >> lane) & 1u) {
+            const int64_t idx = wbase + 32 * r + lane;
+            const int64_t at = pos + __popc(m[r] & lt);
             const uint32_t k = __float_as_uint(depths[idx]);  // depth > znear > 0: bits are ordered
-            keys[pos] = k;
-            vals[pos] = (int32_t)idx;
-            ++pos;
+            keys[at] = k;
+            vals[at] = (int32_t)idx;
 #pragma unroll
             for (int p = 0; p < kMaxPasses; ++p) atomicAdd(&hist[p][(k >> (8 * p)) & 255u], 1u);
         }
+        pos += __popc(m[r]);
     }
     __syncthreads();
 #pragma unroll
@@ -666,6 +674,10 @@ __global__ void __launch_bounds__(kEmitThreads) emit_pairs(
 
 // tile ranges [start, end) from the sorted keys (ranges zeroed beforehand);
 // none when the pair list did not fit (counts[1] > capacity)
+// Each thread takes four consecutive sorted keys with one 16-byte load (the key
+// buffer starts on a 16-byte boundary) and their two neighbours; the grid covers
+// the capacity in a few strides, so each thread has one or two loads in flight
+// rather than a long chain of dependent strides.
 __global__ void __launch_bounds__(256) tile_ranges_kernel(const uint32_t* __restrict__ keys,
                                                           const int64_t* __restrict__ counts,
                                                           int64_t capacity,
@@ -673,11 +685,32 @@ __global__ void __launch_bounds__(256) tile_ranges_kernel(const uint32_t* __rest
     grid_dep_sync();
     if (counts[1] > capacity) return;
     const int64_t n = counts[2];
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const uint32_t t = keys[i];
-        if (i == 0 || keys[i - 1] != t) ranges[t].x = (int)i;
-        if (i == n - 1 || keys[i + 1] != t) ranges[t].y = (int)(i + 1);
+    const int64_t ng = (n + 3) / 4;
+    for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < ng;
+         gi += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i0 = 4 * gi;
+        uint32_t k[4];
+        if (i0 + 4 <= n) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(keys) + gi);
+            k[0] = v.x;
+            k[1] = v.y;
+            k[2] = v.z;
+            k[3] = v.w;
+        } else {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) k[r] = i0 + r < n ? keys[i0 + r] : 0u;
+        }
+        const uint32_t prev = i0 > 0 ? keys[i0 - 1] : 0u;
+        const uint32_t next = i0 + 4 < n ? keys[i0 + 4] : 0u;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int64_t i = i0 + r;
+            if (i >= n) break;
+            const bool first = i == 0 || (r == 0 ? prev : k[r - 1]) != k[r];
+            const bool last = i == n - 1 || (r == 3 ? next : k[r + 1]) != k[r];
+            if (first) ranges[k[r]].x = (int)i;
+            if (last) ranges[k[r]].y = (int)(i + 1);
+        }
     }
 }
 
@@ -840,7 +873,12 @@ cudaError_t run_bin_sort_radix(const CamParams& cam, int64_t n, const float* spl
                          thist, sort_err, st, &pks, nullptr);
         if (err != cudaSuccess) return err;
         // 6. tile ranges
-        err = launch(tile_ranges_kernel, 1024, 256, 0, st, (const uint32_t*)pks,
+        int dev = 0, sms = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const unsigned rg = (unsigned)std::max<int64_t>(
+            1, std::min<int64_t>((capacity + 1023) / 1024, 64 * (int64_t)std::max(sms, 1)));
+        err = launch(tile_ranges_kernel, rg, 256, 0, st, (const uint32_t*)pks,
                      (const int64_t*)counts, capacity, ranges);
         if (err != cudaSuccess) return err;
     }
