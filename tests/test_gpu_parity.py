@@ -262,6 +262,21 @@ def test_equal_depths_full_parity(capacity):
     _full_parity(sc, cam, w, capacity=capacity)
 
 
+@pytest.mark.parametrize("target", [1, 2, 3, 4, 5, 7, 4095, 4096, 4097, 4099])
+def test_radix_path_small_and_ragged_pair_counts(target):
+    """The radix path on pair lists of a few pairs and around one 4096-key block: the
+    passes' partial blocks and the four-keys-per-thread tile ranges' tails."""
+    rng = np.random.default_rng(21)
+    sc, cam = ss.random_scene(rng, 6000, 256, 160, sh_degree=0, log_scale=(-5.5, 0.3))
+    cum = np.cumsum(oracle.project(sc, cam).tiles_touched)
+    sub = sc.subset(np.arange(int(np.searchsorted(cum, target)) + 1))
+    g = run_forward(sub, cam, capacity=RADIX_CAPACITY)
+    ref = oracle.project(sub, cam)
+    check_projection(g, ref, sub)
+    check_binning(g, oracle.bin_sort(cam, ref))
+    assert g.n_pairs == target  # every prefix count is hit on this scene
+
+
 def test_radix_and_bucket_paths_agree():
     sc, cam = ss.make_config(2)
     a = run_forward(sc, cam)
