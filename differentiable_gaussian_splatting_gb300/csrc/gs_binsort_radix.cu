@@ -455,11 +455,20 @@ __global__ void __launch_bounds__(kRsBlock) pairs_count(const int32_t* __restric
     if (threadIdx.x == 0) bsum[blockIdx.x] = total;
 }
 
+// Output pairs per block of the emission: the blocks split the depth-ordered pair
+// list into equal contiguous pieces.
+constexpr int kEmitPairs = 2048;
+
+// poffd[j] = first pair of the depth-rank-j visible Gaussian (poffd[m] = I), and
+// bstart[k] = the depth rank of the Gaussian holding pair k kEmitPairs, for the
+// nbs emission blocks that exist (pairs past the capacity get no block).
 __global__ void __launch_bounds__(kRsBlock) pairs_offsets(const int32_t* __restrict__ order,
                                                           const int32_t* __restrict__ tiles_touched,
                                                           const int64_t* __restrict__ m_dev,
                                                           const int64_t* __restrict__ bsum,
-                                                          int64_t* __restrict__ poff) {
+                                                          int64_t* __restrict__ poffd,
+                                                          int64_t* __restrict__ bstart,
+                                                          int64_t nbs) {
     grid_dep_sync();
     const int64_t m = *m_dev;
     if ((int64_t)blockIdx.x >= nblk_of(m)) return;
@@ -477,33 +486,45 @@ __global__ void __launch_bounds__(kRsBlock) pairs_offsets(const int32_t* __restr
     }
     int64_t total;
     int64_t pos = bsum[blockIdx.x] + block_exclusive_scan_256<int64_t>(sum, s_warp, &total);
-    // indexed by Gaussian id: the emission walks the Gaussians in id order
 #pragma unroll
     for (int r = 0; r < kRsIpt; ++r) {
         const int64_t j = base + r;
-        if (j < m) poff[g[r]] = pos;
+        if (j < m) {
+            poffd[j] = pos;
+            // the emission blocks whose first pair this Gaussian holds
+            for (int64_t k = (pos + kEmitPairs - 1) / kEmitPairs;
+                 k < nbs && k * kEmitPairs < pos + c[r]; ++k)
+                bstart[k] = j;
+            if (j == m - 1) poffd[m] = pos + c[r];
+        }
         pos += c[r];
     }
 }
 
 // emit (tile, Gaussian) pairs into their depth-order places from the exact row
-// spans.  A block takes 256 consecutive Gaussian ids (in id order the large,
-// near splats are spread over the blocks; in depth order they would crowd the
-// first ones); the (splat, tile row) entries of its visible splats are spread
-// evenly over the block's threads (a scan of the row counts and a search for
-// each entry's owner).  A splat's pairs go to its own offset range poff[id], in
-// any order within it (they lie in distinct tiles, and the tile sort is stable
-// across splats).  The digit counts of the tile sort's passes are counted here.
+// spans.  Block k writes the pairs [k kEmitPairs, (k + 1) kEmitPairs) of the
+// depth-ordered list: the Gaussians that hold them (from bstart, in depth order,
+// kEmitThreads at a time), their tile rows spread evenly over the block's threads
+// (a scan of the row counts and a search for each row's owner).  A Gaussian's
+// pairs are numbered row by row, tiles left to right; a row's place in that
+// numbering is the running sum of the earlier rows' span widths (a block scan per
+// round of rows), so a Gaussian split between blocks is cut at the same pair by
+// both.  The block's piece is staged in shared memory and written out coalesced;
+// every block gets the same number of pairs, however large or small its splats.
+// The digit counts of the tile sort's passes are counted here.
 constexpr int kEmitThreads = 256;
 struct EmitRows {
+    uint32_t okey[kEmitPairs];   // the block's piece of the pair list
+    int32_t oval[kEmitPairs];
     float e[8][kEmitThreads];    // Ellipse fields, structure of arrays
     float dyv[kEmitThreads];
     int ty0[kEmitThreads];
     int off[kEmitThreads + 1];   // exclusive prefix of row counts
-    int pcur[kEmitThreads];      // pairs placed so far per splat
-    int64_t pb[kEmitThreads];    // the splat's first pair
+    int64_t pb[kEmitThreads];    // the Gaussian's first pair
+    int64_t gp[kEmitThreads];    // running width sum at the Gaussian's first row
     int32_t gid[kEmitThreads];
     int wsum[kEmitThreads / 32];
+    int64_t wsum64[kEmitThreads / 32];
     uint32_t hist[kMaxPasses][256];
     int diff0[257];              // pass 0 digit counts as a circular difference array
     uint32_t base0;              // + whole cycles of 256 consecutive tiles
@@ -537,36 +558,17 @@ __device__ __forceinline__ void count_tile_range(EmitRows& S, uint32_t a, int w,
 }
 
 __global__ void __launch_bounds__(kEmitThreads) emit_pairs(
-    CamParams cam, const float4* __restrict__ splats, const int32_t* __restrict__ tiles_touched,
-    const int64_t* __restrict__ poff, int64_t n, int64_t capacity, uint32_t* __restrict__ pkeys,
-    int32_t* __restrict__ pvals, int passes, uint32_t* __restrict__ thist) {
+    CamParams cam, const float4* __restrict__ splats, const int32_t* __restrict__ order,
+    const int64_t* __restrict__ poffd, const int64_t* __restrict__ bstart,
+    const int64_t* __restrict__ counts, uint32_t* __restrict__ pkeys, int32_t* __restrict__ pvals,
+    int passes, uint32_t* __restrict__ thist) {
     grid_dep_sync();
     __shared__ EmitRows S;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t j = (int64_t)blockIdx.x * kEmitThreads + tid;  // Gaussian id
-    int nrows = 0;
-    if (j < n && tiles_touched[j] > 0) {
-        const int32_t g = (int32_t)j;
-        const float4 r0 = __ldg(splats + 3 * (int64_t)g), r1 = __ldg(splats + 3 * (int64_t)g + 1),
-                     r2 = __ldg(splats + 3 * (int64_t)g + 2);
-        const Ellipse e = ellipse_of(r0, r1, r2);
-        int ty0, ty1;
-        row_range(e, cam.nty, &ty0, &ty1);
-        nrows = max(ty1 - ty0, 0);
-        S.e[0][tid] = e.mux;
-        S.e[1][tid] = e.muy;
-        S.e[2][tid] = e.l11;
-        S.e[3][tid] = e.l12;
-        S.e[4][tid] = e.l22;
-        S.e[5][tid] = e.tau;
-        S.e[6][tid] = e.rx;
-        S.e[7][tid] = e.ry;
-        S.dyv[tid] = vertex_dy(e);
-        S.ty0[tid] = ty0;
-        S.pb[tid] = poff[j];
-        S.gid[tid] = g;
-    }
-    S.pcur[tid] = 0;
+    const int64_t m = counts[0], icap = counts[2];  // visible Gaussians, min(I, capacity)
+    const int64_t lo = (int64_t)blockIdx.x * kEmitPairs;
+    if (lo >= icap) return;
+    const int64_t hi = min64(lo + kEmitPairs, icap);
 #pragma unroll
     for (int p = 0; p < kMaxPasses; ++p) S.hist[p][tid] = 0;
     S.diff0[tid] = 0;
@@ -574,83 +576,115 @@ __global__ void __launch_bounds__(kEmitThreads) emit_pairs(
         S.diff0[256] = 0;
         S.base0 = 0;
     }
-    int ri = nrows;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int rv = __shfl_up_sync(0xffffffffu, ri, o);
-        if (lane >= o) ri += rv;
-    }
-    if (lane == 31) S.wsum[warp] = ri;
-    __syncthreads();
-    int rbase = 0, rtotal = 0;
-#pragma unroll
-    for (int w = 0; w < kEmitThreads / 32; ++w) {
-        const int rv = S.wsum[w];
-        rbase += w < warp ? rv : 0;
-        rtotal += rv;
-    }
-    S.off[tid] = rbase + ri - nrows;
-    if (tid == 0) S.off[kEmitThreads] = rtotal;
-    __syncthreads();
-    // rows in chunks of one per lane, each warp on its own: a lane finds one row's
-    // span, the warp scans its 32 runs' lengths in registers, and all 32 lanes
-    // write the runs' pairs, consecutive lanes to consecutive places; a pair's run
-    // is found by a 5-step shuffle search.  A wide splat's long rows no longer
-    // hold up one thread, the stores coalesce within runs, and no block barrier
-    // stops the other warps (one thread per row took 324 us on 29.7M pairs, the
-    // block writing each chunk together 280 us)
-    const unsigned F = 0xffffffffu;
-    for (int r0 = warp * 32; r0 < rtotal; r0 += kEmitThreads) {
-        const int r = r0 + lane;
-        int wv = 0;
-        int64_t at = 0;
-        uint32_t a = 0;
-        int32_t gid = 0;
-        if (r < rtotal) {
-            int lo = 0, hi = kEmitThreads;  // the last owner with off[owner] <= r
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (S.off[mid] <= r) lo = mid; else hi = mid;
-            }
-            const Ellipse e{S.e[0][lo], S.e[1][lo], S.e[2][lo], S.e[3][lo],
-                            S.e[4][lo], S.e[5][lo], S.e[6][lo], S.e[7][lo]};
-            const int ty = S.ty0[lo] + (r - S.off[lo]);
-            int tx0, tx1;
-            if (row_span(e, S.dyv[lo], ty, cam.W, cam.H, cam.ntx, &tx0, &tx1)) {
-                const int w = tx1 - tx0;
-                at = S.pb[lo] + atomicAdd(&S.pcur[lo], w);
-                a = (uint32_t)ty * (uint32_t)cam.ntx + (uint32_t)tx0;
-                gid = S.gid[lo];
-                wv = (int)max64(0, min64(w, capacity - at));  // the pairs that fit
-                if (wv > 0) count_tile_range(S, a, wv, passes);
-            }
+    // the Gaussians holding pairs [lo, hi), kEmitThreads at a time in depth order
+    for (int64_t jc = bstart[blockIdx.x];; jc += kEmitThreads) {
+        const int64_t j = jc + tid;
+        int nrows = 0;
+        if (j < m && poffd[j] < hi) {
+            const int32_t g = order[j];
+            const float4 r0 = __ldg(splats + 3 * (int64_t)g), r1 = __ldg(splats + 3 * (int64_t)g + 1),
+                         r2 = __ldg(splats + 3 * (int64_t)g + 2);
+            const Ellipse e = ellipse_of(r0, r1, r2);
+            int ty0, ty1;
+            row_range(e, cam.nty, &ty0, &ty1);
+            nrows = max(ty1 - ty0, 0);
+            S.e[0][tid] = e.mux;
+            S.e[1][tid] = e.muy;
+            S.e[2][tid] = e.l11;
+            S.e[3][tid] = e.l12;
+            S.e[4][tid] = e.l22;
+            S.e[5][tid] = e.tau;
+            S.e[6][tid] = e.rx;
+            S.e[7][tid] = e.ry;
+            S.dyv[tid] = vertex_dy(e);
+            S.ty0[tid] = ty0;
+            S.pb[tid] = poffd[j];
+            S.gid[tid] = g;
         }
-        // exclusive prefix of the warp's runs' lengths
-        int x = wv;
+        // block scan of the row counts
+        int ri = nrows;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(F, x, o);
-            if (lane >= o) x += y;
+            const int rv = __shfl_up_sync(0xffffffffu, ri, o);
+            if (lane >= o) ri += rv;
         }
-        const int excl = x - wv;
-        const int total = __shfl_sync(F, x, 31);
-        for (int p0 = 0; p0 < total; p0 += 32) {
-            const int p = p0 + lane;
-            int src = 0;  // the last lane whose run starts at or before p
+        if (lane == 31) S.wsum[warp] = ri;
+        __syncthreads();
+        int rbase = 0, rtotal = 0;
 #pragma unroll
-            for (int step = 16; step > 0; step >>= 1)
-                if (__shfl_sync(F, excl, src + step) <= p) src += step;
-            const int64_t at_s = __shfl_sync(F, at, src);
-            const uint32_t a_s = __shfl_sync(F, a, src);
-            const int32_t gid_s = __shfl_sync(F, gid, src);
-            const int i = p - __shfl_sync(F, excl, src);
-            if (p < total) {
-                pkeys[at_s + i] = a_s + (uint32_t)i;
-                pvals[at_s + i] = gid_s;
-            }
+        for (int w = 0; w < kEmitThreads / 32; ++w) {
+            const int rv = S.wsum[w];
+            rbase += w < warp ? rv : 0;
+            rtotal += rv;
         }
+        S.off[tid] = rbase + ri - nrows;
+        if (tid == 0) S.off[kEmitThreads] = rtotal;
+        __syncthreads();
+        // rows in rounds of kEmitThreads; carry = the span widths of earlier rounds
+        int64_t carry = 0;
+        for (int r0 = 0; r0 < rtotal; r0 += kEmitThreads) {
+            const int r = r0 + tid;
+            int owner = 0, w = 0;
+            uint32_t a = 0;
+            if (r < rtotal) {
+                int l = 0, h = kEmitThreads;  // the last owner with off[owner] <= r
+                while (h - l > 1) {
+                    const int mid = (l + h) >> 1;
+                    if (S.off[mid] <= r) l = mid; else h = mid;
+                }
+                owner = l;
+                const Ellipse e{S.e[0][l], S.e[1][l], S.e[2][l], S.e[3][l],
+                                S.e[4][l], S.e[5][l], S.e[6][l], S.e[7][l]};
+                const int ty = S.ty0[l] + (r - S.off[l]);
+                int tx0, tx1;
+                if (row_span(e, S.dyv[l], ty, cam.W, cam.H, cam.ntx, &tx0, &tx1)) {
+                    w = tx1 - tx0;
+                    a = (uint32_t)ty * (uint32_t)cam.ntx + (uint32_t)tx0;
+                }
+            }
+            // exclusive block scan of the widths
+            int x = w;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (lane == 31) S.wsum[warp] = x;
+            __syncthreads();
+            int wpre = 0, wtot = 0;
+#pragma unroll
+            for (int q = 0; q < kEmitThreads / 32; ++q) {
+                const int v = S.wsum[q];
+                wpre += q < warp ? v : 0;
+                wtot += v;
+            }
+            const int64_t run = carry + wpre + x - w;  // width sum before this row
+            if (r < rtotal && r == S.off[owner]) S.gp[owner] = run;
+            __syncthreads();
+            if (w > 0) {
+                const int64_t pos = S.pb[owner] + (run - S.gp[owner]);  // its first pair
+                const int64_t s0 = max64(pos, lo), s1 = min64(pos + w, hi);
+                if (s0 < s1) {
+                    const uint32_t a0 = a + (uint32_t)(s0 - pos);
+                    const int32_t gid = S.gid[owner];
+                    count_tile_range(S, a0, (int)(s1 - s0), passes);
+                    for (int64_t q = s0; q < s1; ++q) {
+                        S.okey[q - lo] = a0 + (uint32_t)(q - s0);
+                        S.oval[q - lo] = gid;
+                    }
+                }
+            }
+            carry += wtot;
+            __syncthreads();  // wsum, gp of this round
+        }
+        const int64_t jn = jc + kEmitThreads;
+        if (!(jn < m && poffd[jn] < hi)) break;
     }
     __syncthreads();
+    for (int i = tid; i < (int)(hi - lo); i += kEmitThreads) {
+        pkeys[lo + i] = S.okey[i];
+        pvals[lo + i] = S.oval[i];
+    }
     // pass 0: the running sum of the difference array, plus the whole cycles
     {
         int x = S.diff0[tid];
@@ -659,7 +693,6 @@ __global__ void __launch_bounds__(kEmitThreads) emit_pairs(
             const int y = __shfl_up_sync(0xffffffffu, x, o);
             if (lane >= o) x += y;
         }
-        __syncthreads();
         if (lane == 31) S.wsum[warp] = x;
         __syncthreads();
         int pre = 0;
@@ -792,6 +825,7 @@ RadixBinLayout radix_bin_layout(int64_t n, int64_t capacity, int64_t n_tiles) {
     L.off_dvals0 = take((size_t)nn * 4);
     L.off_dvals1 = take((size_t)nn * 4);
     L.off_poff = take((size_t)(nn + 1) * sizeof(int64_t));
+    L.off_bstart = take((size_t)((cap + kEmitPairs - 1) / kEmitPairs + 1) * sizeof(int64_t));
     L.off_pkeys0 = take((size_t)cap * 4);
     L.off_pkeys1 = take((size_t)cap * 4);
     L.off_pvals0 = take((size_t)cap * 4);
@@ -814,6 +848,8 @@ cudaError_t run_bin_sort_radix(const CamParams& cam, int64_t n, const float* spl
     auto* dv0 = reinterpret_cast<int32_t*>(ws + L.off_dvals0);
     auto* dv1 = reinterpret_cast<int32_t*>(ws + L.off_dvals1);
     auto* poff = reinterpret_cast<int64_t*>(ws + L.off_poff);
+    auto* bstart = reinterpret_cast<int64_t*>(ws + L.off_bstart);
+    const int64_t nbs = (capacity + kEmitPairs - 1) / kEmitPairs;  // emission blocks
     auto* pk0 = reinterpret_cast<uint32_t*>(ws + L.off_pkeys0);
     auto* pk1 = reinterpret_cast<uint32_t*>(ws + L.off_pkeys1);
     auto* pv0 = reinterpret_cast<int32_t*>(ws + L.off_pvals0);
@@ -859,13 +895,14 @@ cudaError_t run_bin_sort_radix(const CamParams& cam, int64_t n, const float* spl
                      (int64_t)0, counts + 1, capacity, counts + 2);
         if (err != cudaSuccess) return err;
         err = launch(pairs_offsets, nb, kRsBlock, 0, st, (const int32_t*)dvs, tiles_touched,
-                     (const int64_t*)(counts + 0), (const int64_t*)bsum, poff);
+                     (const int64_t*)(counts + 0), (const int64_t*)bsum, poff, bstart, nbs);
         if (err != cudaSuccess) return err;
         // 4. emit pairs in depth order
         const int tbits = bits_for(nt - 1);
-        err = launch(emit_pairs, (unsigned)((n + kEmitThreads - 1) / kEmitThreads), kEmitThreads, 0,
-                     st, cam, reinterpret_cast<const float4*>(splats), tiles_touched,
-                     (const int64_t*)poff, n, capacity, pk0, pv0, (tbits + 7) / 8, thist);
+        err = launch(emit_pairs, (unsigned)std::max<int64_t>(1, nbs), kEmitThreads, 0, st, cam,
+                     reinterpret_cast<const float4*>(splats), (const int32_t*)dvs,
+                     (const int64_t*)poff, (const int64_t*)bstart, (const int64_t*)counts, pk0,
+                     pv0, (tbits + 7) / 8, thist);
         if (err != cudaSuccess) return err;
         // 5. stable sort by tile key; values land in sorted_ids
         uint32_t* pks = nullptr;

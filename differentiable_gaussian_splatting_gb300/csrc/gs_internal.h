@@ -57,7 +57,8 @@ struct RadixBinLayout {
     size_t off_counts;   // int64[8]
     size_t off_bsum;     // int64[nblk_n + 1] scan block sums
     size_t off_dkeys0, off_dkeys1, off_dvals0, off_dvals1;  // uint32 / int32 [n]
-    size_t off_poff;     // int64[n + 1]: each visible Gaussian's first pair (by id)
+    size_t off_poff;     // int64[n + 1]: each visible Gaussian's first pair (by depth rank)
+    size_t off_bstart;   // int64[emission blocks + 1]: each emission block's first Gaussian
     size_t off_pkeys0, off_pkeys1, off_pvals0, off_pvals1;  // [capacity]
     size_t off_hist;     // radix sort control: pass tickets, digit counts, look-back words
     size_t off_lruns;    // sorted runs of LPT keys
