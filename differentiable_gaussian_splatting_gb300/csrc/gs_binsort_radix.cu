@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(kRsBlock) pairs_offsets(const int32_t* __restr
 // (a scan of the row counts and a search for each row's owner).  A Gaussian's
 // pairs are numbered row by row, tiles left to right; a row's place in that
 // numbering is the running sum of the earlier rows' span widths (a block scan per
-// round of rows), so a Gaussian split between blocks is cut at the same pair by
+// batch of rows), so a Gaussian split between blocks is cut at the same pair by
 // both.  The block's piece is staged in shared memory and written out coalesced;
 // every block gets the same number of pairs, however large or small its splats.
 // The digit counts of the tile sort's passes are counted here.
@@ -620,7 +620,7 @@ __global__ void __launch_bounds__(kEmitThreads) emit_pairs(
         S.off[tid] = rbase + ri - nrows;
         if (tid == 0) S.off[kEmitThreads] = rtotal;
         __syncthreads();
-        // rows in rounds of kEmitThreads; carry = the span widths of earlier rounds
+        // rows in batches of kEmitThreads; carry = the span widths of earlier batches
         int64_t carry = 0;
         for (int r0 = 0; r0 < rtotal; r0 += kEmitThreads) {
             const int r = r0 + tid;
@@ -675,7 +675,7 @@ __global__ void __launch_bounds__(kEmitThreads) emit_pairs(
                 }
             }
             carry += wtot;
-            __syncthreads();  // wsum, gp of this round
+            __syncthreads();  // wsum and gp are rewritten by the next batch
         }
         const int64_t jn = jc + kEmitThreads;
         if (!(jn < m && poffd[jn] < hi)) break;

@@ -46,7 +46,7 @@ def t(a, dev="cuda"):
 
 
 @dataclass
-class GpuRun:
+class GpuResult:
     r: object                # the Rasterizer
     splats: np.ndarray
     depths: np.ndarray
@@ -75,13 +75,13 @@ def run_forward(sc, cam, settings=None, capacity=None, sh_bf16=False):
     r.forward(t(sc.means), t(sc.scales), t(sc.quats), t(sc.opacities), sh)
     torch.cuda.synchronize()
     I = r.n_pairs
-    return GpuRun(r, r.splats.cpu().numpy(), r.depths.cpu().numpy(), r.radii.cpu().numpy(),
+    return GpuResult(r, r.splats.cpu().numpy(), r.depths.cpu().numpy(), r.radii.cpu().numpy(),
                   r.tiles_touched.cpu().numpy(), I, r.sorted_ids[:I].cpu().numpy(),
                   r.tile_ranges.cpu().numpy(), r.lpt_order.cpu().numpy(), r.image.cpu().numpy(),
                   r.t_final.cpu().numpy(), r.n_contrib.cpu().numpy(), r.last_idx.cpu().numpy())
 
 
-def run_backward(g: GpuRun, w, v=None):
+def run_backward(g: GpuResult, w, v=None):
     import torch
 
     grads = g.r.backward(t(w.astype(np.float32)), None if v is None else t(v.astype(np.float32)))
@@ -90,7 +90,7 @@ def run_backward(g: GpuRun, w, v=None):
             {k: getattr(grads, k).cpu().numpy() for k in ("means", "scales", "quats", "opacities", "sh")})
 
 
-def check_projection(g: GpuRun, ref: oracle.Projection, sc, rows=None):
+def check_projection(g: GpuResult, ref: oracle.Projection, sc, rows=None):
     """Integer outputs and the decision chain bit-exact; colour within tolerance."""
     rows = np.arange(sc.n) if rows is None else rows
     np.testing.assert_array_equal(g.tiles_touched[rows], ref.tiles_touched[rows])
@@ -110,7 +110,7 @@ def check_projection(g: GpuRun, ref: oracle.Projection, sc, rows=None):
     assert np.all(g.splats[culled] == 0)
 
 
-def check_binning(g: GpuRun, ref: oracle.Binning, tiles=None):
+def check_binning(g: GpuResult, ref: oracle.Binning, tiles=None):
     assert g.n_pairs == ref.n_pairs
     np.testing.assert_array_equal(g.ranges[:, 0], ref.ranges[:, 0])
     np.testing.assert_array_equal(g.ranges[:, 1], ref.ranges[:, 1])
@@ -121,7 +121,7 @@ def check_binning(g: GpuRun, ref: oracle.Binning, tiles=None):
         np.testing.assert_array_equal(g.sorted_ids[s:e], ref.tile_ids(tt), err_msg=f"tile {tt}")
 
 
-def check_forward(g: GpuRun, cam, proj, b, im: oracle.Image, name="forward"):
+def check_forward(g: GpuResult, cam, proj, b, im: oracle.Image, name="forward"):
     """Every computed pixel against the oracle: at the oracle's stop near-ties, the outcome
     the GPU took (its last_idx), which the oracle must admit; at clamp near-ties, either
     clamp decision.  Returns stop_last for the backward: the GPU's last_idx at the
