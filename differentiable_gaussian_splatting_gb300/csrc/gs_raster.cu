@@ -149,18 +149,25 @@ __device__ __forceinline__ bool blend_range(const RasterArgs& A, Smem& S, int tx
                             bool write_cmask, BatchCount& bc) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     bc = BatchCount{0, 0, 0};
+    // A pixel blends while its running T is at least 1e-4 (T only falls, so that is
+    // the stop rule); a pixel that takes no part (outside the image, already
+    // stopped, or not being replayed) runs with T = 0 and gets its T back at the end.
+    const bool frozen = st.done;
+    float T = frozen ? 0.f : st.T;
+    bool on_flag = false;
     for (int64_t bs = s; bs < e; bs += kBatch) {
         if (tid == 0)
             S.flag = (sat_slot >= 0 && chunk > 0) ? (*(volatile int*)(A.sat + sat_slot) < chunk) : 0;
-        const int live = __syncthreads_or(!st.done);
+        const int live = __syncthreads_or(T >= kTMin);
         const int left = (int)((e - bs + kBatch - 1) / kBatch);
         if (!live) {
             bc.skip_done = left;
-            return false;
+            break;
         }
         if (S.flag) {
             bc.skip_flag = left;
-            return true;
+            on_flag = true;
+            break;
         }
         ++bc.blended;
         const int64_t j = bs + tid;
@@ -181,7 +188,7 @@ __device__ __forceinline__ bool blend_range(const RasterArgs& A, Smem& S, int tx
         const int nb = (int)min64(kBatch, e - bs);
         const int pos0 = (int)bs;  // list positions fit in 32 bits (capacity < 2^31)
         for (int c = 0; c < nb; c += 32) {
-            if (__ballot_sync(0xffffffffu, !st.done) == 0) break;
+            if (__ballot_sync(0xffffffffu, T >= kTMin) == 0) break;
             const int jj = c + lane;
             const uint32_t bit = jj < nb ? (S.mask[jj] >> warp) & 1u : 0u;
             uint32_t work = __ballot_sync(0xffffffffu, bit);
@@ -194,17 +201,16 @@ __device__ __forceinline__ bool blend_range(const RasterArgs& A, Smem& S, int tx
                 const float dx = rsub(px, r0.x), dy = rsub(py, r0.y);
                 float u1, u2;
                 const float qv = quad_q(r0.z, r0.w, r1.x, dx, dy, &u1, &u2);
-                const bool hit = (qv <= r1.y) && !st.done;
+                const bool hit = (qv <= r1.y) && (T >= kTMin);
                 float alpha = fminf(ex2_approx(fmaf(qv, kNegHalfLog2e, r1.z)), kAlphaMax);
                 alpha = hit ? alpha : 0.f;
-                const float w = alpha * st.T;
+                const float w = alpha * T;
                 st.cr = fmaf(w, r2.x, st.cr);
                 st.cg = fmaf(w, r2.y, st.cg);
                 st.cb = fmaf(w, r2.z, st.cb);
-                st.T = st.T * (1.f - alpha);
+                T = T * (1.f - alpha);
                 // branch-free bookkeeping (no reconvergence point in the loop)
                 blended |= (hit ? 1u : 0u) << q;
-                st.done = st.done || (st.T < kTMin);
             }
             // the chunk's hits, in order: their count, and the last one
             st.n += __popc(blended);
@@ -222,7 +228,11 @@ __device__ __forceinline__ bool blend_range(const RasterArgs& A, Smem& S, int tx
             A.cmask[j] = (uint8_t)m;
         }
     }
-    return false;
+    if (!frozen) {
+        st.T = T;
+        st.done = T < kTMin;
+    }
+    return on_flag;
 }
 
 // ---------------------------------------------------------------------------
