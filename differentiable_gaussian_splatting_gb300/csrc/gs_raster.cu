@@ -208,7 +208,7 @@ __device__ __forceinline__ bool blend_range(const RasterArgs& A, Smem& S, int tx
                 st.cr = fmaf(w, r2.x, st.cr);
                 st.cg = fmaf(w, r2.y, st.cg);
                 st.cb = fmaf(w, r2.z, st.cb);
-                T = T * (1.f - alpha);
+                T = T - w;  // T (1 - alpha), as one subtraction of the blend weight
                 // branch-free bookkeeping (no reconvergence point in the loop)
                 blended |= (hit ? 1u : 0u) << q;
             }
