@@ -853,12 +853,15 @@ __global__ void __launch_bounds__(kBwdThreads, 6) raster_bwd_kernel(RasterArgs A
             // list positions fit in 32 bits (the pair capacity is below 2^31)
             const int rel0 = last0 - (int)cs, rel1 = last1 - (int)cs;
             while (work) {
-                // splats two at a time, back to front: q1 behind q2
+                // splats two at a time, back to front: q1 behind q2.  Every staged
+                // splat was blended by some pixel of the quadrant (its contributor
+                // bit), so its sums are written without asking which lanes took part;
+                // where none did (a split tile's chunk blended it past a pixel's
+                // global stop) they are zero and adding them changes nothing.
                 const int q1 = 31 - __clz(work);
                 work &= ~(1u << q1);
                 float va[6], dxa;
-                const bool act1 = splat_moments2(S, q1, px, py0, py1, rel0, rel1, P0, P1, va, &dxa);
-                const uint32_t b1 = __ballot_sync(F, act1);
+                splat_moments2(S, q1, px, py0, py1, rel0, rel1, P0, P1, va, &dxa);
                 float sum;
                 int q;
                 bool wr;
@@ -866,17 +869,13 @@ __global__ void __launch_bounds__(kBwdThreads, 6) raster_bwd_kernel(RasterArgs A
                     const int q2 = 31 - __clz(work);
                     work &= ~(1u << q2);
                     float vb[6], dxb;
-                    const bool act2 =
-                        splat_moments2(S, q2, px, py0, py1, rel0, rel1, P0, P1, vb, &dxb);
-                    const uint32_t b2 = __ballot_sync(F, act2);
-                    if ((b1 | b2) == 0) continue;
+                    splat_moments2(S, q2, px, py0, py1, rel0, rel1, P0, P1, vb, &dxb);
                     q = first ? q1 : q2;
-                    wr = (first ? b1 : b2) != 0;
+                    wr = true;
                     const float4 r0 = S.r0[q];
                     sum = reduce_moments2(va, vb, dxa, dxb, r0.z, r0.w, S.r1[q].x, lane);
                 } else {
                     // a lone last splat: paired with zeros
-                    if (b1 == 0) continue;
                     const float vz[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                     q = q1;
                     wr = first;
