@@ -125,7 +125,6 @@ struct Smem {
     float4 r0[kBatch];
     float4 r1[kBatch];
     float4 r2[kBatch];
-    int32_t gid[kBatch];
     uint8_t mask[kBatch];
     uint32_t cm[8 * (kBatch / 32)];  // [warp][32-splat chunk] blended bits
     int item;
@@ -699,12 +698,13 @@ struct BwdPixel {
 };
 
 // One row of one splat: recovers the transmittance in front of the splat,
-// updates the colour behind it; returns whether the pixel blended it and its
-// log-alpha derivative gs (zero when it did not or the clamp was active).
-__device__ __forceinline__ bool row_step(const float4& r0, const float4& r1, const float4& r2,
+// updates the colour behind it; gives the pixel's log-alpha derivative gs (zero
+// when it did not blend the splat or the clamp was active) and its blend weight.
+__device__ __forceinline__ void row_step(const float4& r0, const float4& r1, const float4& r2,
                                          float dx, float dy, bool in_range, BwdPixel& P,
-                                         float* u1, float* u2, float* gs, float* wgt) {
-    const float qv = quad_q(r0.z, r0.w, r1.x, dx, dy, u1, u2);
+                                         float* gs, float* wgt) {
+    float u1, u2;
+    const float qv = quad_q(r0.z, r0.w, r1.x, dx, dy, &u1, &u2);
     const bool act = (qv <= r1.y) && in_range;
     float alpha = fminf(ex2_approx(fmaf(qv, kNegHalfLog2e, r1.z)), kAlphaMax);
     alpha = act ? alpha : 0.f;
@@ -719,24 +719,23 @@ __device__ __forceinline__ bool row_step(const float4& r0, const float4& r1, con
     *gs = alpha < kAlphaMax ? alpha * dalpha : 0.f;
     *wgt = w;
     P.T = Tb;
-    return act;
 }
 
 // One splat for the lane's two pixels: its six moments (reduce_moments2) in v
-// and its dx.  Returns whether either pixel blended it.  The conic and mean
+// and its dx.  The conic and mean
 // derivatives are formed from the moments inside the reduction: with the
 // evaluated quadratic's conic a = l11^2, b = l11 l12, c = l12^2 + l22^2,
 // dL/dmux = l11 (l11 sum g dx + l12 sum g dy) and
 // dL/dmuy = l12 (l11 sum g dx + l12 sum g dy) + l22^2 sum g dy.
-__device__ __forceinline__ bool splat_moments2(const BwdSlice& S, int q, float px, float py0,
+__device__ __forceinline__ void splat_moments2(const BwdSlice& S, int q, float px, float py0,
                                                float py1, int rel0, int rel1, BwdPixel& P0,
                                                BwdPixel& P1, float v[6], float* dx_out) {
     const float4 r0 = S.r0[q], r1 = S.r1[q], r2 = S.r2[q];
     const float dx = rsub(px, r0.x);
     const float dy0 = rsub(py0, r0.y), dy1 = rsub(py1, r0.y);
-    float a0, b0, a1, b1, g0, g1, w0, w1;
-    const bool act0 = row_step(r0, r1, r2, dx, dy0, q <= rel0, P0, &a0, &b0, &g0, &w0);
-    const bool act1 = row_step(r0, r1, r2, dx, dy1, q <= rel1, P1, &a1, &b1, &g1, &w1);
+    float g0, g1, w0, w1;
+    row_step(r0, r1, r2, dx, dy0, q <= rel0, P0, &g0, &w0);
+    row_step(r0, r1, r2, dx, dy1, q <= rel1, P1, &g1, &w1);
     const float gdy0 = g0 * dy0, gdy1 = g1 * dy1;
     v[0] = g0 + g1;
     v[1] = gdy0 + gdy1;
@@ -745,7 +744,6 @@ __device__ __forceinline__ bool splat_moments2(const BwdSlice& S, int q, float p
     v[4] = fmaf(w1, P1.Gg, w0 * P0.Gg);
     v[5] = fmaf(w1, P1.Gb, w0 * P0.Gb);
     *dx_out = dx;
-    return act0 || act1;
 }
 
 __device__ __forceinline__ void load_bwd_pixel(const RasterArgs& A, const WorkItem& it, int x, int y,
