@@ -91,6 +91,29 @@ def test_random_ragged_scenes_full(seed, W, H, n, deg):
     _full_parity(sc, cam, w, v)
 
 
+def test_clamp_near_ties_full_parity():
+    """Splats centred on pixel centres with opacities inside the fp32 band of the 0.99
+    clamp, in front of ordinary splats: at those pixels the GPU's image must equal the
+    oracle's with one of the two clamp decisions, and its gradients stay within the
+    bound that spans both (galt)."""
+    rng = np.random.default_rng(31)
+    sc, cam = ss.random_scene(rng, 600, 64, 48, sh_degree=1, log_scale=(-2.6, 0.5),
+                              logit_std=2.0)
+    V = np.asarray(cam.viewmat, np.float64)
+    R, tv = V[:3, :3], V[:3, 3]
+    z = float(((R @ sc.means.T.astype(np.float64)).T[:, 2] + tv[2]).min()) - 0.3
+    for i, d in enumerate([3e-6, -3e-6, 1e-6, -1e-6, 5e-6, -5e-6]):
+        sc.opacities[i] = np.float32(0.99 + d)
+        px, py = 8 + 9 * i + 0.5, 20.5
+        t = np.array([(px - cam.cx) * z / cam.fx, (py - cam.cy) * z / cam.fy, z])
+        sc.means[i] = (R.T @ (t - tv)).astype(np.float32)
+    ref = oracle.render(sc, cam)
+    assert np.count_nonzero(ref.image.flags & oracle.FLAG_CLAMP_TIE) >= 3
+    w = rng.standard_normal((48, 64, 3))
+    v = rng.standard_normal((48, 64))
+    _full_parity(sc, cam, w, v, name="clamp ties:")
+
+
 def test_forced_split_tiles_match_sequential():
     import differentiable_gaussian_splatting_gb300 as gs
 
