@@ -91,6 +91,20 @@ def test_random_ragged_scenes_full(seed, W, H, n, deg):
     _full_parity(sc, cam, w, v)
 
 
+@pytest.mark.parametrize("W,H", [(1, 1), (1, 37), (45, 1), (16, 16), (17, 16), (16, 33),
+                                 (1000, 3)])
+def test_degenerate_image_shapes_full(W, H):
+    # one pixel, one column, one row, exactly one tile, one tile plus a one-pixel
+    # ragged column or row, and a long strip of tiles; with f = 60 the splats are
+    # several pixels wide, so the single pixels saturate and stop early
+    rng = np.random.default_rng(40 + W + H)
+    sc, cam = ss.random_scene(rng, 200, W, H, f=60.0, sh_degree=1, log_scale=(-2.8, 0.8),
+                              logit_std=2.5)
+    w = rng.standard_normal((H, W, 3))
+    v = rng.standard_normal((H, W))
+    _full_parity(sc, cam, w, v)
+
+
 def test_clamp_near_ties_full_parity():
     """Splats centred on pixel centres with opacities inside the fp32 band of the 0.99
     clamp, in front of ordinary splats: at those pixels the GPU's image must equal the
