@@ -92,17 +92,54 @@ def test_random_ragged_scenes_full(seed, W, H, n, deg):
 
 
 @pytest.mark.parametrize("W,H", [(1, 1), (1, 37), (45, 1), (16, 16), (17, 16), (16, 33),
-                                 (1000, 3)])
+                                 (1000, 3), (32768, 2), (3, 32768)])
 def test_degenerate_image_shapes_full(W, H):
     # one pixel, one column, one row, exactly one tile, one tile plus a one-pixel
-    # ragged column or row, and a long strip of tiles; with f = 60 the splats are
-    # several pixels wide, so the single pixels saturate and stop early
+    # ragged column or row, a long strip of tiles, and strips at the largest image
+    # side the calls accept (32768 pixels, 2048 tiles in one row or column); with
+    # f = 60 the splats are several pixels wide, so the single pixels saturate and
+    # stop early
     rng = np.random.default_rng(40 + W + H)
     sc, cam = ss.random_scene(rng, 200, W, H, f=60.0, sh_degree=1, log_scale=(-2.8, 0.8),
                               logit_std=2.5)
     w = rng.standard_normal((H, W, 3))
     v = rng.standard_normal((H, W))
     _full_parity(sc, cam, w, v)
+
+
+def test_cull_boundaries_full_parity():
+    """The two cull decisions at their boundaries, in fp32 steps: view depths one
+    step below, at and above the near plane (in front means strictly beyond it),
+    and opacities around 1/255, where tau = 2 ln(255 o) changes sign (the oracle
+    culls the two lower ones and keeps fp32(1/255) with tau about 1.2e-7), beside
+    the smallest and the largest opacity below 1."""
+    rng = np.random.default_rng(51)
+    f32 = np.float32
+    sc, cam = ss.random_scene(rng, 400, 96, 64, sh_degree=2, log_scale=(-2.8, 0.8),
+                              logit_std=2.5)
+    zn = f32(cam.znear)
+    depths = [np.nextafter(zn, f32(0)), zn, np.nextafter(zn, f32(1)), zn * f32(1.001)]
+    o1 = f32(1.0) / f32(255.0)
+    below = np.nextafter(o1, f32(0))
+    above = np.nextafter(o1, f32(1))
+    opac = [np.nextafter(below, f32(0)), below, o1, above, np.nextafter(above, f32(1)),
+            f32(1e-7), np.nextafter(f32(1), f32(0)), f32(0.5)]
+    for i, z in enumerate(depths):
+        sc.means[i] = [0.02 * (i - 1.5) * z, 0.01 * z, z]
+        sc.scales[i] = [4e-4, 3e-4, 5e-4]
+        sc.opacities[i] = 0.6
+    for j, o in enumerate(opac):
+        k = len(depths) + j
+        sc.means[k] = [(j - 3.5) * 0.3, 0.2, 3.0]
+        sc.scales[k] = [0.03, 0.02, 0.025]
+        sc.opacities[k] = o
+    w = rng.standard_normal((64, 96, 3))
+    g, ref = _full_parity(sc, cam, w)
+    tt = ref.proj.tiles_touched
+    # the boundaries are where the oracle puts them, so the comparison is not vacuous
+    assert list(tt[:2]) == [0, 0] and np.all(tt[2:4] > 0)
+    k = len(depths)
+    assert list(tt[k:k + 2]) == [0, 0] and np.all(tt[k + 2:k + 5] > 0)
 
 
 def test_clamp_near_ties_full_parity():
