@@ -299,7 +299,10 @@ __device__ __forceinline__ Projected project_chain(const CamParams& cam, float m
 // sum over the tile rows a splat's support may cover; rows per splat range
 // from 0 (culled) to the image height, so the block spreads all its
 // (Gaussian, row) pairs evenly over its threads instead of looping per thread.
-constexpr int kProjThreads = 256;
+// The kernel is bound by the latency of its long chain, so it wants many warps in
+// flight: 128-thread blocks at 12 per SM (40 registers) keep 48 warps per SM and
+// wait on smaller blocks at the row pass's barriers.
+constexpr int kProjThreads = 128;
 
 struct ProjShared {
     float e[8][kProjThreads];      // Ellipse fields, structure of arrays
@@ -311,7 +314,7 @@ struct ProjShared {
 };
 
 template <int K, typename ShT>
-__global__ void __launch_bounds__(kProjThreads) project_kernel(CamParams cam, int64_t n,
+__global__ void __launch_bounds__(kProjThreads, 12) project_kernel(CamParams cam, int64_t n,
                                                       const float* __restrict__ means,
                                                       const float* __restrict__ scales,
                                                       const float4* __restrict__ quats,
