@@ -543,19 +543,6 @@ __device__ __forceinline__ uint64_t* block_sort_keys(uint64_t* A, uint64_t* B) {
     return block_merge_rounds(B, A, C, kWarps * C);
 }
 
-// number of elements of run a among the first k of merge(a[0, na), b[0, nb)),
-// both in global memory (keys are unique)
-__device__ __forceinline__ int merge_split_g(const uint64_t* a, int na, const uint64_t* b, int nb,
-                                             int k) {
-    int lo = max(0, k - nb), hi = min(k, na);
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (a[mid] < b[k - 1 - mid]) lo = mid + 1;
-        else hi = mid;
-    }
-    return lo;
-}
-
 // One block sorts a slice of kWarpSortMax + 1 .. kBlockSortMax keys in shared
 // memory (A, B: sk_len(kBlockSortMax) words each) and writes its ids.
 __device__ __forceinline__ void sort_medium_slice(int2 r, const uint64_t* __restrict__ keys,
