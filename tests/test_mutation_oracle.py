@@ -5,8 +5,9 @@ or transposed index, a reversed order) and runs the oracle's own pin tests
 arithmetic the pins do not fix.
 
 The table is checked against the source on every CPU run (each planted text must occur
-exactly once, so the table follows the source as it changes).  Running the mutants
-themselves takes a minute or two on eight cores and is opt-in:
+exactly once, so the table follows the source as it changes), and a sample of eight
+mutants, one from each part of the oracle, runs every time.  Running the whole table
+takes about three minutes on eight cores and is opt-in:
 
     GS_ORACLE_MUTANTS=1 python -m pytest tests/test_mutation_oracle.py -n 8 -q
 
@@ -205,10 +206,27 @@ def _copy_tree(dst: str) -> None:
     shutil.copytree(os.path.join(ROOT, "tests", "golden"), os.path.join(dst, "tests", "golden"))
 
 
+# One mutant from each part of the oracle, run on every CPU run (a few seconds each);
+# the whole table stays opt-in.
+SAMPLE = ("camera_row_index", "span_boundary_sign", "transmittance_update",
+          "contributors_not_counted", "dalpha_behind_sign", "dconic_b_factor",
+          "lpt_ascending", "adam_bias_correction")
+
+
+@pytest.mark.parametrize("name", SAMPLE)
+def test_sampled_mutants_fail_a_pin(tmp_path, name):
+    (old, new), = [(o, n) for m, o, n in MUTANTS if m == name]
+    _run_mutant(tmp_path, name, old, new)
+
+
 @pytest.mark.skipif(os.environ.get("GS_ORACLE_MUTANTS") != "1",
                     reason="mutation run is opt-in: GS_ORACLE_MUTANTS=1")
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_every_mutant_fails_a_pin(tmp_path, name, old, new):
+    _run_mutant(tmp_path, name, old, new)
+
+
+def _run_mutant(tmp_path, name, old, new):
     dst = str(tmp_path / "copy")
     _copy_tree(dst)
     path = os.path.join(dst, "oracle", "gs_oracle.c")
@@ -217,7 +235,7 @@ def test_every_mutant_fails_a_pin(tmp_path, name, old, new):
     with open(path, "w") as f:
         f.write(src.replace(old, new))
     env = dict(os.environ, PYTHONPATH=dst, PYTHONDONTWRITEBYTECODE="1")
-    env.pop("GS_ORACLE_MUTANTS")
+    env.pop("GS_ORACLE_MUTANTS", None)
     # the mutant must build: a planted mistake, not a syntax error
     b = subprocess.run([sys.executable, "-c", "import oracle; oracle.build(force=True)"],
                        cwd=dst, env=env, capture_output=True, text=True, timeout=300)
