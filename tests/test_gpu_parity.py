@@ -107,6 +107,23 @@ def test_degenerate_image_shapes_full(W, H):
     _full_parity(sc, cam, w, v)
 
 
+def test_anisotropic_intrinsics_rotated_camera_full():
+    # fx != fy and a principal point off the image centre, seen from a camera turned
+    # and moved off the origin: a swapped focal length, principal-point coordinate or
+    # view-matrix row in the projection, its Jacobian or its chain rule shows here (the
+    # other scenes have fx = fy and the principal point at the centre)
+    rng = np.random.default_rng(61)
+    W, H = 120, 90
+    sc, _ = ss.random_scene(rng, 800, W, H, f=100.0, sh_degree=3, log_scale=(-2.8, 0.7),
+                            logit_std=2.0)
+    V = ss.look_at(np.array([1.2, -0.7, -1.5]), np.array([0.0, 0.0, 4.0]))
+    cam = ss.Camera(V, 115.0, 80.0, 0.42 * W, 0.61 * H, W, H, 0.2)
+    w = rng.standard_normal((H, W, 3))
+    v = rng.standard_normal((H, W))
+    g, ref = _full_parity(sc, cam, w, v)
+    assert ref.binning.n_pairs > 1000
+
+
 def test_cull_boundaries_full_parity():
     """The two cull decisions at their boundaries, in fp32 steps: view depths one
     step below, at and above the near plane (in front means strictly beyond it),

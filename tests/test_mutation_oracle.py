@@ -7,7 +7,7 @@ arithmetic the pins do not fix.
 The table is checked against the source on every CPU run (each planted text must occur
 exactly once, so the table follows the source as it changes), and a sample of eight
 mutants, one from each part of the oracle, runs every time.  Running the whole table
-takes about three minutes on eight cores and is opt-in:
+takes about four minutes on eight cores and is opt-in:
 
     GS_ORACLE_MUTANTS=1 python -m pytest tests/test_mutation_oracle.py -n 8 -q
 
@@ -43,6 +43,10 @@ MUTANTS = [
      "double t = log(CUTOFF_INV * (double)o);"),
     ("extent_rx_uses_p11", "dreal rx = sqrt(tau * P00);", "dreal rx = sqrt(tau * P11);"),
     ("near_plane_ignored", "if (!(tz > cam->znear) ||", "if (!(tz > 0) ||"),
+    ("principal_point_swapped", "dreal mux = cam->fx * u + cam->cx;",
+     "dreal mux = cam->fx * u + cam->cy;"),
+    ("jacobian_focal_swapped", "dreal j11 = cam->fy / tz;", "dreal j11 = cam->fx / tz;"),
+    ("alpha_cutoff_256", "#define CUTOFF_INV 255.0", "#define CUTOFF_INV 256.0"),
     # ---- exact row spans and tile rows
     ("span_boundary_sign", "return (sqrt(disc) - s->l12 * dy) / s->l11;",
      "return (sqrt(disc) + s->l12 * dy) / s->l11;"),
@@ -58,6 +62,9 @@ MUTANTS = [
      "((dreal)(16 * ty) + (dreal)15.5)"),
     # ---- spherical harmonics and the view direction
     ("sh_sign_y2", "Y[2] = k1 * z;", "Y[2] = -k1 * z;"),
+    ("sh_sign_y15", "Y[15] = k3a * x * (x * x - 3 * y * y);",
+     "Y[15] = -k3a * x * (x * x - 3 * y * y);"),
+    ("sh_y12_constant", "Y[12] = k3d * z * (5 * z * z - 3);", "Y[12] = k3d * z * (5 * z * z - 1);"),
     ("sh_gradient_y9", "dY[9][1] = k3a * (3 * x * x - 3 * y * y);",
      "dY[9][1] = k3a * (3 * x * x - y * y);"),
     ("sh_normalisation_k2b", "double k2b = sqrt(5.0 / (16 * PI));",
@@ -146,6 +153,7 @@ MUTANTS += [
     ("dquat_sign_w", "dw += dR[1] * (-2 * z);", "dw += dR[1] * (2 * z);"),
     ("dquat_sign_x", "dx += dR[5] * (-2 * w);", "dx += dR[5] * (2 * w);"),
     ("dquat_not_projected", "dq[k] = (dqh[k] - qh[k] * dotq) / qn;", "dq[k] = dqh[k] / qn;"),
+    ("dquat_norm_dropped", "dq[k] = (dqh[k] - qh[k] * dotq) / qn;", "dq[k] = (dqh[k] - qh[k] * dotq);"),
     ("dopacity_scaled", "dopac[i] = g2[5];", "dopac[i] = 0.5 * g2[5];"),
     ("dsh_channel", "dshi[3 * k + ch] = Y[k] * gcol[ch];", "dshi[3 * k + ch] = Y[k] * gcol[0];"),
     ("dmeans_sh_not_projected", "dm[j] += (gd[j] - dhat[j] * dotd) / len;",
@@ -158,6 +166,12 @@ MUTANTS += [
     ("policy_next_index", "double next = h < nt ? (double)counts_desc[h] : 0.0;",
      "double next = h < nt ? (double)counts_desc[h - 1] : 0.0;"),
     # ---- raw gradients and Adam
+    ("adam_eps_inside_sqrt", "p[i] -= lr * (m[i] / c1) / (sqrt(v[i] / c2) + eps);",
+     "p[i] -= lr * (m[i] / c1) / sqrt(v[i] / c2 + eps);"),
+    ("loss_weights_swapped", "out[0] = (1.0 - lambda) * out[1] + lambda * (1.0 - out[2]);",
+     "out[0] = lambda * out[1] + (1.0 - lambda) * (1.0 - out[2]);"),
+    ("loss_grad_weights_swapped", "dL_dx[i] = (1.0 - lambda) * inv * sg - lambda * inv * ds;",
+     "dL_dx[i] = lambda * inv * sg - (1.0 - lambda) * inv * ds;"),
     ("adam_second_moment", "v[i] = b2 * v[i] + (1.0 - b2) * g[i] * g[i];",
      "v[i] = b2 * v[i] + (1.0 - b2) * g[i];"),
     ("adam_bias_correction", "p[i] -= lr * (m[i] / c1) / (sqrt(v[i] / c2) + eps);",

@@ -21,7 +21,9 @@ def _scene(seed, n=40, W=64, H=48, deg=3):
     sc, _ = ss.random_scene(rng, n, W, H, sh_degree=deg, log_scale=(-2.3, 0.4), logit_std=1.5)
     eye = np.array([0.3, -0.2, -0.5])
     V = ss.look_at(eye, np.array([0.0, 0.0, 4.0]), up=(0.05, -1.0, 0.0))
-    cam = ss.pinhole(V, 64.0, W, H)
+    # fx != fy and an off-centre principal point: the chain rule's two Jacobian rows
+    # and the two offsets are told apart
+    cam = ss.Camera(V, 64.0, 52.0, 0.47 * W, 0.53 * H, W, H, 0.2)
     w = rng.standard_normal((H, W, 3))
     v = rng.standard_normal((H, W))
     return sc, cam, w, v

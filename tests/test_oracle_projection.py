@@ -66,11 +66,14 @@ def _numerical_jacobian(cam, m, h=1e-6):
 @pytest.mark.parametrize("seed", [0, 1, 2])
 def test_projection_is_linearised_pinhole(seed):
     """Sigma' equals J_num Sigma J_num^T with J_num the numerical Jacobian of the
-    pinhole map and Sigma = R S^2 R^T built with scipy's rotation (f64 oracle build)."""
+    pinhole map and Sigma = R S^2 R^T built with scipy's rotation (f64 oracle build).
+    The focal lengths differ and the principal point is off the image centre, so that
+    Eq. 1's two rows (fx / t_z, fy / t_z) and the two offsets cannot stand in for each
+    other."""
     rng = np.random.default_rng(seed)
     eye = rng.uniform(-1, 1, 3) + np.array([0, 0, -5.0])
     V = ss.look_at(eye, rng.uniform(-0.3, 0.3, 3))
-    cam = ss.pinhole(V, 300.0, 320, 240)
+    cam = ss.Camera(V, 300.0, 230.0, 150.0, 130.0, 320, 240, 0.2)
     n = 50
     means = rng.uniform(-0.6, 0.6, (n, 3))
     scales = np.exp(rng.normal(-3, 0.5, (n, 3)))
