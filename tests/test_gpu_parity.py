@@ -124,6 +124,30 @@ def test_anisotropic_intrinsics_rotated_camera_full():
     assert ref.binning.n_pairs > 1000
 
 
+def test_non_finite_parameters_are_culled_full():
+    # NaN and infinite means, scales, quaternions and opacity, and a zero quaternion:
+    # each such Gaussian is culled (no tiles, zero records and gradients) on both sides,
+    # and the rest of the view renders and differentiates as without them
+    rng = np.random.default_rng(71)
+    W, H = 80, 60
+    sc, cam = ss.random_scene(rng, 300, W, H, sh_degree=2, log_scale=(-2.8, 0.7),
+                              logit_std=2.0)
+    nan, inf = np.float32(np.nan), np.float32(np.inf)
+    sc.means[0] = [nan, 0.0, 3.0]
+    sc.means[1] = [inf, 0.0, 3.0]
+    sc.scales[2] = [inf, 0.1, 0.1]
+    sc.scales[3] = [0.1, nan, 0.1]
+    sc.quats[4] = [nan, 0.0, 0.0, 0.0]
+    sc.quats[5] = [0.0, 0.0, 0.0, 0.0]
+    sc.opacities[6] = nan
+    sc.means[7, 2] = inf
+    w = rng.standard_normal((H, W, 3))
+    g, ref = _full_parity(sc, cam, w)
+    assert np.all(ref.proj.tiles_touched[:8] == 0)
+    assert np.all(np.asarray(g.tiles_touched)[:8] == 0)
+    assert np.isfinite(g.img).all() and ref.binning.n_pairs > 200
+
+
 def test_cull_boundaries_full_parity():
     """The two cull decisions at their boundaries, in fp32 steps: view depths one
     step below, at and above the near plane (in front means strictly beyond it),
