@@ -303,6 +303,8 @@ def run_gpu(args):
                                       "replicas" if world > 1 else "single"),
             "contributing_pairs": E,
             "per_call_ms": per_call,
+            # the two blend calls alone, the figure the pages quote per stage
+            "rast_only_ms": per_call["gs_rasterize_fwd"] + per_call["gs_rasterize_bwd"],
             "roofline": roof,
             "step_roofline": step_roof,
             "imbalance": load,
