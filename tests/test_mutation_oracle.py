@@ -92,6 +92,14 @@ MUTANTS += [
     ("quadratic_form_term", "dreal q = fma(u1, u1, u2 * u2);", "dreal q = fma(u1, u1, u2);"),
     ("termination_threshold", "if (!forced && T < T_MIN) break;",
      "if (!forced && T < 1e-3) break;"),
+    ("stop_exclusive", "blended_t* e = &(*list)[nb++];",
+     "if (!forced && T * (1.0 - alpha) < T_MIN) break;\n        blended_t* e = &(*list)[nb++];"),
+    ("stop_band_halved", "int near = fabs(T - T_MIN) <= 2.0 * err * T;",
+     "int near = fabs(T - T_MIN) <= 0.5 * err * T;"),
+    ("stop_band_doubled", "int near = fabs(T - T_MIN) <= 2.0 * err * T;",
+     "int near = fabs(T - T_MIN) <= 4.0 * err * T;"),
+    ("stop_band_alpha_weight", "err += E_ALPHA * alpha / (1.0 - alpha) + 1.1920928955078125e-07;",
+     "err += E_ALPHA * alpha + 1.1920928955078125e-07;"),
     ("alpha_clamp_dropped", "return c ? ALPHA_MAX : araw;", "return araw;"),
     ("colour_without_transmittance",
      "C[ch] += rgb[3 * (int64_t)e->g + ch] * e->alpha * e->T;",

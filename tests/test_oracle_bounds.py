@@ -513,3 +513,54 @@ def test_parallel_tile_parts_equal_the_single_call():
     for f in ("grad2d", "gabs", "grho", "galt"):
         a, c = getattr(rp, f), getattr(r, f)
         np.testing.assert_allclose(a, c, rtol=1e-9, atol=1e-12 * np.abs(c).max(), err_msg=f)
+
+
+def _stop_band_scene(o2):
+    """Three large splats centred on pixel (12, 12)'s centre, front to back: a clamped
+    one (alpha 0.99), one of opacity o2 (its alpha at the centre pixel is o2) and one
+    behind them, so that the stop test runs once more after the second."""
+    W = H = 25  # cx = cy = 12.5, the centre of pixel (12, 12)
+    cam = ss.pinhole(np.eye(4), 40.0, W, H)
+    means = np.array([[0, 0, 2.0], [0, 0, 2.5], [0, 0, 3.0]], np.float32)
+    scales = np.full((3, 3), 1.0, np.float32)
+    quats = np.tile(np.array([1, 0, 0, 0], np.float32), (3, 1))
+    opac = np.array([0.9999, o2, 0.5], np.float32)
+    sh = np.full((3, 1, 3), 1.0, np.float32)
+    return ss.Scene(means, scales, quats, opac, sh, 0), cam
+
+
+def _stop_band_ratio(o2):
+    """|T - 1e-4| / (err T) after the two front splats at the centre pixel, with the
+    band's definition: err = sum over the blended splats of 2^-17 alpha / (1 - alpha)
+    (the renderer's alpha error, amplified by the transmittance update) + 2^-23 (two
+    fp32 roundings of the update)."""
+    T, err = 1.0, 0.0
+    for a in (ALPHA_MAX, float(np.float32(o2))):
+        T *= 1.0 - a
+        err += E_ALPHA * a / (1.0 - a) + 2.0 ** -23
+    return abs(T - T_MIN) / (err * T)
+
+
+def test_stop_band_is_twice_the_accumulated_error():
+    """A stop decision is a near-tie when the transmittance lies within 2 err T of 1e-4:
+    at the centre pixel, T at 1.5 err T from 1e-4 is flagged, at 3 err T it is not
+    (the second splat's opacity sets T; neither alpha is near the clamp's band)."""
+    # opacities whose T after two splats sits at the wanted multiple of err T
+    def o2_for(ratio):
+        lo, hi = 0.9899, 0.98998  # T falls as o2 rises, and the ratio with it
+        for _ in range(60):
+            mid = 0.5 * (lo + hi)
+            if _stop_band_ratio(mid) > ratio:
+                lo = mid
+            else:
+                hi = mid
+        return np.float32(0.5 * (lo + hi))
+    for ratio, flagged in ((1.5, True), (3.0, False)):
+        o2 = o2_for(ratio)
+        r = _stop_band_ratio(o2)
+        assert abs(r - ratio) < 0.05 and abs(float(o2) - ALPHA_MAX) > 2 * E_ALPHA * ALPHA_MAX
+        sc, cam = _stop_band_scene(o2)
+        proj = oracle.project(sc, cam)
+        im = oracle.blend(cam, proj, oracle.bin_sort(cam, proj))
+        assert im.n_contrib[12, 12] == 3  # T stays above 1e-4: the third splat blends
+        assert bool(im.flags[12, 12] & oracle.FLAG_STOP_TIE) == flagged, (ratio, r)
