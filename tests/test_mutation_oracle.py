@@ -96,6 +96,10 @@ MUTANTS += [
      "if (!forced && T * (1.0 - alpha) < T_MIN) break;\n        blended_t* e = &(*list)[nb++];"),
     ("stop_band_halved", "int near = fabs(T - T_MIN) <= 2.0 * err * T;",
      "int near = fabs(T - T_MIN) <= 0.5 * err * T;"),
+    ("clamp_band_halved", "int near = fabs(araw - ALPHA_MAX) <= 2.0 * E_ALPHA * ALPHA_MAX;",
+     "int near = fabs(araw - ALPHA_MAX) <= 0.5 * E_ALPHA * ALPHA_MAX;"),
+    ("clamp_band_doubled", "int near = fabs(araw - ALPHA_MAX) <= 2.0 * E_ALPHA * ALPHA_MAX;",
+     "int near = fabs(araw - ALPHA_MAX) <= 4.0 * E_ALPHA * ALPHA_MAX;"),
     ("stop_band_doubled", "int near = fabs(T - T_MIN) <= 2.0 * err * T;",
      "int near = fabs(T - T_MIN) <= 4.0 * err * T;"),
     ("stop_band_alpha_weight", "err += E_ALPHA * alpha / (1.0 - alpha) + 1.1920928955078125e-07;",

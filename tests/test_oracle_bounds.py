@@ -564,3 +564,23 @@ def test_stop_band_is_twice_the_accumulated_error():
         im = oracle.blend(cam, proj, oracle.bin_sort(cam, proj))
         assert im.n_contrib[12, 12] == 3  # T stays above 1e-4: the third splat blends
         assert bool(im.flags[12, 12] & oracle.FLAG_STOP_TIE) == flagged, (ratio, r)
+
+
+def test_clamp_band_is_twice_the_alpha_error():
+    """An alpha is a clamp near-tie when o exp(-q/2) lies within 2 E_alpha 0.99 of 0.99
+    (E_alpha = 2^-17, the renderer's alpha error): one splat centred on pixel (12, 12)'s
+    centre (q = 0 there, so its raw alpha is its opacity) at 1.5 and at 3 band units
+    above and below 0.99 is flagged, and not flagged."""
+    unit = E_ALPHA * ALPHA_MAX
+    for ratio, flagged in ((1.5, True), (-1.5, True), (3.0, False), (-3.0, False)):
+        o = np.float32(ALPHA_MAX + ratio * unit)
+        assert abs(abs(float(o) - ALPHA_MAX) / unit - abs(ratio)) < 0.05
+        W = H = 25
+        cam = ss.pinhole(np.eye(4), 40.0, W, H)
+        sc = ss.Scene(np.array([[0, 0, 2.0]], np.float32), np.full((1, 3), 1.0, np.float32),
+                      np.array([[1, 0, 0, 0]], np.float32), np.array([o], np.float32),
+                      np.full((1, 1, 3), 1.0, np.float32), 0)
+        proj = oracle.project(sc, cam)
+        im = oracle.blend(cam, proj, oracle.bin_sort(cam, proj))
+        assert im.n_contrib[12, 12] == 1
+        assert bool(im.flags[12, 12] & oracle.FLAG_CLAMP_TIE) == flagged, ratio
