@@ -57,6 +57,8 @@ MUTANTS = [
      "dreal f1 = floor((Xhi - (dreal)0.5) * (dreal)0.0625);"),
     ("rows_first_row_late", "ceil(((s->muy - ryp) - (dreal)15.5)",
      "ceil(((s->muy - ryp) - (dreal)0.5)"),
+    ("rows_last_row_dropped", "dreal f1 = floor(((s->muy + ryp) - (dreal)0.5) * (dreal)0.0625) + 1;",
+     "dreal f1 = floor(((s->muy + ryp) - (dreal)0.5) * (dreal)0.0625);"),
     ("tile_band_not_clipped",
      "dmin((dreal)(16 * ty) + (dreal)15.5, (dreal)cam->H - (dreal)0.5)",
      "((dreal)(16 * ty) + (dreal)15.5)"),
@@ -84,6 +86,8 @@ MUTANTS += [
      "if (x->id != y->id) return x->id > y->id ? -1 : 1;"),
     ("lpt_ascending", "if (x->count != y->count) return x->count > y->count ? -1 : 1;",
      "if (x->count != y->count) return x->count < y->count ? -1 : 1;"),
+    ("lpt_tie_break_reversed", "return x->tile < y->tile ? -1 : (x->tile > y->tile);",
+     "return x->tile > y->tile ? -1 : (x->tile < y->tile);"),
     ("range_end_off_by_one", "        ranges[2 * t + 1] = acc;\n",
      "        ranges[2 * t + 1] = acc - (acc > 0);\n"),
     # ---- forward blend
@@ -177,6 +181,10 @@ MUTANTS += [
     # ---- chunking policy (Eq. 6)
     ("policy_chunk_cost_k", "double cost = fmax(total + lambda * (double)h * k, Kl) + beta * Kl;",
      "double cost = fmax(total + lambda * (double)h, Kl) + beta * Kl;"),
+    ("policy_beta_term_dropped", "double cost = fmax(total + lambda * (double)h * k, Kl) + beta * Kl;",
+     "double cost = fmax(total + lambda * (double)h * k, Kl);"),
+    ("policy_k16_missing", "const int ks[4] = {2, 4, 8, 16};", "const int ks[4] = {2, 4, 8, 8};"),
+    ("policy_tie_takes_later", "if (cost < best) {", "if (cost <= best) {"),
     ("policy_margin_dropped", "!(best <= (1.0 - eps) * base)", "!(best <= base)"),
     ("policy_next_tile_ignored", "double l = fmax(N1 / k, next);", "double l = N1 / k;"),
     ("policy_next_index", "double next = h < nt ? (double)counts_desc[h] : 0.0;",
@@ -188,6 +196,10 @@ MUTANTS += [
      "out[0] = lambda * out[1] + (1.0 - lambda) * (1.0 - out[2]);"),
     ("loss_grad_weights_swapped", "dL_dx[i] = (1.0 - lambda) * inv * sg - lambda * inv * ds;",
      "dL_dx[i] = lambda * inv * sg - (1.0 - lambda) * inv * ds;"),
+    ("adam_first_moment_weight", "m[i] = b1 * m[i] + (1.0 - b1) * g[i];",
+     "m[i] = b1 * m[i] + g[i];"),
+    ("adam_bias_power", "double c1 = 1.0 - pow(b1, (double)t), c2 = 1.0 - pow(b2, (double)t);",
+     "double c1 = 1.0 - pow(b1, (double)t), c2 = 1.0 - pow(b2, (double)(t + 1));"),
     ("adam_second_moment", "v[i] = b2 * v[i] + (1.0 - b2) * g[i] * g[i];",
      "v[i] = b2 * v[i] + (1.0 - b2) * g[i];"),
     ("adam_bias_correction", "p[i] -= lr * (m[i] / c1) / (sqrt(v[i] / c2) + eps);",
@@ -205,6 +217,10 @@ MUTANTS += [
      "ds += w * (dmu[q] + xv * dxx[q] + yv * dxy[q]);"),
     ("ssim_window_width", "g[k + SSIM_R] = exp(-(double)(k * k) / (2.0 * sigma * sigma));",
      "g[k + SSIM_R] = exp(-(double)(k * k) / (sigma * sigma));"),
+    ("ssim_covariance_term", "cov = exy - mx * my", "cov = exy"),
+    ("ssim_c2_as_c1", "A2 = 2.0 * cov + c2", "A2 = 2.0 * cov + c1"),
+    ("ssim_dxy_factor", "dxy[i] = 2.0 * A1 / D;", "dxy[i] = A1 / D;"),
+    ("loss_mean_over_pixels", "double inv = 1.0 / (double)(3 * np);", "double inv = 1.0 / (double)np;"),
     ("l1_sign", "double sg = xv > yv ? 1.0 : (xv < yv ? -1.0 : 0.0);", "double sg = 1.0;"),
 ]
 
