@@ -63,6 +63,9 @@ MUTANTS = [
      "dmin((dreal)(16 * ty) + (dreal)15.5, (dreal)cam->H - (dreal)0.5)",
      "((dreal)(16 * ty) + (dreal)15.5)"),
     # ---- spherical harmonics and the view direction
+    ("sh_sign_y1", "Y[1] = k1 * y;", "Y[1] = -(k1 * y);"),
+    ("sh_sign_y6", "Y[6] = k2b * (3 * z * z - 1);", "Y[6] = -(k2b * (3 * z * z - 1));"),
+    ("sh_sign_y10", "Y[10] = k3b * x * y * z;", "Y[10] = -(k3b * x * y * z);"),
     ("sh_sign_y2", "Y[2] = k1 * z;", "Y[2] = -k1 * z;"),
     ("sh_sign_y15", "Y[15] = k3a * x * (x * x - 3 * y * y);",
      "Y[15] = -k3a * x * (x * x - 3 * y * y);"),
