@@ -156,6 +156,8 @@ MUTANTS += [
     ("dj12_focal_swapped", "dt[1] += dj12 * (-fy / tz2);", "dt[1] += dj12 * (-fx / tz2);"),
     ("dP11_first_term_sign", "double dP11 = ga * (1.0 / det - P11 * P00 / det2)",
      "double dP11 = ga * (-1.0 / det - P11 * P00 / det2)"),
+    ("magnitude_dt1_focal_swapped", "dt[1] = gmy * fabs(fy) / tz + dj12 * fabs(fy) / tz2;",
+     "dt[1] = gmy * fabs(fx) / tz + dj12 * fabs(fy) / tz2;"),
     ("dP00_sign", "double dP00 = ga * (-P11 * P11 / det2) + gb * (P01 * P11 / det2) +",
      "double dP00 = ga * (-P11 * P11 / det2) + gb * (-P01 * P11 / det2) +"),
     ("dP01_sign", "gb * (-1.0 / det - 2.0 * P01 * P01 / det2)",

@@ -480,7 +480,8 @@ def _chain_restated(sc, cam, tt, g2v, g2m):
 def test_parameter_magnitudes_equal_the_abs_arithmetic_restatement(seed, deg):
     sc, cam, w, v = _scene(seed, 30, 40, 32, deg)
     V = ss.look_at(np.array([0.4, -0.3, -0.6]), np.array([0.0, 0.0, 4.0]), up=(0.1, -1.0, 0.0))
-    cam = ss.pinhole(V, 48.0, 40, 32)  # a rotated camera: every view-matrix entry matters
+    # a rotated camera (every view-matrix entry matters) with fx != fy
+    cam = ss.Camera(V, 48.0, 40.0, 0.47 * 40, 0.55 * 32, 40, 32, 0.2)
     proj = oracle.project(sc, cam)
     b = oracle.bin_sort(cam, proj)
     r = oracle.blend_bwd_bounds(cam, proj, b, w, v)
