@@ -140,6 +140,9 @@ MUTANTS += [
     ("magnitude_behind_doubled", "behind_mag += cG_mag * w;", "behind_mag += 2.0 * cG_mag * w;"),
     ("magnitude_conic_b_factor", "mg[3] = 2.0 * fabs(e->dx * e->dy) * dq_mag;",
      "mg[3] = 4.0 * fabs(e->dx * e->dy) * dq_mag;"),
+    ("error_bound_base_dropped", "double eps = 2.0 * E_ALPHA + 32.0 * U32;", "double eps = 0.0;"),
+    ("error_bound_rounding_term", "eps += 2.0 * (E_ALPHA * list[j].alpha / (1.0 - list[j].alpha) + 8.0 * U32);",
+     "eps += 2.0 * (E_ALPHA * list[j].alpha / (1.0 - list[j].alpha) + U32);"),
     ("error_bound_alpha_weight",
      "eps += 2.0 * (E_ALPHA * list[j].alpha / (1.0 - list[j].alpha) + 8.0 * U32);",
      "eps += 2.0 * (E_ALPHA / (1.0 - list[j].alpha) + 8.0 * U32);"),
