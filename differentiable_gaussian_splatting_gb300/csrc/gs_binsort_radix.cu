@@ -16,8 +16,9 @@
 // Radix sort: LSD, 8-bit digits, one kernel per pass; the digit counts of every
 // pass are taken by the kernel that writes the keys (the visible-Gaussian
 // compaction, the pair emission).  Blocks take 4096-key tiles in ticket order,
-// rank keys within warps from eight ballots and one shared atomic per digit
-// and warp, publish their digit counts and add those of earlier tiles by
+// rank keys within warps from one ballot per digit bit (eight, or fewer in a
+// last pass whose higher bits are zero in every key) and one shared atomic per
+// digit and warp, publish their digit counts and add those of earlier tiles by
 // decoupled look-back (every wait is bounded and sets a give-up flag).
 #include <cuda_runtime.h>
 
@@ -110,7 +111,9 @@ __device__ __forceinline__ void st_relaxed(uint64_t* p, uint64_t v) {
 // before them by looking back through the published words (decoupled
 // look-back: a block only waits on tiles that started before it, so waits
 // end).  Keys are staged in shared memory in block-sorted order so that each
-// digit's run is written to global memory contiguously.
+// digit's run is written to global memory contiguously.  NB is the number of
+// the pass's digit bits that keys can set (keys are below 2^bits): the others
+// are zero in every key and need no ballot.
 struct OnesweepSmem {
     uint32_t keys[kRsTile];
     int32_t vals[kRsTile];
@@ -121,6 +124,7 @@ struct OnesweepSmem {
     int ticket;
 };
 
+template <int NB>
 __global__ void __launch_bounds__(kRsBlock, 4) rs_onesweep(
     const uint32_t* __restrict__ keys_in, const int32_t* __restrict__ vals_in,
     uint32_t* __restrict__ keys_out, int32_t* __restrict__ vals_out, const int64_t* n_dev,
@@ -152,7 +156,7 @@ __global__ void __launch_bounds__(kRsBlock, 4) rs_onesweep(
         k[r] = valid ? __ldg(keys_in + idx) : 0xffffffffu;
         v[r] = valid ? __ldg(vals_in + idx) : 0;
     }
-    // The lanes holding the same digit come from eight ballots; the lowest of them
+    // The lanes holding the same digit come from NB ballots; the lowest of them
     // adds their number to the warp's count of that digit and hands the old count
     // to the others.  Items are ranked in order r = 0, 1, ...: the leaders of
     // item r may be other lanes than those of item r - 1, and __syncwarp() orders
@@ -167,7 +171,7 @@ __global__ void __launch_bounds__(kRsBlock, 4) rs_onesweep(
         const uint32_t d = (k[r] >> shift) & 255u;
         uint32_t peers = __ballot_sync(0xffffffffu, valid);
 #pragma unroll
-        for (int bit = 0; bit < 8; ++bit) {
+        for (int bit = 0; bit < NB; ++bit) {
             const uint32_t m = __ballot_sync(0xffffffffu, (d >> bit) & 1u);
             peers &= ((d >> bit) & 1u) ? m : ~m;
         }
@@ -306,8 +310,21 @@ cudaError_t radix_sort(uint32_t* k0, int32_t* v0, uint32_t* k1, int32_t* v1, int
         const bool last = p == passes - 1;
         uint32_t* kout = kin == k0 ? k1 : k0;
         int32_t* vout = (last && vf) ? vf : (vin == v0 ? v1 : v0);
-        e = launch(rs_onesweep, grid, kRsBlock, 0, st, (const uint32_t*)kin, (const int32_t*)vin, kout,
-                   vout, n_dev, n_static, p, ghist, tickets, lookback, err);
+        const int nb = std::min(8, bits - 8 * p);
+        auto go = [&](auto kernel) {
+            return launch(kernel, grid, kRsBlock, 0, st, (const uint32_t*)kin, (const int32_t*)vin,
+                          kout, vout, n_dev, n_static, p, ghist, tickets, lookback, err);
+        };
+        switch (nb) {
+            case 1: e = go(rs_onesweep<1>); break;
+            case 2: e = go(rs_onesweep<2>); break;
+            case 3: e = go(rs_onesweep<3>); break;
+            case 4: e = go(rs_onesweep<4>); break;
+            case 5: e = go(rs_onesweep<5>); break;
+            case 6: e = go(rs_onesweep<6>); break;
+            case 7: e = go(rs_onesweep<7>); break;
+            default: e = go(rs_onesweep<8>); break;
+        }
         if (e != cudaSuccess) return e;
         kin = kout;
         vin = vout;
@@ -445,7 +462,8 @@ __global__ void __launch_bounds__(kRsBlock) pairs_count(const int32_t* __restric
     __shared__ int64_t s_warp[kRsWarps];
     const int64_t base = (int64_t)blockIdx.x * kRsTile;
     int64_t c = 0;
-#pragma unroll 4
+    // all of a thread's count gathers in flight at once
+#pragma unroll
     for (int i = threadIdx.x; i < kRsTile; i += kRsBlock) {
         int64_t j = base + i;
         if (j < m) c += tiles_touched[order[j]];
@@ -971,7 +989,7 @@ extern "C" gs_status gs_test_lookback_timeout(const uint32_t* keys_in, const int
     auto* ghist = reinterpret_cast<const uint32_t*>(w + off_ghist);
     auto* err = reinterpret_cast<unsigned long long*>(w + off_err);
     const unsigned grid = (unsigned)nblk_of(n);
-    if (launch(rs_onesweep, grid, kRsBlock, 0, st, keys_in, vals_in, keys_out, vals_out,
+    if (launch(rs_onesweep<8>, grid, kRsBlock, 0, st, keys_in, vals_in, keys_out, vals_out,
                (const int64_t*)nullptr, n, 0, ghist, tickets, lookback, err) != cudaSuccess)
         return GS_ERR_CUDA;
     unsigned long long flag = 0;
