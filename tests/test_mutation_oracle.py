@@ -180,6 +180,9 @@ MUTANTS += [
      "ds[k] += dM[3 * r + k] * R[3 * k + r];"),
     ("dquat_sign_w", "dw += dR[1] * (-2 * z);", "dw += dR[1] * (2 * z);"),
     ("dquat_sign_x", "dx += dR[5] * (-2 * w);", "dx += dR[5] * (2 * w);"),
+    ("dquat_sign_y_r6", "dw += dR[6] * (-2 * y);  dx += dR[6] * (2 * z);  dy += dR[6] * (-2 * w);",
+     "dw += dR[6] * (-2 * y);  dx += dR[6] * (2 * z);  dy += dR[6] * (2 * w);"),
+    ("drot_scale_index", "dR[3 * r + k] = dM[3 * r + k] * s[k];", "dR[3 * r + k] = dM[3 * r + k] * s[r];"),
     ("dquat_not_projected", "dq[k] = (dqh[k] - qh[k] * dotq) / qn;", "dq[k] = dqh[k] / qn;"),
     ("dquat_norm_dropped", "dq[k] = (dqh[k] - qh[k] * dotq) / qn;", "dq[k] = (dqh[k] - qh[k] * dotq);"),
     ("dopacity_scaled", "dopac[i] = g2[5];", "dopac[i] = 0.5 * g2[5];"),
