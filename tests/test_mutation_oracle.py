@@ -7,7 +7,7 @@ arithmetic the pins do not fix.
 The table is checked against the source on every CPU run (each planted text must occur
 exactly once, so the table follows the source as it changes), and a sample of eight
 mutants, one from each part of the oracle, runs every time.  Running the whole table
-takes about four minutes on eight cores and is opt-in:
+takes about five minutes on eight cores and is opt-in:
 
     GS_ORACLE_MUTANTS=1 python -m pytest tests/test_mutation_oracle.py -n 8 -q
 
