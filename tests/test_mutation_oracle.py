@@ -55,6 +55,12 @@ MUTANTS = [
     ("span_left_not_mirrored", "dmax(dyv, -hi), -lo)", "dmax(dyv, lo), hi)"),
     ("span_last_column_dropped", "dreal f1 = floor((Xhi - (dreal)0.5) * (dreal)0.0625) + 1;",
      "dreal f1 = floor((Xhi - (dreal)0.5) * (dreal)0.0625);"),
+    ("span_first_column_late", "dreal f0 = ceil((Xlo - (dreal)15.5) * (dreal)0.0625);",
+     "dreal f0 = ceil((Xlo - (dreal)0.5) * (dreal)0.0625);"),
+    ("span_right_edge_unclipped", "if (Xlo > (dreal)cam->W - (dreal)0.5 || Xhi < (dreal)0.5) return 0;",
+     "if (Xlo > (dreal)cam->W + (dreal)0.5 || Xhi < (dreal)0.5) return 0;"),
+    ("radius_rounded_down", "radii[2 * i] = to_int_clamped(ceil(s.rx), 0, RADIUS_MAX);",
+     "radii[2 * i] = to_int_clamped(floor(s.rx), 0, RADIUS_MAX);"),
     ("rows_first_row_late", "ceil(((s->muy - ryp) - (dreal)15.5)",
      "ceil(((s->muy - ryp) - (dreal)0.5)"),
     ("rows_last_row_dropped", "dreal f1 = floor(((s->muy + ryp) - (dreal)0.5) * (dreal)0.0625) + 1;",
